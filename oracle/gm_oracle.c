@@ -1,0 +1,1033 @@
+/*
+ * gm_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow CPU restatement of the hybrid mesh + 3D Gaussian renderer
+ * described on the page "A Lightweight and Differentiable Renderer for Joint
+ * Mesh and 3D Gaussian Splat Scenes" (Design Details: Mesh rasterizer,
+ * Hybrid rendering; Limitations and Todos).  Only the tests, the smoke check
+ * and the CPU-baseline leg of the benchmark load it; the CUDA library never
+ * does, and the two share no code.
+ *
+ * What it computes, step by step, with no tiling, fusion or reordering
+ * beyond what each definition states:
+ *   - triangle tile bins and a brute-force z-buffer that tests every pixel
+ *     centre against every triangle (Mesh rasterizer, item 1);
+ *   - perspective-correct depth and vertex colour at each pixel from its
+ *     face id (Mesh rasterizer, item 2);
+ *   - EWA projection of each Gaussian, SH colour (Hybrid rendering; the
+ *     projection / SH kernels the page says are adapted from gsplat);
+ *   - Gaussian tile bins, sorted by (tile, centre depth, id), with the
+ *     per-tile occlusion cull (Hybrid rendering, cull_occluded bullet;
+ *     Limitations: Gaussians sorted by centre depth);
+ *   - per-pixel front-to-back compositing over the full, fully sorted list
+ *     of Gaussians whose tile rectangle holds the pixel, each depth-tested
+ *     against the mesh, the mesh colour as the terminal layer (Hybrid
+ *     rendering, compositing equation with a hard split);
+ *   - gradients by central finite differences in double precision, with
+ *     every discrete decision (face ids, tile lists, skips, clamps, the
+ *     transmittance cut-off, the depth test) held fixed, and any parameter
+ *     whose perturbation flips one of them reported instead of used.
+ *
+ * Precision.  Every integer the method decides from floating point (face
+ * ids, coverage, tile rectangles, radii, skips, the transmittance stop) is
+ * decided in fp32, the precision the renderer works in, one correctly
+ * rounded operation at a time in the order the formula is written (build
+ * with -ffp-contract=off: no fused multiply-add).  Continuous values that
+ * feed no decision (interpolated depth and colour, conics, means, colours,
+ * colour and depth sums) are computed in double.  The compositing routine
+ * runs in either mode: "f32" rounds sigma, alpha and transmittance to fp32
+ * after every operation (an fp32 result of +, -, *, / or sqrt computed in
+ * double and rounded once is the correctly rounded fp32 result), "f64"
+ * keeps everything in double for finite differences.
+ *
+ * Parity unpinned (the page fixes none of these; each is a stated reading):
+ * the gsplat constants (0.3 px low-pass, 1.3 x half-FOV clamp of the
+ * Jacobian, 3-sigma radius), the real-SH sign convention, the depth/alpha
+ * output definitions and the camera axes.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define TILE 16
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
+
+typedef struct {
+    int32_t width, height;
+    float fx, fy, cx, cy, near_plane, far_plane;
+    float R[9]; /* world -> camera rotation, row-major (OpenCV axes) */
+    float t[3];
+} orc_camera;
+
+static int n_tiles_x(const orc_camera* c) { return (c->width + TILE - 1) / TILE; }
+static int n_tiles_y(const orc_camera* c) { return (c->height + TILE - 1) / TILE; }
+
+/* splat record: the projected 2D Gaussian, 12 floats */
+enum { S_MX = 0, S_MY, S_CA, S_CB, S_CC, S_OP, S_R, S_G, S_B, S_Z, S_STRIDE = 12 };
+
+/* ========================================================================
+ * Mesh rasterizer, item 1: triangle bins and the z-buffer (fp32 decisions)
+ * ====================================================================== */
+
+/* X_c = R X + t, each row summed left to right, one rounding per operation */
+static void world_to_cam_f32(const orc_camera* c, const float* X, float* xc)
+{
+    for (int r = 0; r < 3; ++r) {
+        float s = c->R[3 * r + 0] * X[0];
+        s = s + c->R[3 * r + 1] * X[1];
+        s = s + c->R[3 * r + 2] * X[2];
+        xc[r] = s + c->t[r];
+    }
+}
+
+/* edge function of the directed edge a->b at point p:
+ *   (ub - ua)(py - va) - (vb - va)(px - ua)                                */
+static float edge_f32(float ua, float va, float ub, float vb, float px, float py)
+{
+    float p = (ub - ua) * (py - va);
+    float q = (vb - va) * (px - ua);
+    return p - q;
+}
+
+typedef struct {
+    float u[3], v[3], z[3];
+    float area; /* edge function of v0->v1 at v2: twice the signed area */
+    int x0, x1, y0, y1; /* inclusive pixel-centre box, clamped to the image */
+} tri32;
+
+/* Returns 1 when the triangle is drawn: every vertex strictly beyond the near
+ * plane (triangles with a vertex in front of it are skipped, no clipping:
+ * Mesh rasterizer, last paragraph; Limitations), a non-zero area, and a
+ * non-empty box of pixel centres (i + 0.5, j + 0.5) inside the image.   */
+static int tri_setup_f32(const orc_camera* c, const float* V, const int32_t* F, int f, tri32* t)
+{
+    for (int k = 0; k < 3; ++k) {
+        float xc[3];
+        world_to_cam_f32(c, V + 3 * (int64_t)F[3 * f + k], xc);
+        if (!(xc[2] > c->near_plane))
+            return 0;
+        t->z[k] = xc[2];
+        t->u[k] = (c->fx * xc[0]) / xc[2] + c->cx;
+        t->v[k] = (c->fy * xc[1]) / xc[2] + c->cy;
+    }
+    t->area = edge_f32(t->u[0], t->v[0], t->u[1], t->v[1], t->u[2], t->v[2]);
+    if (!(t->area != 0.0f))
+        return 0;
+    float umin = fminf(fminf(t->u[0], t->u[1]), t->u[2]);
+    float umax = fmaxf(fmaxf(t->u[0], t->u[1]), t->u[2]);
+    float vmin = fminf(fminf(t->v[0], t->v[1]), t->v[2]);
+    float vmax = fmaxf(fmaxf(t->v[0], t->v[1]), t->v[2]);
+    float x0 = fmaxf(ceilf(umin - 0.5f), 0.0f);
+    float x1 = fminf(floorf(umax - 0.5f), (float)(c->width - 1));
+    float y0 = fmaxf(ceilf(vmin - 0.5f), 0.0f);
+    float y1 = fminf(floorf(vmax - 0.5f), (float)(c->height - 1));
+    if (!(x0 <= x1) || !(y0 <= y1))
+        return 0;
+    t->x0 = (int)x0; t->x1 = (int)x1; t->y0 = (int)y0; t->y1 = (int)y1;
+    return 1;
+}
+
+/* coverage of pixel (i, j) and, when covered, its depth D = 1 / sum_k (l_k / z_k)
+ * with screen barycentrics l_k = e_k / area.  Inclusive edges, both windings. */
+static int tri_cover_f32(const tri32* t, int i, int j, float* D)
+{
+    if (i < t->x0 || i > t->x1 || j < t->y0 || j > t->y1)
+        return 0;
+    float px = (float)i + 0.5f, py = (float)j + 0.5f;
+    float e0 = edge_f32(t->u[1], t->v[1], t->u[2], t->v[2], px, py);
+    float e1 = edge_f32(t->u[2], t->v[2], t->u[0], t->v[0], px, py);
+    float e2 = edge_f32(t->u[0], t->v[0], t->u[1], t->v[1], px, py);
+    int in = t->area > 0.0f ? (e0 >= 0.0f && e1 >= 0.0f && e2 >= 0.0f)
+                            : (e0 <= 0.0f && e1 <= 0.0f && e2 <= 0.0f);
+    if (!in)
+        return 0;
+    float l0 = e0 / t->area, l1 = e1 / t->area, l2 = e2 / t->area;
+    float s = l0 / t->z[0];
+    s = s + l1 / t->z[1];
+    s = s + l2 / t->z[2];
+    *D = 1.0f / s;
+    return 1;
+}
+
+/* Triangle tile bins: tile (tx, ty) holds every drawn triangle whose pixel-
+ * centre box meets it; within a tile, face ids ascend.  Returns the number of
+ * (triangle, tile) entries; fills tile_count[T] and, when ids != NULL and the
+ * total fits in cap, the tile-major list of face ids.                      */
+int64_t orc_bin_triangles(const orc_camera* c, const float* V, const int32_t* F, int32_t nF,
+                          int32_t* tile_count, int32_t* ids, int64_t cap)
+{
+    int TW = n_tiles_x(c), TH = n_tiles_y(c);
+    int64_t T = (int64_t)TW * TH;
+    memset(tile_count, 0, sizeof(int32_t) * T);
+    int64_t total = 0;
+    for (int f = 0; f < nF; ++f) {
+        tri32 t;
+        if (!tri_setup_f32(c, V, F, f, &t))
+            continue;
+        for (int ty = t.y0 / TILE; ty <= t.y1 / TILE; ++ty)
+            for (int tx = t.x0 / TILE; tx <= t.x1 / TILE; ++tx) {
+                tile_count[(int64_t)ty * TW + tx]++;
+                total++;
+            }
+    }
+    if (!ids || total > cap)
+        return total;
+    int64_t* fill = (int64_t*)malloc(sizeof(int64_t) * (T + 1));
+    fill[0] = 0;
+    for (int64_t k = 0; k < T; ++k)
+        fill[k + 1] = fill[k] + tile_count[k];
+    for (int f = 0; f < nF; ++f) {
+        tri32 t;
+        if (!tri_setup_f32(c, V, F, f, &t))
+            continue;
+        for (int ty = t.y0 / TILE; ty <= t.y1 / TILE; ++ty)
+            for (int tx = t.x0 / TILE; tx <= t.x1 / TILE; ++tx)
+                ids[fill[(int64_t)ty * TW + tx]++] = f;
+    }
+    free(fill);
+    (void)TH;
+    return total;
+}
+
+/* Brute-force z-buffer: every listed pixel (all pixels when pixels == NULL)
+ * against every triangle.  The nearest depth wins, equal depths go to the
+ * smaller face id.  Also returns the nearest depth and the nearest depth of
+ * any other covering face (+inf if none), so near-ties can be reported.   */
+void orc_zbuffer(const orc_camera* c, const float* V, const int32_t* F, int32_t nF,
+                 const int32_t* pixels, int64_t n_pixels,
+                 int32_t* face_id, float* best_depth, float* second_depth)
+{
+    tri32* tris = (tri32*)malloc(sizeof(tri32) * (nF > 0 ? nF : 1));
+    uint8_t* ok = (uint8_t*)malloc(nF > 0 ? nF : 1);
+    for (int f = 0; f < nF; ++f)
+        ok[f] = (uint8_t)tri_setup_f32(c, V, F, f, &tris[f]);
+    int64_t np = pixels ? n_pixels : (int64_t)c->width * c->height;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t k = 0; k < np; ++k) {
+        int64_t pix = pixels ? pixels[k] : k;
+        int i = (int)(pix % c->width), j = (int)(pix / c->width);
+        int best = -1;
+        float bd = INFINITY, sd = INFINITY;
+        for (int f = 0; f < nF; ++f) {
+            float D;
+            if (!ok[f] || !tri_cover_f32(&tris[f], i, j, &D))
+                continue;
+            if (best < 0 || D < bd) {
+                if (best >= 0) sd = fminf(sd, bd);
+                bd = D;
+                best = f;
+            } else {
+                sd = fminf(sd, D);
+            }
+        }
+        face_id[k] = best;
+        best_depth[k] = bd;
+        second_depth[k] = sd;
+    }
+    free(tris);
+    free(ok);
+}
+
+/* ========================================================================
+ * Mesh rasterizer, item 2: perspective-correct depth and colour (double)
+ * ====================================================================== */
+
+typedef struct {
+    double u[3], v[3], z[3];
+} tri64;
+
+static void tri_setup_f64(const orc_camera* c, const double X[3][3], tri64* t)
+{
+    for (int k = 0; k < 3; ++k) {
+        double xc[3];
+        for (int r = 0; r < 3; ++r)
+            xc[r] = (double)c->R[3 * r + 0] * X[k][0] + (double)c->R[3 * r + 1] * X[k][1] +
+                    (double)c->R[3 * r + 2] * X[k][2] + (double)c->t[r];
+        t->z[k] = xc[2];
+        t->u[k] = (double)c->fx * xc[0] / xc[2] + (double)c->cx;
+        t->v[k] = (double)c->fy * xc[1] / xc[2] + (double)c->cy;
+    }
+}
+
+static double edge_f64(double ua, double va, double ub, double vb, double px, double py)
+{
+    return (ub - ua) * (py - va) - (vb - va) * (px - ua);
+}
+
+/* depth D and weights w_k at pixel centre (px, py) of a triangle given by its
+ * camera-space vertices:  l_k = e_k / area,  D = 1 / sum_k l_k / z_k,
+ * w_k = (l_k / z_k) D, so the colour is sum_k w_k c_k.                     */
+static void interp_f64(const tri64* t, double px, double py, double* D, double w[3])
+{
+    double area = edge_f64(t->u[0], t->v[0], t->u[1], t->v[1], t->u[2], t->v[2]);
+    double e[3];
+    e[0] = edge_f64(t->u[1], t->v[1], t->u[2], t->v[2], px, py);
+    e[1] = edge_f64(t->u[2], t->v[2], t->u[0], t->v[0], px, py);
+    e[2] = edge_f64(t->u[0], t->v[0], t->u[1], t->v[1], px, py);
+    double q[3], s = 0.0;
+    for (int k = 0; k < 3; ++k) {
+        q[k] = (e[k] / area) / t->z[k];
+        s += q[k];
+    }
+    *D = 1.0 / s;
+    for (int k = 0; k < 3; ++k)
+        w[k] = q[k] / s;
+}
+
+static void load_tri(const float* V, const int32_t* F, int f, double X[3][3])
+{
+    for (int k = 0; k < 3; ++k)
+        for (int d = 0; d < 3; ++d)
+            X[k][d] = V[3 * (int64_t)F[3 * f + k] + d];
+}
+
+/* Interpolated mesh depth and colour for the listed pixels (all when NULL).
+ * Uncovered pixels: depth +inf, colour 0.  Per tile (only tiles whose pixels
+ * are all listed, tile_flags[t] = 1 on input): tile_full = every in-image
+ * pixel covered, tile_far = the largest fp32 mesh depth over the tile.     */
+void orc_interp_mesh(const orc_camera* c, const float* V, const int32_t* F, const float* vcol,
+                     const int32_t* pixels, int64_t n_pixels, const int32_t* face_id,
+                     float* mesh_depth, float* mesh_rgb)
+{
+    int64_t np = pixels ? n_pixels : (int64_t)c->width * c->height;
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < np; ++k) {
+        int64_t pix = pixels ? pixels[k] : k;
+        int i = (int)(pix % c->width), j = (int)(pix / c->width);
+        int f = face_id[k];
+        if (f < 0) {
+            mesh_depth[k] = INFINITY;
+            mesh_rgb[3 * k] = mesh_rgb[3 * k + 1] = mesh_rgb[3 * k + 2] = 0.0f;
+            continue;
+        }
+        double X[3][3], D, w[3];
+        tri64 t;
+        load_tri(V, F, f, X);
+        tri_setup_f64(c, X, &t);
+        interp_f64(&t, i + 0.5, j + 0.5, &D, w);
+        mesh_depth[k] = (float)D;
+        for (int ch = 0; ch < 3; ++ch) {
+            double s = 0.0;
+            for (int v = 0; v < 3; ++v)
+                s += w[v] * vcol[3 * (int64_t)F[3 * f + v] + ch];
+            mesh_rgb[3 * k + ch] = (float)s;
+        }
+    }
+}
+
+/* tile_full / tile_far from a full-frame mesh depth image (fp32 values). */
+void orc_tile_depth_bounds(const orc_camera* c, const float* mesh_depth, float* tile_far,
+                           uint8_t* tile_full)
+{
+    int TW = n_tiles_x(c), TH = n_tiles_y(c);
+    for (int ty = 0; ty < TH; ++ty)
+        for (int tx = 0; tx < TW; ++tx) {
+            float far = -INFINITY;
+            int full = 1;
+            for (int j = ty * TILE; j < ty * TILE + TILE && j < c->height; ++j)
+                for (int i = tx * TILE; i < tx * TILE + TILE && i < c->width; ++i) {
+                    float d = mesh_depth[(int64_t)j * c->width + i];
+                    if (!(d < INFINITY)) full = 0;
+                    if (d > far) far = d;
+                }
+            tile_far[ty * TW + tx] = full ? far : INFINITY;
+            tile_full[ty * TW + tx] = (uint8_t)full;
+        }
+}
+
+/* ========================================================================
+ * EWA projection and SH colour of the Gaussians
+ * ====================================================================== */
+
+/* real spherical harmonics Y_lm, m = -l..l, index l*l + l + m, from the
+ * associated Legendre functions without the Condon-Shortley phase:
+ *   Y_l0 = K_l0 P_l(cos t),  Y_lm = sqrt2 K_lm cos(m p) P_l^m,  Y_l-m = sqrt2 K_lm sin(m p) P_l^m,
+ *   K_lm = sqrt((2l+1)/(4 pi) (l-m)!/(l+m)!).                             */
+static double fact(int n)
+{
+    double r = 1.0;
+    for (int k = 2; k <= n; ++k) r *= k;
+    return r;
+}
+
+static double legendre_p(int l, int m, double x)
+{
+    /* P_m^m = (2m-1)!! (1-x^2)^(m/2); P_{m+1}^m = x (2m+1) P_m^m;
+     * (l-m) P_l^m = x (2l-1) P_{l-1}^m - (l+m-1) P_{l-2}^m */
+    double pmm = 1.0, sx = sqrt(fmax(0.0, 1.0 - x * x));
+    for (int k = 1; k <= m; ++k)
+        pmm *= (2.0 * k - 1.0) * sx;
+    if (l == m) return pmm;
+    double pm1 = x * (2.0 * m + 1.0) * pmm;
+    if (l == m + 1) return pm1;
+    double pl = 0.0;
+    for (int ll = m + 2; ll <= l; ++ll) {
+        pl = (x * (2.0 * ll - 1.0) * pm1 - (ll + m - 1.0) * pmm) / (ll - m);
+        pmm = pm1;
+        pm1 = pl;
+    }
+    return pl;
+}
+
+void orc_sh_basis(int deg, const double* dir, double* Y)
+{
+    double x = dir[0], y = dir[1], z = dir[2];
+    double ct = fmax(-1.0, fmin(1.0, z));
+    double ph = atan2(y, x);
+    for (int l = 0; l <= deg; ++l)
+        for (int m = -l; m <= l; ++m) {
+            int am = m < 0 ? -m : m;
+            double K = sqrt((2.0 * l + 1.0) / (4.0 * M_PI) * fact(l - am) / fact(l + am));
+            double P = legendre_p(l, am, ct);
+            double v;
+            if (m == 0) v = K * P;
+            else if (m > 0) v = sqrt(2.0) * K * cos(am * ph) * P;
+            else v = sqrt(2.0) * K * sin(am * ph) * P;
+            Y[l * l + l + m] = v;
+        }
+}
+
+/* The rectangle of tiles a projected Gaussian is binned to (fp32):
+ *   [floor((mx - r)/16), ceil((mx + r)/16)) x [floor((my - r)/16), ceil((my + r)/16)),
+ * clamped to the tile grid.  Returns its area (0 = not binned).           */
+static int64_t gauss_rect(const orc_camera* c, float mx, float my, int32_t r, int rect[4])
+{
+    if (r <= 0) return 0;
+    float fr = (float)r, TW = (float)n_tiles_x(c), TH = (float)n_tiles_y(c);
+    float x0 = floorf((mx - fr) / 16.0f), x1 = ceilf((mx + fr) / 16.0f);
+    float y0 = floorf((my - fr) / 16.0f), y1 = ceilf((my + fr) / 16.0f);
+    x0 = fminf(fmaxf(x0, 0.0f), TW); x1 = fminf(fmaxf(x1, 0.0f), TW);
+    y0 = fminf(fmaxf(y0, 0.0f), TH); y1 = fminf(fmaxf(y1, 0.0f), TH);
+    rect[0] = (int)x0; rect[1] = (int)y0; rect[2] = (int)x1; rect[3] = (int)y1;
+    if (rect[2] <= rect[0] || rect[3] <= rect[1]) return 0;
+    return (int64_t)(rect[2] - rect[0]) * (rect[3] - rect[1]);
+}
+
+/* Projection of one Gaussian (EWA splatting as in the 3DGS projection the
+ * page says was adapted from gsplat):
+ *   t = R mu + t_cw; culled when t_z <= near or t_z > far;
+ *   Sigma = M M^T with M = R(q) diag(exp(log_s)), q = (w, x, y, z) normalised;
+ *   J = [[fx/tz, 0, -fx tx'/tz^2], [0, fy/tz, -fy ty'/tz^2]], where
+ *       tx'/tz, ty'/tz are clamped to 1.3 x the tangent of the half field of
+ *       view on each side of the principal point;
+ *   Sigma2 = J R_cw Sigma R_cw^T J^T + 0.3 I;  conic = Sigma2^-1 as (a, b, c);
+ *   radius = ceil(3 sqrt(lambda_max)), lambda_max = m + sqrt(h^2 + b^2),
+ *       m = (a + c)/2, h = (a - c)/2 of Sigma2 (fp32, decides the bins);
+ *   mean2d = (fx tx/tz + cx, fy ty/tz + cy);  opacity = sigmoid(logit);
+ *   colour = given RGB (sh_degree < 0) or max(0, sum_lm Y_lm(d) coef_lm + 0.5)
+ *       with d = normalize(mu - camera centre).
+ * margin[g] = distance of 3 sqrt(lambda_max) (double) to the nearest integer,
+ * relative to its value (a radius decided within rounding of it is a tie). */
+void orc_project_gaussians(const orc_camera* c, int32_t sh_degree, int32_t N,
+                           const float* means, const float* log_scales, const float* quats,
+                           const float* logits, const float* colors,
+                           float* splats, int32_t* radii, int32_t* tiles_touched, double* margin)
+{
+    int ncoef = sh_degree >= 0 ? (sh_degree + 1) * (sh_degree + 1) : 1;
+    double Rc[3][3], cam_pos[3];
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 3; ++k)
+            Rc[r][k] = c->R[3 * r + k];
+    for (int k = 0; k < 3; ++k)
+        cam_pos[k] = -(Rc[0][k] * c->t[0] + Rc[1][k] * c->t[1] + Rc[2][k] * c->t[2]);
+    double limx_pos = 1.3 * (c->width - (double)c->cx) / c->fx;
+    double limx_neg = 1.3 * (double)c->cx / c->fx;
+    double limy_pos = 1.3 * (c->height - (double)c->cy) / c->fy;
+    double limy_neg = 1.3 * (double)c->cy / c->fy;
+
+#pragma omp parallel for schedule(static)
+    for (int64_t g = 0; g < N; ++g) {
+        float* s = splats + S_STRIDE * g;
+        for (int k = 0; k < S_STRIDE; ++k) s[k] = 0.0f;
+        radii[g] = 0;
+        tiles_touched[g] = 0;
+        margin[g] = INFINITY;
+        const float* mu = means + 3 * g;
+        double t[3];
+        for (int r = 0; r < 3; ++r)
+            t[r] = Rc[r][0] * mu[0] + Rc[r][1] * mu[1] + Rc[r][2] * mu[2] + c->t[r];
+        float tz32 = (float)t[2];
+        if (!(tz32 > c->near_plane) || tz32 > c->far_plane)
+            continue;
+        /* rotation of the quaternion and the 3D covariance */
+        const float* qq = quats + 4 * g;
+        double qn = sqrt((double)qq[0] * qq[0] + (double)qq[1] * qq[1] + (double)qq[2] * qq[2] +
+                         (double)qq[3] * qq[3]);
+        double w = qq[0] / qn, x = qq[1] / qn, y = qq[2] / qn, z = qq[3] / qn;
+        double Rq[3][3] = {
+            {1 - 2 * (y * y + z * z), 2 * (x * y - w * z), 2 * (x * z + w * y)},
+            {2 * (x * y + w * z), 1 - 2 * (x * x + z * z), 2 * (y * z - w * x)},
+            {2 * (x * z - w * y), 2 * (y * z + w * x), 1 - 2 * (x * x + y * y)}};
+        double sc[3], M[3][3], S3[3][3], Sc[3][3], Tmp[3][3];
+        for (int k = 0; k < 3; ++k) sc[k] = exp((double)log_scales[3 * g + k]);
+        for (int r = 0; r < 3; ++r)
+            for (int k = 0; k < 3; ++k) M[r][k] = Rq[r][k] * sc[k];
+        for (int r = 0; r < 3; ++r)
+            for (int k = 0; k < 3; ++k) {
+                S3[r][k] = 0;
+                for (int m = 0; m < 3; ++m) S3[r][k] += M[r][m] * M[k][m];
+            }
+        /* camera-frame covariance R_cw Sigma R_cw^T */
+        for (int r = 0; r < 3; ++r)
+            for (int k = 0; k < 3; ++k) {
+                Tmp[r][k] = 0;
+                for (int m = 0; m < 3; ++m) Tmp[r][k] += Rc[r][m] * S3[m][k];
+            }
+        for (int r = 0; r < 3; ++r)
+            for (int k = 0; k < 3; ++k) {
+                Sc[r][k] = 0;
+                for (int m = 0; m < 3; ++m) Sc[r][k] += Tmp[r][m] * Rc[k][m];
+            }
+        /* Jacobian of the pinhole projection with the clamped direction */
+        double tx = t[2] * fmin(limx_pos, fmax(-limx_neg, t[0] / t[2]));
+        double ty = t[2] * fmin(limy_pos, fmax(-limy_neg, t[1] / t[2]));
+        double J[2][3] = {{c->fx / t[2], 0.0, -c->fx * tx / (t[2] * t[2])},
+                          {0.0, c->fy / t[2], -c->fy * ty / (t[2] * t[2])}};
+        double JS[2][3], S2[2][2];
+        for (int r = 0; r < 2; ++r)
+            for (int k = 0; k < 3; ++k) {
+                JS[r][k] = 0;
+                for (int m = 0; m < 3; ++m) JS[r][k] += J[r][m] * Sc[m][k];
+            }
+        for (int r = 0; r < 2; ++r)
+            for (int k = 0; k < 2; ++k) {
+                S2[r][k] = 0;
+                for (int m = 0; m < 3; ++m) S2[r][k] += JS[r][m] * J[k][m];
+            }
+        S2[0][0] += 0.3;
+        S2[1][1] += 0.3;
+        /* fp32 decisions: positive determinant, radius */
+        float a32 = (float)S2[0][0], b32 = (float)S2[0][1], c32 = (float)S2[1][1];
+        float det32 = a32 * c32 - b32 * b32;
+        if (!(det32 > 0.0f))
+            continue;
+        float m32 = 0.5f * (a32 + c32);
+        float h32 = 0.5f * (a32 - c32);
+        float lam32 = m32 + sqrtf(h32 * h32 + b32 * b32);
+        float r32 = ceilf(3.0f * sqrtf(lam32));
+        double lam64 = 0.5 * (S2[0][0] + S2[1][1]) +
+                       sqrt(0.25 * (S2[0][0] - S2[1][1]) * (S2[0][0] - S2[1][1]) + S2[0][1] * S2[0][1]);
+        double ext = 3.0 * sqrt(lam64);
+        int32_t r = (int32_t)r32;
+        double mx = c->fx * t[0] / t[2] + c->cx;
+        double my = c->fy * t[1] / t[2] + c->cy;
+        int rect[4];
+        int64_t area = gauss_rect(c, (float)mx, (float)my, r, rect);
+        if (area <= 0)
+            continue;
+        margin[g] = fabs(ext - nearbyint(ext)) / ext;
+        double det = S2[0][0] * S2[1][1] - S2[0][1] * S2[0][1];
+        s[S_MX] = (float)mx;
+        s[S_MY] = (float)my;
+        s[S_CA] = (float)(S2[1][1] / det);
+        s[S_CB] = (float)(-S2[0][1] / det);
+        s[S_CC] = (float)(S2[0][0] / det);
+        s[S_OP] = (float)(1.0 / (1.0 + exp(-(double)logits[g])));
+        if (sh_degree < 0) {
+            for (int ch = 0; ch < 3; ++ch) s[S_R + ch] = colors[3 * g + ch];
+        } else {
+            double d[3], dn = 0.0, Y[16];
+            for (int k = 0; k < 3; ++k) {
+                d[k] = mu[k] - cam_pos[k];
+                dn += d[k] * d[k];
+            }
+            dn = sqrt(dn);
+            for (int k = 0; k < 3; ++k) d[k] /= dn;
+            orc_sh_basis(sh_degree, d, Y);
+            for (int ch = 0; ch < 3; ++ch) {
+                double v = 0.5;
+                for (int k = 0; k < ncoef; ++k)
+                    v += Y[k] * colors[((int64_t)g * ncoef + k) * 3 + ch];
+                s[S_R + ch] = (float)fmax(0.0, v);
+            }
+        }
+        s[S_Z] = (float)t[2];
+        radii[g] = r;
+        tiles_touched[g] = (int32_t)area;
+    }
+}
+
+/* ========================================================================
+ * Gaussian tile bins, sorted by (tile, centre depth, id), with the cull
+ * ====================================================================== */
+
+typedef struct {
+    uint64_t key;
+    int32_t gid;
+} kv;
+
+static int kv_cmp(const void* a, const void* b)
+{
+    const kv* x = (const kv*)a;
+    const kv* y = (const kv*)b;
+    if (x->key != y->key) return x->key < y->key ? -1 : 1;
+    return (x->gid > y->gid) - (x->gid < y->gid);
+}
+
+static uint32_t fbits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return u;
+}
+
+/* Emits key = (tile << 32) | bits(depth), value = Gaussian id, for every tile
+ * of every binned Gaussian's rectangle, except (cull != 0) tiles that are
+ * fully covered by the mesh and whose farthest mesh depth is not beyond the
+ * Gaussian's centre depth (depth >= tile_far): such a Gaussian fails the
+ * depth test at every pixel of the tile, so dropping it changes nothing
+ * (Hybrid rendering, cull_occluded bullet).  Sorted ascending by key, then
+ * id.  Returns the number of entries after the cull; *pre gets the number
+ * before it.  keys/gids are written when non-NULL and the total fits cap.  */
+int64_t orc_bin_gaussians(const orc_camera* c, int32_t N, const float* splats, const int32_t* radii,
+                          const float* tile_far, const uint8_t* tile_full, int32_t cull,
+                          uint64_t* keys, int32_t* gids, int64_t cap, int64_t* pre)
+{
+    int TW = n_tiles_x(c);
+    int64_t total = 0, before = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        kv* out = NULL;
+        if (pass == 1) {
+            if (!keys || total > cap) break;
+            out = (kv*)malloc(sizeof(kv) * (total > 0 ? total : 1));
+        }
+        int64_t n = 0;
+        for (int32_t g = 0; g < N; ++g) {
+            int rect[4];
+            const float* s = splats + S_STRIDE * (int64_t)g;
+            if (gauss_rect(c, s[S_MX], s[S_MY], radii[g], rect) <= 0)
+                continue;
+            for (int ty = rect[1]; ty < rect[3]; ++ty)
+                for (int tx = rect[0]; tx < rect[2]; ++tx) {
+                    int64_t tile = (int64_t)ty * TW + tx;
+                    if (pass == 0) before++;
+                    if (cull && tile_full[tile] && s[S_Z] >= tile_far[tile])
+                        continue;
+                    if (pass == 1) {
+                        out[n].key = ((uint64_t)tile << 32) | fbits(s[S_Z]);
+                        out[n].gid = g;
+                    }
+                    n++;
+                }
+        }
+        if (pass == 0) {
+            total = n;
+        } else {
+            qsort(out, (size_t)n, sizeof(kv), kv_cmp);
+            for (int64_t k = 0; k < n; ++k) {
+                keys[k] = out[k].key;
+                gids[k] = out[k].gid;
+            }
+            free(out);
+        }
+    }
+    if (pre) *pre = before;
+    return total;
+}
+
+/* Full per-tile candidate lists for compositing (no cull): tile t holds every
+ * binned Gaussian whose rectangle contains it, ordered by (depth, id).
+ * tile_start[T+1] is filled always; entries when non-NULL and K fits cap. */
+int64_t orc_tile_lists(const orc_camera* c, int32_t N, const float* splats, const int32_t* radii,
+                       int64_t* tile_start, int32_t* entries, int64_t cap)
+{
+    int TW = n_tiles_x(c), TH = n_tiles_y(c);
+    int64_t T = (int64_t)TW * TH;
+    int64_t K = orc_bin_gaussians(c, N, splats, radii, NULL, NULL, 0, NULL, NULL, 0, NULL);
+    if (!entries || K > cap) {
+        /* counts only */
+        memset(tile_start, 0, sizeof(int64_t) * (T + 1));
+        for (int32_t g = 0; g < N; ++g) {
+            int rect[4];
+            const float* s = splats + S_STRIDE * (int64_t)g;
+            if (gauss_rect(c, s[S_MX], s[S_MY], radii[g], rect) <= 0) continue;
+            for (int ty = rect[1]; ty < rect[3]; ++ty)
+                for (int tx = rect[0]; tx < rect[2]; ++tx) tile_start[(int64_t)ty * TW + tx + 1]++;
+        }
+        for (int64_t t = 0; t < T; ++t) tile_start[t + 1] += tile_start[t];
+        return K;
+    }
+    uint64_t* keys = (uint64_t*)malloc(sizeof(uint64_t) * (K > 0 ? K : 1));
+    orc_bin_gaussians(c, N, splats, radii, NULL, NULL, 0, keys, entries, K, NULL);
+    for (int64_t t = 0; t <= T; ++t) tile_start[t] = 0;
+    for (int64_t k = 0; k < K; ++k) tile_start[(keys[k] >> 32) + 1]++;
+    for (int64_t t = 0; t < T; ++t) tile_start[t + 1] += tile_start[t];
+    free(keys);
+    return K;
+}
+
+/* ========================================================================
+ * Hybrid compositing (hard split, mesh colour as the terminal layer)
+ * ====================================================================== */
+
+#define ALPHA_MAX 0.99
+#define ALPHA_MIN (1.0 / 255.0)
+#define T_STOP 1e-4
+
+enum { TR_DEPTH = 1, TR_SIGMA = 2, TR_ALPHA = 3, TR_BLEND = 4, TR_BLEND_CLAMPED = 5, TR_STOP = 6 };
+
+typedef struct {
+    int gid, field;
+    double delta;
+} pert_t;
+
+typedef struct {
+    double rgb[3], depth, alpha, T;
+    int32_t n_contrib;
+    /* smallest relative distance of a decision operand to its threshold */
+    double m_depth, m_alpha, m_clamp, m_stop, m_sigma;
+} pix_t;
+
+static inline double rnd(double x, int f32) { return f32 ? (double)(float)x : x; }
+
+static inline double sfield(const float* splats, int g, int f, const pert_t* p)
+{
+    double v = splats[S_STRIDE * (int64_t)g + f];
+    if (p && p->gid == g && p->field == f) v += p->delta;
+    return v;
+}
+
+/* One pixel, front to back over its tile's sorted list.  Each Gaussian i:
+ *   drawn only where its centre depth is in front of the mesh (z_i < D);
+ *   d = p - mu_i,  sigma = 1/2 (a dx^2 + c dy^2) + b dx dy  (skip sigma < 0);
+ *   alpha = min(0.99, o_i exp(-sigma))  (skip alpha < 1/255);
+ *   T' = T (1 - alpha); stop before i when T' <= 1e-4;
+ *   C += alpha T c_i;  Z += alpha T z_i;  T = T'.
+ * Terminal layer (the opaque mesh, coverage 0 or 1):
+ *   rgb = C + T (covered ? c_mesh : bg);  depth = Z + T covered D;
+ *   alpha = 1 - T (1 - covered).
+ * trace[k] (optional) records the decision taken on list entry k.        */
+static void composite_pixel(int f32, double px, double py, const int32_t* list, int64_t n,
+                            const float* splats, double D, int covered, const double cm[3],
+                            const double bg[3], const pert_t* p, pix_t* o, uint8_t* trace,
+                            int64_t* trace_len)
+{
+    double T = 1.0, C[3] = {0, 0, 0}, Z = 0.0;
+    int32_t last = 0;
+    const double amax = rnd(ALPHA_MAX, f32), amin = rnd(ALPHA_MIN, f32), tstop = rnd(T_STOP, f32);
+    o->m_depth = o->m_alpha = o->m_clamp = o->m_stop = o->m_sigma = INFINITY;
+    int64_t k;
+    for (k = 0; k < n; ++k) {
+        int g = list[k];
+        double z = sfield(splats, g, S_Z, p);
+        if (D < INFINITY) o->m_depth = fmin(o->m_depth, fabs(z - D) / D);
+        if (!(z < D)) {
+            if (trace) trace[k] = TR_DEPTH;
+            continue;
+        }
+        double dx = rnd(px - sfield(splats, g, S_MX, p), f32);
+        double dy = rnd(py - sfield(splats, g, S_MY, p), f32);
+        double ca = sfield(splats, g, S_CA, p), cb = sfield(splats, g, S_CB, p),
+               cc = sfield(splats, g, S_CC, p);
+        double qa = rnd(ca * rnd(dx * dx, f32), f32);
+        double qc = rnd(cc * rnd(dy * dy, f32), f32);
+        double half = rnd(0.5 * rnd(qa + qc, f32), f32);
+        double cross = rnd(rnd(cb * dx, f32) * dy, f32);
+        double sigma = rnd(half + cross, f32);
+        o->m_sigma = fmin(o->m_sigma, fabs(sigma) / (fabs(half) + fabs(cross) + 1e-30));
+        if (sigma < 0.0) {
+            if (trace) trace[k] = TR_SIGMA;
+            continue;
+        }
+        double G = rnd(exp(-sigma), f32);
+        double oG = rnd(sfield(splats, g, S_OP, p) * G, f32);
+        o->m_clamp = fmin(o->m_clamp, fabs(oG - amax) / amax);
+        int clamped = oG > amax;
+        double alpha = clamped ? amax : oG;
+        o->m_alpha = fmin(o->m_alpha, fabs(alpha - amin) / amin);
+        if (alpha < amin) {
+            if (trace) trace[k] = TR_ALPHA;
+            continue;
+        }
+        double Tn = rnd(T * rnd(1.0 - alpha, f32), f32);
+        o->m_stop = fmin(o->m_stop, fabs(Tn - tstop) / tstop);
+        if (Tn <= tstop) {
+            if (trace) trace[k] = TR_STOP;
+            k++;
+            break;
+        }
+        double w = rnd(alpha * T, f32);
+        for (int ch = 0; ch < 3; ++ch) C[ch] += w * sfield(splats, g, S_R + ch, p);
+        Z += w * z;
+        T = Tn;
+        last = (int32_t)(k + 1);
+        if (trace) trace[k] = clamped ? TR_BLEND_CLAMPED : TR_BLEND;
+    }
+    if (trace_len) *trace_len = k;
+    for (int ch = 0; ch < 3; ++ch) o->rgb[ch] = C[ch] + T * (covered ? cm[ch] : bg[ch]);
+    o->depth = Z + (covered ? T * D : 0.0);
+    o->alpha = 1.0 - T * (covered ? 0.0 : 1.0);
+    o->T = T;
+    o->n_contrib = last;
+}
+
+/* Forward composite of the listed tiles (all when tiles == NULL) with the
+ * full lists of orc_tile_lists (tile_start over all T tiles).  Outputs are
+ * full-frame arrays; only pixels of the listed tiles are written.  margins
+ * (optional, [H*W*5]) get the per-pixel decision margins (depth, alpha skip,
+ * clamp, stop, sigma) of the fp32 evaluation.                              */
+void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats,
+                       const int64_t* tile_start, const int32_t* entries,
+                       const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
+                       const int32_t* tiles, int32_t n_tiles_req,
+                       float* out_rgb, float* out_depth, float* out_alpha, float* T_final,
+                       int32_t* n_contrib, double* margins)
+{
+    int TW = n_tiles_x(c), TH = n_tiles_y(c);
+    int32_t nt = tiles ? n_tiles_req : TW * TH;
+    double bgd[3] = {bg[0], bg[1], bg[2]};
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t q = 0; q < nt; ++q) {
+        int32_t tile = tiles ? tiles[q] : q;
+        int tx = tile % TW, ty = tile / TW;
+        const int32_t* list = entries + tile_start[tile];
+        int64_t n = tile_start[tile + 1] - tile_start[tile];
+        for (int j = ty * TILE; j < ty * TILE + TILE && j < c->height; ++j)
+            for (int i = tx * TILE; i < tx * TILE + TILE && i < c->width; ++i) {
+                int64_t pix = (int64_t)j * c->width + i;
+                int cov = face_id[pix] >= 0;
+                double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
+                pix_t o;
+                composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, (double)mesh_depth[pix], cov, cm,
+                                bgd, NULL, &o, NULL, NULL);
+                for (int ch = 0; ch < 3; ++ch) out_rgb[3 * pix + ch] = (float)o.rgb[ch];
+                out_depth[pix] = (float)o.depth;
+                out_alpha[pix] = (float)o.alpha;
+                T_final[pix] = (float)o.T;
+                n_contrib[pix] = o.n_contrib;
+                if (margins) {
+                    margins[5 * pix + 0] = o.m_depth;
+                    margins[5 * pix + 1] = o.m_alpha;
+                    margins[5 * pix + 2] = o.m_clamp;
+                    margins[5 * pix + 3] = o.m_stop;
+                    margins[5 * pix + 4] = o.m_sigma;
+                }
+            }
+    }
+    (void)TH;
+}
+
+/* ========================================================================
+ * Gradients by central finite differences (double), decisions held fixed
+ * ====================================================================== */
+
+enum { FD_OK = 0, FD_FLIP = 1, FD_PRECISION = 2, FD_TIE = 3, FD_ORDER = 4, FD_UNUSED = 5 };
+
+static double pixel_loss(const pix_t* o, const float* g_rgb, const float* g_depth,
+                         const float* g_alpha, int64_t pix)
+{
+    return g_rgb[3 * pix] * o->rgb[0] + g_rgb[3 * pix + 1] * o->rgb[1] + g_rgb[3 * pix + 2] * o->rgb[2] +
+           g_depth[pix] * o->depth + g_alpha[pix] * o->alpha;
+}
+
+static int same_trace(const uint8_t* a, int64_t na, const uint8_t* b, int64_t nb)
+{
+    return na == nb && memcmp(a, b, (size_t)na) == 0;
+}
+
+static int tie_pixel(const pix_t* o, double band)
+{
+    return o->m_alpha < band || o->m_clamp < band || o->m_stop < band || o->m_sigma < band;
+}
+
+/* dL/d(splat field) for the requested (Gaussian, field) pairs, L = sum over
+ * pixels of g_rgb . rgb + g_depth depth + g_alpha alpha.  Only pixels of the
+ * tiles in the Gaussian's rectangle can change; the tile lists stay fixed.
+ * status: FD_OK; FD_FLIP a decision differs between +h and -h;
+ * FD_PRECISION the double and fp32 evaluations decide differently at h = 0;
+ * FD_TIE an fp32 decision margin is below tie_band on an affected pixel;
+ * FD_ORDER a depth step would reorder the list.                          */
+void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats, const int32_t* radii,
+                      const int64_t* tile_start, const int32_t* entries,
+                      const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
+                      const float* g_rgb, const float* g_depth, const float* g_alpha,
+                      int32_t n_req, const int32_t* req_gid, const int32_t* req_field,
+                      const double* req_h, double tie_band, double* grad, int32_t* status)
+{
+    int TW = n_tiles_x(c);
+    double bgd[3] = {bg[0], bg[1], bg[2]};
+    int64_t maxlist = 1;
+    for (int64_t t = 0; t < (int64_t)TW * n_tiles_y(c); ++t)
+        if (tile_start[t + 1] - tile_start[t] > maxlist) maxlist = tile_start[t + 1] - tile_start[t];
+#pragma omp parallel
+    {
+        uint8_t* tr[4];
+        for (int k = 0; k < 4; ++k) tr[k] = (uint8_t*)malloc((size_t)maxlist);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t q = 0; q < n_req; ++q) {
+            int g = req_gid[q], field = req_field[q];
+            double h = req_h[q];
+            int rect[4];
+            const float* s = splats + S_STRIDE * (int64_t)g;
+            grad[q] = 0.0;
+            status[q] = FD_OK;
+            if (gauss_rect(c, s[S_MX], s[S_MY], radii[g], rect) <= 0) {
+                status[q] = FD_UNUSED;
+                continue;
+            }
+            pert_t pp = {g, field, h}, pm = {g, field, -h};
+            double lp = 0.0, lm = 0.0;
+            int st = FD_OK;
+            for (int ty = rect[1]; ty < rect[3] && st == FD_OK; ++ty)
+                for (int tx = rect[0]; tx < rect[2] && st == FD_OK; ++tx) {
+                    int64_t tile = (int64_t)ty * TW + tx;
+                    const int32_t* list = entries + tile_start[tile];
+                    int64_t n = tile_start[tile + 1] - tile_start[tile];
+                    if (field == S_Z) {
+                        for (int64_t k = 0; k < n; ++k) {
+                            if (list[k] != g) continue;
+                            double z = s[S_Z];
+                            if (k > 0 && !(splats[S_STRIDE * (int64_t)list[k - 1] + S_Z] < z - h)) st = FD_ORDER;
+                            if (k + 1 < n && !(z + h < splats[S_STRIDE * (int64_t)list[k + 1] + S_Z])) st = FD_ORDER;
+                        }
+                        if (st != FD_OK) break;
+                    }
+                    for (int j = ty * TILE; j < ty * TILE + TILE && j < c->height && st == FD_OK; ++j)
+                        for (int i = tx * TILE; i < tx * TILE + TILE && i < c->width; ++i) {
+                            int64_t pix = (int64_t)j * c->width + i;
+                            int cov = face_id[pix] >= 0;
+                            double D = mesh_depth[pix];
+                            double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
+                            pix_t o32, o0, op, om;
+                            int64_t n32, n0, np_, nm;
+                            composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o32, tr[0], &n32);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o0, tr[1], &n0);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pp, &op, tr[2], &np_);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pm, &om, tr[3], &nm);
+                            if (tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
+                            if (!same_trace(tr[0], n32, tr[1], n0)) { st = FD_PRECISION; break; }
+                            if (!same_trace(tr[1], n0, tr[2], np_) || !same_trace(tr[1], n0, tr[3], nm)) {
+                                st = FD_FLIP;
+                                break;
+                            }
+                            lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
+                            lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
+                        }
+                }
+            status[q] = st;
+            grad[q] = st == FD_OK ? (lp - lm) / (2.0 * h) : 0.0;
+        }
+        for (int k = 0; k < 4; ++k) free(tr[k]);
+    }
+}
+
+/* dL/d(vertex position or colour) through the interpolated mesh depth and
+ * colour (face ids held fixed).  req_field 0..2 = world x, y, z of the vertex,
+ * 3..5 = its r, g, b.  Pixels whose face uses the vertex are re-evaluated:
+ * depth and colour in double from the perturbed mesh, then the composite in
+ * double with that depth.  The fp32 reference decisions use mesh_depth as
+ * given.  Status codes as for orc_composite_fd.                           */
+void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t nV, const int32_t* F,
+                 int32_t nF, const float* vcol, const int32_t* face_id, const float* splats,
+                 const int64_t* tile_start, const int32_t* entries, const float* mesh_depth,
+                 const float* mesh_rgb, const float* g_rgb, const float* g_depth, const float* g_alpha,
+                 int32_t n_req, const int32_t* req_vid, const int32_t* req_field, const double* req_h,
+                 double tie_band, double* grad, int32_t* status)
+{
+    int TW = n_tiles_x(c);
+    int64_t P = (int64_t)c->width * c->height;
+    double bgd[3] = {bg[0], bg[1], bg[2]};
+    /* pixels of each face (CSR) */
+    int64_t* fstart = (int64_t*)calloc((size_t)nF + 1, sizeof(int64_t));
+    for (int64_t p = 0; p < P; ++p)
+        if (face_id[p] >= 0) fstart[face_id[p] + 1]++;
+    for (int f = 0; f < nF; ++f) fstart[f + 1] += fstart[f];
+    int64_t* fpix = (int64_t*)malloc(sizeof(int64_t) * (fstart[nF] > 0 ? fstart[nF] : 1));
+    int64_t* ffill = (int64_t*)malloc(sizeof(int64_t) * (nF > 0 ? nF : 1));
+    for (int f = 0; f < nF; ++f) ffill[f] = fstart[f];
+    for (int64_t p = 0; p < P; ++p)
+        if (face_id[p] >= 0) fpix[ffill[face_id[p]]++] = p;
+    /* faces of each vertex (CSR) */
+    int64_t* vstart = (int64_t*)calloc((size_t)nV + 1, sizeof(int64_t));
+    for (int f = 0; f < nF; ++f)
+        for (int k = 0; k < 3; ++k) vstart[F[3 * f + k] + 1]++;
+    for (int v = 0; v < nV; ++v) vstart[v + 1] += vstart[v];
+    int32_t* vface = (int32_t*)malloc(sizeof(int32_t) * (vstart[nV] > 0 ? vstart[nV] : 1));
+    int64_t* vfill = (int64_t*)malloc(sizeof(int64_t) * (nV > 0 ? nV : 1));
+    for (int v = 0; v < nV; ++v) vfill[v] = vstart[v];
+    for (int f = 0; f < nF; ++f)
+        for (int k = 0; k < 3; ++k) vface[vfill[F[3 * f + k]]++] = f;
+    int64_t maxlist = 1;
+    for (int64_t t = 0; t < (int64_t)TW * n_tiles_y(c); ++t)
+        if (tile_start[t + 1] - tile_start[t] > maxlist) maxlist = tile_start[t + 1] - tile_start[t];
+
+#pragma omp parallel
+    {
+        uint8_t* tr[4];
+        for (int k = 0; k < 4; ++k) tr[k] = (uint8_t*)malloc((size_t)maxlist);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t q = 0; q < n_req; ++q) {
+            int vid = req_vid[q], field = req_field[q];
+            double h = req_h[q];
+            double lp = 0.0, lm = 0.0;
+            int st = FD_OK, any = 0;
+            for (int64_t fk = vstart[vid]; fk < vstart[vid + 1] && st == FD_OK; ++fk) {
+                int f = vface[fk];
+                for (int64_t pk = fstart[f]; pk < fstart[f + 1]; ++pk) {
+                    int64_t pix = fpix[pk];
+                    int i = (int)(pix % c->width), j = (int)(pix / c->width);
+                    int64_t tile = (int64_t)(j / TILE) * TW + i / TILE;
+                    const int32_t* list = entries + tile_start[tile];
+                    int64_t n = tile_start[tile + 1] - tile_start[tile];
+                    double Dv[3], cmv[3][3];
+                    for (int sgn = 0; sgn < 3; ++sgn) {
+                        double X[3][3], C3[3][3], D, w[3];
+                        load_tri(V, F, f, X);
+                        for (int k = 0; k < 3; ++k)
+                            for (int d = 0; d < 3; ++d) C3[k][d] = vcol[3 * (int64_t)F[3 * f + k] + d];
+                        double delta = sgn == 0 ? 0.0 : (sgn == 1 ? h : -h);
+                        for (int k = 0; k < 3; ++k) {
+                            if (F[3 * f + k] != vid) continue;
+                            if (field < 3) X[k][field] += delta;
+                            else C3[k][field - 3] += delta;
+                        }
+                        tri64 t;
+                        tri_setup_f64(c, X, &t);
+                        interp_f64(&t, i + 0.5, j + 0.5, &D, w);
+                        Dv[sgn] = D;
+                        for (int ch = 0; ch < 3; ++ch)
+                            cmv[sgn][ch] = w[0] * C3[0][ch] + w[1] * C3[1][ch] + w[2] * C3[2][ch];
+                    }
+                    double cm32[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
+                    pix_t o32, o0, op, om;
+                    int64_t n32, n0, np_, nm;
+                    composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, mesh_depth[pix], 1, cm32, bgd, NULL, &o32, tr[0], &n32);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[0], 1, cmv[0], bgd, NULL, &o0, tr[1], &n0);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[1], 1, cmv[1], bgd, NULL, &op, tr[2], &np_);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[2], 1, cmv[2], bgd, NULL, &om, tr[3], &nm);
+                    if (o32.m_depth < tie_band || tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
+                    if (!same_trace(tr[0], n32, tr[1], n0)) { st = FD_PRECISION; break; }
+                    if (!same_trace(tr[1], n0, tr[2], np_) || !same_trace(tr[1], n0, tr[3], nm)) {
+                        st = FD_FLIP;
+                        break;
+                    }
+                    lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
+                    lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
+                    any = 1;
+                }
+            }
+            if (st == FD_OK && !any) st = FD_UNUSED;
+            status[q] = st;
+            grad[q] = st == FD_OK ? (lp - lm) / (2.0 * h) : 0.0;
+        }
+        for (int k = 0; k < 4; ++k) free(tr[k]);
+    }
+    free(fstart); free(fpix); free(ffill); free(vstart); free(vface); free(vfill);
+}
+
+/* Single-pixel composite, exported for closed-form checks of the routine
+ * itself (list of Gaussian ids into splats, f32 = 1 for the fp32 mode).
+ * out: rgb[3], depth, alpha, T, n_contrib.                                */
+void orc_composite_one(int32_t f32, double px, double py, const int32_t* list, int64_t n,
+                       const float* splats, double D, int32_t covered, const double* cm,
+                       const double* bg, double* out)
+{
+    pix_t o;
+    composite_pixel(f32, px, py, list, n, splats, D, covered, cm, bg, NULL, &o, NULL, NULL);
+    out[0] = o.rgb[0]; out[1] = o.rgb[1]; out[2] = o.rgb[2];
+    out[3] = o.depth; out[4] = o.alpha; out[5] = o.T; out[6] = o.n_contrib;
+}
