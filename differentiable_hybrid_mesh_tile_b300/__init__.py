@@ -1,0 +1,366 @@
+"""Python binding of libgm, the B300 CUDA library for tile-based forward and
+backward rendering of scenes holding a triangle mesh and 3D Gaussians (the
+hybrid renderer of "A Lightweight and Differentiable Renderer for Joint Mesh
+and 3D Gaussian Splat Scenes").
+
+The ``gm_*`` functions mirror the C ABI of ``include/gm.h`` one to one: they
+check and marshal torch CUDA tensors into raw device pointers and the current
+CUDA stream, and raise :class:`GmError` on a non-zero status.  Every step of
+the computation runs in the library's kernels; there is no CPU path, and the
+import fails loudly when ``libgm.so`` has not been built.
+
+:class:`HybridRenderer` sequences the seven calls for one camera and owns the
+device buffers between them (allocation and ordering only).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgm.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "gm.h")
+
+GM_OK, GM_ERR_INVALID_ARG, GM_ERR_CAPACITY, GM_ERR_CUDA, GM_ERR_TIMEOUT, GM_ERR_INTERNAL = range(6)
+GM_CNT_K, GM_CNT_K_PRECULL, GM_CNT_FLAGS = 0, 1, 2
+GM_FLAG_OVERFLOW, GM_FLAG_TIMEOUT = 1, 2
+TILE = 16
+SPLAT_STRIDE = 12
+
+
+class GmError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__("%s failed with status %d: %s" % (where, status, msg))
+        self.status = status
+
+
+class gm_camera(C.Structure):
+    _fields_ = [("width", C.c_int32), ("height", C.c_int32),
+                ("fx", C.c_float), ("fy", C.c_float), ("cx", C.c_float), ("cy", C.c_float),
+                ("near_plane", C.c_float), ("far_plane", C.c_float),
+                ("R", C.c_float * 9), ("t", C.c_float * 3)]
+
+
+class gm_opts(C.Structure):
+    _fields_ = [("bg", C.c_float * 3), ("cull_occluded", C.c_int32), ("sh_degree", C.c_int32)]
+
+
+_VP = C.c_void_p
+_I32 = C.c_int32
+_SIGS = {
+    "gm_bin_triangles_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
+    "gm_bin_triangles": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, C.c_size_t, _VP]),
+    "gm_zbuffer": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP]),
+    "gm_interp_mesh": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "gm_project_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "gm_bin_sort_gaussians_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
+    "gm_bin_sort_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
+                                        C.c_size_t, _VP]),
+    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 13),
+    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 13 + [_I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "gm_last_error": (C.c_char_p, []),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libgm.so (raises when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libgm.so not built: run differentiable_hybrid_mesh_tile_b300/build.py "
+                              "(or __graft_entry__.build()); there is no CPU fallback")
+        _lib = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(_lib, name)
+            fn.restype = res
+            fn.argtypes = args
+    return _lib
+
+
+def header_functions():
+    """Names of the functions include/gm.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(gm_\w+)\s*\(", text, re.M)))
+
+
+# ------------------------------------------------------------ marshalling --
+
+def make_camera(cam) -> gm_camera:
+    c = gm_camera()
+    c.width, c.height = int(cam.width), int(cam.height)
+    c.fx, c.fy, c.cx, c.cy = float(cam.fx), float(cam.fy), float(cam.cx), float(cam.cy)
+    c.near_plane, c.far_plane = float(cam.near), float(cam.far)
+    R = [float(x) for x in torch.as_tensor(cam.R, dtype=torch.float32).reshape(9)]
+    t = [float(x) for x in torch.as_tensor(cam.t, dtype=torch.float32).reshape(3)]
+    for k in range(9):
+        c.R[k] = R[k]
+    for k in range(3):
+        c.t[k] = t[k]
+    return c
+
+
+def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1) -> gm_opts:
+    o = gm_opts()
+    for k in range(3):
+        o.bg[k] = float(bg[k])
+    o.cull_occluded = int(bool(cull_occluded))
+    o.sh_degree = int(sh_degree)
+    return o
+
+
+def _p(t: Optional[torch.Tensor], dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("expected %s, got %s" % (dtype, t.dtype))
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != GM_OK:
+        raise GmError(status, where, lib().gm_last_error().decode())
+
+
+F32, I32, U8, I64 = torch.float32, torch.int32, torch.uint8, torch.int64
+
+
+# -------------------------------------------------------- the seven calls --
+
+def gm_bin_triangles_workspace_size(nF: int, cap: int, width: int, height: int) -> int:
+    return int(lib().gm_bin_triangles_workspace_size(nF, cap, width, height))
+
+
+def gm_bin_triangles(cam: gm_camera, V, F, tile_range, tri_ids, cap: int, counters, ws, sync: bool = True):
+    """Returns the needed number of entries when ``sync`` (K read back to the
+    host), else None; raises GmError(GM_ERR_CAPACITY) when K > cap."""
+    k = C.c_int32(0)
+    st = lib().gm_bin_triangles(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(tile_range, I32),
+                                _p(tri_ids, I32), cap, _p(counters, I32), C.byref(k) if sync else None,
+                                _p(ws), ws.numel() * ws.element_size(), _stream())
+    if st == GM_ERR_CAPACITY:
+        raise GmError(st, "gm_bin_triangles", "capacity %d < needed %d" % (cap, k.value))
+    _check(st, "gm_bin_triangles")
+    return k.value if sync else None
+
+
+def gm_zbuffer(cam: gm_camera, V, F, tile_range, tri_ids, face_id):
+    _check(lib().gm_zbuffer(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(tile_range, I32),
+                            _p(tri_ids, I32), _p(face_id, I32), _stream()), "gm_zbuffer")
+
+
+def gm_interp_mesh(cam: gm_camera, V, F, vcol, face_id, mesh_depth, mesh_rgb, tile_far, tile_full):
+    _check(lib().gm_interp_mesh(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(vcol, F32),
+                                _p(face_id, I32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(tile_far, F32),
+                                _p(tile_full, U8), _stream()), "gm_interp_mesh")
+
+
+def gm_project_gaussians(cam: gm_camera, opts: gm_opts, means, log_scales, quats, logits, colors, splats, radii,
+                         tiles_touched):
+    _check(lib().gm_project_gaussians(C.byref(cam), C.byref(opts), means.shape[0], _p(means, F32),
+                                      _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
+                                      _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32), _stream()),
+           "gm_project_gaussians")
+
+
+def gm_bin_sort_gaussians_workspace_size(N: int, cap: int, width: int, height: int) -> int:
+    return int(lib().gm_bin_sort_gaussians_workspace_size(N, cap, width, height))
+
+
+def gm_bin_sort_gaussians(cam: gm_camera, opts: gm_opts, splats, radii, tile_far, tile_full, keys, gids, tile_range,
+                          cap: int, counters, ws, sync: bool = True):
+    k = C.c_int32(0)
+    st = lib().gm_bin_sort_gaussians(C.byref(cam), C.byref(opts), radii.shape[0], _p(splats, F32), _p(radii, I32),
+                                     _p(tile_far, F32), _p(tile_full, U8), _p(keys, I64), _p(gids, I32),
+                                     _p(tile_range, I32), cap, _p(counters, I32), C.byref(k) if sync else None,
+                                     _p(ws), ws.numel() * ws.element_size(), _stream())
+    if st == GM_ERR_CAPACITY:
+        raise GmError(st, "gm_bin_sort_gaussians", "capacity %d < needed %d" % (cap, k.value))
+    _check(st, "gm_bin_sort_gaussians")
+    return k.value if sync else None
+
+
+def gm_composite_hybrid_fwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
+                            out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None):
+    _check(lib().gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
+                                         _p(gids, I32),
+                                         _p(splats, F32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
+                                         _p(out_rgb, F32), _p(out_depth, F32), _p(out_alpha, F32), _p(T_final, F32),
+                                         _p(n_contrib, I32), _p(stats, I64), _stream()), "gm_composite_hybrid_fwd")
+
+
+def gm_composite_hybrid_bwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
+                            T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, V=None, F=None, vcol=None,
+                            v_verts=None, v_vcol=None, stats=None):
+    nV = 0 if V is None else V.shape[0]
+    nF = 0 if F is None else F.shape[0]
+    _check(lib().gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
+                                         _p(gids, I32),
+                                         _p(splats, F32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
+                                         _p(T_final, F32), _p(n_contrib, I32), _p(g_rgb, F32), _p(g_depth, F32),
+                                         _p(g_alpha, F32), _p(v_splats, F32), _p(V, F32), nV, _p(F, I32), nF,
+                                         _p(vcol, F32), _p(v_verts, F32), _p(v_vcol, F32), _p(stats, I64), _stream()),
+           "gm_composite_hybrid_bwd")
+
+
+# ------------------------------------------------------------- renderer --
+
+class HybridRenderer:
+    """One camera's forward / backward pass through the seven calls.
+
+    ``upload`` copies a scene's mesh and Gaussians to the device; ``forward``
+    renders (rgb, depth, alpha); ``backward`` takes dL/d(rgb, depth, alpha)
+    and returns dL/d(splats) and dL/d(vertex positions, colours).  Buffers
+    are kept between calls; the tile-entry capacities grow on demand (a
+    GM_ERR_CAPACITY status triggers one reallocation and a retry).  With
+    ``sync=False`` the binning calls do not read K back, so a whole step can
+    be captured in a CUDA graph; the caller then checks ``overflowed()``.
+    """
+
+    def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25):
+        self.cam_desc = cam
+        self.cam = make_camera(cam)
+        self.W, self.H = int(cam.width), int(cam.height)
+        self.TW, self.TH = (self.W + TILE - 1) // TILE, (self.H + TILE - 1) // TILE
+        self.T = self.TW * self.TH
+        self.bg = tuple(float(x) for x in bg)
+        self.cull = bool(cull_occluded)
+        self.dev = torch.device(device)
+        self.headroom = headroom
+        self.tri_cap = 0
+        self.g_cap = 0
+        self.sh_degree = -1
+        d = self.dev
+        H, W = self.H, self.W
+        self.tri_range = torch.zeros(self.T, 2, dtype=I32, device=d)
+        self.g_range = torch.zeros(self.T, 2, dtype=I32, device=d)
+        self.tri_counters = torch.zeros(4, dtype=I32, device=d)
+        self.g_counters = torch.zeros(4, dtype=I32, device=d)
+        self.face_id = torch.empty(H, W, dtype=I32, device=d)
+        self.mesh_depth = torch.empty(H, W, dtype=F32, device=d)
+        self.mesh_rgb = torch.empty(H, W, 3, dtype=F32, device=d)
+        self.tile_far = torch.empty(self.T, dtype=F32, device=d)
+        self.tile_full = torch.empty(self.T, dtype=U8, device=d)
+        self.out_rgb = torch.empty(H, W, 3, dtype=F32, device=d)
+        self.out_depth = torch.empty(H, W, dtype=F32, device=d)
+        self.out_alpha = torch.empty(H, W, dtype=F32, device=d)
+        self.T_final = torch.empty(H, W, dtype=F32, device=d)
+        self.n_contrib = torch.empty(H, W, dtype=I32, device=d)
+
+    def set_camera(self, cam):
+        assert int(cam.width) == self.W and int(cam.height) == self.H
+        self.cam_desc = cam
+        self.cam = make_camera(cam)
+
+    @property
+    def opts(self) -> gm_opts:
+        return make_opts(self.bg, self.cull, self.sh_degree)
+
+    def upload(self, mesh, gaussians):
+        d = self.dev
+
+        def t(x, dt):
+            return torch.as_tensor(x).to(device=d, dtype=dt).contiguous()
+
+        self.V, self.F, self.vcol = t(mesh.verts, F32), t(mesh.faces, I32), t(mesh.vcol, F32)
+        self.means, self.log_scales = t(gaussians.means, F32), t(gaussians.log_scales, F32)
+        self.quats, self.logits = t(gaussians.quats, F32), t(gaussians.logits, F32)
+        self.colors = t(gaussians.colors, F32)
+        self.sh_degree = int(gaussians.sh_degree)
+        self._alloc_gauss(int(self.means.shape[0]))
+        self._alloc_tri(max(self.tri_cap, 1))
+
+    def _alloc_gauss(self, N):
+        d = self.dev
+        self.N = N
+        self.splats = torch.zeros(N, SPLAT_STRIDE, dtype=F32, device=d)
+        self.radii = torch.zeros(N, dtype=I32, device=d)
+        self.tiles_touched = torch.zeros(N, dtype=I32, device=d)
+        self.v_splats = torch.zeros(N, SPLAT_STRIDE, dtype=F32, device=d)
+        self._alloc_g(max(self.g_cap, 1))
+
+    def _alloc_g(self, cap):
+        d = self.dev
+        self.g_cap = cap
+        self.keys = torch.empty(cap, dtype=I64, device=d)
+        self.gids = torch.empty(cap, dtype=I32, device=d)
+        nb = gm_bin_sort_gaussians_workspace_size(self.N, cap, self.W, self.H)
+        self.g_ws = torch.empty((nb + 15) // 16 * 16, dtype=U8, device=d)
+
+    def _alloc_tri(self, cap):
+        d = self.dev
+        self.tri_cap = cap
+        self.tri_ids = torch.empty(cap, dtype=I32, device=d)
+        nb = gm_bin_triangles_workspace_size(int(self.F.shape[0]), cap, self.W, self.H)
+        self.tri_ws = torch.empty((nb + 15) // 16 * 16, dtype=U8, device=d)
+
+    def _grow(self, needed):
+        return max(int(needed * self.headroom) + 16, 16)
+
+    def forward(self, sync: bool = True):
+        cam, opts = self.cam, self.opts
+        for attempt in range(2):
+            try:
+                k = gm_bin_triangles(cam, self.V, self.F, self.tri_range, self.tri_ids, self.tri_cap,
+                                     self.tri_counters, self.tri_ws, sync=sync)
+                self.K_tri = k
+                break
+            except GmError as e:
+                if e.status != GM_ERR_CAPACITY or attempt:
+                    raise
+                self._alloc_tri(self._grow(int(self.tri_counters[GM_CNT_K].item())))
+        gm_zbuffer(cam, self.V, self.F, self.tri_range, self.tri_ids, self.face_id)
+        gm_interp_mesh(cam, self.V, self.F, self.vcol, self.face_id, self.mesh_depth, self.mesh_rgb, self.tile_far,
+                       self.tile_full)
+        gm_project_gaussians(cam, opts, self.means, self.log_scales, self.quats, self.logits, self.colors,
+                             self.splats, self.radii, self.tiles_touched)
+        for attempt in range(2):
+            try:
+                k = gm_bin_sort_gaussians(cam, opts, self.splats, self.radii, self.tile_far, self.tile_full,
+                                          self.keys, self.gids, self.g_range, self.g_cap, self.g_counters,
+                                          self.g_ws, sync=sync)
+                self.K_gauss = k
+                break
+            except GmError as e:
+                if e.status != GM_ERR_CAPACITY or attempt:
+                    raise
+                self._alloc_g(self._grow(int(self.g_counters[GM_CNT_K].item())))
+        gm_composite_hybrid_fwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
+                                self.face_id, self.out_rgb, self.out_depth, self.out_alpha, self.T_final,
+                                self.n_contrib)
+        return self.out_rgb, self.out_depth, self.out_alpha
+
+    def backward(self, g_rgb, g_depth, g_alpha, mesh_grads: bool = True):
+        self.v_splats.zero_()
+        if mesh_grads:
+            if not hasattr(self, "v_verts") or self.v_verts.shape != self.V.shape:
+                self.v_verts = torch.zeros_like(self.V)
+                self.v_vcol = torch.zeros_like(self.vcol)
+            self.v_verts.zero_()
+            self.v_vcol.zero_()
+        gm_composite_hybrid_bwd(self.cam, self.opts, self.g_range, self.gids, self.splats, self.mesh_depth,
+                                self.mesh_rgb, self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha,
+                                self.v_splats, self.V if mesh_grads else None, self.F if mesh_grads else None,
+                                self.vcol if mesh_grads else None, self.v_verts if mesh_grads else None,
+                                self.v_vcol if mesh_grads else None)
+        if mesh_grads:
+            return self.v_splats, self.v_verts, self.v_vcol
+        return self.v_splats, None, None
+
+    def overflowed(self) -> bool:
+        f = int(self.tri_counters[GM_CNT_FLAGS].item()) | int(self.g_counters[GM_CNT_FLAGS].item())
+        return bool(f & (GM_FLAG_OVERFLOW | GM_FLAG_TIMEOUT))

@@ -1,0 +1,234 @@
+// extern "C" entry points of libgm (declared in include/gm.h): argument
+// checks, workspace carving, launches on the caller's stream, status codes.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "gm_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where)
+{
+    return fail(GM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_cam(const gm_camera* cam)
+{
+    if (!cam) return fail(GM_ERR_INVALID_ARG, "camera is NULL");
+    if (cam->width <= 0 || cam->height <= 0) return fail(GM_ERR_INVALID_ARG, "image size %dx%d", cam->width, cam->height);
+    if (cam->width > (1 << 20) || cam->height > (1 << 20))
+        return fail(GM_ERR_INVALID_ARG, "image size %dx%d too large", cam->width, cam->height);
+    const float v[6] = {cam->fx, cam->fy, cam->cx, cam->cy, cam->near_plane, cam->far_plane};
+    for (float x : v)
+        if (!isfinite(x)) return fail(GM_ERR_INVALID_ARG, "camera intrinsics must be finite");
+    if (!(cam->fx > 0.0f) || !(cam->fy > 0.0f)) return fail(GM_ERR_INVALID_ARG, "focal lengths must be > 0");
+    if (!(cam->near_plane > 0.0f) || !(cam->far_plane > cam->near_plane))
+        return fail(GM_ERR_INVALID_ARG, "need 0 < near < far");
+    for (int i = 0; i < 9; ++i)
+        if (!isfinite(cam->R[i])) return fail(GM_ERR_INVALID_ARG, "R must be finite");
+    for (int i = 0; i < 3; ++i)
+        if (!isfinite(cam->t[i])) return fail(GM_ERR_INVALID_ARG, "t must be finite");
+    int64_t tiles = (int64_t)((cam->width + GM_TILE - 1) / GM_TILE) * ((cam->height + GM_TILE - 1) / GM_TILE);
+    if (tiles > (1 << 24)) return fail(GM_ERR_INVALID_ARG, "too many tiles");
+    return GM_OK;
+}
+
+#define GM_REQUIRE(cond, ...)                                   \
+    do {                                                        \
+        if (!(cond)) return fail(GM_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+// after the launches: optional host read-back of the counters
+int finish_binning(int32_t* counters, int32_t* K_host, int32_t cap, cudaStream_t s)
+{
+    if (!K_host) return GM_OK;
+    int32_t h[4];
+    cudaError_t e = cudaMemcpyAsync(h, counters, sizeof(h), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading counters");
+    *K_host = h[GM_CNT_K];
+    if (h[GM_CNT_FLAGS] & GM_FLAG_TIMEOUT) return fail(GM_ERR_TIMEOUT, "a bounded inter-block wait gave up");
+    if (h[GM_CNT_K] > cap) return fail(GM_ERR_CAPACITY, "need %d entries, capacity %d", h[GM_CNT_K], cap);
+    return GM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gm_last_error(void) { return g_err; }
+
+size_t gm_bin_triangles_workspace_size(int32_t nF, int32_t cap, int32_t width, int32_t height)
+{
+    (void)width;
+    (void)height;
+    return gm::tri_bin_ws_bytes(nF < 0 ? 0 : nF, cap < 0 ? 0 : cap);
+}
+
+int gm_bin_triangles(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                     int32_t* tile_range, int32_t* tri_ids, int32_t cap, int32_t* counters, int32_t* K_host, void* ws,
+                     size_t ws_bytes, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0 && cap >= 0, "negative size");
+    GM_REQUIRE(nV == 0 || V, "V is NULL");
+    GM_REQUIRE(nF == 0 || F, "F is NULL");
+    GM_REQUIRE(tile_range && counters, "tile_range / counters is NULL");
+    GM_REQUIRE(cap == 0 || tri_ids, "tri_ids is NULL");
+    const size_t need = gm::tri_bin_ws_bytes(nF, cap);
+    GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
+    GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = gm::tri_bin(gm::make_cam(*cam), V, nV, F, nF, tile_range, tri_ids, cap, counters, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gm_bin_triangles");
+    return finish_binning(counters, K_host, cap, s);
+}
+
+int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+               const int32_t* tile_range, const int32_t* tri_ids, int32_t* face_id, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
+    GM_REQUIRE(nV == 0 || V, "V is NULL");
+    GM_REQUIRE(nF == 0 || F, "F is NULL");
+    GM_REQUIRE(tile_range && face_id, "tile_range / face_id is NULL");
+    GM_REQUIRE(tri_ids || nF == 0, "tri_ids is NULL");
+    cudaError_t e = gm::zbuffer(gm::make_cam(*cam), V, nV, F, tile_range, tri_ids, face_id, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_zbuffer");
+}
+
+int gm_interp_mesh(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF, const float* vcol,
+                   const int32_t* face_id, float* mesh_depth, float* mesh_rgb, float* tile_far, uint8_t* tile_full,
+                   void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
+    GM_REQUIRE(nV == 0 || (V && vcol), "V / vcol is NULL");
+    GM_REQUIRE(nF == 0 || F, "F is NULL");
+    GM_REQUIRE(face_id && mesh_depth && mesh_rgb && tile_far && tile_full, "an output is NULL");
+    cudaError_t e = gm::interp(gm::make_cam(*cam), V, nV, F, nF, vcol, face_id, mesh_depth, mesh_rgb, tile_far,
+                               tile_full, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_interp_mesh");
+}
+
+int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
+                         const float* log_scales, const float* quats, const float* logits, const float* colors,
+                         float* splats, int32_t* radii, int32_t* tiles_touched, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(N >= 0, "negative N");
+    GM_REQUIRE(opts->sh_degree >= -1 && opts->sh_degree <= 3, "sh_degree %d not in -1..3", opts->sh_degree);
+    if (N > 0) {
+        GM_REQUIRE(means && log_scales && quats && logits && colors, "an input is NULL");
+        GM_REQUIRE(splats && radii && tiles_touched, "an output is NULL");
+        GM_REQUIRE(aligned16(quats) && aligned16(splats), "quats / splats must be 16-byte aligned");
+        if (opts->sh_degree == 1 || opts->sh_degree == 3)
+            GM_REQUIRE(aligned16(colors), "SH coefficients must be 16-byte aligned");
+    }
+    cudaError_t e = gm::project(gm::make_cam(*cam), opts->sh_degree, N, means, log_scales, quats, logits, colors, splats,
+                                radii, tiles_touched, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians");
+}
+
+size_t gm_bin_sort_gaussians_workspace_size(int32_t N, int32_t cap, int32_t width, int32_t height)
+{
+    (void)width;
+    (void)height;
+    return gm::gauss_bin_ws_bytes(N < 0 ? 0 : N, cap < 0 ? 0 : cap);
+}
+
+int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* splats,
+                          const int32_t* radii, const float* tile_far, const uint8_t* tile_full, uint64_t* keys,
+                          int32_t* gids, int32_t* tile_range, int32_t cap, int32_t* counters, int32_t* K_host,
+                          void* ws, size_t ws_bytes, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(N >= 0 && cap >= 0, "negative size");
+    GM_REQUIRE(N == 0 || (splats && radii), "splats / radii is NULL");
+    GM_REQUIRE(N == 0 || aligned16(splats), "splats must be 16-byte aligned");
+    GM_REQUIRE(!opts->cull_occluded || (tile_far && tile_full), "cull_occluded needs tile_far and tile_full");
+    GM_REQUIRE(tile_range && counters, "tile_range / counters is NULL");
+    GM_REQUIRE(cap == 0 || (keys && gids), "keys / gids is NULL");
+    const size_t need = gm::gauss_bin_ws_bytes(N, cap);
+    GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
+    GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), opts->cull_occluded != 0, N, splats, radii, tile_far,
+                                       tile_full, keys, gids, tile_range, cap, counters, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gm_bin_sort_gaussians");
+    return finish_binning(counters, K_host, cap, s);
+}
+
+int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const int32_t* tile_range,
+                            const int32_t* gids,
+                            const float* splats, const float* mesh_depth, const float* mesh_rgb,
+                            const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha, float* T_final,
+                            int32_t* n_contrib, uint64_t* stats, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id, "an input is NULL");
+    GM_REQUIRE(out_rgb && out_depth && out_alpha && T_final && n_contrib, "an output is NULL");
+    GM_REQUIRE(N >= 0, "negative N");
+    GM_REQUIRE(N == 0 || (splats && gids), "splats / gids is NULL");
+    GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
+    cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, tile_range, gids, splats, mesh_depth, mesh_rgb,
+                                      face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, stats,
+                                      (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_fwd");
+}
+
+int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const int32_t* tile_range,
+                            const int32_t* gids,
+                            const float* splats, const float* mesh_depth, const float* mesh_rgb,
+                            const int32_t* face_id, const float* T_final, const int32_t* n_contrib,
+                            const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
+                            const float* V, int32_t nV, const int32_t* F, int32_t nF, const float* vcol,
+                            float* v_verts, float* v_vcol, uint64_t* stats, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id && T_final && n_contrib, "an input is NULL");
+    GM_REQUIRE(g_rgb && g_depth && g_alpha, "an upstream gradient is NULL");
+    GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
+    GM_REQUIRE(!v_splats || aligned16(v_splats), "v_splats must be 16-byte aligned");
+    GM_REQUIRE(nV >= 0 && nF >= 0 && N >= 0, "negative size");
+    GM_REQUIRE(N == 0 || !v_splats || (splats && gids), "splats / gids is NULL");
+    const bool mesh_grads = v_verts || v_vcol;
+    if (mesh_grads) GM_REQUIRE(v_verts && v_vcol && (nF == 0 || (F && V && vcol)), "mesh gradient arguments incomplete");
+    cudaStream_t s = (cudaStream_t)stream;
+    const gm::Cam c = gm::make_cam(*cam);
+    cudaError_t e = cudaSuccess;
+    if (v_splats)
+        e = gm::composite_bwd(c, opts->bg, N, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id, T_final, n_contrib,
+                              g_rgb, g_depth, g_alpha, v_splats, stats, s);
+    if (e == cudaSuccess && mesh_grads && nF > 0)
+        e = gm::mesh_bwd(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, v_verts, v_vcol, s);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_bwd");
+}
+
+}  // extern "C"

@@ -1,0 +1,318 @@
+// Gaussian side of the hybrid renderer ("A Lightweight and Differentiable
+// Renderer for Joint Mesh and 3D Gaussian Splat Scenes", Hybrid rendering):
+// EWA projection with SH colour, and the tile binning by 64-bit
+// (tile | depth) keys with the per-tile occlusion cull.
+#include <algorithm>
+
+#include "gm_internal.cuh"
+
+namespace gm {
+namespace {
+
+// Real spherical harmonics, index l*l + l + m (m = -l..l), orthonormal on the
+// sphere, without the Condon-Shortley phase: e.g. Y_1,-1 = sqrt(3/4pi) y.
+constexpr float SH_C0 = 0.28209479177387814f;   // 1/(2 sqrt(pi))
+constexpr float SH_C1 = 0.4886025119029199f;    // sqrt(3/(4 pi))
+constexpr float SH_C2a = 1.0925484305920792f;   // sqrt(15/pi)/2
+constexpr float SH_C2c = 0.31539156525252005f;  // sqrt(5/pi)/4
+constexpr float SH_C2e = 0.5462742152960396f;   // sqrt(15/pi)/4
+constexpr float SH_C3a = 0.5900435899266435f;   // sqrt(35/(2 pi))/4
+constexpr float SH_C3b = 2.890611442640554f;    // sqrt(105/pi)/2
+constexpr float SH_C3c = 0.4570457994644658f;   // sqrt(21/(2 pi))/4
+constexpr float SH_C3d = 0.3731763325901154f;   // sqrt(7/pi)/4
+constexpr float SH_C3f = 1.445305721320277f;    // sqrt(105/pi)/4
+
+template <int DEG>
+__device__ __forceinline__ void sh_basis(float x, float y, float z, float* Y)
+{
+    Y[0] = SH_C0;
+    if (DEG >= 1) {
+        Y[1] = SH_C1 * y;
+        Y[2] = SH_C1 * z;
+        Y[3] = SH_C1 * x;
+    }
+    if (DEG >= 2) {
+        const float xx = x * x, yy = y * y, zz = z * z;
+        Y[4] = SH_C2a * x * y;
+        Y[5] = SH_C2a * y * z;
+        Y[6] = SH_C2c * (3.0f * zz - 1.0f);
+        Y[7] = SH_C2a * x * z;
+        Y[8] = SH_C2e * (xx - yy);
+        if (DEG >= 3) {
+            Y[9] = SH_C3a * y * (3.0f * xx - yy);
+            Y[10] = SH_C3b * x * y * z;
+            Y[11] = SH_C3c * y * (5.0f * zz - 1.0f);
+            Y[12] = SH_C3d * z * (5.0f * zz - 3.0f);
+            Y[13] = SH_C3c * x * (5.0f * zz - 1.0f);
+            Y[14] = SH_C3f * z * (xx - yy);
+            Y[15] = SH_C3a * x * (xx - 3.0f * yy);
+        }
+    }
+}
+
+struct ProjConsts {
+    float limx_pos, limx_neg, limy_pos, limy_neg;  // clamp of tx/tz, ty/tz
+    float cpx, cpy, cpz;                           // camera centre in world space
+};
+
+// DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
+template <int DEG>
+__global__ void __launch_bounds__(256)
+k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+          const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
+          float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= N) return;
+    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0, o2 = o0;
+    int rad = 0, touched = 0;
+    const float mx = __ldg(means + 3 * (int64_t)g), my = __ldg(means + 3 * (int64_t)g + 1),
+                mz = __ldg(means + 3 * (int64_t)g + 2);
+    const float tx = fmaf(c.R[0], mx, fmaf(c.R[1], my, fmaf(c.R[2], mz, c.t[0])));
+    const float ty = fmaf(c.R[3], mx, fmaf(c.R[4], my, fmaf(c.R[5], mz, c.t[1])));
+    const float tz = fmaf(c.R[6], mx, fmaf(c.R[7], my, fmaf(c.R[8], mz, c.t[2])));
+    if (tz > c.znear && tz <= c.zfar) {
+        // M = R(q) diag(exp(log_s)); camera-frame factor WM = R_cw M
+        const float4 q = __ldg(quats + g);
+        const float qi = 1.0f / sqrtf(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
+        const float w = q.x * qi, x = q.y * qi, y = q.z * qi, z = q.w * qi;
+        const float Rq[3][3] = {{1.f - 2.f * (y * y + z * z), 2.f * (x * y - w * z), 2.f * (x * z + w * y)},
+                                {2.f * (x * y + w * z), 1.f - 2.f * (x * x + z * z), 2.f * (y * z - w * x)},
+                                {2.f * (x * z - w * y), 2.f * (y * z + w * x), 1.f - 2.f * (x * x + y * y)}};
+        float s[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) s[k] = expf(__ldg(log_scales + 3 * (int64_t)g + k));
+        float WM[3][3];
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+                WM[r][k] = (c.R[3 * r] * Rq[0][k] + c.R[3 * r + 1] * Rq[1][k] + c.R[3 * r + 2] * Rq[2][k]) * s[k];
+        // Jacobian of the pinhole map at the clamped direction; G = J WM, Sigma2 = G G^T + 0.3 I
+        const float iz = 1.0f / tz;
+        const float txc = tz * fminf(pc.limx_pos, fmaxf(-pc.limx_neg, tx * iz));
+        const float tyc = tz * fminf(pc.limy_pos, fmaxf(-pc.limy_neg, ty * iz));
+        const float j00 = c.fx * iz, j02 = -c.fx * txc * iz * iz;
+        const float j11 = c.fy * iz, j12 = -c.fy * tyc * iz * iz;
+        float G0[3], G1[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            G0[k] = fmaf(j00, WM[0][k], j02 * WM[2][k]);
+            G1[k] = fmaf(j11, WM[1][k], j12 * WM[2][k]);
+        }
+        const float a = G0[0] * G0[0] + G0[1] * G0[1] + G0[2] * G0[2] + 0.3f;
+        const float b = G0[0] * G1[0] + G0[1] * G1[1] + G0[2] * G1[2];
+        const float cc = G1[0] * G1[0] + G1[1] * G1[1] + G1[2] * G1[2] + 0.3f;
+        const float det = a * cc - b * b;
+        if (det > 0.0f) {
+            const float m = 0.5f * (a + cc), h = 0.5f * (a - cc);
+            const float lam = m + sqrtf(h * h + b * b);
+            rad = (int)ceilf(3.0f * sqrtf(lam));
+            const float u = fmaf(c.fx * tx, iz, c.cx);
+            const float v = fmaf(c.fy * ty, iz, c.cy);
+            int x0, y0, x1, y1;
+            if (gauss_rect(c, u, v, rad, x0, y0, x1, y1)) {
+                touched = (x1 - x0) * (y1 - y0);
+                const float idet = 1.0f / det;
+                const float op = 1.0f / (1.0f + expf(-__ldg(logits + g)));
+                float rgb[3];
+                if (DEG < 0) {
+#pragma unroll
+                    for (int ch = 0; ch < 3; ++ch) rgb[ch] = __ldg(colors + 3 * (int64_t)g + ch);
+                } else {
+                    constexpr int K = (DEG < 0 ? 1 : (DEG + 1) * (DEG + 1));
+                    float dx = mx - pc.cpx, dy = my - pc.cpy, dz = mz - pc.cpz;
+                    const float dn = 1.0f / sqrtf(dx * dx + dy * dy + dz * dz);
+                    dx *= dn; dy *= dn; dz *= dn;
+                    float Y[16];
+                    sh_basis<DEG>(dx, dy, dz, Y);
+                    float acc[3] = {0.5f, 0.5f, 0.5f};
+                    const float* cf = colors + (int64_t)g * (3 * K);
+                    if ((3 * K) % 4 == 0) {
+                        const float4* cf4 = reinterpret_cast<const float4*>(cf);
+#pragma unroll
+                        for (int v4 = 0; v4 < 3 * K / 4; ++v4) {
+                            const float4 e = __ldg(cf4 + v4);
+                            const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                            for (int l = 0; l < 4; ++l) {
+                                const int idx = 4 * v4 + l;
+                                acc[idx % 3] = fmaf(Y[idx / 3], ev[l], acc[idx % 3]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int idx = 0; idx < 3 * K; ++idx) acc[idx % 3] = fmaf(Y[idx / 3], __ldg(cf + idx), acc[idx % 3]);
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 3; ++ch) rgb[ch] = fmaxf(acc[ch], 0.0f);
+                }
+                o0 = make_float4(u, v, cc * idet, -b * idet);
+                o1 = make_float4(a * idet, op, rgb[0], rgb[1]);
+                o2 = make_float4(rgb[2], tz, 0.0f, 0.0f);
+            } else {
+                rad = 0;
+            }
+        }
+    }
+    splats[3 * (int64_t)g] = o0;
+    splats[3 * (int64_t)g + 1] = o1;
+    splats[3 * (int64_t)g + 2] = o2;
+    radii[g] = rad;
+    tiles_touched[g] = touched;
+}
+
+// ------------------------------------------------------------- binning ----
+
+__device__ __forceinline__ bool culled(bool cull, const float* __restrict__ tile_far,
+                                       const uint8_t* __restrict__ tile_full, int t, float depth)
+{
+    return cull && __ldg(tile_full + t) && depth >= __ldg(tile_far + t);
+}
+
+__global__ void __launch_bounds__(256)
+k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
+              const float* __restrict__ tile_far, const uint8_t* __restrict__ tile_full, int32_t* __restrict__ counts,
+              int32_t* counters)
+{
+    __shared__ int s_pre[8];
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    int pre = 0, post = 0;
+    if (g < N) {
+        const int r = radii[g];
+        int x0, y0, x1, y1;
+        if (r > 0) {
+            const float4 s0 = splats[3 * (int64_t)g];
+            const float depth = splats[3 * (int64_t)g + 2].y;
+            if (gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1)) {
+                pre = (x1 - x0) * (y1 - y0);
+                if (!cull) {
+                    post = pre;
+                } else {
+                    for (int ty = y0; ty < y1; ++ty)
+                        for (int tx = x0; tx < x1; ++tx) post += !culled(true, tile_far, tile_full, ty * c.TW + tx, depth);
+                }
+            }
+        }
+        counts[g] = post;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    if ((threadIdx.x & 31) == 0) s_pre[threadIdx.x >> 5] = pre;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int w = 0; w < 8; ++w) t += s_pre[w];
+        if (t) atomicAdd(counters + GM_CNT_K_PRECULL, t);
+    }
+}
+
+__global__ void __launch_bounds__(256)
+k_gauss_emit(Cam c, bool cull, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
+             const float* __restrict__ tile_far, const uint8_t* __restrict__ tile_full,
+             const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
+             int32_t* __restrict__ vals)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
+    if (g >= N) return;
+    const int r = radii[g];
+    if (r <= 0) return;
+    const float4 s0 = splats[3 * (int64_t)g];
+    const float depth = splats[3 * (int64_t)g + 2].y;
+    int x0, y0, x1, y1;
+    if (!gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1)) return;
+    const uint32_t dbits = __float_as_uint(depth);
+    int64_t o = offsets[g];
+    for (int ty = y0; ty < y1; ++ty)
+        for (int tx = x0; tx < x1; ++tx) {
+            const int t = ty * c.TW + tx;
+            if (culled(cull, tile_far, tile_full, t, depth)) continue;
+            if (o >= cap) return;
+            keys[o] = ((uint64_t)(uint32_t)t << 32) | dbits;
+            vals[o] = g;
+            ++o;
+        }
+}
+
+int tile_bits(int n_tiles) { return n_tiles > 1 ? 32 - __builtin_clz((unsigned)(n_tiles - 1)) : 0; }
+
+size_t a256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+}  // namespace
+
+cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
+                    const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
+                    int32_t* tiles_touched, cudaStream_t s)
+{
+    if (N <= 0) return cudaSuccess;
+    ProjConsts pc;
+    pc.limx_pos = 1.3f * ((float)c.W - c.cx) / c.fx;
+    pc.limx_neg = 1.3f * c.cx / c.fx;
+    pc.limy_pos = 1.3f * ((float)c.H - c.cy) / c.fy;
+    pc.limy_neg = 1.3f * c.cy / c.fy;
+    // camera centre = -R^T t
+    pc.cpx = -(c.R[0] * c.t[0] + c.R[3] * c.t[1] + c.R[6] * c.t[2]);
+    pc.cpy = -(c.R[1] * c.t[0] + c.R[4] * c.t[1] + c.R[7] * c.t[2]);
+    pc.cpz = -(c.R[2] * c.t[0] + c.R[5] * c.t[1] + c.R[8] * c.t[2]);
+    const int grid = (N + 255) / 256;
+    auto* q4 = reinterpret_cast<const float4*>(quats);
+    auto* s4 = reinterpret_cast<float4*>(splats);
+#define GM_PROJ(D) k_project<D><<<grid, 256, 0, s>>>(c, pc, N, means, log_scales, q4, logits, colors, s4, radii, tiles_touched)
+    switch (sh_degree) {
+        case -1: GM_PROJ(-1); break;
+        case 0: GM_PROJ(0); break;
+        case 1: GM_PROJ(1); break;
+        case 2: GM_PROJ(2); break;
+        case 3: GM_PROJ(3); break;
+        default: return cudaErrorInvalidValue;
+    }
+#undef GM_PROJ
+    return cudaGetLastError();
+}
+
+size_t gauss_bin_ws_bytes(int N, int cap)
+{
+    int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
+    return scan_ws_bytes(n) + 2 * a256(sizeof(int32_t) * n) + sort_ws_bytes(k);
+}
+
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, const int32_t* radii,
+                           const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
+                           int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
+{
+    int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
+    uint8_t* b = (uint8_t*)ws;
+    ScanWs sw;
+    b += carve_scan_ws(b, n, sw);
+    int32_t* counts = (int32_t*)b;
+    b += a256(sizeof(int32_t) * n);
+    int32_t* offsets = (int32_t*)b;
+    b += a256(sizeof(int32_t) * n);
+    SortWs so;
+    carve_sort_ws(b, k, so);
+
+    cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+    const int T = c.TW * c.TH;
+    const int end_bit = 32 + tile_bits(T);
+    const int passes = sort_passes(0, end_bit);
+    uint64_t* ek = passes % 2 ? so.keys_alt : keys;
+    int32_t* ev = passes % 2 ? so.vals_alt : gids;
+    if (N > 0) {
+        auto* s4 = reinterpret_cast<const float4*>(splats);
+        k_gauss_count<<<(N + 255) / 256, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, counts, counters);
+        if ((e = exclusive_scan(counts, offsets, N, counters, sw, s)) != cudaSuccess) return e;
+        k_gauss_emit<<<(N + 255) / 256, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, offsets, cap,
+                                                     counters, ek, ev);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (passes % 2)
+            e = radix_sort(so.keys_alt, so.vals_alt, keys, gids, cap, 0, end_bit, counters, so, s);
+        else
+            e = radix_sort(keys, gids, so.keys_alt, so.vals_alt, cap, 0, end_bit, counters, so, s);
+        if (e != cudaSuccess) return e;
+    }
+    return tile_ranges(keys, N > 0 ? cap : 0, counters, tile_range, T, s);
+}
+
+}  // namespace gm

@@ -1,0 +1,204 @@
+// Internal definitions shared by the libgm CUDA sources (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gm.h"
+
+namespace gm {
+
+constexpr int TILE = GM_TILE;
+constexpr int TILE_PIX = TILE * TILE;
+
+// Camera as passed to kernels (by value).
+struct Cam {
+    int W, H, TW, TH;
+    float fx, fy, cx, cy, znear, zfar;
+    float R[9];
+    float t[3];
+};
+
+inline Cam make_cam(const gm_camera& c)
+{
+    Cam k;
+    k.W = c.width;
+    k.H = c.height;
+    k.TW = (c.width + TILE - 1) / TILE;
+    k.TH = (c.height + TILE - 1) / TILE;
+    k.fx = c.fx; k.fy = c.fy; k.cx = c.cx; k.cy = c.cy;
+    k.znear = c.near_plane; k.zfar = c.far_plane;
+    for (int i = 0; i < 9; ++i) k.R[i] = c.R[i];
+    for (int i = 0; i < 3; ++i) k.t[i] = c.t[i];
+    return k;
+}
+
+// ---------------------------------------------------------------------------
+// Coverage arithmetic.  Face ids and triangle bins are integers decided from
+// fp32 arithmetic; these helpers evaluate each formula one correctly rounded
+// operation at a time, in the written order, with no fused multiply-add, so
+// the decisions are reproducible by any IEEE fp32 evaluation of the same
+// formulas:
+//   X_c = ((R0 X + R1 Y) + R2 Z) + t per row;   u = (fx x) / z + cx;
+//   e(a -> b, p) = (ub - ua)(py - va) - (vb - va)(px - ua).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float cam_row_rn(const Cam& c, int r, float X, float Y, float Z)
+{
+    float s = __fmul_rn(c.R[3 * r + 0], X);
+    s = __fadd_rn(s, __fmul_rn(c.R[3 * r + 1], Y));
+    s = __fadd_rn(s, __fmul_rn(c.R[3 * r + 2], Z));
+    return __fadd_rn(s, c.t[r]);
+}
+
+__device__ __forceinline__ float edge_rn(float ua, float va, float ub, float vb, float px, float py)
+{
+    float p = __fmul_rn(__fsub_rn(ub, ua), __fsub_rn(py, va));
+    float q = __fmul_rn(__fsub_rn(vb, va), __fsub_rn(px, ua));
+    return __fsub_rn(p, q);
+}
+
+struct Tri {
+    float u[3], v[3], z[3];
+    float area;          // edge function of v0 -> v1 at v2 (twice the signed area)
+    int x0, x1, y0, y1;  // inclusive pixel-centre box, clamped to the image
+};
+
+// Projects face f; returns false when it is not drawn: a vertex index out of
+// range, a vertex at or in front of the near plane (no clipping), zero area,
+// or a pixel-centre box that misses the image.
+__device__ __forceinline__ bool tri_setup(const Cam& c, const float* __restrict__ V, int nV,
+                                          const int32_t* __restrict__ F, int f, Tri& t)
+{
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        int vi = __ldg(F + 3 * (int64_t)f + k);
+        if (vi < 0 || vi >= nV) return false;
+        float X = __ldg(V + 3 * (int64_t)vi), Y = __ldg(V + 3 * (int64_t)vi + 1), Z = __ldg(V + 3 * (int64_t)vi + 2);
+        float x = cam_row_rn(c, 0, X, Y, Z);
+        float y = cam_row_rn(c, 1, X, Y, Z);
+        float z = cam_row_rn(c, 2, X, Y, Z);
+        if (!(z > c.znear)) return false;
+        t.z[k] = z;
+        t.u[k] = __fadd_rn(__fdiv_rn(__fmul_rn(c.fx, x), z), c.cx);
+        t.v[k] = __fadd_rn(__fdiv_rn(__fmul_rn(c.fy, y), z), c.cy);
+    }
+    t.area = edge_rn(t.u[0], t.v[0], t.u[1], t.v[1], t.u[2], t.v[2]);
+    if (!(t.area != 0.0f)) return false;
+    float umin = fminf(fminf(t.u[0], t.u[1]), t.u[2]);
+    float umax = fmaxf(fmaxf(t.u[0], t.u[1]), t.u[2]);
+    float vmin = fminf(fminf(t.v[0], t.v[1]), t.v[2]);
+    float vmax = fmaxf(fmaxf(t.v[0], t.v[1]), t.v[2]);
+    float x0 = fmaxf(ceilf(__fsub_rn(umin, 0.5f)), 0.0f);
+    float x1 = fminf(floorf(__fsub_rn(umax, 0.5f)), (float)(c.W - 1));
+    float y0 = fmaxf(ceilf(__fsub_rn(vmin, 0.5f)), 0.0f);
+    float y1 = fminf(floorf(__fsub_rn(vmax, 0.5f)), (float)(c.H - 1));
+    if (!(x0 <= x1) || !(y0 <= y1)) return false;
+    t.x0 = (int)x0; t.x1 = (int)x1; t.y0 = (int)y0; t.y1 = (int)y1;
+    return true;
+}
+
+// Tile rectangle [x0, x1) x [y0, y1) of a projected Gaussian of radius r:
+// floor((m - r) / 16) .. ceil((m + r) / 16), clamped to the tile grid.
+__device__ __forceinline__ bool gauss_rect(const Cam& c, float mx, float my, int r, int& x0, int& y0,
+                                           int& x1, int& y1)
+{
+    if (r <= 0) return false;
+    float fr = (float)r;
+    float fx0 = floorf(__fdiv_rn(__fsub_rn(mx, fr), 16.0f));
+    float fx1 = ceilf(__fdiv_rn(__fadd_rn(mx, fr), 16.0f));
+    float fy0 = floorf(__fdiv_rn(__fsub_rn(my, fr), 16.0f));
+    float fy1 = ceilf(__fdiv_rn(__fadd_rn(my, fr), 16.0f));
+    float TW = (float)c.TW, TH = (float)c.TH;
+    fx0 = fminf(fmaxf(fx0, 0.0f), TW); fx1 = fminf(fmaxf(fx1, 0.0f), TW);
+    fy0 = fminf(fmaxf(fy0, 0.0f), TH); fy1 = fminf(fmaxf(fy1, 0.0f), TH);
+    x0 = (int)fx0; x1 = (int)fx1; y0 = (int)fy0; y1 = (int)fy1;
+    return x1 > x0 && y1 > y0;
+}
+
+// ---------------------------------------------------------------------------
+// Sort / scan (gm_sort.cu)
+// ---------------------------------------------------------------------------
+constexpr int SCAN_THREADS = 256;
+constexpr int SCAN_IPT = 16;
+constexpr int SCAN_PART = SCAN_THREADS * SCAN_IPT;
+constexpr int SORT_THREADS = 256;
+constexpr int SORT_IPT = 15;
+constexpr int SORT_PART = SORT_THREADS * SORT_IPT;
+constexpr int SORT_MAX_PASSES = 8;
+
+// bounded inter-block wait: polls before a waiting block gives up
+constexpr uint32_t SPIN_LIMIT = 1u << 22;
+
+struct ScanWs {
+    uint32_t* desc;    // [parts]
+    uint32_t* ticket;  // [1]
+    int parts;
+};
+
+struct SortWs {
+    uint64_t* keys_alt;  // [cap]
+    int32_t* vals_alt;   // [cap]
+    uint32_t* hist;      // [SORT_MAX_PASSES][256]
+    uint32_t* desc;      // [passes][max_parts][256]
+    uint32_t* tickets;   // [SORT_MAX_PASSES]
+    int max_parts;
+};
+
+size_t scan_ws_bytes(int64_t n);
+size_t sort_ws_bytes(int64_t cap);
+// carve workspaces out of a byte buffer; returns bytes used (256-aligned pieces)
+size_t carve_scan_ws(void* base, int64_t n, ScanWs& ws);
+size_t carve_sort_ws(void* base, int64_t cap, SortWs& ws);
+// bytes of ws that must be zero before each use (they start at the carve base)
+size_t scan_zero_bytes(const ScanWs& ws);
+
+// exclusive scan of counts[n] into offsets[n]; total -> counters[GM_CNT_K]
+cudaError_t exclusive_scan(const int32_t* counts, int32_t* offsets, int n, int32_t* counters,
+                           const ScanWs& ws, cudaStream_t s);
+// Sort (keys, values) ascending by key bits [begin_bit, end_bit), stable.
+// The count is min(counters[GM_CNT_K], cap), read on the device.  Input is in
+// (k0, v0); the result is in (k0, v0) when the number of passes is even and
+// in the alternate buffers otherwise -- sort_passes() tells which.
+int sort_passes(int begin_bit, int end_bit);
+cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int cap, int begin_bit,
+                       int end_bit, int32_t* counters, const SortWs& ws, cudaStream_t s);
+// tile_range[T][2] from sorted keys (tile id in the high 32 bits); range zeroed first
+cudaError_t tile_ranges(const uint64_t* keys, int cap, const int32_t* counters, int32_t* tile_range,
+                        int n_tiles, cudaStream_t s);
+
+int num_sms();
+
+// ---------------------------------------------------------------------------
+// Host launchers of the path's steps (enqueue on stream s, no synchronisation)
+// ---------------------------------------------------------------------------
+size_t tri_bin_ws_bytes(int nF, int cap);
+cudaError_t tri_bin(const Cam& c, const float* V, int nV, const int32_t* F, int nF, int32_t* tile_range,
+                    int32_t* tri_ids, int cap, int32_t* counters, void* ws, cudaStream_t s);
+cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, const int32_t* tile_range,
+                    const int32_t* tri_ids, int32_t* face_id, cudaStream_t s);
+cudaError_t interp(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
+                   const int32_t* face_id, float* mesh_depth, float* mesh_rgb, float* tile_far, uint8_t* tile_full,
+                   cudaStream_t s);
+cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
+                     const int32_t* face_id, const float* T_final, const float* g_rgb, const float* g_depth,
+                     float* v_verts, float* v_vcol, cudaStream_t s);
+
+cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
+                    const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
+                    int32_t* tiles_touched, cudaStream_t s);
+size_t gauss_bin_ws_bytes(int N, int cap);
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, const int32_t* radii,
+                           const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
+                           int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
+
+cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, const int32_t* tile_range, const int32_t* gids,
+                          const float* splats, const float* mesh_depth, const float* mesh_rgb,
+                          const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
+                          float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s);
+cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, const int32_t* tile_range, const int32_t* gids,
+                          const float* splats, const float* mesh_depth, const float* mesh_rgb,
+                          const int32_t* face_id, const float* T_final, const int32_t* n_contrib,
+                          const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
+                          uint64_t* stats, cudaStream_t s);
+
+}  // namespace gm

@@ -1,0 +1,428 @@
+// Mesh layer of the hybrid renderer ("A Lightweight and Differentiable
+// Renderer for Joint Mesh and 3D Gaussian Splat Scenes", Design Details >
+// Mesh rasterizer, items 1 and 2): triangle tile bins, the z-buffer, the
+// perspective-correct interpolation of depth and vertex colour, and its
+// backward pass to vertex positions and colours.
+#include "gm_internal.cuh"
+
+namespace gm {
+namespace {
+
+// ------------------------------------------------------------- bins ------
+
+__global__ void __launch_bounds__(256)
+k_tri_count(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
+            int32_t* __restrict__ counts)
+{
+    int f = blockIdx.x * blockDim.x + threadIdx.x;
+    if (f >= nF) return;
+    Tri t;
+    int n = 0;
+    if (tri_setup(c, V, nV, F, f, t))
+        n = (t.x1 / TILE - t.x0 / TILE + 1) * (t.y1 / TILE - t.y0 / TILE + 1);
+    counts[f] = n;
+}
+
+__global__ void __launch_bounds__(256)
+k_tri_emit(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
+           const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
+           int32_t* __restrict__ vals)
+{
+    int f = blockIdx.x * blockDim.x + threadIdx.x;
+    if (f == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
+    if (f >= nF) return;
+    Tri t;
+    if (!tri_setup(c, V, nV, F, f, t)) return;
+    int64_t o = offsets[f];
+    for (int ty = t.y0 / TILE; ty <= t.y1 / TILE; ++ty)
+        for (int tx = t.x0 / TILE; tx <= t.x1 / TILE; ++tx, ++o) {
+            if (o >= cap) return;
+            keys[o] = (uint64_t)(uint32_t)(ty * c.TW + tx) << 32;
+            vals[o] = f;
+        }
+}
+
+// ---------------------------------------------------------- z-buffer ------
+
+struct TriRec {
+    float u0, v0, u1, v1, u2, v2;
+    float area;
+    float w0, w1, w2;  // 1 / (area z_k): depth reciprocal = sum_k e_k w_k
+    int fid;
+    int x0, x1, y0, y1;
+};
+
+__global__ void __launch_bounds__(TILE_PIX)
+k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F,
+          const int2* __restrict__ tile_range, const int32_t* __restrict__ tri_ids, int32_t* __restrict__ face_id)
+{
+    __shared__ TriRec sm[TILE_PIX];
+    const int tile = blockIdx.x;
+    const int tx = tile % c.TW, ty = tile / c.TW;
+    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
+    const int j = ty * TILE + (threadIdx.x >> 4);
+    const bool inside = i < c.W && j < c.H;
+    const float px = (float)i + 0.5f, py = (float)j + 0.5f;
+    const int2 r = tile_range[tile];
+    float best = 0.0f;  // reciprocal depth of the winner (0 = none)
+    int best_f = -1;
+    for (int b = r.x; b < r.y; b += TILE_PIX) {
+        const int n = min(TILE_PIX, r.y - b);
+        if ((int)threadIdx.x < n) {
+            int f = tri_ids[b + threadIdx.x];
+            Tri t;
+            TriRec& q = sm[threadIdx.x];
+            if (tri_setup(c, V, nV, F, f, t)) {
+                q.u0 = t.u[0]; q.v0 = t.v[0]; q.u1 = t.u[1]; q.v1 = t.v[1]; q.u2 = t.u[2]; q.v2 = t.v[2];
+                q.area = t.area;
+                q.w0 = 1.0f / (t.area * t.z[0]);
+                q.w1 = 1.0f / (t.area * t.z[1]);
+                q.w2 = 1.0f / (t.area * t.z[2]);
+                q.fid = f;
+                q.x0 = t.x0; q.x1 = t.x1; q.y0 = t.y0; q.y1 = t.y1;
+            } else {
+                q.fid = -1;
+                q.x0 = 1; q.x1 = 0; q.y0 = 1; q.y1 = 0;
+            }
+        }
+        __syncthreads();
+        if (inside) {
+            for (int k = 0; k < n; ++k) {
+                const TriRec& q = sm[k];
+                if (i < q.x0 || i > q.x1 || j < q.y0 || j > q.y1) continue;
+                float e0 = edge_rn(q.u1, q.v1, q.u2, q.v2, px, py);
+                float e1 = edge_rn(q.u2, q.v2, q.u0, q.v0, px, py);
+                float e2 = edge_rn(q.u0, q.v0, q.u1, q.v1, px, py);
+                bool in = q.area > 0.0f ? (e0 >= 0.0f && e1 >= 0.0f && e2 >= 0.0f)
+                                        : (e0 <= 0.0f && e1 <= 0.0f && e2 <= 0.0f);
+                if (!in) continue;
+                float inv_d = fmaf(e0, q.w0, fmaf(e1, q.w1, e2 * q.w2));
+                if (inv_d > best) {  // lists ascend in face id: an equal depth keeps the smaller id
+                    best = inv_d;
+                    best_f = q.fid;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (inside) face_id[(int64_t)j * c.W + i] = best_f;
+}
+
+// ------------------------------------------------------------- interp -----
+
+struct Persp {
+    float u[3], v[3], z[3], x[3], y[3];
+    float e[3], area, lam[3], q[3], s, D, w[3];
+};
+
+// false when a vertex index is out of range (the face is then treated as absent)
+__device__ __forceinline__ bool load_face(const float* __restrict__ V, int nV, const int32_t* __restrict__ F,
+                                          int f, int vid[3], float X[3][3])
+{
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        vid[k] = __ldg(F + 3 * (int64_t)f + k);
+        if (vid[k] < 0 || vid[k] >= nV) return false;
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+        for (int d = 0; d < 3; ++d) X[k][d] = __ldg(V + 3 * (int64_t)vid[k] + d);
+    return true;
+}
+
+// perspective-correct weights at pixel centre (px, py)
+__device__ __forceinline__ void persp(const Cam& c, const float X[3][3], float px, float py, Persp& P)
+{
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        float x = fmaf(c.R[0], X[k][0], fmaf(c.R[1], X[k][1], fmaf(c.R[2], X[k][2], c.t[0])));
+        float y = fmaf(c.R[3], X[k][0], fmaf(c.R[4], X[k][1], fmaf(c.R[5], X[k][2], c.t[1])));
+        float z = fmaf(c.R[6], X[k][0], fmaf(c.R[7], X[k][1], fmaf(c.R[8], X[k][2], c.t[2])));
+        P.x[k] = x; P.y[k] = y; P.z[k] = z;
+        float iz = 1.0f / z;
+        P.u[k] = fmaf(c.fx * x, iz, c.cx);
+        P.v[k] = fmaf(c.fy * y, iz, c.cy);
+    }
+    P.area = (P.u[1] - P.u[0]) * (P.v[2] - P.v[0]) - (P.u[2] - P.u[0]) * (P.v[1] - P.v[0]);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int a = (k + 1) % 3, b = (k + 2) % 3;
+        P.e[k] = (P.u[b] - P.u[a]) * (py - P.v[a]) - (P.v[b] - P.v[a]) * (px - P.u[a]);
+    }
+    float ia = 1.0f / P.area;
+    P.s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        P.lam[k] = P.e[k] * ia;
+        P.q[k] = P.lam[k] / P.z[k];
+        P.s += P.q[k];
+    }
+    P.D = 1.0f / P.s;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) P.w[k] = P.q[k] * P.D;
+}
+
+__global__ void __launch_bounds__(TILE_PIX)
+k_interp(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
+         const float* __restrict__ vcol, const int32_t* __restrict__ face_id, float* __restrict__ mesh_depth,
+         float* __restrict__ mesh_rgb, float* __restrict__ tile_far, uint8_t* __restrict__ tile_full)
+{
+    __shared__ float s_max[TILE_PIX / 32];
+    const int tile = blockIdx.x;
+    const int tx = tile % c.TW, ty = tile / c.TW;
+    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
+    const int j = ty * TILE + (threadIdx.x >> 4);
+    const bool inside = i < c.W && j < c.H;
+    float D = INFINITY;
+    bool covered = false;
+    if (inside) {
+        const int64_t pix = (int64_t)j * c.W + i;
+        int f = face_id[pix];
+        float rgb[3] = {0.0f, 0.0f, 0.0f};
+        int vid[3];
+        float X[3][3];
+        if (f >= 0 && f < nF && load_face(V, nV, F, f, vid, X)) {
+            Persp P;
+            persp(c, X, (float)i + 0.5f, (float)j + 0.5f, P);
+            D = P.D;
+            covered = true;
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+#pragma unroll
+                for (int ch = 0; ch < 3; ++ch) rgb[ch] = fmaf(P.w[k], __ldg(vcol + 3 * (int64_t)vid[k] + ch), rgb[ch]);
+        }
+        mesh_depth[pix] = D;
+        mesh_rgb[3 * pix + 0] = rgb[0];
+        mesh_rgb[3 * pix + 1] = rgb[1];
+        mesh_rgb[3 * pix + 2] = rgb[2];
+    }
+    const int all = __syncthreads_and(!inside || covered);
+    float m = inside ? D : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float far = s_max[0];
+        for (int w = 1; w < TILE_PIX / 32; ++w) far = fmaxf(far, s_max[w]);
+        tile_far[tile] = all ? far : INFINITY;
+        tile_full[tile] = (uint8_t)(all ? 1 : 0);
+    }
+}
+
+// ------------------------------------------------------------ backward ----
+
+// dL/d(world vertex positions, vertex colours) of one covered pixel, given
+// dL/dD (gD) and dL/d(mesh colour) (gc), for the interpolation of k_interp.
+__device__ __forceinline__ void interp_grad(const Cam& c, const float X[3][3], const float C[3][3], float px,
+                                            float py, float gD, const float gc[3], float gX[3][3], float gC[3][3])
+{
+    Persp P;
+    persp(c, X, px, py, P);
+    float gw[3];
+    float cm[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        gw[k] = gc[0] * C[k][0] + gc[1] * C[k][1] + gc[2] * C[k][2];
+#pragma unroll
+        for (int ch = 0; ch < 3; ++ch) {
+            gC[k][ch] = P.w[k] * gc[ch];
+            cm[ch] = fmaf(P.w[k], C[k][ch], cm[ch]);
+        }
+    }
+    const float gwbar = gc[0] * cm[0] + gc[1] * cm[1] + gc[2] * cm[2];
+    // q_k = l_k / z_k, s = sum q, D = 1/s, w_k = q_k D
+    float gl[3], gz[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        float gq = -gD * P.D * P.D + P.D * (gw[k] - gwbar);
+        gl[k] = gq / P.z[k];
+        gz[k] = -gq * P.q[k] / P.z[k];
+    }
+    // l_k = e_k / area
+    const float ia = 1.0f / P.area;
+    float garea = 0.0f;
+    float ge[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        ge[k] = gl[k] * ia;
+        garea -= gl[k] * P.lam[k] * ia;
+    }
+    float gu[3] = {0.0f, 0.0f, 0.0f}, gv[3] = {0.0f, 0.0f, 0.0f};
+    // e_k = (ub - ua)(py - va) - (vb - va)(px - ua), a = k+1, b = k+2
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int a = (k + 1) % 3, b = (k + 2) % 3;
+        gu[b] += ge[k] * (py - P.v[a]);
+        gu[a] += ge[k] * (P.v[b] - py);
+        gv[b] -= ge[k] * (px - P.u[a]);
+        gv[a] += ge[k] * (px - P.u[b]);
+    }
+    // area = (u1 - u0)(v2 - v0) - (u2 - u0)(v1 - v0)
+    gu[0] += garea * (P.v[1] - P.v[2]);
+    gu[1] += garea * (P.v[2] - P.v[0]);
+    gu[2] += garea * (P.v[0] - P.v[1]);
+    gv[0] += garea * (P.u[2] - P.u[1]);
+    gv[1] += garea * (P.u[0] - P.u[2]);
+    gv[2] += garea * (P.u[1] - P.u[0]);
+    // u = fx x / z + cx, v = fy y / z + cy; then world = R^T camera
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const float iz = 1.0f / P.z[k];
+        const float gx = gu[k] * c.fx * iz;
+        const float gy = gv[k] * c.fy * iz;
+        const float gzz = gz[k] - (gu[k] * (P.u[k] - c.cx) + gv[k] * (P.v[k] - c.cy)) * iz;
+        gX[k][0] = c.R[0] * gx + c.R[3] * gy + c.R[6] * gzz;
+        gX[k][1] = c.R[1] * gx + c.R[4] * gy + c.R[7] * gzz;
+        gX[k][2] = c.R[2] * gx + c.R[5] * gy + c.R[8] * gzz;
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(TILE_PIX)
+k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
+           const float* __restrict__ vcol, const int32_t* __restrict__ face_id, const float* __restrict__ T_final,
+           const float* __restrict__ g_rgb, const float* __restrict__ g_depth, float* __restrict__ v_verts,
+           float* __restrict__ v_vcol)
+{
+    const int tile = blockIdx.x;
+    const int tx = tile % c.TW, ty = tile / c.TW;
+    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
+    const int j = ty * TILE + (threadIdx.x >> 4);
+    const int lane = threadIdx.x & 31;
+    int f = -1;
+    if (i < c.W && j < c.H) f = face_id[(int64_t)j * c.W + i];
+    float gX[3][3], gC[3][3];
+    int vid[3] = {0, 0, 0};
+    float X[3][3], C[3][3];
+    const bool act = f >= 0 && f < nF && load_face(V, nV, F, f, vid, X);
+    if (act) {
+        const int64_t pix = (int64_t)j * c.W + i;
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+#pragma unroll
+            for (int ch = 0; ch < 3; ++ch) C[k][ch] = __ldg(vcol + 3 * (int64_t)vid[k] + ch);
+        const float T = T_final[pix];
+        const float gc[3] = {T * g_rgb[3 * pix], T * g_rgb[3 * pix + 1], T * g_rgb[3 * pix + 2]};
+        interp_grad(c, X, C, (float)i + 0.5f, (float)j + 0.5f, T * g_depth[pix], gc, gX, gC);
+    }
+    // one set of atomics per distinct face in the warp
+    unsigned pending = __ballot_sync(0xffffffffu, act);
+    while (pending) {
+        const int leader = __ffs(pending) - 1;
+        const int fl = __shfl_sync(0xffffffffu, f, leader);
+        const bool mine = act && f == fl;
+        const unsigned m = __ballot_sync(0xffffffffu, mine);
+        if (__popc(m) == 1) {
+            if (lane == leader) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k)
+#pragma unroll
+                    for (int d = 0; d < 3; ++d) {
+                        atomicAdd(v_verts + 3 * (int64_t)vid[k] + d, gX[k][d]);
+                        atomicAdd(v_vcol + 3 * (int64_t)vid[k] + d, gC[k][d]);
+                    }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    float a = warp_sum(mine ? gX[k][d] : 0.0f);
+                    float b = warp_sum(mine ? gC[k][d] : 0.0f);
+                    if (lane == leader) {
+                        atomicAdd(v_verts + 3 * (int64_t)vid[k] + d, a);
+                        atomicAdd(v_vcol + 3 * (int64_t)vid[k] + d, b);
+                    }
+                }
+        }
+        pending &= ~m;
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ host side ---
+
+static int tile_bits(int n_tiles)
+{
+    return n_tiles > 1 ? 32 - __builtin_clz((unsigned)(n_tiles - 1)) : 0;
+}
+
+size_t tri_bin_ws_bytes(int nF, int cap)
+{
+    int64_t n = nF > 0 ? nF : 1, k = cap > 0 ? cap : 1;
+    return scan_ws_bytes(n) + 2 * ((sizeof(int32_t) * n + 255) & ~(size_t)255) +
+           ((sizeof(uint64_t) * k + 255) & ~(size_t)255) + sort_ws_bytes(k);
+}
+
+cudaError_t tri_bin(const Cam& c, const float* V, int nV, const int32_t* F, int nF, int32_t* tile_range,
+                    int32_t* tri_ids, int cap, int32_t* counters, void* ws, cudaStream_t s)
+{
+    int64_t n = nF > 0 ? nF : 1, k = cap > 0 ? cap : 1;
+    uint8_t* b = (uint8_t*)ws;
+    ScanWs sw;
+    b += carve_scan_ws(b, n, sw);
+    int32_t* counts = (int32_t*)b;
+    b += (sizeof(int32_t) * n + 255) & ~(size_t)255;
+    int32_t* offsets = (int32_t*)b;
+    b += (sizeof(int32_t) * n + 255) & ~(size_t)255;
+    uint64_t* keysA = (uint64_t*)b;
+    b += (sizeof(uint64_t) * k + 255) & ~(size_t)255;
+    SortWs so;
+    carve_sort_ws(b, k, so);
+
+    cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+    const int T = c.TW * c.TH;
+    const int passes = sort_passes(32, 32 + tile_bits(T));
+    uint64_t* ek = passes % 2 ? so.keys_alt : keysA;
+    int32_t* ev = passes % 2 ? so.vals_alt : tri_ids;
+    if (nF > 0) {
+        k_tri_count<<<(nF + 255) / 256, 256, 0, s>>>(c, V, nV, F, nF, counts);
+        if ((e = exclusive_scan(counts, offsets, nF, counters, sw, s)) != cudaSuccess) return e;
+        k_tri_emit<<<(nF + 255) / 256, 256, 0, s>>>(c, V, nV, F, nF, offsets, cap, counters, ek, ev);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (passes % 2)
+            e = radix_sort(so.keys_alt, so.vals_alt, keysA, tri_ids, cap, 32, 32 + tile_bits(T), counters, so, s);
+        else
+            e = radix_sort(keysA, tri_ids, so.keys_alt, so.vals_alt, cap, 32, 32 + tile_bits(T), counters, so, s);
+        if (e != cudaSuccess) return e;
+    }
+    return tile_ranges(keysA, nF > 0 ? cap : 0, counters, tile_range, T, s);
+}
+
+cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, const int32_t* tile_range,
+                    const int32_t* tri_ids, int32_t* face_id, cudaStream_t s)
+{
+    k_zbuffer<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, reinterpret_cast<const int2*>(tile_range), tri_ids,
+                                                face_id);
+    return cudaGetLastError();
+}
+
+cudaError_t interp(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
+                   const int32_t* face_id, float* mesh_depth, float* mesh_rgb, float* tile_far, uint8_t* tile_full,
+                   cudaStream_t s)
+{
+    k_interp<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, mesh_depth, mesh_rgb, tile_far,
+                                               tile_full);
+    return cudaGetLastError();
+}
+
+cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
+                     const int32_t* face_id, const float* T_final, const float* g_rgb, const float* g_depth,
+                     float* v_verts, float* v_vcol, cudaStream_t s)
+{
+    k_mesh_bwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, v_verts,
+                                                 v_vcol);
+    return cudaGetLastError();
+}
+
+}  // namespace gm

@@ -1,0 +1,241 @@
+/*
+ * gm.h -- C ABI of libgm, a B300 (sm_103a) CUDA library for the tile-based
+ * forward and backward rendering of scenes that hold both a triangle mesh
+ * and 3D Gaussians.
+ *
+ * The method is the hybrid renderer of "A Lightweight and Differentiable
+ * Renderer for Joint Mesh and 3D Gaussian Splat Scenes" (Design Details:
+ * Mesh rasterizer items 1-2, Hybrid rendering), restricted to a hard depth
+ * test between each Gaussian and the mesh and a fully opaque, non-antialiased
+ * mesh layer.  The renderer's call (rgb, depth, alpha from a mesh, Gaussians
+ * and a camera pose) is split into seven steps; a forward pass is
+ *
+ *   gm_bin_triangles -> gm_zbuffer -> gm_interp_mesh          (mesh layer)
+ *   gm_project_gaussians -> gm_bin_sort_gaussians             (Gaussians)
+ *   gm_composite_hybrid_fwd                                   (image)
+ *
+ * and gm_composite_hybrid_bwd returns the gradients of a loss with respect to
+ * the projected Gaussians and to the mesh's vertex positions and colours.
+ *
+ * Conventions shared by every call
+ *   - Camera: pinhole, world -> camera  X_c = R X_w + t  (R row-major),
+ *     OpenCV axes (x right, y down, z forward).  Pixel (i, j) has its centre
+ *     at (i + 0.5, j + 0.5).  Images are row-major [height][width]; colour
+ *     images interleave RGB ([height][width][3]).  Tiles are 16 x 16 pixels,
+ *     tile id = ty * ceil(width / 16) + tx.
+ *   - Memory: every pointer argument is a device pointer (memory the caller
+ *     allocated with cudaMalloc or an equivalent), except the gm_camera /
+ *     gm_opts structs and *K_host, which are host memory.  The library never
+ *     allocates, frees or keeps caller memory; scratch memory comes from the
+ *     caller's workspace (see the *_workspace_size calls).  Arrays marked
+ *     "16-byte aligned" are read or written with 16-byte vector accesses.
+ *   - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *     Every call only enqueues work on it and returns, unless K_host is given
+ *     (then it waits for that stream once, at the end).
+ *   - Errors: every call returns a gm_status.  GM_ERR_INVALID_ARG is returned
+ *     before any work is enqueued.  GM_ERR_CUDA means a launch failed; the
+ *     stream may hold partial work.  gm_last_error() returns a message for
+ *     the calling thread's last failure.  Gradient outputs are accumulated
+ *     (+=); the caller zeroes them.
+ *   - Sizes: counts (N, nV, nF, capacities) are int32 and must be >= 0; the
+ *     number of (primitive, tile) entries must stay below 2^30.
+ */
+#ifndef GM_H
+#define GM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GM_TILE 16
+#define GM_SPLAT_STRIDE 12 /* floats per projected-Gaussian record */
+
+typedef enum gm_status {
+    GM_OK = 0,
+    GM_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative size, bad camera */
+    GM_ERR_CAPACITY = 2,    /* more entries than the caller's capacity (needed K in *K_host) */
+    GM_ERR_CUDA = 3,        /* a kernel launch or CUDA runtime call failed */
+    GM_ERR_TIMEOUT = 4,     /* a bounded inter-block wait in the sort gave up (see counters) */
+    GM_ERR_INTERNAL = 5
+} gm_status;
+
+/* counters: a caller-owned device int32[4] written by the two binning calls */
+enum { GM_CNT_K = 0,        /* entries needed (after the occlusion cull) */
+       GM_CNT_K_PRECULL = 1,/* entries before the cull (Gaussians only) */
+       GM_CNT_FLAGS = 2 };  /* bit 0: capacity overflow, bit 1: wait timeout */
+#define GM_FLAG_OVERFLOW 1
+#define GM_FLAG_TIMEOUT 2
+
+typedef struct gm_camera {
+    int32_t width, height;          /* pixels, > 0 */
+    float fx, fy, cx, cy;           /* focal lengths and principal point, pixels */
+    float near_plane, far_plane;    /* camera-z range, 0 < near < far */
+    float R[9];                     /* world -> camera rotation, row-major */
+    float t[3];                     /* world -> camera translation */
+} gm_camera;
+
+typedef struct gm_opts {
+    float bg[3];            /* background colour behind uncovered pixels */
+    int32_t cull_occluded;  /* 1: drop Gaussians hidden behind fully covered tiles */
+    int32_t sh_degree;      /* -1: colours are RGB [N][3]; 0..3: SH coefficients [N][(d+1)^2][3] */
+} gm_opts;
+
+/*
+ * Projected-Gaussian record ("splat"), GM_SPLAT_STRIDE floats, 16-byte aligned:
+ *   [0] mean2d x  [1] mean2d y      (pixels)
+ *   [2] conic a   [3] conic b   [4] conic c   (inverse 2D covariance:
+ *        sigma(d) = (a dx^2 + c dy^2) / 2 + b dx dy)
+ *   [5] opacity   [6..8] RGB    [9] camera-space depth of the centre
+ *   [10], [11] reserved (0)
+ * Gradient buffers of the same layout hold dL/d of each field.
+ */
+
+/* ------------------------------------------------------------------------
+ * gm_bin_triangles -- Mesh rasterizer, item 1 (triangles binned into 16x16
+ * tiles).  A triangle is drawn when every vertex is strictly beyond the near
+ * plane (no clipping; Mesh rasterizer, last paragraph), its projected area
+ * is non-zero and its box of pixel centres meets the image; it is binned to
+ * every tile that box touches.
+ *   V [nV][3] f32 world positions; F [nF][3] i32 vertex indices (checked
+ *   against nV: an out-of-range index drops the face and sets no error).
+ *   tile_range [T][2] i32 out: [first, last) entries of each tile in tri_ids.
+ *   tri_ids [cap] i32 out: face ids, tile-major, ascending within a tile.
+ *   counters [4] i32 out (device): GM_CNT_K = entries needed; flags.
+ *   K_host: NULL, or a host int32 that receives the needed K after a stream
+ *   synchronisation; then GM_ERR_CAPACITY is returned when K > cap.  With
+ *   K_host == NULL nothing waits: when K > cap the outputs are invalid
+ *   (GM_FLAG_OVERFLOW is set in counters) but no write leaves the buffers.
+ *   ws / ws_bytes: workspace of at least gm_bin_triangles_workspace_size().
+ * ---------------------------------------------------------------------- */
+size_t gm_bin_triangles_workspace_size(int32_t nF, int32_t cap, int32_t width, int32_t height);
+int gm_bin_triangles(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                     int32_t* tile_range, int32_t* tri_ids, int32_t cap, int32_t* counters,
+                     int32_t* K_host, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_zbuffer -- Mesh rasterizer, item 1 (nearest triangle at each pixel
+ * centre; the only non-differentiable step).  Over the tile's triangles: a
+ * pixel centre is covered when it lies in the triangle's pixel-centre box and
+ * every edge function has the sign of the area (edges inclusive, both
+ * windings).  The nearest perspective-correct depth wins; equal depths go to
+ * the smaller face id.
+ *   tile_range / tri_ids: from gm_bin_triangles.  face_id [H][W] i32 out
+ *   (-1 = uncovered).
+ * ---------------------------------------------------------------------- */
+int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+               const int32_t* tile_range, const int32_t* tri_ids, int32_t* face_id, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_interp_mesh -- Mesh rasterizer, item 2 (depth and vertex colours
+ * recomputed from the face ids with perspective-correct interpolation).
+ *   l_k = e_k / area (screen barycentrics), D = 1 / sum_k l_k / z_k,
+ *   w_k = (l_k / z_k) D, colour = sum_k w_k vcol_k.
+ *   vcol [nV][3] f32.  mesh_depth [H][W] f32 out (+inf where uncovered);
+ *   mesh_rgb [H][W][3] f32 out (0 where uncovered).
+ *   tile_far [T] f32 out: largest mesh depth of a fully covered tile, +inf
+ *   otherwise; tile_full [T] u8 out: 1 when every in-image pixel of the tile
+ *   is covered.  Both feed the occlusion cull of gm_bin_sort_gaussians.
+ * ---------------------------------------------------------------------- */
+int gm_interp_mesh(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                   const float* vcol, const int32_t* face_id, float* mesh_depth, float* mesh_rgb,
+                   float* tile_far, uint8_t* tile_full, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_project_gaussians -- EWA projection and colour of each Gaussian
+ * (Hybrid rendering; the 3DGS projection and SH kernels).  Inputs in the
+ * stored parameterisation: means [N][3], log_scales [N][3], quats [N][4]
+ * (w, x, y, z; normalised here), logits [N] (opacity = sigmoid), colors
+ * [N][3] RGB (opts->sh_degree = -1) or [N][(d+1)^2][3] real SH coefficients
+ * (rgb = max(0, sum Y_lm(view dir) c_lm + 0.5)).
+ *   splats [N][12] f32 out, 16-byte aligned (layout above; all zero for a
+ *   culled Gaussian).  radii [N] i32 out: ceil(3 sqrt(largest eigenvalue of
+ *   the 2D covariance)), 0 = culled (behind near / beyond far, or its tile
+ *   rectangle misses the image).  tiles_touched [N] i32 out: tiles in the
+ *   rectangle [floor((m - r)/16), ceil((m + r)/16)) per axis, clamped.
+ * ---------------------------------------------------------------------- */
+int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
+                         const float* log_scales, const float* quats, const float* logits,
+                         const float* colors, float* splats, int32_t* radii, int32_t* tiles_touched,
+                         void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_bin_sort_gaussians -- tile intersection and sort (Hybrid rendering;
+ * Limitations: Gaussians ordered by centre depth) with the per-tile cull
+ * (Hybrid rendering, cull_occluded bullet: Gaussians certainly hidden behind
+ * the mesh in fully covered tiles are removed; the image does not change).
+ * Every (Gaussian, tile) pair of a rectangle gets the 64-bit key
+ *   (tile id << 32) | bits(depth)
+ * and the Gaussian id as value; with opts->cull_occluded a pair is dropped
+ * when tile_full[tile] and depth >= tile_far[tile].  Keys are sorted
+ * ascending by a stable LSD radix sort, so equal depths keep ascending ids.
+ *   splats / radii: from gm_project_gaussians.  tile_far / tile_full: from
+ *   gm_interp_mesh (read only when cull_occluded).
+ *   keys [cap] u64 out, gids [cap] i32 out, tile_range [T][2] i32 out.
+ *   counters [4] i32 out (device): GM_CNT_K, GM_CNT_K_PRECULL, flags.
+ *   K_host, cap, ws: as for gm_bin_triangles.  GM_ERR_TIMEOUT is returned
+ *   (K_host != NULL) when a bounded inter-block wait of the sort gave up.
+ * ---------------------------------------------------------------------- */
+size_t gm_bin_sort_gaussians_workspace_size(int32_t N, int32_t cap, int32_t width, int32_t height);
+int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* splats,
+                          const int32_t* radii, const float* tile_far, const uint8_t* tile_full,
+                          uint64_t* keys, int32_t* gids, int32_t* tile_range, int32_t cap,
+                          int32_t* counters, int32_t* K_host, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_composite_hybrid_fwd -- Hybrid rendering, compositing with a hard
+ * split: per pixel, front to back over its tile's sorted Gaussians, each
+ * drawn only where its centre depth is in front of the mesh (z < D);
+ *   sigma = (a dx^2 + c dy^2)/2 + b dx dy, d = pixel centre - mean (skip
+ *   sigma < 0); alpha = min(0.99, opacity exp(-sigma)) (skip alpha < 1/255);
+ *   stop before a Gaussian that would bring T to 1e-4 or below;
+ *   C += alpha T rgb, Z += alpha T z, T *= 1 - alpha.
+ * The opaque mesh is the terminal layer (covered = face_id >= 0):
+ *   out_rgb = C + T (covered ? mesh_rgb : bg), out_depth = Z + T covered D,
+ *   out_alpha = 1 - T (1 - covered).
+ *   N: number of splat records; tile_range / gids come from
+ *   gm_bin_sort_gaussians over the same splats (an id outside [0, N) is
+ *   treated as an entry that draws nothing).
+ *   Saved for the backward pass: T_final [H][W] f32 and n_contrib [H][W]
+ *   i32 (1 + position in the tile's list of the last composited Gaussian).
+ *   stats: NULL, or a device uint64 that is incremented by the number of
+ *   (pixel, Gaussian) pairs evaluated (a profiling count; the caller zeroes it).
+ * ---------------------------------------------------------------------- */
+int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
+                            const int32_t* tile_range, const int32_t* gids, const float* splats, const float* mesh_depth,
+                            const float* mesh_rgb, const int32_t* face_id, float* out_rgb,
+                            float* out_depth, float* out_alpha, float* T_final, int32_t* n_contrib,
+                            uint64_t* stats, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_composite_hybrid_bwd -- Hybrid rendering ("everything is
+ * differentiable"): gradients of L = sum g_rgb . out_rgb + g_depth out_depth
+ * + g_alpha out_alpha, given the saved T_final / n_contrib of the forward
+ * pass over the same inputs.
+ *   v_splats [N][12] f32 (+=, 16-byte aligned): dL/d mean2d, conic, opacity,
+ *   rgb, depth of each Gaussian (the hard depth test, the skips and the sort
+ *   carry no gradient; alpha clamped at 0.99 has none w.r.t. opacity/conic).
+ *   v_verts [nV][3], v_vcol [nV][3] f32 (+=): dL/d vertex world position and
+ *   colour through the interpolated mesh depth and colour of covered pixels
+ *   (face ids held fixed).  V / F / vcol / v_verts / v_vcol may all be NULL
+ *   (with nV = nF = 0) to skip the mesh gradients.
+ *   stats: NULL, or a device uint64 incremented by the number of (pixel,
+ *   Gaussian) pairs whose gradient terms were evaluated (profiling count).
+ * ---------------------------------------------------------------------- */
+int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
+                            const int32_t* tile_range, const int32_t* gids, const float* splats, const float* mesh_depth,
+                            const float* mesh_rgb, const int32_t* face_id, const float* T_final,
+                            const int32_t* n_contrib, const float* g_rgb, const float* g_depth,
+                            const float* g_alpha, float* v_splats, const float* V, int32_t nV,
+                            const int32_t* F, int32_t nF, const float* vcol, float* v_verts,
+                            float* v_vcol, uint64_t* stats, void* stream);
+
+/* Message describing the calling thread's last failure ("" if none). */
+const char* gm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GM_H */

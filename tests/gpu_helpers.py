@@ -1,0 +1,161 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+binding and bring results back as numpy; tolerances derived from fp32 error
+bounds (each stated where it is used)."""
+
+import numpy as np
+import pytest
+import torch
+
+import differentiable_hybrid_mesh_tile_b300 as gm
+from differentiable_hybrid_mesh_tile_b300 import build as gm_build
+from differentiable_hybrid_mesh_tile_b300 import scenes
+
+EPS32 = float(np.finfo(np.float32).eps)
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gm_build.build()
+    gm.lib()
+
+
+def dev(x, dtype=None):
+    t = torch.as_tensor(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda().contiguous()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.detach().cpu().numpy()
+
+
+def n_tiles(cam):
+    return ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
+
+
+def run_mesh(cam, mesh):
+    """GPU gm_bin_triangles -> gm_zbuffer -> gm_interp_mesh."""
+    c = gm.make_camera(cam)
+    V, F, vcol = dev(mesh.verts, torch.float32), dev(mesh.faces, torch.int32), dev(mesh.vcol, torch.float32)
+    T = n_tiles(cam)
+    tr = torch.zeros(T, 2, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(4, dtype=torch.int32, device="cuda")
+    cap = 16
+    for _ in range(2):
+        ids = torch.zeros(cap, dtype=torch.int32, device="cuda")
+        ws = torch.empty(gm.gm_bin_triangles_workspace_size(len(F), cap, cam.width, cam.height), dtype=torch.uint8,
+                         device="cuda")
+        try:
+            K = gm.gm_bin_triangles(c, V, F, tr, ids, cap, cnt, ws)
+            break
+        except gm.GmError as e:
+            assert e.status == gm.GM_ERR_CAPACITY
+            cap = int(host(cnt)[0]) + 1
+    fid = torch.full((cam.height, cam.width), -7, dtype=torch.int32, device="cuda")
+    gm.gm_zbuffer(c, V, F, tr, ids, fid)
+    md = torch.empty(cam.height, cam.width, dtype=torch.float32, device="cuda")
+    mrgb = torch.empty(cam.height, cam.width, 3, dtype=torch.float32, device="cuda")
+    tfar = torch.empty(T, dtype=torch.float32, device="cuda")
+    tfull = torch.empty(T, dtype=torch.uint8, device="cuda")
+    gm.gm_interp_mesh(c, V, F, vcol, fid, md, mrgb, tfar, tfull)
+    return dict(K=K, tile_range=host(tr), tri_ids=host(ids)[:K], face_id=host(fid), mesh_depth=host(md),
+                mesh_rgb=host(mrgb), tile_far=host(tfar), tile_full=host(tfull), counters=host(cnt))
+
+
+def run_project(cam, g, bg=(1, 1, 1)):
+    c = gm.make_camera(cam)
+    o = gm.make_opts(bg, True, g.sh_degree)
+    N = len(g.means)
+    splats = torch.full((N, 12), 7.0, dtype=torch.float32, device="cuda")
+    radii = torch.full((N,), -3, dtype=torch.int32, device="cuda")
+    touched = torch.full((N,), -3, dtype=torch.int32, device="cuda")
+    gm.gm_project_gaussians(c, o, dev(g.means, torch.float32), dev(g.log_scales, torch.float32),
+                            dev(g.quats, torch.float32), dev(g.logits, torch.float32), dev(g.colors, torch.float32),
+                            splats, radii, touched)
+    return host(splats), host(radii), host(touched)
+
+
+def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=None, sync=True):
+    c = gm.make_camera(cam)
+    o = gm.make_opts((1, 1, 1), cull, -1)
+    N = len(radii)
+    T = n_tiles(cam)
+    tf = dev(np.full(T, np.inf, np.float32) if tile_far is None else tile_far, torch.float32)
+    tu = dev(np.zeros(T, np.uint8) if tile_full is None else tile_full, torch.uint8)
+    tr = torch.full((T, 2), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((4,), -9, dtype=torch.int32, device="cuda")
+    if cap is None:
+        cap = int(np.asarray(radii > 0).sum() * 4) + 64
+    while True:
+        keys = torch.zeros(cap, dtype=torch.int64, device="cuda")
+        gids = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+        ws = torch.empty(gm.gm_bin_sort_gaussians_workspace_size(N, cap, cam.width, cam.height), dtype=torch.uint8,
+                         device="cuda")
+        try:
+            K = gm.gm_bin_sort_gaussians(c, o, dev(splats, torch.float32), dev(radii, torch.int32), tf, tu, keys,
+                                         gids, tr, cap, cnt, ws, sync=sync)
+            break
+        except gm.GmError as e:
+            assert e.status == gm.GM_ERR_CAPACITY
+            cap = int(host(cnt)[0]) + 1
+    cn = host(cnt)
+    K = int(cn[0]) if K is None else K
+    k = min(K, cap)
+    return dict(K=K, keys=host(keys)[:k].view(np.uint64), gids=host(gids)[:k], tile_range=host(tr), counters=cn,
+                cap=cap)
+
+
+def run_composite(cam, bg, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id):
+    c = gm.make_camera(cam)
+    o = gm.make_opts(bg, True, -1)
+    H, W = cam.height, cam.width
+    out = {k: torch.full(s, -3.0, dtype=torch.float32, device="cuda")
+           for k, s in [("rgb", (H, W, 3)), ("depth", (H, W)), ("alpha", (H, W)), ("T", (H, W))]}
+    nc = torch.full((H, W), -3, dtype=torch.int32, device="cuda")
+    args = [dev(tile_range, torch.int32), dev(gids if len(gids) else np.zeros(1, np.int32), torch.int32),
+            dev(splats if len(splats) else np.zeros((1, 12), np.float32), torch.float32),
+            dev(mesh_depth, torch.float32), dev(mesh_rgb, torch.float32), dev(face_id, torch.int32)]
+    gm.gm_composite_hybrid_fwd(c, o, *args, out["rgb"], out["depth"], out["alpha"], out["T"], nc)
+    res = {k: host(v) for k, v in out.items()}
+    res["n_contrib"] = host(nc)
+    res["_args"] = args
+    res["_dev"] = dict(T=out["T"], n_contrib=nc)
+    return res
+
+
+def run_composite_bwd(cam, bg, fwd, grads, N, mesh=None, mesh_grads=False):
+    c = gm.make_camera(cam)
+    o = gm.make_opts(bg, True, -1)
+    v_splats = torch.zeros(max(N, 1), 12, dtype=torch.float32, device="cuda")
+    g_rgb, g_depth, g_alpha = (dev(x, torch.float32) for x in grads)
+    V = F = vcol = v_verts = v_vcol = None
+    if mesh_grads:
+        V, F, vcol = dev(mesh.verts, torch.float32), dev(mesh.faces, torch.int32), dev(mesh.vcol, torch.float32)
+        v_verts = torch.zeros_like(V)
+        v_vcol = torch.zeros_like(vcol)
+    gm.gm_composite_hybrid_bwd(c, o, *fwd["_args"], fwd["_dev"]["T"], fwd["_dev"]["n_contrib"], g_rgb, g_depth,
+                               g_alpha, v_splats, V, F, vcol, v_verts, v_vcol)
+    out = dict(v_splats=host(v_splats)[:N])
+    if mesh_grads:
+        out.update(v_verts=host(v_verts), v_vcol=host(v_vcol))
+    return out
+
+
+def lists_from_bins(cam, keys, gids):
+    """(tile_start[T+1], entries) CSR lists from sorted GPU keys."""
+    T = n_tiles(cam)
+    start = np.zeros(T + 1, np.int64)
+    if len(keys):
+        np.add.at(start, (keys >> np.uint64(32)).astype(np.int64) + 1, 1)
+    return np.cumsum(start), np.asarray(gids, np.int32)
+
+
+def tie_pixels(margins, alpha_band=2e-6, stop_band=1e-4, sigma_band=1e-5, clamp_band=None):
+    m = margins
+    t = (m[..., 1] < alpha_band) | (m[..., 3] < stop_band) | (m[..., 4] < sigma_band)
+    if clamp_band is not None:
+        t |= m[..., 2] < clamp_band
+    return t

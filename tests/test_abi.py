@@ -1,0 +1,94 @@
+"""The C ABI library loads and exports every function include/gm.h declares;
+argument checks answer GM_ERR_INVALID_ARG before any CUDA work (no GPU
+needed: these calls return before touching the device)."""
+
+import ctypes as C
+
+import pytest
+
+import differentiable_hybrid_mesh_tile_b300 as gm
+from differentiable_hybrid_mesh_tile_b300 import build as gm_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gm_build.build()
+    return gm.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = gm.header_functions()
+    assert len(names) >= 10
+    for n in ["gm_bin_triangles", "gm_zbuffer", "gm_interp_mesh", "gm_project_gaussians",
+              "gm_bin_sort_gaussians", "gm_composite_hybrid_fwd", "gm_composite_hybrid_bwd", "gm_last_error"]:
+        assert n in names
+    raw = C.CDLL(gm.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_workspace_queries_are_host_only(lib):
+    a = gm.gm_bin_triangles_workspace_size(1000, 5000, 64, 64)
+    b = gm.gm_bin_triangles_workspace_size(1000, 50000, 64, 64)
+    assert 0 < a < b
+    c = gm.gm_bin_sort_gaussians_workspace_size(100000, 400000, 512, 512)
+    assert c > 400000 * 12
+
+
+def _cam(**kw):
+    c = gm.gm_camera()
+    c.width, c.height, c.fx, c.fy, c.cx, c.cy = 64, 48, 50.0, 50.0, 32.0, 24.0
+    c.near_plane, c.far_plane = 0.01, 100.0
+    for k in range(9):
+        c.R[k] = 1.0 if k in (0, 4, 8) else 0.0
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("bad", [dict(width=0), dict(fx=-1.0), dict(near_plane=0.0), dict(far_plane=0.001),
+                                 dict(fy=float("nan"))])
+def test_bad_camera_rejected(lib, bad):
+    cam = _cam(**bad)
+    st = lib.gm_zbuffer(C.byref(cam), None, 0, None, 0, C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), None)
+    assert st == gm.GM_ERR_INVALID_ARG
+    assert len(lib.gm_last_error()) > 0
+
+
+def test_null_and_size_checks(lib):
+    cam = _cam()
+    opts = gm.make_opts()
+    # NULL camera
+    assert lib.gm_interp_mesh(None, None, 0, None, 0, None, None, None, None, None, None, None) == gm.GM_ERR_INVALID_ARG
+    # negative N
+    st = lib.gm_project_gaussians(C.byref(cam), C.byref(opts), -1, *([None] * 9))
+    assert st == gm.GM_ERR_INVALID_ARG
+    # sh degree out of range
+    bad = gm.make_opts(sh_degree=4)
+    st = lib.gm_project_gaussians(C.byref(cam), C.byref(bad), 0, *([None] * 9))
+    assert st == gm.GM_ERR_INVALID_ARG and b"sh_degree" in lib.gm_last_error()
+    # misaligned splats
+    st = lib.gm_project_gaussians(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 5), C.c_void_p(260),
+                                  C.c_void_p(256), C.c_void_p(256), None)
+    assert st == gm.GM_ERR_INVALID_ARG
+    # workspace too small
+    st = lib.gm_bin_sort_gaussians(C.byref(cam), C.byref(opts), 10, C.c_void_p(256), C.c_void_p(256),
+                                   C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), C.c_void_p(256),
+                                   C.c_void_p(256), 100, C.c_void_p(256), None, C.c_void_p(256), 10, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"workspace" in lib.gm_last_error()
+    # cull without tile bounds
+    st = lib.gm_bin_sort_gaussians(C.byref(cam), C.byref(opts), 10, C.c_void_p(256), C.c_void_p(256), None, None,
+                                   C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), 100, C.c_void_p(256), None,
+                                   C.c_void_p(256), 1 << 30, None)
+    assert st == gm.GM_ERR_INVALID_ARG
+    # incomplete mesh-gradient arguments
+    st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 12), None, 3,
+                                     None, 1, None, C.c_void_p(256), None, None, None)
+    assert st == gm.GM_ERR_INVALID_ARG
+
+
+def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(gm, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(gm, "_lib", None)
+    with pytest.raises(ImportError):
+        gm.lib()

@@ -1,0 +1,203 @@
+"""GPU parity of hybrid compositing (gm_composite_hybrid_fwd / _bwd) against
+the CPU oracle ("A Lightweight and Differentiable Renderer for Joint Mesh and
+3D Gaussian Splat Scenes", Hybrid rendering: depth-tested Gaussians over one
+opaque mesh layer; culling does not change the result; gradients w.r.t.
+Gaussians and mesh vertices / colours).
+
+Tolerances: rgb, depth and alpha within 1e-4 absolute; gradients within
+1e-5 absolute + 1e-3 relative of the finite-difference value.  Pixels where
+an fp32 decision of the oracle lies within rounding of its threshold (alpha
+vs 1/255 within 2e-6 relative -- the GPU's exp differs from the oracle's by a
+few ulp --, transmittance vs 1e-4 within 1e-4 relative) are counted, reported
+and left out of the value check; their number must stay tiny."""
+
+import numpy as np
+import pytest
+
+from differentiable_hybrid_mesh_tile_b300 import scenes
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+ATOL_IMG = 1e-4
+G_ATOL, G_RTOL = 1e-5, 1e-3
+FIELDS = ["mx", "my", "ca", "cb", "cc", "op", "r", "g", "b", "z"]
+
+
+def pipeline(scene, cull=True, cam=None):
+    cam = scene.camera if cam is None else cam
+    m = H.run_mesh(cam, scene.mesh)
+    sp, rad, tt = H.run_project(cam, scene.gaussians, scene.bg)
+    b = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull)
+    f = H.run_composite(cam, scene.bg, b["tile_range"], b["gids"], sp, m["mesh_depth"], m["mesh_rgb"], m["face_id"])
+    return dict(cam=cam, mesh=m, splats=sp, radii=rad, bins=b, fwd=f)
+
+
+def _scene(name):
+    if name == "tiny":
+        return scenes.tiny()
+    if name == "sphere512":
+        return scenes.sphere512()
+    if name == "soup_small":
+        s = scenes.soup1080(n_gauss=150_000, n_tri=30_000)
+        cam = scenes.look_at((0, 0, 6), (0, 0, 0), 480, 272, 300, 300)
+        return scenes.Scene(s.name, [cam], s.mesh, s.gaussians, s.bg)
+    raise KeyError(name)
+
+
+@pytest.fixture(scope="module", params=["tiny", "sphere512", "soup_small"])
+def run(request):
+    H.need_gpu()
+    s = _scene(request.param)
+    return request.param, s, pipeline(s)
+
+
+def test_forward_matches_oracle(run, orc):
+    name, s, r = run
+    cam, f, m = r["cam"], r["fwd"], r["mesh"]
+    lists = orc.tile_lists(cam, r["splats"], r["radii"])
+    o = orc.composite_fwd(cam, s.bg, r["splats"], lists, m["mesh_depth"], m["mesh_rgb"], m["face_id"])
+    tie = H.tie_pixels(o["margins"])
+    ok = ~tie
+    for k in ("rgb", "depth", "alpha"):
+        err = np.abs(f[k] - o[k])
+        if err.ndim == 3:
+            err = err.max(-1)
+        assert np.all(err[ok] <= ATOL_IMG), (k, err[ok].max(), np.argwhere((err > ATOL_IMG) & ok)[:5])
+    np.testing.assert_array_equal(f["n_contrib"][ok], o["n_contrib"][ok])
+    np.testing.assert_allclose(f["T"][ok], o["T"][ok], rtol=1e-4, atol=1e-7)
+    n_tie = int(tie.sum())
+    print("%s: %d px, %d threshold-tie px, max |rgb err| %.2e, mean n_contrib %.1f" % (
+        name, tie.size, n_tie, np.abs(f["rgb"] - o["rgb"])[ok].max(), f["n_contrib"].mean()))
+    assert n_tie <= max(2, tie.size // 10000)
+
+
+def test_cull_changes_nothing(run):
+    """Bit-identical forward with and without the per-tile occlusion cull."""
+    name, s, r = run
+    cam, m = r["cam"], r["mesh"]
+    b0 = H.run_bin(cam, r["splats"], r["radii"], m["tile_far"], m["tile_full"], cull=False)
+    f0 = H.run_composite(cam, s.bg, b0["tile_range"], b0["gids"], r["splats"], m["mesh_depth"], m["mesh_rgb"],
+                         m["face_id"])
+    f1 = r["fwd"]
+    for k in ("rgb", "depth", "alpha", "T", "n_contrib"):
+        np.testing.assert_array_equal(f0[k], f1[k])
+    print("%s: K %d -> %d with the cull" % (name, b0["K"], r["bins"]["K"]))
+    if m["tile_full"].any():
+        assert r["bins"]["K"] < b0["K"]
+
+
+def _fd_requests(rng, radii, n_gauss, fields=range(10)):
+    vis = np.nonzero(radii > 0)[0]
+    pick = vis if len(vis) <= n_gauss else np.sort(rng.choice(vis, n_gauss, replace=False))
+    gid = np.repeat(pick, len(fields))
+    fld = np.tile(np.array(list(fields)), len(pick))
+    return gid, fld
+
+
+def _steps(splats, gid, fld):
+    s = splats[gid]
+    h = np.empty(len(gid))
+    h[fld <= 1] = 1e-3
+    sc = np.maximum(np.abs(s[:, 2]), np.abs(s[:, 4]))
+    h[(fld >= 2) & (fld <= 4)] = 1e-4 * sc[(fld >= 2) & (fld <= 4)]
+    h[fld == 5] = 1e-4
+    h[(fld >= 6) & (fld <= 8)] = 1e-2
+    h[fld == 9] = 1e-5 * s[fld == 9, 9]
+    return h
+
+
+@pytest.mark.parametrize("name,n_gauss,n_vert", [("tiny", 1000, 42), ("sphere512", 300, 120)])
+def test_backward_matches_finite_differences(name, n_gauss, n_vert, orc):
+    H.need_gpu()
+    s = _scene(name)
+    r = pipeline(s)
+    cam, m, f = r["cam"], r["mesh"], r["fwd"]
+    grads = scenes.upstream_grads(7, cam.width, cam.height)
+    b = H.run_composite_bwd(cam, s.bg, f, grads, len(r["radii"]), s.mesh, mesh_grads=True)
+    lists = orc.tile_lists(cam, r["splats"], r["radii"])
+    rng = np.random.default_rng(5)
+    gid, fld = _fd_requests(rng, r["radii"], n_gauss)
+    hs = _steps(r["splats"], gid, fld)
+    fd, st = orc.composite_fd(cam, np.float64(s.bg), r["splats"], r["radii"], lists, m["mesh_depth"], m["mesh_rgb"],
+                              m["face_id"], grads, gid, fld, hs)
+    got = b["v_splats"][gid, fld].astype(np.float64)
+    ok = st == 0
+    err = np.abs(got - fd)
+    tol = G_ATOL + G_RTOL * np.abs(fd)
+    bad = ok & (err > tol)
+    for k in np.nonzero(bad)[0][:10]:
+        print("  gaussian %d %s: gpu %.7g fd %.7g" % (gid[k], FIELDS[fld[k]], got[k], fd[k]))
+    print("%s: %d splat parameters checked, %d excluded (%s)" % (
+        name, ok.sum(), (~ok).sum(), {orc.FD_STATUS[v]: int((st == v).sum()) for v in np.unique(st[~ok])}))
+    assert not bad.any()
+    assert ok.sum() >= 0.8 * len(st)
+    # mesh: vertex positions and colours through the interpolated depth and colour
+    covered_faces = np.unique(m["face_id"][m["face_id"] >= 0])
+    verts = np.unique(s.mesh.faces[covered_faces].reshape(-1))
+    if len(verts) > n_vert:
+        verts = np.sort(rng.choice(verts, n_vert, replace=False))
+    vid = np.repeat(verts, 6)
+    vf = np.tile(np.arange(6), len(verts))
+    vh = np.where(vf < 3, 1e-4, 1e-2)
+    vfd, vst = orc.mesh_fd(cam, np.float64(s.bg), s.mesh.verts, s.mesh.faces, s.mesh.vcol, m["face_id"].reshape(-1),
+                           r["splats"], lists, m["mesh_depth"].reshape(-1), m["mesh_rgb"].reshape(-1, 3), grads,
+                           vid, vf, vh)
+    vgot = np.where(vf < 3, b["v_verts"][vid, np.minimum(vf, 2)], b["v_vcol"][vid, np.maximum(vf - 3, 0)])
+    vok = vst == 0
+    verr = np.abs(vgot - vfd)
+    vbad = vok & (verr > G_ATOL + G_RTOL * np.abs(vfd))
+    for k in np.nonzero(vbad)[0][:10]:
+        print("  vertex %d field %d: gpu %.7g fd %.7g" % (vid[k], vf[k], vgot[k], vfd[k]))
+    print("%s: %d mesh parameters checked, %d excluded" % (name, vok.sum(), (~vok).sum()))
+    assert not vbad.any()
+    assert vok.sum() >= 0.8 * len(vst)
+
+
+def test_linear_in_colour_exactly():
+    """dL/d rgb_i is the sum over pixels of g_rgb * w_i: doubling the upstream
+    rgb gradient doubles it and the depth / alpha gradients leave it alone."""
+    H.need_gpu()
+    s = scenes.tiny()
+    r = pipeline(s)
+    cam, f = r["cam"], r["fwd"]
+    g = scenes.upstream_grads(1, cam.width, cam.height)
+    zero = np.zeros_like(g[1])
+    b1 = H.run_composite_bwd(cam, s.bg, f, (g[0], zero, zero), len(r["radii"]))
+    b2 = H.run_composite_bwd(cam, s.bg, f, (2 * g[0], g[1], g[2]), len(r["radii"]))
+    np.testing.assert_allclose(b2["v_splats"][:, 6:9], 2 * b1["v_splats"][:, 6:9], rtol=1e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("what", ["no_gaussians", "no_mesh", "empty", "ragged"])
+def test_degenerate_scenes(what, orc):
+    H.need_gpu()
+    base = scenes.tiny()
+    cam = base.camera
+    if what == "no_gaussians":
+        s = scenes.with_parts(base, gaussians=scenes.subset_gaussians(base.gaussians, np.arange(0)))
+    elif what == "no_mesh":
+        s = scenes.with_parts(base, mesh=scenes.empty_mesh())
+    elif what == "empty":
+        s = scenes.with_parts(base, mesh=scenes.empty_mesh(),
+                              gaussians=scenes.subset_gaussians(base.gaussians, np.arange(0)))
+    else:
+        cam = scenes.look_at((0.2, -0.3, 3.6), (0, 0, 0), 77, 45, 70, 70, 40.5, 20.25)
+        s = base
+    r = pipeline(s, cam=cam)
+    f, m = r["fwd"], r["mesh"]
+    lists = orc.tile_lists(cam, r["splats"], r["radii"])
+    o = orc.composite_fwd(cam, s.bg, r["splats"], lists, m["mesh_depth"], m["mesh_rgb"], m["face_id"])
+    tie = H.tie_pixels(o["margins"])
+    for k in ("rgb", "depth", "alpha"):
+        err = np.abs(f[k] - o[k])
+        err = err.max(-1) if err.ndim == 3 else err
+        assert np.all(err[~tie] <= ATOL_IMG), (k, err.max())
+    if what == "empty":
+        assert np.all(f["rgb"] == 1.0) and np.all(f["alpha"] == 0) and np.all(f["depth"] == 0)
+    if what == "no_gaussians":
+        cov = m["face_id"] >= 0
+        np.testing.assert_array_equal(f["rgb"][cov], m["mesh_rgb"][cov])
+        np.testing.assert_array_equal(f["depth"][cov], m["mesh_depth"][cov])
+    grads = scenes.upstream_grads(2, cam.width, cam.height)
+    b = H.run_composite_bwd(cam, s.bg, f, grads, len(r["radii"]), s.mesh, mesh_grads=len(s.mesh.faces) > 0)
+    assert np.all(np.isfinite(b["v_splats"]))

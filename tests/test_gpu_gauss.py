@@ -1,0 +1,184 @@
+"""GPU parity of the Gaussian steps (gm_project_gaussians, gm_bin_sort_gaussians)
+against the CPU oracle ("A Lightweight and Differentiable Renderer for Joint
+Mesh and 3D Gaussian Splat Scenes", Hybrid rendering: the projection, SH and
+tile sorting kernels; the cull_occluded bullet; Limitations: centre-depth
+order)."""
+
+import math
+
+import numpy as np
+import pytest
+
+from differentiable_hybrid_mesh_tile_b300 import scenes
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+# radius ties: 3 sqrt(lambda_max) within this relative distance of an integer.
+# lambda_max comes from the stable form m + sqrt(h^2 + b^2) of fp32 entries
+# whose relative error stays below ~1e-6, so 3 sqrt(.) errs by < 1e-6.
+RADIUS_TIE = 4e-6
+
+
+def _proj_cases():
+    tiny = scenes.tiny()
+    sph = scenes.sphere512()
+    soup = scenes.soup1080(n_gauss=60_000, n_tri=10)
+    out = [("tiny_rgb", tiny.camera, tiny.gaussians), ("sphere_rgb", sph.camera, sph.gaussians),
+           ("soup_sh3", soup.camera, soup.gaussians)]
+    rng = np.random.default_rng(12)
+    for d in (0, 1, 2):
+        g = soup.gaussians
+        k = (d + 1) ** 2
+        sub = scenes.Gaussians(g.means[:20000], g.log_scales[:20000], g.quats[:20000], g.logits[:20000],
+                               np.ascontiguousarray(g.colors[:20000, :k]), d)
+        out.append(("soup_sh%d" % d, soup.camera, sub))
+    # unnormalised quaternions, a Gaussian behind the camera, one past far
+    g = tiny.gaussians
+    q = g.quats * rng.uniform(0.2, 5.0, size=(len(g.quats), 1)).astype(np.float32)
+    m = g.means.copy()
+    m[0] = [0, 0, 10.0]
+    m[1] = [0, 0, 3.995]
+    out.append(("tiny_edge", tiny.camera, scenes.Gaussians(m, g.log_scales, q, g.logits, g.colors, -1)))
+    return out
+
+
+@pytest.fixture(scope="module", params=_proj_cases(), ids=lambda c: c[0])
+def pcase(request):
+    H.need_gpu()
+    return request.param
+
+
+def test_projection_matches_oracle(pcase, orc):
+    name, cam, g = pcase
+    sp, rad, tt = H.run_project(cam, g)
+    osp, orad, ott, margin = orc.project(cam, g)
+    tie = margin < RADIUS_TIE
+    both = (rad > 0) & (orad > 0)
+    mism = rad != orad
+    print("%s: %d projected, %d radius ties, %d radius mismatches" % (name, (orad > 0).sum(), tie.sum(), mism.sum()))
+    # a mismatch is a culled/visible flip only at a tie, or a one-unit radius step at a tie
+    assert np.all(tie[mism]), np.nonzero(mism & ~tie)[0][:10]
+    assert np.all(np.abs(rad[mism] - orad[mism]) <= 1)
+    # culled Gaussians write zero records
+    assert np.all(sp[rad == 0] == 0) and np.all(tt[rad == 0] == 0)
+    ok = both & ~mism
+    # mean2d: ~8 fp32 operations, |error| <= 16 eps |m| + 1e-5 px
+    m_err = np.abs(sp[ok, :2] - osp[ok, :2])
+    assert np.all(m_err <= 16 * H.EPS32 * np.abs(osp[ok, :2]) + 1e-5), m_err.max()
+    # conic: Sigma2 entries carry an absolute fp32 error ~ eps * lambda_max; the inverse
+    # amplifies it by 1 / lambda_min^2 (both eigenvalues from the oracle's fp64 values)
+    a, b, c = (osp[ok, k].astype(np.float64) for k in (2, 3, 4))
+    det = a * c - b * b
+    tr = a + c
+    lam_min_inv = 0.5 * (tr + np.sqrt(np.maximum((a - c) ** 2 + 4 * b * b, 0)))  # largest conic eigenvalue
+    lam_max_inv = det / lam_min_inv                                              # smallest conic eigenvalue
+    bound = 64 * H.EPS32 * lam_min_inv ** 2 / lam_max_inv
+    c_err = np.abs(sp[ok, 2:5] - osp[ok, 2:5]).max(1)
+    assert np.all(c_err <= bound), (c_err / bound).max()
+    np.testing.assert_allclose(sp[ok, 5], osp[ok, 5], rtol=4 * H.EPS32, atol=1e-7)      # opacity
+    np.testing.assert_allclose(sp[ok, 6:9], osp[ok, 6:9], rtol=0, atol=2e-6)           # colour
+    np.testing.assert_allclose(sp[ok, 9], osp[ok, 9], rtol=4 * H.EPS32)               # depth
+    assert np.all(sp[:, 10:] == 0)
+    # tile rectangles agree except where a rectangle edge (m +- r)/16 lies within the
+    # mean's error of an integer
+    same_rect = tt[ok] == ott[ok]
+    if not same_rect.all():
+        idx = np.nonzero(ok)[0][~same_rect]
+        for k in idx:
+            edges = np.array([osp[k, 0] - orad[k], osp[k, 0] + orad[k], osp[k, 1] - orad[k], osp[k, 1] + orad[k]]) / 16
+            assert np.min(np.abs(edges - np.round(edges))) * 16 < 1e-3, k
+
+
+def test_sh_colour_clamp_and_view_dependence(orc):
+    H.need_gpu()
+    cam = scenes.look_at((0, 0, 3), (0, 0, 0), 64, 64, 60, 60)
+    n = 256
+    rng = np.random.default_rng(0)
+    sh = rng.normal(0, 1.0, size=(n, 16, 3)).astype(np.float32)  # large: many colours clamp at 0
+    g = scenes.Gaussians(rng.uniform(-0.5, 0.5, (n, 3)).astype(np.float32), np.full((n, 3), -3, np.float32),
+                         np.tile(np.float32([1, 0, 0, 0]), (n, 1)), np.zeros(n, np.float32), sh, 3)
+    sp, rad, _ = H.run_project(cam, g)
+    osp, orad, _, _ = orc.project(cam, g)
+    ok = (rad > 0) & (orad > 0)
+    assert (sp[ok, 6:9] == 0).sum() > 50
+    np.testing.assert_allclose(sp[ok, 6:9], osp[ok, 6:9], atol=2e-5)
+
+
+def _bin_inputs(name):
+    if name == "tiny":
+        s = scenes.tiny()
+    elif name == "sphere512":
+        s = scenes.sphere512()
+    else:
+        s = scenes.soup1080(n_gauss=200_000, n_tri=40_000)
+    m = H.run_mesh(s.camera, s.mesh)
+    sp, rad, _ = H.run_project(s.camera, s.gaussians)
+    return s.camera, sp, rad, m
+
+
+@pytest.fixture(scope="module", params=["tiny", "sphere512", "soup_200k"])
+def bcase(request):
+    H.need_gpu()
+    return (request.param,) + _bin_inputs(request.param)
+
+
+@pytest.mark.parametrize("cull", [False, True])
+def test_bin_sort_teacher_forced_exact(bcase, cull, orc):
+    """Keys, ids and tile ranges from the GPU's own projected splats equal the
+    oracle's (stable sort on (tile, depth bits), then id) bit for bit, with
+    and without the occlusion cull; the pre-cull count too."""
+    name, cam, sp, rad, m = bcase
+    g = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull)
+    keys, gids, pre = orc.bin_gaussians(cam, sp, rad, m["tile_far"], m["tile_full"], cull)
+    assert g["K"] == len(keys) and g["counters"][1] == pre and g["counters"][2] == 0
+    np.testing.assert_array_equal(g["keys"], keys)
+    np.testing.assert_array_equal(g["gids"], gids)
+    start, _ = H.lists_from_bins(cam, keys, gids)
+    tr = g["tile_range"]
+    cnt = np.diff(start)
+    np.testing.assert_array_equal(tr[:, 1] - tr[:, 0], cnt)
+    np.testing.assert_array_equal(tr[cnt > 0, 0], start[:-1][cnt > 0])
+    print("%s cull=%d: K=%d (pre-cull %d), %d sort partitions" % (name, cull, len(keys), pre, -(-len(keys) // 3840)))
+
+
+def test_sort_stability_and_ragged_sizes(orc):
+    """Many Gaussians at one depth in the same tiles (ids must stay ascending),
+    K not a multiple of the partition size, several thousand partitions."""
+    H.need_gpu()
+    cam = scenes.look_at((0, 0, 3), (0, 0, 0), 480, 272, 300, 300)
+    rng = np.random.default_rng(3)
+    for n in (1, 7, 3839, 3841, 50_001):
+        sp = np.zeros((n, 12), np.float32)
+        sp[:, 0] = rng.uniform(0, 480, n)
+        sp[:, 1] = rng.uniform(0, 272, n)
+        sp[:, 9] = rng.choice(np.float32([0.5, 1.0, 1.0, 2.0]), n)  # heavy duplicates
+        rad = rng.integers(1, 40, n).astype(np.int32)
+        g = H.run_bin(cam, sp, rad)
+        keys, gids, _ = orc.bin_gaussians(cam, sp, rad)
+        np.testing.assert_array_equal(g["keys"], keys)
+        np.testing.assert_array_equal(g["gids"], gids)
+
+
+def test_capacity_overflow_is_reported_and_contained(orc):
+    H.need_gpu()
+    s = scenes.tiny()
+    sp, rad, tt = H.run_project(s.camera, s.gaussians)
+    need = int(tt.sum())
+    # synchronous mode: GM_ERR_CAPACITY with the needed count, then a retry that fits
+    g = H.run_bin(s.camera, sp, rad, cap=need // 3)
+    assert g["cap"] == need + 1 and g["K"] == need
+    # asynchronous mode: no error at the call, the overflow flag is set, no write past cap
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    cap = need // 2
+    keys = torch.zeros(cap + 64, dtype=torch.int64, device="cuda")
+    gids = torch.full((cap + 64,), -1, dtype=torch.int32, device="cuda")
+    tr = torch.zeros(H.n_tiles(s.camera), 2, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ws = torch.empty(gm.gm_bin_sort_gaussians_workspace_size(len(rad), cap, 64, 64), dtype=torch.uint8, device="cuda")
+    gm.gm_bin_sort_gaussians(gm.make_camera(s.camera), gm.make_opts(cull_occluded=False), H.dev(sp), H.dev(rad),
+                             None, None, keys, gids, tr, cap, cnt, ws, sync=False)
+    c = H.host(cnt)
+    assert c[0] == need and c[2] & gm.GM_FLAG_OVERFLOW
+    assert np.all(H.host(gids)[cap:] == -1) and np.all(H.host(keys)[cap:] == 0)
