@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the hybrid mesh + 3D Gaussian renderer on B300.
+
+One step = the whole path over one frame: triangle bins, z-buffer, mesh
+interpolation, Gaussian projection, Gaussian bins + sort (with the occlusion
+cull), compositing forward, compositing backward with mesh gradients.  The
+default workload is the 1920x1080 scene (200,000-triangle soup, 1,000,000
+Gaussians with degree-3 SH), inputs seeded and synthetic.
+
+Prints one JSON line (rank 0).  ``value`` is forward+backward megapixels per
+second over all ranks (each rank renders its own replica of the frame;
+weak scaling), with inputs resident in device memory and L2 flushed between
+steps; ``fwd_mpix_s`` is the forward alone.  ``e2e`` is the same metric
+measured through the public calls with host buffers: every step copies the
+inputs from pinned host memory and reads the image and gradients back.
+
+``--impl reference`` times the CPU oracle (the plain C restatement used by
+the tests) on a bounded sample of tiles of the same frame.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid render Mpix/s fwd and fwd+bwd at 1080p; % of per-stage roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gm", choices=["gm", "reference"])
+    ap.add_argument("--config", default="soup_1080p")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tiles", type=int, default=48, help="tiles of the frame the CPU oracle renders")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def run_gm(args, ws, rank, local):
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    from differentiable_hybrid_mesh_tile_b300 import build as gm_build
+    from differentiable_hybrid_mesh_tile_b300 import scenes
+
+    gm_build.build()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    scene = scenes.make(args.config)
+    cam = scene.camera
+    W, H = cam.width, cam.height
+    r = gm.HybridRenderer(cam, bg=scene.bg, cull_occluded=True, device="cuda")
+    r.upload(scene.mesh, scene.gaussians)
+    grads_np = scenes.upstream_grads(0, W, H)
+    g_dev = [torch.as_tensor(x).cuda() for x in grads_np]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stats_f = torch.zeros(1, dtype=torch.int64, device="cuda")
+    stats_b = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    cam_c, opts = r.cam, r.opts
+    names = ["tri_bin", "zbuffer", "interp", "project", "bin_sort", "composite_fwd", "composite_bwd"]
+
+    def step(evs=None, count=False):
+        def mark(k):
+            if evs is not None:
+                evs[k].record(stream)
+
+        mark(0)
+        gm.gm_bin_triangles(cam_c, r.V, r.F, r.tri_range, r.tri_ids, r.tri_cap, r.tri_counters, r.tri_ws, sync=False)
+        mark(1)
+        gm.gm_zbuffer(cam_c, r.V, r.F, r.tri_range, r.tri_ids, r.face_id)
+        mark(2)
+        gm.gm_interp_mesh(cam_c, r.V, r.F, r.vcol, r.face_id, r.mesh_depth, r.mesh_rgb, r.tile_far, r.tile_full)
+        mark(3)
+        gm.gm_project_gaussians(cam_c, opts, r.means, r.log_scales, r.quats, r.logits, r.colors, r.splats, r.radii,
+                                r.tiles_touched)
+        mark(4)
+        gm.gm_bin_sort_gaussians(cam_c, opts, r.splats, r.radii, r.tile_far, r.tile_full, r.keys, r.gids, r.g_range,
+                                 r.g_cap, r.g_counters, r.g_ws, sync=False)
+        mark(5)
+        gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                   r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
+                                   stats_f if count else None)
+        mark(6)
+        r.v_splats.zero_()
+        r.v_verts.zero_()
+        r.v_vcol.zero_()
+        gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                   r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats, r.V, r.F,
+                                   r.vcol, r.v_verts, r.v_vcol, stats_b if count else None)
+        mark(7)
+
+    # sizing pass (host read-back of K, capacities grow), then warm-up without syncs
+    r.forward(sync=True)
+    r.backward(*g_dev)
+    torch.cuda.synchronize()
+    stats_f.zero_()
+    stats_b.zero_()
+    step(count=True)
+    torch.cuda.synchronize()
+    pairs_f, pairs_b = int(stats_f.item()), int(stats_b.item())
+    K_tri = int(r.tri_counters[0].item())
+    K_g = int(r.g_counters[0].item())
+    K_pre = int(r.g_counters[1].item())
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush.zero_()
+            step(evs[k])
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    clocks = clk.summary()
+    overflow = r.overflowed()
+    st = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(7)] for k in range(args.steps)])
+    step_ms = st.sum(1)
+    fwd_ms = st[:, :6].sum(1)
+    ms_step = float(step_ms.mean())
+    ms_fwd = float(fwd_ms.mean())
+    if dist is not None:
+        t = torch.tensor([ms_step, ms_fwd], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_fwd = float(t[0]), float(t[1])
+    n = ws
+    mpix = W * H / 1e6
+    value = n * mpix / (ms_step / 1e3)
+    fwd_value = n * mpix / (ms_fwd / 1e3)
+    stage_ms = {names[i]: float(st[:, i].mean()) for i in range(7)}
+
+    # ---- roofline of each stage (algorithmic work per launch / measured duration)
+    import json as _json
+    peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm_peak = float(peaks.get("hbm_gbs", 6400.0))
+    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    clk_mhz = clocks["sm_mhz"] or peaks.get("sm_max_mhz", 2032.0)
+    alu_peak = sms * 128 * clk_mhz * 1e6 / 1e12  # FP32 lane-ops/s, Tops
+    N = r.N
+    sh = r.sh_degree
+    col_bytes = 12 if sh < 0 else 12 * (sh + 1) ** 2
+    F = int(r.F.shape[0])
+    T = r.T
+    passes_g = math.ceil((32 + max((T - 1).bit_length(), 0)) / 8)
+    passes_t = math.ceil(max((T - 1).bit_length(), 0) / 8)
+    work = {
+        # bytes the stage must move at least once
+        "project": ("hbm", N * (12 + 12 + 16 + 4 + col_bytes) + N * (48 + 4 + 4)),
+        "bin_sort": ("hbm", N * (4 + 16) + N * 4 + N * 8 + N * (4 + 16 + 4) + K_g * 12 + K_g * 8
+                     + passes_g * K_g * 24 + K_g * 8 + T * 8),
+        "tri_bin": ("hbm", F * (12 + 36) * 2 + F * 12 + K_tri * 12 + K_tri * 8 + passes_t * K_tri * 24
+                    + K_tri * 8 + T * 8),
+        "interp": ("hbm", W * H * (4 + 4 + 12) + T * 5),
+        # FP32 lane operations: 20 per evaluated (pixel, Gaussian) pair forward, 60 backward
+        "composite_fwd": ("alu", 20 * pairs_f),
+        "composite_bwd": ("alu", 60 * pairs_b),
+    }
+    stages = {}
+    for k, (bound, amount) in work.items():
+        t_s = stage_ms[k] / 1e3
+        if bound == "hbm":
+            ach = amount / t_s / 1e9
+            stages[k] = {"bound": "hbm", "ms": stage_ms[k], "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": ach / hbm_peak, "algorithmic": amount}
+        else:
+            ach = amount / t_s / 1e12
+            stages[k] = {"bound": "alu", "ms": stage_ms[k], "achieved": ach, "peak": alu_peak, "unit": "Tops/s",
+                         "frac": ach / alu_peak, "algorithmic": amount}
+    stages["zbuffer"] = {"bound": "alu", "ms": stage_ms["zbuffer"], "note": "reported, no target"}
+    top = max(work, key=lambda k: stage_ms[k])
+    roof = dict(stages[top])
+    roof.update(kernel=top, traffic=None, peak_source=hbm_src if roof["bound"] == "hbm" else
+                "SMs x 128 FP32 lanes x median SM clock under load")
+    roof.pop("ms", None)
+    roof.pop("algorithmic", None)
+
+    launches = (3 + 2 + passes_t + 1) + 1 + 1 + 1 + (3 + 2 + passes_g + 1) + 1 + 2
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, r, scene, grads_np, flush, ws, dist)
+
+    return dict(value=value, fwd=fwd_value, ms_step=ms_step, ms_fwd=ms_fwd, stages=stages, roofline=roof,
+                clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_tri=K_tri, K_g=K_g, K_pre=K_pre,
+                pairs_f=pairs_f, pairs_b=pairs_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
+                gpu_name=props.name)
+
+
+def run_e2e(args, r, scene, grads_np, flush, ws, dist):
+    """Same step through the public calls with host buffers: pinned H2D of the
+    inputs and upstream gradients, the seven calls, D2H of image and gradients."""
+    import torch
+    ins = [(r.means, scene.gaussians.means), (r.log_scales, scene.gaussians.log_scales),
+           (r.quats, scene.gaussians.quats), (r.logits, scene.gaussians.logits), (r.colors, scene.gaussians.colors),
+           (r.V, scene.mesh.verts), (r.F, scene.mesh.faces), (r.vcol, scene.mesh.vcol)]
+    host_in = [(d, torch.as_tensor(np.ascontiguousarray(h)).pin_memory()) for d, h in ins]
+    g_host = [torch.as_tensor(x).pin_memory() for x in grads_np]
+    g_dev = [torch.empty_like(x, device="cuda") for x in g_host]
+    outs = [r.out_rgb, r.out_depth, r.out_alpha, r.v_splats, r.v_verts, r.v_vcol]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in) + sum(x.numel() * x.element_size() for x in g_host)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(g_dev, g_host):
+            d.copy_(h, non_blocking=True)
+        r.forward(sync=False)
+        r.backward(*g_dev)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.mean(times))
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    val = ws * r.W * r.H / 1e6 / (ms / 1e3)
+    return {"value": val, "unit": "Mpix/s", "ms_per_step": ms, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# -------------------------------------------------------------- CPU arm ---
+
+def oracle_sample(scene, n_tiles, seed=0):
+    import oracle
+    from differentiable_hybrid_mesh_tile_b300 import scenes
+    oracle.build()
+    cam = scene.camera
+    tiles = scenes.sample_tiles(seed, oracle.n_tiles(cam), n_tiles)
+    t0 = time.perf_counter()
+    out = oracle.render(scene, tiles=tiles)
+    dt = time.perf_counter() - t0
+    px = int(sum(min(16, cam.width - (t % ((cam.width + 15) // 16)) * 16) *
+                 min(16, cam.height - (t // ((cam.width + 15) // 16)) * 16) for t in tiles))
+    return px, dt, out
+
+
+def omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v else (os.cpu_count() or 1)
+
+
+def cpu_baseline(args, scene):
+    px, dt, _ = oracle_sample(scene, args.cpu_tiles)
+    return {"value": px / 1e6 / dt, "unit": "Mpix/s", "cores": omp_threads(), "kind": "oracle",
+            "sample": "forward of %d seeded tiles (%d px) of the %dx%d frame: brute-force z-buffer over all "
+                      "%d triangles, projection of all %d Gaussians, full per-tile sort, fp32 composite; %.1f s"
+                      % (args.cpu_tiles, px, scene.camera.width, scene.camera.height, len(scene.mesh.faces),
+                         len(scene.gaussians.means), dt)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from differentiable_hybrid_mesh_tile_b300 import scenes
+    scene = scenes.make(args.config)
+    n_tiles = 4
+    for k in range(args.warmup):
+        oracle_sample(scene, n_tiles, seed=100 + k)
+    times, pxs = [], []
+    for k in range(args.steps):
+        px, dt, _ = oracle_sample(scene, n_tiles, seed=k)
+        times.append(dt)
+        pxs.append(px)
+    ms = 1e3 * float(np.mean(times))
+    val = float(np.sum(pxs)) / 1e6 / float(np.sum(times))
+    cfg = config_dict(args, scene, ws)
+    sample = "forward of %d seeded tiles per step (~%d px) of the %dx%d frame" % (
+        n_tiles, int(np.mean(pxs)), scene.camera.width, scene.camera.height)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "Mpix/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": val, "unit": "Mpix/s", "cores": omp_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "Mpix/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_dict(args, scene, ws):
+    cam = scene.camera
+    g = scene.gaussians
+    return {"workload": "%s: %dx%d px, %d-triangle mesh, %d Gaussians (SH degree %d), one view" % (
+                args.config, cam.width, cam.height, len(scene.mesh.faces), len(g.means), g.sh_degree),
+            "width": cam.width, "height": cam.height, "triangles": len(scene.mesh.faces),
+            "gaussians": len(g.means), "sh_degree": g.sh_degree, "cull_occluded": True,
+            "parallelism": "replica x%d" % ws, "l2": "flushed between steps (512 MiB write)"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    ws, rank, local = dist_env()
+    res = run_gm(args, ws, rank, local)
+    dist = res["dist"]
+    if rank == 0:
+        from differentiable_hybrid_mesh_tile_b300 import scenes
+        scene = scenes.make(args.config)
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            cpu = cpu_baseline(args, scene)
+        line = {
+            "metric": METRIC, "value": res["value"], "unit": "Mpix/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(args, scene, ws),
+            "fwd_mpix_s": res["fwd"], "ms_fwd": res["ms_fwd"], "fps_fwd": 1e3 / res["ms_fwd"],
+            "fps_fwd_bwd": 1e3 / res["ms_step"],
+            "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
+            "gpu_launches": res["launches"] * args.steps, "clocks": res["clocks"],
+            "counts": {"K_triangle_tile": res["K_tri"], "K_gauss_tile": res["K_g"], "K_gauss_tile_precull":
+                       res["K_pre"], "pairs_fwd": res["pairs_f"], "pairs_bwd": res["pairs_b"]},
+            "overflow": res["overflow"], "gpu": res["gpu_name"], "wall_s_timed": res["wall"],
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

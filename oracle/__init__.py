@@ -21,7 +21,7 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
           "-Wall", "-Wextra", "-shared", "-fPIC"]
 
 S_STRIDE = 12
-FD_STATUS = {0: "ok", 1: "flip", 2: "precision", 3: "tie", 4: "order", 5: "unused"}
+FD_STATUS = {0: "ok", 1: "flip", 2: "precision", 3: "tie", 4: "order", 5: "unused", 6: "nonsmooth"}
 
 
 def build(force: bool = False) -> str:
@@ -165,15 +165,20 @@ def bin_gaussians(cam, splats, radii, tile_far=None, tile_full=None, cull=False)
     return keys[:K], gids[:K], int(pre.value)
 
 
-def tile_lists(cam, splats, radii):
+def tile_lists(cam, splats, radii, tiles=None):
+    """CSR lists (tile_start[T+1], entries) over all tiles, or only ``tiles``."""
     splats, radii = _c(splats, np.float32), _c(radii, np.int32)
     T = n_tiles(cam)
+    mask = None
+    if tiles is not None:
+        mask = np.zeros(T, np.uint8)
+        mask[np.asarray(tiles, np.int64)] = 1
     start = np.zeros(T + 1, np.int64)
     c = _cam(cam)
-    K = lib().orc_tile_lists(C.byref(c), C.c_int32(len(radii)), _p(splats), _p(radii), _p(start), None,
+    K = lib().orc_tile_lists(C.byref(c), C.c_int32(len(radii)), _p(splats), _p(radii), _p(mask), _p(start), None,
                              C.c_int64(0))
     entries = np.zeros(max(K, 1), np.int32)
-    lib().orc_tile_lists(C.byref(c), C.c_int32(len(radii)), _p(splats), _p(radii), _p(start),
+    lib().orc_tile_lists(C.byref(c), C.c_int32(len(radii)), _p(splats), _p(radii), _p(mask), _p(start),
                          _p(entries), C.c_int64(K))
     return start, entries
 
@@ -275,7 +280,7 @@ def render(scene, cam=None, tiles=None):
     face_id[sel], mesh_depth[sel], mesh_rgb[sel] = fid_s, depth_s, rgb_s
     best[sel], second[sel] = best_s, second_s
     splats, radii, touched, margin = project(cam, scene.gaussians)
-    lists = tile_lists(cam, splats, radii)
+    lists = tile_lists(cam, splats, radii, tiles_arr)
     out = composite_fwd(cam, scene.bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles_arr)
     out.update(face_id=face_id.reshape(H, W), mesh_depth=mesh_depth.reshape(H, W),
                mesh_rgb=mesh_rgb.reshape(H, W, 3), zbest=best.reshape(H, W),

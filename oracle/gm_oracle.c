@@ -583,9 +583,24 @@ static uint32_t fbits(float f)
  * (Hybrid rendering, cull_occluded bullet).  Sorted ascending by key, then
  * id.  Returns the number of entries after the cull; *pre gets the number
  * before it.  keys/gids are written when non-NULL and the total fits cap.  */
+int64_t orc_bin_gaussians_masked(const orc_camera* c, int32_t N, const float* splats, const int32_t* radii,
+                                 const float* tile_far, const uint8_t* tile_full, int32_t cull,
+                                 const uint8_t* tile_mask, uint64_t* keys, int32_t* gids, int64_t cap,
+                                 int64_t* pre);
+
 int64_t orc_bin_gaussians(const orc_camera* c, int32_t N, const float* splats, const int32_t* radii,
                           const float* tile_far, const uint8_t* tile_full, int32_t cull,
                           uint64_t* keys, int32_t* gids, int64_t cap, int64_t* pre)
+{
+    return orc_bin_gaussians_masked(c, N, splats, radii, tile_far, tile_full, cull, NULL, keys, gids, cap, pre);
+}
+
+/* As orc_bin_gaussians, restricted to the tiles with tile_mask[t] != 0 (all
+ * tiles when tile_mask is NULL): the same entries, fewer tiles.            */
+int64_t orc_bin_gaussians_masked(const orc_camera* c, int32_t N, const float* splats, const int32_t* radii,
+                                 const float* tile_far, const uint8_t* tile_full, int32_t cull,
+                                 const uint8_t* tile_mask, uint64_t* keys, int32_t* gids, int64_t cap,
+                                 int64_t* pre)
 {
     int TW = n_tiles_x(c);
     int64_t total = 0, before = 0;
@@ -604,6 +619,7 @@ int64_t orc_bin_gaussians(const orc_camera* c, int32_t N, const float* splats, c
             for (int ty = rect[1]; ty < rect[3]; ++ty)
                 for (int tx = rect[0]; tx < rect[2]; ++tx) {
                     int64_t tile = (int64_t)ty * TW + tx;
+                    if (tile_mask && !tile_mask[tile]) continue;
                     if (pass == 0) before++;
                     if (cull && tile_full[tile] && s[S_Z] >= tile_far[tile])
                         continue;
@@ -630,14 +646,15 @@ int64_t orc_bin_gaussians(const orc_camera* c, int32_t N, const float* splats, c
 }
 
 /* Full per-tile candidate lists for compositing (no cull): tile t holds every
- * binned Gaussian whose rectangle contains it, ordered by (depth, id).
+ * binned Gaussian whose rectangle contains it, ordered by (depth, id); only
+ * tiles with tile_mask[t] != 0 get entries when a mask is given.
  * tile_start[T+1] is filled always; entries when non-NULL and K fits cap. */
 int64_t orc_tile_lists(const orc_camera* c, int32_t N, const float* splats, const int32_t* radii,
-                       int64_t* tile_start, int32_t* entries, int64_t cap)
+                       const uint8_t* tile_mask, int64_t* tile_start, int32_t* entries, int64_t cap)
 {
     int TW = n_tiles_x(c), TH = n_tiles_y(c);
     int64_t T = (int64_t)TW * TH;
-    int64_t K = orc_bin_gaussians(c, N, splats, radii, NULL, NULL, 0, NULL, NULL, 0, NULL);
+    int64_t K = orc_bin_gaussians_masked(c, N, splats, radii, NULL, NULL, 0, tile_mask, NULL, NULL, 0, NULL);
     if (!entries || K > cap) {
         /* counts only */
         memset(tile_start, 0, sizeof(int64_t) * (T + 1));
@@ -646,13 +663,14 @@ int64_t orc_tile_lists(const orc_camera* c, int32_t N, const float* splats, cons
             const float* s = splats + S_STRIDE * (int64_t)g;
             if (gauss_rect(c, s[S_MX], s[S_MY], radii[g], rect) <= 0) continue;
             for (int ty = rect[1]; ty < rect[3]; ++ty)
-                for (int tx = rect[0]; tx < rect[2]; ++tx) tile_start[(int64_t)ty * TW + tx + 1]++;
+                for (int tx = rect[0]; tx < rect[2]; ++tx)
+                    if (!tile_mask || tile_mask[(int64_t)ty * TW + tx]) tile_start[(int64_t)ty * TW + tx + 1]++;
         }
         for (int64_t t = 0; t < T; ++t) tile_start[t + 1] += tile_start[t];
         return K;
     }
     uint64_t* keys = (uint64_t*)malloc(sizeof(uint64_t) * (K > 0 ? K : 1));
-    orc_bin_gaussians(c, N, splats, radii, NULL, NULL, 0, keys, entries, K, NULL);
+    orc_bin_gaussians_masked(c, N, splats, radii, NULL, NULL, 0, tile_mask, keys, entries, K, NULL);
     for (int64_t t = 0; t <= T; ++t) tile_start[t] = 0;
     for (int64_t k = 0; k < K; ++k) tile_start[(keys[k] >> 32) + 1]++;
     for (int64_t t = 0; t < T; ++t) tile_start[t + 1] += tile_start[t];
@@ -680,6 +698,10 @@ typedef struct {
     int32_t n_contrib;
     /* smallest relative distance of a decision operand to its threshold */
     double m_depth, m_alpha, m_clamp, m_stop, m_sigma;
+    /* the watched Gaussian: its trace code (0 = not reached) and the smallest
+     * margin of its own decisions */
+    int self_code;
+    double m_self;
 } pix_t;
 
 static inline double rnd(double x, int f32) { return f32 ? (double)(float)x : x; }
@@ -701,22 +723,34 @@ static inline double sfield(const float* splats, int g, int f, const pert_t* p)
  *   rgb = C + T (covered ? c_mesh : bg);  depth = Z + T covered D;
  *   alpha = 1 - T (1 - covered).
  * trace[k] (optional) records the decision taken on list entry k.        */
+#define SET_CODE(c)                      \
+    do {                                 \
+        if (trace) trace[k] = (c);       \
+        if (g == watch) o->self_code = (c); \
+    } while (0)
+
 static void composite_pixel(int f32, double px, double py, const int32_t* list, int64_t n,
                             const float* splats, double D, int covered, const double cm[3],
                             const double bg[3], const pert_t* p, pix_t* o, uint8_t* trace,
-                            int64_t* trace_len)
+                            int64_t* trace_len, int watch)
 {
     double T = 1.0, C[3] = {0, 0, 0}, Z = 0.0;
     int32_t last = 0;
     const double amax = rnd(ALPHA_MAX, f32), amin = rnd(ALPHA_MIN, f32), tstop = rnd(T_STOP, f32);
     o->m_depth = o->m_alpha = o->m_clamp = o->m_stop = o->m_sigma = INFINITY;
+    o->self_code = 0;
+    o->m_self = INFINITY;
     int64_t k;
     for (k = 0; k < n; ++k) {
         int g = list[k];
         double z = sfield(splats, g, S_Z, p);
-        if (D < INFINITY) o->m_depth = fmin(o->m_depth, fabs(z - D) / D);
+        if (D < INFINITY) {
+            double m = fabs(z - D) / D;
+            o->m_depth = fmin(o->m_depth, m);
+            if (g == watch) o->m_self = fmin(o->m_self, m);
+        }
         if (!(z < D)) {
-            if (trace) trace[k] = TR_DEPTH;
+            SET_CODE(TR_DEPTH);
             continue;
         }
         double dx = rnd(px - sfield(splats, g, S_MX, p), f32);
@@ -728,25 +762,31 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
         double half = rnd(0.5 * rnd(qa + qc, f32), f32);
         double cross = rnd(rnd(cb * dx, f32) * dy, f32);
         double sigma = rnd(half + cross, f32);
-        o->m_sigma = fmin(o->m_sigma, fabs(sigma) / (fabs(half) + fabs(cross) + 1e-30));
+        double ms = fabs(sigma) / (fabs(half) + fabs(cross) + 1e-30);
+        o->m_sigma = fmin(o->m_sigma, ms);
         if (sigma < 0.0) {
-            if (trace) trace[k] = TR_SIGMA;
+            SET_CODE(TR_SIGMA);
             continue;
         }
         double G = rnd(exp(-sigma), f32);
         double oG = rnd(sfield(splats, g, S_OP, p) * G, f32);
-        o->m_clamp = fmin(o->m_clamp, fabs(oG - amax) / amax);
+        double mc = fabs(oG - amax) / amax;
+        o->m_clamp = fmin(o->m_clamp, mc);
         int clamped = oG > amax;
         double alpha = clamped ? amax : oG;
-        o->m_alpha = fmin(o->m_alpha, fabs(alpha - amin) / amin);
+        double ma = fabs(alpha - amin) / amin;
+        o->m_alpha = fmin(o->m_alpha, ma);
+        if (g == watch) o->m_self = fmin(o->m_self, fmin(ms, fmin(mc, ma)));
         if (alpha < amin) {
-            if (trace) trace[k] = TR_ALPHA;
+            SET_CODE(TR_ALPHA);
             continue;
         }
         double Tn = rnd(T * rnd(1.0 - alpha, f32), f32);
-        o->m_stop = fmin(o->m_stop, fabs(Tn - tstop) / tstop);
+        double mt = fabs(Tn - tstop) / tstop;
+        o->m_stop = fmin(o->m_stop, mt);
+        if (g == watch) o->m_self = fmin(o->m_self, mt);
         if (Tn <= tstop) {
-            if (trace) trace[k] = TR_STOP;
+            SET_CODE(TR_STOP);
             k++;
             break;
         }
@@ -755,7 +795,7 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
         Z += w * z;
         T = Tn;
         last = (int32_t)(k + 1);
-        if (trace) trace[k] = clamped ? TR_BLEND_CLAMPED : TR_BLEND;
+        SET_CODE(clamped ? TR_BLEND_CLAMPED : TR_BLEND);
     }
     if (trace_len) *trace_len = k;
     for (int ch = 0; ch < 3; ++ch) o->rgb[ch] = C[ch] + T * (covered ? cm[ch] : bg[ch]);
@@ -793,7 +833,7 @@ void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats
                 double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
                 pix_t o;
                 composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, (double)mesh_depth[pix], cov, cm,
-                                bgd, NULL, &o, NULL, NULL);
+                                bgd, NULL, &o, NULL, NULL, -1);
                 for (int ch = 0; ch < 3; ++ch) out_rgb[3 * pix + ch] = (float)o.rgb[ch];
                 out_depth[pix] = (float)o.depth;
                 out_alpha[pix] = (float)o.alpha;
@@ -815,7 +855,18 @@ void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats
  * Gradients by central finite differences (double), decisions held fixed
  * ====================================================================== */
 
-enum { FD_OK = 0, FD_FLIP = 1, FD_PRECISION = 2, FD_TIE = 3, FD_ORDER = 4, FD_UNUSED = 5 };
+enum { FD_OK = 0, FD_FLIP = 1, FD_PRECISION = 2, FD_TIE = 3, FD_ORDER = 4, FD_UNUSED = 5, FD_NONSMOOTH = 6 };
+
+/* Central differences at steps h and h/2 combined by Richardson's rule
+ * (error O(h^4)).  Where the two differ by more than 1% the loss is too
+ * curved at this scale for either to be trusted: FD_NONSMOOTH.            */
+static int richardson(double lp, double lm, double lp2, double lm2, double h, double* g)
+{
+    double g1 = (lp - lm) / (2.0 * h);
+    double g2 = (lp2 - lm2) / h;
+    *g = g2 + (g2 - g1) / 3.0;
+    return fabs(g1 - g2) <= 1e-2 * fabs(g2) + 1e-7 ? FD_OK : FD_NONSMOOTH;
+}
 
 static double pixel_loss(const pix_t* o, const float* g_rgb, const float* g_depth,
                          const float* g_alpha, int64_t pix)
@@ -839,8 +890,10 @@ static int tie_pixel(const pix_t* o, double band)
  * tiles in the Gaussian's rectangle can change; the tile lists stay fixed.
  * status: FD_OK; FD_FLIP a decision differs between +h and -h;
  * FD_PRECISION the double and fp32 evaluations decide differently at h = 0;
- * FD_TIE an fp32 decision margin is below tie_band on an affected pixel;
- * FD_ORDER a depth step would reorder the list.                          */
+ * FD_TIE an fp32 decision margin is below tie_band where it matters;
+ * FD_ORDER a depth step would reorder the list; FD_NONSMOOTH the steps h and
+ * h/2 disagree (see richardson).  Decisions are compared at +-h, which
+ * brackets the +-h/2 evaluations.                                        */
 void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats, const int32_t* radii,
                       const int64_t* tile_start, const int32_t* entries,
                       const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
@@ -869,8 +922,8 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                 status[q] = FD_UNUSED;
                 continue;
             }
-            pert_t pp = {g, field, h}, pm = {g, field, -h};
-            double lp = 0.0, lm = 0.0;
+            pert_t pp = {g, field, h}, pm = {g, field, -h}, pp2 = {g, field, 0.5 * h}, pm2 = {g, field, -0.5 * h};
+            double lp = 0.0, lm = 0.0, lp2 = 0.0, lm2 = 0.0;
             int st = FD_OK;
             for (int ty = rect[1]; ty < rect[3] && st == FD_OK; ++ty)
                 for (int tx = rect[0]; tx < rect[2] && st == FD_OK; ++tx) {
@@ -894,11 +947,15 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                             double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
                             pix_t o32, o0, op, om;
                             int64_t n32, n0, np_, nm;
-                            composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o32, tr[0], &n32);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o0, tr[1], &n0);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pp, &op, tr[2], &np_);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pm, &om, tr[3], &nm);
-                            if (tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
+                            composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o32, tr[0], &n32, g);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o0, tr[1], &n0, g);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pp, &op, tr[2], &np_, g);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pm, &om, tr[3], &nm, g);
+                            /* a decision within rounding of its threshold matters where this
+                             * Gaussian is composited (every decision of the pixel enters its
+                             * gradient) or in its own decisions */
+                            int blended = o32.self_code == TR_BLEND || o32.self_code == TR_BLEND_CLAMPED;
+                            if ((blended && tie_pixel(&o32, tie_band)) || o32.m_self < tie_band) { st = FD_TIE; break; }
                             if (!same_trace(tr[0], n32, tr[1], n0)) { st = FD_PRECISION; break; }
                             if (!same_trace(tr[1], n0, tr[2], np_) || !same_trace(tr[1], n0, tr[3], nm)) {
                                 st = FD_FLIP;
@@ -906,10 +963,16 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                             }
                             lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
                             lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pp2, &op, NULL, NULL, -1);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pm2, &om, NULL, NULL, -1);
+                            lp2 += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
+                            lm2 += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
                         }
                 }
+            double gv = 0.0;
+            if (st == FD_OK) st = richardson(lp, lm, lp2, lm2, h, &gv);
             status[q] = st;
-            grad[q] = st == FD_OK ? (lp - lm) / (2.0 * h) : 0.0;
+            grad[q] = st == FD_OK ? gv : 0.0;
         }
         for (int k = 0; k < 4; ++k) free(tr[k]);
     }
@@ -963,7 +1026,7 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
         for (int32_t q = 0; q < n_req; ++q) {
             int vid = req_vid[q], field = req_field[q];
             double h = req_h[q];
-            double lp = 0.0, lm = 0.0;
+            double lp = 0.0, lm = 0.0, lp2 = 0.0, lm2 = 0.0;
             int st = FD_OK, any = 0;
             for (int64_t fk = vstart[vid]; fk < vstart[vid + 1] && st == FD_OK; ++fk) {
                 int f = vface[fk];
@@ -973,13 +1036,14 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                     int64_t tile = (int64_t)(j / TILE) * TW + i / TILE;
                     const int32_t* list = entries + tile_start[tile];
                     int64_t n = tile_start[tile + 1] - tile_start[tile];
-                    double Dv[3], cmv[3][3];
-                    for (int sgn = 0; sgn < 3; ++sgn) {
+                    double Dv[5], cmv[5][3];
+                    for (int sgn = 0; sgn < 5; ++sgn) {
                         double X[3][3], C3[3][3], D, w[3];
                         load_tri(V, F, f, X);
                         for (int k = 0; k < 3; ++k)
                             for (int d = 0; d < 3; ++d) C3[k][d] = vcol[3 * (int64_t)F[3 * f + k] + d];
-                        double delta = sgn == 0 ? 0.0 : (sgn == 1 ? h : -h);
+                        const double steps[5] = {0.0, h, -h, 0.5 * h, -0.5 * h};
+                        double delta = steps[sgn];
                         for (int k = 0; k < 3; ++k) {
                             if (F[3 * f + k] != vid) continue;
                             if (field < 3) X[k][field] += delta;
@@ -995,11 +1059,13 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                     double cm32[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
                     pix_t o32, o0, op, om;
                     int64_t n32, n0, np_, nm;
-                    composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, mesh_depth[pix], 1, cm32, bgd, NULL, &o32, tr[0], &n32);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[0], 1, cmv[0], bgd, NULL, &o0, tr[1], &n0);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[1], 1, cmv[1], bgd, NULL, &op, tr[2], &np_);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[2], 1, cmv[2], bgd, NULL, &om, tr[3], &nm);
-                    if (o32.m_depth < tie_band || tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
+                    composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, mesh_depth[pix], 1, cm32, bgd, NULL, &o32, tr[0], &n32, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[0], 1, cmv[0], bgd, NULL, &o0, tr[1], &n0, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[1], 1, cmv[1], bgd, NULL, &op, tr[2], &np_, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[2], 1, cmv[2], bgd, NULL, &om, tr[3], &nm, -1);
+                    /* depth-test decisions: the PRECISION check below compares them
+                     * exactly; alpha / stop / sigma decisions within rounding: a tie */
+                    if (tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
                     if (!same_trace(tr[0], n32, tr[1], n0)) { st = FD_PRECISION; break; }
                     if (!same_trace(tr[1], n0, tr[2], np_) || !same_trace(tr[1], n0, tr[3], nm)) {
                         st = FD_FLIP;
@@ -1007,12 +1073,18 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                     }
                     lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
                     lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[3], 1, cmv[3], bgd, NULL, &op, NULL, NULL, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[4], 1, cmv[4], bgd, NULL, &om, NULL, NULL, -1);
+                    lp2 += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
+                    lm2 += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
                     any = 1;
                 }
             }
             if (st == FD_OK && !any) st = FD_UNUSED;
+            double gv = 0.0;
+            if (st == FD_OK) st = richardson(lp, lm, lp2, lm2, h, &gv);
             status[q] = st;
-            grad[q] = st == FD_OK ? (lp - lm) / (2.0 * h) : 0.0;
+            grad[q] = st == FD_OK ? gv : 0.0;
         }
         for (int k = 0; k < 4; ++k) free(tr[k]);
     }
@@ -1027,7 +1099,7 @@ void orc_composite_one(int32_t f32, double px, double py, const int32_t* list, i
                        const double* bg, double* out)
 {
     pix_t o;
-    composite_pixel(f32, px, py, list, n, splats, D, covered, cm, bg, NULL, &o, NULL, NULL);
+    composite_pixel(f32, px, py, list, n, splats, D, covered, cm, bg, NULL, &o, NULL, NULL, -1);
     out[0] = o.rgb[0]; out[1] = o.rgb[1]; out[2] = o.rgb[2];
     out[3] = o.depth; out[4] = o.alpha; out[5] = o.T; out[6] = o.n_contrib;
 }

@@ -159,3 +159,19 @@ def tie_pixels(margins, alpha_band=2e-6, stop_band=1e-4, sigma_band=1e-5, clamp_
     if clamp_band is not None:
         t |= m[..., 2] < clamp_band
     return t
+
+
+def input_ulp_perturbations(cam, V, draws=3, seed=0):
+    """World vertex sets moved by about one fp32 rounding of the camera-space
+    coordinates: each coordinate by 2 eps (|V| + |camera centre|) with a random
+    sign.  The oracle evaluated on them bounds how far any fp32 evaluation of
+    an ill-conditioned quantity (an edge-on triangle) can land from the exact
+    value."""
+    rng = np.random.default_rng(seed)
+    C = -cam.R.astype(np.float64).T @ cam.t.astype(np.float64)
+    scale = 2 * EPS32 * (np.abs(V.astype(np.float64)) + np.linalg.norm(C))
+    out = []
+    for _ in range(draws):
+        r = rng.choice([-1.0, 1.0], size=V.shape)
+        out.append((V.astype(np.float64) + scale * r).astype(np.float32))
+    return out
