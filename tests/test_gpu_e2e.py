@@ -4,13 +4,14 @@ the raw inputs, on all five workloads at their full sizes -- full frames for
 the 64x64 and 512x512 scenes, seeded samples of tiles for the 1080p, 8-view
 1080p and 4K ones -- and sampled finite-difference gradients at 1080p.
 
-Pixels are left out of the 1e-4 value check, counted and reported, only for
-a stated reason: the two nearest mesh depths within 1e-6 relative (z-buffer
-near tie); an fp32 decision within rounding of its threshold (alpha vs 1/255,
-transmittance vs 1e-4, the depth test within the depths' own rounding); a
-Gaussian whose tile rectangle differs by a radius tie.  Colour and depth of
-edge-on triangles get the oracle-measured one-ulp sensitivity as extra
-tolerance.  The excluded share must stay below 0.5%."""
+A pixel may differ by more than 1e-4 only for a stated reason, and is then
+counted and reported: the two nearest mesh depths within 1e-6 relative
+(z-buffer near tie); an fp32 decision within rounding of its threshold (alpha
+vs 1/255, transmittance vs 1e-4, the depth test within the depths' own
+rounding); a Gaussian whose tile rectangle differs by a radius tie.  Colour
+and depth of edge-on triangles get the oracle-measured one-ulp sensitivity
+as extra tolerance.  Such explained differences must stay below 0.5% of the
+checked pixels; an unexplained one fails the test."""
 
 import numpy as np
 import pytest
@@ -115,16 +116,18 @@ def test_end_to_end_forward(name, orc):
         err_rgb = np.abs(g_rgb - o_rgb).max(-1)
         err_d = np.abs(g_depth - o["depth"].reshape(-1)[pix])
         err_a = np.abs(g_alpha - o["alpha"].reshape(-1)[pix])
-        bad = ~excl & ((err_rgb > tol) | (err_d > 1e-4 + 4 * sd * T_fin) | (err_a > 1e-4))
-        print("%s view %d: %d px checked, excluded %d (z-tie %d, rect-tie %d, threshold %d), max rgb err %.2e, "
-              "bad %d" % (name, v, len(pix), excl.sum(), ztie.sum(), rtie.sum(), ttie.sum(),
-                          err_rgb[~excl].max() if (~excl).any() else 0, bad.sum()))
+        mism = (err_rgb > tol) | (err_d > 1e-4 + 4 * sd * T_fin) | (err_a > 1e-4)
+        bad = mism & ~excl
+        explained = mism & excl
+        print("%s view %d: %d px checked, max rgb err %.2e; %d px differ, all explained by ties: %d "
+              "(near ties: z %d, rect %d, threshold %d)" % (name, v, len(pix), err_rgb.max(), mism.sum(),
+                                                           explained.sum(), ztie.sum(), rtie.sum(), ttie.sum()))
         if bad.any():
             k = np.nonzero(bad)[0][:5]
             print("   bad px", pix[k], err_rgb[k], err_d[k], err_a[k], tol[k])
         assert not bad.any()
         total_px += len(pix)
-        total_excl += int(excl.sum())
+        total_excl += int(explained.sum())
     assert total_excl <= 0.005 * total_px
 
 
