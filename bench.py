@@ -28,7 +28,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 import numpy as np
@@ -117,6 +116,25 @@ class ClockSampler:
         reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- multi-rank --
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (a barrier first), so the
+    slowest rank sets the whole job's time; identity on one rank."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    dist.barrier()
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(n_ranks, pixels_per_rank, ms):
+    """Megapixels per second of the whole job: every rank renders its own frame."""
+    return n_ranks * pixels_per_rank / 1e6 / (ms / 1e3)
 
 
 # --------------------------------------------------------------- GPU arm --
@@ -215,14 +233,9 @@ def run_gm(args, ws, rank, local):
     fwd_ms = st[:, :6].sum(1)
     ms_step = float(step_ms.mean())
     ms_fwd = float(fwd_ms.mean())
-    if dist is not None:
-        t = torch.tensor([ms_step, ms_fwd], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd = float(t[0]), float(t[1])
-    n = ws
-    mpix = W * H / 1e6
-    value = n * mpix / (ms_step / 1e3)
-    fwd_value = n * mpix / (ms_fwd / 1e3)
+    ms_step, ms_fwd = max_over_ranks([ms_step, ms_fwd], dist, "cuda")
+    value = job_throughput(ws, W * H, ms_step)
+    fwd_value = job_throughput(ws, W * H, ms_fwd)
     stage_ms = {names[i]: float(st[:, i].mean()) for i in range(7)}
 
     # ---- roofline of each stage (algorithmic work per launch / measured duration)
@@ -325,12 +338,8 @@ def run_e2e(args, r, scene, grads_np, flush, ws, dist):
         b.record(stream)
         b.synchronize()
         times.append(a.elapsed_time(b))
-    ms = float(np.mean(times))
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-    val = ws * r.W * r.H / 1e6 / (ms / 1e3)
+    ms = max_over_ranks([float(np.mean(times))], dist, "cuda")[0]
+    val = job_throughput(ws, r.W * r.H, ms)
     return {"value": val, "unit": "Mpix/s", "ms_per_step": ms, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}
 
