@@ -63,6 +63,7 @@ _SIGS = {
                                         C.c_size_t, _VP]),
     "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 13),
     "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 13 + [_I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "gm_bin_triangles_noalloc": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP]),
     "gm_last_error": (C.c_char_p, []),
 }
 
@@ -155,6 +156,20 @@ def gm_bin_triangles(cam: gm_camera, V, F, tile_range, tri_ids, cap: int, counte
     if st == GM_ERR_CAPACITY:
         raise GmError(st, "gm_bin_triangles", "capacity %d < needed %d" % (cap, k.value))
     _check(st, "gm_bin_triangles")
+    return k.value if sync else None
+
+
+def gm_bin_triangles_noalloc(cam: gm_camera, V, F, tile_range, tri_ids, cap: int, counters, sync: bool = True):
+    """gm_bin_triangles for callers that may not allocate device memory: the
+    scratch is the library's static device array (GM_NOALLOC_TRI_SCRATCH_BYTES),
+    so no workspace is passed.  Overlapping calls share that array and race."""
+    k = C.c_int32(0)
+    st = lib().gm_bin_triangles_noalloc(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0],
+                                        _p(tile_range, I32), _p(tri_ids, I32), cap, _p(counters, I32),
+                                        C.byref(k) if sync else None, _stream())
+    if st == GM_ERR_CAPACITY:
+        raise GmError(st, "gm_bin_triangles_noalloc", "capacity %d < needed %d" % (cap, k.value))
+    _check(st, "gm_bin_triangles_noalloc")
     return k.value if sync else None
 
 

@@ -69,6 +69,19 @@ int finish_binning(int32_t* counters, int32_t* K_host, int32_t cap, cudaStream_t
 
 }  // namespace
 
+namespace gm {
+// Records a message for gm_last_error() and returns code (used by entry
+// points defined in other files).
+int set_last_error(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+}  // namespace gm
+
 extern "C" {
 
 const char* gm_last_error(void) { return g_err; }

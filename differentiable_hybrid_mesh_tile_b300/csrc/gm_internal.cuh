@@ -167,6 +167,7 @@ cudaError_t tile_ranges(const uint64_t* keys, int cap, const int32_t* counters, 
                         int n_tiles, cudaStream_t s);
 
 int num_sms();
+int set_last_error(int code, const char* fmt, ...);
 
 // ---------------------------------------------------------------------------
 // Host launchers of the path's steps (enqueue on stream s, no synchronisation)

@@ -232,6 +232,29 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const int32_t* F, int32_t nF, const float* vcol, float* v_verts,
                             float* v_vcol, uint64_t* stats, void* stream);
 
+/* ------------------------------------------------------------------------
+ * gm_bin_triangles_noalloc -- gm_bin_triangles for callers that may not
+ * allocate device memory at all (a plugin or engine inside a host
+ * application that owns all device memory through its own pool and budget,
+ * so a library cudaMalloc would fail against that budget or stall the
+ * device).  The paper has no counterpart: this is a packaging of the same
+ * triangle binning.  The caller still passes V, F and the outputs; the
+ * scratch memory is a static device array of GM_NOALLOC_TRI_SCRATCH_BYTES
+ * that every GPU loading libgm holds until the process exits.  Calls whose
+ * gm_bin_triangles_workspace_size(nF, cap, ...) exceeds that size are
+ * rejected with GM_ERR_INVALID_ARG (message in gm_last_error).  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * then cached per device), so make that first call before any stream
+ * capture.  All calls share the one array (each call clears what must start
+ * at zero): calls that overlap on the GPU -- concurrent streams or host
+ * threads -- race and corrupt each other's results.  Everything else as
+ * gm_bin_triangles; no cudaMalloc / cudaFree or allocating library call.
+ * ---------------------------------------------------------------------- */
+#define GM_NOALLOC_TRI_SCRATCH_BYTES (32u << 20)
+int gm_bin_triangles_noalloc(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F,
+                             int32_t nF, int32_t* tile_range, int32_t* tri_ids, int32_t cap,
+                             int32_t* counters, int32_t* K_host, void* stream);
+
 /* Message describing the calling thread's last failure ("" if none). */
 const char* gm_last_error(void);
 
