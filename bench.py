@@ -160,8 +160,8 @@ def run_gm(args, ws, rank, local):
     g_dev = [torch.as_tensor(x).cuda() for x in grads_np]
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    stats_f = torch.zeros(1, dtype=torch.int64, device="cuda")
-    stats_b = torch.zeros(1, dtype=torch.int64, device="cuda")
+    stats_f = torch.zeros(2, dtype=torch.int64, device="cuda")
+    stats_b = torch.zeros(2, dtype=torch.int64, device="cuda")
 
     cam_c, opts = r.cam, r.opts
     names = ["tri_bin", "zbuffer", "interp", "project", "bin_sort", "composite_fwd", "composite_bwd"]
@@ -204,7 +204,8 @@ def run_gm(args, ws, rank, local):
     stats_b.zero_()
     step(count=True)
     torch.cuda.synchronize()
-    pairs_f, pairs_b = int(stats_f.item()), int(stats_b.item())
+    pairs_f, blend_f = (int(x) for x in stats_f.tolist())
+    pairs_b, blend_b = (int(x) for x in stats_b.tolist())
     K_tri = int(r.tri_counters[0].item())
     K_g = int(r.g_counters[0].item())
     K_pre = int(r.g_counters[1].item())
@@ -263,9 +264,10 @@ def run_gm(args, ws, rank, local):
         "tri_bin": ("hbm", F * (12 + 36) * 2 + F * 12 + K_tri * 12 + K_tri * 8 + passes_t * K_tri * 24
                     + K_tri * 8 + T * 8),
         "interp": ("hbm", W * H * (4 + 4 + 12) + T * 5),
-        # FP32 lane operations: 20 per evaluated (pixel, Gaussian) pair forward, 60 backward
-        "composite_fwd": ("alu", 20 * pairs_f),
-        "composite_bwd": ("alu", 60 * pairs_b),
+        # FP32 lane operations: 18 per evaluated (pixel, Gaussian) pair forward (alpha and
+        # the tests), 60 per composited pair backward (the gradient terms)
+        "composite_fwd": ("alu", 18 * pairs_f),
+        "composite_bwd": ("alu", 60 * blend_b),
     }
     stages = {}
     for k, (bound, amount) in work.items():
@@ -294,7 +296,7 @@ def run_gm(args, ws, rank, local):
 
     return dict(value=value, fwd=fwd_value, ms_step=ms_step, ms_fwd=ms_fwd, stages=stages, roofline=roof,
                 clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_tri=K_tri, K_g=K_g, K_pre=K_pre,
-                pairs_f=pairs_f, pairs_b=pairs_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
+                pairs_f=pairs_f, pairs_b=pairs_b, blend_f=blend_f, blend_b=blend_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
                 gpu_name=props.name)
 
 
@@ -435,7 +437,8 @@ def main():
             "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["launches"] * args.steps, "clocks": res["clocks"],
             "counts": {"K_triangle_tile": res["K_tri"], "K_gauss_tile": res["K_g"], "K_gauss_tile_precull":
-                       res["K_pre"], "pairs_fwd": res["pairs_f"], "pairs_bwd": res["pairs_b"]},
+                       res["K_pre"], "pairs_evaluated_fwd": res["pairs_f"], "pairs_composited_fwd": res["blend_f"],
+                       "pairs_evaluated_bwd": res["pairs_b"], "pairs_composited_bwd": res["blend_b"]},
             "overflow": res["overflow"], "gpu": res["gpu_name"], "wall_s_timed": res["wall"],
         }
         print(json.dumps(line))

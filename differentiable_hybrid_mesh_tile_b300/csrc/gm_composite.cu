@@ -2,8 +2,12 @@
 // Mesh and 3D Gaussian Splat Scenes", Hybrid rendering) with a hard depth
 // test: every Gaussian is tested against the mesh depth at the pixel, and the
 // opaque mesh is the terminal layer.  Forward and backward, one CTA per
-// 16 x 16 tile, one thread per pixel; the tile's sorted records are staged in
-// shared memory in batches of 256.
+// 16 x 16 tile, one thread per pixel, each warp an 8 x 4 pixel block; the
+// tile's sorted records are staged in shared memory in batches of 256.
+//
+// Each warp first asks, per staged record, whether the Gaussian's ellipse of
+// alpha >= 1/255 meets its 8 x 4 pixel block, and then visits only those
+// records (the other pairs would be skipped anyway).
 #include "gm_internal.cuh"
 
 namespace gm {
@@ -12,13 +16,74 @@ namespace {
 constexpr float ALPHA_MAX = 0.99f;
 constexpr float ALPHA_MIN = 1.0f / 255.0f;
 constexpr float T_STOP = 1e-4f;
+constexpr float LOG2E = 1.4426950408889634f;
 
-// sigma, exp(-sigma) and alpha of one splat at pixel centre (px, py).  Both
-// passes call this one routine with explicit roundings so that they take the
-// same skip / clamp decisions bit for bit.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Staged record.  The conic is stored pre-multiplied so that
+// exp(-sigma) = 2^l, l = a2 dx^2 + b2 dx dy + c2 dy^2, a2 = -a log2e / 2,
+// b2 = -b log2e, c2 = -c log2e / 2 (a2, c2 < 0 for a positive definite conic):
+//   A = (mx, my, a2, b2), B = (c2, opacity, r, g), C = (b, depth, -, -),
+//   H = (lmin, ka, kc, -): alpha >= 1/255 needs l >= lmin = -log2(255 o);
+//   ka = -1 / (2 a2), kc = -1 / (2 c2) locate the maximum of l along a line.
+__device__ __forceinline__ void stage(const float4* __restrict__ splats, int64_t g, float4& A, float4& B, float4& C,
+                                      float4& H)
+{
+    const float4 s0 = splats[3 * g], s1 = splats[3 * g + 1], s2 = splats[3 * g + 2];
+    // s0 = (mx, my, a, b), s1 = (c, o, r, g), s2 = (b, depth, 0, 0)
+    A = make_float4(s0.x, s0.y, -0.5f * LOG2E * s0.z, -LOG2E * s0.w);
+    B = make_float4(-0.5f * LOG2E * s1.x, s1.y, s1.z, s1.w);
+    C = make_float4(s2.x, s2.y, 0.0f, 0.0f);
+    const float o255 = 255.0f * s1.y;
+    const float det = s0.z * s1.x - s0.w * s0.w;
+    if (!(det > 0.0f) || !(s0.z > 0.0f)) {
+        H = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);  // degenerate conic: every pixel is evaluated
+    } else if (!(o255 >= 1.0f)) {
+        H = make_float4(INFINITY, 0.0f, 0.0f, 0.0f);   // exp(-sigma) <= 1: never reaches 1/255
+    } else {
+        // lowered by 0.1 % + 1e-4 so that rounding in the block test never drops a
+        // pixel the exact evaluation keeps
+        const float lmin = -log2f(o255) * 1.001f - 1e-4f;
+        H = make_float4(lmin, -0.5f / A.z, -0.5f / B.x, 0.0f);
+    }
+}
+
+// Whether the Gaussian can reach alpha >= 1/255 at any pixel centre of the
+// warp's 8 x 4 block (centres x0 .. x0 + 7, y0 .. y0 + 3): the maximum of the
+// concave l over that rectangle is 0 when it holds the mean, else it lies on
+// an edge, where l is a 1D parabola maximised at a clamped vertex.
+__device__ __forceinline__ bool block_hits(const float4& A, const float4& B, const float4& H, float x0, float y0)
+{
+    if (!(H.x <= 0.0f)) return false;       // invisible
+    if (H.x == -INFINITY) return true;       // degenerate: evaluate
+    const float u0 = x0 - A.x, u1 = u0 + 7.0f, v0 = y0 - A.y, v1 = v0 + 3.0f;
+    if (u0 <= 0.0f && u1 >= 0.0f && v0 <= 0.0f && v1 >= 0.0f) return true;
+    const float a2 = A.z, b2 = A.w, c2 = B.x;
+    float best = -INFINITY;
+    {   // edges u = u0, u1: v* = b2 u kc
+        const float va = fminf(fmaxf(b2 * u0 * H.z, v0), v1), vb = fminf(fmaxf(b2 * u1 * H.z, v0), v1);
+        best = fmaxf(best, fmaf(fmaf(a2, u0, b2 * va), u0, c2 * va * va));
+        best = fmaxf(best, fmaf(fmaf(a2, u1, b2 * vb), u1, c2 * vb * vb));
+    }
+    {   // edges v = v0, v1: u* = b2 v ka
+        const float ua = fminf(fmaxf(b2 * v0 * H.y, u0), u1), ub = fminf(fmaxf(b2 * v1 * H.y, u0), u1);
+        best = fmaxf(best, fmaf(fmaf(c2, v0, b2 * ua), v0, a2 * ua * ua));
+        best = fmaxf(best, fmaf(fmaf(c2, v1, b2 * ub), v1, a2 * ub * ub));
+    }
+    return best >= H.x;
+}
+
+// alpha of one staged record at pixel centre (px, py).  Both passes call this
+// one routine with explicit roundings, so they take the same skip / clamp
+// decisions bit for bit.
 struct Eval {
-    float dx, dy, sigma, G, alpha;
-    bool clamped;
+    float dx, dy, G, alpha;
+    bool skip, clamped;
 };
 
 __device__ __forceinline__ Eval eval_splat(const float4& A, const float4& B, float px, float py)
@@ -26,22 +91,48 @@ __device__ __forceinline__ Eval eval_splat(const float4& A, const float4& B, flo
     Eval e;
     e.dx = __fsub_rn(px, A.x);
     e.dy = __fsub_rn(py, A.y);
-    const float q = __fmaf_rn(A.z, __fmul_rn(e.dx, e.dx), __fmul_rn(B.x, __fmul_rn(e.dy, e.dy)));
-    e.sigma = __fmaf_rn(0.5f, q, __fmul_rn(A.w, __fmul_rn(e.dx, e.dy)));
-    e.G = __expf(-e.sigma);
+    const float q = __fmaf_rn(B.x, __fmul_rn(e.dy, e.dy), __fmul_rn(A.w, __fmul_rn(e.dx, e.dy)));
+    const float l = __fmaf_rn(A.z, __fmul_rn(e.dx, e.dx), q);  // = -sigma log2(e)
+    e.G = ex2(l);
     const float oG = __fmul_rn(B.y, e.G);
     e.clamped = oG > ALPHA_MAX;
     e.alpha = e.clamped ? ALPHA_MAX : oG;
+    e.skip = l > 0.0f || e.alpha < ALPHA_MIN;  // sigma < 0, or alpha below 1/255
     return e;
 }
 
-// adds a per-thread count over the block to *stats (one atomic per block)
+// adds a per-thread count over the block to *stats (one atomic per warp)
 __device__ __forceinline__ void block_count(uint32_t v, unsigned long long* stats)
 {
     unsigned long long x = v;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     if ((threadIdx.x & 31) == 0 && x) atomicAdd(stats, x);
+}
+
+struct PixelMap {
+    int i, j;      // this thread's pixel
+    float x0, y0;  // centre of the warp block's first pixel
+};
+
+// warp w of the tile covers the 8 x 4 block at (8 (w % 2), 4 (w / 2))
+__device__ __forceinline__ PixelMap pixel_of(const Cam& c, int tile)
+{
+    const int tx = tile % c.TW, ty = tile / c.TW;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * TILE + (warp & 1) * 8, by = ty * TILE + (warp >> 1) * 4;
+    PixelMap m;
+    m.i = bx + (lane & 7);
+    m.j = by + (lane >> 3);
+    m.x0 = (float)bx + 0.5f;
+    m.y0 = (float)by + 0.5f;
+    return m;
+}
+
+__device__ __forceinline__ void stage_empty(float4& C, float4& H)
+{
+    H = make_float4(INFINITY, 0.0f, 0.0f, 0.0f);
+    C = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(TILE_PIX)
@@ -51,14 +142,12 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 float* __restrict__ out_depth, float* __restrict__ out_alpha, float* __restrict__ T_final,
                 int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ stats)
 {
-    __shared__ float4 sA[TILE_PIX], sB[TILE_PIX], sC[TILE_PIX];
+    __shared__ float4 sA[TILE_PIX], sB[TILE_PIX], sC[TILE_PIX], sH[TILE_PIX];
     const int tile = blockIdx.x;
-    const int tx = tile % c.TW, ty = tile / c.TW;
-    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
-    const int j = ty * TILE + (threadIdx.x >> 4);
-    const bool inside = i < c.W && j < c.H;
-    const int64_t pix = (int64_t)j * c.W + i;
-    const float px = (float)i + 0.5f, py = (float)j + 0.5f;
+    const PixelMap pm = pixel_of(c, tile);
+    const bool inside = pm.i < c.W && pm.j < c.H;
+    const int64_t pix = (int64_t)pm.j * c.W + pm.i;
+    const float px = (float)pm.i + 0.5f, py = (float)pm.j + 0.5f;
     float D = -INFINITY;
     bool cov = false;
     if (inside) {
@@ -67,7 +156,7 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     }
     float T = 1.0f, Cr = 0.0f, Cg = 0.0f, Cb = 0.0f, Z = 0.0f;
     int last = 0;
-    uint32_t visited = 0;
+    uint32_t visited = 0, blended = 0;
     bool done = !inside;
     const int2 r = tile_range[tile];
     for (int b = r.x; b < r.y; b += TILE_PIX) {
@@ -75,33 +164,37 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         const int n = min(TILE_PIX, r.y - b);
         if ((int)threadIdx.x < n) {
             const int64_t g = gids[b + threadIdx.x];
-            if (g >= 0 && g < N) {
-                sA[threadIdx.x] = splats[3 * g];
-                sB[threadIdx.x] = splats[3 * g + 1];
-                sC[threadIdx.x] = splats[3 * g + 2];
-            } else {  // an id outside [0, N): an entry that draws nothing
-                sA[threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
-                sB[threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
-                sC[threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            if (g >= 0 && g < N)
+                stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
+            else  // an id outside [0, N): an entry that draws nothing
+                stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
         }
         __syncthreads();
-        if (!done) {
-            int k = 0;
-            for (; k < n; ++k) {
+        // walk this warp's hits: a ballot per 32 staged records marks those that can
+        // reach its pixels; the warp visits only those, in list order
+        for (int m = 0; m * 32 < n; ++m) {
+            if (__all_sync(0xffffffffu, done)) break;
+            const int kk = m * 32 + (threadIdx.x & 31);
+            uint32_t mask =
+                __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0));
+            while (mask) {
+                const int k = m * 32 + __ffs(mask) - 1;
+                mask &= mask - 1;
+                if (done) continue;
                 const float4 C3 = sC[k];
                 // sorted by depth: once a Gaussian is not in front of the mesh, none after it is
                 if (!(C3.y < D)) {
                     done = true;
-                    break;
+                    continue;
                 }
+                ++visited;
                 const float4 A = sA[k], B = sB[k];
                 const Eval e = eval_splat(A, B, px, py);
-                if (e.sigma < 0.0f || e.alpha < ALPHA_MIN) continue;
+                if (e.skip) continue;
                 const float Tn = __fmul_rn(T, __fsub_rn(1.0f, e.alpha));
                 if (Tn <= T_STOP) {
                     done = true;
-                    break;
+                    continue;
                 }
                 const float w = e.alpha * T;
                 Cr = fmaf(w, B.z, Cr);
@@ -110,12 +203,15 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 Z = fmaf(w, C3.y, Z);
                 T = Tn;
                 last = b - r.x + k + 1;
+                ++blended;
             }
-            visited += (uint32_t)min(k + 1, n);
         }
         __syncthreads();
     }
-    if (stats) block_count(visited, stats);
+    if (stats) {
+        block_count(visited, stats);
+        block_count(blended, stats + 1);
+    }
     if (inside) {
         float tr, tg, tb;
         if (cov) {
@@ -133,16 +229,28 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     }
 }
 
-__device__ __forceinline__ float warp_sum(float v)
+constexpr int NGRAD = 10;
+constexpr int GROUP = 4;
+
+// Sums v[0..3] (one value per entry of a group of four) over the warp and
+// leaves in every lane the total of entry 2 bit4(lane) + bit3(lane): two
+// halving exchanges (xor 16, xor 8), then a butterfly over xor 4, 2, 1 --
+// six shuffles for four entries instead of five per entry.
+__device__ __forceinline__ float reduce_scatter4(const float v[GROUP], int lane)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    const bool hi16 = lane & 16, hi8 = lane & 8;
+    const float keep0 = hi16 ? v[2] : v[0], keep1 = hi16 ? v[3] : v[1];
+    const float send0 = hi16 ? v[0] : v[2], send1 = hi16 ? v[1] : v[3];
+    const float b0 = keep0 + __shfl_xor_sync(0xffffffffu, send0, 16);
+    const float b1 = keep1 + __shfl_xor_sync(0xffffffffu, send1, 16);
+    float x = (hi8 ? b1 : b0) + __shfl_xor_sync(0xffffffffu, hi8 ? b0 : b1, 8);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
 }
 
-constexpr int NGRAD = 10;
-
-__global__ void __launch_bounds__(TILE_PIX)
+__global__ void __launch_bounds__(TILE_PIX, 4)
 k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
                 const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
@@ -150,18 +258,16 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 const float* __restrict__ g_rgb, const float* __restrict__ g_depth, const float* __restrict__ g_alpha,
                 float* __restrict__ v_splats, unsigned long long* __restrict__ stats)
 {
-    __shared__ float4 sA[TILE_PIX], sB[TILE_PIX], sC[TILE_PIX];
+    __shared__ float4 sA[TILE_PIX], sB[TILE_PIX], sC[TILE_PIX], sH[TILE_PIX];
     __shared__ int sG[TILE_PIX];
     __shared__ float sAcc[TILE_PIX][NGRAD + 1];
     __shared__ int s_max_last;
     const int tile = blockIdx.x;
-    const int tx = tile % c.TW, ty = tile / c.TW;
-    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
-    const int j = ty * TILE + (threadIdx.x >> 4);
+    const PixelMap pm = pixel_of(c, tile);
     const int lane = threadIdx.x & 31;
-    const bool inside = i < c.W && j < c.H;
-    const int64_t pix = (int64_t)j * c.W + i;
-    const float px = (float)i + 0.5f, py = (float)j + 0.5f;
+    const bool inside = pm.i < c.W && pm.j < c.H;
+    const int64_t pix = (int64_t)pm.j * c.W + pm.i;
+    const float px = (float)pm.i + 0.5f, py = (float)pm.j + 0.5f;
 
     float D = -INFINITY, T = 1.0f, gr = 0.f, gg = 0.f, gb = 0.f, gz = 0.f, ga = 0.f;
     int last = 0;
@@ -174,7 +280,7 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         gr = g_rgb[3 * pix]; gg = g_rgb[3 * pix + 1]; gb = g_rgb[3 * pix + 2];
         gz = g_depth[pix];
         ga = g_alpha[pix];
-        // the terminal layer, everything behind the last composited Gaussian
+        // the terminal layer: everything behind the last composited Gaussian
         if (cov) {
             BCr = T * mesh_rgb[3 * pix]; BCg = T * mesh_rgb[3 * pix + 1]; BCb = T * mesh_rgb[3 * pix + 2];
             BZ = T * D;
@@ -183,13 +289,17 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
             aterm = ga * T;  // out_alpha = 1 - T_final when uncovered
         }
     }
+    int warp_last = last;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) warp_last = max(warp_last, __shfl_xor_sync(0xffffffffu, warp_last, o));
     if (threadIdx.x == 0) s_max_last = 0;
     __syncthreads();
-    if (last > 0) atomicMax(&s_max_last, last);
+    if (lane == 0 && warp_last > 0) atomicMax(&s_max_last, warp_last);
     __syncthreads();
     const int2 r = tile_range[tile];
     const int end = r.x + s_max_last;
-    if (stats) block_count(inside ? (uint32_t)last : 0u, stats);
+    uint32_t visited = 0, contributed = 0;
+    const int my_entry = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
     for (int b_end = end; b_end > r.x; b_end -= TILE_PIX) {
         const int b0 = max(r.x, b_end - TILE_PIX);
         const int n = b_end - b0;
@@ -197,57 +307,100 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
             int g = gids[b0 + threadIdx.x];
             if (g < 0 || g >= N) g = -1;  // an entry that draws nothing and gets no gradient
             sG[threadIdx.x] = g;
-            const int64_t gg = g < 0 ? 0 : g;
-            sA[threadIdx.x] = g < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : splats[3 * gg];
-            sB[threadIdx.x] = g < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : splats[3 * gg + 1];
-            sC[threadIdx.x] = g < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : splats[3 * gg + 2];
+            if (g >= 0)
+                stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
+            else
+                stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
 #pragma unroll
             for (int q = 0; q < NGRAD; ++q) sAcc[threadIdx.x][q] = 0.0f;
         }
         __syncthreads();
-        for (int k = n - 1; k >= 0; --k) {
-            const int pos = b0 - r.x + k;
-            bool on = inside && pos < last;
-            float v[NGRAD];
+        // this warp only needs the entries in front of its last composited one, and of
+        // those only the ones that can reach its pixels (a ballot per 32 entries);
+        // they are taken four at a time from the back
+        const int k_top = min(n, warp_last - (b0 - r.x)) - 1;
+        for (int m = k_top >> 5; m >= 0; --m) {
+            const int kk = m * 32 + lane;
+            uint32_t mask =
+                __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0));
+            while (mask) {
+                int kj[GROUP];
 #pragma unroll
-            for (int q = 0; q < NGRAD; ++q) v[q] = 0.0f;
-            if (on) {
-                const float4 A = sA[k], B = sB[k], C3 = sC[k];
-                const Eval e = eval_splat(A, B, px, py);
-                on = C3.y < D && !(e.sigma < 0.0f) && !(e.alpha < ALPHA_MIN);
-                if (on) {
-                    const float om = 1.0f - e.alpha;
-                    const float Tp = T / om;  // transmittance in front of this Gaussian
+                for (int jj = 0; jj < GROUP; ++jj) {
+                    if (mask) {
+                        const int bit = 31 - __clz(mask);
+                        kj[jj] = m * 32 + bit;
+                        mask &= ~(1u << bit);
+                    } else {
+                        kj[jj] = -1;
+                    }
+                }
+                // per entry: w = alpha T_front, vo = dL/d opacity, ds = dL/d sigma, dx, dy
+                float pw[GROUP], pvo[GROUP], pds[GROUP], pdx[GROUP], pdy[GROUP];
+                bool any = false;
+#pragma unroll
+                for (int jj = 0; jj < GROUP; ++jj) {
+                    pw[jj] = pvo[jj] = pds[jj] = pdx[jj] = pdy[jj] = 0.0f;
+                    const int k = kj[jj];
+                    if (k < 0 || !inside || b0 - r.x + k >= last) continue;
+                    const float4 C3 = sC[k];
+                    if (!(C3.y < D)) continue;
+                    ++visited;
+                    const float4 A = sA[k], B = sB[k];
+                    const Eval e = eval_splat(A, B, px, py);
+                    if (e.skip) continue;
+                    ++contributed;
+                    any = true;
+                    const float rom = __frcp_rn(1.0f - e.alpha);
+                    const float Tp = T * rom;  // transmittance in front of this Gaussian
                     const float w = e.alpha * Tp;
-                    v[6] = w * gr;
-                    v[7] = w * gg;
-                    v[8] = w * gb;
-                    v[9] = w * gz;
                     const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
                     const float behind = BCr * gr + BCg * gg + BCb * gb + BZ * gz;
-                    const float dLda = Tp * front + (aterm - behind) / om;
+                    const float dLda = Tp * front + (aterm - behind) * rom;
                     BCr = fmaf(w, B.z, BCr);
                     BCg = fmaf(w, B.w, BCg);
                     BCb = fmaf(w, C3.x, BCb);
                     BZ = fmaf(w, C3.y, BZ);
                     T = Tp;
-                    if (!e.clamped) {
-                        v[5] = dLda * e.G;
-                        const float dLds = -dLda * e.alpha;
-                        v[2] = dLds * 0.5f * e.dx * e.dx;
-                        v[3] = dLds * e.dx * e.dy;
-                        v[4] = dLds * 0.5f * e.dy * e.dy;
-                        v[0] = -dLds * (A.z * e.dx + A.w * e.dy);
-                        v[1] = -dLds * (A.w * e.dx + B.x * e.dy);
+                    pw[jj] = w;
+                    if (!e.clamped) {  // alpha clamped at 0.99 has no opacity / sigma gradient
+                        pvo[jj] = dLda * e.G;
+                        pds[jj] = -dLda * e.alpha;  // d alpha / d sigma = -alpha
                     }
+                    pdx[jj] = e.dx;
+                    pdy[jj] = e.dy;
                 }
-            }
-            if (__any_sync(0xffffffffu, on)) {
+                if (__any_sync(0xffffffffu, any)) {
+                    const int k = my_entry == 0 ? kj[0] : my_entry == 1 ? kj[1] : my_entry == 2 ? kj[2] : kj[3];
+                    const int sub = lane & 7;
 #pragma unroll
-                for (int q = 0; q < NGRAD; ++q) v[q] = warp_sum(v[q]);
-                if (lane == 0) {
+                    for (int q = 0; q < NGRAD; ++q) {
+                        float col[GROUP];
 #pragma unroll
-                    for (int q = 0; q < NGRAD; ++q) atomicAdd(&sAcc[k][q], v[q]);
+                        for (int jj = 0; jj < GROUP; ++jj) {
+                            const float ds = pds[jj], dx = pdx[jj], dy = pdy[jj];
+                            if (q == 0 || q == 1) {
+                                // d sigma / d mean = -(a dx + b dy, b dx + c dy),
+                                // a = -2 a2 / log2e, b = -b2 / log2e, c = -2 c2 / log2e
+                                const int kq = kj[jj] < 0 ? 0 : kj[jj];
+                                const float a2 = sA[kq].z, b2 = sA[kq].w, c2 = sB[kq].x;
+                                const float sl = ds * (1.0f / LOG2E);
+                                col[jj] = q == 0 ? sl * (2.0f * a2 * dx + b2 * dy) : sl * (b2 * dx + 2.0f * c2 * dy);
+                            } else if (q == 2) {
+                                col[jj] = 0.5f * ds * dx * dx;
+                            } else if (q == 3) {
+                                col[jj] = ds * dx * dy;
+                            } else if (q == 4) {
+                                col[jj] = 0.5f * ds * dy * dy;
+                            } else if (q == 5) {
+                                col[jj] = pvo[jj];
+                            } else {
+                                col[jj] = pw[jj] * (q == 6 ? gr : q == 7 ? gg : q == 8 ? gb : gz);
+                            }
+                        }
+                        const float sum = reduce_scatter4(col, lane);
+                        if (sub == (q & 7) && (q < 8 || sub < 2) && k >= 0 && sum != 0.0f) atomicAdd(&sAcc[k][q], sum);
+                    }
                 }
             }
         }
@@ -261,6 +414,10 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
             }
         }
         __syncthreads();
+    }
+    if (stats) {
+        block_count(visited, stats);
+        block_count(contributed, stats + 1);
     }
 }
 

@@ -200,8 +200,9 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
  *   treated as an entry that draws nothing).
  *   Saved for the backward pass: T_final [H][W] f32 and n_contrib [H][W]
  *   i32 (1 + position in the tile's list of the last composited Gaussian).
- *   stats: NULL, or a device uint64 that is incremented by the number of
- *   (pixel, Gaussian) pairs evaluated (a profiling count; the caller zeroes it).
+ *   stats: NULL, or a device uint64[2] incremented by the number of
+ *   (pixel, Gaussian) pairs evaluated [0] and composited [1] (profiling
+ *   counts; the caller zeroes them).
  * ---------------------------------------------------------------------- */
 int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
                             const int32_t* tile_range, const int32_t* gids, const float* splats, const float* mesh_depth,
@@ -221,8 +222,8 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  *   colour through the interpolated mesh depth and colour of covered pixels
  *   (face ids held fixed).  V / F / vcol / v_verts / v_vcol may all be NULL
  *   (with nV = nF = 0) to skip the mesh gradients.
- *   stats: NULL, or a device uint64 incremented by the number of (pixel,
- *   Gaussian) pairs whose gradient terms were evaluated (profiling count).
+ *   stats: NULL, or a device uint64[2] incremented by the number of (pixel,
+ *   Gaussian) pairs evaluated [0] and given gradient terms [1] (profiling).
  * ---------------------------------------------------------------------- */
 int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
                             const int32_t* tile_range, const int32_t* gids, const float* splats, const float* mesh_depth,

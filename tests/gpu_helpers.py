@@ -153,7 +153,10 @@ def lists_from_bins(cam, keys, gids):
     return np.cumsum(start), np.asarray(gids, np.int32)
 
 
-def tie_pixels(margins, alpha_band=2e-6, stop_band=1e-4, sigma_band=1e-5, clamp_band=None):
+# The kernels evaluate exp(-sigma) as 2^l with l from a conic pre-scaled by
+# -log2(e)/2: the rounding of l (a few ulp of |l| <= 8 near alpha = 1/255) and
+# ex2's own 2 ulp keep alpha within 8e-6 relative of the oracle's.
+def tie_pixels(margins, alpha_band=8e-6, stop_band=1e-4, sigma_band=1e-5, clamp_band=None):
     m = margins
     t = (m[..., 1] < alpha_band) | (m[..., 3] < stop_band) | (m[..., 4] < sigma_band)
     if clamp_band is not None:
