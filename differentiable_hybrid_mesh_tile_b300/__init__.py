@@ -376,6 +376,26 @@ class HybridRenderer:
             return self.v_splats, self.v_verts, self.v_vcol
         return self.v_splats, None, None
 
+    def capture_step(self, g_rgb, g_depth, g_alpha, mesh_grads: bool = True):
+        """Records one forward + backward pass (the seven calls, no host
+        synchronisation) into a CUDA graph and returns it; ``graph.replay()``
+        then re-runs the step on the current inputs.  Call after a sizing
+        ``forward(sync=True)`` so the capacities fit, and check
+        ``overflowed()`` after replays."""
+        if not hasattr(self, "v_verts"):
+            self.backward(g_rgb, g_depth, g_alpha, mesh_grads)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # warm the capture stream once
+            self.forward(sync=False)
+            self.backward(g_rgb, g_depth, g_alpha, mesh_grads)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.forward(sync=False)
+            self.backward(g_rgb, g_depth, g_alpha, mesh_grads)
+        return graph
+
     def overflowed(self) -> bool:
         f = int(self.tri_counters[GM_CNT_FLAGS].item()) | int(self.g_counters[GM_CNT_FLAGS].item())
         return bool(f & (GM_FLAG_OVERFLOW | GM_FLAG_TIMEOUT))

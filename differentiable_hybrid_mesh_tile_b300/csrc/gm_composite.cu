@@ -135,6 +135,7 @@ __device__ __forceinline__ void stage_empty(float4& C, float4& H)
     C = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+template <bool STATS>
 __global__ void __launch_bounds__(TILE_PIX)
 k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
                 const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
@@ -187,7 +188,7 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                     done = true;
                     continue;
                 }
-                ++visited;
+                if (STATS) ++visited;
                 const float4 A = sA[k], B = sB[k];
                 const Eval e = eval_splat(A, B, px, py);
                 if (e.skip) continue;
@@ -203,12 +204,12 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 Z = fmaf(w, C3.y, Z);
                 T = Tn;
                 last = b - r.x + k + 1;
-                ++blended;
+                if (STATS) ++blended;
             }
         }
         __syncthreads();
     }
-    if (stats) {
+    if (STATS) {
         block_count(visited, stats);
         block_count(blended, stats + 1);
     }
@@ -250,6 +251,7 @@ __device__ __forceinline__ float reduce_scatter4(const float v[GROUP], int lane)
     return x;
 }
 
+template <bool STATS>
 __global__ void __launch_bounds__(TILE_PIX, 4)
 k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
                 const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
@@ -269,9 +271,11 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     const int64_t pix = (int64_t)pm.j * c.W + pm.i;
     const float px = (float)pm.i + 0.5f, py = (float)pm.j + 0.5f;
 
-    float D = -INFINITY, T = 1.0f, gr = 0.f, gg = 0.f, gb = 0.f, gz = 0.f, ga = 0.f;
+    float D = -INFINITY, T = 1.0f, gr = 0.f, gg = 0.f, gb = 0.f, gz = 0.f;
     int last = 0;
-    float BCr = 0.f, BCg = 0.f, BCb = 0.f, BZ = 0.f, aterm = 0.f;
+    // behind = (colour, depth) accumulated behind the current Gaussian, dotted with
+    // this pixel's upstream gradient (g_rgb, g_depth); starts with the terminal layer
+    float behind = 0.f, aterm = 0.f;
     if (inside) {
         D = mesh_depth[pix];
         const bool cov = face_id[pix] >= 0;
@@ -279,14 +283,11 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         last = n_contrib[pix];
         gr = g_rgb[3 * pix]; gg = g_rgb[3 * pix + 1]; gb = g_rgb[3 * pix + 2];
         gz = g_depth[pix];
-        ga = g_alpha[pix];
-        // the terminal layer: everything behind the last composited Gaussian
         if (cov) {
-            BCr = T * mesh_rgb[3 * pix]; BCg = T * mesh_rgb[3 * pix + 1]; BCb = T * mesh_rgb[3 * pix + 2];
-            BZ = T * D;
+            behind = T * (mesh_rgb[3 * pix] * gr + mesh_rgb[3 * pix + 1] * gg + mesh_rgb[3 * pix + 2] * gb + D * gz);
         } else {
-            BCr = T * bg.x; BCg = T * bg.y; BCb = T * bg.z;
-            aterm = ga * T;  // out_alpha = 1 - T_final when uncovered
+            behind = T * (bg.x * gr + bg.y * gg + bg.z * gb);
+            aterm = g_alpha[pix] * T;  // out_alpha = 1 - T_final when uncovered
         }
     }
     int warp_last = last;
@@ -345,22 +346,18 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                     if (k < 0 || !inside || b0 - r.x + k >= last) continue;
                     const float4 C3 = sC[k];
                     if (!(C3.y < D)) continue;
-                    ++visited;
+                    if (STATS) ++visited;
                     const float4 A = sA[k], B = sB[k];
                     const Eval e = eval_splat(A, B, px, py);
                     if (e.skip) continue;
-                    ++contributed;
+                    if (STATS) ++contributed;
                     any = true;
-                    const float rom = __frcp_rn(1.0f - e.alpha);
+                    const float rom = __fdividef(1.0f, 1.0f - e.alpha);
                     const float Tp = T * rom;  // transmittance in front of this Gaussian
                     const float w = e.alpha * Tp;
                     const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
-                    const float behind = BCr * gr + BCg * gg + BCb * gb + BZ * gz;
                     const float dLda = Tp * front + (aterm - behind) * rom;
-                    BCr = fmaf(w, B.z, BCr);
-                    BCg = fmaf(w, B.w, BCg);
-                    BCb = fmaf(w, C3.x, BCb);
-                    BZ = fmaf(w, C3.y, BZ);
+                    behind = fmaf(w, front, behind);
                     T = Tp;
                     pw[jj] = w;
                     if (!e.clamped) {  // alpha clamped at 0.99 has no opacity / sigma gradient
@@ -373,33 +370,40 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 if (__any_sync(0xffffffffu, any)) {
                     const int k = my_entry == 0 ? kj[0] : my_entry == 1 ? kj[1] : my_entry == 2 ? kj[2] : kj[3];
                     const int sub = lane & 7;
+                    // reduced per entry: Sx = sum ds dx, Sy = sum ds dy, the three conic
+                    // terms, opacity, rgb and depth; the mean gradient follows from Sx, Sy:
+                    // d sigma / d mean = -(a dx + b dy, b dx + c dy) with a = -2 a2 / log2e,
+                    // b = -b2 / log2e, c = -2 c2 / log2e
+                    float sx = 0.0f, sy = 0.0f;
 #pragma unroll
                     for (int q = 0; q < NGRAD; ++q) {
                         float col[GROUP];
 #pragma unroll
                         for (int jj = 0; jj < GROUP; ++jj) {
                             const float ds = pds[jj], dx = pdx[jj], dy = pdy[jj];
-                            if (q == 0 || q == 1) {
-                                // d sigma / d mean = -(a dx + b dy, b dx + c dy),
-                                // a = -2 a2 / log2e, b = -b2 / log2e, c = -2 c2 / log2e
-                                const int kq = kj[jj] < 0 ? 0 : kj[jj];
-                                const float a2 = sA[kq].z, b2 = sA[kq].w, c2 = sB[kq].x;
-                                const float sl = ds * (1.0f / LOG2E);
-                                col[jj] = q == 0 ? sl * (2.0f * a2 * dx + b2 * dy) : sl * (b2 * dx + 2.0f * c2 * dy);
-                            } else if (q == 2) {
-                                col[jj] = 0.5f * ds * dx * dx;
-                            } else if (q == 3) {
-                                col[jj] = ds * dx * dy;
-                            } else if (q == 4) {
-                                col[jj] = 0.5f * ds * dy * dy;
-                            } else if (q == 5) {
-                                col[jj] = pvo[jj];
-                            } else {
-                                col[jj] = pw[jj] * (q == 6 ? gr : q == 7 ? gg : q == 8 ? gb : gz);
-                            }
+                            col[jj] = q == 0 ? ds * dx
+                                    : q == 1 ? ds * dy
+                                    : q == 2 ? 0.5f * ds * dx * dx
+                                    : q == 3 ? ds * dx * dy
+                                    : q == 4 ? 0.5f * ds * dy * dy
+                                    : q == 5 ? pvo[jj]
+                                    : pw[jj] * (q == 6 ? gr : q == 7 ? gg : q == 8 ? gb : gz);
                         }
                         const float sum = reduce_scatter4(col, lane);
-                        if (sub == (q & 7) && (q < 8 || sub < 2) && k >= 0 && sum != 0.0f) atomicAdd(&sAcc[k][q], sum);
+                        if (q == 0) {
+                            sx = sum;
+                        } else if (q == 1) {
+                            sy = sum;
+                        } else if (k >= 0 && sub == (q & 7) && (q < 8 || sub < 2) && sum != 0.0f) {
+                            // lane sub of the entry's eight lanes adds component sub (and sub + 8)
+                            atomicAdd(&sAcc[k][q], sum);
+                        }
+                    }
+                    if (k >= 0 && sub < 2) {
+                        const float a2 = sA[k].z, b2 = sA[k].w, c2 = sB[k].x;
+                        const float tx = sx * (1.0f / LOG2E), ty = sy * (1.0f / LOG2E);
+                        const float m = sub == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
+                        if (m != 0.0f) atomicAdd(&sAcc[k][sub], m);
                     }
                 }
             }
@@ -415,7 +419,7 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         }
         __syncthreads();
     }
-    if (stats) {
+    if (STATS) {
         block_count(visited, stats);
         block_count(contributed, stats + 1);
     }
@@ -428,7 +432,8 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, const int32_t*
                           const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
                           float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s)
 {
-    k_composite_fwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(
+    auto kern = stats ? k_composite_fwd<true> : k_composite_fwd<false>;
+    kern<<<c.TW * c.TH, TILE_PIX, 0, s>>>(
         c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
         reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
         T_final, n_contrib, reinterpret_cast<unsigned long long*>(stats));
@@ -441,7 +446,8 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, const int32_t*
                           const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
                           uint64_t* stats, cudaStream_t s)
 {
-    k_composite_bwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(
+    auto kern = stats ? k_composite_bwd<true> : k_composite_bwd<false>;
+    kern<<<c.TW * c.TH, TILE_PIX, 0, s>>>(
         c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
         reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth,
         g_alpha, v_splats, reinterpret_cast<unsigned long long*>(stats));

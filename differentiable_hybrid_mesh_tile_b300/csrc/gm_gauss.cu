@@ -170,35 +170,64 @@ __device__ __forceinline__ bool culled(bool cull, const float* __restrict__ tile
     return cull && __ldg(tile_full + t) && depth >= __ldg(tile_far + t);
 }
 
+// Rectangles up to this many tiles are walked by their own thread; larger ones
+// (near-camera Gaussians) by the whole warp, 32 tiles at a time, so one large
+// Gaussian does not hold up the other 31 lanes.
+constexpr int SMALL_RECT = 16;
+
+// Per Gaussian: the number of tiles it is binned to after the cull, and its
+// depth key (float bits of the centre depth; 0xffffffff when it emits nothing)
+// for the depth pre-sort.
 __global__ void __launch_bounds__(256)
 k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
               const float* __restrict__ tile_far, const uint8_t* __restrict__ tile_full, int32_t* __restrict__ counts,
-              int32_t* counters)
+              uint64_t* __restrict__ dkey, int32_t* __restrict__ dval, int32_t* n_dev, int32_t* counters)
 {
     __shared__ int s_pre[8];
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    if (g == 0) *n_dev = N;
     int pre = 0, post = 0;
+    int x0 = 0, y0 = 0, x1 = 0, y1 = 0;
+    float depth = 0.0f;
     if (g < N) {
         const int r = radii[g];
-        int x0, y0, x1, y1;
         if (r > 0) {
             const float4 s0 = splats[3 * (int64_t)g];
-            const float depth = splats[3 * (int64_t)g + 2].y;
-            if (gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1)) {
-                pre = (x1 - x0) * (y1 - y0);
-                if (!cull) {
-                    post = pre;
-                } else {
-                    for (int ty = y0; ty < y1; ++ty)
-                        for (int tx = x0; tx < x1; ++tx) post += !culled(true, tile_far, tile_full, ty * c.TW + tx, depth);
-                }
-            }
+            depth = splats[3 * (int64_t)g + 2].y;
+            if (gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1)) pre = (x1 - x0) * (y1 - y0);
         }
+    }
+    if (!cull) {
+        post = pre;
+    } else {
+        if (pre <= SMALL_RECT) {
+            for (int ty = y0; ty < y1; ++ty)
+                for (int tx = x0; tx < x1; ++tx) post += !culled(true, tile_far, tile_full, ty * c.TW + tx, depth);
+        }
+        uint32_t big = __ballot_sync(0xffffffffu, pre > SMALL_RECT);
+        while (big) {
+            const int j = __ffs(big) - 1;
+            big &= big - 1;
+            const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
+            const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, pre, j);
+            const float jd = __shfl_sync(0xffffffffu, depth, j);
+            int cnt = 0;
+            for (int t = lane; t < jarea; t += 32)
+                cnt += !culled(true, tile_far, tile_full, (jy0 + t / jw) * c.TW + jx0 + t % jw, jd);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if (lane == j) post = cnt;
+        }
+    }
+    if (g < N) {
         counts[g] = post;
+        dkey[g] = post > 0 ? (uint64_t)__float_as_uint(depth) : 0xffffffffull;
+        dval[g] = g;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
-    if ((threadIdx.x & 31) == 0) s_pre[threadIdx.x >> 5] = pre;
+    if (lane == 0) s_pre[threadIdx.x >> 5] = pre;
     __syncthreads();
     if (threadIdx.x == 0) {
         int t = 0;
@@ -207,32 +236,71 @@ k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const 
     }
 }
 
+// Emits the (tile << 32 | depth bits, id) entries of the i-th Gaussian in
+// ascending (depth, id) order at offsets[i]: entries come out depth-sorted,
+// so a stable sort on the tile bits alone completes the (tile, depth, id) order.
 __global__ void __launch_bounds__(256)
 k_gauss_emit(Cam c, bool cull, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
              const float* __restrict__ tile_far, const uint8_t* __restrict__ tile_full,
+             const int32_t* __restrict__ order, const int32_t* __restrict__ counts,
              const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
              int32_t* __restrict__ vals)
 {
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;
-    if (g == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
-    if (g >= N) return;
-    const int r = radii[g];
-    if (r <= 0) return;
-    const float4 s0 = splats[3 * (int64_t)g];
-    const float depth = splats[3 * (int64_t)g + 2].y;
-    int x0, y0, x1, y1;
-    if (!gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1)) return;
-    const uint32_t dbits = __float_as_uint(depth);
-    int64_t o = offsets[g];
-    for (int ty = y0; ty < y1; ++ty)
-        for (int tx = x0; tx < x1; ++tx) {
-            const int t = ty * c.TW + tx;
-            if (culled(cull, tile_far, tile_full, t, depth)) continue;
-            if (o >= cap) return;
-            keys[o] = ((uint64_t)(uint32_t)t << 32) | dbits;
-            vals[o] = g;
-            ++o;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    if (i == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
+    int g = -1, x0 = 0, y0 = 0, x1 = 0, y1 = 0, area = 0;
+    float depth = 0.0f;
+    int64_t o = 0;
+    if (i < N) {
+        g = order[i];
+        if (g >= 0 && g < N && counts[g] > 0) {
+            const float4 s0 = splats[3 * (int64_t)g];
+            depth = splats[3 * (int64_t)g + 2].y;
+            if (gauss_rect(c, s0.x, s0.y, radii[g], x0, y0, x1, y1)) area = (x1 - x0) * (y1 - y0);
+            o = offsets[i];
         }
+    }
+    const uint32_t dbits = __float_as_uint(depth);
+    if (area > 0 && area <= SMALL_RECT) {
+        for (int ty = y0; ty < y1; ++ty)
+            for (int tx = x0; tx < x1; ++tx) {
+                const int t = ty * c.TW + tx;
+                if (culled(cull, tile_far, tile_full, t, depth)) continue;
+                if (o < cap) {
+                    keys[o] = ((uint64_t)(uint32_t)t << 32) | dbits;
+                    vals[o] = g;
+                }
+                ++o;
+            }
+    }
+    uint32_t big = __ballot_sync(0xffffffffu, area > SMALL_RECT);
+    while (big) {
+        const int j = __ffs(big) - 1;
+        big &= big - 1;
+        const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
+        const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, area, j);
+        const int jg = __shfl_sync(0xffffffffu, g, j);
+        const float jd = __shfl_sync(0xffffffffu, depth, j);
+        const uint32_t jbits = __float_as_uint(jd);
+        int64_t jo = __shfl_sync(0xffffffffu, o, j);
+        for (int base = 0; base < jarea; base += 32) {
+            const int t_in = base + lane;
+            int t = 0;
+            bool keep = false;
+            if (t_in < jarea) {
+                t = (jy0 + t_in / jw) * c.TW + jx0 + t_in % jw;
+                keep = !culled(cull, tile_far, tile_full, t, jd);
+            }
+            const uint32_t km = __ballot_sync(0xffffffffu, keep);
+            const int64_t dst = jo + __popc(km & ((1u << lane) - 1u));
+            if (keep && dst < cap) {
+                keys[dst] = ((uint64_t)(uint32_t)t << 32) | jbits;
+                vals[dst] = jg;
+            }
+            jo += __popc(km);
+        }
+    }
 }
 
 int tile_bits(int n_tiles) { return n_tiles > 1 ? 32 - __builtin_clz((unsigned)(n_tiles - 1)) : 0; }
@@ -274,9 +342,14 @@ cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, cons
 size_t gauss_bin_ws_bytes(int N, int cap)
 {
     int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
-    return scan_ws_bytes(n) + 2 * a256(sizeof(int32_t) * n) + sort_ws_bytes(k);
+    return scan_ws_bytes(n) + 2 * a256(sizeof(int32_t) * n) + 2 * a256(sizeof(uint64_t) * n) +
+           2 * a256(sizeof(int32_t) * n) + 256 + sort_ws_bytes(n > k ? n : k);
 }
 
+// Tile binning of the Gaussians.  The entries' order (tile, depth, id) is
+// reached in two stable LSD sorts: the N Gaussians by depth (32 bits), then,
+// after emitting each Gaussian's tiles in that order, the K entries by tile
+// only (ceil(log2 T) bits) -- instead of one 32 + log2 T bit sort of K keys.
 cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, const int32_t* radii,
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
@@ -289,28 +362,47 @@ cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, 
     b += a256(sizeof(int32_t) * n);
     int32_t* offsets = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
+    uint64_t* dkey = (uint64_t*)b;
+    b += a256(sizeof(uint64_t) * n);
+    uint64_t* dkey_alt = (uint64_t*)b;
+    b += a256(sizeof(uint64_t) * n);
+    int32_t* dval = (int32_t*)b;
+    b += a256(sizeof(int32_t) * n);
+    int32_t* dval_alt = (int32_t*)b;
+    b += a256(sizeof(int32_t) * n);
+    int32_t* n_dev = (int32_t*)b;
+    b += 256;
     SortWs so;
-    carve_sort_ws(b, k, so);
+    carve_sort_ws(b, n > k ? n : k, so);
 
     cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
     if (e != cudaSuccess) return e;
     const int T = c.TW * c.TH;
-    const int end_bit = 32 + tile_bits(T);
-    const int passes = sort_passes(0, end_bit);
+    const int tb = tile_bits(T);
+    const int passes = sort_passes(32, 32 + tb);
     uint64_t* ek = passes % 2 ? so.keys_alt : keys;
     int32_t* ev = passes % 2 ? so.vals_alt : gids;
     if (N > 0) {
         auto* s4 = reinterpret_cast<const float4*>(splats);
-        k_gauss_count<<<(N + 255) / 256, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, counts, counters);
-        if ((e = exclusive_scan(counts, offsets, N, counters, sw, s)) != cudaSuccess) return e;
-        k_gauss_emit<<<(N + 255) / 256, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, offsets, cap,
-                                                     counters, ek, ev);
+        const int grid = (N + 255) / 256;
+        k_gauss_count<<<grid, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, counts, dkey, dval, n_dev,
+                                           counters);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (passes % 2)
-            e = radix_sort(so.keys_alt, so.vals_alt, keys, gids, cap, 0, end_bit, counters, so, s);
-        else
-            e = radix_sort(keys, gids, so.keys_alt, so.vals_alt, cap, 0, end_bit, counters, so, s);
-        if (e != cudaSuccess) return e;
+        // depth pre-sort of the Gaussians (4 passes: even, the result is back in dkey / dval)
+        if ((e = radix_sort(dkey, dval, dkey_alt, dval_alt, N, 0, 32, n_dev, counters, so, s)) != cudaSuccess) return e;
+        if ((e = exclusive_scan(counts, dval, offsets, N, counters, sw, s)) != cudaSuccess) return e;
+        k_gauss_emit<<<grid, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, dval, counts, offsets, cap,
+                                          counters, ek, ev);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (tb > 0) {
+            if (passes % 2)
+                e = radix_sort(so.keys_alt, so.vals_alt, keys, gids, cap, 32, 32 + tb, counters + GM_CNT_K, counters,
+                               so, s);
+            else
+                e = radix_sort(keys, gids, so.keys_alt, so.vals_alt, cap, 32, 32 + tb, counters + GM_CNT_K, counters,
+                               so, s);
+            if (e != cudaSuccess) return e;
+        }
     }
     return tile_ranges(keys, N > 0 ? cap : 0, counters, tile_range, T, s);
 }

@@ -122,7 +122,7 @@ constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_PART = SCAN_THREADS * SCAN_IPT;
 constexpr int SORT_THREADS = 256;
-constexpr int SORT_IPT = 15;
+constexpr int SORT_IPT = 8;
 constexpr int SORT_PART = SORT_THREADS * SORT_IPT;
 constexpr int SORT_MAX_PASSES = 8;
 
@@ -152,16 +152,18 @@ size_t carve_sort_ws(void* base, int64_t cap, SortWs& ws);
 // bytes of ws that must be zero before each use (they start at the carve base)
 size_t scan_zero_bytes(const ScanWs& ws);
 
-// exclusive scan of counts[n] into offsets[n]; total -> counters[GM_CNT_K]
-cudaError_t exclusive_scan(const int32_t* counts, int32_t* offsets, int n, int32_t* counters,
+// exclusive scan of counts[idx[i]] (counts[i] when idx is NULL) into
+// offsets[i], i < n; total -> counters[GM_CNT_K]
+cudaError_t exclusive_scan(const int32_t* counts, const int32_t* idx, int32_t* offsets, int n, int32_t* counters,
                            const ScanWs& ws, cudaStream_t s);
 // Sort (keys, values) ascending by key bits [begin_bit, end_bit), stable.
-// The count is min(counters[GM_CNT_K], cap), read on the device.  Input is in
-// (k0, v0); the result is in (k0, v0) when the number of passes is even and
-// in the alternate buffers otherwise -- sort_passes() tells which.
+// The count is min(*n_dev, cap), read on the device; a bounded wait that gives
+// up sets GM_FLAG_TIMEOUT in counters.  Input is in (k0, v0); the result is
+// in (k0, v0) when the number of passes is even and in the alternate buffers
+// otherwise -- sort_passes() tells which.
 int sort_passes(int begin_bit, int end_bit);
 cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int cap, int begin_bit,
-                       int end_bit, int32_t* counters, const SortWs& ws, cudaStream_t s);
+                       int end_bit, const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s);
 // tile_range[T][2] from sorted keys (tile id in the high 32 bits); range zeroed first
 cudaError_t tile_ranges(const uint64_t* keys, int cap, const int32_t* counters, int32_t* tile_range,
                         int n_tiles, cudaStream_t s);

@@ -59,8 +59,11 @@ k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict_
     __shared__ TriRec sm[TILE_PIX];
     const int tile = blockIdx.x;
     const int tx = tile % c.TW, ty = tile / c.TW;
-    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
-    const int j = ty * TILE + (threadIdx.x >> 4);
+    // warp w covers the 8 x 4 pixel block at (8 (w % 2), 4 (w / 2)) of the tile
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * TILE + (warp & 1) * 8, by = ty * TILE + (warp >> 1) * 4;
+    const int i = bx + (lane & 7);
+    const int j = by + (lane >> 3);
     const bool inside = i < c.W && j < c.H;
     const float px = (float)i + 0.5f, py = (float)j + 0.5f;
     const int2 r = tile_range[tile];
@@ -86,10 +89,21 @@ k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict_
             }
         }
         __syncthreads();
-        if (inside) {
-            for (int k = 0; k < n; ++k) {
+        // per 32 staged triangles, a ballot of those whose pixel-centre box meets
+        // this warp's block; the warp visits only those, in ascending face order
+        for (int m = 0; m * 32 < n; ++m) {
+            const int kk = m * 32 + lane;
+            bool h = false;
+            if (kk < n) {
+                const TriRec& q = sm[kk];
+                h = q.x1 >= bx && q.x0 <= bx + 7 && q.y1 >= by && q.y0 <= by + 3;
+            }
+            uint32_t mask = __ballot_sync(0xffffffffu, h);
+            while (mask) {
+                const int k = m * 32 + __ffs(mask) - 1;
+                mask &= mask - 1;
                 const TriRec& q = sm[k];
-                if (i < q.x0 || i > q.x1 || j < q.y0 || j > q.y1) continue;
+                if (!inside || i < q.x0 || i > q.x1 || j < q.y0 || j > q.y1) continue;
                 float e0 = edge_rn(q.u1, q.v1, q.u2, q.v2, px, py);
                 float e1 = edge_rn(q.u2, q.v2, q.u0, q.v0, px, py);
                 float e2 = edge_rn(q.u0, q.v0, q.u1, q.v1, px, py);
@@ -387,13 +401,15 @@ cudaError_t tri_bin(const Cam& c, const float* V, int nV, const int32_t* F, int 
     int32_t* ev = passes % 2 ? so.vals_alt : tri_ids;
     if (nF > 0) {
         k_tri_count<<<(nF + 255) / 256, 256, 0, s>>>(c, V, nV, F, nF, counts);
-        if ((e = exclusive_scan(counts, offsets, nF, counters, sw, s)) != cudaSuccess) return e;
+        if ((e = exclusive_scan(counts, nullptr, offsets, nF, counters, sw, s)) != cudaSuccess) return e;
         k_tri_emit<<<(nF + 255) / 256, 256, 0, s>>>(c, V, nV, F, nF, offsets, cap, counters, ek, ev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (passes % 2)
-            e = radix_sort(so.keys_alt, so.vals_alt, keysA, tri_ids, cap, 32, 32 + tile_bits(T), counters, so, s);
+            e = radix_sort(so.keys_alt, so.vals_alt, keysA, tri_ids, cap, 32, 32 + tile_bits(T), counters + GM_CNT_K,
+                           counters, so, s);
         else
-            e = radix_sort(keysA, tri_ids, so.keys_alt, so.vals_alt, cap, 32, 32 + tile_bits(T), counters, so, s);
+            e = radix_sort(keysA, tri_ids, so.keys_alt, so.vals_alt, cap, 32, 32 + tile_bits(T), counters + GM_CNT_K,
+                           counters, so, s);
         if (e != cudaSuccess) return e;
     }
     return tile_ranges(keysA, nF > 0 ? cap : 0, counters, tile_range, T, s);

@@ -90,8 +90,8 @@ __device__ __forceinline__ uint32_t look_back(uint32_t* desc, int p, int stride,
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS)
-k_scan(const int32_t* __restrict__ in, int32_t* __restrict__ out, int n, uint32_t* desc, uint32_t* ticket,
-       int32_t* counters)
+k_scan(const int32_t* __restrict__ in, const int32_t* __restrict__ idx, int32_t* __restrict__ out, int n,
+       uint32_t* desc, uint32_t* ticket, int32_t* counters)
 {
     __shared__ uint32_t s_warp[SCAN_THREADS / 32];
     __shared__ int s_part;
@@ -104,8 +104,8 @@ k_scan(const int32_t* __restrict__ in, int32_t* __restrict__ out, int n, uint32_
     uint32_t sum = 0;
 #pragma unroll
     for (int i = 0; i < SCAN_IPT; ++i) {
-        int64_t idx = base + i;
-        v[i] = idx < n ? (uint32_t)in[idx] : 0u;
+        int64_t e = base + i;
+        v[i] = e < n ? (uint32_t)in[idx ? idx[e] : e] : 0u;
         sum += v[i];
     }
     uint32_t total;
@@ -125,8 +125,8 @@ k_scan(const int32_t* __restrict__ in, int32_t* __restrict__ out, int n, uint32_
     uint32_t run = s_excl + ex;
 #pragma unroll
     for (int i = 0; i < SCAN_IPT; ++i) {
-        int64_t idx = base + i;
-        if (idx < n) out[idx] = (int32_t)run;
+        int64_t e = base + i;
+        if (e < n) out[e] = (int32_t)run;
         run += v[i];
     }
     if (p == gridDim.x - 1 && threadIdx.x == SCAN_THREADS - 1) counters[GM_CNT_K] = (int32_t)(s_excl + total);
@@ -135,13 +135,13 @@ k_scan(const int32_t* __restrict__ in, int32_t* __restrict__ out, int n, uint32_
 // Histograms of every digit pass in one read of the keys; also clears the
 // look-back descriptors of the partitions the passes will use.
 __global__ void __launch_bounds__(256)
-k_hist(const uint64_t* __restrict__ keys, const int32_t* __restrict__ counters, int cap, int begin_bit,
+k_hist(const uint64_t* __restrict__ keys, const int32_t* __restrict__ n_dev, int cap, int begin_bit,
        int passes, uint32_t* __restrict__ hist, uint32_t* __restrict__ desc, int max_parts)
 {
     __shared__ uint32_t sh[SORT_MAX_PASSES * 256];
     for (int i = threadIdx.x; i < passes * 256; i += blockDim.x) sh[i] = 0;
     __syncthreads();
-    const int n = min(counters[GM_CNT_K], cap);
+    const int n = min(*n_dev, cap);
     const int nparts = (n + SORT_PART - 1) / SORT_PART;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)passes * nparts * 256; i += stride) {
@@ -149,7 +149,7 @@ k_hist(const uint64_t* __restrict__ keys, const int32_t* __restrict__ counters, 
         desc[p * max_parts * 256 + r] = 0u;
     }
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        uint64_t k = keys[i];
+        const uint64_t k = keys[i];
         for (int p = 0; p < passes; ++p)
             atomicAdd(&sh[p * 256 + (uint32_t)((k >> (begin_bit + 8 * p)) & 0xffu)], 1u);
     }
@@ -179,15 +179,15 @@ struct OnesweepSmem {
     int part;
 };
 
-__global__ void __launch_bounds__(SORT_THREADS, 2)
+__global__ void __launch_bounds__(SORT_THREADS, 4)
 k_onesweep(const uint64_t* __restrict__ kin, const int32_t* __restrict__ vin, uint64_t* __restrict__ kout,
-           int32_t* __restrict__ vout, int32_t* counters, int cap, int shift,
+           int32_t* __restrict__ vout, const int32_t* __restrict__ n_dev, int32_t* counters, int cap, int shift,
            const uint32_t* __restrict__ digit_start, uint32_t* desc, uint32_t* ticket)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     OnesweepSmem& S = *reinterpret_cast<OnesweepSmem*>(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n = min(counters[GM_CNT_K], cap);
+    const int n = min(*n_dev, cap);
     const int nparts = (n + SORT_PART - 1) / SORT_PART;
     const uint32_t lt_mask = (1u << lane) - 1u;
 
@@ -341,13 +341,13 @@ size_t carve_sort_ws(void* base, int64_t cap, SortWs& ws)
     return sort_ws_bytes(cap);
 }
 
-cudaError_t exclusive_scan(const int32_t* counts, int32_t* offsets, int n, int32_t* counters,
+cudaError_t exclusive_scan(const int32_t* counts, const int32_t* idx, int32_t* offsets, int n, int32_t* counters,
                            const ScanWs& ws, cudaStream_t s)
 {
     cudaError_t e = cudaMemsetAsync(ws.ticket, 0, scan_zero_bytes(ws), s);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaMemsetAsync(counters + GM_CNT_K, 0, sizeof(int32_t), s);
-    k_scan<<<scan_parts(n), SCAN_THREADS, 0, s>>>(counts, offsets, n, ws.desc, ws.ticket, counters);
+    k_scan<<<scan_parts(n), SCAN_THREADS, 0, s>>>(counts, idx, offsets, n, ws.desc, ws.ticket, counters);
     return cudaGetLastError();
 }
 
@@ -357,7 +357,7 @@ int sort_passes(int begin_bit, int end_bit)
 }
 
 cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int cap, int begin_bit, int end_bit,
-                       int32_t* counters, const SortWs& ws, cudaStream_t s)
+                       const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s)
 {
     const int passes = sort_passes(begin_bit, end_bit);
     if (passes == 0 || cap <= 0) return cudaSuccess;
@@ -367,19 +367,19 @@ cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int
     if (e != cudaSuccess) return e;
     const int sms = num_sms();
     int hgrid = (int)std::min<int64_t>(((int64_t)cap + 255) / 256, (int64_t)sms * 4);
-    k_hist<<<hgrid, 256, 0, s>>>(k0, counters, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
+    k_hist<<<hgrid, 256, 0, s>>>(k0, n_dev, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
     k_hist_scan<<<1, 256, 0, s>>>(ws.hist, passes);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(OnesweepSmem));
         attr = true;
     }
-    const int grid = std::min(ws.max_parts, sms * 2);
+    const int grid = std::min(ws.max_parts, sms * 4);
     uint64_t* kin = k0; int32_t* vin = v0;
     uint64_t* kout = k1; int32_t* vout = v1;
     for (int p = 0; p < passes; ++p) {
         k_onesweep<<<grid, SORT_THREADS, sizeof(OnesweepSmem), s>>>(
-            kin, vin, kout, vout, counters, cap, begin_bit + 8 * p, ws.hist + p * 256,
+            kin, vin, kout, vout, n_dev, counters, cap, begin_bit + 8 * p, ws.hist + p * 256,
             ws.desc + (size_t)p * ws.max_parts * 256, ws.tickets + p);
         std::swap(kin, kout);
         std::swap(vin, vout);
