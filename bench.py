@@ -42,7 +42,7 @@ L2_FLUSH_BYTES = 512 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gm", choices=["gm", "reference"])
     ap.add_argument("--config", default="soup_1080p")
@@ -82,6 +82,17 @@ class ClockSampler:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # nvidia-smi takes a moment to start: wait for its first sample (taken before
+        # the timed region) so that the samples kept all fall inside the region
+        self.skip = 0
+        t_end = time.time() + 5.0
+        while self.proc is not None and time.time() < t_end:
+            with open(self.path) as f:
+                n = sum(1 for _ in f)
+            if n:
+                self.skip = n
+                break
+            time.sleep(0.02)
         return self
 
     def __exit__(self, *a):
@@ -101,6 +112,8 @@ class ClockSampler:
                     rows.append(p)
         finally:
             os.unlink(self.path)
+        if len(rows) > self.skip:
+            rows = rows[self.skip:]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
 
