@@ -150,6 +150,40 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
     return n_ranks * pixels_per_rank / 1e6 / (ms / 1e3)
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
+# stage's kernel on soup_1080p, from one ncu capture (summary and command in the
+# named profile).  A figure holds only for the kernel sources it was taken on:
+# when any of them has changed since, the traffic is reported as null.
+PROFILED_TRAFFIC = {
+    "composite_bwd": {
+        "kernel": "k_composite_bwd",
+        "bytes": 169306880 + 12965632,
+        "sources": {
+            "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
+                "72046edb8317098c221ae514a3376a1970f74495ace6085b5e5882b06e1e58f9",
+            "differentiable_hybrid_mesh_tile_b300/csrc/gm_internal.cuh":
+                "1afa195e183d2d16258906e809871781fd5812223a41df10a22ba89235611604",
+        },
+        "profile": "profiles/composite_bwd_soup_1080p.md",
+    },
+}
+
+
+def profiled_traffic(stage):
+    import hashlib
+    rec = PROFILED_TRAFFIC.get(stage)
+    if rec is None:
+        return None
+    for path, sha in rec["sources"].items():
+        try:
+            with open(os.path.join(ROOT, path), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != sha:
+                    return None
+        except OSError:
+            return None
+    return rec["bytes"]
+
+
 # --------------------------------------------------------------- GPU arm --
 
 def run_gm(args, ws, rank, local):
@@ -177,7 +211,8 @@ def run_gm(args, ws, rank, local):
     stats_b = torch.zeros(2, dtype=torch.int64, device="cuda")
 
     cam_c, opts = r.cam, r.opts
-    names = ["tri_bin", "zbuffer", "interp", "project", "bin_sort", "composite_fwd", "composite_bwd"]
+    names = ["tri_bin", "zbuffer", "interp", "project", "bin_sort", "composite_fwd", "grad_zero", "composite_bwd",
+             "mesh_bwd"]
 
     def step(evs=None, count=False):
         def mark(k):
@@ -204,10 +239,17 @@ def run_gm(args, ws, rank, local):
         r.v_splats.zero_()
         r.v_verts.zero_()
         r.v_vcol.zero_()
-        gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
-                                   r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats, r.V, r.F,
-                                   r.vcol, r.v_verts, r.v_vcol, stats_b if count else None)
         mark(7)
+        # the backward call split in two (Gaussian gradients, then mesh gradients) so
+        # that each kernel gets its own events; the timed graph step makes one call
+        gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                   r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats, None, None,
+                                   None, None, None, stats_b if count else None)
+        mark(8)
+        gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                   r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], None, r.V, r.F,
+                                   r.vcol, r.v_verts, r.v_vcol, None)
+        mark(9)
 
     # sizing pass (host read-back of K, capacities grow), then warm-up without syncs
     r.forward(sync=True)
@@ -222,6 +264,7 @@ def run_gm(args, ws, rank, local):
     K_tri = int(r.tri_counters[0].item())
     K_g = int(r.g_counters[0].item())
     K_pre = int(r.g_counters[1].item())
+    covered = int((r.face_id >= 0).sum().item())
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -251,7 +294,7 @@ def run_gm(args, ws, rank, local):
     overflow = r.overflowed()
     ms_graph = float(np.mean([a.elapsed_time(b) for a, b in gev]))
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -260,7 +303,7 @@ def run_gm(args, ws, rank, local):
         step(evs[k])
     torch.cuda.synchronize()
     overflow = overflow or r.overflowed()
-    st = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(7)] for k in range(args.steps)])
+    st = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(len(names))] for k in range(args.steps)])
     ms_eager = float(st.sum(1).mean())
     # forward alone, also as a graph
     fgraph = torch.cuda.CUDAGraph()
@@ -283,7 +326,7 @@ def run_gm(args, ws, rank, local):
     ms_step, ms_fwd = max_over_ranks([ms_step, ms_fwd], dist, "cuda")
     value = job_throughput(ws, W * H, ms_step)
     fwd_value = job_throughput(ws, W * H, ms_fwd)
-    stage_ms = {names[i]: float(st[:, i].mean()) for i in range(7)}
+    stage_ms = {names[i]: float(st[:, i].mean()) for i in range(len(names))}
 
     # ---- roofline of each stage (algorithmic work per launch / measured duration)
     import json as _json
@@ -299,6 +342,7 @@ def run_gm(args, ws, rank, local):
     sh = r.sh_degree
     col_bytes = 12 if sh < 0 else 12 * (sh + 1) ** 2
     F = int(r.F.shape[0])
+    nV = int(r.V.shape[0])
     T = r.T
     tbits = max((T - 1).bit_length(), 0)
     passes_g = math.ceil(tbits / 8)   # tile passes after the 4-pass depth pre-sort
@@ -318,6 +362,11 @@ def run_gm(args, ws, rank, local):
         # the tests), 60 per composited pair backward (the gradient terms)
         "composite_fwd": ("alu", 18 * pairs_f),
         "composite_bwd": ("alu", 60 * blend_b),
+        # zero fills of the three gradient outputs
+        "grad_zero": ("hbm", 4 * (r.v_splats.numel() + r.v_verts.numel() + r.v_vcol.numel())),
+        # face id of every pixel; T, upstream rgb + depth gradient of covered pixels;
+        # face indices; vertex positions and colours read, their gradients read + written
+        "mesh_bwd": ("hbm", W * H * 4 + covered * 20 + F * 12 + nV * 24 + nV * 24 * 2),
     }
     stages = {}
     for k, (bound, amount) in work.items():
@@ -333,7 +382,7 @@ def run_gm(args, ws, rank, local):
     stages["zbuffer"] = {"bound": "alu", "ms": stage_ms["zbuffer"], "note": "reported, no target"}
     top = max(work, key=lambda k: stage_ms[k])
     roof = dict(stages[top])
-    roof.update(kernel=top, traffic=None, peak_source=hbm_src if roof["bound"] == "hbm" else
+    roof.update(kernel=top, traffic=profiled_traffic(top), peak_source=hbm_src if roof["bound"] == "hbm" else
                 "SMs x 128 FP32 lanes x median SM clock under load")
     roof.pop("ms", None)
     roof.pop("algorithmic", None)

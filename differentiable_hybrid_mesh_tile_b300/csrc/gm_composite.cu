@@ -1,13 +1,19 @@
 // Hybrid compositing ("A Lightweight and Differentiable Renderer for Joint
 // Mesh and 3D Gaussian Splat Scenes", Hybrid rendering) with a hard depth
 // test: every Gaussian is tested against the mesh depth at the pixel, and the
-// opaque mesh is the terminal layer.  Forward and backward, one CTA per
-// 16 x 16 tile, one thread per pixel, each warp an 8 x 4 pixel block; the
-// tile's sorted records are staged in shared memory in batches of 256.
+// opaque mesh is the terminal layer.  Forward and backward, two CTAs of four
+// warps per 16 x 16 tile (each CTA one 16 x 8 half), one thread per pixel,
+// each warp an 8 x 4 pixel block; the tile's sorted records are staged in
+// shared memory in batches of 128.
 //
 // Each warp first asks, per staged record, whether the Gaussian's ellipse of
 // alpha >= 1/255 meets its 8 x 4 pixel block, and then visits only those
 // records (the other pairs would be skipped anyway).
+//
+// Half-tile CTAs: the warps of a CTA wait for one another at every batch and
+// at exit, so the slowest 8 x 4 block holds the CTA; four blocks per CTA
+// instead of eight lose less to that imbalance than staging the list twice
+// per tile costs.
 #include "gm_internal.cuh"
 
 namespace gm {
@@ -17,6 +23,10 @@ constexpr float ALPHA_MAX = 0.99f;
 constexpr float ALPHA_MIN = 1.0f / 255.0f;
 constexpr float T_STOP = 1e-4f;
 constexpr float LOG2E = 1.4426950408889634f;
+
+constexpr int CTA_WARPS = 4;                  // 8 x 4 blocks per CTA: half a tile
+constexpr int CTA_THREADS = 32 * CTA_WARPS;   // = staging batch
+constexpr int CTAS_PER_TILE = 8 / CTA_WARPS;
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -115,11 +125,13 @@ struct PixelMap {
     float x0, y0;  // centre of the warp block's first pixel
 };
 
-// warp w of the tile covers the 8 x 4 block at (8 (w % 2), 4 (w / 2))
-__device__ __forceinline__ PixelMap pixel_of(const Cam& c, int tile)
+// CTA b covers half b % 2 of tile b / 2; warp w of the tile (w = 4 half + warp
+// of the CTA) covers the 8 x 4 block at (8 (w % 2), 4 (w / 2))
+__device__ __forceinline__ PixelMap pixel_of(const Cam& c, int& tile)
 {
+    tile = blockIdx.x / CTAS_PER_TILE;
     const int tx = tile % c.TW, ty = tile / c.TW;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = (blockIdx.x % CTAS_PER_TILE) * CTA_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int bx = tx * TILE + (warp & 1) * 8, by = ty * TILE + (warp >> 1) * 4;
     PixelMap m;
     m.i = bx + (lane & 7);
@@ -136,15 +148,15 @@ __device__ __forceinline__ void stage_empty(float4& C, float4& H)
 }
 
 template <bool STATS>
-__global__ void __launch_bounds__(TILE_PIX)
+__global__ void __launch_bounds__(CTA_THREADS)
 k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
                 const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id, float* __restrict__ out_rgb,
                 float* __restrict__ out_depth, float* __restrict__ out_alpha, float* __restrict__ T_final,
                 int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ stats)
 {
-    __shared__ float4 sA[TILE_PIX], sB[TILE_PIX], sC[TILE_PIX], sH[TILE_PIX];
-    const int tile = blockIdx.x;
+    __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
+    int tile;
     const PixelMap pm = pixel_of(c, tile);
     const bool inside = pm.i < c.W && pm.j < c.H;
     const int64_t pix = (int64_t)pm.j * c.W + pm.i;
@@ -160,9 +172,11 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     uint32_t visited = 0, blended = 0;
     bool done = !inside;
     const int2 r = tile_range[tile];
-    for (int b = r.x; b < r.y; b += TILE_PIX) {
-        if (__syncthreads_count(done) == TILE_PIX) break;
-        const int n = min(TILE_PIX, r.y - b);
+    for (int b = r.x; b < r.y; b += CTA_THREADS) {
+        // this barrier also keeps the staging below from overwriting records that
+        // another warp of the CTA is still reading from the previous batch
+        if (__syncthreads_count(done) == CTA_THREADS) break;
+        const int n = min(CTA_THREADS, r.y - b);
         if ((int)threadIdx.x < n) {
             const int64_t g = gids[b + threadIdx.x];
             if (g >= 0 && g < N)
@@ -207,7 +221,6 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 if (STATS) ++blended;
             }
         }
-        __syncthreads();
     }
     if (STATS) {
         block_count(visited, stats);
@@ -251,8 +264,21 @@ __device__ __forceinline__ float reduce_scatter4(const float v[GROUP], int lane)
     return x;
 }
 
+// Adds a staged entry's accumulated gradient (components 0..9 of the record
+// layout) to its Gaussian's row of v_splats: three 16-byte vector atomics, the
+// last of which adds zero to the two padding floats.
+__device__ __forceinline__ void flush_grad(float* __restrict__ v_splats, int g, const float* acc)
+{
+    float4* dst = reinterpret_cast<float4*>(v_splats + 12 * (int64_t)g);
+    atomicAdd(dst, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    atomicAdd(dst + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    atomicAdd(dst + 2, make_float4(acc[8], acc[9], 0.0f, 0.0f));
+}
+
+// Ten CTAs of 128 threads per SM (at most 51 registers a thread): the kernel
+// is bound by instruction latency, and resident warps hide it.
 template <bool STATS>
-__global__ void __launch_bounds__(TILE_PIX, 4)
+__global__ void __launch_bounds__(CTA_THREADS, 10)
 k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
                 const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
@@ -260,11 +286,11 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                 const float* __restrict__ g_rgb, const float* __restrict__ g_depth, const float* __restrict__ g_alpha,
                 float* __restrict__ v_splats, unsigned long long* __restrict__ stats)
 {
-    __shared__ float4 sA[TILE_PIX], sB[TILE_PIX], sC[TILE_PIX], sH[TILE_PIX];
-    __shared__ int sG[TILE_PIX];
-    __shared__ float sAcc[TILE_PIX][NGRAD + 1];
+    __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
+    __shared__ int sG[CTA_THREADS];
+    __shared__ float sAcc[CTA_THREADS][NGRAD + 1];
     __shared__ int s_max_last;
-    const int tile = blockIdx.x;
+    int tile;
     const PixelMap pm = pixel_of(c, tile);
     const int lane = threadIdx.x & 31;
     const bool inside = pm.i < c.W && pm.j < c.H;
@@ -301,8 +327,13 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     const int end = r.x + s_max_last;
     uint32_t visited = 0, contributed = 0;
     const int my_entry = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-    for (int b_end = end; b_end > r.x; b_end -= TILE_PIX) {
-        const int b0 = max(r.x, b_end - TILE_PIX);
+    int n_prev = 0;
+    for (int b_end = end;; b_end -= CTA_THREADS) {
+        // the previous batch's gradients go out and the next batch comes in, each
+        // thread on its own slot, so one barrier covers both
+        if ((int)threadIdx.x < n_prev && sG[threadIdx.x] >= 0) flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x]);
+        if (b_end <= r.x) break;
+        const int b0 = max(r.x, b_end - CTA_THREADS);
         const int n = b_end - b0;
         if ((int)threadIdx.x < n) {
             int g = gids[b0 + threadIdx.x];
@@ -336,12 +367,12 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                         kj[jj] = -1;
                     }
                 }
-                // per entry: w = alpha T_front, vo = dL/d opacity, ds = dL/d sigma, dx, dy
-                float pw[GROUP], pvo[GROUP], pds[GROUP], pdx[GROUP], pdy[GROUP];
+                // per entry: w = alpha T_front, vo = dL/d opacity, ds = dL/d sigma
+                float pw[GROUP], pvo[GROUP], pds[GROUP];
                 bool any = false;
 #pragma unroll
                 for (int jj = 0; jj < GROUP; ++jj) {
-                    pw[jj] = pvo[jj] = pds[jj] = pdx[jj] = pdy[jj] = 0.0f;
+                    pw[jj] = pvo[jj] = pds[jj] = 0.0f;
                     const int k = kj[jj];
                     if (k < 0 || !inside || b0 - r.x + k >= last) continue;
                     const float4 C3 = sC[k];
@@ -364,8 +395,6 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                         pvo[jj] = dLda * e.G;
                         pds[jj] = -dLda * e.alpha;  // d alpha / d sigma = -alpha
                     }
-                    pdx[jj] = e.dx;
-                    pdy[jj] = e.dy;
                 }
                 if (__any_sync(0xffffffffu, any)) {
                     const int k = my_entry == 0 ? kj[0] : my_entry == 1 ? kj[1] : my_entry == 2 ? kj[2] : kj[3];
@@ -375,6 +404,15 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                     // d sigma / d mean = -(a dx + b dy, b dx + c dy) with a = -2 a2 / log2e,
                     // b = -b2 / log2e, c = -2 c2 / log2e
                     float sx = 0.0f, sy = 0.0f;
+                    // pixel offsets recomputed here (the same roundings as eval_splat)
+                    // rather than kept live through the group: fewer registers
+                    float pdx[GROUP], pdy[GROUP];
+#pragma unroll
+                    for (int jj = 0; jj < GROUP; ++jj) {
+                        const float2 mean = *reinterpret_cast<const float2*>(&sA[kj[jj] < 0 ? 0 : kj[jj]]);
+                        pdx[jj] = __fsub_rn(px, mean.x);
+                        pdy[jj] = __fsub_rn(py, mean.y);
+                    }
 #pragma unroll
                     for (int q = 0; q < NGRAD; ++q) {
                         float col[GROUP];
@@ -402,22 +440,14 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                     if (k >= 0 && sub < 2) {
                         const float a2 = sA[k].z, b2 = sA[k].w, c2 = sB[k].x;
                         const float tx = sx * (1.0f / LOG2E), ty = sy * (1.0f / LOG2E);
-                        const float m = sub == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
-                        if (m != 0.0f) atomicAdd(&sAcc[k][sub], m);
+                        const float mg = sub == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
+                        if (mg != 0.0f) atomicAdd(&sAcc[k][sub], mg);
                     }
                 }
             }
         }
         __syncthreads();
-        if ((int)threadIdx.x < n && sG[threadIdx.x] >= 0) {
-            float* dst = v_splats + 12 * (int64_t)sG[threadIdx.x];
-#pragma unroll
-            for (int q = 0; q < NGRAD; ++q) {
-                const float a = sAcc[threadIdx.x][q];
-                if (a != 0.0f) atomicAdd(dst + q, a);
-            }
-        }
-        __syncthreads();
+        n_prev = n;
     }
     if (STATS) {
         block_count(visited, stats);
@@ -433,7 +463,7 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, const int32_t*
                           float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s)
 {
     auto kern = stats ? k_composite_fwd<true> : k_composite_fwd<false>;
-    kern<<<c.TW * c.TH, TILE_PIX, 0, s>>>(
+    kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
         c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
         reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
         T_final, n_contrib, reinterpret_cast<unsigned long long*>(stats));
@@ -447,7 +477,7 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, const int32_t*
                           uint64_t* stats, cudaStream_t s)
 {
     auto kern = stats ? k_composite_bwd<true> : k_composite_bwd<false>;
-    kern<<<c.TW * c.TH, TILE_PIX, 0, s>>>(
+    kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
         c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
         reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth,
         g_alpha, v_splats, reinterpret_cast<unsigned long long*>(stats));

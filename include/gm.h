@@ -218,6 +218,8 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  *   v_splats [N][12] f32 (+=, 16-byte aligned): dL/d mean2d, conic, opacity,
  *   rgb, depth of each Gaussian (the hard depth test, the skips and the sort
  *   carry no gradient; alpha clamped at 0.99 has none w.r.t. opacity/conic).
+ *   Sums are added with 16-byte vector atomics; the two padding floats of a
+ *   row receive += 0.  Summation order varies between runs (last-bit noise).
  *   v_verts [nV][3], v_vcol [nV][3] f32 (+=): dL/d vertex world position and
  *   colour through the interpolated mesh depth and colour of covered pixels
  *   (face ids held fixed).  V / F / vcol / v_verts / v_vcol may all be NULL
