@@ -123,7 +123,7 @@ int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* 
     GM_REQUIRE(nF == 0 || F, "F is NULL");
     GM_REQUIRE(tile_range && face_id, "tile_range / face_id is NULL");
     GM_REQUIRE(tri_ids || nF == 0, "tri_ids is NULL");
-    cudaError_t e = gm::zbuffer(gm::make_cam(*cam), V, nV, F, tile_range, tri_ids, face_id, (cudaStream_t)stream);
+    cudaError_t e = gm::zbuffer(gm::make_cam(*cam), V, nV, F, nF, tile_range, tri_ids, face_id, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_zbuffer");
 }
 

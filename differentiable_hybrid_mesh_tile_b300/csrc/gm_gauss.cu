@@ -267,7 +267,7 @@ k_gauss_emit(Cam c, bool cull, int N, const float4* __restrict__ splats, const i
             for (int tx = x0; tx < x1; ++tx) {
                 const int t = ty * c.TW + tx;
                 if (culled(cull, tile_far, tile_full, t, depth)) continue;
-                if (o < cap) {
+                if (o >= 0 && o < cap) {
                     keys[o] = ((uint64_t)(uint32_t)t << 32) | dbits;
                     vals[o] = g;
                 }
@@ -294,7 +294,7 @@ k_gauss_emit(Cam c, bool cull, int N, const float4* __restrict__ splats, const i
             }
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
             const int64_t dst = jo + __popc(km & ((1u << lane) - 1u));
-            if (keep && dst < cap) {
+            if (keep && dst >= 0 && dst < cap) {
                 keys[dst] = ((uint64_t)(uint32_t)t << 32) | jbits;
                 vals[dst] = jg;
             }

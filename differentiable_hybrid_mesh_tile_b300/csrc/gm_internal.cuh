@@ -177,7 +177,7 @@ int set_last_error(int code, const char* fmt, ...);
 size_t tri_bin_ws_bytes(int nF, int cap);
 cudaError_t tri_bin(const Cam& c, const float* V, int nV, const int32_t* F, int nF, int32_t* tile_range,
                     int32_t* tri_ids, int cap, int32_t* counters, void* ws, cudaStream_t s);
-cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, const int32_t* tile_range,
+cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* tile_range,
                     const int32_t* tri_ids, int32_t* face_id, cudaStream_t s);
 cudaError_t interp(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
                    const int32_t* face_id, float* mesh_depth, float* mesh_rgb, float* tile_far, uint8_t* tile_full,

@@ -36,7 +36,7 @@ k_tri_emit(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
     int64_t o = offsets[f];
     for (int ty = t.y0 / TILE; ty <= t.y1 / TILE; ++ty)
         for (int tx = t.x0 / TILE; tx <= t.x1 / TILE; ++tx, ++o) {
-            if (o >= cap) return;
+            if (o < 0 || o >= cap) return;
             keys[o] = (uint64_t)(uint32_t)(ty * c.TW + tx) << 32;
             vals[o] = f;
         }
@@ -53,7 +53,7 @@ struct TriRec {
 };
 
 __global__ void __launch_bounds__(TILE_PIX)
-k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F,
+k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
           const int2* __restrict__ tile_range, const int32_t* __restrict__ tri_ids, int32_t* __restrict__ face_id)
 {
     __shared__ TriRec sm[TILE_PIX];
@@ -75,7 +75,9 @@ k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict_
             int f = tri_ids[b + threadIdx.x];
             Tri t;
             TriRec& q = sm[threadIdx.x];
-            if (tri_setup(c, V, nV, F, f, t)) {
+            // an id outside [0, nF) (possible only when the sort that built the
+            // lists gave up a bounded wait) is skipped
+            if (f >= 0 && f < nF && tri_setup(c, V, nV, F, f, t)) {
                 q.u0 = t.u[0]; q.v0 = t.v[0]; q.u1 = t.u[1]; q.v1 = t.v[1]; q.u2 = t.u[2]; q.v2 = t.v[2];
                 q.area = t.area;
                 q.w0 = 1.0f / (t.area * t.z[0]);
@@ -415,10 +417,10 @@ cudaError_t tri_bin(const Cam& c, const float* V, int nV, const int32_t* F, int 
     return tile_ranges(keysA, nF > 0 ? cap : 0, counters, tile_range, T, s);
 }
 
-cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, const int32_t* tile_range,
+cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* tile_range,
                     const int32_t* tri_ids, int32_t* face_id, cudaStream_t s)
 {
-    k_zbuffer<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, reinterpret_cast<const int2*>(tile_range), tri_ids,
+    k_zbuffer<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, reinterpret_cast<const int2*>(tile_range), tri_ids,
                                                 face_id);
     return cudaGetLastError();
 }

@@ -105,7 +105,10 @@ k_scan(const int32_t* __restrict__ in, const int32_t* __restrict__ idx, int32_t*
 #pragma unroll
     for (int i = 0; i < SCAN_IPT; ++i) {
         int64_t e = base + i;
-        v[i] = e < n ? (uint32_t)in[idx ? idx[e] : e] : 0u;
+        // a gathered index outside [0, n) (possible only when the sort that
+        // produced idx gave up a bounded wait) counts as zero
+        const int64_t j = e < n ? (idx ? (int64_t)idx[e] : e) : -1;
+        v[i] = (j >= 0 && j < n) ? (uint32_t)in[j] : 0u;
         sum += v[i];
     }
     uint32_t total;

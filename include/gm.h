@@ -122,8 +122,8 @@ int gm_bin_triangles(const gm_camera* cam, const float* V, int32_t nV, const int
  * every edge function has the sign of the area (edges inclusive, both
  * windings).  The nearest perspective-correct depth wins; equal depths go to
  * the smaller face id.
- *   tile_range / tri_ids: from gm_bin_triangles.  face_id [H][W] i32 out
- *   (-1 = uncovered).
+ *   tile_range / tri_ids: from gm_bin_triangles (ids outside [0, nF) are
+ *   skipped).  face_id [H][W] i32 out (-1 = uncovered).
  * ---------------------------------------------------------------------- */
 int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
                const int32_t* tile_range, const int32_t* tri_ids, int32_t* face_id, void* stream);
