@@ -141,6 +141,30 @@ def project(cam, g):
     return splats, radii, touched, margin
 
 
+PROJ_PARAMS = ("mean", "log_scale", "quat", "logit", "color")
+
+
+def proj_nparams(sh_degree):
+    """Parameters of one Gaussian in the projection gradient's numbering:
+    mean 0-2, log-scale 3-5, quaternion (w, x, y, z) 6-9, logit 10, colour
+    coefficient k of channel ch at 11 + 3 k + ch."""
+    return 11 + 3 * ((sh_degree + 1) ** 2 if sh_degree >= 0 else 1)
+
+
+def project_fd(cam, g, v_splats, gids, params, hs):
+    """dL/d(3D parameter) by central differences (double, Richardson) for
+    L = sum over record fields of v_splats . record; see orc_project_fd."""
+    n = len(gids)
+    grad = np.zeros(n, np.float64)
+    status = np.zeros(n, np.int32)
+    lib().orc_project_fd(C.byref(_cam(cam)), C.c_int32(g.sh_degree), _p(_c(g.means, np.float32)),
+                         _p(_c(g.log_scales, np.float32)), _p(_c(g.quats, np.float32)),
+                         _p(_c(g.logits, np.float32)), _p(_c(g.colors, np.float32)),
+                         _p(_c(v_splats, np.float32)), C.c_int32(n), _p(_c(gids, np.int32)),
+                         _p(_c(params, np.int32)), _p(_c(hs, np.float64)), _p(grad), _p(status))
+    return grad, status
+
+
 def sh_basis(deg, direction):
     d = _c(direction, np.float64)
     Y = np.zeros(16, np.float64)

@@ -1103,3 +1103,193 @@ void orc_composite_one(int32_t f32, double px, double py, const int32_t* list, i
     out[0] = o.rgb[0]; out[1] = o.rgb[1]; out[2] = o.rgb[2];
     out[3] = o.depth; out[4] = o.alpha; out[5] = o.T; out[6] = o.n_contrib;
 }
+
+/* ========================================================================
+ * Gradients of the projection (the projection / SH backward: dL/d of the
+ * 3D parameters), for L = sum over the record fields of v . record, by
+ * central differences in double
+ * ====================================================================== */
+
+/* Parameters of one Gaussian as one double vector:
+ *   p[0..2] mean, p[3..5] log-scales, p[6..9] quaternion (w, x, y, z),
+ *   p[10] opacity logit, p[11 + 3 k + ch] colour coefficient k of channel
+ *   ch (k < (d+1)^2 for SH degree d; k = 0 = plain RGB when d < 0).      */
+#define PROJ_NPAR(deg) (11 + 3 * ((deg) >= 0 ? ((deg) + 1) * ((deg) + 1) : 1))
+
+static void proj_load(int sh_degree, int64_t g, const float* means, const float* log_scales, const float* quats,
+                      const float* logits, const float* colors, double* p)
+{
+    int ncoef = sh_degree >= 0 ? (sh_degree + 1) * (sh_degree + 1) : 1;
+    for (int k = 0; k < 3; ++k) p[k] = means[3 * g + k];
+    for (int k = 0; k < 3; ++k) p[3 + k] = log_scales[3 * g + k];
+    for (int k = 0; k < 4; ++k) p[6 + k] = quats[4 * g + k];
+    p[10] = logits[g];
+    for (int k = 0; k < 3 * ncoef; ++k) p[11 + k] = colors[(int64_t)g * 3 * ncoef + k];
+}
+
+/* The record of one Gaussian (fields S_MX .. S_Z) from double parameters,
+ * every value in double, by the definitions orc_project_gaussians states.
+ * The decisions that make the map non-smooth go to trace: [0] culled (near
+ * / far, determinant, empty tile rectangle -- decided in fp32 as the
+ * forward decides them), [1] [2] the x / y clamps of the Jacobian
+ * direction, [3..5] the colour clamps at 0.  A culled Gaussian's record is
+ * all zeros.                                                              */
+static void proj_record_f64(const orc_camera* c, int sh_degree, const double* p, double rec[10], uint8_t trace[6])
+{
+    int ncoef = sh_degree >= 0 ? (sh_degree + 1) * (sh_degree + 1) : 1;
+    double Rc[3][3], cam_pos[3], t[3];
+    for (int k = 0; k < 10; ++k) rec[k] = 0.0;
+    for (int k = 0; k < 6; ++k) trace[k] = 0;
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 3; ++k) Rc[r][k] = c->R[3 * r + k];
+    for (int k = 0; k < 3; ++k)
+        cam_pos[k] = -(Rc[0][k] * c->t[0] + Rc[1][k] * c->t[1] + Rc[2][k] * c->t[2]);
+    for (int r = 0; r < 3; ++r) t[r] = Rc[r][0] * p[0] + Rc[r][1] * p[1] + Rc[r][2] * p[2] + c->t[r];
+    float tz32 = (float)t[2];
+    if (!(tz32 > c->near_plane) || tz32 > c->far_plane) {
+        trace[0] = 1;
+        return;
+    }
+    double qn = sqrt(p[6] * p[6] + p[7] * p[7] + p[8] * p[8] + p[9] * p[9]);
+    double w = p[6] / qn, x = p[7] / qn, y = p[8] / qn, z = p[9] / qn;
+    double Rq[3][3] = {
+        {1 - 2 * (y * y + z * z), 2 * (x * y - w * z), 2 * (x * z + w * y)},
+        {2 * (x * y + w * z), 1 - 2 * (x * x + z * z), 2 * (y * z - w * x)},
+        {2 * (x * z - w * y), 2 * (y * z + w * x), 1 - 2 * (x * x + y * y)}};
+    double sc[3], M[3][3], S3[3][3], Tmp[3][3], Sc[3][3];
+    for (int k = 0; k < 3; ++k) sc[k] = exp(p[3 + k]);
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 3; ++k) M[r][k] = Rq[r][k] * sc[k];
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 3; ++k) {
+            S3[r][k] = 0;
+            for (int m = 0; m < 3; ++m) S3[r][k] += M[r][m] * M[k][m];
+        }
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 3; ++k) {
+            Tmp[r][k] = 0;
+            for (int m = 0; m < 3; ++m) Tmp[r][k] += Rc[r][m] * S3[m][k];
+        }
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 3; ++k) {
+            Sc[r][k] = 0;
+            for (int m = 0; m < 3; ++m) Sc[r][k] += Tmp[r][m] * Rc[k][m];
+        }
+    double limx_pos = 1.3 * (c->width - (double)c->cx) / c->fx, limx_neg = 1.3 * (double)c->cx / c->fx;
+    double limy_pos = 1.3 * (c->height - (double)c->cy) / c->fy, limy_neg = 1.3 * (double)c->cy / c->fy;
+    double rx = t[0] / t[2], ry = t[1] / t[2];
+    trace[1] = rx > limx_pos || rx < -limx_neg;
+    trace[2] = ry > limy_pos || ry < -limy_neg;
+    double tx = t[2] * fmin(limx_pos, fmax(-limx_neg, rx));
+    double ty = t[2] * fmin(limy_pos, fmax(-limy_neg, ry));
+    double J[2][3] = {{c->fx / t[2], 0.0, -c->fx * tx / (t[2] * t[2])},
+                      {0.0, c->fy / t[2], -c->fy * ty / (t[2] * t[2])}};
+    double JS[2][3], S2[2][2];
+    for (int r = 0; r < 2; ++r)
+        for (int k = 0; k < 3; ++k) {
+            JS[r][k] = 0;
+            for (int m = 0; m < 3; ++m) JS[r][k] += J[r][m] * Sc[m][k];
+        }
+    for (int r = 0; r < 2; ++r)
+        for (int k = 0; k < 2; ++k) {
+            S2[r][k] = 0;
+            for (int m = 0; m < 3; ++m) S2[r][k] += JS[r][m] * J[k][m];
+        }
+    S2[0][0] += 0.3;
+    S2[1][1] += 0.3;
+    /* the cull decisions, in fp32 as the forward takes them */
+    float a32 = (float)S2[0][0], b32 = (float)S2[0][1], c32 = (float)S2[1][1];
+    float det32 = a32 * c32 - b32 * b32;
+    double mx = c->fx * t[0] / t[2] + c->cx, my = c->fy * t[1] / t[2] + c->cy;
+    int rect[4];
+    if (!(det32 > 0.0f)) {
+        trace[0] = 1;
+        return;
+    }
+    float m32 = 0.5f * (a32 + c32), h32 = 0.5f * (a32 - c32);
+    float lam32 = m32 + sqrtf(h32 * h32 + b32 * b32);
+    if (gauss_rect(c, (float)mx, (float)my, (int32_t)ceilf(3.0f * sqrtf(lam32)), rect) <= 0) {
+        trace[0] = 1;
+        return;
+    }
+    double det = S2[0][0] * S2[1][1] - S2[0][1] * S2[0][1];
+    rec[S_MX] = mx;
+    rec[S_MY] = my;
+    rec[S_CA] = S2[1][1] / det;
+    rec[S_CB] = -S2[0][1] / det;
+    rec[S_CC] = S2[0][0] / det;
+    rec[S_OP] = 1.0 / (1.0 + exp(-p[10]));
+    if (sh_degree < 0) {
+        for (int ch = 0; ch < 3; ++ch) rec[S_R + ch] = p[11 + ch];
+    } else {
+        double d[3], dn = 0.0, Y[16];
+        for (int k = 0; k < 3; ++k) {
+            d[k] = p[k] - cam_pos[k];
+            dn += d[k] * d[k];
+        }
+        dn = sqrt(dn);
+        for (int k = 0; k < 3; ++k) d[k] /= dn;
+        orc_sh_basis(sh_degree, d, Y);
+        for (int ch = 0; ch < 3; ++ch) {
+            double v = 0.5;
+            for (int k = 0; k < ncoef; ++k) v += Y[k] * p[11 + 3 * k + ch];
+            trace[3 + ch] = v < 0.0;
+            rec[S_R + ch] = fmax(0.0, v);
+        }
+    }
+    rec[S_Z] = t[2];
+}
+
+static double proj_loss(const orc_camera* c, int sh_degree, const double* p, const float* v, uint8_t trace[6])
+{
+    double rec[10];
+    proj_record_f64(c, sh_degree, p, rec, trace);
+    double L = 0.0;
+    for (int f = 0; f < 10; ++f) L += (double)v[f] * rec[f];
+    return L;
+}
+
+/* dL/d p[param] of Gaussian gid for the requested pairs, L = sum_f
+ * v_splats[gid][f] record_f (central differences at h and h/2, Richardson).
+ * status: FD_OK; FD_FLIP a decision in the trace differs anywhere in
+ * [-h, +h]; FD_NONSMOOTH the two step sizes disagree.  A Gaussian culled
+ * throughout gets 0 with FD_OK.                                           */
+void orc_project_fd(const orc_camera* c, int32_t sh_degree, const float* means, const float* log_scales,
+                    const float* quats, const float* logits, const float* colors, const float* v_splats,
+                    int32_t n, const int32_t* gids, const int32_t* params, const double* hs, double* grad,
+                    int32_t* status)
+{
+    int np = PROJ_NPAR(sh_degree);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int32_t i = 0; i < n; ++i) {
+        double p[PROJ_NPAR(3)], q[PROJ_NPAR(3)];
+        int64_t g = gids[i];
+        int k = params[i];
+        double h = hs[i];
+        const float* v = v_splats + S_STRIDE * g;
+        grad[i] = 0.0;
+        status[i] = FD_OK;
+        if (k < 0 || k >= np) {
+            status[i] = FD_UNUSED;
+            continue;
+        }
+        proj_load(sh_degree, g, means, log_scales, quats, logits, colors, p);
+        uint8_t t0[6], tp[6], tm[6], tp2[6], tm2[6];
+        proj_loss(c, sh_degree, p, v, t0);
+        memcpy(q, p, sizeof(double) * np);
+        q[k] = p[k] + h;
+        double lp = proj_loss(c, sh_degree, q, v, tp);
+        q[k] = p[k] - h;
+        double lm = proj_loss(c, sh_degree, q, v, tm);
+        q[k] = p[k] + 0.5 * h;
+        double lp2 = proj_loss(c, sh_degree, q, v, tp2);
+        q[k] = p[k] - 0.5 * h;
+        double lm2 = proj_loss(c, sh_degree, q, v, tm2);
+        if (memcmp(t0, tp, 6) || memcmp(t0, tm, 6) || memcmp(t0, tp2, 6) || memcmp(t0, tm2, 6)) {
+            status[i] = FD_FLIP;
+            continue;
+        }
+        if (t0[0]) continue; /* culled throughout: zero gradient */
+        status[i] = richardson(lp, lm, lp2, lm2, h, &grad[i]);
+    }
+}
