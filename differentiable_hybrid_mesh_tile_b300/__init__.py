@@ -58,6 +58,7 @@ _SIGS = {
     "gm_zbuffer": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP]),
     "gm_interp_mesh": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "gm_project_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "gm_project_gaussians_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 7 + [_I32] + [_VP] * 6),
     "gm_bin_sort_gaussians_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
     "gm_bin_sort_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
                                         C.c_size_t, _VP]),
@@ -190,6 +191,16 @@ def gm_project_gaussians(cam: gm_camera, opts: gm_opts, means, log_scales, quats
                                       _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
                                       _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32), _stream()),
            "gm_project_gaussians")
+
+
+def gm_project_gaussians_bwd(cam: gm_camera, opts: gm_opts, means, log_scales, quats, logits, colors, radii,
+                             v_splats, v_means, v_log_scales, v_quats, v_logits, v_colors, accumulate=False):
+    _check(lib().gm_project_gaussians_bwd(C.byref(cam), C.byref(opts), means.shape[0], _p(means, F32),
+                                          _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
+                                          _p(radii, I32), _p(v_splats, F32), int(bool(accumulate)), _p(v_means, F32),
+                                          _p(v_log_scales, F32), _p(v_quats, F32), _p(v_logits, F32),
+                                          _p(v_colors, F32), _stream()),
+           "gm_project_gaussians_bwd")
 
 
 def gm_bin_sort_gaussians_workspace_size(N: int, cap: int, width: int, height: int) -> int:

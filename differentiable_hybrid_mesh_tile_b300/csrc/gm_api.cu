@@ -163,6 +163,31 @@ int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, c
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians");
 }
 
+int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
+                             const float* log_scales, const float* quats, const float* logits, const float* colors,
+                             const int32_t* radii, const float* v_splats, int32_t accumulate, float* v_means,
+                             float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(N >= 0, "negative N");
+    GM_REQUIRE(opts->sh_degree >= -1 && opts->sh_degree <= 3, "sh_degree %d not in -1..3", opts->sh_degree);
+    if (N > 0) {
+        GM_REQUIRE(means && log_scales && quats && logits && colors && radii && v_splats, "an input is NULL");
+        GM_REQUIRE(v_means && v_log_scales && v_quats && v_logits && v_colors, "an output is NULL");
+        GM_REQUIRE(aligned16(quats) && aligned16(v_splats) && aligned16(v_quats),
+                   "quats / v_splats / v_quats must be 16-byte aligned");
+        if (opts->sh_degree == 1 || opts->sh_degree == 3)
+            GM_REQUIRE(aligned16(colors) && aligned16(v_colors), "SH coefficients and their gradient must be "
+                       "16-byte aligned");
+    }
+    cudaError_t e = gm::project_bwd(gm::make_cam(*cam), opts->sh_degree, N, means, log_scales, quats, logits, colors,
+                                    radii, v_splats, accumulate != 0, v_means, v_log_scales, v_quats, v_logits,
+                                    v_colors, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_bwd");
+}
+
 size_t gm_bin_sort_gaussians_workspace_size(int32_t N, int32_t cap, int32_t width, int32_t height)
 {
     (void)width;

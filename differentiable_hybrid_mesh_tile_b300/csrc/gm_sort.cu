@@ -219,7 +219,15 @@ k_onesweep(const uint64_t* __restrict__ kin, const int32_t* __restrict__ vin, ui
         for (int i = 0; i < SORT_IPT; ++i) {
             uint32_t d = (uint32_t)(key[i] >> shift) & 0xffu;
             if (key[i] == ~0ull) d = 0xffu;
-            uint32_t peers = __match_any_sync(0xffffffffu, d);
+            // lanes holding the same digit: eight ballots, one per digit bit
+            // (cheaper here than match.any, which queues on a narrow pipe)
+            uint32_t peers = 0xffffffffu;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const uint32_t bit = (d >> b) & 1u;
+                const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+                peers &= bit ? bal : ~bal;
+            }
             uint32_t before = S.whist[warp][d];
             __syncwarp();
             if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);

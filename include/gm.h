@@ -162,6 +162,29 @@ int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, c
                          void* stream);
 
 /* ------------------------------------------------------------------------
+ * gm_project_gaussians_bwd -- backward of gm_project_gaussians (Hybrid
+ * rendering: everything is differentiable; the page's Gaussian kernels are
+ * adapted from gsplat).  Given dL/d of each projected record, the chain rule
+ * through the EWA projection and the SH colour:
+ *   inputs: the same camera, opts, N and parameters as the forward call;
+ *   radii [N] i32 from that call (radius 0 = culled: zero gradients);
+ *   v_splats [N][12] f32, 16-byte aligned: dL/d record, e.g. the output of
+ *   gm_composite_hybrid_bwd (the two padding floats are ignored).
+ *   v_means [N][3], v_log_scales [N][3], v_quats [N][4] (16-byte aligned),
+ *   v_logits [N], v_colors (the layout of colors; 16-byte aligned for SH
+ *   degree 1 and 3) f32 out: dL/d of each parameter, written when
+ *   accumulate = 0, added (+=) when accumulate != 0 (e.g. over views).
+ * Non-smooth points take these one-sided choices: a colour clamped at 0
+ * passes no gradient; past the Jacobian's direction clamp the clamped
+ * component is constant; the quaternion gradient is orthogonal to q (the
+ * projection depends on q / |q| only).
+ * ---------------------------------------------------------------------- */
+int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
+                             const float* log_scales, const float* quats, const float* logits, const float* colors,
+                             const int32_t* radii, const float* v_splats, int32_t accumulate, float* v_means,
+                             float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, void* stream);
+
+/* ------------------------------------------------------------------------
  * gm_bin_sort_gaussians -- tile intersection and sort (Hybrid rendering;
  * Limitations: Gaussians ordered by centre depth) with the per-tile cull
  * (Hybrid rendering, cull_occluded bullet: Gaussians certainly hidden behind

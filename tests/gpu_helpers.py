@@ -178,3 +178,25 @@ def input_ulp_perturbations(cam, V, draws=3, seed=0):
         r = rng.choice([-1.0, 1.0], size=V.shape)
         out.append((V.astype(np.float64) + scale * r).astype(np.float32))
     return out
+
+
+def run_project_bwd(cam, g, v_splats, accumulate_into=None):
+    """GPU projection, then its backward for the upstream v_splats.  Returns
+    radii and the gradients (v_means, v_log_scales, v_quats, v_logits, v_colors)
+    as numpy; accumulate_into = previous gradients to add to (accumulate mode)."""
+    c = gm.make_camera(cam)
+    o = gm.make_opts((1, 1, 1), True, g.sh_degree)
+    N = len(g.means)
+    args = [dev(g.means, torch.float32), dev(g.log_scales, torch.float32), dev(g.quats, torch.float32),
+            dev(g.logits, torch.float32), dev(g.colors, torch.float32)]
+    splats = torch.zeros((N, 12), dtype=torch.float32, device="cuda")
+    radii = torch.zeros((N,), dtype=torch.int32, device="cuda")
+    touched = torch.zeros((N,), dtype=torch.int32, device="cuda")
+    gm.gm_project_gaussians(c, o, *args, splats, radii, touched)
+    if accumulate_into is None:
+        outs = [torch.full(a.shape, 3.0, dtype=torch.float32, device="cuda") for a in args]
+    else:
+        outs = [dev(x, torch.float32).clone() for x in accumulate_into]
+    gm.gm_project_gaussians_bwd(c, o, *args, radii, dev(v_splats, torch.float32), *outs,
+                                accumulate=accumulate_into is not None)
+    return host(radii), [host(x) for x in outs]
