@@ -255,9 +255,16 @@ class HybridRenderer:
     GM_ERR_CAPACITY status triggers one reallocation and a retry).  With
     ``sync=False`` the binning calls do not read K back, so a whole step can
     be captured in a CUDA graph; the caller then checks ``overflowed()``.
+
+    With ``concurrent=True`` the calls that do not depend on each other run on
+    a second stream: the Gaussian projection beside the mesh binning,
+    z-buffer and interpolation, and the mesh backward beside the composite
+    backward (joined back into the caller's stream before anything reads
+    their results; a captured graph keeps the two branches).
     """
 
-    def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25):
+    def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
+                 concurrent=True):
         self.cam_desc = cam
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
@@ -267,6 +274,8 @@ class HybridRenderer:
         self.cull = bool(cull_occluded)
         self.dev = torch.device(device)
         self.headroom = headroom
+        self.concurrent = bool(concurrent)
+        self._side = None
         self.tri_cap = 0
         self.g_cap = 0
         self.sh_degree = -1
@@ -337,8 +346,20 @@ class HybridRenderer:
     def _grow(self, needed):
         return max(int(needed * self.headroom) + 16, 16)
 
+    def _side_stream(self):
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.dev)
+        return self._side
+
     def forward(self, sync: bool = True):
         cam, opts = self.cam, self.opts
+        main = torch.cuda.current_stream(self.dev)
+        side = self._side_stream() if self.concurrent else main
+        if self.concurrent:
+            side.wait_stream(main)
+        with torch.cuda.stream(side):
+            gm_project_gaussians(cam, opts, self.means, self.log_scales, self.quats, self.logits, self.colors,
+                                 self.splats, self.radii, self.tiles_touched)
         for attempt in range(2):
             try:
                 k = gm_bin_triangles(cam, self.V, self.F, self.tri_range, self.tri_ids, self.tri_cap,
@@ -352,8 +373,8 @@ class HybridRenderer:
         gm_zbuffer(cam, self.V, self.F, self.tri_range, self.tri_ids, self.face_id)
         gm_interp_mesh(cam, self.V, self.F, self.vcol, self.face_id, self.mesh_depth, self.mesh_rgb, self.tile_far,
                        self.tile_full)
-        gm_project_gaussians(cam, opts, self.means, self.log_scales, self.quats, self.logits, self.colors,
-                             self.splats, self.radii, self.tiles_touched)
+        if self.concurrent:
+            main.wait_stream(side)
         for attempt in range(2):
             try:
                 k = gm_bin_sort_gaussians(cam, opts, self.splats, self.radii, self.tile_far, self.tile_full,
@@ -371,18 +392,26 @@ class HybridRenderer:
         return self.out_rgb, self.out_depth, self.out_alpha
 
     def backward(self, g_rgb, g_depth, g_alpha, mesh_grads: bool = True):
-        self.v_splats.zero_()
+        cam, opts = self.cam, self.opts
+        main = torch.cuda.current_stream(self.dev)
         if mesh_grads:
             if not hasattr(self, "v_verts") or self.v_verts.shape != self.V.shape:
                 self.v_verts = torch.zeros_like(self.V)
                 self.v_vcol = torch.zeros_like(self.vcol)
-            self.v_verts.zero_()
-            self.v_vcol.zero_()
-        gm_composite_hybrid_bwd(self.cam, self.opts, self.g_range, self.gids, self.splats, self.mesh_depth,
-                                self.mesh_rgb, self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha,
-                                self.v_splats, self.V if mesh_grads else None, self.F if mesh_grads else None,
-                                self.vcol if mesh_grads else None, self.v_verts if mesh_grads else None,
-                                self.v_vcol if mesh_grads else None)
+            side = self._side_stream() if self.concurrent else main
+            if self.concurrent:
+                side.wait_stream(main)
+            with torch.cuda.stream(side):
+                self.v_verts.zero_()
+                self.v_vcol.zero_()
+                gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth,
+                                        self.mesh_rgb, self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth,
+                                        g_alpha, None, self.V, self.F, self.vcol, self.v_verts, self.v_vcol)
+        self.v_splats.zero_()
+        gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
+                                self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha, self.v_splats)
+        if mesh_grads and self.concurrent:
+            main.wait_stream(side)
         if mesh_grads:
             return self.v_splats, self.v_verts, self.v_vcol
         return self.v_splats, None, None
