@@ -47,7 +47,8 @@ class gm_camera(C.Structure):
 
 
 class gm_opts(C.Structure):
-    _fields_ = [("bg", C.c_float * 3), ("cull_occluded", C.c_int32), ("sh_degree", C.c_int32)]
+    _fields_ = [("bg", C.c_float * 3), ("cull_occluded", C.c_int32), ("sh_degree", C.c_int32),
+                ("tile_test", C.c_int32)]
 
 
 _VP = C.c_void_p
@@ -108,12 +109,13 @@ def make_camera(cam) -> gm_camera:
     return c
 
 
-def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1) -> gm_opts:
+def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1, tile_test=True) -> gm_opts:
     o = gm_opts()
     for k in range(3):
         o.bg[k] = float(bg[k])
     o.cull_occluded = int(bool(cull_occluded))
     o.sh_degree = int(sh_degree)
+    o.tile_test = int(bool(tile_test))
     return o
 
 
@@ -264,7 +266,7 @@ class HybridRenderer:
     """
 
     def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
-                 concurrent=True):
+                 concurrent=True, tile_test=True):
         self.cam_desc = cam
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
@@ -275,6 +277,7 @@ class HybridRenderer:
         self.dev = torch.device(device)
         self.headroom = headroom
         self.concurrent = bool(concurrent)
+        self.tile_test = bool(tile_test)
         self._side = None
         self.tri_cap = 0
         self.g_cap = 0
@@ -303,7 +306,7 @@ class HybridRenderer:
 
     @property
     def opts(self) -> gm_opts:
-        return make_opts(self.bg, self.cull, self.sh_degree)
+        return make_opts(self.bg, self.cull, self.sh_degree, self.tile_test)
 
     def upload(self, mesh, gaussians):
         d = self.dev

@@ -213,7 +213,8 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
     GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), opts->cull_occluded != 0, N, splats, radii, tile_far,
+    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), opts->cull_occluded != 0, opts->tile_test != 0, N, splats,
+                                       radii, tile_far,
                                        tile_full, keys, gids, tile_range, cap, counters, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "gm_bin_sort_gaussians");
     return finish_binning(counters, K_host, cap, s);

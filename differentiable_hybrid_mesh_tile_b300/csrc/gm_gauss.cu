@@ -119,10 +119,81 @@ k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const fl
 
 // ------------------------------------------------------------- binning ----
 
-__device__ __forceinline__ bool culled(bool cull, const float* __restrict__ tile_far,
-                                       const uint8_t* __restrict__ tile_full, int t, float depth)
+// Which tiles of a Gaussian's rectangle get an entry.
+struct BinRule {
+    bool cull;        // drop tiles where the mesh hides the Gaussian (tile_full, depth >= tile_far)
+    bool tile_test;   // drop tiles no pixel centre of which the Gaussian reaches with alpha >= 1/255
+    const float* __restrict__ tile_far;
+    const uint8_t* __restrict__ tile_full;
+    int TW;
+};
+
+// What the per-tile tests need of one Gaussian.
+struct BinShape {
+    float mx, my, a, b, c;  // mean and conic: sigma(d) = (a dx^2 + c dy^2) / 2 + b dx dy
+    float nba, nbc;         // -b / a, -b / c: vertex of sigma along a line of constant v / u
+    float smax;             // alpha >= 1/255 needs sigma <= ln(255 o); smax adds a margin
+    float depth;
+    bool degenerate;        // conic not positive definite: every tile is kept
+};
+
+__device__ __forceinline__ BinShape bin_shape(const float4* __restrict__ splats, int g)
 {
-    return cull && __ldg(tile_full + t) && depth >= __ldg(tile_far + t);
+    const float4 s0 = splats[3 * (int64_t)g], s1 = splats[3 * (int64_t)g + 1];
+    BinShape b;
+    b.mx = s0.x; b.my = s0.y; b.a = s0.z; b.b = s0.w; b.c = s1.x;
+    b.degenerate = !(b.a > 0.0f) || !(b.a * b.c - b.b * b.b > 0.0f);
+    b.nba = b.degenerate ? 0.0f : -b.b / b.a;
+    b.nbc = b.degenerate ? 0.0f : -b.b / b.c;
+    // 0.1 % + 1e-4 above ln(255 o): the fp32 evaluation of sigma at a pixel centre
+    // (compositing) can never keep a pair this test drops
+    const float thr = logf(255.0f * s1.y);
+    b.smax = thr + 1e-3f * fabsf(thr) + 1e-4f;
+    b.depth = splats[3 * (int64_t)g + 2].y;
+    return b;
+}
+
+__device__ __forceinline__ BinShape shfl_shape(const BinShape& s, int j)
+{
+    BinShape o;
+    o.mx = __shfl_sync(0xffffffffu, s.mx, j); o.my = __shfl_sync(0xffffffffu, s.my, j);
+    o.a = __shfl_sync(0xffffffffu, s.a, j); o.b = __shfl_sync(0xffffffffu, s.b, j);
+    o.c = __shfl_sync(0xffffffffu, s.c, j); o.smax = __shfl_sync(0xffffffffu, s.smax, j);
+    o.nba = __shfl_sync(0xffffffffu, s.nba, j); o.nbc = __shfl_sync(0xffffffffu, s.nbc, j);
+    o.depth = __shfl_sync(0xffffffffu, s.depth, j);
+    o.degenerate = __shfl_sync(0xffffffffu, (int)s.degenerate, j) != 0;
+    return o;
+}
+
+// Smallest sigma over the pixel centres of tile (tx, ty), relaxed to the
+// tile's 15 x 15 px square of centres: 0 when it holds the mean, else on an
+// edge, where sigma is a 1D parabola minimised at a clamped vertex.  A
+// degenerate conic gives -inf (the tile is kept).
+__device__ __forceinline__ float tile_min_sigma(const BinShape& s, int tx, int ty)
+{
+    if (s.degenerate) return -INFINITY;
+    const float u0 = (float)(tx * TILE) + 0.5f - s.mx, u1 = u0 + (float)(TILE - 1);
+    const float v0 = (float)(ty * TILE) + 0.5f - s.my, v1 = v0 + (float)(TILE - 1);
+    if (u0 <= 0.0f && u1 >= 0.0f && v0 <= 0.0f && v1 >= 0.0f) return 0.0f;
+    float best = INFINITY;
+    {   // edges u = u0, u1: v* = -b u / c
+        const float va = fminf(fmaxf(s.nbc * u0, v0), v1), vb = fminf(fmaxf(s.nbc * u1, v0), v1);
+        best = fminf(best, 0.5f * (s.a * u0 * u0 + s.c * va * va) + s.b * u0 * va);
+        best = fminf(best, 0.5f * (s.a * u1 * u1 + s.c * vb * vb) + s.b * u1 * vb);
+    }
+    {   // edges v = v0, v1: u* = -b v / a
+        const float ua = fminf(fmaxf(s.nba * v0, u0), u1), ub = fminf(fmaxf(s.nba * v1, u0), u1);
+        best = fminf(best, 0.5f * (s.a * ua * ua + s.c * v0 * v0) + s.b * ua * v0);
+        best = fminf(best, 0.5f * (s.a * ub * ub + s.c * v1 * v1) + s.b * ub * v1);
+    }
+    return best;
+}
+
+__device__ __forceinline__ bool keep_tile(const BinRule& r, const BinShape& s, int tx, int ty)
+{
+    const int t = ty * r.TW + tx;
+    if (r.cull && __ldg(r.tile_full + t) && s.depth >= __ldg(r.tile_far + t)) return false;
+    return !r.tile_test || tile_min_sigma(s, tx, ty) <= s.smax;
 }
 
 // Rectangles up to this many tiles are walked by their own thread; larger ones
@@ -130,35 +201,41 @@ __device__ __forceinline__ bool culled(bool cull, const float* __restrict__ tile
 // Gaussian does not hold up the other 31 lanes.
 constexpr int SMALL_RECT = 16;
 
-// Per Gaussian: the number of tiles it is binned to after the cull, and its
-// depth key (float bits of the centre depth; 0xffffffff when it emits nothing)
-// for the depth pre-sort.
+// Per Gaussian: the number of tiles it is binned to after the cull and the
+// tile test, and its depth key (float bits of the centre depth; 0xffffffff
+// when it emits nothing) for the depth pre-sort.
 __global__ void __launch_bounds__(256)
-k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
-              const float* __restrict__ tile_far, const uint8_t* __restrict__ tile_full, int32_t* __restrict__ counts,
-              uint64_t* __restrict__ dkey, int32_t* __restrict__ dval, int32_t* n_dev, int32_t* counters)
+k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
+              int32_t* __restrict__ counts, uint32_t* __restrict__ kept, uint64_t* __restrict__ dkey,
+              int32_t* __restrict__ dval, int32_t* n_dev, int32_t* counters)
 {
     __shared__ int s_pre[8];
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     if (g == 0) *n_dev = N;
     int pre = 0, post = 0;
+    uint32_t mask = 0;
     int x0 = 0, y0 = 0, x1 = 0, y1 = 0;
-    float depth = 0.0f;
+    BinShape sh = {};
     if (g < N) {
         const int r = radii[g];
         if (r > 0) {
-            const float4 s0 = splats[3 * (int64_t)g];
-            depth = splats[3 * (int64_t)g + 2].y;
-            if (gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1)) pre = (x1 - x0) * (y1 - y0);
+            sh = bin_shape(splats, g);
+            if (gauss_rect(c, sh.mx, sh.my, r, x0, y0, x1, y1)) pre = (x1 - x0) * (y1 - y0);
         }
     }
-    if (!cull) {
+    if (!rule.cull && !rule.tile_test) {
         post = pre;
+        mask = 0xffffffffu;
     } else {
         if (pre <= SMALL_RECT) {
+            int i = 0;
             for (int ty = y0; ty < y1; ++ty)
-                for (int tx = x0; tx < x1; ++tx) post += !culled(true, tile_far, tile_full, ty * c.TW + tx, depth);
+                for (int tx = x0; tx < x1; ++tx, ++i)
+                    if (keep_tile(rule, sh, tx, ty)) {
+                        mask |= 1u << i;
+                        ++post;
+                    }
         }
         uint32_t big = __ballot_sync(0xffffffffu, pre > SMALL_RECT);
         while (big) {
@@ -166,10 +243,9 @@ k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const 
             big &= big - 1;
             const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
             const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, pre, j);
-            const float jd = __shfl_sync(0xffffffffu, depth, j);
+            const BinShape js = shfl_shape(sh, j);
             int cnt = 0;
-            for (int t = lane; t < jarea; t += 32)
-                cnt += !culled(true, tile_far, tile_full, (jy0 + t / jw) * c.TW + jx0 + t % jw, jd);
+            for (int t = lane; t < jarea; t += 32) cnt += keep_tile(rule, js, jx0 + t % jw, jy0 + t / jw);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
             if (lane == j) post = cnt;
@@ -177,7 +253,8 @@ k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const 
     }
     if (g < N) {
         counts[g] = post;
-        dkey[g] = post > 0 ? (uint64_t)__float_as_uint(depth) : 0xffffffffull;
+        kept[g] = mask;
+        dkey[g] = post > 0 ? (uint64_t)__float_as_uint(sh.depth) : 0xffffffffull;
         dval[g] = g;
     }
 #pragma unroll
@@ -194,36 +271,39 @@ k_gauss_count(Cam c, bool cull, int N, const float4* __restrict__ splats, const 
 // Emits the (tile << 32 | depth bits, id) entries of the i-th Gaussian in
 // ascending (depth, id) order at offsets[i]: entries come out depth-sorted,
 // so a stable sort on the tile bits alone completes the (tile, depth, id) order.
+// The tiles kept are exactly those k_gauss_count counted: its bit mask for
+// small rectangles, the same predicate for large ones.
 __global__ void __launch_bounds__(256)
-k_gauss_emit(Cam c, bool cull, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
-             const float* __restrict__ tile_far, const uint8_t* __restrict__ tile_full,
+k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
              const int32_t* __restrict__ order, const int32_t* __restrict__ counts,
-             const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
-             int32_t* __restrict__ vals)
+             const uint32_t* __restrict__ kept, const int32_t* __restrict__ offsets, int cap, int32_t* counters,
+             uint64_t* __restrict__ keys, int32_t* __restrict__ vals)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     if (i == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
     int g = -1, x0 = 0, y0 = 0, x1 = 0, y1 = 0, area = 0;
-    float depth = 0.0f;
+    BinShape sh = {};
+    uint32_t mask = 0;
     int64_t o = 0;
     if (i < N) {
         g = order[i];
         if (g >= 0 && g < N && counts[g] > 0) {
-            const float4 s0 = splats[3 * (int64_t)g];
-            depth = splats[3 * (int64_t)g + 2].y;
-            if (gauss_rect(c, s0.x, s0.y, radii[g], x0, y0, x1, y1)) area = (x1 - x0) * (y1 - y0);
+            sh = bin_shape(splats, g);
+            if (gauss_rect(c, sh.mx, sh.my, radii[g], x0, y0, x1, y1)) area = (x1 - x0) * (y1 - y0);
             o = offsets[i];
+            mask = kept[g];
         }
     }
-    const uint32_t dbits = __float_as_uint(depth);
+    const uint32_t dbits = __float_as_uint(sh.depth);
     if (area > 0 && area <= SMALL_RECT) {
+        // the tiles k_gauss_count kept, one bit each in row-major rectangle order
+        int k = 0;
         for (int ty = y0; ty < y1; ++ty)
-            for (int tx = x0; tx < x1; ++tx) {
-                const int t = ty * c.TW + tx;
-                if (culled(cull, tile_far, tile_full, t, depth)) continue;
+            for (int tx = x0; tx < x1; ++tx, ++k) {
+                if (!((mask >> k) & 1u)) continue;
                 if (o >= 0 && o < cap) {
-                    keys[o] = ((uint64_t)(uint32_t)t << 32) | dbits;
+                    keys[o] = ((uint64_t)(uint32_t)(ty * c.TW + tx) << 32) | dbits;
                     vals[o] = g;
                 }
                 ++o;
@@ -236,21 +316,22 @@ k_gauss_emit(Cam c, bool cull, int N, const float4* __restrict__ splats, const i
         const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
         const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, area, j);
         const int jg = __shfl_sync(0xffffffffu, g, j);
-        const float jd = __shfl_sync(0xffffffffu, depth, j);
-        const uint32_t jbits = __float_as_uint(jd);
+        const BinShape js = shfl_shape(sh, j);
+        const uint32_t jbits = __float_as_uint(js.depth);
         int64_t jo = __shfl_sync(0xffffffffu, o, j);
         for (int base = 0; base < jarea; base += 32) {
             const int t_in = base + lane;
-            int t = 0;
+            int tx = 0, ty = 0;
             bool keep = false;
             if (t_in < jarea) {
-                t = (jy0 + t_in / jw) * c.TW + jx0 + t_in % jw;
-                keep = !culled(cull, tile_far, tile_full, t, jd);
+                tx = jx0 + t_in % jw;
+                ty = jy0 + t_in / jw;
+                keep = keep_tile(rule, js, tx, ty);
             }
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
             const int64_t dst = jo + __popc(km & ((1u << lane) - 1u));
             if (keep && dst >= 0 && dst < cap) {
-                keys[dst] = ((uint64_t)(uint32_t)t << 32) | jbits;
+                keys[dst] = ((uint64_t)(uint32_t)(ty * c.TW + tx) << 32) | jbits;
                 vals[dst] = jg;
             }
             jo += __popc(km);
@@ -289,7 +370,7 @@ cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, cons
 size_t gauss_bin_ws_bytes(int N, int cap)
 {
     int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
-    return scan_ws_bytes(n) + 2 * a256(sizeof(int32_t) * n) + 2 * a256(sizeof(uint64_t) * n) +
+    return scan_ws_bytes(n) + 3 * a256(sizeof(int32_t) * n) + 2 * a256(sizeof(uint64_t) * n) +
            2 * a256(sizeof(int32_t) * n) + 256 + sort_ws_bytes(n > k ? n : k);
 }
 
@@ -297,7 +378,7 @@ size_t gauss_bin_ws_bytes(int N, int cap)
 // reached in two stable LSD sorts: the N Gaussians by depth (32 bits), then,
 // after emitting each Gaussian's tiles in that order, the K entries by tile
 // only (ceil(log2 T) bits) -- instead of one 32 + log2 T bit sort of K keys.
-cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, const int32_t* radii,
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
 {
@@ -309,6 +390,8 @@ cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, 
     b += a256(sizeof(int32_t) * n);
     int32_t* offsets = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
+    uint32_t* kept = (uint32_t*)b;
+    b += a256(sizeof(uint32_t) * n);
     uint64_t* dkey = (uint64_t*)b;
     b += a256(sizeof(uint64_t) * n);
     uint64_t* dkey_alt = (uint64_t*)b;
@@ -332,14 +415,19 @@ cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, 
     if (N > 0) {
         auto* s4 = reinterpret_cast<const float4*>(splats);
         const int grid = (N + 255) / 256;
-        k_gauss_count<<<grid, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, counts, dkey, dval, n_dev,
-                                           counters);
+        BinRule rule;
+        rule.cull = cull;
+        rule.tile_test = tile_test;
+        rule.tile_far = tile_far;
+        rule.tile_full = tile_full;
+        rule.TW = c.TW;
+        k_gauss_count<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, counts, kept, dkey, dval, n_dev, counters);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // depth pre-sort of the Gaussians (4 passes: even, the result is back in dkey / dval)
         if ((e = radix_sort(dkey, dval, dkey_alt, dval_alt, N, 0, 32, n_dev, counters, so, s)) != cudaSuccess) return e;
         if ((e = exclusive_scan(counts, dval, offsets, N, counters, sw, s)) != cudaSuccess) return e;
-        k_gauss_emit<<<grid, 256, 0, s>>>(c, cull, N, s4, radii, tile_far, tile_full, dval, counts, offsets, cap,
-                                          counters, ek, ev);
+        k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, dval, counts, kept, offsets, cap, counters, ek,
+                                          ev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (tb > 0) {
             if (passes % 2)

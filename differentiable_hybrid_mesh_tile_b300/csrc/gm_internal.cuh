@@ -194,7 +194,7 @@ cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, 
                         const float* v_splats, bool accumulate, float* v_means, float* v_log_scales, float* v_quats,
                         float* v_logits, float* v_colors, cudaStream_t s);
 size_t gauss_bin_ws_bytes(int N, int cap);
-cudaError_t gauss_bin_sort(const Cam& c, bool cull, int N, const float* splats, const int32_t* radii,
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
 

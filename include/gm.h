@@ -81,6 +81,8 @@ typedef struct gm_opts {
     float bg[3];            /* background colour behind uncovered pixels */
     int32_t cull_occluded;  /* 1: drop Gaussians hidden behind fully covered tiles */
     int32_t sh_degree;      /* -1: colours are RGB [N][3]; 0..3: SH coefficients [N][(d+1)^2][3] */
+    int32_t tile_test;      /* 1: also drop a (Gaussian, tile) pair when no pixel centre of the tile
+                               can reach alpha >= 1/255 (see gm_bin_sort_gaussians) */
 } gm_opts;
 
 /*
@@ -192,8 +194,12 @@ int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t 
  * Every (Gaussian, tile) pair of a rectangle gets the 64-bit key
  *   (tile id << 32) | bits(depth)
  * and the Gaussian id as value; with opts->cull_occluded a pair is dropped
- * when tile_full[tile] and depth >= tile_far[tile].  Keys are sorted
- * ascending by a stable LSD radix sort, so equal depths keep ascending ids.
+ * when tile_full[tile] and depth >= tile_far[tile]; with opts->tile_test a
+ * pair is dropped when the smallest sigma over the tile's square of pixel
+ * centres exceeds ln(255 opacity) by a margin (0.1 % + 1e-4): the Gaussian
+ * cannot reach alpha >= 1/255 at any of those pixels, so the image and the
+ * gradients do not change.  Keys are sorted ascending by a stable LSD radix
+ * sort, so equal depths keep ascending ids.
  *   splats / radii: from gm_project_gaussians.  tile_far / tile_full: from
  *   gm_interp_mesh (read only when cull_occluded).
  *   keys [cap] u64 out, gids [cap] i32 out, tile_range [T][2] i32 out.

@@ -78,9 +78,9 @@ def run_project(cam, g, bg=(1, 1, 1)):
     return host(splats), host(radii), host(touched)
 
 
-def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=None, sync=True):
+def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=None, sync=True, tile_test=False):
     c = gm.make_camera(cam)
-    o = gm.make_opts((1, 1, 1), cull, -1)
+    o = gm.make_opts((1, 1, 1), cull, -1, tile_test)
     N = len(radii)
     T = n_tiles(cam)
     tf = dev(np.full(T, np.inf, np.float32) if tile_far is None else tile_far, torch.float32)

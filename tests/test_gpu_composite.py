@@ -87,6 +87,26 @@ def test_cull_changes_nothing(run):
         assert r["bins"]["K"] < b0["K"]
 
 
+def test_tile_test_changes_nothing(run):
+    """The opts.tile_test bins (unreachable tiles dropped) give a bit-identical
+    image, depth, alpha and transmittance, and the same gradients up to the
+    order of the atomic sums."""
+    name, s, r = run
+    cam, m = r["cam"], r["mesh"]
+    b1 = H.run_bin(cam, r["splats"], r["radii"], m["tile_far"], m["tile_full"], cull=True, tile_test=True)
+    f1 = H.run_composite(cam, s.bg, b1["tile_range"], b1["gids"], r["splats"], m["mesh_depth"], m["mesh_rgb"],
+                         m["face_id"])
+    f0 = r["fwd"]
+    for k in ("rgb", "depth", "alpha", "T"):
+        np.testing.assert_array_equal(f0[k], f1[k])
+    grads = scenes.upstream_grads(11, cam.width, cam.height)
+    N = len(r["radii"])
+    g0 = H.run_composite_bwd(cam, s.bg, f0, grads, N)["v_splats"]
+    g1 = H.run_composite_bwd(cam, s.bg, f1, grads, N)["v_splats"]
+    np.testing.assert_allclose(g1, g0, rtol=1e-5, atol=1e-6 * max(1.0, float(np.abs(g0).max())))
+    print("%s: K %d -> %d with the tile test" % (name, r["bins"]["K"], b1["K"]))
+
+
 def _fd_requests(rng, radii, n_gauss, fields=range(10)):
     vis = np.nonzero(radii > 0)[0]
     pick = vis if len(vis) <= n_gauss else np.sort(rng.choice(vis, n_gauss, replace=False))

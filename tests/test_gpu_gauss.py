@@ -178,8 +178,72 @@ def test_capacity_overflow_is_reported_and_contained(orc):
     tr = torch.zeros(H.n_tiles(s.camera), 2, dtype=torch.int32, device="cuda")
     cnt = torch.zeros(4, dtype=torch.int32, device="cuda")
     ws = torch.empty(gm.gm_bin_sort_gaussians_workspace_size(len(rad), cap, 64, 64), dtype=torch.uint8, device="cuda")
-    gm.gm_bin_sort_gaussians(gm.make_camera(s.camera), gm.make_opts(cull_occluded=False), H.dev(sp), H.dev(rad),
+    gm.gm_bin_sort_gaussians(gm.make_camera(s.camera), gm.make_opts(cull_occluded=False, tile_test=False), H.dev(sp), H.dev(rad),
                              None, None, keys, gids, tr, cap, cnt, ws, sync=False)
     c = H.host(cnt)
     assert c[0] == need and c[2] & gm.GM_FLAG_OVERFLOW
     assert np.all(H.host(gids)[cap:] == -1) and np.all(H.host(keys)[cap:] == 0)
+
+
+def _tile_test_cases():
+    soup = scenes.soup1080(n_gauss=150_000, n_tri=30_000)
+    cam = scenes.look_at((0, 0, 6), (0, 0, 0), 480, 272, 300, 300)
+    return [("tiny", scenes.tiny()), ("sphere512", scenes.sphere512()),
+            ("soup_small", scenes.Scene(soup.name, [cam], soup.mesh, soup.gaussians, soup.bg))]
+
+
+@pytest.mark.parametrize("case", _tile_test_cases(), ids=lambda c: c[0])
+def test_tile_test_drops_only_unreachable_pairs(case, orc):
+    """With opts.tile_test each tile's list is the exact rectangle list with some
+    entries removed, in the same order, and every removed (Gaussian, tile) pair
+    is one whose alpha stays below 1/255 at every pixel centre of the tile
+    (checked in double from the oracle's projection), so compositing cannot
+    change."""
+    H.need_gpu()
+    name, s = case
+    cam = s.camera
+    sp, rad, _ = H.run_project(cam, s.gaussians)
+    m = H.run_mesh(cam, s.mesh)
+    ex = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull=True)
+    ti = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull=True, tile_test=True)
+    assert ti["K"] <= ex["K"]
+    T = H.n_tiles(cam)
+    TW = (cam.width + 15) // 16
+    dropped_g, dropped_t = [], []
+    for t in range(T):
+        a0, a1 = ex["tile_range"][t]
+        b0, b1 = ti["tile_range"][t]
+        le = ex["gids"][a0:a1] if a1 > a0 else np.zeros(0, np.int32)
+        lt = ti["gids"][b0:b1] if b1 > b0 else np.zeros(0, np.int32)
+        keep = np.isin(le, lt)
+        np.testing.assert_array_equal(le[keep], lt)  # same order, nothing new
+        dropped_g.append(le[~keep])
+        dropped_t.append(np.full((~keep).sum(), t))
+    dg = np.concatenate(dropped_g)
+    dt = np.concatenate(dropped_t)
+    osp, _, _, _ = orc.project(cam, s.gaussians)
+    rng = np.random.default_rng(2)
+    if len(dg) > 20000:
+        sel = rng.choice(len(dg), 20000, replace=False)
+        dg, dt = dg[sel], dt[sel]
+    # max over the tile's in-image pixel centres of o exp(-sigma), in double
+    off = np.arange(16) + 0.5
+    worst = 0.0
+    for lo in range(0, len(dg), 4096):
+        g, t = dg[lo:lo + 4096], dt[lo:lo + 4096]
+        rec = osp[g].astype(np.float64)
+        tx, ty = (t % TW) * 16, (t // TW) * 16
+        xs = tx[:, None] + off[None, :]
+        ys = ty[:, None] + off[None, :]
+        dx = xs[:, None, :] - rec[:, 0, None, None]
+        dy = ys[:, :, None] - rec[:, 1, None, None]
+        sig = 0.5 * (rec[:, 2, None, None] * dx * dx + rec[:, 4, None, None] * dy * dy) + rec[:, 3, None, None] * dx * dy
+        inside = (xs[:, None, :] < cam.width) & (ys[:, :, None] < cam.height)
+        a = rec[:, 5, None, None] * np.exp(-np.maximum(sig, 0.0))
+        a = np.where(inside & (sig >= 0), a, 0.0)
+        worst = max(worst, float(a.max()) if a.size else 0.0)
+    print("%s: K %d -> %d (%.1f %% dropped); largest alpha of a dropped pair %.3g" % (
+        name, ex["K"], ti["K"], 100.0 * (1 - ti["K"] / max(ex["K"], 1)), worst))
+    assert worst < 1.0 / 255.0
+    if name == "soup_small":
+        assert ti["K"] < 0.9 * ex["K"]
