@@ -157,10 +157,10 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 PROFILED_TRAFFIC = {
     "composite_bwd": {
         "kernel": "k_composite_bwd",
-        "bytes": 169306880 + 12965632,
+        "bytes": 160724992 + 11533312,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "72046edb8317098c221ae514a3376a1970f74495ace6085b5e5882b06e1e58f9",
+                "6830216f1bf4844931d28e37435aeb645848e4fdba96c2b25f2c3212e818e284",
         },
         "profile": "profiles/composite_bwd_soup_1080p.md",
     },

@@ -246,22 +246,69 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
 constexpr int NGRAD = 10;
 constexpr int GROUP = 4;
 
-// Sums v[0..3] (one value per entry of a group of four) over the warp and
-// leaves in every lane the total of entry 2 bit4(lane) + bit3(lane): two
-// halving exchanges (xor 16, xor 8), then a butterfly over xor 4, 2, 1 --
-// six shuffles for four entries instead of five per entry.
-__device__ __forceinline__ float reduce_scatter4(const float v[GROUP], int lane)
+// One level of a reduce-scatter over the lanes xor o: of each pair of values
+// (a, b) the lane keeps the one its bit o selects and adds its partner's copy
+// of it.
+__device__ __forceinline__ float rs_combine(float a, float b, int lane, int o)
 {
-    const bool hi16 = lane & 16, hi8 = lane & 8;
-    const float keep0 = hi16 ? v[2] : v[0], keep1 = hi16 ? v[3] : v[1];
-    const float send0 = hi16 ? v[0] : v[2], send1 = hi16 ? v[1] : v[3];
-    const float b0 = keep0 + __shfl_xor_sync(0xffffffffu, send0, 16);
-    const float b1 = keep1 + __shfl_xor_sync(0xffffffffu, send1, 16);
-    float x = (hi8 ? b1 : b0) + __shfl_xor_sync(0xffffffffu, hi8 ? b0 : b1, 8);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    return x;
+    const bool hi = lane & o;
+    return (hi ? b : a) + __shfl_xor_sync(0xffffffffu, hi ? a : b, o);
+}
+
+// The per-lane gradient terms of a group of four entries: 40 values, value i
+// < 32 is component i >> 2 of entry i & 3 (0 ds dx, 1 ds dy, 2 ds dx^2 / 2,
+// 3 ds dx dy, 4 ds dy^2 / 2, 5 dL/d opacity, 6 w g_r, 7 w g_g), value 32 + i
+// is component 8 + (i >> 2) (w g_b, w g_depth) of entry i & 3.
+struct GroupTerms {
+    float pw[GROUP], pvo[GROUP], pds[GROUP], pdx[GROUP], pdy[GROUP];
+    float gr, gg, gb, gz;
+    __device__ __forceinline__ float v(int i) const
+    {
+        const int q = i < 32 ? i >> 2 : 8 + ((i - 32) >> 2), e = i & 3;
+        switch (q) {
+            case 0: return pds[e] * pdx[e];
+            case 1: return pds[e] * pdy[e];
+            case 2: return 0.5f * pds[e] * pdx[e] * pdx[e];
+            case 3: return pds[e] * pdx[e] * pdy[e];
+            case 4: return 0.5f * pds[e] * pdy[e] * pdy[e];
+            case 5: return pvo[e];
+            case 6: return pw[e] * gr;
+            case 7: return pw[e] * gg;
+            case 8: return pw[e] * gb;
+            default: return pw[e] * gz;
+        }
+    }
+};
+
+// Reduce-scatter of values 0..31 over the warp: lane L ends with the warp sum
+// of value L (levels xor 16, 8, 4, 2, 1; 31 shuffles).  Node I of level L
+// combines nodes I and I + 32 / 2^L of level L - 1; the tree is walked depth
+// first so that few partial sums are live at once.
+template <int L, int I>
+__device__ __forceinline__ float rs32(const GroupTerms& g, int lane)
+{
+    if constexpr (L == 0) {
+        return g.v(I);
+    } else {
+        const float a = rs32<L - 1, I>(g, lane);
+        const float b = rs32<L - 1, I + (32 >> L)>(g, lane);
+        return rs_combine(a, b, lane, 16 >> (L - 1));
+    }
+}
+
+// Values 32..39 over levels xor 16, 8, 4: lane L ends with the sum over its
+// eight-lane orbit of value 32 + ((L >> 2) & 7); a butterfly over xor 2, 1
+// completes the warp sum.
+template <int L, int I>
+__device__ __forceinline__ float rs8(const GroupTerms& g, int lane)
+{
+    if constexpr (L == 0) {
+        return g.v(32 + I);
+    } else {
+        const float a = rs8<L - 1, I>(g, lane);
+        const float b = rs8<L - 1, I + (8 >> L)>(g, lane);
+        return rs_combine(a, b, lane, 16 >> (L - 1));
+    }
 }
 
 // Adds a staged entry's accumulated gradient (components 0..9 of the record
@@ -326,7 +373,6 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     const int2 r = tile_range[tile];
     const int end = r.x + s_max_last;
     uint32_t visited = 0, contributed = 0;
-    const int my_entry = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
     int n_prev = 0;
     for (int b_end = end;; b_end -= CTA_THREADS) {
         // the previous batch's gradients go out and the next batch comes in, each
@@ -397,52 +443,41 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                     }
                 }
                 if (__any_sync(0xffffffffu, any)) {
-                    const int k = my_entry == 0 ? kj[0] : my_entry == 1 ? kj[1] : my_entry == 2 ? kj[2] : kj[3];
-                    const int sub = lane & 7;
-                    // reduced per entry: Sx = sum ds dx, Sy = sum ds dy, the three conic
-                    // terms, opacity, rgb and depth; the mean gradient follows from Sx, Sy:
+                    // the ten gradient components of the four entries summed over the
+                    // warp by one reduce-scatter of 40 values (41 shuffles); the mean
+                    // gradient follows from Sx = sum ds dx, Sy = sum ds dy:
                     // d sigma / d mean = -(a dx + b dy, b dx + c dy) with a = -2 a2 / log2e,
                     // b = -b2 / log2e, c = -2 c2 / log2e
-                    float sx = 0.0f, sy = 0.0f;
-                    // pixel offsets recomputed here (the same roundings as eval_splat)
-                    // rather than kept live through the group: fewer registers
-                    float pdx[GROUP], pdy[GROUP];
+                    GroupTerms gt;
 #pragma unroll
                     for (int jj = 0; jj < GROUP; ++jj) {
+                        gt.pw[jj] = pw[jj];
+                        gt.pvo[jj] = pvo[jj];
+                        gt.pds[jj] = pds[jj];
+                        // pixel offsets recomputed (the same roundings as eval_splat)
+                        // rather than kept live through the group: fewer registers
                         const float2 mean = *reinterpret_cast<const float2*>(&sA[kj[jj] < 0 ? 0 : kj[jj]]);
-                        pdx[jj] = __fsub_rn(px, mean.x);
-                        pdy[jj] = __fsub_rn(py, mean.y);
+                        gt.pdx[jj] = __fsub_rn(px, mean.x);
+                        gt.pdy[jj] = __fsub_rn(py, mean.y);
                     }
-#pragma unroll
-                    for (int q = 0; q < NGRAD; ++q) {
-                        float col[GROUP];
-#pragma unroll
-                        for (int jj = 0; jj < GROUP; ++jj) {
-                            const float ds = pds[jj], dx = pdx[jj], dy = pdy[jj];
-                            col[jj] = q == 0 ? ds * dx
-                                    : q == 1 ? ds * dy
-                                    : q == 2 ? 0.5f * ds * dx * dx
-                                    : q == 3 ? ds * dx * dy
-                                    : q == 4 ? 0.5f * ds * dy * dy
-                                    : q == 5 ? pvo[jj]
-                                    : pw[jj] * (q == 6 ? gr : q == 7 ? gg : q == 8 ? gb : gz);
-                        }
-                        const float sum = reduce_scatter4(col, lane);
-                        if (q == 0) {
-                            sx = sum;
-                        } else if (q == 1) {
-                            sy = sum;
-                        } else if (k >= 0 && sub == (q & 7) && (q < 8 || sub < 2) && sum != 0.0f) {
-                            // lane sub of the entry's eight lanes adds component sub (and sub + 8)
-                            atomicAdd(&sAcc[k][q], sum);
-                        }
-                    }
-                    if (k >= 0 && sub < 2) {
+                    gt.gr = gr; gt.gg = gg; gt.gb = gb; gt.gz = gz;
+                    float tot = rs32<5, 0>(gt, lane);  // component lane >> 2 of entry lane & 3
+                    const int q = lane >> 2, e = lane & 3;
+                    const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
+                    const float other = __shfl_xor_sync(0xffffffffu, tot, 4);  // Sx <-> Sy of the entry
+                    if (q < 2 && k >= 0) {
                         const float a2 = sA[k].z, b2 = sA[k].w, c2 = sB[k].x;
-                        const float tx = sx * (1.0f / LOG2E), ty = sy * (1.0f / LOG2E);
-                        const float mg = sub == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
-                        if (mg != 0.0f) atomicAdd(&sAcc[k][sub], mg);
+                        const float tx = (q == 0 ? tot : other) * (1.0f / LOG2E);
+                        const float ty = (q == 0 ? other : tot) * (1.0f / LOG2E);
+                        tot = q == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
                     }
+                    if (k >= 0 && tot != 0.0f) atomicAdd(&sAcc[k][q], tot);
+                    float t8 = rs8<3, 0>(gt, lane);
+                    t8 += __shfl_xor_sync(0xffffffffu, t8, 2);
+                    t8 += __shfl_xor_sync(0xffffffffu, t8, 1);
+                    const int j = (lane >> 2) & 7, e8 = j & 3;
+                    const int k8 = e8 == 0 ? kj[0] : e8 == 1 ? kj[1] : e8 == 2 ? kj[2] : kj[3];
+                    if ((lane & 3) == 0 && k8 >= 0 && t8 != 0.0f) atomicAdd(&sAcc[k8][8 + (j >> 2)], t8);
                 }
             }
         }
