@@ -210,8 +210,11 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
               int32_t* __restrict__ dval, int32_t* n_dev, int32_t* counters)
 {
     __shared__ int s_pre[8];
+    __shared__ BinShape s_shape[256];
+    __shared__ int4 s_rect[256];  // x0, y0, width, -
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
+    const int wbase = threadIdx.x & ~31;
     if (g == 0) *n_dev = N;
     int pre = 0, post = 0;
     uint32_t mask = 0;
@@ -228,15 +231,46 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
         post = pre;
         mask = 0xffffffffu;
     } else {
-        if (pre <= SMALL_RECT) {
-            int i = 0;
-            for (int ty = y0; ty < y1; ++ty)
-                for (int tx = x0; tx < x1; ++tx, ++i)
-                    if (keep_tile(rule, sh, tx, ty)) {
-                        mask |= 1u << i;
-                        ++post;
-                    }
+        // the (Gaussian, tile) pairs of the warp's small rectangles, flattened so
+        // that each lane tests one pair per round whatever the rectangle sizes
+        const int a = pre <= SMALL_RECT ? pre : 0;
+        int o = a;  // inclusive prefix sum over the lanes
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, o, d);
+            if (lane >= d) o += y;
         }
+        const int total = __shfl_sync(0xffffffffu, o, 31);
+        o -= a;  // exclusive
+        s_shape[threadIdx.x] = sh;
+        s_rect[threadIdx.x] = make_int4(x0, y0, x1 - x0, 0);
+        __syncwarp();
+        for (int base = 0; base < total; base += 32) {
+            const int p = base + lane;
+            // owner of pair p: the last lane whose first pair is at or before p (all
+            // lanes take part in the search; lanes past the last pair test nothing)
+            int j = 0;
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1) {
+                const int oj = __shfl_sync(0xffffffffu, o, j + step);
+                if (oj <= p) j += step;
+            }
+            const int oj = __shfl_sync(0xffffffffu, o, j);
+            bool keep = false;
+            if (p < total) {
+                const int4 rc = s_rect[wbase + j];
+                const int t_in = p - oj;
+                keep = keep_tile(rule, s_shape[wbase + j], rc.x + t_in % rc.z, rc.y + t_in / rc.z);
+            }
+            const uint32_t km = __ballot_sync(0xffffffffu, keep);
+            // this lane's own pairs in the round: positions [lo, hi) of km
+            const int lo = max(o, base) - base, hi = min(o + a, base + 32) - base;
+            if (lo < hi) {
+                const uint32_t bits = (hi - lo == 32 ? km : (km >> lo) & ((1u << (hi - lo)) - 1u));
+                mask |= bits << (lo + base - o);
+            }
+        }
+        post = __popc(mask);
         uint32_t big = __ballot_sync(0xffffffffu, pre > SMALL_RECT);
         while (big) {
             const int j = __ffs(big) - 1;
@@ -279,35 +313,78 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
              const uint32_t* __restrict__ kept, const int32_t* __restrict__ offsets, int cap, int32_t* counters,
              uint64_t* __restrict__ keys, int32_t* __restrict__ vals)
 {
+    __shared__ int4 s_a[256];   // x0, y0, width, Gaussian id
+    __shared__ int2 s_b[256];   // depth bits, first output slot
+    __shared__ uint32_t s_m[256];
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
+    const int wbase = threadIdx.x & ~31;
     if (i == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
     int g = -1, x0 = 0, y0 = 0, x1 = 0, y1 = 0, area = 0;
     BinShape sh = {};
     uint32_t mask = 0;
     int64_t o = 0;
+    float depth = 0.0f;
     if (i < N) {
         g = order[i];
         if (g >= 0 && g < N && counts[g] > 0) {
-            sh = bin_shape(splats, g);
-            if (gauss_rect(c, sh.mx, sh.my, radii[g], x0, y0, x1, y1)) area = (x1 - x0) * (y1 - y0);
+            const float4 s0 = splats[3 * (int64_t)g];
+            depth = splats[3 * (int64_t)g + 2].y;
+            if (gauss_rect(c, s0.x, s0.y, radii[g], x0, y0, x1, y1)) area = (x1 - x0) * (y1 - y0);
             o = offsets[i];
             mask = kept[g];
+            if (area > SMALL_RECT) sh = bin_shape(splats, g);  // the big-rectangle path tests again
         }
     }
-    const uint32_t dbits = __float_as_uint(sh.depth);
-    if (area > 0 && area <= SMALL_RECT) {
-        // the tiles k_gauss_count kept, one bit each in row-major rectangle order
-        int k = 0;
-        for (int ty = y0; ty < y1; ++ty)
-            for (int tx = x0; tx < x1; ++tx, ++k) {
-                if (!((mask >> k) & 1u)) continue;
-                if (o >= 0 && o < cap) {
-                    keys[o] = ((uint64_t)(uint32_t)(ty * c.TW + tx) << 32) | dbits;
-                    vals[o] = g;
-                }
-                ++o;
+    const uint32_t dbits = __float_as_uint(depth);
+    {
+        // the kept tiles of the warp's small rectangles, flattened: one entry per
+        // lane per round, consecutive lanes writing consecutive slots
+        const uint32_t m = (area > 0 && area <= SMALL_RECT) ? mask & ((1u << area) - 1u) : 0u;
+        const int a = __popc(m);
+        int p0 = a;  // inclusive prefix sum over the lanes
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, p0, d);
+            if (lane >= d) p0 += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, p0, 31);
+        p0 -= a;
+        s_a[threadIdx.x] = make_int4(x0, y0, x1 - x0, g);
+        s_b[threadIdx.x] = make_int2((int)dbits, (int)o);
+        s_m[threadIdx.x] = m;
+        __syncwarp();
+        for (int base = 0; base < total; base += 32) {
+            const int p = base + lane;
+            int j = 0;
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1) {
+                const int pj = __shfl_sync(0xffffffffu, p0, j + step);
+                if (pj <= p) j += step;
             }
+            const int pj = __shfl_sync(0xffffffffu, p0, j);
+            if (p < total) {
+                const int r = p - pj;  // the r-th kept tile of lane j's rectangle
+                const uint32_t mj = s_m[wbase + j];
+                int pos = 0, rr = r;
+#pragma unroll
+                for (int st = 8; st > 0; st >>= 1) {
+                    const int cnt = __popc((mj >> pos) & ((1u << st) - 1u));
+                    if (cnt <= rr) {
+                        rr -= cnt;
+                        pos += st;
+                    }
+                }
+                const int4 ra = s_a[wbase + j];
+                const int2 rb = s_b[wbase + j];
+                const int64_t dst = (int64_t)rb.y + r;
+                if (dst >= 0 && dst < cap) {
+                    const int t = (ra.y + pos / ra.z) * c.TW + ra.x + pos % ra.z;
+                    keys[dst] = ((uint64_t)(uint32_t)t << 32) | (uint32_t)rb.x;
+                    vals[dst] = ra.w;
+                }
+            }
+        }
     }
     uint32_t big = __ballot_sync(0xffffffffu, area > SMALL_RECT);
     while (big) {
