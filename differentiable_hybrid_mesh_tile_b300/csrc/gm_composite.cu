@@ -193,32 +193,51 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
             uint32_t mask =
                 __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0));
             while (mask) {
-                const int k = m * 32 + __ffs(mask) - 1;
+                // two hits at a time: both evaluated (independent) before the
+                // transmittance chain takes them in list order
+                int kk2[2];
+                kk2[0] = m * 32 + __ffs(mask) - 1;
                 mask &= mask - 1;
+                kk2[1] = -1;
+                if (mask) {
+                    kk2[1] = m * 32 + __ffs(mask) - 1;
+                    mask &= mask - 1;
+                }
                 if (done) continue;
-                const float4 C3 = sC[k];
-                // sorted by depth: once a Gaussian is not in front of the mesh, none after it is
-                if (!(C3.y < D)) {
-                    done = true;
-                    continue;
+                float4 Cq[2], Bq[2];
+                Eval ev[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int k = kk2[h] < 0 ? kk2[0] : kk2[h];
+                    Cq[h] = sC[k];
+                    const float4 A = sA[k];
+                    Bq[h] = sB[k];
+                    ev[h] = eval_splat(A, Bq[h], px, py);
                 }
-                if (STATS) ++visited;
-                const float4 A = sA[k], B = sB[k];
-                const Eval e = eval_splat(A, B, px, py);
-                if (e.skip) continue;
-                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, e.alpha));
-                if (Tn <= T_STOP) {
-                    done = true;
-                    continue;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (done || kk2[h] < 0) continue;
+                    // sorted by depth: once a Gaussian is not in front of the mesh, none after it is
+                    if (!(Cq[h].y < D)) {
+                        done = true;
+                        continue;
+                    }
+                    if (STATS) ++visited;
+                    if (ev[h].skip) continue;
+                    const float Tn = __fmul_rn(T, __fsub_rn(1.0f, ev[h].alpha));
+                    if (Tn <= T_STOP) {
+                        done = true;
+                        continue;
+                    }
+                    const float w = ev[h].alpha * T;
+                    Cr = fmaf(w, Bq[h].z, Cr);
+                    Cg = fmaf(w, Bq[h].w, Cg);
+                    Cb = fmaf(w, Cq[h].x, Cb);
+                    Z = fmaf(w, Cq[h].y, Z);
+                    T = Tn;
+                    last = b - r.x + kk2[h] + 1;
+                    if (STATS) ++blended;
                 }
-                const float w = e.alpha * T;
-                Cr = fmaf(w, B.z, Cr);
-                Cg = fmaf(w, B.w, Cg);
-                Cb = fmaf(w, C3.x, Cb);
-                Z = fmaf(w, C3.y, Z);
-                T = Tn;
-                last = b - r.x + k + 1;
-                if (STATS) ++blended;
             }
         }
     }

@@ -196,6 +196,16 @@ __device__ __forceinline__ bool keep_tile(const BinRule& r, const BinShape& s, i
     return !r.tile_test || tile_min_sigma(s, tx, ty) <= s.smax;
 }
 
+// q = t / w and r = t % w for 0 <= t < 2^21 and w >= 1 with one fp32 multiply:
+// (t + 0.5) / w lies at least 0.5 / w from every integer, far more than the
+// rounding error of (t + 0.5) * rn(1 / w).  (Integer division by a variable
+// costs tens of instructions.)
+__device__ __forceinline__ void divmod_small(int t, int w, float inv_w, int& q, int& r)
+{
+    q = t < (1 << 21) ? (int)(((float)t + 0.5f) * inv_w) : t / w;
+    r = t - q * w;
+}
+
 // Rectangles up to this many tiles are walked by their own thread; larger ones
 // (near-camera Gaussians) by the whole warp, 32 tiles at a time, so one large
 // Gaussian does not hold up the other 31 lanes.
@@ -243,7 +253,7 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
         const int total = __shfl_sync(0xffffffffu, o, 31);
         o -= a;  // exclusive
         s_shape[threadIdx.x] = sh;
-        s_rect[threadIdx.x] = make_int4(x0, y0, x1 - x0, 0);
+        s_rect[threadIdx.x] = make_int4(x0, y0, x1 - x0, __float_as_int(__frcp_rn((float)max(x1 - x0, 1))));
         __syncwarp();
         for (int base = 0; base < total; base += 32) {
             const int p = base + lane;
@@ -260,7 +270,9 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
             if (p < total) {
                 const int4 rc = s_rect[wbase + j];
                 const int t_in = p - oj;
-                keep = keep_tile(rule, s_shape[wbase + j], rc.x + t_in % rc.z, rc.y + t_in / rc.z);
+                int row, col;
+                divmod_small(t_in, rc.z, __int_as_float(rc.w), row, col);
+                keep = keep_tile(rule, s_shape[wbase + j], rc.x + col, rc.y + row);
             }
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
             // this lane's own pairs in the round: positions [lo, hi) of km
@@ -278,8 +290,13 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
             const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
             const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, pre, j);
             const BinShape js = shfl_shape(sh, j);
+            const float jinv = __frcp_rn((float)jw);
             int cnt = 0;
-            for (int t = lane; t < jarea; t += 32) cnt += keep_tile(rule, js, jx0 + t % jw, jy0 + t / jw);
+            for (int t = lane; t < jarea; t += 32) {
+                int row, col;
+                divmod_small(t, jw, jinv, row, col);
+                cnt += keep_tile(rule, js, jx0 + col, jy0 + row);
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
             if (lane == j) post = cnt;
@@ -379,7 +396,9 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
                 const int2 rb = s_b[wbase + j];
                 const int64_t dst = (int64_t)rb.y + r;
                 if (dst >= 0 && dst < cap) {
-                    const int t = (ra.y + pos / ra.z) * c.TW + ra.x + pos % ra.z;
+                    int row, col;
+                    divmod_small(pos, ra.z, __frcp_rn((float)ra.z), row, col);
+                    const int t = (ra.y + row) * c.TW + ra.x + col;
                     keys[dst] = ((uint64_t)(uint32_t)t << 32) | (uint32_t)rb.x;
                     vals[dst] = ra.w;
                 }
@@ -395,14 +414,17 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
         const int jg = __shfl_sync(0xffffffffu, g, j);
         const BinShape js = shfl_shape(sh, j);
         const uint32_t jbits = __float_as_uint(js.depth);
+        const float jinv = __frcp_rn((float)jw);
         int64_t jo = __shfl_sync(0xffffffffu, o, j);
         for (int base = 0; base < jarea; base += 32) {
             const int t_in = base + lane;
             int tx = 0, ty = 0;
             bool keep = false;
             if (t_in < jarea) {
-                tx = jx0 + t_in % jw;
-                ty = jy0 + t_in / jw;
+                int row, col;
+                divmod_small(t_in, jw, jinv, row, col);
+                tx = jx0 + col;
+                ty = jy0 + row;
                 keep = keep_tile(rule, js, tx, ty);
             }
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
