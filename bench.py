@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--config", default="soup_1080p")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-multiview", action="store_true", help="skip the batched 8-view measurement")
     ap.add_argument("--cpu-tiles", type=int, default=48, help="tiles of the frame the CPU oracle renders")
     return ap.parse_args()
 
@@ -409,11 +410,86 @@ def run_gm(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, r, scene, grads_np, flush, ws, dist)
+    multiview = None
+    if not args.no_multiview:
+        del graph, fgraph
+        multiview = run_multiview(args, flush, dist)
 
     return dict(value=value, fwd=fwd_value, ms_step=ms_step, ms_fwd=ms_fwd, ms_eager=ms_eager, stages=stages, roofline=roof,
                 clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_tri=K_tri, K_g=K_g, K_pre=K_pre,
+                multiview=multiview,
                 pairs_f=pairs_f, pairs_b=pairs_b, blend_f=blend_f, blend_b=blend_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
                 gpu_name=props.name)
+
+
+def run_multiview(args, flush, dist):
+    """The 8-view orbit workload (3M Gaussians SH3, 8 x 1920x1080) as one batch
+    (MultiViewRenderer: batched projection and projection backward, per-view
+    steps on parallel streams, one CUDA graph), against the same 8 views
+    rendered one after another by single-view graph steps.  Both include the
+    projection backward (the parameter gradients summed over the views)."""
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    from differentiable_hybrid_mesh_tile_b300 import scenes
+    sc = scenes.make("orbit_8x1080p")
+    cams = sc.cameras
+    steps = max(3, min(args.steps, 20))
+    grads = [[torch.as_tensor(x).cuda() for x in scenes.upstream_grads(k, c.width, c.height)]
+             for k, c in enumerate(cams)]
+    mv = gm.MultiViewRenderer(cams, bg=sc.bg)
+    mv.upload(sc.mesh, sc.gaussians)
+    graph = mv.capture_step(grads)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 2)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        stream = torch.cuda.current_stream()
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.mean(ts))
+
+    ms_batch = timed(graph.replay)
+    overflow = mv.overflowed()
+    del graph
+    # the same views one at a time: a single-view graph step each, plus the
+    # projection backward of that view accumulated into the parameter gradients
+    singles = []
+    for k, c in enumerate(cams):
+        r = gm.HybridRenderer(c, bg=sc.bg)
+        r.upload(sc.mesh, sc.gaussians)
+        r.forward(sync=True)
+        g = r.capture_step(*grads[k])
+        singles.append((r, g))
+    pb = [torch.zeros_like(x) for x in (singles[0][0].means, singles[0][0].log_scales, singles[0][0].quats,
+                                         singles[0][0].logits, singles[0][0].colors)]
+
+    def sequential():
+        for k, (r, g) in enumerate(singles):
+            g.replay()
+            gm.gm_project_gaussians_bwd(r.cam, r.opts, r.means, r.log_scales, r.quats, r.logits, r.colors, r.radii,
+                                        r.v_splats, *pb, accumulate=k > 0)
+
+    ms_seq = timed(sequential)
+    overflow = overflow or any(r.overflowed() for r, _ in singles)
+    ms_batch, ms_seq = max_over_ranks([ms_batch, ms_seq], dist, "cuda")
+    px = sum(c.width * c.height for c in cams)
+    g = sc.gaussians
+    return {"workload": "orbit_8x1080p: 8 views of 1920x1080 on a radius-5 orbit, %d-triangle icosphere, %d "
+                        "Gaussians (SH degree %d), forward + backward of all views + projection backward"
+                        % (len(sc.mesh.faces), len(g.means), g.sh_degree),
+            "views": len(cams), "steps": steps, "ms_per_step": ms_batch, "mpix_s": px / 1e6 / (ms_batch / 1e3),
+            "sequential_ms_per_step": ms_seq, "sequential_mpix_s": px / 1e6 / (ms_seq / 1e3),
+            "overflow": overflow}
 
 
 def run_e2e(args, r, scene, grads_np, flush, ws, dist):
@@ -559,6 +635,7 @@ def main():
                        res["K_pre"], "pairs_evaluated_fwd": res["pairs_f"], "pairs_composited_fwd": res["blend_f"],
                        "pairs_evaluated_bwd": res["pairs_b"], "pairs_composited_bwd": res["blend_b"]},
             "overflow": res["overflow"], "gpu": res["gpu_name"], "wall_s_timed": res["wall"],
+            "multiview": res["multiview"],
         }
         print(json.dumps(line))
     if dist is not None:

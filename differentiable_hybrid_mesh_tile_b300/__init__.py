@@ -60,6 +60,8 @@ _SIGS = {
     "gm_interp_mesh": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "gm_project_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "gm_project_gaussians_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 7 + [_I32] + [_VP] * 6),
+    "gm_project_gaussians_views": (C.c_int, [_VP, _I32, _VP, _I32] + [_VP] * 8 + [_VP]),
+    "gm_project_gaussians_bwd_views": (C.c_int, [_VP, _I32, _VP, _I32] + [_VP] * 7 + [_I32] + [_VP] * 6),
     "gm_bin_sort_gaussians_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
     "gm_bin_sort_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
                                         C.c_size_t, _VP]),
@@ -193,6 +195,34 @@ def gm_project_gaussians(cam: gm_camera, opts: gm_opts, means, log_scales, quats
                                       _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
                                       _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32), _stream()),
            "gm_project_gaussians")
+
+
+def _cam_array(cams):
+    arr = (gm_camera * len(cams))()
+    for k, c in enumerate(cams):
+        arr[k] = c
+    return arr
+
+
+def gm_project_gaussians_views(cams, opts: gm_opts, means, log_scales, quats, logits, colors, splats, radii,
+                               tiles_touched):
+    """cams: a list of gm_camera; splats [V][N][12], radii / tiles_touched [V][N]."""
+    arr = _cam_array(cams)
+    _check(lib().gm_project_gaussians_views(arr, len(cams), C.byref(opts), means.shape[0], _p(means, F32),
+                                            _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
+                                            _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32), _stream()),
+           "gm_project_gaussians_views")
+
+
+def gm_project_gaussians_bwd_views(cams, opts: gm_opts, means, log_scales, quats, logits, colors, radii, v_splats,
+                                   v_means, v_log_scales, v_quats, v_logits, v_colors, accumulate=False):
+    arr = _cam_array(cams)
+    _check(lib().gm_project_gaussians_bwd_views(arr, len(cams), C.byref(opts), means.shape[0], _p(means, F32),
+                                                _p(log_scales, F32), _p(quats, F32), _p(logits, F32),
+                                                _p(colors, F32), _p(radii, I32), _p(v_splats, F32),
+                                                int(bool(accumulate)), _p(v_means, F32), _p(v_log_scales, F32),
+                                                _p(v_quats, F32), _p(v_logits, F32), _p(v_colors, F32), _stream()),
+           "gm_project_gaussians_bwd_views")
 
 
 def gm_project_gaussians_bwd(cam: gm_camera, opts: gm_opts, means, log_scales, quats, logits, colors, radii,
@@ -442,3 +472,144 @@ class HybridRenderer:
     def overflowed(self) -> bool:
         f = int(self.tri_counters[GM_CNT_FLAGS].item()) | int(self.g_counters[GM_CNT_FLAGS].item())
         return bool(f & (GM_FLAG_OVERFLOW | GM_FLAG_TIMEOUT))
+
+
+class MultiViewRenderer:
+    """Several cameras of one scene rendered and differentiated as one batch.
+
+    The projection and its backward run once for all views
+    (``gm_project_gaussians_views`` / ``_bwd_views``); each view's binning,
+    z-buffer, interpolation and compositing run on one of ``streams`` CUDA
+    streams, so the views overlap on the GPU.  ``backward`` sums the Gaussian
+    parameter gradients over the views (in view order) and accumulates the
+    mesh gradients of all views; ``capture_step`` records the whole batch as
+    one CUDA graph.  Per-view buffers are those of one ``HybridRenderer`` per
+    camera (``views[k]``), whose ``splats`` / ``radii`` / ``v_splats`` are
+    slices of the batch arrays.
+    """
+
+    def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4):
+        self.views = [HybridRenderer(c, bg=bg, cull_occluded=cull_occluded, device=device, concurrent=False,
+                                     tile_test=tile_test) for c in cams]
+        self.V = len(self.views)
+        self.dev = torch.device(device)
+        self.n_streams = max(1, min(int(streams), self.V))
+        self._streams = None
+
+    @property
+    def cams(self):
+        return [v.cam for v in self.views]
+
+    @property
+    def opts(self) -> gm_opts:
+        return self.views[0].opts
+
+    def _pool(self):
+        if self._streams is None:
+            self._streams = [torch.cuda.Stream(device=self.dev) for _ in range(self.n_streams)]
+        return self._streams
+
+    def upload(self, mesh, gaussians):
+        """Copies the scene once; sizes every view's tile-entry buffers with one
+        synchronous forward pass per view."""
+        v0 = self.views[0]
+        v0.upload(mesh, gaussians)
+        N, d = v0.N, self.dev
+        self.N = N
+        self.splats = torch.zeros(self.V, N, SPLAT_STRIDE, dtype=F32, device=d)
+        self.radii = torch.zeros(self.V, N, dtype=I32, device=d)
+        self.tiles_touched = torch.zeros(self.V, N, dtype=I32, device=d)
+        self.v_splats = torch.zeros(self.V, N, SPLAT_STRIDE, dtype=F32, device=d)
+        for k, r in enumerate(self.views):
+            if k:
+                for name in ("V", "F", "vcol", "means", "log_scales", "quats", "logits", "colors", "sh_degree"):
+                    setattr(r, name, getattr(v0, name))
+                r.N = N
+                r._alloc_g(max(r.g_cap, 1))
+                r._alloc_tri(max(r.tri_cap, 1))
+            r.splats, r.radii, r.tiles_touched = self.splats[k], self.radii[k], self.tiles_touched[k]
+            r.v_splats = self.v_splats[k]
+            r.forward(sync=True)
+        self.v_verts = torch.zeros_like(v0.V)
+        self.v_vcol = torch.zeros_like(v0.vcol)
+        self.v_means = torch.zeros_like(v0.means)
+        self.v_log_scales = torch.zeros_like(v0.log_scales)
+        self.v_quats = torch.zeros_like(v0.quats)
+        self.v_logits = torch.zeros_like(v0.logits)
+        self.v_colors = torch.zeros_like(v0.colors)
+        torch.cuda.synchronize(self.dev)
+
+    def forward(self):
+        """All views' (rgb, depth, alpha), without host synchronisation (check
+        ``overflowed()``)."""
+        main = torch.cuda.current_stream(self.dev)
+        pool = self._pool()
+        start = torch.cuda.Event()
+        start.record(main)
+        v0 = self.views[0]
+        gm_project_gaussians_views(self.cams, self.opts, v0.means, v0.log_scales, v0.quats, v0.logits, v0.colors,
+                                   self.splats, self.radii, self.tiles_touched)
+        projected = torch.cuda.Event()
+        projected.record(main)
+        for k, r in enumerate(self.views):
+            s = pool[k % len(pool)]
+            s.wait_event(start)
+            with torch.cuda.stream(s):
+                cam, opts = r.cam, r.opts
+                gm_bin_triangles(cam, r.V, r.F, r.tri_range, r.tri_ids, r.tri_cap, r.tri_counters, r.tri_ws,
+                                 sync=False)
+                gm_zbuffer(cam, r.V, r.F, r.tri_range, r.tri_ids, r.face_id)
+                gm_interp_mesh(cam, r.V, r.F, r.vcol, r.face_id, r.mesh_depth, r.mesh_rgb, r.tile_far, r.tile_full)
+                s.wait_event(projected)
+                gm_bin_sort_gaussians(cam, opts, r.splats, r.radii, r.tile_far, r.tile_full, r.keys, r.gids,
+                                      r.g_range, r.g_cap, r.g_counters, r.g_ws, sync=False)
+                gm_composite_hybrid_fwd(cam, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                        r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib)
+        for s in pool:
+            main.wait_stream(s)
+        return [(r.out_rgb, r.out_depth, r.out_alpha) for r in self.views]
+
+    def backward(self, grads):
+        """grads: per view (g_rgb, g_depth, g_alpha).  Returns the gradients of
+        (means, log_scales, quats, logits, colors) summed over the views and of
+        (vertex positions, vertex colours) accumulated over the views."""
+        main = torch.cuda.current_stream(self.dev)
+        pool = self._pool()
+        self.v_splats.zero_()
+        self.v_verts.zero_()
+        self.v_vcol.zero_()
+        start = torch.cuda.Event()
+        start.record(main)
+        for k, (r, (g_rgb, g_depth, g_alpha)) in enumerate(zip(self.views, grads)):
+            s = pool[k % len(pool)]
+            s.wait_event(start)
+            with torch.cuda.stream(s):
+                gm_composite_hybrid_bwd(r.cam, r.opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb,
+                                        r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
+                                        r.V, r.F, r.vcol, self.v_verts, self.v_vcol)
+        for s in pool:
+            main.wait_stream(s)
+        v0 = self.views[0]
+        gm_project_gaussians_bwd_views(self.cams, self.opts, v0.means, v0.log_scales, v0.quats, v0.logits, v0.colors,
+                                       self.radii, self.v_splats, self.v_means, self.v_log_scales, self.v_quats,
+                                       self.v_logits, self.v_colors)
+        return (self.v_means, self.v_log_scales, self.v_quats, self.v_logits, self.v_colors, self.v_verts,
+                self.v_vcol)
+
+    def capture_step(self, grads):
+        """Records forward + backward of all views into one CUDA graph."""
+        side = torch.cuda.Stream(device=self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):  # warm the capture stream once
+            self.forward()
+            self.backward(grads)
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.forward()
+            self.backward(grads)
+        return graph
+
+    def overflowed(self) -> bool:
+        return any(r.overflowed() for r in self.views)
+

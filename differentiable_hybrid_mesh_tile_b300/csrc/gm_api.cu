@@ -188,6 +188,61 @@ int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t 
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_bwd");
 }
 
+int gm_project_gaussians_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N, const float* means,
+                               const float* log_scales, const float* quats, const float* logits, const float* colors,
+                               float* splats, int32_t* radii, int32_t* tiles_touched, void* stream)
+{
+    g_err[0] = 0;
+    GM_REQUIRE(cams && V >= 1 && V <= GM_MAX_VIEWS, "cams is NULL or V = %d not in 1..%d", V, GM_MAX_VIEWS);
+    for (int v = 0; v < V; ++v)
+        if (int st = check_cam(cams + v)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(N >= 0, "negative N");
+    GM_REQUIRE(opts->sh_degree >= -1 && opts->sh_degree <= 3, "sh_degree %d not in -1..3", opts->sh_degree);
+    if (N > 0) {
+        GM_REQUIRE(means && log_scales && quats && logits && colors, "an input is NULL");
+        GM_REQUIRE(splats && radii && tiles_touched, "an output is NULL");
+        GM_REQUIRE(aligned16(quats) && aligned16(splats), "quats / splats must be 16-byte aligned");
+        if (opts->sh_degree == 1 || opts->sh_degree == 3)
+            GM_REQUIRE(aligned16(colors), "SH coefficients must be 16-byte aligned");
+    }
+    gm::Cam c[GM_MAX_VIEWS];
+    for (int v = 0; v < V; ++v) c[v] = gm::make_cam(cams[v]);
+    cudaError_t e = gm::project_views(c, V, opts->sh_degree, N, means, log_scales, quats, logits, colors, splats, radii,
+                                      tiles_touched, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_views");
+}
+
+int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N,
+                                   const float* means, const float* log_scales, const float* quats,
+                                   const float* logits, const float* colors, const int32_t* radii,
+                                   const float* v_splats, int32_t accumulate, float* v_means, float* v_log_scales,
+                                   float* v_quats, float* v_logits, float* v_colors, void* stream)
+{
+    g_err[0] = 0;
+    GM_REQUIRE(cams && V >= 1 && V <= GM_MAX_VIEWS, "cams is NULL or V = %d not in 1..%d", V, GM_MAX_VIEWS);
+    for (int v = 0; v < V; ++v)
+        if (int st = check_cam(cams + v)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(N >= 0, "negative N");
+    GM_REQUIRE(opts->sh_degree >= -1 && opts->sh_degree <= 3, "sh_degree %d not in -1..3", opts->sh_degree);
+    if (N > 0) {
+        GM_REQUIRE(means && log_scales && quats && logits && colors && radii && v_splats, "an input is NULL");
+        GM_REQUIRE(v_means && v_log_scales && v_quats && v_logits && v_colors, "an output is NULL");
+        GM_REQUIRE(aligned16(quats) && aligned16(v_splats) && aligned16(v_quats),
+                   "quats / v_splats / v_quats must be 16-byte aligned");
+        if (opts->sh_degree == 1 || opts->sh_degree == 3)
+            GM_REQUIRE(aligned16(colors) && aligned16(v_colors), "SH coefficients and their gradient must be "
+                       "16-byte aligned");
+    }
+    gm::Cam c[GM_MAX_VIEWS];
+    for (int v = 0; v < V; ++v) c[v] = gm::make_cam(cams[v]);
+    cudaError_t e = gm::project_bwd_views(c, V, opts->sh_degree, N, means, log_scales, quats, logits, colors, radii,
+                                          v_splats, accumulate != 0, v_means, v_log_scales, v_quats, v_logits,
+                                          v_colors, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_bwd_views");
+}
+
 size_t gm_bin_sort_gaussians_workspace_size(int32_t N, int32_t cap, int32_t width, int32_t height)
 {
     (void)width;

@@ -10,17 +10,21 @@
 namespace gm {
 namespace {
 
+// The record, radius and tile count of Gaussian g seen by camera c.
 // DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
 template <int DEG>
-__global__ void __launch_bounds__(256)
-k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
-          const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
-          float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched)
+__device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts& pc, int g,
+                                                 const float* __restrict__ means,
+                                                 const float* __restrict__ log_scales,
+                                                 const float4* __restrict__ quats, const float* __restrict__ logits,
+                                                 const float* __restrict__ colors, float4& o0, float4& o1, float4& o2,
+                                                 int& rad, int& touched)
 {
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= N) return;
-    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0, o2 = o0;
-    int rad = 0, touched = 0;
+    o0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    o1 = o0;
+    o2 = o0;
+    rad = 0;
+    touched = 0;
     const float mx = __ldg(means + 3 * (int64_t)g), my = __ldg(means + 3 * (int64_t)g + 1),
                 mz = __ldg(means + 3 * (int64_t)g + 2);
     const float tx = fmaf(c.R[0], mx, fmaf(c.R[1], my, fmaf(c.R[2], mz, c.t[0])));
@@ -110,11 +114,49 @@ k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const fl
             }
         }
     }
+}
+
+template <int DEG>
+__global__ void __launch_bounds__(256)
+k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+          const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
+          float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= N) return;
+    float4 o0, o1, o2;
+    int rad, touched;
+    project_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, o0, o1, o2, rad, touched);
     splats[3 * (int64_t)g] = o0;
     splats[3 * (int64_t)g + 1] = o1;
     splats[3 * (int64_t)g + 2] = o2;
     radii[g] = rad;
     tiles_touched[g] = touched;
+}
+
+// Several views in one launch: each thread takes one Gaussian through every
+// view of the batch, so its parameters come from DRAM once (later views find
+// them in L1 / L2); outputs are [view][N] arrays.
+template <int DEG>
+__global__ void __launch_bounds__(256)
+k_project_views(ViewBatch vb, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+                const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
+                float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= N) return;
+    for (int v = 0; v < vb.n; ++v) {
+        float4 o0, o1, o2;
+        int rad, touched;
+        project_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors, o0, o1, o2, rad,
+                              touched);
+        const int64_t i = (int64_t)v * N + g;
+        splats[3 * i] = o0;
+        splats[3 * i + 1] = o1;
+        splats[3 * i + 2] = o2;
+        radii[i] = rad;
+        tiles_touched[i] = touched;
+    }
 }
 
 // ------------------------------------------------------------- binning ----
@@ -464,6 +506,39 @@ cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, cons
     }
 #undef GM_PROJ
     return cudaGetLastError();
+}
+
+cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const float* means, const float* log_scales,
+                          const float* quats, const float* logits, const float* colors, float* splats,
+                          int32_t* radii, int32_t* tiles_touched, cudaStream_t s)
+{
+    if (N <= 0) return cudaSuccess;
+    const int grid = (N + 255) / 256;
+    auto* q4 = reinterpret_cast<const float4*>(quats);
+    for (int v0 = 0; v0 < V; v0 += MAX_VIEWS) {
+        ViewBatch vb;
+        vb.n = std::min(MAX_VIEWS, V - v0);
+        for (int v = 0; v < vb.n; ++v) {
+            vb.cam[v] = cams[v0 + v];
+            vb.pc[v] = make_proj_consts(cams[v0 + v]);
+        }
+        const int64_t off = (int64_t)v0 * N;
+        auto* s4 = reinterpret_cast<float4*>(splats + 12 * off);
+#define GM_PROJ_V(D) k_project_views<D><<<grid, 256, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, s4, \
+                                                             radii + off, tiles_touched + off)
+        switch (sh_degree) {
+            case -1: GM_PROJ_V(-1); break;
+            case 0: GM_PROJ_V(0); break;
+            case 1: GM_PROJ_V(1); break;
+            case 2: GM_PROJ_V(2); break;
+            case 3: GM_PROJ_V(3); break;
+            default: return cudaErrorInvalidValue;
+        }
+#undef GM_PROJ_V
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 size_t gauss_bin_ws_bytes(int N, int cap)

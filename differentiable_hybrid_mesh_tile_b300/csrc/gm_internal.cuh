@@ -189,6 +189,13 @@ cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int
 cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
                     const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
                     int32_t* tiles_touched, cudaStream_t s);
+cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const float* means, const float* log_scales,
+                          const float* quats, const float* logits, const float* colors, float* splats,
+                          int32_t* radii, int32_t* tiles_touched, cudaStream_t s);
+cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, const float* means,
+                              const float* log_scales, const float* quats, const float* logits, const float* colors,
+                              const int32_t* radii, const float* v_splats, bool accumulate, float* v_means,
+                              float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s);
 cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
                         const float* quats, const float* logits, const float* colors, const int32_t* radii,
                         const float* v_splats, bool accumulate, float* v_means, float* v_log_scales, float* v_quats,

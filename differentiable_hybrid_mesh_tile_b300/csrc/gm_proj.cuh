@@ -68,4 +68,12 @@ inline ProjConsts make_proj_consts(const Cam& c)
     return pc;
 }
 
+// Cameras of one batched launch (passed by value as a kernel parameter).
+constexpr int MAX_VIEWS = 8;
+struct ViewBatch {
+    Cam cam[MAX_VIEWS];
+    ProjConsts pc[MAX_VIEWS];
+    int n;
+};
+
 }  // namespace gm

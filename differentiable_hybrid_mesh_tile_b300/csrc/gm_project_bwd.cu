@@ -10,6 +10,8 @@
 // from the inputs (nothing is stored between the passes), and each thread
 // writes only its own Gaussian's rows, so no atomics are needed.  Gaussians
 // the forward culled (radius 0) get zero gradients.
+#include <algorithm>
+
 #include "gm_internal.cuh"
 #include "gm_proj.cuh"
 
@@ -48,29 +50,51 @@ __device__ __forceinline__ void sh_basis_vjp(float x, float y, float z, const fl
     }
 }
 
+// The additions of gradients over calls or views are separately rounded
+// (__fadd_rn is never contracted into a multiply-add), so a batched sum over
+// views and a sequence of accumulating per-view calls agree bit for bit.
 __device__ __forceinline__ void put(float* dst, float v, bool acc)
 {
-    *dst = acc ? *dst + v : v;
+    *dst = acc ? __fadd_rn(*dst, v) : v;
 }
 
-// DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
-template <int DEG>
-__global__ void __launch_bounds__(256)
-k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
-              const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
-              const int32_t* __restrict__ radii, const float4* __restrict__ v_splats, bool acc,
-              float* __restrict__ v_means, float* __restrict__ v_log_scales, float4* __restrict__ v_quats,
-              float* __restrict__ v_logits, float* __restrict__ v_colors)
+__device__ __forceinline__ void add_or_set(float& x, float v, bool first)
 {
-    constexpr int K = DEG < 0 ? 1 : (DEG + 1) * (DEG + 1);
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= N) return;
-    float vmu[3] = {0.f, 0.f, 0.f}, vls[3] = {0.f, 0.f, 0.f}, vq[4] = {0.f, 0.f, 0.f, 0.f}, vlogit = 0.f;
-    float vcol[3 * K];
-#pragma unroll
-    for (int i = 0; i < 3 * K; ++i) vcol[i] = 0.0f;
+    x = first ? v : __fadd_rn(x, v);
+}
 
-    if (__ldg(radii + g) > 0) {
+// The gradient of one Gaussian's parameters from one view's record gradient.
+template <int DEG>
+struct ProjGrad {
+    static constexpr int K = DEG < 0 ? 1 : (DEG + 1) * (DEG + 1);
+    float vmu[3], vls[3], vq[4], vlogit;
+    float vcol[3 * K];
+};
+
+// DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
+// radius: of this Gaussian in this view (0 = culled: zero gradient);
+// vsp: its record gradient (3 float4).
+template <int DEG>
+__device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjConsts& pc, int g,
+                                                     const float* __restrict__ means,
+                                                     const float* __restrict__ log_scales,
+                                                     const float4* __restrict__ quats,
+                                                     const float* __restrict__ logits,
+                                                     const float* __restrict__ colors, int radius,
+                                                     const float4* __restrict__ vsp, bool first,
+                                                     ProjGrad<DEG>& out)
+{
+    constexpr int K = ProjGrad<DEG>::K;
+    // this view's gradient: written into out (first view) or added to it, one
+    // finished value per parameter, so the sum over views is taken in view order
+    float vmu[3] = {0.f, 0.f, 0.f}, vls[3] = {0.f, 0.f, 0.f}, vq[4] = {0.f, 0.f, 0.f, 0.f}, vlogit = 0.f;
+    float* vcol = out.vcol;
+    if (first) {
+#pragma unroll
+        for (int i = 0; i < 3 * K; ++i) vcol[i] = 0.0f;
+    }
+
+    if (radius > 0) {
         const float mx = __ldg(means + 3 * (int64_t)g), my = __ldg(means + 3 * (int64_t)g + 1),
                     mz = __ldg(means + 3 * (int64_t)g + 2);
         const float tx = fmaf(c.R[0], mx, fmaf(c.R[1], my, fmaf(c.R[2], mz, c.t[0])));
@@ -114,8 +138,7 @@ k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, cons
         const float idet = 1.0f / (a * cc - b * b);
 
         // upstream: record = (u, v, A, B, C | o, r, g | b, depth)
-        const float4 v0 = __ldg(v_splats + 3 * (int64_t)g), v1 = __ldg(v_splats + 3 * (int64_t)g + 1),
-                     v2 = __ldg(v_splats + 3 * (int64_t)g + 2);
+        const float4 v0 = __ldg(vsp), v1 = __ldg(vsp + 1), v2 = __ldg(vsp + 2);
         const float gu = v0.x, gv = v0.y, gA = v0.z, gB = v0.w, gC = v1.x, go = v1.y, gz = v2.y;
         const float grgb[3] = {v1.z, v1.w, v2.x};
 
@@ -197,7 +220,7 @@ k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, cons
         // colour
         if (DEG < 0) {
 #pragma unroll
-            for (int ch = 0; ch < 3; ++ch) vcol[ch] = grgb[ch];
+            for (int ch = 0; ch < 3; ++ch) add_or_set(vcol[ch], grgb[ch], first);
         } else {
             float dx = mx - pc.cpx, dy = my - pc.cpy, dz = mz - pc.cpz;
             const float dn = 1.0f / sqrtf(dx * dx + dy * dy + dz * dz);
@@ -231,7 +254,7 @@ k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, cons
             for (int k = 0; k < K; ++k) {
                 vY[k] = gch[0] * cf[3 * k] + gch[1] * cf[3 * k + 1] + gch[2] * cf[3 * k + 2];
 #pragma unroll
-                for (int ch = 0; ch < 3; ++ch) vcol[3 * k + ch] = gch[ch] * Y[k];
+                for (int ch = 0; ch < 3; ++ch) add_or_set(vcol[3 * k + ch], gch[ch] * Y[k], first);
             }
             // direction d = n / |n|, n = mu - camera centre
             float gx, gy, gzd;
@@ -245,34 +268,88 @@ k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, cons
 
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-        put(v_means + 3 * (int64_t)g + k, vmu[k], acc);
-        put(v_log_scales + 3 * (int64_t)g + k, vls[k], acc);
+        add_or_set(out.vmu[k], vmu[k], first);
+        add_or_set(out.vls[k], vls[k], first);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) add_or_set(out.vq[k], vq[k], first);
+    add_or_set(out.vlogit, vlogit, first);
+}
+
+template <int DEG>
+__device__ __forceinline__ void store_grad(int g, const ProjGrad<DEG>& G, bool acc, float* __restrict__ v_means,
+                                           float* __restrict__ v_log_scales, float4* __restrict__ v_quats,
+                                           float* __restrict__ v_logits, float* __restrict__ v_colors)
+{
+    constexpr int K = ProjGrad<DEG>::K;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        put(v_means + 3 * (int64_t)g + k, G.vmu[k], acc);
+        put(v_log_scales + 3 * (int64_t)g + k, G.vls[k], acc);
     }
     {
-        float4 o = make_float4(vq[0], vq[1], vq[2], vq[3]);
+        float4 o = make_float4(G.vq[0], G.vq[1], G.vq[2], G.vq[3]);
         if (acc) {
             const float4 p = v_quats[g];
-            o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+            o = make_float4(__fadd_rn(p.x, o.x), __fadd_rn(p.y, o.y), __fadd_rn(p.z, o.z), __fadd_rn(p.w, o.w));
         }
         v_quats[g] = o;
     }
-    put(v_logits + g, vlogit, acc);
+    put(v_logits + g, G.vlogit, acc);
     float* dst = v_colors + (int64_t)g * (3 * K);
     if ((3 * K) % 4 == 0) {
         float4* dst4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
         for (int v4 = 0; v4 < 3 * K / 4; ++v4) {
-            float4 o = make_float4(vcol[4 * v4], vcol[4 * v4 + 1], vcol[4 * v4 + 2], vcol[4 * v4 + 3]);
+            float4 o = make_float4(G.vcol[4 * v4], G.vcol[4 * v4 + 1], G.vcol[4 * v4 + 2], G.vcol[4 * v4 + 3]);
             if (acc) {
                 const float4 p = dst4[v4];
-                o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+                o = make_float4(__fadd_rn(p.x, o.x), __fadd_rn(p.y, o.y), __fadd_rn(p.z, o.z), __fadd_rn(p.w, o.w));
             }
             dst4[v4] = o;
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 3 * K; ++i) put(dst + i, vcol[i], acc);
+        for (int i = 0; i < 3 * K; ++i) put(dst + i, G.vcol[i], acc);
     }
+}
+
+template <int DEG>
+__global__ void __launch_bounds__(256)
+k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+              const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
+              const int32_t* __restrict__ radii, const float4* __restrict__ v_splats, bool acc,
+              float* __restrict__ v_means, float* __restrict__ v_log_scales, float4* __restrict__ v_quats,
+              float* __restrict__ v_logits, float* __restrict__ v_colors)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= N) return;
+    ProjGrad<DEG> G;
+    project_bwd_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, __ldg(radii + g),
+                              v_splats + 3 * (int64_t)g, true, G);
+    store_grad<DEG>(g, G, acc, v_means, v_log_scales, v_quats, v_logits, v_colors);
+}
+
+// The views of a batch summed in registers (in view order, the order in which
+// per-view calls with accumulation would add them), written once.
+template <int DEG>
+__global__ void __launch_bounds__(128)
+k_project_bwd_views(ViewBatch vb, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+                    const float4* __restrict__ quats, const float* __restrict__ logits,
+                    const float* __restrict__ colors, const int32_t* __restrict__ radii,
+                    const float4* __restrict__ v_splats, bool acc, float* __restrict__ v_means,
+                    float* __restrict__ v_log_scales, float4* __restrict__ v_quats, float* __restrict__ v_logits,
+                    float* __restrict__ v_colors)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= N) return;
+    ProjGrad<DEG> total;
+    for (int v = 0; v < vb.n; ++v) {
+        const int64_t i = (int64_t)v * N + g;
+        project_bwd_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors,
+                                  __ldg(radii + i), v_splats + 3 * i, v == 0, total);
+    }
+    store_grad<DEG>(g, total, acc, v_means, v_log_scales, v_quats, v_logits, v_colors);
 }
 
 }  // namespace
@@ -301,6 +378,43 @@ cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, 
     }
 #undef GM_PROJ_BWD
     return cudaGetLastError();
+}
+
+cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, const float* means,
+                              const float* log_scales, const float* quats, const float* logits, const float* colors,
+                              const int32_t* radii, const float* v_splats, bool accumulate, float* v_means,
+                              float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s)
+{
+    if (N <= 0) return cudaSuccess;
+    const int grid = (N + 127) / 128;  // 128-thread CTAs: the SH-3 body is register heavy
+    auto* q4 = reinterpret_cast<const float4*>(quats);
+    auto* vq4 = reinterpret_cast<float4*>(v_quats);
+    for (int v0 = 0; v0 < V; v0 += MAX_VIEWS) {
+        ViewBatch vb;
+        vb.n = std::min(MAX_VIEWS, V - v0);
+        for (int v = 0; v < vb.n; ++v) {
+            vb.cam[v] = cams[v0 + v];
+            vb.pc[v] = make_proj_consts(cams[v0 + v]);
+        }
+        const int64_t off = (int64_t)v0 * N;
+        auto* vs4 = reinterpret_cast<const float4*>(v_splats + 12 * off);
+        const bool acc = accumulate || v0 > 0;  // later batches add to the earlier ones
+#define GM_PROJ_BWD_V(D)                                                                                          \
+    k_project_bwd_views<D><<<grid, 128, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, radii + off, vs4, acc, \
+                                                v_means, v_log_scales, vq4, v_logits, v_colors)
+        switch (sh_degree) {
+            case -1: GM_PROJ_BWD_V(-1); break;
+            case 0: GM_PROJ_BWD_V(0); break;
+            case 1: GM_PROJ_BWD_V(1); break;
+            case 2: GM_PROJ_BWD_V(2); break;
+            case 3: GM_PROJ_BWD_V(3); break;
+            default: return cudaErrorInvalidValue;
+        }
+#undef GM_PROJ_BWD_V
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace gm

@@ -265,6 +265,34 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             float* v_vcol, uint64_t* stats, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Batched views (several cameras of one scene, e.g. the views of a training
+ * batch): the projection and its backward for V cameras in one call.  Each
+ * thread takes one Gaussian through every view, so its parameters are read
+ * from memory once, and the backward sums the views' gradients in registers
+ * (in view order, the order in which per-view calls with accumulate = 1
+ * would add them) before writing once.  The per-view steps between the two
+ * (binning, z-buffer, compositing) take one view's slice of these arrays.
+ *   cams [V] host array, 1 <= V <= GM_MAX_VIEWS.
+ *   gm_project_gaussians_views: as gm_project_gaussians for every view;
+ *   splats [V][N][12], radii [V][N], tiles_touched [V][N] out (view v at
+ *   offset v N).
+ *   gm_project_gaussians_bwd_views: as gm_project_gaussians_bwd with radii
+ *   [V][N] and v_splats [V][N][12] from the views; the parameter gradients
+ *   are the sum over the views (written, or added when accumulate != 0),
+ *   summed in view order within each group of 8 views, the groups added in
+ *   order (so up to 8 views the result is that of per-view calls).
+ * ---------------------------------------------------------------------- */
+#define GM_MAX_VIEWS 64
+int gm_project_gaussians_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N, const float* means,
+                               const float* log_scales, const float* quats, const float* logits, const float* colors,
+                               float* splats, int32_t* radii, int32_t* tiles_touched, void* stream);
+int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N,
+                                   const float* means, const float* log_scales, const float* quats,
+                                   const float* logits, const float* colors, const int32_t* radii,
+                                   const float* v_splats, int32_t accumulate, float* v_means, float* v_log_scales,
+                                   float* v_quats, float* v_logits, float* v_colors, void* stream);
+
+/* ------------------------------------------------------------------------
  * gm_bin_triangles_noalloc -- gm_bin_triangles for callers that may not
  * allocate device memory at all (a plugin or engine inside a host
  * application that owns all device memory through its own pool and budget,
