@@ -137,8 +137,24 @@ def project(cam, g):
     margin = np.zeros(N, np.float64)
     lib().orc_project_gaussians(C.byref(_cam(cam)), C.c_int32(g.sh_degree), C.c_int32(N),
                                 _p(means), _p(ls), _p(q), _p(lo), _p(col),
-                                _p(splats), _p(radii), _p(touched), _p(margin))
+                                _p(splats), _p(radii), _p(touched), _p(margin), None)
     return splats, radii, touched, margin
+
+
+def project_depth_model(cam, g):
+    """Soft-split depth model [N][4] = (g_u, g_v, sigma_z, 0) of each Gaussian
+    (zeros where culled); see depth_model_f64."""
+    N = len(g.means)
+    splats = np.zeros((N, S_STRIDE), np.float32)
+    radii = np.zeros(N, np.int32)
+    touched = np.zeros(N, np.int32)
+    margin = np.zeros(N, np.float64)
+    dm = np.zeros((N, 4), np.float32)
+    lib().orc_project_gaussians(C.byref(_cam(cam)), C.c_int32(g.sh_degree), C.c_int32(N),
+                                _p(_c(g.means, np.float32)), _p(_c(g.log_scales, np.float32)),
+                                _p(_c(g.quats, np.float32)), _p(_c(g.logits, np.float32)),
+                                _p(_c(g.colors, np.float32)), _p(splats), _p(radii), _p(touched), _p(margin), _p(dm))
+    return dm
 
 
 PROJ_PARAMS = ("mean", "log_scale", "quat", "logit", "color")
@@ -151,16 +167,18 @@ def proj_nparams(sh_degree):
     return 11 + 3 * ((sh_degree + 1) ** 2 if sh_degree >= 0 else 1)
 
 
-def project_fd(cam, g, v_splats, gids, params, hs):
+def project_fd(cam, g, v_splats, gids, params, hs, v_depth_model=None):
     """dL/d(3D parameter) by central differences (double, Richardson) for
-    L = sum over record fields of v_splats . record; see orc_project_fd."""
+    L = sum over record fields of v_splats . record (+ v_depth_model . depth
+    model); see orc_project_fd."""
     n = len(gids)
     grad = np.zeros(n, np.float64)
     status = np.zeros(n, np.int32)
+    vd = None if v_depth_model is None else _c(v_depth_model, np.float32)
     lib().orc_project_fd(C.byref(_cam(cam)), C.c_int32(g.sh_degree), _p(_c(g.means, np.float32)),
                          _p(_c(g.log_scales, np.float32)), _p(_c(g.quats, np.float32)),
                          _p(_c(g.logits, np.float32)), _p(_c(g.colors, np.float32)),
-                         _p(_c(v_splats, np.float32)), C.c_int32(n), _p(_c(gids, np.int32)),
+                         _p(_c(v_splats, np.float32)), _p(vd), C.c_int32(n), _p(_c(gids, np.int32)),
                          _p(_c(params, np.int32)), _p(_c(hs, np.float64)), _p(grad), _p(status))
     return grad, status
 
@@ -207,8 +225,17 @@ def tile_lists(cam, splats, radii, tiles=None):
     return start, entries
 
 
-def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=None):
-    """Full-frame outputs; only pixels of ``tiles`` (all when None) are written."""
+def _soft(depth_model, softness):
+    if depth_model is None or not softness > 0.0:
+        return None, C.c_double(0.0)
+    return _c(depth_model, np.float32), C.c_double(float(softness))
+
+
+def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=None, depth_model=None,
+                  softness=0.0):
+    """Full-frame outputs; only pixels of ``tiles`` (all when None) are written.
+    With depth_model and softness > 0: the soft split."""
+    dm, sf = _soft(depth_model, softness)
     start, entries = lists
     H, W = cam.height, cam.width
     out = {
@@ -223,12 +250,14 @@ def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=N
         _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
         _p(_c(face_id, np.int32)), _p(tl), C.c_int32(0 if tiles is None else len(tiles)),
         _p(out["rgb"]), _p(out["depth"]), _p(out["alpha"]), _p(out["T"]), _p(out["n_contrib"]),
-        _p(out["margins"]))
+        _p(out["margins"]), _p(dm), sf)
     return out
 
 
 def composite_fd(cam, bg, splats, radii, lists, mesh_depth, mesh_rgb, face_id, grads,
-                 gids, fields, hs, tie_band=1e-5):
+                 gids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0):
+    """fields 0..9: record fields; 12, 13, 14: depth model g_u, g_v, sigma_z."""
+    dm, sf = _soft(depth_model, softness)
     start, entries = lists
     g_rgb, g_depth, g_alpha = (_c(x, np.float32) for x in grads)
     n = len(gids)
@@ -239,12 +268,13 @@ def composite_fd(cam, bg, splats, radii, lists, mesh_depth, mesh_rgb, face_id, g
         _p(_c(start, np.int64)), _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)),
         _p(_c(mesh_rgb, np.float32)), _p(_c(face_id, np.int32)), _p(g_rgb), _p(g_depth), _p(g_alpha),
         C.c_int32(n), _p(_c(gids, np.int32)), _p(_c(fields, np.int32)), _p(_c(hs, np.float64)),
-        C.c_double(tie_band), _p(grad), _p(status))
+        C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf)
     return grad, status
 
 
 def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, grads,
-            vids, fields, hs, tie_band=1e-5):
+            vids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0):
+    dm, sf = _soft(depth_model, softness)
     start, entries = lists
     V, F, vcol = _c(V, np.float32), _c(F, np.int32), _c(vcol, np.float32)
     g_rgb, g_depth, g_alpha = (_c(x, np.float32) for x in grads)
@@ -256,24 +286,27 @@ def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, g
         _p(vcol), _p(_c(face_id, np.int32)), _p(_c(splats, np.float32)), _p(_c(start, np.int64)),
         _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
         _p(g_rgb), _p(g_depth), _p(g_alpha), C.c_int32(n), _p(_c(vids, np.int32)),
-        _p(_c(fields, np.int32)), _p(_c(hs, np.float64)), C.c_double(tie_band), _p(grad), _p(status))
+        _p(_c(fields, np.int32)), _p(_c(hs, np.float64)), C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf)
     return grad, status
 
 
-def composite_one(px, py, splats, order, D=np.inf, covered=False, cm=(0, 0, 0), bg=(1, 1, 1), f32=True):
+def composite_one(px, py, splats, order, D=np.inf, covered=False, cm=(0, 0, 0), bg=(1, 1, 1), f32=True,
+                  depth_model=None, softness=0.0):
     """One pixel over an explicit ordered list of splat ids: rgb, depth, alpha, T, n_contrib."""
+    dm, sf = _soft(depth_model, softness)
     out = np.zeros(7, np.float64)
     lst = _c(order, np.int32)
     lib().orc_composite_one(C.c_int32(int(f32)), C.c_double(px), C.c_double(py), _p(lst), C.c_int64(len(lst)),
                             _p(_c(splats, np.float32)), C.c_double(D), C.c_int32(int(covered)),
-                            _p(_c(cm, np.float64)), _p(_c(bg, np.float64)), _p(out))
+                            _p(_c(cm, np.float64)), _p(_c(bg, np.float64)), _p(out), _p(dm), sf)
     return {"rgb": out[:3], "depth": out[3], "alpha": out[4], "T": out[5], "n_contrib": int(out[6])}
 
 
 # ------------------------------------------------------------ pipeline ----
 
-def render(scene, cam=None, tiles=None):
-    """Whole forward pass from raw inputs for the listed tiles (all when None).
+def render(scene, cam=None, tiles=None, softness=0.0):
+    """Whole forward pass from raw inputs for the listed tiles (all when None),
+    with the soft split when softness > 0.
 
     Returns a dict of full-frame arrays (pixels outside ``tiles`` are zero)
     with every intermediate the parity tests look at."""
@@ -305,9 +338,11 @@ def render(scene, cam=None, tiles=None):
     best[sel], second[sel] = best_s, second_s
     splats, radii, touched, margin = project(cam, scene.gaussians)
     lists = tile_lists(cam, splats, radii, tiles_arr)
-    out = composite_fwd(cam, scene.bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles_arr)
+    dm = project_depth_model(cam, scene.gaussians) if softness > 0.0 else None
+    out = composite_fwd(cam, scene.bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles_arr,
+                        depth_model=dm, softness=softness)
     out.update(face_id=face_id.reshape(H, W), mesh_depth=mesh_depth.reshape(H, W),
                mesh_rgb=mesh_rgb.reshape(H, W, 3), zbest=best.reshape(H, W),
                zsecond=second.reshape(H, W), splats=splats, radii=radii,
-               tiles_touched=touched, radius_margin=margin, lists=lists, pixels=pixels)
+               tiles_touched=touched, radius_margin=margin, lists=lists, pixels=pixels, depth_model=dm)
     return out

@@ -55,6 +55,9 @@
 #ifndef M_PI
 #define M_PI 3.14159265358979323846
 #endif
+#ifndef M_SQRT1_2
+#define M_SQRT1_2 0.70710678118654752440
+#endif
 
 typedef struct {
     int32_t width, height;
@@ -407,6 +410,29 @@ static int64_t gauss_rect(const orc_camera* c, float mx, float my, int32_t r, in
     return (int64_t)(rect[2] - rect[0]) * (rect[3] - rect[1]);
 }
 
+/* Depth model of the soft split (Hybrid rendering): under the same local
+ * affine map as the splat, (u, v, z) of a point of the Gaussian are jointly
+ * Gaussian with covariance M Sigma_c M^T, M = [J; e_z^T]; the depth given
+ * the pixel p is Gaussian with mean z*(p) = z_c + g . (p - mean2d) and
+ * standard deviation sigma_z, where
+ *   g = (Sigma_uv + eps I)^-1 Sigma_uv,z,   sigma_z^2 = Sigma_zz - Sigma_z,uv g,
+ * Sigma_uv = J Sigma_c J^T, Sigma_uv,z = J Sigma_c e_z, Sigma_zz = e_z^T Sigma_c e_z.
+ * eps = 0.3 px^2, the low-pass of the splat (reading: Sigma_uv + eps I is the
+ * 2D covariance whose inverse is the conic); sigma_z^2 is floored at 1e-12.
+ * JS = J Sigma_c (2 x 3), S2 = Sigma_uv + eps I, Sc = Sigma_c.
+ * dm = (g_u, g_v, sigma_z).                                               */
+static void depth_model_f64(const double JS[2][3], const double S2[2][2], const double Sc[3][3], double dm[3])
+{
+    double det = S2[0][0] * S2[1][1] - S2[0][1] * S2[1][0];
+    double bu = JS[0][2], bv = JS[1][2];
+    double gu = (S2[1][1] * bu - S2[0][1] * bv) / det;
+    double gv = (-S2[1][0] * bu + S2[0][0] * bv) / det;
+    double var = Sc[2][2] - (bu * gu + bv * gv);
+    dm[0] = gu;
+    dm[1] = gv;
+    dm[2] = sqrt(fmax(var, 1e-12));
+}
+
 /* Projection of one Gaussian (EWA splatting as in the 3DGS projection the
  * page says was adapted from gsplat):
  *   t = R mu + t_cw; culled when t_z <= near or t_z > far;
@@ -425,7 +451,8 @@ static int64_t gauss_rect(const orc_camera* c, float mx, float my, int32_t r, in
 void orc_project_gaussians(const orc_camera* c, int32_t sh_degree, int32_t N,
                            const float* means, const float* log_scales, const float* quats,
                            const float* logits, const float* colors,
-                           float* splats, int32_t* radii, int32_t* tiles_touched, double* margin)
+                           float* splats, int32_t* radii, int32_t* tiles_touched, double* margin,
+                           float* depth_model)
 {
     int ncoef = sh_degree >= 0 ? (sh_degree + 1) * (sh_degree + 1) : 1;
     double Rc[3][3], cam_pos[3];
@@ -443,6 +470,8 @@ void orc_project_gaussians(const orc_camera* c, int32_t sh_degree, int32_t N,
     for (int64_t g = 0; g < N; ++g) {
         float* s = splats + S_STRIDE * g;
         for (int k = 0; k < S_STRIDE; ++k) s[k] = 0.0f;
+        if (depth_model)
+            for (int k = 0; k < 4; ++k) depth_model[4 * g + k] = 0.0f;
         radii[g] = 0;
         tiles_touched[g] = 0;
         margin[g] = INFINITY;
@@ -548,6 +577,11 @@ void orc_project_gaussians(const orc_camera* c, int32_t sh_degree, int32_t N,
         s[S_Z] = (float)t[2];
         radii[g] = r;
         tiles_touched[g] = (int32_t)area;
+        if (depth_model) {
+            double dm[3];
+            depth_model_f64(JS, S2, Sc, dm);
+            for (int k = 0; k < 3; ++k) depth_model[4 * g + k] = (float)dm[k];
+        }
     }
 }
 
@@ -693,6 +727,22 @@ typedef struct {
     double delta;
 } pert_t;
 
+/* Soft split (Hybrid rendering): the depth model [N][4] = (g_u, g_v,
+ * sigma_z, -) of each Gaussian (see depth_model_f64) and the softness.
+ * Perturbation fields F_GU, F_GV, F_SZ address the depth model.          */
+typedef struct {
+    const float* dm;
+    double softness;
+} soft_t;
+enum { F_GU = 12, F_GV = 13, F_SZ = 14 };
+
+static inline double dmfield(const soft_t* sm, int g, int k, const pert_t* p)
+{
+    double v = sm->dm[4 * (int64_t)g + k];
+    if (p && p->gid == g && p->field == F_GU + k) v += p->delta;
+    return v;
+}
+
 typedef struct {
     double rgb[3], depth, alpha, T;
     int32_t n_contrib;
@@ -719,6 +769,10 @@ static inline double sfield(const float* splats, int g, int f, const pert_t* p)
  *   alpha = min(0.99, o_i exp(-sigma))  (skip alpha < 1/255);
  *   T' = T (1 - alpha); stop before i when T' <= 1e-4;
  *   C += alpha T c_i;  Z += alpha T z_i;  T = T'.
+ * Soft split (sm != NULL) at a covered pixel: no hard depth test; the
+ * Gaussian's front part f = Phi((D - z*(p)) / (sigma_z softness)),
+ * z*(p) = z_i + g . d, replaces alpha by alpha f in the skip, the stop and
+ * the sums (the back parts lie behind the opaque mesh and are not seen).
  * Terminal layer (the opaque mesh, coverage 0 or 1):
  *   rgb = C + T (covered ? c_mesh : bg);  depth = Z + T covered D;
  *   alpha = 1 - T (1 - covered).
@@ -730,7 +784,7 @@ static inline double sfield(const float* splats, int g, int f, const pert_t* p)
     } while (0)
 
 static void composite_pixel(int f32, double px, double py, const int32_t* list, int64_t n,
-                            const float* splats, double D, int covered, const double cm[3],
+                            const float* splats, const soft_t* sm, double D, int covered, const double cm[3],
                             const double bg[3], const pert_t* p, pix_t* o, uint8_t* trace,
                             int64_t* trace_len, int watch)
 {
@@ -744,14 +798,17 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
     for (k = 0; k < n; ++k) {
         int g = list[k];
         double z = sfield(splats, g, S_Z, p);
-        if (D < INFINITY) {
-            double m = fabs(z - D) / D;
-            o->m_depth = fmin(o->m_depth, m);
-            if (g == watch) o->m_self = fmin(o->m_self, m);
-        }
-        if (!(z < D)) {
-            SET_CODE(TR_DEPTH);
-            continue;
+        const int soft = sm && covered;
+        if (!soft) {
+            if (D < INFINITY) {
+                double m = fabs(z - D) / D;
+                o->m_depth = fmin(o->m_depth, m);
+                if (g == watch) o->m_self = fmin(o->m_self, m);
+            }
+            if (!(z < D)) {
+                SET_CODE(TR_DEPTH);
+                continue;
+            }
         }
         double dx = rnd(px - sfield(splats, g, S_MX, p), f32);
         double dy = rnd(py - sfield(splats, g, S_MY, p), f32);
@@ -774,6 +831,13 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
         o->m_clamp = fmin(o->m_clamp, mc);
         int clamped = oG > amax;
         double alpha = clamped ? amax : oG;
+        if (soft) {
+            double zs = rnd(z + rnd(rnd(dmfield(sm, g, 0, p) * dx, f32) + rnd(dmfield(sm, g, 1, p) * dy, f32), f32),
+                            f32);
+            double xa = rnd(rnd(D - zs, f32) / rnd(dmfield(sm, g, 2, p) * sm->softness, f32), f32);
+            double f = rnd(0.5 * erfc(-xa * M_SQRT1_2), f32);
+            alpha = rnd(alpha * f, f32);
+        }
         double ma = fabs(alpha - amin) / amin;
         o->m_alpha = fmin(o->m_alpha, ma);
         if (g == watch) o->m_self = fmin(o->m_self, fmin(ms, fmin(mc, ma)));
@@ -815,8 +879,10 @@ void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats
                        const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
                        const int32_t* tiles, int32_t n_tiles_req,
                        float* out_rgb, float* out_depth, float* out_alpha, float* T_final,
-                       int32_t* n_contrib, double* margins)
+                       int32_t* n_contrib, double* margins, const float* depth_model, double softness)
 {
+    soft_t smv = {depth_model, softness};
+    const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     int TW = n_tiles_x(c), TH = n_tiles_y(c);
     int32_t nt = tiles ? n_tiles_req : TW * TH;
     double bgd[3] = {bg[0], bg[1], bg[2]};
@@ -832,7 +898,7 @@ void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats
                 int cov = face_id[pix] >= 0;
                 double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
                 pix_t o;
-                composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, (double)mesh_depth[pix], cov, cm,
+                composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, (double)mesh_depth[pix], cov, cm,
                                 bgd, NULL, &o, NULL, NULL, -1);
                 for (int ch = 0; ch < 3; ++ch) out_rgb[3 * pix + ch] = (float)o.rgb[ch];
                 out_depth[pix] = (float)o.depth;
@@ -899,8 +965,11 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                       const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
                       const float* g_rgb, const float* g_depth, const float* g_alpha,
                       int32_t n_req, const int32_t* req_gid, const int32_t* req_field,
-                      const double* req_h, double tie_band, double* grad, int32_t* status)
+                      const double* req_h, double tie_band, double* grad, int32_t* status,
+                      const float* depth_model, double softness)
 {
+    soft_t smv = {depth_model, softness};
+    const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     int TW = n_tiles_x(c);
     double bgd[3] = {bg[0], bg[1], bg[2]};
     int64_t maxlist = 1;
@@ -947,10 +1016,10 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                             double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
                             pix_t o32, o0, op, om;
                             int64_t n32, n0, np_, nm;
-                            composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o32, tr[0], &n32, g);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, NULL, &o0, tr[1], &n0, g);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pp, &op, tr[2], &np_, g);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pm, &om, tr[3], &nm, g);
+                            composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, NULL, &o32, tr[0], &n32, g);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, NULL, &o0, tr[1], &n0, g);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, &pp, &op, tr[2], &np_, g);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, &pm, &om, tr[3], &nm, g);
                             /* a decision within rounding of its threshold matters where this
                              * Gaussian is composited (every decision of the pixel enters its
                              * gradient) or in its own decisions */
@@ -963,8 +1032,8 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                             }
                             lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
                             lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pp2, &op, NULL, NULL, -1);
-                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, D, cov, cm, bgd, &pm2, &om, NULL, NULL, -1);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, &pp2, &op, NULL, NULL, -1);
+                            composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, &pm2, &om, NULL, NULL, -1);
                             lp2 += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
                             lm2 += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
                         }
@@ -989,8 +1058,10 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                  const int64_t* tile_start, const int32_t* entries, const float* mesh_depth,
                  const float* mesh_rgb, const float* g_rgb, const float* g_depth, const float* g_alpha,
                  int32_t n_req, const int32_t* req_vid, const int32_t* req_field, const double* req_h,
-                 double tie_band, double* grad, int32_t* status)
+                 double tie_band, double* grad, int32_t* status, const float* depth_model, double softness)
 {
+    soft_t smv = {depth_model, softness};
+    const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     int TW = n_tiles_x(c);
     int64_t P = (int64_t)c->width * c->height;
     double bgd[3] = {bg[0], bg[1], bg[2]};
@@ -1059,10 +1130,10 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                     double cm32[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
                     pix_t o32, o0, op, om;
                     int64_t n32, n0, np_, nm;
-                    composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, mesh_depth[pix], 1, cm32, bgd, NULL, &o32, tr[0], &n32, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[0], 1, cmv[0], bgd, NULL, &o0, tr[1], &n0, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[1], 1, cmv[1], bgd, NULL, &op, tr[2], &np_, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[2], 1, cmv[2], bgd, NULL, &om, tr[3], &nm, -1);
+                    composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, mesh_depth[pix], 1, cm32, bgd, NULL, &o32, tr[0], &n32, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[0], 1, cmv[0], bgd, NULL, &o0, tr[1], &n0, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[1], 1, cmv[1], bgd, NULL, &op, tr[2], &np_, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[2], 1, cmv[2], bgd, NULL, &om, tr[3], &nm, -1);
                     /* depth-test decisions: the PRECISION check below compares them
                      * exactly; alpha / stop / sigma decisions within rounding: a tie */
                     if (tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
@@ -1073,8 +1144,8 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                     }
                     lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
                     lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[3], 1, cmv[3], bgd, NULL, &op, NULL, NULL, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, Dv[4], 1, cmv[4], bgd, NULL, &om, NULL, NULL, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[3], 1, cmv[3], bgd, NULL, &op, NULL, NULL, -1);
+                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[4], 1, cmv[4], bgd, NULL, &om, NULL, NULL, -1);
                     lp2 += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
                     lm2 += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
                     any = 1;
@@ -1096,10 +1167,12 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
  * out: rgb[3], depth, alpha, T, n_contrib.                                */
 void orc_composite_one(int32_t f32, double px, double py, const int32_t* list, int64_t n,
                        const float* splats, double D, int32_t covered, const double* cm,
-                       const double* bg, double* out)
+                       const double* bg, double* out, const float* depth_model, double softness)
 {
+    soft_t smv = {depth_model, softness};
+    const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     pix_t o;
-    composite_pixel(f32, px, py, list, n, splats, D, covered, cm, bg, NULL, &o, NULL, NULL, -1);
+    composite_pixel(f32, px, py, list, n, splats, sm, D, covered, cm, bg, NULL, &o, NULL, NULL, -1);
     out[0] = o.rgb[0]; out[1] = o.rgb[1]; out[2] = o.rgb[2];
     out[3] = o.depth; out[4] = o.alpha; out[5] = o.T; out[6] = o.n_contrib;
 }
@@ -1134,11 +1207,11 @@ static void proj_load(int sh_degree, int64_t g, const float* means, const float*
  * forward decides them), [1] [2] the x / y clamps of the Jacobian
  * direction, [3..5] the colour clamps at 0.  A culled Gaussian's record is
  * all zeros.                                                              */
-static void proj_record_f64(const orc_camera* c, int sh_degree, const double* p, double rec[10], uint8_t trace[6])
+static void proj_record_f64(const orc_camera* c, int sh_degree, const double* p, double rec[13], uint8_t trace[6])
 {
     int ncoef = sh_degree >= 0 ? (sh_degree + 1) * (sh_degree + 1) : 1;
     double Rc[3][3], cam_pos[3], t[3];
-    for (int k = 0; k < 10; ++k) rec[k] = 0.0;
+    for (int k = 0; k < 13; ++k) rec[k] = 0.0;
     for (int k = 0; k < 6; ++k) trace[k] = 0;
     for (int r = 0; r < 3; ++r)
         for (int k = 0; k < 3; ++k) Rc[r][k] = c->R[3 * r + k];
@@ -1238,14 +1311,19 @@ static void proj_record_f64(const orc_camera* c, int sh_degree, const double* p,
         }
     }
     rec[S_Z] = t[2];
+    depth_model_f64(JS, S2, Sc, rec + 10);
 }
 
-static double proj_loss(const orc_camera* c, int sh_degree, const double* p, const float* v, uint8_t trace[6])
+/* L = v . record (+ vd . depth model when vd is given) */
+static double proj_loss(const orc_camera* c, int sh_degree, const double* p, const float* v, const float* vd,
+                        uint8_t trace[6])
 {
-    double rec[10];
+    double rec[13];
     proj_record_f64(c, sh_degree, p, rec, trace);
     double L = 0.0;
     for (int f = 0; f < 10; ++f) L += (double)v[f] * rec[f];
+    if (vd)
+        for (int f = 0; f < 3; ++f) L += (double)vd[f] * rec[10 + f];
     return L;
 }
 
@@ -1256,8 +1334,8 @@ static double proj_loss(const orc_camera* c, int sh_degree, const double* p, con
  * throughout gets 0 with FD_OK.                                           */
 void orc_project_fd(const orc_camera* c, int32_t sh_degree, const float* means, const float* log_scales,
                     const float* quats, const float* logits, const float* colors, const float* v_splats,
-                    int32_t n, const int32_t* gids, const int32_t* params, const double* hs, double* grad,
-                    int32_t* status)
+                    const float* v_depth_model, int32_t n, const int32_t* gids, const int32_t* params,
+                    const double* hs, double* grad, int32_t* status)
 {
     int np = PROJ_NPAR(sh_degree);
 #pragma omp parallel for schedule(dynamic, 4)
@@ -1267,6 +1345,7 @@ void orc_project_fd(const orc_camera* c, int32_t sh_degree, const float* means, 
         int k = params[i];
         double h = hs[i];
         const float* v = v_splats + S_STRIDE * g;
+        const float* vd = v_depth_model ? v_depth_model + 4 * g : NULL;
         grad[i] = 0.0;
         status[i] = FD_OK;
         if (k < 0 || k >= np) {
@@ -1275,16 +1354,16 @@ void orc_project_fd(const orc_camera* c, int32_t sh_degree, const float* means, 
         }
         proj_load(sh_degree, g, means, log_scales, quats, logits, colors, p);
         uint8_t t0[6], tp[6], tm[6], tp2[6], tm2[6];
-        proj_loss(c, sh_degree, p, v, t0);
+        proj_loss(c, sh_degree, p, v, vd, t0);
         memcpy(q, p, sizeof(double) * np);
         q[k] = p[k] + h;
-        double lp = proj_loss(c, sh_degree, q, v, tp);
+        double lp = proj_loss(c, sh_degree, q, v, vd, tp);
         q[k] = p[k] - h;
-        double lm = proj_loss(c, sh_degree, q, v, tm);
+        double lm = proj_loss(c, sh_degree, q, v, vd, tm);
         q[k] = p[k] + 0.5 * h;
-        double lp2 = proj_loss(c, sh_degree, q, v, tp2);
+        double lp2 = proj_loss(c, sh_degree, q, v, vd, tp2);
         q[k] = p[k] - 0.5 * h;
-        double lm2 = proj_loss(c, sh_degree, q, v, tm2);
+        double lm2 = proj_loss(c, sh_degree, q, v, vd, tm2);
         if (memcmp(t0, tp, 6) || memcmp(t0, tm, 6) || memcmp(t0, tp2, 6) || memcmp(t0, tm2, 6)) {
             status[i] = FD_FLIP;
             continue;

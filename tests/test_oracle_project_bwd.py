@@ -166,3 +166,25 @@ def test_unknown_parameter_is_unused(orc):
     g = one((0.0, 0.0, 4.0))
     gr, st = grad(orc, cam, g, F_MX, [orc.proj_nparams(-1), -1])
     assert (st == 5).all()
+
+
+def test_depth_model_gradient_closed_form(orc):
+    # identity rotation on the optical axis: Sigma_c = diag(s^2), J e_z = 0, so g = 0 and
+    # sigma_z = s_2: d sigma_z / d log s = (0, 0, s_2); d g_u / d log s_0 = 0
+    cam = cam_identity()
+    ls = (-2.0, -1.5, -1.0)
+    g = one((0.0, 0.0, 5.0), log_s=ls)
+    v = np.zeros((1, 12), np.float32)
+    vd = np.zeros((1, 4), np.float32)
+    vd[0, 2] = 1.0
+    gr, st = orc.project_fd(cam, g, v, np.zeros(3, np.int32), np.array([LOGS, LOGS + 1, LOGS + 2], np.int32),
+                            np.full(3, 1e-3), v_depth_model=vd)
+    assert (st == 0).all()
+    np.testing.assert_allclose(gr, [0.0, 0.0, float(np.exp(np.float32(ls[2])))], rtol=1e-7, atol=1e-9)
+    # off axis the slope g_u = Sigma_uv,z / (Sigma_uv + 0.3) grows with x: d g_u / d mean_x < 0
+    # for an isotropic Gaussian (j02 = -f x / z^2 turns negative)
+    g = one((0.2, 0.0, 5.0), log_s=(-1.0, -1.0, -1.0))
+    vd[0] = [1.0, 0.0, 0.0, 0.0]
+    gr, st = orc.project_fd(cam, g, v, np.zeros(1, np.int32), np.array([MEAN], np.int32), np.full(1, 1e-4),
+                            v_depth_model=vd)
+    assert st[0] == 0 and gr[0] < 0
