@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-multiview", action="store_true", help="skip the batched 8-view measurement")
+    ap.add_argument("--no-soft", action="store_true", help="skip the soft-split measurement")
     ap.add_argument("--cpu-tiles", type=int, default=48, help="tiles of the frame the CPU oracle renders")
     return ap.parse_args()
 
@@ -410,16 +411,76 @@ def run_gm(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, r, scene, grads_np, flush, ws, dist)
+    del graph, fgraph
+    soft = None
+    if not args.no_soft:
+        soft = run_soft(args, scene, grads_np, flush, dist)
     multiview = None
     if not args.no_multiview:
-        del graph, fgraph
         multiview = run_multiview(args, flush, dist)
 
     return dict(value=value, fwd=fwd_value, ms_step=ms_step, ms_fwd=ms_fwd, ms_eager=ms_eager, stages=stages, roofline=roof,
                 clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_tri=K_tri, K_g=K_g, K_pre=K_pre,
-                multiview=multiview,
+                multiview=multiview, soft=soft,
                 pairs_f=pairs_f, pairs_b=pairs_b, blend_f=blend_f, blend_b=blend_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
                 gpu_name=props.name)
+
+
+def run_soft(args, scene, grads_np, flush, dist, softness=1.0):
+    """The same workload with the soft split at the mesh surface (no occlusion
+    cull, depth model from the projection, split-scaled alpha at covered
+    pixels): one forward + backward step as a CUDA graph, and the two
+    composite kernels timed eagerly with events."""
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    cam = scene.camera
+    W, H = cam.width, cam.height
+    r = gm.HybridRenderer(cam, bg=scene.bg, softness=softness)
+    r.upload(scene.mesh, scene.gaussians)
+    g_dev = [torch.as_tensor(x).cuda() for x in grads_np]
+    r.forward(sync=True)
+    r.backward(*g_dev)
+    graph = r.capture_step(*g_dev)
+    steps = max(3, min(args.steps, 100))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 2)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+    cam_c, opts = r.cam, r.opts
+
+    def fwd():
+        gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                   r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
+                                   depth_model=r.depth_model)
+
+    def bwd():
+        gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                                   r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats,
+                                   depth_model=r.depth_model, v_depth_model=r.v_depth_model,
+                                   v_mesh_depth=r.v_mesh_depth)
+
+    ms_step = timed(graph.replay)
+    ms_fwd = timed(fwd)
+    ms_bwd = timed(bwd)
+    overflow = r.overflowed()
+    K = int(r.g_counters[0].item())
+    ms_step, ms_fwd, ms_bwd = max_over_ranks([ms_step, ms_fwd, ms_bwd], dist, "cuda")
+    del graph
+    return {"softness": softness, "steps": steps, "ms_per_step": ms_step,
+            "mpix_s": W * H / 1e6 / (ms_step / 1e3), "composite_fwd_ms": ms_fwd, "composite_bwd_ms": ms_bwd,
+            "tile_entries": K, "overflow": overflow}
 
 
 def run_multiview(args, flush, dist):
@@ -635,7 +696,7 @@ def main():
                        res["K_pre"], "pairs_evaluated_fwd": res["pairs_f"], "pairs_composited_fwd": res["blend_f"],
                        "pairs_evaluated_bwd": res["pairs_b"], "pairs_composited_bwd": res["blend_b"]},
             "overflow": res["overflow"], "gpu": res["gpu_name"], "wall_s_timed": res["wall"],
-            "multiview": res["multiview"],
+            "multiview": res["multiview"], "soft_split": res["soft"],
         }
         print(json.dumps(line))
     if dist is not None:

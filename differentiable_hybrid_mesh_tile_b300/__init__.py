@@ -48,7 +48,7 @@ class gm_camera(C.Structure):
 
 class gm_opts(C.Structure):
     _fields_ = [("bg", C.c_float * 3), ("cull_occluded", C.c_int32), ("sh_degree", C.c_int32),
-                ("tile_test", C.c_int32)]
+                ("tile_test", C.c_int32), ("softness", C.c_float)]
 
 
 _VP = C.c_void_p
@@ -58,15 +58,15 @@ _SIGS = {
     "gm_bin_triangles": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, C.c_size_t, _VP]),
     "gm_zbuffer": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP]),
     "gm_interp_mesh": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "gm_project_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "gm_project_gaussians_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 7 + [_I32] + [_VP] * 6),
-    "gm_project_gaussians_views": (C.c_int, [_VP, _I32, _VP, _I32] + [_VP] * 8 + [_VP]),
-    "gm_project_gaussians_bwd_views": (C.c_int, [_VP, _I32, _VP, _I32] + [_VP] * 7 + [_I32] + [_VP] * 6),
+    "gm_project_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "gm_project_gaussians_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 8 + [_I32] + [_VP] * 6),
+    "gm_project_gaussians_views": (C.c_int, [_VP, _I32, _VP, _I32] + [_VP] * 9 + [_VP]),
+    "gm_project_gaussians_bwd_views": (C.c_int, [_VP, _I32, _VP, _I32] + [_VP] * 8 + [_I32] + [_VP] * 6),
     "gm_bin_sort_gaussians_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
     "gm_bin_sort_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
                                         C.c_size_t, _VP]),
-    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 13),
-    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 13 + [_I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 14),
+    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16 + [_I32, _VP, _I32] + [_VP] * 5),
     "gm_bin_triangles_noalloc": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP]),
     "gm_last_error": (C.c_char_p, []),
 }
@@ -111,13 +111,14 @@ def make_camera(cam) -> gm_camera:
     return c
 
 
-def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1, tile_test=True) -> gm_opts:
+def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1, tile_test=True, softness=0.0) -> gm_opts:
     o = gm_opts()
     for k in range(3):
         o.bg[k] = float(bg[k])
     o.cull_occluded = int(bool(cull_occluded))
     o.sh_degree = int(sh_degree)
     o.tile_test = int(bool(tile_test))
+    o.softness = float(softness)
     return o
 
 
@@ -190,10 +191,11 @@ def gm_interp_mesh(cam: gm_camera, V, F, vcol, face_id, mesh_depth, mesh_rgb, ti
 
 
 def gm_project_gaussians(cam: gm_camera, opts: gm_opts, means, log_scales, quats, logits, colors, splats, radii,
-                         tiles_touched):
+                         tiles_touched, depth_model=None):
     _check(lib().gm_project_gaussians(C.byref(cam), C.byref(opts), means.shape[0], _p(means, F32),
                                       _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
-                                      _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32), _stream()),
+                                      _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32),
+                                      _p(depth_model, F32), _stream()),
            "gm_project_gaussians")
 
 
@@ -205,31 +207,36 @@ def _cam_array(cams):
 
 
 def gm_project_gaussians_views(cams, opts: gm_opts, means, log_scales, quats, logits, colors, splats, radii,
-                               tiles_touched):
-    """cams: a list of gm_camera; splats [V][N][12], radii / tiles_touched [V][N]."""
+                               tiles_touched, depth_model=None):
+    """cams: a list of gm_camera; splats [V][N][12], radii / tiles_touched [V][N],
+    depth_model [V][N][4] or None."""
     arr = _cam_array(cams)
     _check(lib().gm_project_gaussians_views(arr, len(cams), C.byref(opts), means.shape[0], _p(means, F32),
                                             _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
-                                            _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32), _stream()),
+                                            _p(splats, F32), _p(radii, I32), _p(tiles_touched, I32),
+                                            _p(depth_model, F32), _stream()),
            "gm_project_gaussians_views")
 
 
 def gm_project_gaussians_bwd_views(cams, opts: gm_opts, means, log_scales, quats, logits, colors, radii, v_splats,
-                                   v_means, v_log_scales, v_quats, v_logits, v_colors, accumulate=False):
+                                   v_means, v_log_scales, v_quats, v_logits, v_colors, accumulate=False,
+                                   v_depth_model=None):
     arr = _cam_array(cams)
     _check(lib().gm_project_gaussians_bwd_views(arr, len(cams), C.byref(opts), means.shape[0], _p(means, F32),
                                                 _p(log_scales, F32), _p(quats, F32), _p(logits, F32),
                                                 _p(colors, F32), _p(radii, I32), _p(v_splats, F32),
-                                                int(bool(accumulate)), _p(v_means, F32), _p(v_log_scales, F32),
+                                                _p(v_depth_model, F32), int(bool(accumulate)), _p(v_means, F32), _p(v_log_scales, F32),
                                                 _p(v_quats, F32), _p(v_logits, F32), _p(v_colors, F32), _stream()),
            "gm_project_gaussians_bwd_views")
 
 
 def gm_project_gaussians_bwd(cam: gm_camera, opts: gm_opts, means, log_scales, quats, logits, colors, radii,
-                             v_splats, v_means, v_log_scales, v_quats, v_logits, v_colors, accumulate=False):
+                             v_splats, v_means, v_log_scales, v_quats, v_logits, v_colors, accumulate=False,
+                             v_depth_model=None):
     _check(lib().gm_project_gaussians_bwd(C.byref(cam), C.byref(opts), means.shape[0], _p(means, F32),
                                           _p(log_scales, F32), _p(quats, F32), _p(logits, F32), _p(colors, F32),
-                                          _p(radii, I32), _p(v_splats, F32), int(bool(accumulate)), _p(v_means, F32),
+                                          _p(radii, I32), _p(v_splats, F32), _p(v_depth_model, F32),
+                                          int(bool(accumulate)), _p(v_means, F32),
                                           _p(v_log_scales, F32), _p(v_quats, F32), _p(v_logits, F32),
                                           _p(v_colors, F32), _stream()),
            "gm_project_gaussians_bwd")
@@ -253,24 +260,26 @@ def gm_bin_sort_gaussians(cam: gm_camera, opts: gm_opts, splats, radii, tile_far
 
 
 def gm_composite_hybrid_fwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
-                            out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None):
+                            out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None, depth_model=None):
     _check(lib().gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
-                                         _p(gids, I32),
-                                         _p(splats, F32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
+                                         _p(gids, I32), _p(splats, F32), _p(depth_model, F32),
+                                         _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
                                          _p(out_rgb, F32), _p(out_depth, F32), _p(out_alpha, F32), _p(T_final, F32),
                                          _p(n_contrib, I32), _p(stats, I64), _stream()), "gm_composite_hybrid_fwd")
 
 
 def gm_composite_hybrid_bwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
                             T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, V=None, F=None, vcol=None,
-                            v_verts=None, v_vcol=None, stats=None):
+                            v_verts=None, v_vcol=None, stats=None, depth_model=None, v_depth_model=None,
+                            v_mesh_depth=None):
     nV = 0 if V is None else V.shape[0]
     nF = 0 if F is None else F.shape[0]
     _check(lib().gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
-                                         _p(gids, I32),
-                                         _p(splats, F32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
+                                         _p(gids, I32), _p(splats, F32), _p(depth_model, F32),
+                                         _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
                                          _p(T_final, F32), _p(n_contrib, I32), _p(g_rgb, F32), _p(g_depth, F32),
-                                         _p(g_alpha, F32), _p(v_splats, F32), _p(V, F32), nV, _p(F, I32), nF,
+                                         _p(g_alpha, F32), _p(v_splats, F32), _p(v_depth_model, F32),
+                                         _p(v_mesh_depth, F32), _p(V, F32), nV, _p(F, I32), nF,
                                          _p(vcol, F32), _p(v_verts, F32), _p(v_vcol, F32), _p(stats, I64), _stream()),
            "gm_composite_hybrid_bwd")
 
@@ -293,10 +302,16 @@ class HybridRenderer:
     z-buffer and interpolation, and the mesh backward beside the composite
     backward (joined back into the caller's stream before anything reads
     their results; a captured graph keeps the two branches).
+
+    ``softness > 0`` selects the soft split at the mesh surface: the
+    projection also writes each Gaussian's depth model (``depth_model``), the
+    backward pass writes its gradient (``v_depth_model``) and dL/d mesh depth
+    through the split (``v_mesh_depth``), and the mesh backward then runs
+    after the Gaussian backward on one stream (it reads ``v_mesh_depth``).
     """
 
     def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
-                 concurrent=True, tile_test=True):
+                 concurrent=True, tile_test=True, softness=0.0):
         self.cam_desc = cam
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
@@ -308,6 +323,10 @@ class HybridRenderer:
         self.headroom = headroom
         self.concurrent = bool(concurrent)
         self.tile_test = bool(tile_test)
+        self.softness = float(softness)
+        if not self.softness >= 0.0:
+            raise ValueError("softness must be >= 0")
+        self.soft = self.softness > 0.0
         self._side = None
         self.tri_cap = 0
         self.g_cap = 0
@@ -328,6 +347,8 @@ class HybridRenderer:
         self.out_alpha = torch.empty(H, W, dtype=F32, device=d)
         self.T_final = torch.empty(H, W, dtype=F32, device=d)
         self.n_contrib = torch.empty(H, W, dtype=I32, device=d)
+        self.v_mesh_depth = torch.zeros(H, W, dtype=F32, device=d) if self.soft else None
+        self.depth_model = self.v_depth_model = None
 
     def set_camera(self, cam):
         assert int(cam.width) == self.W and int(cam.height) == self.H
@@ -336,7 +357,7 @@ class HybridRenderer:
 
     @property
     def opts(self) -> gm_opts:
-        return make_opts(self.bg, self.cull, self.sh_degree, self.tile_test)
+        return make_opts(self.bg, self.cull, self.sh_degree, self.tile_test, self.softness)
 
     def upload(self, mesh, gaussians):
         d = self.dev
@@ -359,6 +380,9 @@ class HybridRenderer:
         self.radii = torch.zeros(N, dtype=I32, device=d)
         self.tiles_touched = torch.zeros(N, dtype=I32, device=d)
         self.v_splats = torch.zeros(N, SPLAT_STRIDE, dtype=F32, device=d)
+        if self.soft:
+            self.depth_model = torch.zeros(N, 4, dtype=F32, device=d)
+            self.v_depth_model = torch.zeros(N, 4, dtype=F32, device=d)
         self._alloc_g(max(self.g_cap, 1))
 
     def _alloc_g(self, cap):
@@ -392,7 +416,7 @@ class HybridRenderer:
             side.wait_stream(main)
         with torch.cuda.stream(side):
             gm_project_gaussians(cam, opts, self.means, self.log_scales, self.quats, self.logits, self.colors,
-                                 self.splats, self.radii, self.tiles_touched)
+                                 self.splats, self.radii, self.tiles_touched, self.depth_model)
         for attempt in range(2):
             try:
                 k = gm_bin_triangles(cam, self.V, self.F, self.tri_range, self.tri_ids, self.tri_cap,
@@ -421,12 +445,28 @@ class HybridRenderer:
                 self._alloc_g(self._grow(int(self.g_counters[GM_CNT_K].item())))
         gm_composite_hybrid_fwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
                                 self.face_id, self.out_rgb, self.out_depth, self.out_alpha, self.T_final,
-                                self.n_contrib)
+                                self.n_contrib, depth_model=self.depth_model)
         return self.out_rgb, self.out_depth, self.out_alpha
 
     def backward(self, g_rgb, g_depth, g_alpha, mesh_grads: bool = True):
         cam, opts = self.cam, self.opts
         main = torch.cuda.current_stream(self.dev)
+        if self.soft:
+            # the mesh part reads dL/dD that the Gaussian part writes: one call, one stream
+            if mesh_grads:
+                if not hasattr(self, "v_verts") or self.v_verts.shape != self.V.shape:
+                    self.v_verts = torch.zeros_like(self.V)
+                    self.v_vcol = torch.zeros_like(self.vcol)
+                self.v_verts.zero_()
+                self.v_vcol.zero_()
+            self.v_splats.zero_()
+            self.v_depth_model.zero_()
+            mesh = (self.V, self.F, self.vcol, self.v_verts, self.v_vcol) if mesh_grads else (None,) * 5
+            gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
+                                    self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha,
+                                    self.v_splats, *mesh, depth_model=self.depth_model,
+                                    v_depth_model=self.v_depth_model, v_mesh_depth=self.v_mesh_depth)
+            return (self.v_splats,) + ((self.v_verts, self.v_vcol) if mesh_grads else (None, None))
         if mesh_grads:
             if not hasattr(self, "v_verts") or self.v_verts.shape != self.V.shape:
                 self.v_verts = torch.zeros_like(self.V)
@@ -488,9 +528,11 @@ class MultiViewRenderer:
     slices of the batch arrays.
     """
 
-    def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4):
+    def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4,
+                 softness=0.0):
         self.views = [HybridRenderer(c, bg=bg, cull_occluded=cull_occluded, device=device, concurrent=False,
-                                     tile_test=tile_test) for c in cams]
+                                     tile_test=tile_test, softness=softness) for c in cams]
+        self.soft = self.views[0].soft
         self.V = len(self.views)
         self.dev = torch.device(device)
         self.n_streams = max(1, min(int(streams), self.V))
@@ -520,6 +562,8 @@ class MultiViewRenderer:
         self.radii = torch.zeros(self.V, N, dtype=I32, device=d)
         self.tiles_touched = torch.zeros(self.V, N, dtype=I32, device=d)
         self.v_splats = torch.zeros(self.V, N, SPLAT_STRIDE, dtype=F32, device=d)
+        self.depth_model = torch.zeros(self.V, N, 4, dtype=F32, device=d) if self.soft else None
+        self.v_depth_model = torch.zeros(self.V, N, 4, dtype=F32, device=d) if self.soft else None
         for k, r in enumerate(self.views):
             if k:
                 for name in ("V", "F", "vcol", "means", "log_scales", "quats", "logits", "colors", "sh_degree"):
@@ -529,6 +573,8 @@ class MultiViewRenderer:
                 r._alloc_tri(max(r.tri_cap, 1))
             r.splats, r.radii, r.tiles_touched = self.splats[k], self.radii[k], self.tiles_touched[k]
             r.v_splats = self.v_splats[k]
+            if self.soft:
+                r.depth_model, r.v_depth_model = self.depth_model[k], self.v_depth_model[k]
             r.forward(sync=True)
         self.v_verts = torch.zeros_like(v0.V)
         self.v_vcol = torch.zeros_like(v0.vcol)
@@ -548,7 +594,7 @@ class MultiViewRenderer:
         start.record(main)
         v0 = self.views[0]
         gm_project_gaussians_views(self.cams, self.opts, v0.means, v0.log_scales, v0.quats, v0.logits, v0.colors,
-                                   self.splats, self.radii, self.tiles_touched)
+                                   self.splats, self.radii, self.tiles_touched, self.depth_model)
         projected = torch.cuda.Event()
         projected.record(main)
         for k, r in enumerate(self.views):
@@ -564,7 +610,8 @@ class MultiViewRenderer:
                 gm_bin_sort_gaussians(cam, opts, r.splats, r.radii, r.tile_far, r.tile_full, r.keys, r.gids,
                                       r.g_range, r.g_cap, r.g_counters, r.g_ws, sync=False)
                 gm_composite_hybrid_fwd(cam, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
-                                        r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib)
+                                        r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
+                                        depth_model=r.depth_model)
         for s in pool:
             main.wait_stream(s)
         return [(r.out_rgb, r.out_depth, r.out_alpha) for r in self.views]
@@ -576,6 +623,8 @@ class MultiViewRenderer:
         main = torch.cuda.current_stream(self.dev)
         pool = self._pool()
         self.v_splats.zero_()
+        if self.soft:
+            self.v_depth_model.zero_()
         self.v_verts.zero_()
         self.v_vcol.zero_()
         start = torch.cuda.Event()
@@ -586,13 +635,14 @@ class MultiViewRenderer:
             with torch.cuda.stream(s):
                 gm_composite_hybrid_bwd(r.cam, r.opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb,
                                         r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
-                                        r.V, r.F, r.vcol, self.v_verts, self.v_vcol)
+                                        r.V, r.F, r.vcol, self.v_verts, self.v_vcol, depth_model=r.depth_model,
+                                        v_depth_model=r.v_depth_model, v_mesh_depth=r.v_mesh_depth)
         for s in pool:
             main.wait_stream(s)
         v0 = self.views[0]
         gm_project_gaussians_bwd_views(self.cams, self.opts, v0.means, v0.log_scales, v0.quats, v0.logits, v0.colors,
                                        self.radii, self.v_splats, self.v_means, self.v_log_scales, self.v_quats,
-                                       self.v_logits, self.v_colors)
+                                       self.v_logits, self.v_colors, v_depth_model=self.v_depth_model)
         return (self.v_means, self.v_log_scales, self.v_quats, self.v_logits, self.v_colors, self.v_verts,
                 self.v_vcol)
 

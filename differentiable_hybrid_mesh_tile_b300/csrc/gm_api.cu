@@ -144,7 +144,7 @@ int gm_interp_mesh(const gm_camera* cam, const float* V, int32_t nV, const int32
 
 int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
                          const float* log_scales, const float* quats, const float* logits, const float* colors,
-                         float* splats, int32_t* radii, int32_t* tiles_touched, void* stream)
+                         float* splats, int32_t* radii, int32_t* tiles_touched, float* depth_model, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
@@ -158,15 +158,17 @@ int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, c
         if (opts->sh_degree == 1 || opts->sh_degree == 3)
             GM_REQUIRE(aligned16(colors), "SH coefficients must be 16-byte aligned");
     }
+    GM_REQUIRE(!depth_model || aligned16(depth_model), "depth_model must be 16-byte aligned");
     cudaError_t e = gm::project(gm::make_cam(*cam), opts->sh_degree, N, means, log_scales, quats, logits, colors, splats,
-                                radii, tiles_touched, (cudaStream_t)stream);
+                                radii, tiles_touched, depth_model, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians");
 }
 
 int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
                              const float* log_scales, const float* quats, const float* logits, const float* colors,
-                             const int32_t* radii, const float* v_splats, int32_t accumulate, float* v_means,
-                             float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, void* stream)
+                             const int32_t* radii, const float* v_splats, const float* v_depth_model,
+                             int32_t accumulate, float* v_means, float* v_log_scales, float* v_quats,
+                             float* v_logits, float* v_colors, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
@@ -182,18 +184,21 @@ int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t 
             GM_REQUIRE(aligned16(colors) && aligned16(v_colors), "SH coefficients and their gradient must be "
                        "16-byte aligned");
     }
+    GM_REQUIRE(!v_depth_model || aligned16(v_depth_model), "v_depth_model must be 16-byte aligned");
     cudaError_t e = gm::project_bwd(gm::make_cam(*cam), opts->sh_degree, N, means, log_scales, quats, logits, colors,
-                                    radii, v_splats, accumulate != 0, v_means, v_log_scales, v_quats, v_logits,
-                                    v_colors, (cudaStream_t)stream);
+                                    radii, v_splats, v_depth_model, accumulate != 0, v_means, v_log_scales, v_quats,
+                                    v_logits, v_colors, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_bwd");
 }
 
 int gm_project_gaussians_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N, const float* means,
                                const float* log_scales, const float* quats, const float* logits, const float* colors,
-                               float* splats, int32_t* radii, int32_t* tiles_touched, void* stream)
+                               float* splats, int32_t* radii, int32_t* tiles_touched, float* depth_model,
+                               void* stream)
 {
     g_err[0] = 0;
     GM_REQUIRE(cams && V >= 1 && V <= GM_MAX_VIEWS, "cams is NULL or V = %d not in 1..%d", V, GM_MAX_VIEWS);
+    GM_REQUIRE(!depth_model || aligned16(depth_model), "depth_model must be 16-byte aligned");
     for (int v = 0; v < V; ++v)
         if (int st = check_cam(cams + v)) return st;
     GM_REQUIRE(opts, "opts is NULL");
@@ -209,15 +214,16 @@ int gm_project_gaussians_views(const gm_camera* cams, int32_t V, const gm_opts* 
     gm::Cam c[GM_MAX_VIEWS];
     for (int v = 0; v < V; ++v) c[v] = gm::make_cam(cams[v]);
     cudaError_t e = gm::project_views(c, V, opts->sh_degree, N, means, log_scales, quats, logits, colors, splats, radii,
-                                      tiles_touched, (cudaStream_t)stream);
+                                      tiles_touched, depth_model, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_views");
 }
 
 int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N,
                                    const float* means, const float* log_scales, const float* quats,
                                    const float* logits, const float* colors, const int32_t* radii,
-                                   const float* v_splats, int32_t accumulate, float* v_means, float* v_log_scales,
-                                   float* v_quats, float* v_logits, float* v_colors, void* stream)
+                                   const float* v_splats, const float* v_depth_model, int32_t accumulate,
+                                   float* v_means, float* v_log_scales, float* v_quats, float* v_logits,
+                                   float* v_colors, void* stream)
 {
     g_err[0] = 0;
     GM_REQUIRE(cams && V >= 1 && V <= GM_MAX_VIEWS, "cams is NULL or V = %d not in 1..%d", V, GM_MAX_VIEWS);
@@ -237,9 +243,10 @@ int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_op
     }
     gm::Cam c[GM_MAX_VIEWS];
     for (int v = 0; v < V; ++v) c[v] = gm::make_cam(cams[v]);
+    GM_REQUIRE(!v_depth_model || aligned16(v_depth_model), "v_depth_model must be 16-byte aligned");
     cudaError_t e = gm::project_bwd_views(c, V, opts->sh_degree, N, means, log_scales, quats, logits, colors, radii,
-                                          v_splats, accumulate != 0, v_means, v_log_scales, v_quats, v_logits,
-                                          v_colors, (cudaStream_t)stream);
+                                          v_splats, v_depth_model, accumulate != 0, v_means, v_log_scales, v_quats,
+                                          v_logits, v_colors, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_bwd_views");
 }
 
@@ -268,7 +275,9 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
     GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), opts->cull_occluded != 0, opts->tile_test != 0, N, splats,
+    // the soft split lets a Gaussian behind the mesh show through a little: no cull
+    const bool cull = opts->cull_occluded != 0 && !(opts->softness > 0.0f);
+    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), cull, opts->tile_test != 0, N, splats,
                                        radii, tile_far,
                                        tile_full, keys, gids, tile_range, cap, counters, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "gm_bin_sort_gaussians");
@@ -276,36 +285,45 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
 }
 
 int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const int32_t* tile_range,
-                            const int32_t* gids,
-                            const float* splats, const float* mesh_depth, const float* mesh_rgb,
-                            const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha, float* T_final,
-                            int32_t* n_contrib, uint64_t* stats, void* stream)
+                            const int32_t* gids, const float* splats, const float* depth_model,
+                            const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id, float* out_rgb,
+                            float* out_depth, float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats,
+                            void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
     GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(opts->softness >= 0.0f, "negative softness");
     GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id, "an input is NULL");
     GM_REQUIRE(out_rgb && out_depth && out_alpha && T_final && n_contrib, "an output is NULL");
     GM_REQUIRE(N >= 0, "negative N");
     GM_REQUIRE(N == 0 || (splats && gids), "splats / gids is NULL");
     GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
-    cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, tile_range, gids, splats, mesh_depth, mesh_rgb,
-                                      face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, stats,
-                                      (cudaStream_t)stream);
+    const bool soft = opts->softness > 0.0f;
+    GM_REQUIRE(!soft || N == 0 || (depth_model && aligned16(depth_model)),
+               "the soft split needs a 16-byte aligned depth_model");
+    cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, opts->softness, tile_range, gids, splats,
+                                      depth_model, mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
+                                      T_final, n_contrib, stats, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_fwd");
 }
 
 int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const int32_t* tile_range,
-                            const int32_t* gids,
-                            const float* splats, const float* mesh_depth, const float* mesh_rgb,
-                            const int32_t* face_id, const float* T_final, const int32_t* n_contrib,
-                            const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
+                            const int32_t* gids, const float* splats, const float* depth_model,
+                            const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
+                            const float* T_final, const int32_t* n_contrib, const float* g_rgb, const float* g_depth,
+                            const float* g_alpha, float* v_splats, float* v_depth_model, float* v_mesh_depth,
                             const float* V, int32_t nV, const int32_t* F, int32_t nF, const float* vcol,
                             float* v_verts, float* v_vcol, uint64_t* stats, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
     GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(opts->softness >= 0.0f, "negative softness");
+    const bool soft = opts->softness > 0.0f;
+    if (soft && v_splats && N > 0)
+        GM_REQUIRE(depth_model && aligned16(depth_model) && v_depth_model && aligned16(v_depth_model),
+                   "the soft split needs 16-byte aligned depth_model and v_depth_model");
     GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id && T_final && n_contrib, "an input is NULL");
     GM_REQUIRE(g_rgb && g_depth && g_alpha, "an upstream gradient is NULL");
     GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
@@ -314,14 +332,17 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     GM_REQUIRE(N == 0 || !v_splats || (splats && gids), "splats / gids is NULL");
     const bool mesh_grads = v_verts || v_vcol;
     if (mesh_grads) GM_REQUIRE(v_verts && v_vcol && (nF == 0 || (F && V && vcol)), "mesh gradient arguments incomplete");
+    if (soft && mesh_grads) GM_REQUIRE(v_mesh_depth, "the soft split's mesh gradients need v_mesh_depth");
     cudaStream_t s = (cudaStream_t)stream;
     const gm::Cam c = gm::make_cam(*cam);
     cudaError_t e = cudaSuccess;
     if (v_splats)
-        e = gm::composite_bwd(c, opts->bg, N, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id, T_final, n_contrib,
-                              g_rgb, g_depth, g_alpha, v_splats, stats, s);
+        e = gm::composite_bwd(c, opts->bg, N, opts->softness, tile_range, gids, splats, depth_model, mesh_depth,
+                              mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model,
+                              soft ? v_mesh_depth : nullptr, stats, s);
     if (e == cudaSuccess && mesh_grads && nF > 0)
-        e = gm::mesh_bwd(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, v_verts, v_vcol, s);
+        e = gm::mesh_bwd(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, soft ? v_mesh_depth : nullptr,
+                         v_verts, v_vcol, s);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_bwd");
 }
 

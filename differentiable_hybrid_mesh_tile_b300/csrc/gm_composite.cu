@@ -147,15 +147,46 @@ __device__ __forceinline__ void stage_empty(float4& C, float4& H)
     C = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-template <bool STATS>
+// f = Phi(x) <= Phi(-SPLIT_TAIL) = 0.0030 once x <= -SPLIT_TAIL, so alpha f
+// <= 0.99 x 0.0030 < 1/255: the Gaussian is skipped at that pixel.
+constexpr float SPLIT_TAIL = 2.75f;
+
+// Staged depth model of the soft split: (g_u, g_v, kappa = 1 / (sigma_z
+// softness), z_hide); f = Phi((D - z*) kappa), z* = z_c + g . (p - mean2d).
+// With the reach R (z* >= z_c - R wherever alpha can reach 1/255), a mesh depth
+// D < z_hide = z_c - R - SPLIT_TAIL sigma_z softness (less a rounding margin)
+// puts x below -SPLIT_TAIL: the Gaussian is hidden at every such pixel.
+__device__ __forceinline__ float4 stage_depth_model(const float4* __restrict__ depth_model, int64_t g, float softness,
+                                                    float z)
+{
+    const float4 m = depth_model[g];
+    const float band = m.z * softness;
+    const float hide = z - fmaf(SPLIT_TAIL, band, m.w) * 1.0001f - 2e-6f * fabsf(z);
+    return make_float4(m.x, m.y, 1.0f / band, hide);
+}
+
+// The largest mesh depth over this warp's covered pixels (+inf if one of its
+// pixels in the image is not covered: there every Gaussian is seen whole), with
+// a rounding margin; Gaussians whose z_hide lies beyond it draw nothing here.
+__device__ __forceinline__ float warp_hide_depth(bool inside, bool cov, float D)
+{
+    float k = !inside ? -INFINITY : (cov ? D : INFINITY);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) k = fmaxf(k, __shfl_xor_sync(0xffffffffu, k, o));
+    return isinf(k) ? k : k + 4e-6f * fabsf(k);
+}
+
+template <bool STATS, bool SOFT>
 __global__ void __launch_bounds__(CTA_THREADS)
-k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
-                const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
+k_composite_fwd(Cam c, float3 bg, int N, float softness, const int2* __restrict__ tile_range,
+                const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id, float* __restrict__ out_rgb,
                 float* __restrict__ out_depth, float* __restrict__ out_alpha, float* __restrict__ T_final,
                 int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ stats)
 {
     __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
+    __shared__ float4 sD[SOFT ? CTA_THREADS : 1];
     int tile;
     const PixelMap pm = pixel_of(c, tile);
     const bool inside = pm.i < c.W && pm.j < c.H;
@@ -167,6 +198,9 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         D = mesh_depth[pix];
         cov = face_id[pix] >= 0;
     }
+    // soft split at this pixel: covered by the mesh (elsewhere D = +inf, f = 1)
+    const bool soft = SOFT && cov;
+    const float Dw = SOFT ? warp_hide_depth(inside, cov, D) : INFINITY;
     float T = 1.0f, Cr = 0.0f, Cg = 0.0f, Cb = 0.0f, Z = 0.0f;
     int last = 0;
     uint32_t visited = 0, blended = 0;
@@ -179,10 +213,12 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         const int n = min(CTA_THREADS, r.y - b);
         if ((int)threadIdx.x < n) {
             const int64_t g = gids[b + threadIdx.x];
-            if (g >= 0 && g < N)
+            if (g >= 0 && g < N) {
                 stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
-            else  // an id outside [0, N): an entry that draws nothing
+                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, softness, sC[threadIdx.x].y);
+            } else {  // an id outside [0, N): an entry that draws nothing
                 stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
+            }
         }
         __syncthreads();
         // walk this warp's hits: a ballot per 32 staged records marks those that can
@@ -191,7 +227,8 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
             if (__all_sync(0xffffffffu, done)) break;
             const int kk = m * 32 + (threadIdx.x & 31);
             uint32_t mask =
-                __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0));
+                __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0) &&
+                                               !(SOFT && sD[kk].w > Dw));
             while (mask) {
                 // two hits at a time: both evaluated (independent) before the
                 // transmittance chain takes them in list order
@@ -217,19 +254,27 @@ k_composite_fwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (done || kk2[h] < 0) continue;
-                    // sorted by depth: once a Gaussian is not in front of the mesh, none after it is
-                    if (!(Cq[h].y < D)) {
+                    // hard test, sorted by depth: once a Gaussian is not in front of the
+                    // mesh, none after it is
+                    if (!soft && !(Cq[h].y < D)) {
                         done = true;
                         continue;
                     }
                     if (STATS) ++visited;
                     if (ev[h].skip) continue;
-                    const float Tn = __fmul_rn(T, __fsub_rn(1.0f, ev[h].alpha));
+                    float a = ev[h].alpha;
+                    if (soft) {  // the Gaussian's part in front of the mesh
+                        const float4 Dm = sD[kk2[h]];
+                        const float zs = fmaf(Dm.x, ev[h].dx, fmaf(Dm.y, ev[h].dy, Cq[h].y));
+                        a *= normcdff((D - zs) * Dm.z);
+                        if (a < ALPHA_MIN) continue;
+                    }
+                    const float Tn = __fmul_rn(T, __fsub_rn(1.0f, a));
                     if (Tn <= T_STOP) {
                         done = true;
                         continue;
                     }
-                    const float w = ev[h].alpha * T;
+                    const float w = a * T;
                     Cr = fmaf(w, Bq[h].z, Cr);
                     Cg = fmaf(w, Bq[h].w, Cg);
                     Cb = fmaf(w, Cq[h].x, Cb);
@@ -278,8 +323,11 @@ __device__ __forceinline__ float rs_combine(float a, float b, int lane, int o)
 // < 32 is component i >> 2 of entry i & 3 (0 ds dx, 1 ds dy, 2 ds dx^2 / 2,
 // 3 ds dx dy, 4 ds dy^2 / 2, 5 dL/d opacity, 6 w g_r, 7 w g_g), value 32 + i
 // is component 8 + (i >> 2) (w g_b, w g_depth) of entry i & 3.
+// With the soft split, four more per entry: 10 pz, 11 pz dx, 12 pz dy, 13 psx,
+// where pz = dL/dx kappa and psx = dL/dx x for the split's argument x.
 struct GroupTerms {
     float pw[GROUP], pvo[GROUP], pds[GROUP], pdx[GROUP], pdy[GROUP];
+    float pz[GROUP], psx[GROUP];
     float gr, gg, gb, gz;
     __device__ __forceinline__ float v(int i) const
     {
@@ -294,7 +342,12 @@ struct GroupTerms {
             case 6: return pw[e] * gr;
             case 7: return pw[e] * gg;
             case 8: return pw[e] * gb;
-            default: return pw[e] * gz;
+            case 9: return pw[e] * gz;
+            case 10: return pz[e];
+            case 11: return pz[e] * pdx[e];
+            case 12: return pz[e] * pdy[e];
+            case 13: return psx[e];
+            default: return 0.0f;
         }
     }
 };
@@ -303,14 +356,14 @@ struct GroupTerms {
 // of value L (levels xor 16, 8, 4, 2, 1; 31 shuffles).  Node I of level L
 // combines nodes I and I + 32 / 2^L of level L - 1; the tree is walked depth
 // first so that few partial sums are live at once.
-template <int L, int I>
+template <int L, int I, int BASE = 0>
 __device__ __forceinline__ float rs32(const GroupTerms& g, int lane)
 {
     if constexpr (L == 0) {
-        return g.v(I);
+        return g.v(BASE + I);
     } else {
-        const float a = rs32<L - 1, I>(g, lane);
-        const float b = rs32<L - 1, I + (32 >> L)>(g, lane);
+        const float a = rs32<L - 1, I, BASE>(g, lane);
+        const float b = rs32<L - 1, I + (32 >> L), BASE>(g, lane);
         return rs_combine(a, b, lane, 16 >> (L - 1));
     }
 }
@@ -341,20 +394,40 @@ __device__ __forceinline__ void flush_grad(float* __restrict__ v_splats, int g, 
     atomicAdd(dst + 2, make_float4(acc[8], acc[9], 0.0f, 0.0f));
 }
 
+// The soft split's sums of one entry, acc[10..13] = (sum pz, sum pz dx,
+// sum pz dy, sum psx), become gradients: the split's argument x = (D - z*)
+// kappa, z* = z_c + g . (p - mean2d), so dL/d mean2d += pz g, dL/d z_c -= pz,
+// dL/d g -= pz d, dL/d sigma_z = -psx / sigma_z (kappa = 1 / (sigma_z s)).
+__device__ __forceinline__ void flush_grad_soft(float* __restrict__ v_splats, float* __restrict__ v_depth_model,
+                                                int g, float* acc, float4 Dm, float softness)
+{
+    acc[0] += acc[10] * Dm.x;
+    acc[1] += acc[10] * Dm.y;
+    acc[9] -= acc[10];
+    flush_grad(v_splats, g, acc);
+    atomicAdd(reinterpret_cast<float4*>(v_depth_model) + g,
+              make_float4(-acc[11], -acc[12], -acc[13] * Dm.z * softness, 0.0f));
+}
+
 // Ten CTAs of 128 threads per SM (at most 51 registers a thread): the kernel
-// is bound by instruction latency, and resident warps hide it.
-template <bool STATS>
-__global__ void __launch_bounds__(CTA_THREADS, 10)
-k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
-                const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
+// is bound by instruction latency, and resident warps hide it.  The soft split
+// carries four more terms per entry: eight CTAs (64 registers).
+template <bool STATS, bool SOFT>
+__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : 10)
+k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict__ tile_range,
+                const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
                 const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
                 const float* __restrict__ g_rgb, const float* __restrict__ g_depth, const float* __restrict__ g_alpha,
-                float* __restrict__ v_splats, unsigned long long* __restrict__ stats)
+                float* __restrict__ v_splats, float* __restrict__ v_depth_model, float* __restrict__ v_mesh_depth,
+                unsigned long long* __restrict__ stats)
 {
+    constexpr int NACC = SOFT ? NGRAD + 4 : NGRAD;
     __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
+    __shared__ float4 sD[SOFT ? CTA_THREADS : 1];
     __shared__ int sG[CTA_THREADS];
-    __shared__ float sAcc[CTA_THREADS][NGRAD + 1];
+    __shared__ float sAcc[CTA_THREADS][NACC + 1];
     __shared__ int s_max_last;
     int tile;
     const PixelMap pm = pixel_of(c, tile);
@@ -368,9 +441,11 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     // behind = (colour, depth) accumulated behind the current Gaussian, dotted with
     // this pixel's upstream gradient (g_rgb, g_depth); starts with the terminal layer
     float behind = 0.f, aterm = 0.f;
+    bool cov = false;
+    float vD = 0.0f;  // soft split: dL/d mesh depth at this pixel
     if (inside) {
         D = mesh_depth[pix];
-        const bool cov = face_id[pix] >= 0;
+        cov = face_id[pix] >= 0;
         T = T_final[pix];
         last = n_contrib[pix];
         gr = g_rgb[3 * pix]; gg = g_rgb[3 * pix + 1]; gb = g_rgb[3 * pix + 2];
@@ -391,12 +466,20 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
     __syncthreads();
     const int2 r = tile_range[tile];
     const int end = r.x + s_max_last;
+    const bool soft = SOFT && cov;
+    const float Dw = SOFT ? warp_hide_depth(inside, cov, D) : INFINITY;
     uint32_t visited = 0, contributed = 0;
     int n_prev = 0;
     for (int b_end = end;; b_end -= CTA_THREADS) {
         // the previous batch's gradients go out and the next batch comes in, each
         // thread on its own slot, so one barrier covers both
-        if ((int)threadIdx.x < n_prev && sG[threadIdx.x] >= 0) flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x]);
+        if ((int)threadIdx.x < n_prev && sG[threadIdx.x] >= 0) {
+            if (SOFT)
+                flush_grad_soft(v_splats, v_depth_model, sG[threadIdx.x], sAcc[threadIdx.x], sD[threadIdx.x],
+                                softness);
+            else
+                flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x]);
+        }
         if (b_end <= r.x) break;
         const int b0 = max(r.x, b_end - CTA_THREADS);
         const int n = b_end - b0;
@@ -404,12 +487,14 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
             int g = gids[b0 + threadIdx.x];
             if (g < 0 || g >= N) g = -1;  // an entry that draws nothing and gets no gradient
             sG[threadIdx.x] = g;
-            if (g >= 0)
+            if (g >= 0) {
                 stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
-            else
+                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, softness, sC[threadIdx.x].y);
+            } else {
                 stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
+            }
 #pragma unroll
-            for (int q = 0; q < NGRAD; ++q) sAcc[threadIdx.x][q] = 0.0f;
+            for (int q = 0; q < NACC; ++q) sAcc[threadIdx.x][q] = 0.0f;
         }
         __syncthreads();
         // this warp only needs the entries in front of its last composited one, and of
@@ -419,7 +504,8 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         for (int m = k_top >> 5; m >= 0; --m) {
             const int kk = m * 32 + lane;
             uint32_t mask =
-                __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0));
+                __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0) &&
+                                               !(SOFT && sD[kk].w > Dw));
             while (mask) {
                 int kj[GROUP];
 #pragma unroll
@@ -433,32 +519,50 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                     }
                 }
                 // per entry: w = alpha T_front, vo = dL/d opacity, ds = dL/d sigma
-                float pw[GROUP], pvo[GROUP], pds[GROUP];
+                // (soft split: pz = dL/dx kappa, psx = dL/dx x)
+                float pw[GROUP], pvo[GROUP], pds[GROUP], pz[GROUP], psx[GROUP];
                 bool any = false;
 #pragma unroll
                 for (int jj = 0; jj < GROUP; ++jj) {
-                    pw[jj] = pvo[jj] = pds[jj] = 0.0f;
+                    pw[jj] = pvo[jj] = pds[jj] = pz[jj] = psx[jj] = 0.0f;
                     const int k = kj[jj];
                     if (k < 0 || !inside || b0 - r.x + k >= last) continue;
                     const float4 C3 = sC[k];
-                    if (!(C3.y < D)) continue;
+                    if (!soft && !(C3.y < D)) continue;
                     if (STATS) ++visited;
                     const float4 A = sA[k], B = sB[k];
                     const Eval e = eval_splat(A, B, px, py);
                     if (e.skip) continue;
+                    float a = e.alpha, f = 1.0f, x = 0.0f, kap = 0.0f;
+                    if (soft) {  // the composited alpha is alpha f, f = Phi(x)
+                        const float4 Dm = sD[k];
+                        const float zs = fmaf(Dm.x, e.dx, fmaf(Dm.y, e.dy, C3.y));
+                        kap = Dm.z;
+                        x = (D - zs) * kap;
+                        f = normcdff(x);
+                        a = e.alpha * f;
+                        if (a < ALPHA_MIN) continue;
+                    }
                     if (STATS) ++contributed;
                     any = true;
-                    const float rom = __fdividef(1.0f, 1.0f - e.alpha);
+                    const float rom = __fdividef(1.0f, 1.0f - a);
                     const float Tp = T * rom;  // transmittance in front of this Gaussian
-                    const float w = e.alpha * Tp;
+                    const float w = a * Tp;
                     const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
-                    const float dLda = Tp * front + (aterm - behind) * rom;
+                    const float dLda = Tp * front + (aterm - behind) * rom;  // dL / d(composited alpha)
                     behind = fmaf(w, front, behind);
                     T = Tp;
                     pw[jj] = w;
+                    const float dLdal = SOFT ? dLda * f : dLda;  // dL / d alpha
                     if (!e.clamped) {  // alpha clamped at 0.99 has no opacity / sigma gradient
-                        pvo[jj] = dLda * e.G;
-                        pds[jj] = -dLda * e.alpha;  // d alpha / d sigma = -alpha
+                        pvo[jj] = dLdal * e.G;
+                        pds[jj] = -dLdal * e.alpha;  // d alpha / d sigma = -alpha
+                    }
+                    if (soft) {  // dL/dx = dLda alpha phi(x), phi the standard normal density
+                        const float psi = dLda * e.alpha * (0.3989422804014327f * __expf(-0.5f * x * x));
+                        pz[jj] = psi * kap;
+                        psx[jj] = psi * x;
+                        vD += psi * kap;
                     }
                 }
                 if (__any_sync(0xffffffffu, any)) {
@@ -480,6 +584,13 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                         gt.pdy[jj] = __fsub_rn(py, mean.y);
                     }
                     gt.gr = gr; gt.gg = gg; gt.gb = gb; gt.gz = gz;
+                    if (SOFT) {
+#pragma unroll
+                        for (int jj = 0; jj < GROUP; ++jj) {
+                            gt.pz[jj] = pz[jj];
+                            gt.psx[jj] = psx[jj];
+                        }
+                    }
                     float tot = rs32<5, 0>(gt, lane);  // component lane >> 2 of entry lane & 3
                     const int q = lane >> 2, e = lane & 3;
                     const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
@@ -491,12 +602,18 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
                         tot = q == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
                     }
                     if (k >= 0 && tot != 0.0f) atomicAdd(&sAcc[k][q], tot);
-                    float t8 = rs8<3, 0>(gt, lane);
-                    t8 += __shfl_xor_sync(0xffffffffu, t8, 2);
-                    t8 += __shfl_xor_sync(0xffffffffu, t8, 1);
-                    const int j = (lane >> 2) & 7, e8 = j & 3;
-                    const int k8 = e8 == 0 ? kj[0] : e8 == 1 ? kj[1] : e8 == 2 ? kj[2] : kj[3];
-                    if ((lane & 3) == 0 && k8 >= 0 && t8 != 0.0f) atomicAdd(&sAcc[k8][8 + (j >> 2)], t8);
+                    if (SOFT) {
+                        // values 32..55 (components 8..13): a second full reduce-scatter
+                        const float t2 = rs32<5, 0, 32>(gt, lane);
+                        if (q < 6 && k >= 0 && t2 != 0.0f) atomicAdd(&sAcc[k][8 + q], t2);
+                    } else {
+                        float t8 = rs8<3, 0>(gt, lane);
+                        t8 += __shfl_xor_sync(0xffffffffu, t8, 2);
+                        t8 += __shfl_xor_sync(0xffffffffu, t8, 1);
+                        const int j = (lane >> 2) & 7, e8 = j & 3;
+                        const int k8 = e8 == 0 ? kj[0] : e8 == 1 ? kj[1] : e8 == 2 ? kj[2] : kj[3];
+                        if ((lane & 3) == 0 && k8 >= 0 && t8 != 0.0f) atomicAdd(&sAcc[k8][8 + (j >> 2)], t8);
+                    }
                 }
             }
         }
@@ -507,34 +624,41 @@ k_composite_bwd(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, co
         block_count(visited, stats);
         block_count(contributed, stats + 1);
     }
+    if (SOFT && inside && v_mesh_depth) v_mesh_depth[pix] = vD;
 }
 
 }  // namespace
 
-cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, const int32_t* tile_range, const int32_t* gids,
-                          const float* splats, const float* mesh_depth, const float* mesh_rgb,
-                          const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
-                          float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s)
+cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+                          const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
+                          const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
+                          float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s)
 {
-    auto kern = stats ? k_composite_fwd<true> : k_composite_fwd<false>;
+    const bool soft = softness > 0.0f;
+    auto kern = soft ? (stats ? k_composite_fwd<true, true> : k_composite_fwd<false, true>)
+                     : (stats ? k_composite_fwd<true, false> : k_composite_fwd<false, false>);
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
-        c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
-        reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
-        T_final, n_contrib, reinterpret_cast<unsigned long long*>(stats));
+        c, make_float3(bg[0], bg[1], bg[2]), N, softness, reinterpret_cast<const int2*>(tile_range), gids,
+        reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
+        face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, reinterpret_cast<unsigned long long*>(stats));
     return cudaGetLastError();
 }
 
-cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, const int32_t* tile_range, const int32_t* gids,
-                          const float* splats, const float* mesh_depth, const float* mesh_rgb,
-                          const int32_t* face_id, const float* T_final, const int32_t* n_contrib,
-                          const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
-                          uint64_t* stats, cudaStream_t s)
+cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+                          const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
+                          const float* mesh_rgb, const int32_t* face_id, const float* T_final,
+                          const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
+                          float* v_splats, float* v_depth_model, float* v_mesh_depth, uint64_t* stats,
+                          cudaStream_t s)
 {
-    auto kern = stats ? k_composite_bwd<true> : k_composite_bwd<false>;
+    const bool soft = softness > 0.0f;
+    auto kern = soft ? (stats ? k_composite_bwd<true, true> : k_composite_bwd<false, true>)
+                     : (stats ? k_composite_bwd<true, false> : k_composite_bwd<false, false>);
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
-        c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
-        reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth,
-        g_alpha, v_splats, reinterpret_cast<unsigned long long*>(stats));
+        c, make_float3(bg[0], bg[1], bg[2]), N, softness, reinterpret_cast<const int2*>(tile_range), gids,
+        reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
+        face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth,
+        reinterpret_cast<unsigned long long*>(stats));
     return cudaGetLastError();
 }
 

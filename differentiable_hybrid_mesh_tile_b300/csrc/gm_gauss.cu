@@ -18,11 +18,12 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
                                                  const float* __restrict__ log_scales,
                                                  const float4* __restrict__ quats, const float* __restrict__ logits,
                                                  const float* __restrict__ colors, float4& o0, float4& o1, float4& o2,
-                                                 int& rad, int& touched)
+                                                 float4& dm, int& rad, int& touched)
 {
     o0 = make_float4(0.f, 0.f, 0.f, 0.f);
     o1 = o0;
     o2 = o0;
+    dm = o0;
     rad = 0;
     touched = 0;
     const float mx = __ldg(means + 3 * (int64_t)g), my = __ldg(means + 3 * (int64_t)g + 1),
@@ -109,6 +110,20 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
                 o0 = make_float4(u, v, cc * idet, -b * idet);
                 o1 = make_float4(a * idet, op, rgb[0], rgb[1]);
                 o2 = make_float4(rgb[2], tz, 0.0f, 0.0f);
+                // depth model of the soft split: with Sigma_c = WM WM^T, Sigma_uv,z =
+                // J Sigma_c e_z = G WM_2^T and Sigma_zz = |WM_2|^2; g = conic Sigma_uv,z
+                // (the conic is (Sigma_uv + 0.3 I)^-1), sigma_z^2 = Sigma_zz - Sigma_uv,z . g
+                const float bu = G0[0] * WM[2][0] + G0[1] * WM[2][1] + G0[2] * WM[2][2];
+                const float bv = G1[0] * WM[2][0] + G1[1] * WM[2][1] + G1[2] * WM[2][2];
+                const float szz = WM[2][0] * WM[2][0] + WM[2][1] * WM[2][1] + WM[2][2] * WM[2][2];
+                const float gu = (cc * bu - b * bv) * idet, gv = (a * bv - b * bu) * idet;
+                const float quad = bu * gu + bv * gv;  // g^T (Sigma_uv + 0.3 I) g
+                const float var = szz - quad;
+                // reach: over the ellipse where alpha can reach 1/255 (sigma <= ln(255 o),
+                // with the tile test's margins), g . d <= sqrt(2 ln(255 o) g^T Sigma2 g)
+                const float L = fmaf(fmaxf(logf(255.0f * op), 0.0f), 1.001f, 1e-4f);
+                const float reach = sqrtf(2.0f * L * fmaxf(quad, 0.0f)) * 1.002f;
+                dm = make_float4(gu, gv, sqrtf(fmaxf(var, 1e-12f)), reach);
             } else {
                 rad = 0;
             }
@@ -120,18 +135,20 @@ template <int DEG>
 __global__ void __launch_bounds__(256)
 k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
           const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
-          float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched)
+          float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched,
+          float4* __restrict__ depth_model)
 {
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= N) return;
-    float4 o0, o1, o2;
+    float4 o0, o1, o2, dm;
     int rad, touched;
-    project_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, o0, o1, o2, rad, touched);
+    project_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad, touched);
     splats[3 * (int64_t)g] = o0;
     splats[3 * (int64_t)g + 1] = o1;
     splats[3 * (int64_t)g + 2] = o2;
     radii[g] = rad;
     tiles_touched[g] = touched;
+    if (depth_model) depth_model[g] = dm;
 }
 
 // Several views in one launch: each thread takes one Gaussian through every
@@ -141,14 +158,15 @@ template <int DEG>
 __global__ void __launch_bounds__(256)
 k_project_views(ViewBatch vb, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
                 const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
-                float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched)
+                float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched,
+                float4* __restrict__ depth_model)
 {
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= N) return;
     for (int v = 0; v < vb.n; ++v) {
-        float4 o0, o1, o2;
+        float4 o0, o1, o2, dm;
         int rad, touched;
-        project_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors, o0, o1, o2, rad,
+        project_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad,
                               touched);
         const int64_t i = (int64_t)v * N + g;
         splats[3 * i] = o0;
@@ -156,6 +174,7 @@ k_project_views(ViewBatch vb, int N, const float* __restrict__ means, const floa
         splats[3 * i + 2] = o2;
         radii[i] = rad;
         tiles_touched[i] = touched;
+        if (depth_model) depth_model[i] = dm;
     }
 }
 
@@ -488,14 +507,16 @@ size_t a256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
                     const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
-                    int32_t* tiles_touched, cudaStream_t s)
+                    int32_t* tiles_touched, float* depth_model, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
     const ProjConsts pc = make_proj_consts(c);
     const int grid = (N + 255) / 256;
     auto* q4 = reinterpret_cast<const float4*>(quats);
     auto* s4 = reinterpret_cast<float4*>(splats);
-#define GM_PROJ(D) k_project<D><<<grid, 256, 0, s>>>(c, pc, N, means, log_scales, q4, logits, colors, s4, radii, tiles_touched)
+    auto* dm4 = reinterpret_cast<float4*>(depth_model);
+#define GM_PROJ(D) k_project<D><<<grid, 256, 0, s>>>(c, pc, N, means, log_scales, q4, logits, colors, s4, radii, \
+                                                     tiles_touched, dm4)
     switch (sh_degree) {
         case -1: GM_PROJ(-1); break;
         case 0: GM_PROJ(0); break;
@@ -510,7 +531,7 @@ cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, cons
 
 cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const float* means, const float* log_scales,
                           const float* quats, const float* logits, const float* colors, float* splats,
-                          int32_t* radii, int32_t* tiles_touched, cudaStream_t s)
+                          int32_t* radii, int32_t* tiles_touched, float* depth_model, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
     const int grid = (N + 255) / 256;
@@ -524,8 +545,9 @@ cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const fl
         }
         const int64_t off = (int64_t)v0 * N;
         auto* s4 = reinterpret_cast<float4*>(splats + 12 * off);
+        auto* dm4 = depth_model ? reinterpret_cast<float4*>(depth_model + 4 * off) : nullptr;
 #define GM_PROJ_V(D) k_project_views<D><<<grid, 256, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, s4, \
-                                                             radii + off, tiles_touched + off)
+                                                             radii + off, tiles_touched + off, dm4)
         switch (sh_degree) {
             case -1: GM_PROJ_V(-1); break;
             case 0: GM_PROJ_V(0); break;

@@ -184,35 +184,37 @@ cudaError_t interp(const Cam& c, const float* V, int nV, const int32_t* F, int n
                    cudaStream_t s);
 cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
                      const int32_t* face_id, const float* T_final, const float* g_rgb, const float* g_depth,
-                     float* v_verts, float* v_vcol, cudaStream_t s);
+                     const float* v_mesh_depth, float* v_verts, float* v_vcol, cudaStream_t s);
 
 cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
                     const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
-                    int32_t* tiles_touched, cudaStream_t s);
+                    int32_t* tiles_touched, float* depth_model, cudaStream_t s);
 cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const float* means, const float* log_scales,
                           const float* quats, const float* logits, const float* colors, float* splats,
-                          int32_t* radii, int32_t* tiles_touched, cudaStream_t s);
+                          int32_t* radii, int32_t* tiles_touched, float* depth_model, cudaStream_t s);
 cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, const float* means,
                               const float* log_scales, const float* quats, const float* logits, const float* colors,
-                              const int32_t* radii, const float* v_splats, bool accumulate, float* v_means,
-                              float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s);
+                              const int32_t* radii, const float* v_splats, const float* v_depth_model,
+                              bool accumulate, float* v_means, float* v_log_scales, float* v_quats, float* v_logits,
+                              float* v_colors, cudaStream_t s);
 cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
                         const float* quats, const float* logits, const float* colors, const int32_t* radii,
-                        const float* v_splats, bool accumulate, float* v_means, float* v_log_scales, float* v_quats,
-                        float* v_logits, float* v_colors, cudaStream_t s);
+                        const float* v_splats, const float* v_depth_model, bool accumulate, float* v_means,
+                        float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s);
 size_t gauss_bin_ws_bytes(int N, int cap);
 cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
 
-cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, const int32_t* tile_range, const int32_t* gids,
-                          const float* splats, const float* mesh_depth, const float* mesh_rgb,
-                          const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
-                          float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s);
-cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, const int32_t* tile_range, const int32_t* gids,
-                          const float* splats, const float* mesh_depth, const float* mesh_rgb,
-                          const int32_t* face_id, const float* T_final, const int32_t* n_contrib,
-                          const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
-                          uint64_t* stats, cudaStream_t s);
+cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+                          const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
+                          const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
+                          float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s);
+cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+                          const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
+                          const float* mesh_rgb, const int32_t* face_id, const float* T_final,
+                          const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
+                          float* v_splats, float* v_depth_model, float* v_mesh_depth, uint64_t* stats,
+                          cudaStream_t s);
 
 }  // namespace gm

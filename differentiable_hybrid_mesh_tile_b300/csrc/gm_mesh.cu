@@ -305,8 +305,8 @@ __device__ __forceinline__ float warp_sum(float v)
 __global__ void __launch_bounds__(TILE_PIX)
 k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
            const float* __restrict__ vcol, const int32_t* __restrict__ face_id, const float* __restrict__ T_final,
-           const float* __restrict__ g_rgb, const float* __restrict__ g_depth, float* __restrict__ v_verts,
-           float* __restrict__ v_vcol)
+           const float* __restrict__ g_rgb, const float* __restrict__ g_depth,
+           const float* __restrict__ v_mesh_depth, float* __restrict__ v_verts, float* __restrict__ v_vcol)
 {
     const int tile = blockIdx.x;
     const int tx = tile % c.TW, ty = tile / c.TW;
@@ -327,7 +327,9 @@ k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
             for (int ch = 0; ch < 3; ++ch) C[k][ch] = __ldg(vcol + 3 * (int64_t)vid[k] + ch);
         const float T = T_final[pix];
         const float gc[3] = {T * g_rgb[3 * pix], T * g_rgb[3 * pix + 1], T * g_rgb[3 * pix + 2]};
-        interp_grad(c, X, C, (float)i + 0.5f, (float)j + 0.5f, T * g_depth[pix], gc, gX, gC);
+        // dL/dD: through the depth output (T D), and through the soft split when given
+        const float gD = T * g_depth[pix] + (v_mesh_depth ? v_mesh_depth[pix] : 0.0f);
+        interp_grad(c, X, C, (float)i + 0.5f, (float)j + 0.5f, gD, gc, gX, gC);
     }
     // one set of atomics per distinct face in the warp
     unsigned pending = __ballot_sync(0xffffffffu, act);
@@ -436,10 +438,10 @@ cudaError_t interp(const Cam& c, const float* V, int nV, const int32_t* F, int n
 
 cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
                      const int32_t* face_id, const float* T_final, const float* g_rgb, const float* g_depth,
-                     float* v_verts, float* v_vcol, cudaStream_t s)
+                     const float* v_mesh_depth, float* v_verts, float* v_vcol, cudaStream_t s)
 {
-    k_mesh_bwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, v_verts,
-                                                 v_vcol);
+    k_mesh_bwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, v_mesh_depth,
+                                                 v_verts, v_vcol);
     return cudaGetLastError();
 }
 

@@ -81,7 +81,8 @@ __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjCon
                                                      const float4* __restrict__ quats,
                                                      const float* __restrict__ logits,
                                                      const float* __restrict__ colors, int radius,
-                                                     const float4* __restrict__ vsp, bool first,
+                                                     const float4* __restrict__ vsp,
+                                                     const float4* __restrict__ vdm, bool first,
                                                      ProjGrad<DEG>& out)
 {
     constexpr int K = ProjGrad<DEG>::K;
@@ -139,8 +140,30 @@ __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjCon
 
         // upstream: record = (u, v, A, B, C | o, r, g | b, depth)
         const float4 v0 = __ldg(vsp), v1 = __ldg(vsp + 1), v2 = __ldg(vsp + 2);
-        const float gu = v0.x, gv = v0.y, gA = v0.z, gB = v0.w, gC = v1.x, go = v1.y, gz = v2.y;
+        const float gu = v0.x, gv = v0.y, go = v1.y, gz = v2.y;
+        float gA = v0.z, gB = v0.w, gC = v1.x;
         const float grgb[3] = {v1.z, v1.w, v2.x};
+
+        // depth model of the soft split, when its gradient is given: g = conic b,
+        // sigma_z^2 = szz - b . g, with b = G WM_2^T and szz = |WM_2|^2
+        float vbu = 0.f, vbv = 0.f, vszz = 0.f;
+        if (vdm) {
+            const float4 vd = __ldg(vdm);
+            const float bu = G0[0] * WM[2][0] + G0[1] * WM[2][1] + G0[2] * WM[2][2];
+            const float bv = G1[0] * WM[2][0] + G1[1] * WM[2][1] + G1[2] * WM[2][2];
+            const float szz = WM[2][0] * WM[2][0] + WM[2][1] * WM[2][1] + WM[2][2] * WM[2][2];
+            const float cA = cc * idet, cB = -b * idet, cC = a * idet;
+            const float dgu = cA * bu + cB * bv, dgv = cB * bu + cC * bv;
+            const float var = szz - (bu * dgu + bv * dgv);
+            const float vvar = var > 1e-12f ? 0.5f * vd.z / sqrtf(var) : 0.0f;  // sigma_z = sqrt(var)
+            vszz = vvar;
+            const float wgu = vd.x - vvar * bu, wgv = vd.y - vvar * bv;  // dL/dg, the variance path included
+            vbu = cA * wgu + cB * wgv - vvar * dgu;
+            vbv = cB * wgu + cC * wgv - vvar * dgv;
+            gA += wgu * bu;  // dL/d conic = dL/dg b^T (the off-diagonal B appears twice)
+            gB += wgu * bv + wgv * bu;
+            gC += wgv * bv;
+        }
 
         // conic (A, B, C) = (cc, -b, a) / det, det = a cc - b^2
         const float Qd = (gA * cc - gB * b + gC * a) * idet;  // L_conic = Q / det, Qd = Q / det
@@ -151,8 +174,8 @@ __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjCon
         float vG0[3], vG1[3];
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
-            vG0[k] = 2.0f * ga * G0[k] + gb * G1[k];
-            vG1[k] = 2.0f * gcc * G1[k] + gb * G0[k];
+            vG0[k] = 2.0f * ga * G0[k] + gb * G1[k] + vbu * WM[2][k];
+            vG1[k] = 2.0f * gcc * G1[k] + gb * G0[k] + vbv * WM[2][k];
         }
         // G0 = j00 WM0 + j02 WM2, G1 = j11 WM1 + j12 WM2
         float vWM[3][3];
@@ -161,7 +184,7 @@ __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjCon
         for (int k = 0; k < 3; ++k) {
             vWM[0][k] = j00 * vG0[k];
             vWM[1][k] = j11 * vG1[k];
-            vWM[2][k] = j02 * vG0[k] + j12 * vG1[k];
+            vWM[2][k] = j02 * vG0[k] + j12 * vG1[k] + vbu * G0[k] + vbv * G1[k] + 2.0f * vszz * WM[2][k];
             vj00 = fmaf(vG0[k], WM[0][k], vj00);
             vj02 = fmaf(vG0[k], WM[2][k], vj02);
             vj11 = fmaf(vG1[k], WM[1][k], vj11);
@@ -318,15 +341,16 @@ template <int DEG>
 __global__ void __launch_bounds__(256)
 k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
               const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
-              const int32_t* __restrict__ radii, const float4* __restrict__ v_splats, bool acc,
-              float* __restrict__ v_means, float* __restrict__ v_log_scales, float4* __restrict__ v_quats,
-              float* __restrict__ v_logits, float* __restrict__ v_colors)
+              const int32_t* __restrict__ radii, const float4* __restrict__ v_splats,
+              const float4* __restrict__ v_depth_model, bool acc, float* __restrict__ v_means,
+              float* __restrict__ v_log_scales, float4* __restrict__ v_quats, float* __restrict__ v_logits,
+              float* __restrict__ v_colors)
 {
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= N) return;
     ProjGrad<DEG> G;
     project_bwd_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, __ldg(radii + g),
-                              v_splats + 3 * (int64_t)g, true, G);
+                              v_splats + 3 * (int64_t)g, v_depth_model ? v_depth_model + g : nullptr, true, G);
     store_grad<DEG>(g, G, acc, v_means, v_log_scales, v_quats, v_logits, v_colors);
 }
 
@@ -337,7 +361,8 @@ __global__ void __launch_bounds__(128)
 k_project_bwd_views(ViewBatch vb, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
                     const float4* __restrict__ quats, const float* __restrict__ logits,
                     const float* __restrict__ colors, const int32_t* __restrict__ radii,
-                    const float4* __restrict__ v_splats, bool acc, float* __restrict__ v_means,
+                    const float4* __restrict__ v_splats, const float4* __restrict__ v_depth_model, bool acc,
+                    float* __restrict__ v_means,
                     float* __restrict__ v_log_scales, float4* __restrict__ v_quats, float* __restrict__ v_logits,
                     float* __restrict__ v_colors)
 {
@@ -347,7 +372,8 @@ k_project_bwd_views(ViewBatch vb, int N, const float* __restrict__ means, const 
     for (int v = 0; v < vb.n; ++v) {
         const int64_t i = (int64_t)v * N + g;
         project_bwd_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors,
-                                  __ldg(radii + i), v_splats + 3 * i, v == 0, total);
+                                  __ldg(radii + i), v_splats + 3 * i, v_depth_model ? v_depth_model + i : nullptr,
+                                  v == 0, total);
     }
     store_grad<DEG>(g, total, acc, v_means, v_log_scales, v_quats, v_logits, v_colors);
 }
@@ -356,18 +382,19 @@ k_project_bwd_views(ViewBatch vb, int N, const float* __restrict__ means, const 
 
 cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
                         const float* quats, const float* logits, const float* colors, const int32_t* radii,
-                        const float* v_splats, bool accumulate, float* v_means, float* v_log_scales, float* v_quats,
-                        float* v_logits, float* v_colors, cudaStream_t s)
+                        const float* v_splats, const float* v_depth_model, bool accumulate, float* v_means,
+                        float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
     const ProjConsts pc = make_proj_consts(c);
     const int grid = (N + 255) / 256;
     auto* q4 = reinterpret_cast<const float4*>(quats);
     auto* vs4 = reinterpret_cast<const float4*>(v_splats);
+    auto* vd4 = reinterpret_cast<const float4*>(v_depth_model);
     auto* vq4 = reinterpret_cast<float4*>(v_quats);
 #define GM_PROJ_BWD(D)                                                                                      \
-    k_project_bwd<D><<<grid, 256, 0, s>>>(c, pc, N, means, log_scales, q4, logits, colors, radii, vs4, accumulate, \
-                                          v_means, v_log_scales, vq4, v_logits, v_colors)
+    k_project_bwd<D><<<grid, 256, 0, s>>>(c, pc, N, means, log_scales, q4, logits, colors, radii, vs4, vd4,        \
+                                          accumulate, v_means, v_log_scales, vq4, v_logits, v_colors)
     switch (sh_degree) {
         case -1: GM_PROJ_BWD(-1); break;
         case 0: GM_PROJ_BWD(0); break;
@@ -382,8 +409,9 @@ cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, 
 
 cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, const float* means,
                               const float* log_scales, const float* quats, const float* logits, const float* colors,
-                              const int32_t* radii, const float* v_splats, bool accumulate, float* v_means,
-                              float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s)
+                              const int32_t* radii, const float* v_splats, const float* v_depth_model,
+                              bool accumulate, float* v_means, float* v_log_scales, float* v_quats, float* v_logits,
+                              float* v_colors, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
     const int grid = (N + 127) / 128;  // 128-thread CTAs: the SH-3 body is register heavy
@@ -398,10 +426,11 @@ cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, cons
         }
         const int64_t off = (int64_t)v0 * N;
         auto* vs4 = reinterpret_cast<const float4*>(v_splats + 12 * off);
+        auto* vd4 = v_depth_model ? reinterpret_cast<const float4*>(v_depth_model + 4 * off) : nullptr;
         const bool acc = accumulate || v0 > 0;  // later batches add to the earlier ones
 #define GM_PROJ_BWD_V(D)                                                                                          \
-    k_project_bwd_views<D><<<grid, 128, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, radii + off, vs4, acc, \
-                                                v_means, v_log_scales, vq4, v_logits, v_colors)
+    k_project_bwd_views<D><<<grid, 128, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, radii + off, vs4,   \
+                                                vd4, acc, v_means, v_log_scales, vq4, v_logits, v_colors)
         switch (sh_degree) {
             case -1: GM_PROJ_BWD_V(-1); break;
             case 0: GM_PROJ_BWD_V(0); break;

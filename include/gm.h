@@ -83,6 +83,8 @@ typedef struct gm_opts {
     int32_t sh_degree;      /* -1: colours are RGB [N][3]; 0..3: SH coefficients [N][(d+1)^2][3] */
     int32_t tile_test;      /* 1: also drop a (Gaussian, tile) pair when no pixel centre of the tile
                                can reach alpha >= 1/255 (see gm_bin_sort_gaussians) */
+    float softness;         /* 0: hard depth test; > 0: soft split of each Gaussian at the mesh
+                               (see gm_composite_hybrid_fwd) with this width factor */
 } gm_opts;
 
 /*
@@ -157,11 +159,23 @@ int gm_interp_mesh(const gm_camera* cam, const float* V, int32_t nV, const int32
  *   the 2D covariance)), 0 = culled (behind near / beyond far, or its tile
  *   rectangle misses the image).  tiles_touched [N] i32 out: tiles in the
  *   rectangle [floor((m - r)/16), ceil((m + r)/16)) per axis, clamped.
+ *   depth_model [N][4] f32 out, 16-byte aligned, or NULL: the soft split's
+ *   depth model (g_u, g_v, sigma_z, R) of each Gaussian (Hybrid rendering:
+ *   the depth given the pixel p is Gaussian with mean z*(p) = z_c + g .
+ *   (p - mean2d) and standard deviation sigma_z); with the camera-frame
+ *   covariance Sigma_c and the splat's Jacobian J, g = (J Sigma_c J^T +
+ *   0.3 I)^-1 J Sigma_c e_z and sigma_z^2 = e_z^T Sigma_c e_z - (J Sigma_c
+ *   e_z) . g, floored at 1e-12 (0.3: the splat's low-pass).  R >= 0, the
+ *   reach, bounds g . (p - mean2d) over the pixels where the Gaussian's
+ *   alpha can reach 1/255 (sqrt(2 ln(255 opacity) g^T Sigma2 g), with a
+ *   margin); the compositing uses it only to skip Gaussians hidden behind
+ *   the mesh (a depth model made elsewhere must bound the same, or hold
+ *   +inf there).
  * ---------------------------------------------------------------------- */
 int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
                          const float* log_scales, const float* quats, const float* logits,
                          const float* colors, float* splats, int32_t* radii, int32_t* tiles_touched,
-                         void* stream);
+                         float* depth_model, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_project_gaussians_bwd -- backward of gm_project_gaussians (Hybrid
@@ -172,6 +186,10 @@ int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, c
  *   radii [N] i32 from that call (radius 0 = culled: zero gradients);
  *   v_splats [N][12] f32, 16-byte aligned: dL/d record, e.g. the output of
  *   gm_composite_hybrid_bwd (the two padding floats are ignored).
+ *   v_depth_model [N][4] f32, 16-byte aligned, or NULL: dL/d of the soft
+ *   split's depth model (g_u, g_v, sigma_z, -), chained through g and
+ *   sigma_z into the same parameters (no gradient where sigma_z^2 sits at
+ *   its floor).
  *   v_means [N][3], v_log_scales [N][3], v_quats [N][4] (16-byte aligned),
  *   v_logits [N], v_colors (the layout of colors; 16-byte aligned for SH
  *   degree 1 and 3) f32 out: dL/d of each parameter, written when
@@ -183,8 +201,9 @@ int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, c
  * ---------------------------------------------------------------------- */
 int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* means,
                              const float* log_scales, const float* quats, const float* logits, const float* colors,
-                             const int32_t* radii, const float* v_splats, int32_t accumulate, float* v_means,
-                             float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, void* stream);
+                             const int32_t* radii, const float* v_splats, const float* v_depth_model,
+                             int32_t accumulate, float* v_means, float* v_log_scales, float* v_quats,
+                             float* v_logits, float* v_colors, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_bin_sort_gaussians -- tile intersection and sort (Hybrid rendering;
@@ -232,12 +251,22 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
  *   stats: NULL, or a device uint64[2] incremented by the number of
  *   (pixel, Gaussian) pairs evaluated [0] and composited [1] (profiling
  *   counts; the caller zeroes them).
+ * Soft split (opts->softness > 0; Hybrid rendering, the split at the mesh
+ * surface): at a covered pixel there is no hard test; each Gaussian's part
+ * in front of the mesh, f = Phi((D - z*(p)) / (sigma_z softness)) with
+ * z*(p) = z + g . (p - mean2d) from depth_model [N][4] (gm_project_gaussians,
+ * required, 16-byte aligned), scales its alpha: alpha f replaces alpha in the
+ * skip, the stop and the sums (the back parts lie behind the opaque mesh).
+ * Uncovered pixels are unchanged.  depth_model is ignored when softness = 0.
+ * Each warp's 8 x 4 pixel block passes over the Gaussians with z_c - R -
+ * 2.75 sigma_z softness beyond the largest mesh depth of its pixels (all
+ * covered): f <= Phi(-2.75) puts alpha f below 1/255 at each of them.
  * ---------------------------------------------------------------------- */
 int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
-                            const int32_t* tile_range, const int32_t* gids, const float* splats, const float* mesh_depth,
-                            const float* mesh_rgb, const int32_t* face_id, float* out_rgb,
-                            float* out_depth, float* out_alpha, float* T_final, int32_t* n_contrib,
-                            uint64_t* stats, void* stream);
+                            const int32_t* tile_range, const int32_t* gids, const float* splats,
+                            const float* depth_model, const float* mesh_depth, const float* mesh_rgb,
+                            const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
+                            float* T_final, int32_t* n_contrib, uint64_t* stats, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_composite_hybrid_bwd -- Hybrid rendering ("everything is
@@ -255,12 +284,19 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  *   (with nV = nF = 0) to skip the mesh gradients.
  *   stats: NULL, or a device uint64[2] incremented by the number of (pixel,
  *   Gaussian) pairs evaluated [0] and given gradient terms [1] (profiling).
+ *   Soft split (opts->softness > 0): depth_model as for the forward pass;
+ *   v_depth_model [N][4] f32 (+=, 16-byte aligned, required with v_splats):
+ *   dL/d(g_u, g_v, sigma_z, -); v_mesh_depth [H][W] f32 (required with the
+ *   mesh gradients): dL/dD through the split, written by the Gaussian part
+ *   (v_splats != NULL) and read by the mesh part (v_verts != NULL), so a
+ *   call with only the mesh part must follow one with the Gaussian part.
  * ---------------------------------------------------------------------- */
 int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
-                            const int32_t* tile_range, const int32_t* gids, const float* splats, const float* mesh_depth,
-                            const float* mesh_rgb, const int32_t* face_id, const float* T_final,
-                            const int32_t* n_contrib, const float* g_rgb, const float* g_depth,
-                            const float* g_alpha, float* v_splats, const float* V, int32_t nV,
+                            const int32_t* tile_range, const int32_t* gids, const float* splats,
+                            const float* depth_model, const float* mesh_depth, const float* mesh_rgb,
+                            const int32_t* face_id, const float* T_final, const int32_t* n_contrib,
+                            const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
+                            float* v_depth_model, float* v_mesh_depth, const float* V, int32_t nV,
                             const int32_t* F, int32_t nF, const float* vcol, float* v_verts,
                             float* v_vcol, uint64_t* stats, void* stream);
 
@@ -274,8 +310,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  * (binning, z-buffer, compositing) take one view's slice of these arrays.
  *   cams [V] host array, 1 <= V <= GM_MAX_VIEWS.
  *   gm_project_gaussians_views: as gm_project_gaussians for every view;
- *   splats [V][N][12], radii [V][N], tiles_touched [V][N] out (view v at
- *   offset v N).
+ *   splats [V][N][12], radii [V][N], tiles_touched [V][N], depth_model
+ *   [V][N][4] (or NULL) out (view v at offset v N).
  *   gm_project_gaussians_bwd_views: as gm_project_gaussians_bwd with radii
  *   [V][N] and v_splats [V][N][12] from the views; the parameter gradients
  *   are the sum over the views (written, or added when accumulate != 0),
@@ -285,12 +321,14 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
 #define GM_MAX_VIEWS 64
 int gm_project_gaussians_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N, const float* means,
                                const float* log_scales, const float* quats, const float* logits, const float* colors,
-                               float* splats, int32_t* radii, int32_t* tiles_touched, void* stream);
+                               float* splats, int32_t* radii, int32_t* tiles_touched, float* depth_model,
+                               void* stream);
 int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_opts* opts, int32_t N,
                                    const float* means, const float* log_scales, const float* quats,
                                    const float* logits, const float* colors, const int32_t* radii,
-                                   const float* v_splats, int32_t accumulate, float* v_means, float* v_log_scales,
-                                   float* v_quats, float* v_logits, float* v_colors, void* stream);
+                                   const float* v_splats, const float* v_depth_model, int32_t accumulate,
+                                   float* v_means, float* v_log_scales, float* v_quats, float* v_logits,
+                                   float* v_colors, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_bin_triangles_noalloc -- gm_bin_triangles for callers that may not

@@ -65,16 +65,21 @@ def run_mesh(cam, mesh):
                 mesh_rgb=host(mrgb), tile_far=host(tfar), tile_full=host(tfull), counters=host(cnt))
 
 
-def run_project(cam, g, bg=(1, 1, 1)):
+def run_project(cam, g, bg=(1, 1, 1), depth_model=False):
+    """GPU projection: splats, radii, tiles_touched (+ the soft split's depth
+    model [N][4] when depth_model is set)."""
     c = gm.make_camera(cam)
     o = gm.make_opts(bg, True, g.sh_degree)
     N = len(g.means)
     splats = torch.full((N, 12), 7.0, dtype=torch.float32, device="cuda")
     radii = torch.full((N,), -3, dtype=torch.int32, device="cuda")
     touched = torch.full((N,), -3, dtype=torch.int32, device="cuda")
+    dm = torch.full((max(N, 1), 4), 7.0, dtype=torch.float32, device="cuda") if depth_model else None
     gm.gm_project_gaussians(c, o, dev(g.means, torch.float32), dev(g.log_scales, torch.float32),
                             dev(g.quats, torch.float32), dev(g.logits, torch.float32), dev(g.colors, torch.float32),
-                            splats, radii, touched)
+                            splats, radii, touched, dm)
+    if depth_model:
+        return host(splats), host(radii), host(touched), host(dm)[:N]
     return host(splats), host(radii), host(touched)
 
 
@@ -108,9 +113,10 @@ def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=N
                 cap=cap)
 
 
-def run_composite(cam, bg, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id):
+def run_composite(cam, bg, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id, softness=0.0,
+                  depth_model=None):
     c = gm.make_camera(cam)
-    o = gm.make_opts(bg, True, -1)
+    o = gm.make_opts(bg, True, -1, True, softness)
     H, W = cam.height, cam.width
     out = {k: torch.full(s, -3.0, dtype=torch.float32, device="cuda")
            for k, s in [("rgb", (H, W, 3)), ("depth", (H, W)), ("alpha", (H, W)), ("T", (H, W))]}
@@ -118,18 +124,29 @@ def run_composite(cam, bg, tile_range, gids, splats, mesh_depth, mesh_rgb, face_
     args = [dev(tile_range, torch.int32), dev(gids if len(gids) else np.zeros(1, np.int32), torch.int32),
             dev(splats if len(splats) else np.zeros((1, 12), np.float32), torch.float32),
             dev(mesh_depth, torch.float32), dev(mesh_rgb, torch.float32), dev(face_id, torch.int32)]
-    gm.gm_composite_hybrid_fwd(c, o, *args, out["rgb"], out["depth"], out["alpha"], out["T"], nc)
+    dm = None
+    if depth_model is not None:
+        dm = dev(depth_model if len(depth_model) else np.zeros((1, 4), np.float32), torch.float32)
+    gm.gm_composite_hybrid_fwd(c, o, *args, out["rgb"], out["depth"], out["alpha"], out["T"], nc, depth_model=dm)
     res = {k: host(v) for k, v in out.items()}
     res["n_contrib"] = host(nc)
     res["_args"] = args
     res["_dev"] = dict(T=out["T"], n_contrib=nc)
+    res["_soft"] = (softness, dm)
     return res
 
 
 def run_composite_bwd(cam, bg, fwd, grads, N, mesh=None, mesh_grads=False):
+    """GPU composite backward over the saved state of run_composite (its
+    softness and depth model included).  Returns v_splats (+ v_verts / v_vcol
+    with mesh_grads; + v_depth_model and v_mesh_depth with the soft split)."""
     c = gm.make_camera(cam)
-    o = gm.make_opts(bg, True, -1)
+    softness, dm = fwd.get("_soft", (0.0, None))
+    o = gm.make_opts(bg, True, -1, True, softness)
+    soft = softness > 0.0
     v_splats = torch.zeros(max(N, 1), 12, dtype=torch.float32, device="cuda")
+    v_dm = torch.zeros(max(N, 1), 4, dtype=torch.float32, device="cuda") if soft else None
+    v_md = torch.full((cam.height, cam.width), 5.0, dtype=torch.float32, device="cuda") if soft else None
     g_rgb, g_depth, g_alpha = (dev(x, torch.float32) for x in grads)
     V = F = vcol = v_verts = v_vcol = None
     if mesh_grads:
@@ -137,8 +154,11 @@ def run_composite_bwd(cam, bg, fwd, grads, N, mesh=None, mesh_grads=False):
         v_verts = torch.zeros_like(V)
         v_vcol = torch.zeros_like(vcol)
     gm.gm_composite_hybrid_bwd(c, o, *fwd["_args"], fwd["_dev"]["T"], fwd["_dev"]["n_contrib"], g_rgb, g_depth,
-                               g_alpha, v_splats, V, F, vcol, v_verts, v_vcol)
+                               g_alpha, v_splats, V, F, vcol, v_verts, v_vcol, depth_model=dm, v_depth_model=v_dm,
+                               v_mesh_depth=v_md)
     out = dict(v_splats=host(v_splats)[:N])
+    if soft:
+        out.update(v_depth_model=host(v_dm)[:N], v_mesh_depth=host(v_md))
     if mesh_grads:
         out.update(v_verts=host(v_verts), v_vcol=host(v_vcol))
     return out
@@ -180,7 +200,7 @@ def input_ulp_perturbations(cam, V, draws=3, seed=0):
     return out
 
 
-def run_project_bwd(cam, g, v_splats, accumulate_into=None):
+def run_project_bwd(cam, g, v_splats, accumulate_into=None, v_depth_model=None):
     """GPU projection, then its backward for the upstream v_splats.  Returns
     radii and the gradients (v_means, v_log_scales, v_quats, v_logits, v_colors)
     as numpy; accumulate_into = previous gradients to add to (accumulate mode)."""
@@ -197,6 +217,7 @@ def run_project_bwd(cam, g, v_splats, accumulate_into=None):
         outs = [torch.full(a.shape, 3.0, dtype=torch.float32, device="cuda") for a in args]
     else:
         outs = [dev(x, torch.float32).clone() for x in accumulate_into]
+    vdm = None if v_depth_model is None else dev(v_depth_model, torch.float32)
     gm.gm_project_gaussians_bwd(c, o, *args, radii, dev(v_splats, torch.float32), *outs,
-                                accumulate=accumulate_into is not None)
+                                accumulate=accumulate_into is not None, v_depth_model=vdm)
     return host(radii), [host(x) for x in outs]

@@ -61,15 +61,15 @@ def test_null_and_size_checks(lib):
     # NULL camera
     assert lib.gm_interp_mesh(None, None, 0, None, 0, None, None, None, None, None, None, None) == gm.GM_ERR_INVALID_ARG
     # negative N
-    st = lib.gm_project_gaussians(C.byref(cam), C.byref(opts), -1, *([None] * 9))
+    st = lib.gm_project_gaussians(C.byref(cam), C.byref(opts), -1, *([None] * 10))
     assert st == gm.GM_ERR_INVALID_ARG
     # sh degree out of range
     bad = gm.make_opts(sh_degree=4)
-    st = lib.gm_project_gaussians(C.byref(cam), C.byref(bad), 0, *([None] * 9))
+    st = lib.gm_project_gaussians(C.byref(cam), C.byref(bad), 0, *([None] * 10))
     assert st == gm.GM_ERR_INVALID_ARG and b"sh_degree" in lib.gm_last_error()
     # misaligned splats
     st = lib.gm_project_gaussians(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 5), C.c_void_p(260),
-                                  C.c_void_p(256), C.c_void_p(256), None)
+                                  C.c_void_p(256), C.c_void_p(256), None, None)
     assert st == gm.GM_ERR_INVALID_ARG
     # workspace too small
     st = lib.gm_bin_sort_gaussians(C.byref(cam), C.byref(opts), 10, C.c_void_p(256), C.c_void_p(256),
@@ -82,9 +82,29 @@ def test_null_and_size_checks(lib):
                                    C.c_void_p(256), 1 << 30, None)
     assert st == gm.GM_ERR_INVALID_ARG
     # incomplete mesh-gradient arguments
-    st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 12), None, 3,
-                                     None, 1, None, C.c_void_p(256), None, None, None)
+    st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 13), None, None,
+                                     None, 3, None, 1, None, C.c_void_p(256), None, None, None)
     assert st == gm.GM_ERR_INVALID_ARG
+    # soft split: negative softness; Gaussian gradients without the depth model or its gradient;
+    # mesh gradients without dL/d mesh depth
+    neg = gm.make_opts(softness=-1.0)
+    st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(neg), 4, *([C.c_void_p(256)] * 12), None, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"softness" in lib.gm_last_error()
+    soft = gm.make_opts(softness=1.0)
+    st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(soft), 4, C.c_void_p(256), C.c_void_p(256),
+                                     C.c_void_p(256), None, *([C.c_void_p(256)] * 8), None, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"depth_model" in lib.gm_last_error()
+    st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(soft), 4, *([C.c_void_p(256)] * 13), None, None,
+                                     None, 0, None, 0, None, None, None, None, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"depth_model" in lib.gm_last_error()
+    st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(soft), 4, *([C.c_void_p(256)] * 12), None, None,
+                                     None, C.c_void_p(256), 3, C.c_void_p(256), 1, C.c_void_p(256),
+                                     C.c_void_p(256), C.c_void_p(256), None, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"v_mesh_depth" in lib.gm_last_error()
+    # misaligned v_depth_model in the projection backward
+    st = lib.gm_project_gaussians_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 7), C.c_void_p(260),
+                                      0, *([C.c_void_p(256)] * 5), None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"v_depth_model" in lib.gm_last_error()
 
 
 def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):

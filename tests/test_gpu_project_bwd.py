@@ -46,13 +46,13 @@ def _one_ulp(g, rng):
                             g.sh_degree)
 
 
-def _compare(orc, name, cam, g, v, pick, gpu, rng):
+def _compare(orc, name, cam, g, v, pick, gpu, rng, vd=None):
     P = orc.proj_nparams(g.sh_degree)
     gids = np.repeat(pick, P).astype(np.int32)
     params = np.tile(np.arange(P), len(pick)).astype(np.int32)
     hs = np.full(len(gids), H_STEP)
-    fd, st = orc.project_fd(cam, g, v, gids, params, hs)
-    fd2, st2 = orc.project_fd(cam, _one_ulp(g, rng), v, gids, params, hs)
+    fd, st = orc.project_fd(cam, g, v, gids, params, hs, v_depth_model=vd)
+    fd2, st2 = orc.project_fd(cam, _one_ulp(g, rng), v, gids, params, hs, v_depth_model=vd)
     cond = np.abs(fd2 - fd)
     ok = (st == 0) & (st2 == 0)
     got = gpu[gids, params]
@@ -92,6 +92,25 @@ def test_projection_backward_matches_fd(case, orc):
     np.testing.assert_array_equal(gpu[culled], 0.0)  # culled: zero gradients, every row written
     pick = rng.choice(vis, size=min(96, len(vis)), replace=False)
     _compare(orc, name, cam, g, v, pick, gpu, rng)
+
+
+def test_depth_model_gradient_matches_fd(case, orc):
+    """dL/d(g_u, g_v, sigma_z) of the soft split's depth model chained into the
+    3D parameters (record gradient zero, so only that chain is exercised)."""
+    name, cam, g = case
+    N = len(g.means)
+    rng = np.random.default_rng(37)
+    v = np.zeros((N, 12), np.float32)
+    vd = rng.normal(size=(N, 4)).astype(np.float32)
+    vd[:, 3] = 0.0
+    radii, (vm, vls, vq, vlo, vc) = H.run_project_bwd(cam, g, v, v_depth_model=vd)
+    gpu = np.concatenate([vm, vls, vq, vlo[:, None], vc.reshape(N, -1)], 1)
+    vis = np.flatnonzero(radii > 0)
+    np.testing.assert_array_equal(gpu[np.flatnonzero(radii == 0)], 0.0)
+    np.testing.assert_array_equal(vlo, 0.0)  # opacity and colour do not enter the depth model
+    np.testing.assert_array_equal(vc, 0.0)
+    pick = rng.choice(vis, size=min(96, len(vis)), replace=False)
+    _compare(orc, name + "_depth_model", cam, g, v, pick, gpu, rng, vd=vd)
 
 
 def test_accumulate_adds(case, orc):
