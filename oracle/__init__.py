@@ -225,6 +225,9 @@ def tile_lists(cam, splats, radii, tiles=None):
     return start, entries
 
 
+SPLIT_PHI, SPLIT_LOGISTIC = 0, 1
+
+
 def _soft(depth_model, softness):
     if depth_model is None or not softness > 0.0:
         return None, C.c_double(0.0)
@@ -232,9 +235,10 @@ def _soft(depth_model, softness):
 
 
 def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=None, depth_model=None,
-                  softness=0.0):
+                  softness=0.0, split=SPLIT_PHI):
     """Full-frame outputs; only pixels of ``tiles`` (all when None) are written.
-    With depth_model and softness > 0: the soft split."""
+    With depth_model and softness > 0: the soft split (front fraction Phi, or
+    its logistic approximation with split=SPLIT_LOGISTIC)."""
     dm, sf = _soft(depth_model, softness)
     start, entries = lists
     H, W = cam.height, cam.width
@@ -250,12 +254,12 @@ def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=N
         _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
         _p(_c(face_id, np.int32)), _p(tl), C.c_int32(0 if tiles is None else len(tiles)),
         _p(out["rgb"]), _p(out["depth"]), _p(out["alpha"]), _p(out["T"]), _p(out["n_contrib"]),
-        _p(out["margins"]), _p(dm), sf)
+        _p(out["margins"]), _p(dm), sf, C.c_int32(split))
     return out
 
 
 def composite_fd(cam, bg, splats, radii, lists, mesh_depth, mesh_rgb, face_id, grads,
-                 gids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0):
+                 gids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0, split=SPLIT_PHI):
     """fields 0..9: record fields; 12, 13, 14: depth model g_u, g_v, sigma_z."""
     dm, sf = _soft(depth_model, softness)
     start, entries = lists
@@ -268,12 +272,12 @@ def composite_fd(cam, bg, splats, radii, lists, mesh_depth, mesh_rgb, face_id, g
         _p(_c(start, np.int64)), _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)),
         _p(_c(mesh_rgb, np.float32)), _p(_c(face_id, np.int32)), _p(g_rgb), _p(g_depth), _p(g_alpha),
         C.c_int32(n), _p(_c(gids, np.int32)), _p(_c(fields, np.int32)), _p(_c(hs, np.float64)),
-        C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf)
+        C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf, C.c_int32(split))
     return grad, status
 
 
 def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, grads,
-            vids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0):
+            vids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0, split=SPLIT_PHI):
     dm, sf = _soft(depth_model, softness)
     start, entries = lists
     V, F, vcol = _c(V, np.float32), _c(F, np.int32), _c(vcol, np.float32)
@@ -286,25 +290,26 @@ def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, g
         _p(vcol), _p(_c(face_id, np.int32)), _p(_c(splats, np.float32)), _p(_c(start, np.int64)),
         _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
         _p(g_rgb), _p(g_depth), _p(g_alpha), C.c_int32(n), _p(_c(vids, np.int32)),
-        _p(_c(fields, np.int32)), _p(_c(hs, np.float64)), C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf)
+        _p(_c(fields, np.int32)), _p(_c(hs, np.float64)), C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf,
+        C.c_int32(split))
     return grad, status
 
 
 def composite_one(px, py, splats, order, D=np.inf, covered=False, cm=(0, 0, 0), bg=(1, 1, 1), f32=True,
-                  depth_model=None, softness=0.0):
+                  depth_model=None, softness=0.0, split=SPLIT_PHI):
     """One pixel over an explicit ordered list of splat ids: rgb, depth, alpha, T, n_contrib."""
     dm, sf = _soft(depth_model, softness)
     out = np.zeros(7, np.float64)
     lst = _c(order, np.int32)
     lib().orc_composite_one(C.c_int32(int(f32)), C.c_double(px), C.c_double(py), _p(lst), C.c_int64(len(lst)),
                             _p(_c(splats, np.float32)), C.c_double(D), C.c_int32(int(covered)),
-                            _p(_c(cm, np.float64)), _p(_c(bg, np.float64)), _p(out), _p(dm), sf)
+                            _p(_c(cm, np.float64)), _p(_c(bg, np.float64)), _p(out), _p(dm), sf, C.c_int32(split))
     return {"rgb": out[:3], "depth": out[3], "alpha": out[4], "T": out[5], "n_contrib": int(out[6])}
 
 
 # ------------------------------------------------------------ pipeline ----
 
-def render(scene, cam=None, tiles=None, softness=0.0):
+def render(scene, cam=None, tiles=None, softness=0.0, split=SPLIT_PHI):
     """Whole forward pass from raw inputs for the listed tiles (all when None),
     with the soft split when softness > 0.
 
@@ -340,7 +345,7 @@ def render(scene, cam=None, tiles=None, softness=0.0):
     lists = tile_lists(cam, splats, radii, tiles_arr)
     dm = project_depth_model(cam, scene.gaussians) if softness > 0.0 else None
     out = composite_fwd(cam, scene.bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles_arr,
-                        depth_model=dm, softness=softness)
+                        depth_model=dm, softness=softness, split=split)
     out.update(face_id=face_id.reshape(H, W), mesh_depth=mesh_depth.reshape(H, W),
                mesh_rgb=mesh_rgb.reshape(H, W, 3), zbest=best.reshape(H, W),
                zsecond=second.reshape(H, W), splats=splats, radii=radii,

@@ -728,12 +728,21 @@ typedef struct {
 } pert_t;
 
 /* Soft split (Hybrid rendering): the depth model [N][4] = (g_u, g_v,
- * sigma_z, -) of each Gaussian (see depth_model_f64) and the softness.
+ * sigma_z, -) of each Gaussian (see depth_model_f64), the softness and the
+ * form of the front fraction (the exported calls take it as `split`).
  * Perturbation fields F_GU, F_GV, F_SZ address the depth model.          */
 typedef struct {
     const float* dm;
     double softness;
+    int logistic; /* 0: f = Phi(x); 1: f = 1 / (1 + exp(-1.702 x)) */
 } soft_t;
+
+/* The split's front fraction: the standard normal CDF, or its logistic
+ * approximation with slope 1.702 (the two agree within 0.01 everywhere). */
+static inline double split_front(double x, int logistic)
+{
+    return logistic ? 1.0 / (1.0 + exp(-1.702 * x)) : 0.5 * erfc(-x * M_SQRT1_2);
+}
 enum { F_GU = 12, F_GV = 13, F_SZ = 14 };
 
 static inline double dmfield(const soft_t* sm, int g, int k, const pert_t* p)
@@ -770,8 +779,9 @@ static inline double sfield(const float* splats, int g, int f, const pert_t* p)
  *   T' = T (1 - alpha); stop before i when T' <= 1e-4;
  *   C += alpha T c_i;  Z += alpha T z_i;  T = T'.
  * Soft split (sm != NULL) at a covered pixel: no hard depth test; the
- * Gaussian's front part f = Phi((D - z*(p)) / (sigma_z softness)),
- * z*(p) = z_i + g . d, replaces alpha by alpha f in the skip, the stop and
+ * Gaussian's front part f = Phi((D - z*(p)) / (sigma_z softness)) (or its
+ * logistic approximation, split_front), z*(p) = z_i + g . d, replaces
+ * alpha by alpha f in the skip, the stop and
  * the sums (the back parts lie behind the opaque mesh and are not seen).
  * Terminal layer (the opaque mesh, coverage 0 or 1):
  *   rgb = C + T (covered ? c_mesh : bg);  depth = Z + T covered D;
@@ -835,7 +845,7 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
             double zs = rnd(z + rnd(rnd(dmfield(sm, g, 0, p) * dx, f32) + rnd(dmfield(sm, g, 1, p) * dy, f32), f32),
                             f32);
             double xa = rnd(rnd(D - zs, f32) / rnd(dmfield(sm, g, 2, p) * sm->softness, f32), f32);
-            double f = rnd(0.5 * erfc(-xa * M_SQRT1_2), f32);
+            double f = rnd(split_front(xa, sm->logistic), f32);
             alpha = rnd(alpha * f, f32);
         }
         double ma = fabs(alpha - amin) / amin;
@@ -879,9 +889,9 @@ void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats
                        const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
                        const int32_t* tiles, int32_t n_tiles_req,
                        float* out_rgb, float* out_depth, float* out_alpha, float* T_final,
-                       int32_t* n_contrib, double* margins, const float* depth_model, double softness)
+                       int32_t* n_contrib, double* margins, const float* depth_model, double softness, int32_t split)
 {
-    soft_t smv = {depth_model, softness};
+    soft_t smv = {depth_model, softness, split != 0};
     const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     int TW = n_tiles_x(c), TH = n_tiles_y(c);
     int32_t nt = tiles ? n_tiles_req : TW * TH;
@@ -966,9 +976,9 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                       const float* g_rgb, const float* g_depth, const float* g_alpha,
                       int32_t n_req, const int32_t* req_gid, const int32_t* req_field,
                       const double* req_h, double tie_band, double* grad, int32_t* status,
-                      const float* depth_model, double softness)
+                      const float* depth_model, double softness, int32_t split)
 {
-    soft_t smv = {depth_model, softness};
+    soft_t smv = {depth_model, softness, split != 0};
     const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     int TW = n_tiles_x(c);
     double bgd[3] = {bg[0], bg[1], bg[2]};
@@ -1058,9 +1068,9 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                  const int64_t* tile_start, const int32_t* entries, const float* mesh_depth,
                  const float* mesh_rgb, const float* g_rgb, const float* g_depth, const float* g_alpha,
                  int32_t n_req, const int32_t* req_vid, const int32_t* req_field, const double* req_h,
-                 double tie_band, double* grad, int32_t* status, const float* depth_model, double softness)
+                 double tie_band, double* grad, int32_t* status, const float* depth_model, double softness, int32_t split)
 {
-    soft_t smv = {depth_model, softness};
+    soft_t smv = {depth_model, softness, split != 0};
     const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     int TW = n_tiles_x(c);
     int64_t P = (int64_t)c->width * c->height;
@@ -1167,9 +1177,9 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
  * out: rgb[3], depth, alpha, T, n_contrib.                                */
 void orc_composite_one(int32_t f32, double px, double py, const int32_t* list, int64_t n,
                        const float* splats, double D, int32_t covered, const double* cm,
-                       const double* bg, double* out, const float* depth_model, double softness)
+                       const double* bg, double* out, const float* depth_model, double softness, int32_t split)
 {
-    soft_t smv = {depth_model, softness};
+    soft_t smv = {depth_model, softness, split != 0};
     const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     pix_t o;
     composite_pixel(f32, px, py, list, n, splats, sm, D, covered, cm, bg, NULL, &o, NULL, NULL, -1);

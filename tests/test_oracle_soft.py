@@ -9,7 +9,9 @@ The depth model is pinned by closed forms and by the page's own property of
 flat Gaussians; the compositing by a single-Gaussian closed form with an
 independent normal CDF (scipy.special.ndtr), by the hard-split limit and by
 the unchanged uncovered pixels; the finite differences through the depth
-model by closed-form derivatives."""
+model by closed-form derivatives.  The same pins cover the optional logistic
+form of the front fraction, sigmoid(1.702 x) (scipy.special.expit), which
+stays within 0.0095 of Phi."""
 
 import math
 
@@ -107,7 +109,21 @@ def _one(D, softness, alpha_logit=0.5, z=4.0, gu=0.01, gv=-0.02, sz=0.05, px=10.
     return splats, dm
 
 
-def test_single_gaussian_soft_split_closed_form(orc):
+def _front(x, split):
+    # the two forms of the front fraction: scipy's normal CDF, or the logistic
+    # approximation sigmoid(1.702 x) through scipy's expit
+    return float(ndtr(x)) if split == 0 else float(expit(1.702 * x))
+
+
+def _front_density(x, split):
+    if split == 0:
+        return math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)
+    f = float(expit(1.702 * x))
+    return 1.702 * f * (1.0 - f)
+
+
+@pytest.mark.parametrize("split", [0, 1], ids=["phi", "logistic"])
+def test_single_gaussian_soft_split_closed_form(orc, split):
     cm, bg = (0.1, 0.7, 0.3), (1.0, 1.0, 1.0)
     for D in (3.9, 4.0, 4.05, 4.2):
         for softness in (0.5, 1.0, 2.0):
@@ -117,9 +133,9 @@ def test_single_gaussian_soft_split_closed_form(orc):
             sigma = 0.5 * (s[S_CA] * d[0] ** 2 + s[S_CC] * d[1] ** 2) + s[S_CB] * d[0] * d[1]
             alpha = min(0.99, s[S_OP] * math.exp(-sigma))
             zs = s[S_Z] + float(dm[0, 0]) * d[0] + float(dm[0, 1]) * d[1]
-            f = float(ndtr((D - zs) / (float(dm[0, 2]) * softness)))
+            f = _front((D - zs) / (float(dm[0, 2]) * softness), split)
             o = orc.composite_one(10.5, 9.5, splats, [0], D=D, covered=True, cm=cm, bg=bg, f32=False,
-                                  depth_model=dm, softness=softness)
+                                  depth_model=dm, softness=softness, split=split)
             a = alpha * f
             if a < 1.0 / 255.0:  # the skip applies to the composited alpha
                 a = 0.0
@@ -167,6 +183,34 @@ def test_soft_split_limits(orc):
     assert 0.0 < 1.0 - s1["T"] < 0.2
 
 
+def test_logistic_split_is_close_to_phi(orc):
+    """The logistic form differs from Phi by at most 0.0095 in f (the known bound of
+    the 1.702 approximation), so a single Gaussian's composited alpha by at most
+    0.0095 alpha; both reach the hard split as the softness vanishes."""
+    cm = (0.1, 0.7, 0.3)
+    xs = np.linspace(-6, 6, 2001)
+    assert np.abs(ndtr(xs) - expit(1.702 * xs)).max() < 0.0095
+    for D in (3.95, 4.0, 4.03, 4.1):
+        splats, dm = _one(D, 1.0)
+        a = [1.0 - orc.composite_one(10.5, 9.5, splats, [0], D=D, covered=True, cm=cm, f32=False,
+                                     depth_model=dm, softness=1.0, split=k)["T"] for k in (0, 1)]
+        assert abs(a[0] - a[1]) <= 0.0095 * 0.99 + 1e-12
+    rng = np.random.default_rng(3)
+    n = 5
+    splats = np.zeros((n, 12), np.float32)
+    splats[:, 0:2] = rng.uniform(8, 12, (n, 2))
+    splats[:, 2] = splats[:, 4] = 0.05
+    splats[:, 5] = rng.uniform(0.3, 0.9, n)
+    splats[:, 6:9] = rng.uniform(size=(n, 3))
+    splats[:, 9] = np.sort(rng.uniform(3.0, 5.0, n))
+    dm = np.zeros((n, 4), np.float32)
+    dm[:, 2] = 0.02
+    hard = orc.composite_one(10.5, 10.5, splats, np.arange(n), D=4.0, covered=True, cm=cm, f32=False)
+    sharp = orc.composite_one(10.5, 10.5, splats, np.arange(n), D=4.0, covered=True, cm=cm, f32=False,
+                              depth_model=dm, softness=1e-3, split=1)
+    np.testing.assert_allclose(sharp["rgb"], hard["rgb"], atol=1e-12)
+
+
 def _flat_scene():
     """A 16 x 16 image fully covered by a mesh at depth D = 4 (mesh colour cm),
     one Gaussian near the surface."""
@@ -182,9 +226,11 @@ def _flat_scene():
     return cam, splats, dm, radii, lists, D, cm, face
 
 
-def test_finite_differences_through_the_depth_model(orc):
+@pytest.mark.parametrize("split", [0, 1], ids=["phi", "logistic"])
+def test_finite_differences_through_the_depth_model(orc, split):
     """d/d(sigma_z, g_u, z_c) of L = sum_p g_rgb . rgb against the closed forms
-    sum_p alpha (c - cm) . g_rgb phi(x) dx/d(.), x = (D - z_c - g . d) / (sigma_z s)."""
+    sum_p alpha (c - cm) . g_rgb f'(x) dx/d(.), x = (D - z_c - g . d) / (sigma_z s),
+    f' the normal density or, for the logistic form, 1.702 f (1 - f)."""
     cam, splats, dm, radii, lists, D, cm, face = _flat_scene()
     rng = np.random.default_rng(5)
     g_rgb = rng.uniform(-1, 1, (16, 16, 3)).astype(np.float32)
@@ -199,10 +245,10 @@ def test_finite_differences_through_the_depth_model(orc):
             sig = 0.5 * (s[S_CA] * d[0] ** 2 + s[S_CC] * d[1] ** 2) + s[S_CB] * d[0] * d[1]
             alpha = min(0.99, s[S_OP] * math.exp(-sig))
             x = (4.0 - s[S_Z] - gu * d[0] - gv * d[1]) / (sz * softness)
-            f = ndtr(x)
+            f = _front(x, split)
             if sig < 0 or alpha * f < 1 / 255:
                 continue
-            phi = math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)
+            phi = _front_density(x, split)
             k = alpha * float(np.dot(s[S_R:S_B + 1] - cm[0].astype(np.float64), g_rgb[j, i])) * phi
             want[F_SZ] += k * (-x / sz)
             want[F_GU] += k * (-d[0] / (sz * softness))
@@ -211,7 +257,7 @@ def test_finite_differences_through_the_depth_model(orc):
     hs = np.array([1e-5, 1e-6, 1e-6])
     got, st = orc.composite_fd(cam, (1, 1, 1), splats, radii, lists, D.reshape(16, 16), cm.reshape(16, 16, 3),
                                face.reshape(16, 16), (g_rgb, zero, zero), np.zeros(3, np.int32), fields, hs,
-                               depth_model=dm, softness=softness)
+                               depth_model=dm, softness=softness, split=split)
     assert (st == 0).all(), st
     for k, fld in enumerate(fields):
         np.testing.assert_allclose(got[k], want[int(fld)], rtol=2e-5, atol=1e-9)
