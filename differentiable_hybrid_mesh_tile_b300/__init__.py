@@ -29,6 +29,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "gm.h")
 GM_OK, GM_ERR_INVALID_ARG, GM_ERR_CAPACITY, GM_ERR_CUDA, GM_ERR_TIMEOUT, GM_ERR_INTERNAL = range(6)
 GM_CNT_K, GM_CNT_K_PRECULL, GM_CNT_FLAGS = 0, 1, 2
 GM_FLAG_OVERFLOW, GM_FLAG_TIMEOUT = 1, 2
+GM_SPLIT_PHI, GM_SPLIT_LOGISTIC = 0, 1
 TILE = 16
 SPLAT_STRIDE = 12
 
@@ -48,7 +49,7 @@ class gm_camera(C.Structure):
 
 class gm_opts(C.Structure):
     _fields_ = [("bg", C.c_float * 3), ("cull_occluded", C.c_int32), ("sh_degree", C.c_int32),
-                ("tile_test", C.c_int32), ("softness", C.c_float)]
+                ("tile_test", C.c_int32), ("softness", C.c_float), ("soft_split", C.c_int32)]
 
 
 _VP = C.c_void_p
@@ -111,7 +112,8 @@ def make_camera(cam) -> gm_camera:
     return c
 
 
-def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1, tile_test=True, softness=0.0) -> gm_opts:
+def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1, tile_test=True, softness=0.0,
+              soft_split=0) -> gm_opts:
     o = gm_opts()
     for k in range(3):
         o.bg[k] = float(bg[k])
@@ -119,6 +121,7 @@ def make_opts(bg=(1.0, 1.0, 1.0), cull_occluded=True, sh_degree=-1, tile_test=Tr
     o.sh_degree = int(sh_degree)
     o.tile_test = int(bool(tile_test))
     o.softness = float(softness)
+    o.soft_split = int(soft_split)
     return o
 
 
@@ -303,7 +306,8 @@ class HybridRenderer:
     backward (joined back into the caller's stream before anything reads
     their results; a captured graph keeps the two branches).
 
-    ``softness > 0`` selects the soft split at the mesh surface: the
+    ``softness > 0`` selects the soft split at the mesh surface (front
+    fraction ``soft_split``: GM_SPLIT_PHI or GM_SPLIT_LOGISTIC): the
     projection also writes each Gaussian's depth model (``depth_model``), the
     backward pass writes its gradient (``v_depth_model``) and dL/d mesh depth
     through the split (``v_mesh_depth``), and the mesh backward then runs
@@ -311,7 +315,7 @@ class HybridRenderer:
     """
 
     def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
-                 concurrent=True, tile_test=True, softness=0.0):
+                 concurrent=True, tile_test=True, softness=0.0, soft_split=GM_SPLIT_PHI):
         self.cam_desc = cam
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
@@ -327,6 +331,7 @@ class HybridRenderer:
         if not self.softness >= 0.0:
             raise ValueError("softness must be >= 0")
         self.soft = self.softness > 0.0
+        self.soft_split = int(soft_split)
         self._side = None
         self.tri_cap = 0
         self.g_cap = 0
@@ -357,7 +362,7 @@ class HybridRenderer:
 
     @property
     def opts(self) -> gm_opts:
-        return make_opts(self.bg, self.cull, self.sh_degree, self.tile_test, self.softness)
+        return make_opts(self.bg, self.cull, self.sh_degree, self.tile_test, self.softness, self.soft_split)
 
     def upload(self, mesh, gaussians):
         d = self.dev
@@ -529,9 +534,9 @@ class MultiViewRenderer:
     """
 
     def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4,
-                 softness=0.0):
+                 softness=0.0, soft_split=GM_SPLIT_PHI):
         self.views = [HybridRenderer(c, bg=bg, cull_occluded=cull_occluded, device=device, concurrent=False,
-                                     tile_test=tile_test, softness=softness) for c in cams]
+                                     tile_test=tile_test, softness=softness, soft_split=soft_split) for c in cams]
         self.soft = self.views[0].soft
         self.V = len(self.views)
         self.dev = torch.device(device)

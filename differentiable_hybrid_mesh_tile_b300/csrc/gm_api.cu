@@ -294,6 +294,8 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     if (int st = check_cam(cam)) return st;
     GM_REQUIRE(opts, "opts is NULL");
     GM_REQUIRE(opts->softness >= 0.0f, "negative softness");
+    GM_REQUIRE(opts->soft_split == GM_SPLIT_PHI || opts->soft_split == GM_SPLIT_LOGISTIC, "soft_split %d unknown",
+               opts->soft_split);
     GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id, "an input is NULL");
     GM_REQUIRE(out_rgb && out_depth && out_alpha && T_final && n_contrib, "an output is NULL");
     GM_REQUIRE(N >= 0, "negative N");
@@ -302,7 +304,8 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     const bool soft = opts->softness > 0.0f;
     GM_REQUIRE(!soft || N == 0 || (depth_model && aligned16(depth_model)),
                "the soft split needs a 16-byte aligned depth_model");
-    cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, opts->softness, tile_range, gids, splats,
+    cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, opts->softness, opts->soft_split, tile_range,
+                                      gids, splats,
                                       depth_model, mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
                                       T_final, n_contrib, stats, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_fwd");
@@ -320,6 +323,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     if (int st = check_cam(cam)) return st;
     GM_REQUIRE(opts, "opts is NULL");
     GM_REQUIRE(opts->softness >= 0.0f, "negative softness");
+    GM_REQUIRE(opts->soft_split == GM_SPLIT_PHI || opts->soft_split == GM_SPLIT_LOGISTIC, "soft_split %d unknown",
+               opts->soft_split);
     const bool soft = opts->softness > 0.0f;
     if (soft && v_splats && N > 0)
         GM_REQUIRE(depth_model && aligned16(depth_model) && v_depth_model && aligned16(v_depth_model),
@@ -337,7 +342,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     const gm::Cam c = gm::make_cam(*cam);
     cudaError_t e = cudaSuccess;
     if (v_splats)
-        e = gm::composite_bwd(c, opts->bg, N, opts->softness, tile_range, gids, splats, depth_model, mesh_depth,
+        e = gm::composite_bwd(c, opts->bg, N, opts->softness, opts->soft_split, tile_range, gids, splats, depth_model,
+                              mesh_depth,
                               mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model,
                               soft ? v_mesh_depth : nullptr, stats, s);
     if (e == cudaSuccess && mesh_grads && nF > 0)

@@ -147,21 +147,36 @@ __device__ __forceinline__ void stage_empty(float4& C, float4& H)
     C = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// f = Phi(x) <= Phi(-SPLIT_TAIL) = 0.0030 once x <= -SPLIT_TAIL, so alpha f
-// <= 0.99 x 0.0030 < 1/255: the Gaussian is skipped at that pixel.
-constexpr float SPLIT_TAIL = 2.75f;
+// The soft split: its width factor and the form of the front fraction f(x),
+// Phi(x) or the logistic 1 / (1 + exp(-1.702 x)).  Past x <= -tail, f(x) <=
+// 0.0030 (Phi(-2.75)) or 0.0026 (logistic at -3.5), so alpha f <= 0.99 f <
+// 1/255 and the Gaussian is skipped at that pixel.
+struct Split {
+    float softness;
+    int logistic;
+    __device__ __forceinline__ float tail() const { return logistic ? 3.5f : 2.75f; }
+    __device__ __forceinline__ float front(float x) const
+    {
+        return logistic ? 1.0f / (1.0f + __expf(-1.702f * x)) : normcdff(x);
+    }
+    // df/dx, given f = front(x)
+    __device__ __forceinline__ float density(float x, float f) const
+    {
+        return logistic ? 1.702f * f * (1.0f - f) : 0.3989422804014327f * __expf(-0.5f * x * x);
+    }
+};
 
 // Staged depth model of the soft split: (g_u, g_v, kappa = 1 / (sigma_z
-// softness), z_hide); f = Phi((D - z*) kappa), z* = z_c + g . (p - mean2d).
+// softness), z_hide); f = f((D - z*) kappa), z* = z_c + g . (p - mean2d).
 // With the reach R (z* >= z_c - R wherever alpha can reach 1/255), a mesh depth
-// D < z_hide = z_c - R - SPLIT_TAIL sigma_z softness (less a rounding margin)
-// puts x below -SPLIT_TAIL: the Gaussian is hidden at every such pixel.
-__device__ __forceinline__ float4 stage_depth_model(const float4* __restrict__ depth_model, int64_t g, float softness,
-                                                    float z)
+// D < z_hide = z_c - R - tail sigma_z softness (less a rounding margin) puts x
+// below -tail: the Gaussian is hidden at every such pixel.
+__device__ __forceinline__ float4 stage_depth_model(const float4* __restrict__ depth_model, int64_t g,
+                                                    const Split& sp, float z)
 {
     const float4 m = depth_model[g];
-    const float band = m.z * softness;
-    const float hide = z - fmaf(SPLIT_TAIL, band, m.w) * 1.0001f - 2e-6f * fabsf(z);
+    const float band = m.z * sp.softness;
+    const float hide = z - fmaf(sp.tail(), band, m.w) * 1.0001f - 2e-6f * fabsf(z);
     return make_float4(m.x, m.y, 1.0f / band, hide);
 }
 
@@ -178,7 +193,7 @@ __device__ __forceinline__ float warp_hide_depth(bool inside, bool cov, float D)
 
 template <bool STATS, bool SOFT>
 __global__ void __launch_bounds__(CTA_THREADS)
-k_composite_fwd(Cam c, float3 bg, int N, float softness, const int2* __restrict__ tile_range,
+k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
                 const int32_t* __restrict__ gids, const float4* __restrict__ splats,
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id, float* __restrict__ out_rgb,
@@ -215,7 +230,7 @@ k_composite_fwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
             const int64_t g = gids[b + threadIdx.x];
             if (g >= 0 && g < N) {
                 stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
-                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, softness, sC[threadIdx.x].y);
+                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, sp, sC[threadIdx.x].y);
             } else {  // an id outside [0, N): an entry that draws nothing
                 stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
             }
@@ -266,7 +281,7 @@ k_composite_fwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
                     if (soft) {  // the Gaussian's part in front of the mesh
                         const float4 Dm = sD[kk2[h]];
                         const float zs = fmaf(Dm.x, ev[h].dx, fmaf(Dm.y, ev[h].dy, Cq[h].y));
-                        a *= normcdff((D - zs) * Dm.z);
+                        a *= sp.front((D - zs) * Dm.z);
                         if (a < ALPHA_MIN) continue;
                     }
                     const float Tn = __fmul_rn(T, __fsub_rn(1.0f, a));
@@ -414,7 +429,7 @@ __device__ __forceinline__ void flush_grad_soft(float* __restrict__ v_splats, fl
 // carries four more terms per entry: eight CTAs (64 registers).
 template <bool STATS, bool SOFT>
 __global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : 10)
-k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict__ tile_range,
+k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
                 const int32_t* __restrict__ gids, const float4* __restrict__ splats,
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
@@ -476,7 +491,7 @@ k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
         if ((int)threadIdx.x < n_prev && sG[threadIdx.x] >= 0) {
             if (SOFT)
                 flush_grad_soft(v_splats, v_depth_model, sG[threadIdx.x], sAcc[threadIdx.x], sD[threadIdx.x],
-                                softness);
+                                sp.softness);
             else
                 flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x]);
         }
@@ -489,7 +504,7 @@ k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
             sG[threadIdx.x] = g;
             if (g >= 0) {
                 stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
-                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, softness, sC[threadIdx.x].y);
+                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, sp, sC[threadIdx.x].y);
             } else {
                 stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
             }
@@ -534,12 +549,12 @@ k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
                     const Eval e = eval_splat(A, B, px, py);
                     if (e.skip) continue;
                     float a = e.alpha, f = 1.0f, x = 0.0f, kap = 0.0f;
-                    if (soft) {  // the composited alpha is alpha f, f = Phi(x)
+                    if (soft) {  // the composited alpha is alpha f, f = f(x)
                         const float4 Dm = sD[k];
                         const float zs = fmaf(Dm.x, e.dx, fmaf(Dm.y, e.dy, C3.y));
                         kap = Dm.z;
                         x = (D - zs) * kap;
-                        f = normcdff(x);
+                        f = sp.front(x);
                         a = e.alpha * f;
                         if (a < ALPHA_MIN) continue;
                     }
@@ -558,8 +573,8 @@ k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
                         pvo[jj] = dLdal * e.G;
                         pds[jj] = -dLdal * e.alpha;  // d alpha / d sigma = -alpha
                     }
-                    if (soft) {  // dL/dx = dLda alpha phi(x), phi the standard normal density
-                        const float psi = dLda * e.alpha * (0.3989422804014327f * __expf(-0.5f * x * x));
+                    if (soft) {  // dL/dx = dLda alpha f'(x)
+                        const float psi = dLda * e.alpha * sp.density(x, f);
                         pz[jj] = psi * kap;
                         psx[jj] = psi * x;
                         vD += psi * kap;
@@ -629,7 +644,7 @@ k_composite_bwd(Cam c, float3 bg, int N, float softness, const int2* __restrict_
 
 }  // namespace
 
-cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
                           float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s)
@@ -638,13 +653,14 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness
     auto kern = soft ? (stats ? k_composite_fwd<true, true> : k_composite_fwd<false, true>)
                      : (stats ? k_composite_fwd<true, false> : k_composite_fwd<false, false>);
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
-        c, make_float3(bg[0], bg[1], bg[2]), N, softness, reinterpret_cast<const int2*>(tile_range), gids,
+        c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
+        gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
         face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, reinterpret_cast<unsigned long long*>(stats));
     return cudaGetLastError();
 }
 
-cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, const float* T_final,
                           const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
@@ -655,7 +671,8 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
     auto kern = soft ? (stats ? k_composite_bwd<true, true> : k_composite_bwd<false, true>)
                      : (stats ? k_composite_bwd<true, false> : k_composite_bwd<false, false>);
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
-        c, make_float3(bg[0], bg[1], bg[2]), N, softness, reinterpret_cast<const int2*>(tile_range), gids,
+        c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
+        gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
         face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth,
         reinterpret_cast<unsigned long long*>(stats));

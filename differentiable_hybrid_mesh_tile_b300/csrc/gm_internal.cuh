@@ -206,11 +206,11 @@ cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
 
-cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
                           float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s);
-cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, const int32_t* tile_range,
+cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, const float* T_final,
                           const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,

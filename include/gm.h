@@ -85,7 +85,12 @@ typedef struct gm_opts {
                                can reach alpha >= 1/255 (see gm_bin_sort_gaussians) */
     float softness;         /* 0: hard depth test; > 0: soft split of each Gaussian at the mesh
                                (see gm_composite_hybrid_fwd) with this width factor */
+    int32_t soft_split;     /* form of the split's front fraction f(x): GM_SPLIT_PHI (the
+                               standard normal CDF) or GM_SPLIT_LOGISTIC (1 / (1 + exp(-1.702 x))) */
 } gm_opts;
+
+#define GM_SPLIT_PHI 0
+#define GM_SPLIT_LOGISTIC 1
 
 /*
  * Projected-Gaussian record ("splat"), GM_SPLAT_STRIDE floats, 16-byte aligned:
@@ -258,9 +263,12 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
  * required, 16-byte aligned), scales its alpha: alpha f replaces alpha in the
  * skip, the stop and the sums (the back parts lie behind the opaque mesh).
  * Uncovered pixels are unchanged.  depth_model is ignored when softness = 0.
+ * opts->soft_split picks f = Phi (GM_SPLIT_PHI) or the logistic 1 / (1 +
+ * exp(-1.702 x)) (GM_SPLIT_LOGISTIC) as the front fraction.
  * Each warp's 8 x 4 pixel block passes over the Gaussians with z_c - R -
- * 2.75 sigma_z softness beyond the largest mesh depth of its pixels (all
- * covered): f <= Phi(-2.75) puts alpha f below 1/255 at each of them.
+ * t sigma_z softness beyond the largest mesh depth of its pixels (all
+ * covered), t = 2.75 for Phi and 3.5 for the logistic: f(-t) puts alpha f
+ * below 1/255 at each of them.
  * ---------------------------------------------------------------------- */
 int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
                             const int32_t* tile_range, const int32_t* gids, const float* splats,

@@ -841,14 +841,24 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
         o->m_clamp = fmin(o->m_clamp, mc);
         int clamped = oG > amax;
         double alpha = clamped ? amax : oG;
+        double a_lo = -1.0, a_hi = -1.0; /* the split's alpha f at x -+ its rounding bound */
         if (soft) {
             double zs = rnd(z + rnd(rnd(dmfield(sm, g, 0, p) * dx, f32) + rnd(dmfield(sm, g, 1, p) * dy, f32), f32),
                             f32);
-            double xa = rnd(rnd(D - zs, f32) / rnd(dmfield(sm, g, 2, p) * sm->softness, f32), f32);
+            double band = rnd(dmfield(sm, g, 2, p) * sm->softness, f32);
+            double xa = rnd(rnd(D - zs, f32) / band, f32);
             double f = rnd(split_front(xa, sm->logistic), f32);
+            /* an fp32 evaluation of x = (D - z*) / band in another order lands within
+             * about 4 eps ((|D| + |z*|) / band + |x|) of this one */
+            double ex = 4.0 * FLT_EPSILON * ((fabs(D) + fabs(zs)) / band + fabs(xa));
+            a_lo = alpha * split_front(xa - ex, sm->logistic);
+            a_hi = alpha * split_front(xa + ex, sm->logistic);
             alpha = rnd(alpha * f, f32);
         }
+        /* relative distance of the skip operand to 1/255; under the split, of the
+         * whole range that the rounding of x allows (negative: either side is possible) */
         double ma = fabs(alpha - amin) / amin;
+        if (soft) ma = a_hi < amin ? (amin - a_hi) / amin : (a_lo >= amin ? (a_lo - amin) / amin : -1.0);
         o->m_alpha = fmin(o->m_alpha, ma);
         if (g == watch) o->m_self = fmin(o->m_self, fmin(ms, fmin(mc, ma)));
         if (alpha < amin) {

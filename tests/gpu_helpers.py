@@ -114,9 +114,9 @@ def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=N
 
 
 def run_composite(cam, bg, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id, softness=0.0,
-                  depth_model=None):
+                  depth_model=None, soft_split=0):
     c = gm.make_camera(cam)
-    o = gm.make_opts(bg, True, -1, True, softness)
+    o = gm.make_opts(bg, True, -1, True, softness, soft_split)
     H, W = cam.height, cam.width
     out = {k: torch.full(s, -3.0, dtype=torch.float32, device="cuda")
            for k, s in [("rgb", (H, W, 3)), ("depth", (H, W)), ("alpha", (H, W)), ("T", (H, W))]}
@@ -132,7 +132,7 @@ def run_composite(cam, bg, tile_range, gids, splats, mesh_depth, mesh_rgb, face_
     res["n_contrib"] = host(nc)
     res["_args"] = args
     res["_dev"] = dict(T=out["T"], n_contrib=nc)
-    res["_soft"] = (softness, dm)
+    res["_soft"] = (softness, dm, soft_split)
     return res
 
 
@@ -141,8 +141,8 @@ def run_composite_bwd(cam, bg, fwd, grads, N, mesh=None, mesh_grads=False):
     softness and depth model included).  Returns v_splats (+ v_verts / v_vcol
     with mesh_grads; + v_depth_model and v_mesh_depth with the soft split)."""
     c = gm.make_camera(cam)
-    softness, dm = fwd.get("_soft", (0.0, None))
-    o = gm.make_opts(bg, True, -1, True, softness)
+    softness, dm, split = fwd.get("_soft", (0.0, None, 0))
+    o = gm.make_opts(bg, True, -1, True, softness, split)
     soft = softness > 0.0
     v_splats = torch.zeros(max(N, 1), 12, dtype=torch.float32, device="cuda")
     v_dm = torch.zeros(max(N, 1), 4, dtype=torch.float32, device="cuda") if soft else None

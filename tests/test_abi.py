@@ -101,6 +101,9 @@ def test_null_and_size_checks(lib):
                                      None, C.c_void_p(256), 3, C.c_void_p(256), 1, C.c_void_p(256),
                                      C.c_void_p(256), C.c_void_p(256), None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"v_mesh_depth" in lib.gm_last_error()
+    bad_split = gm.make_opts(softness=1.0, soft_split=2)
+    st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(bad_split), 4, *([C.c_void_p(256)] * 12), None, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"soft_split" in lib.gm_last_error()
     # misaligned v_depth_model in the projection backward
     st = lib.gm_project_gaussians_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 7), C.c_void_p(260),
                                       0, *([C.c_void_p(256)] * 5), None)
@@ -112,3 +115,18 @@ def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(gm, "_lib", None)
     with pytest.raises(ImportError):
         gm.lib()
+
+
+def test_header_constants_match_binding():
+    """Every GM_* integer constant the header defines has the same value in the binding."""
+    import re
+    text = open(gm.HEADER).read()
+    found = dict((k, int(v)) for k, v in re.findall(r"^#define\s+(GM_\w+)\s+(\d+)\s*$", text, re.M))
+    assert "GM_SPLIT_LOGISTIC" in found and "GM_FLAG_TIMEOUT" in found
+    for name, value in found.items():
+        if hasattr(gm, name):
+            assert getattr(gm, name) == value, name
+    # the option struct's fields in header order
+    body = re.search(r"typedef struct gm_opts \{(.*?)\} gm_opts;", text, re.S).group(1)
+    names = re.findall(r"^\s*(?:float|int32_t)\s+(\w+)(?:\[\d+\])?;", body, re.M)
+    assert names == [f[0] for f in gm.gm_opts._fields_]

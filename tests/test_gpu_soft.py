@@ -11,7 +11,9 @@ against the CPU oracle.
   the hard split at pixels the mesh does not cover;
 - the soft backward (record fields, depth-model fields, and the mesh vertices
   through dL/dD at the split) against the oracle's central differences;
-- the renderer classes with softness > 0 against the per-call path."""
+- the renderer classes with softness > 0 against the per-call path;
+- the logistic form of the front fraction on the same checks (forward, skip,
+  finite differences)."""
 
 import numpy as np
 import pytest
@@ -41,7 +43,7 @@ def _scene(name):
     raise KeyError(name)
 
 
-def soft_pipeline(scene, softness=SOFTNESS):
+def soft_pipeline(scene, softness=SOFTNESS, split=0):
     """Mesh, projection with the depth model, bins without the occlusion cull
     (the soft split turns it off), soft composite."""
     cam = scene.camera
@@ -49,15 +51,18 @@ def soft_pipeline(scene, softness=SOFTNESS):
     sp, rad, tt, dm = H.run_project(cam, scene.gaussians, scene.bg, depth_model=True)
     b = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull=False)
     f = H.run_composite(cam, scene.bg, b["tile_range"], b["gids"], sp, m["mesh_depth"], m["mesh_rgb"],
-                        m["face_id"], softness=softness, depth_model=dm)
-    return dict(cam=cam, mesh=m, splats=sp, radii=rad, dm=dm, bins=b, fwd=f)
+                        m["face_id"], softness=softness, depth_model=dm, soft_split=split)
+    return dict(cam=cam, mesh=m, splats=sp, radii=rad, dm=dm, bins=b, fwd=f, split=split)
 
 
-@pytest.fixture(scope="module", params=["tiny", "sphere512", "soup_small"])
+# scene, front fraction (0: Phi, 1: logistic)
+@pytest.fixture(scope="module", params=[("tiny", 0), ("sphere512", 0), ("soup_small", 0), ("tiny", 1),
+                                        ("sphere512", 1)], ids=lambda p: p[0] + ("_logistic" if p[1] else ""))
 def run(request):
     H.need_gpu()
-    s = _scene(request.param)
-    return request.param, s, soft_pipeline(s)
+    name, split = request.param
+    s = _scene(name)
+    return name + ("_logistic" if split else ""), s, soft_pipeline(s, split=split)
 
 
 def _quat_rot(q):
@@ -148,7 +153,7 @@ def test_hidden_gaussian_skip_changes_nothing(run):
     dm = r["dm"].copy()
     dm[:, 3] = np.inf
     f0 = H.run_composite(cam, s.bg, b["tile_range"], b["gids"], r["splats"], m["mesh_depth"], m["mesh_rgb"],
-                         m["face_id"], softness=SOFTNESS, depth_model=dm)
+                         m["face_id"], softness=SOFTNESS, depth_model=dm, soft_split=r["split"])
     f1 = r["fwd"]
     for k in ("rgb", "depth", "alpha", "T", "n_contrib"):
         np.testing.assert_array_equal(f0[k], f1[k])
@@ -167,7 +172,7 @@ def test_soft_forward_matches_oracle(run, orc):
     cam, f, m = r["cam"], r["fwd"], r["mesh"]
     lists = orc.tile_lists(cam, r["splats"], r["radii"])
     o = orc.composite_fwd(cam, s.bg, r["splats"], lists, m["mesh_depth"], m["mesh_rgb"], m["face_id"],
-                          depth_model=r["dm"], softness=SOFTNESS)
+                          depth_model=r["dm"], softness=SOFTNESS, split=r["split"])
     tie = H.tie_pixels(o["margins"])
     ok = ~tie
     for k in ("rgb", "depth", "alpha"):
@@ -201,9 +206,20 @@ def test_uncovered_pixels_as_hard_split(run):
         np.testing.assert_array_equal(hard[k][unc], r["fwd"][k][unc])
 
 
-def _fd_requests(rng, radii, n_gauss, fields):
-    vis = np.nonzero(radii > 0)[0]
-    pick = vis if len(vis) <= n_gauss else np.sort(rng.choice(vis, n_gauss, replace=False))
+def _fd_requests(rng, r, n_gauss, fields):
+    """Half of the sample among the Gaussians whose centre lies within 3 sigma_z of
+    the mesh surface at its own pixel (where the split acts), half among the rest."""
+    radii, sp, dm, m = r["radii"], r["splats"], r["dm"], r["mesh"]
+    H_, W_ = m["face_id"].shape
+    ix = np.clip(np.floor(sp[:, 0]).astype(np.int64), 0, W_ - 1)
+    iy = np.clip(np.floor(sp[:, 1]).astype(np.int64), 0, H_ - 1)
+    D = m["mesh_depth"][iy, ix]
+    near = (radii > 0) & (m["face_id"][iy, ix] >= 0) & (np.abs(sp[:, 9] - D) < 3 * SOFTNESS * dm[:, 2])
+    pick = []
+    for pool, k in ((np.flatnonzero(near), n_gauss // 2), (np.flatnonzero((radii > 0) & ~near), n_gauss)):
+        k = min(k, len(pool), n_gauss - len(pick))
+        pick.extend(rng.choice(pool, k, replace=False).tolist())
+    pick = np.sort(np.asarray(pick, np.int64))
     return np.repeat(pick, len(fields)), np.tile(np.array(list(fields)), len(pick))
 
 
@@ -225,11 +241,12 @@ def _steps(splats, dm, gid, fld):
     return h
 
 
-@pytest.mark.parametrize("name,n_gauss,n_vert", [("tiny", 600, 42), ("sphere512", 250, 120)])
-def test_soft_backward_matches_finite_differences(name, n_gauss, n_vert, orc):
+@pytest.mark.parametrize("name,n_gauss,n_vert,split", [("tiny", 600, 42, 0), ("sphere512", 250, 120, 0),
+                                                       ("tiny", 600, 42, 1)])
+def test_soft_backward_matches_finite_differences(name, n_gauss, n_vert, split, orc):
     H.need_gpu()
     s = _scene(name)
-    r = soft_pipeline(s)
+    r = soft_pipeline(s, split=split)
     cam, m, f, dm = r["cam"], r["mesh"], r["fwd"], r["dm"]
     grads = scenes.upstream_grads(17, cam.width, cam.height)
     b = H.run_composite_bwd(cam, s.bg, f, grads, len(r["radii"]), s.mesh, mesh_grads=True)
@@ -239,10 +256,11 @@ def test_soft_backward_matches_finite_differences(name, n_gauss, n_vert, orc):
     lists = orc.tile_lists(cam, r["splats"], r["radii"])
     rng = np.random.default_rng(9)
     fields = list(range(10)) + [F_GU, F_GV, F_SZ]
-    gid, fld = _fd_requests(rng, r["radii"], n_gauss, fields)
+    gid, fld = _fd_requests(rng, r, n_gauss, fields)
     hs = _steps(r["splats"], dm, gid, fld)
     fd, st = orc.composite_fd(cam, np.float64(s.bg), r["splats"], r["radii"], lists, m["mesh_depth"],
-                              m["mesh_rgb"], m["face_id"], grads, gid, fld, hs, depth_model=dm, softness=SOFTNESS)
+                              m["mesh_rgb"], m["face_id"], grads, gid, fld, hs, depth_model=dm, softness=SOFTNESS,
+                              split=split)
     got = np.where(fld < 12, b["v_splats"][gid, np.minimum(fld, 11)],
                    b["v_depth_model"][gid, np.clip(fld - 12, 0, 3)]).astype(np.float64)
     ok = st == 0
@@ -268,12 +286,12 @@ def test_soft_backward_matches_finite_differences(name, n_gauss, n_vert, orc):
     args = (cam, np.float64(s.bg))
     rest = (s.mesh.faces, s.mesh.vcol, m["face_id"].reshape(-1), r["splats"], lists, m["mesh_depth"].reshape(-1),
             m["mesh_rgb"].reshape(-1, 3), grads, vid, vf, vh)
-    vfd, vst = orc.mesh_fd(*args, s.mesh.verts, *rest, depth_model=dm, softness=SOFTNESS)
+    vfd, vst = orc.mesh_fd(*args, s.mesh.verts, *rest, depth_model=dm, softness=SOFTNESS, split=split)
     vgot = np.where(vf < 3, b["v_verts"][vid, np.minimum(vf, 2)], b["v_vcol"][vid, np.maximum(vf - 3, 0)])
     vok = vst == 0
     sens = np.zeros(len(vid))
     for V2 in H.input_ulp_perturbations(cam, s.mesh.verts, draws=2):
-        v2, st2 = orc.mesh_fd(*args, V2, *rest, depth_model=dm, softness=SOFTNESS)
+        v2, st2 = orc.mesh_fd(*args, V2, *rest, depth_model=dm, softness=SOFTNESS, split=split)
         sens = np.maximum(sens, np.where(st2 == 0, np.abs(v2 - vfd), np.inf))
     vok &= np.isfinite(sens)
     verr = np.abs(vgot - vfd)

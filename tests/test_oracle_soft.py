@@ -261,3 +261,29 @@ def test_finite_differences_through_the_depth_model(orc, split):
     assert (st == 0).all(), st
     for k, fld in enumerate(fields):
         np.testing.assert_allclose(got[k], want[int(fld)], rtol=2e-5, atol=1e-9)
+
+
+@pytest.mark.parametrize("split", [0, 1], ids=["phi", "logistic"])
+def test_skip_margin_carries_the_split_rounding(orc, split):
+    """The reported alpha-skip margin of a covered pixel covers the rounding bound
+    of x = (D - z*) / (sigma_z softness): a thin depth extent makes the decision
+    ill-conditioned where the surface z* meets the mesh, and the margin says so
+    there (negative) and only there."""
+    cam, splats, dm, radii, lists, D, cm, face = _flat_scene()
+    out = {}
+    for sz in (0.5, 1e-6):
+        d = dm.copy()
+        d[0, 2] = sz
+        o = orc.composite_fwd(cam, (1, 1, 1), splats, lists, D.reshape(16, 16), cm.reshape(16, 16, 3),
+                              face.reshape(16, 16), depth_model=d, softness=1.0, split=split)
+        out[sz] = o["margins"][..., 1]
+    wide, thin = out[0.5], out[1e-6]
+    assert np.isfinite(wide).all() and (wide > 1e-3).mean() > 0.9
+    # with sigma_z = 1e-6 the decision is ill-conditioned exactly where the surface
+    # z*(p) passes within a few hundred sigma_z of the mesh depth, and nowhere else
+    s = splats[0].astype(np.float64)
+    j, i = np.mgrid[0:16, 0:16]
+    zs = s[S_Z] + float(dm[0, 0]) * (i + 0.5 - s[S_MX]) + float(dm[0, 1]) * (j + 0.5 - s[S_MY])
+    near = np.abs(4.0 - zs) < 1e-4
+    assert near.any() and (thin[near] < 0).all()
+    assert (thin[np.abs(4.0 - zs) > 1e-3] > 0).all()
