@@ -116,6 +116,45 @@ def interp_mesh(cam, V, F, vcol, face_id, pixels=None):
     return depth, rgb
 
 
+def _opt(a, dt):
+    return None if a is None else _c(a, dt)
+
+
+def mesh_edges(F):
+    """Edge adjacency [nF][3]: the face across edge k (corners k+1, k+2) of each
+    face, -1 none, -2 shared by more than two faces."""
+    F = _c(F, np.int32)
+    adj = np.zeros((len(F), 3), np.int32)
+    lib().orc_mesh_edges(_p(F), C.c_int32(len(F)), _p(adj))
+    return adj
+
+
+def antialias(cam, V, F, adj, face_id, mesh_depth, mesh_rgb, pixels=None):
+    """Antialiased mesh layer from full-frame face ids, depth and colour: cov
+    [H][W], premultiplied colour [H][W][3], split depth [H][W] and the pair
+    decision codes [H][W][4] (written at the listed pixels, all when None)."""
+    H, W = cam.height, cam.width
+    cov = np.zeros((H, W), np.float32)
+    rgb = np.zeros((H, W, 3), np.float32)
+    depth = np.full((H, W), np.inf, np.float32)
+    codes = np.zeros((H, W, 4), np.int32)
+    pix = None if pixels is None else _c(pixels, np.int32)
+    lib().orc_antialias(C.byref(_cam(cam)), _p(_c(V, np.float32)), _p(_c(F, np.int32)), _p(_c(adj, np.int32)),
+                        _p(_c(face_id, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
+                        _p(pix), C.c_int64(0 if pixels is None else len(pixels)), _p(cov), _p(rgb), _p(depth),
+                        _p(codes))
+    return cov, rgb, depth, codes
+
+
+def tile_bounds_cov(cam, cov, depth):
+    T = n_tiles(cam)
+    far = np.zeros(T, np.float32)
+    full = np.zeros(T, np.uint8)
+    lib().orc_tile_bounds_cov(C.byref(_cam(cam)), _p(_c(cov, np.float32)), _p(_c(depth, np.float32)), _p(far),
+                              _p(full))
+    return far, full
+
+
 def tile_depth_bounds(cam, mesh_depth):
     md = _c(mesh_depth, np.float32).reshape(-1)
     T = n_tiles(cam)
@@ -235,10 +274,11 @@ def _soft(depth_model, softness):
 
 
 def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=None, depth_model=None,
-                  softness=0.0, split=SPLIT_PHI):
+                  softness=0.0, split=SPLIT_PHI, mesh_cov=None):
     """Full-frame outputs; only pixels of ``tiles`` (all when None) are written.
     With depth_model and softness > 0: the soft split (front fraction Phi, or
-    its logistic approximation with split=SPLIT_LOGISTIC)."""
+    its logistic approximation with split=SPLIT_LOGISTIC).  With mesh_cov: the
+    antialiased mesh layer (mesh_rgb premultiplied, mesh_depth the split depth)."""
     dm, sf = _soft(depth_model, softness)
     start, entries = lists
     H, W = cam.height, cam.width
@@ -252,15 +292,17 @@ def composite_fwd(cam, bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles=N
     lib().orc_composite_fwd(
         C.byref(_cam(cam)), _p(bgv), _p(_c(splats, np.float32)), _p(_c(start, np.int64)),
         _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
-        _p(_c(face_id, np.int32)), _p(tl), C.c_int32(0 if tiles is None else len(tiles)),
+        _p(_c(face_id, np.int32)), _p(_opt(mesh_cov, np.float32)), _p(tl),
+        C.c_int32(0 if tiles is None else len(tiles)),
         _p(out["rgb"]), _p(out["depth"]), _p(out["alpha"]), _p(out["T"]), _p(out["n_contrib"]),
         _p(out["margins"]), _p(dm), sf, C.c_int32(split))
     return out
 
 
 def composite_fd(cam, bg, splats, radii, lists, mesh_depth, mesh_rgb, face_id, grads,
-                 gids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0, split=SPLIT_PHI):
-    """fields 0..9: record fields; 12, 13, 14: depth model g_u, g_v, sigma_z."""
+                 gids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0, split=SPLIT_PHI, mesh_cov=None):
+    """fields 0..9: record fields; 12, 13, 14: depth model g_u, g_v, sigma_z.
+    With mesh_cov: over the antialiased mesh layer (as composite_fwd)."""
     dm, sf = _soft(depth_model, softness)
     start, entries = lists
     g_rgb, g_depth, g_alpha = (_c(x, np.float32) for x in grads)
@@ -270,14 +312,17 @@ def composite_fd(cam, bg, splats, radii, lists, mesh_depth, mesh_rgb, face_id, g
     lib().orc_composite_fd(
         C.byref(_cam(cam)), _p(_c(bg, np.float32)), _p(_c(splats, np.float32)), _p(_c(radii, np.int32)),
         _p(_c(start, np.int64)), _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)),
-        _p(_c(mesh_rgb, np.float32)), _p(_c(face_id, np.int32)), _p(g_rgb), _p(g_depth), _p(g_alpha),
+        _p(_c(mesh_rgb, np.float32)), _p(_c(face_id, np.int32)), _p(_opt(mesh_cov, np.float32)), _p(g_rgb),
+        _p(g_depth), _p(g_alpha),
         C.c_int32(n), _p(_c(gids, np.int32)), _p(_c(fields, np.int32)), _p(_c(hs, np.float64)),
         C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf, C.c_int32(split))
     return grad, status
 
 
 def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, grads,
-            vids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0, split=SPLIT_PHI):
+            vids, fields, hs, tie_band=1e-5, depth_model=None, softness=0.0, split=SPLIT_PHI, adj=None):
+    """dL/d(vertex position 0..2, colour 3..5); with adj (mesh_edges) through the
+    antialiased layer as well.  mesh_depth / mesh_rgb: the interpolated images."""
     dm, sf = _soft(depth_model, softness)
     start, entries = lists
     V, F, vcol = _c(V, np.float32), _c(F, np.int32), _c(vcol, np.float32)
@@ -287,7 +332,8 @@ def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, g
     status = np.zeros(n, np.int32)
     lib().orc_mesh_fd(
         C.byref(_cam(cam)), _p(_c(bg, np.float32)), _p(V), C.c_int32(len(V)), _p(F), C.c_int32(len(F)),
-        _p(vcol), _p(_c(face_id, np.int32)), _p(_c(splats, np.float32)), _p(_c(start, np.int64)),
+        _p(vcol), _p(_c(face_id, np.int32)), _p(_opt(adj, np.int32)), _p(_c(splats, np.float32)),
+        _p(_c(start, np.int64)),
         _p(_c(entries, np.int32)), _p(_c(mesh_depth, np.float32)), _p(_c(mesh_rgb, np.float32)),
         _p(g_rgb), _p(g_depth), _p(g_alpha), C.c_int32(n), _p(_c(vids, np.int32)),
         _p(_c(fields, np.int32)), _p(_c(hs, np.float64)), C.c_double(tie_band), _p(grad), _p(status), _p(dm), sf,
@@ -296,22 +342,28 @@ def mesh_fd(cam, bg, V, F, vcol, face_id, splats, lists, mesh_depth, mesh_rgb, g
 
 
 def composite_one(px, py, splats, order, D=np.inf, covered=False, cm=(0, 0, 0), bg=(1, 1, 1), f32=True,
-                  depth_model=None, softness=0.0, split=SPLIT_PHI):
-    """One pixel over an explicit ordered list of splat ids: rgb, depth, alpha, T, n_contrib."""
+                  depth_model=None, softness=0.0, split=SPLIT_PHI, cov=None):
+    """One pixel over an explicit ordered list of splat ids: rgb, depth, alpha, T,
+    n_contrib.  The mesh layer: covered (0/1) with colour cm, or, with cov, a
+    coverage in [0, 1] with premultiplied colour cm."""
     dm, sf = _soft(depth_model, softness)
     out = np.zeros(7, np.float64)
     lst = _c(order, np.int32)
+    a = float(cov) if cov is not None else (1.0 if covered else 0.0)
+    M = np.asarray(cm, np.float64) if (cov is not None or covered) else np.zeros(3)
     lib().orc_composite_one(C.c_int32(int(f32)), C.c_double(px), C.c_double(py), _p(lst), C.c_int64(len(lst)),
-                            _p(_c(splats, np.float32)), C.c_double(D), C.c_int32(int(covered)),
-                            _p(_c(cm, np.float64)), _p(_c(bg, np.float64)), _p(out), _p(dm), sf, C.c_int32(split))
+                            _p(_c(splats, np.float32)), C.c_double(D), C.c_double(a),
+                            _p(_c(M, np.float64)), _p(_c(bg, np.float64)), _p(out), _p(dm), sf, C.c_int32(split))
     return {"rgb": out[:3], "depth": out[3], "alpha": out[4], "T": out[5], "n_contrib": int(out[6])}
 
 
 # ------------------------------------------------------------ pipeline ----
 
-def render(scene, cam=None, tiles=None, softness=0.0, split=SPLIT_PHI):
+def render(scene, cam=None, tiles=None, softness=0.0, split=SPLIT_PHI, antialias_edges=False):
     """Whole forward pass from raw inputs for the listed tiles (all when None),
-    with the soft split when softness > 0.
+    with the soft split when softness > 0 and the antialiased mesh layer when
+    antialias_edges is set (the z-buffer and interpolation then also cover a
+    one-pixel ring around the tiles, whose pairs the antialiasing reads).
 
     Returns a dict of full-frame arrays (pixels outside ``tiles`` are zero)
     with every intermediate the parity tests look at."""
@@ -321,6 +373,7 @@ def render(scene, cam=None, tiles=None, softness=0.0, split=SPLIT_PHI):
     if tiles is None:
         pixels = None
         tiles_arr = None
+        mesh_pixels = None
     else:
         tiles_arr = np.asarray(tiles, np.int32)
         pix = []
@@ -330,24 +383,40 @@ def render(scene, cam=None, tiles=None, softness=0.0, split=SPLIT_PHI):
             xs = np.arange(tx * 16, min(tx * 16 + 16, W))
             pix.append((ys[:, None] * W + xs[None, :]).reshape(-1))
         pixels = np.concatenate(pix).astype(np.int32)
+        mesh_pixels = pixels
+        if antialias_edges:
+            ring = [pixels]
+            i, j = pixels % W, pixels // W
+            for di, dj in ((-1, 0), (1, 0), (0, -1), (0, 1)):
+                ok = (i + di >= 0) & (i + di < W) & (j + dj >= 0) & (j + dj < H)
+                ring.append(((j + dj) * W + (i + di))[ok])
+            mesh_pixels = np.unique(np.concatenate(ring)).astype(np.int32)
     m = scene.mesh
-    fid_s, best_s, second_s = zbuffer(cam, m.verts, m.faces, pixels)
-    depth_s, rgb_s = interp_mesh(cam, m.verts, m.faces, m.vcol, fid_s, pixels)
+    fid_s, best_s, second_s = zbuffer(cam, m.verts, m.faces, mesh_pixels)
+    depth_s, rgb_s = interp_mesh(cam, m.verts, m.faces, m.vcol, fid_s, mesh_pixels)
     face_id = np.full(W * H, -1, np.int32)
     mesh_depth = np.full(W * H, np.inf, np.float32)
     mesh_rgb = np.zeros((W * H, 3), np.float32)
     best = np.full(W * H, np.inf, np.float32)
     second = np.full(W * H, np.inf, np.float32)
-    sel = np.arange(W * H) if pixels is None else pixels
+    sel = np.arange(W * H) if mesh_pixels is None else mesh_pixels
     face_id[sel], mesh_depth[sel], mesh_rgb[sel] = fid_s, depth_s, rgb_s
     best[sel], second[sel] = best_s, second_s
     splats, radii, touched, margin = project(cam, scene.gaussians)
     lists = tile_lists(cam, splats, radii, tiles_arr)
     dm = project_depth_model(cam, scene.gaussians) if softness > 0.0 else None
-    out = composite_fwd(cam, scene.bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles_arr,
-                        depth_model=dm, softness=softness, split=split)
+    layer = {}
+    if antialias_edges:
+        adj = mesh_edges(m.faces)
+        cov, rgb_aa, depth_aa, codes = antialias(cam, m.verts, m.faces, adj, face_id, mesh_depth, mesh_rgb, pixels)
+        layer = dict(adj=adj, cov=cov, rgb_aa=rgb_aa, depth_aa=depth_aa, aa_codes=codes)
+        out = composite_fwd(cam, scene.bg, splats, lists, depth_aa, rgb_aa, face_id, tiles_arr,
+                            depth_model=dm, softness=softness, split=split, mesh_cov=cov)
+    else:
+        out = composite_fwd(cam, scene.bg, splats, lists, mesh_depth, mesh_rgb, face_id, tiles_arr,
+                            depth_model=dm, softness=softness, split=split)
     out.update(face_id=face_id.reshape(H, W), mesh_depth=mesh_depth.reshape(H, W),
                mesh_rgb=mesh_rgb.reshape(H, W, 3), zbest=best.reshape(H, W),
                zsecond=second.reshape(H, W), splats=splats, radii=radii,
-               tiles_touched=touched, radius_margin=margin, lists=lists, pixels=pixels, depth_model=dm)
+               tiles_touched=touched, radius_margin=margin, lists=lists, pixels=pixels, depth_model=dm, **layer)
     return out

@@ -343,6 +343,327 @@ void orc_tile_depth_bounds(const orc_camera* c, const float* mesh_depth, float* 
 }
 
 /* ========================================================================
+ * Mesh rasterizer, item 3: analytic edge antialiasing at silhouettes
+ * ====================================================================== */
+
+/* Edge k of face f joins its corners k+1 and k+2 (mod 3), the edge opposite
+ * corner k (the edge function e_k of the coverage test).  adj[3 f + k] is the
+ * other face with the same two vertices, -1 when there is none, -2 when more
+ * than two faces share them.                                              */
+typedef struct {
+    uint64_t key;
+    int32_t fe;
+} edge_rec;
+
+static int edge_rec_cmp(const void* a, const void* b)
+{
+    const edge_rec* x = (const edge_rec*)a;
+    const edge_rec* y = (const edge_rec*)b;
+    if (x->key != y->key) return x->key < y->key ? -1 : 1;
+    return (x->fe > y->fe) - (x->fe < y->fe);
+}
+
+void orc_mesh_edges(const int32_t* F, int32_t nF, int32_t* adj)
+{
+    int64_t n = 3 * (int64_t)nF;
+    edge_rec* e = (edge_rec*)malloc(sizeof(edge_rec) * (n > 0 ? n : 1));
+    for (int f = 0; f < nF; ++f)
+        for (int k = 0; k < 3; ++k) {
+            uint32_t a = (uint32_t)F[3 * f + (k + 1) % 3], b = (uint32_t)F[3 * f + (k + 2) % 3];
+            uint32_t lo = a < b ? a : b, hi = a < b ? b : a;
+            e[3 * f + k].key = ((uint64_t)lo << 32) | hi;
+            e[3 * f + k].fe = 3 * f + k;
+        }
+    qsort(e, (size_t)n, sizeof(edge_rec), edge_rec_cmp);
+    for (int64_t i = 0; i < n;) {
+        int64_t j = i;
+        while (j < n && e[j].key == e[i].key) ++j;
+        for (int64_t q = i; q < j; ++q)
+            adj[e[q].fe] = j - i == 1 ? -1 : (j - i == 2 ? e[i + j - 1 - q].fe / 3 : -2);
+        i = j;
+    }
+    free(e);
+}
+
+/* The mesh as the antialiasing sees it: vertices (one of them optionally
+ * moved by delta along one axis, for finite differences), faces, adjacency,
+ * the z-buffer's face ids, and the interpolated depth and colour per pixel
+ * (fp32 images, with optional double values overriding a sorted pixel set). */
+typedef struct {
+    const orc_camera* c;
+    const float* V;
+    const int32_t* F;
+    const int32_t* adj;
+    const int32_t* face_id;
+    const float* depth;
+    const float* rgb;
+    int pvid, pfield;
+    double pdelta;
+    const int64_t* ov_pix;
+    const double* ov_depth;
+    const double* ov_rgb;
+    int64_t n_ov;
+} aa_view;
+
+static int64_t aa_find(const aa_view* w, int64_t pix)
+{
+    int64_t lo = 0, hi = w->n_ov;
+    while (lo < hi) {
+        int64_t mid = (lo + hi) / 2;
+        if (w->ov_pix[mid] < pix) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo < w->n_ov && w->ov_pix[lo] == pix ? lo : -1;
+}
+
+static double aa_depth(const aa_view* w, int64_t pix)
+{
+    int64_t k = w->n_ov ? aa_find(w, pix) : -1;
+    return k >= 0 ? w->ov_depth[k] : (double)w->depth[pix];
+}
+
+static void aa_rgb(const aa_view* w, int64_t pix, double c[3])
+{
+    int64_t k = w->n_ov ? aa_find(w, pix) : -1;
+    for (int ch = 0; ch < 3; ++ch) c[ch] = k >= 0 ? w->ov_rgb[3 * k + ch] : (double)w->rgb[3 * pix + ch];
+}
+
+/* screen position (u, v) of vertex vid: fp32 one rounding per operation in
+ * the rasterizer's order (f32 = 1; the vertex must be unmoved), or double.
+ * Returns 0 when the vertex is not beyond the near plane.                */
+static int aa_vertex(const aa_view* w, int f32, int vid, double* u, double* v)
+{
+    const orc_camera* c = w->c;
+    if (f32) {
+        float xc[3];
+        world_to_cam_f32(c, w->V + 3 * (int64_t)vid, xc);
+        if (!(xc[2] > c->near_plane)) return 0;
+        *u = (float)((c->fx * xc[0]) / xc[2] + c->cx);
+        *v = (float)((c->fy * xc[1]) / xc[2] + c->cy);
+        return 1;
+    }
+    double X[3];
+    for (int d = 0; d < 3; ++d)
+        X[d] = (double)w->V[3 * (int64_t)vid + d] + (vid == w->pvid && d == w->pfield ? w->pdelta : 0.0);
+    double xc[3];
+    for (int r = 0; r < 3; ++r)
+        xc[r] = (double)c->R[3 * r] * X[0] + (double)c->R[3 * r + 1] * X[1] + (double)c->R[3 * r + 2] * X[2] +
+                (double)c->t[r];
+    if (!(xc[2] > (double)c->near_plane)) return 0;
+    *u = (double)c->fx * xc[0] / xc[2] + (double)c->cx;
+    *v = (double)c->fy * xc[1] / xc[2] + (double)c->cy;
+    return 1;
+}
+
+static double aa_edge(int f32, double ua, double va, double ub, double vb, double px, double py)
+{
+    if (f32) return edge_f32((float)ua, (float)va, (float)ub, (float)vb, (float)px, (float)py);
+    return edge_f64(ua, va, ub, vb, px, py);
+}
+
+/* faces the walk below may cross before it gives up */
+#define AA_WALK 8
+
+/* One pair of neighbouring pixels p and q (Mesh rasterizer, item 3): where
+ * they see different faces, the nearer of the two surfaces (smaller mesh
+ * depth; none when equal) is the occluder o, whose face A covers o's centre.
+ * The segment from o's centre to the other centre is followed through the
+ * surface: it leaves the current face through the edge with the smallest
+ * crossing t_k = e_k(o) / (e_k(o) - e_k(other)) among those its far end lies
+ * outside of (ties: smaller k; the edge it entered by is skipped); across an
+ * internal edge -- one other face shares it and lies on the other side of
+ * the edge in the image -- it goes on into that face (at most AA_WALK faces);
+ * at a silhouette edge -- no other face, more than one, or one folded onto
+ * the same side -- it stops, and the crossing t in [0, 1] gives the weight
+ * w = |t - 0.5| on one pixel: the other one when t >= 0.5 (the surface
+ * reaches into it), o when t < 0.5 (it leaves part of o).  A pair along x
+ * only takes a silhouette edge more vertical than horizontal in the image
+ * (|dv| > |du|), a pair along y only the others (the per-axis 1D model counts
+ * each edge along one axis).  Decisions are taken in fp32 (f32 = 1) or
+ * double; the returned t is evaluated in double.  Returns 0 (nothing), else
+ * 1 with *occ = o's pixel, *t and a code naming the silhouette edge and the
+ * side.                                                                   */
+static int aa_pair(const aa_view* w, int f32, int64_t pp, int64_t pq, int64_t* occ, double* t_out, int* code)
+{
+    const orc_camera* c = w->c;
+    int fp = w->face_id[pp], fq = w->face_id[pq];
+    if (fp == fq) return 0;
+    double Dp = fp >= 0 ? aa_depth(w, pp) : INFINITY, Dq = fq >= 0 ? aa_depth(w, pq) : INFINITY;
+    if (f32) {
+        Dp = (float)Dp;
+        Dq = (float)Dq;
+    }
+    int64_t o, nb;
+    if (Dp < Dq) { o = pp; nb = pq; }
+    else if (Dq < Dp) { o = pq; nb = pp; }
+    else return 0;
+    double ox = (double)(o % c->width) + 0.5, oy = (double)(o / c->width) + 0.5;
+    double nx = (double)(nb % c->width) + 0.5, ny = (double)(nb / c->width) + 0.5;
+    int X = w->face_id[o], entry = -1, exit_k = -1;
+    double u[3], v[3], best = INFINITY;
+    for (int step = 0;; ++step) {
+        if (step == AA_WALK) return 0;
+        for (int k = 0; k < 3; ++k)
+            if (!aa_vertex(w, f32, w->F[3 * X + k], &u[k], &v[k])) return 0;
+        double area = aa_edge(f32, u[0], v[0], u[1], v[1], u[2], v[2]);
+        double sgn = area > 0.0 ? 1.0 : -1.0;
+        exit_k = -1;
+        best = INFINITY;
+        for (int k = 0; k < 3; ++k) {
+            if (k == entry) continue;
+            int a = (k + 1) % 3, b = (k + 2) % 3;
+            double eo = aa_edge(f32, u[a], v[a], u[b], v[b], ox, oy);
+            double en = aa_edge(f32, u[a], v[a], u[b], v[b], nx, ny);
+            if (step == 0 && sgn * eo < 0.0) return 0; /* A no longer covers o's centre */
+            if (!(sgn * en < 0.0)) continue;
+            if (sgn * eo < 0.0) return 0; /* the segment misses this face */
+            double tk = f32 ? (double)((float)eo / ((float)eo - (float)en)) : eo / (eo - en);
+            if (tk < best) {
+                best = tk;
+                exit_k = k;
+            }
+        }
+        if (exit_k < 0) return 0; /* the other centre lies on the surface */
+        int a = (exit_k + 1) % 3, b = (exit_k + 2) % 3;
+        int nf = w->adj[3 * X + exit_k];
+        if (nf < 0) break;
+        int va_ = w->F[3 * X + a], vb_ = w->F[3 * X + b], third = -1, back = -1;
+        for (int k = 0; k < 3; ++k) {
+            int vk = w->F[3 * nf + k];
+            if (vk != va_ && vk != vb_) { third = vk; back = k; }
+        }
+        double u3, v3;
+        if (third < 0 || !aa_vertex(w, f32, third, &u3, &v3)) break;
+        double sX = aa_edge(f32, u[a], v[a], u[b], v[b], u[exit_k], v[exit_k]);
+        double sN = aa_edge(f32, u[a], v[a], u[b], v[b], u3, v3);
+        if (!(sX * sN < 0.0)) break; /* folded onto the same side: a silhouette */
+        X = nf;                       /* the surface goes on across the edge */
+        entry = back;
+    }
+    int a = (exit_k + 1) % 3, b = (exit_k + 2) % 3;
+    {
+        double du = f32 ? (double)((float)u[b] - (float)u[a]) : u[b] - u[a];
+        double dv = f32 ? (double)((float)v[b] - (float)v[a]) : v[b] - v[a];
+        int along_x = (o / c->width) == (nb / c->width);
+        if (along_x != (fabs(dv) > fabs(du))) return 0;
+    }
+    /* the crossing in double */
+    double ud[3], vd[3];
+    for (int k = 0; k < 3; ++k)
+        if (!aa_vertex(w, 0, w->F[3 * X + k], &ud[k], &vd[k])) return 0;
+    double eo = edge_f64(ud[a], vd[a], ud[b], vd[b], ox, oy);
+    double en = edge_f64(ud[a], vd[a], ud[b], vd[b], nx, ny);
+    double t = eo / (eo - en);
+    t = t < 0.0 ? 0.0 : (t > 1.0 ? 1.0 : t);
+    *occ = o;
+    *t_out = t;
+    *code = 2 * (3 * X + exit_k + 1) + (best >= 0.5 ? 1 : 0);
+    return 1;
+}
+
+/* The antialiased mesh layer of pixel (i, j): coverage a, premultiplied colour
+ * M and the depth D the Gaussians are split at.  Without antialiasing the
+ * layer is a0 = covered, M0 = a0 c, D.  Each of the pixel's four pairs whose
+ * weight falls on it moves the layer towards the other pixel's by w (colours
+ * and coverage of both as they were before any pair):
+ *   onto the occluder o:   (a, M) += w ((a0, M0)(other) - (1, c_o)),
+ *   onto the other pixel:  (a, M) += w ((1, c_o) - (a0, M0)(other)),
+ * and a pixel the mesh does not cover takes the depth of the nearest
+ * occluder that reaches into it (w > 0).  a is clamped to [0, 1] (two pairs
+ * can act on one pixel near corners).  codes (optional) get each pair's
+ * decision code (left, right, up, down), 0 when it does nothing here.     */
+static void aa_pixel(const aa_view* w, int f32, int i, int j, double* a_out, double M[3], double* D_out,
+                     int codes[4])
+{
+    const orc_camera* c = w->c;
+    int64_t pp = (int64_t)j * c->width + i;
+    int cov = w->face_id[pp] >= 0;
+    double cp[3];
+    aa_rgb(w, pp, cp);
+    double a = cov ? 1.0 : 0.0;
+    for (int ch = 0; ch < 3; ++ch) M[ch] = cov ? cp[ch] : 0.0;
+    double Dp = cov ? aa_depth(w, pp) : INFINITY, Dnear = INFINITY;
+    const int di[4] = {-1, 1, 0, 0}, dj[4] = {0, 0, -1, 1};
+    for (int s = 0; s < 4; ++s) {
+        if (codes) codes[s] = 0;
+        int qi = i + di[s], qj = j + dj[s];
+        if (qi < 0 || qj < 0 || qi >= c->width || qj >= c->height) continue;
+        int64_t pq = (int64_t)qj * c->width + qi, o;
+        double t;
+        int code;
+        if (!aa_pair(w, f32, pp, pq, &o, &t, &code)) continue;
+        int onto_other = (code & 1) != 0;
+        int onto_me = onto_other ? o != pp : o == pp;
+        if (!onto_me) continue;
+        if (codes) codes[s] = code;
+        double wgt = fabs(t - 0.5);
+        int64_t other = o == pp ? pq : pp;
+        int cov_o = 1, cov_n = w->face_id[other] >= 0;
+        double co[3], cn[3];
+        aa_rgb(w, o, co);
+        aa_rgb(w, other, cn);
+        if (o == pp) { /* A leaves part of this pixel: towards the other pixel's layer */
+            a += wgt * ((cov_n ? 1.0 : 0.0) - 1.0);
+            for (int ch = 0; ch < 3; ++ch) M[ch] += wgt * ((cov_n ? cn[ch] : 0.0) - co[ch]);
+        } else { /* A reaches into this pixel */
+            a += wgt * (1.0 - (cov ? 1.0 : 0.0));
+            for (int ch = 0; ch < 3; ++ch) M[ch] += wgt * (co[ch] - (cov ? cp[ch] : 0.0));
+            if (!cov && wgt > 0.0) Dnear = fmin(Dnear, aa_depth(w, o));
+        }
+        (void)cov_o;
+    }
+    *a_out = a < 0.0 ? 0.0 : (a > 1.0 ? 1.0 : a);
+    *D_out = cov ? Dp : Dnear;
+}
+
+/* Antialiased mesh layer for the listed pixels (all when NULL): cov [H*W],
+ * premultiplied colour rgb_aa [H*W*3], split depth depth_aa [H*W], written at
+ * the listed pixels.  face_id / mesh_depth / mesh_rgb are full-frame images
+ * (the pixels' 4-neighbours are read).                                    */
+void orc_antialias(const orc_camera* c, const float* V, const int32_t* F, const int32_t* adj,
+                   const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
+                   const int32_t* pixels, int64_t n_pixels, float* cov, float* rgb_aa, float* depth_aa,
+                   int32_t* codes)
+{
+    aa_view w = {c, V, F, adj, face_id, mesh_depth, mesh_rgb, -1, 0, 0.0, NULL, NULL, NULL, 0};
+    int64_t np = pixels ? n_pixels : (int64_t)c->width * c->height;
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < np; ++k) {
+        int64_t pix = pixels ? pixels[k] : k;
+        int i = (int)(pix % c->width), j = (int)(pix / c->width);
+        double a, M[3], D;
+        int cd[4];
+        aa_pixel(&w, 1, i, j, &a, M, &D, cd);
+        cov[pix] = (float)a;
+        for (int ch = 0; ch < 3; ++ch) rgb_aa[3 * pix + ch] = (float)M[ch];
+        depth_aa[pix] = (float)D;
+        if (codes)
+            for (int s = 0; s < 4; ++s) codes[4 * pix + s] = cd[s];
+    }
+}
+
+/* tile_full / tile_far over an antialiased layer: full = every in-image pixel
+ * fully covered (a = 1), far = the largest split depth over the tile.     */
+void orc_tile_bounds_cov(const orc_camera* c, const float* cov, const float* depth, float* tile_far,
+                         uint8_t* tile_full)
+{
+    int TW = n_tiles_x(c), TH = n_tiles_y(c);
+    for (int ty = 0; ty < TH; ++ty)
+        for (int tx = 0; tx < TW; ++tx) {
+            float far = -INFINITY;
+            int full = 1;
+            for (int j = ty * TILE; j < ty * TILE + TILE && j < c->height; ++j)
+                for (int i = tx * TILE; i < tx * TILE + TILE && i < c->width; ++i) {
+                    int64_t p = (int64_t)j * c->width + i;
+                    if (!(cov[p] >= 1.0f)) full = 0;
+                    if (depth[p] > far) far = depth[p];
+                }
+            tile_far[ty * TW + tx] = full ? far : INFINITY;
+            tile_full[ty * TW + tx] = (uint8_t)full;
+        }
+}
+
+/* ========================================================================
  * EWA projection and SH colour of the Gaussians
  * ====================================================================== */
 
@@ -772,51 +1093,92 @@ static inline double sfield(const float* splats, int g, int f, const pert_t* p)
     return v;
 }
 
-/* One pixel, front to back over its tile's sorted list.  Each Gaussian i:
- *   drawn only where its centre depth is in front of the mesh (z_i < D);
+/* One pixel, front to back over its tile's sorted list, onto a mesh layer of
+ * coverage a, premultiplied colour M (= a c_mesh) and depth D (+inf where no
+ * mesh reaches the pixel).  Each Gaussian i:
  *   d = p - mu_i,  sigma = 1/2 (a dx^2 + c dy^2) + b dx dy  (skip sigma < 0);
- *   alpha = min(0.99, o_i exp(-sigma))  (skip alpha < 1/255);
- *   T' = T (1 - alpha); stop before i when T' <= 1e-4;
- *   C += alpha T c_i;  Z += alpha T z_i;  T = T'.
- * Soft split (sm != NULL) at a covered pixel: no hard depth test; the
- * Gaussian's front part f = Phi((D - z*(p)) / (sigma_z softness)) (or its
- * logistic approximation, split_front), z*(p) = z_i + g . d, replaces
- * alpha by alpha f in the skip, the stop and
- * the sums (the back parts lie behind the opaque mesh and are not seen).
- * Terminal layer (the opaque mesh, coverage 0 or 1):
- *   rgb = C + T (covered ? c_mesh : bg);  depth = Z + T covered D;
- *   alpha = 1 - T (1 - covered).
- * trace[k] (optional) records the decision taken on list entry k.        */
+ *   alpha = min(0.99, o_i exp(-sigma));
+ * and is split at the mesh (Hybrid rendering) into a front part, composited
+ * over the layer, and a back part, composited behind it:
+ *   hard split: front = alpha if z_i < D (else 0), back = alpha - front;
+ *   soft split (sm != NULL, D finite): front = alpha f, back = alpha (1 - f),
+ *     f = Phi((D - z*(p)) / (sigma_z softness)) or its logistic
+ *     approximation (split_front), z*(p) = z_i + g . d.
+ * Each of the two chains (front; back) composites its parts on its own:
+ *   skip a part below 1/255; stop the chain before a part that would bring
+ *   its T to 1e-4 or below; C += part T c_i, Z += part T z_i, T *= 1 - part.
+ * With the back chain (C_b, Z_b, T_b), the page's two-layer equation:
+ *   rgb = C + T (M + (1 - a)(C_b + T_b bg));  depth = Z + T (a D + (1 - a) Z_b);
+ *   alpha = 1 - T (1 - a) T_b.
+ * The back chain is evaluated only where it is seen (a < 1 and D finite):
+ * with a in {0, 1} (no antialiasing) it never is, and the pixel reduces to
+ * the one-layer form rgb = C + T (covered ? c_mesh : bg).
+ * trace[k] (optional) records the decision taken on list entry k: the front
+ * chain's code in bits 0-2, the back chain's in bits 3-5.               */
 #define SET_CODE(c)                      \
     do {                                 \
         if (trace) trace[k] = (c);       \
         if (g == watch) o->self_code = (c); \
     } while (0)
 
+typedef struct {
+    double T, C[3], Z;
+    int on;
+} chain_t;
+
+/* one part (alpha already split) into one chain; returns the trace code */
+static int chain_add(chain_t* ch, int f32, double part, double amin, double tstop, int clamped,
+                     const float* splats, int g, const pert_t* p, pix_t* o, int watch, double ma)
+{
+    o->m_alpha = fmin(o->m_alpha, ma);
+    if (g == watch) o->m_self = fmin(o->m_self, ma);
+    if (part < amin) return TR_ALPHA;
+    double Tn = rnd(ch->T * rnd(1.0 - part, f32), f32);
+    double mt = fabs(Tn - tstop) / tstop;
+    o->m_stop = fmin(o->m_stop, mt);
+    if (g == watch) o->m_self = fmin(o->m_self, mt);
+    if (Tn <= tstop) {
+        ch->on = 0;
+        return TR_STOP;
+    }
+    double w = rnd(part * ch->T, f32);
+    for (int c = 0; c < 3; ++c) ch->C[c] += w * sfield(splats, g, S_R + c, p);
+    ch->Z += w * sfield(splats, g, S_Z, p);
+    ch->T = Tn;
+    return clamped ? TR_BLEND_CLAMPED : TR_BLEND;
+}
+
 static void composite_pixel(int f32, double px, double py, const int32_t* list, int64_t n,
-                            const float* splats, const soft_t* sm, double D, int covered, const double cm[3],
+                            const float* splats, const soft_t* sm, double D, double acov, const double M[3],
                             const double bg[3], const pert_t* p, pix_t* o, uint8_t* trace,
                             int64_t* trace_len, int watch)
 {
-    double T = 1.0, C[3] = {0, 0, 0}, Z = 0.0;
+    chain_t fr = {1.0, {0, 0, 0}, 0.0, 1}, bk = {1.0, {0, 0, 0}, 0.0, 0};
     int32_t last = 0;
     const double amax = rnd(ALPHA_MAX, f32), amin = rnd(ALPHA_MIN, f32), tstop = rnd(T_STOP, f32);
+    const int has_mesh = D < INFINITY;
+    const int soft = sm && has_mesh;
+    bk.on = has_mesh && acov < 1.0;
     o->m_depth = o->m_alpha = o->m_clamp = o->m_stop = o->m_sigma = INFINITY;
     o->self_code = 0;
     o->m_self = INFINITY;
     int64_t k;
-    for (k = 0; k < n; ++k) {
+    for (k = 0; k < n && (fr.on || bk.on); ++k) {
         int g = list[k];
         double z = sfield(splats, g, S_Z, p);
-        const int soft = sm && covered;
+        int code_f = 0, code_b = 0;
+        int in_front = 1, in_back = 0; /* hard split: which chain takes the Gaussian */
         if (!soft) {
-            if (D < INFINITY) {
+            if (has_mesh) {
                 double m = fabs(z - D) / D;
                 o->m_depth = fmin(o->m_depth, m);
                 if (g == watch) o->m_self = fmin(o->m_self, m);
             }
-            if (!(z < D)) {
-                SET_CODE(TR_DEPTH);
+            in_front = z < D;
+            in_back = !in_front;
+            if ((in_front && !fr.on) || (in_back && !bk.on)) {
+                if (in_back) SET_CODE(TR_DEPTH);
+                else SET_CODE(0);
                 continue;
             }
         }
@@ -831,73 +1193,77 @@ static void composite_pixel(int f32, double px, double py, const int32_t* list, 
         double sigma = rnd(half + cross, f32);
         double ms = fabs(sigma) / (fabs(half) + fabs(cross) + 1e-30);
         o->m_sigma = fmin(o->m_sigma, ms);
+        if (g == watch) o->m_self = fmin(o->m_self, ms);
         if (sigma < 0.0) {
-            SET_CODE(TR_SIGMA);
+            SET_CODE(TR_SIGMA | (bk.on && (soft || in_back) ? TR_SIGMA << 3 : 0));
             continue;
         }
         double G = rnd(exp(-sigma), f32);
         double oG = rnd(sfield(splats, g, S_OP, p) * G, f32);
         double mc = fabs(oG - amax) / amax;
         o->m_clamp = fmin(o->m_clamp, mc);
+        if (g == watch) o->m_self = fmin(o->m_self, mc);
         int clamped = oG > amax;
         double alpha = clamped ? amax : oG;
-        double a_lo = -1.0, a_hi = -1.0; /* the split's alpha f at x -+ its rounding bound */
+        double pf = alpha, pb = alpha;             /* the front and back parts */
+        double mf = fabs(alpha - amin) / amin, mb = mf; /* their skip margins */
         if (soft) {
             double zs = rnd(z + rnd(rnd(dmfield(sm, g, 0, p) * dx, f32) + rnd(dmfield(sm, g, 1, p) * dy, f32), f32),
                             f32);
             double band = rnd(dmfield(sm, g, 2, p) * sm->softness, f32);
             double xa = rnd(rnd(D - zs, f32) / band, f32);
             double f = rnd(split_front(xa, sm->logistic), f32);
+            pf = rnd(alpha * f, f32);
+            pb = rnd(alpha * rnd(1.0 - f, f32), f32);
             /* an fp32 evaluation of x = (D - z*) / band in another order lands within
-             * about 4 eps ((|D| + |z*|) / band + |x|) of this one */
+             * about 4 eps ((|D| + |z*|) / band + |x|) of this one: the skip margin of
+             * each part is that of its whole interval (negative: either side possible) */
             double ex = 4.0 * FLT_EPSILON * ((fabs(D) + fabs(zs)) / band + fabs(xa));
-            a_lo = alpha * split_front(xa - ex, sm->logistic);
-            a_hi = alpha * split_front(xa + ex, sm->logistic);
-            alpha = rnd(alpha * f, f32);
+            double flo = split_front(xa - ex, sm->logistic), fhi = split_front(xa + ex, sm->logistic);
+            double lo = alpha * flo, hi = alpha * fhi;
+            mf = hi < amin ? (amin - hi) / amin : (lo >= amin ? (lo - amin) / amin : -1.0);
+            lo = alpha * (1.0 - fhi);
+            hi = alpha * (1.0 - flo);
+            mb = hi < amin ? (amin - hi) / amin : (lo >= amin ? (lo - amin) / amin : -1.0);
         }
-        /* relative distance of the skip operand to 1/255; under the split, of the
-         * whole range that the rounding of x allows (negative: either side is possible) */
-        double ma = fabs(alpha - amin) / amin;
-        if (soft) ma = a_hi < amin ? (amin - a_hi) / amin : (a_lo >= amin ? (a_lo - amin) / amin : -1.0);
-        o->m_alpha = fmin(o->m_alpha, ma);
-        if (g == watch) o->m_self = fmin(o->m_self, fmin(ms, fmin(mc, ma)));
-        if (alpha < amin) {
-            SET_CODE(TR_ALPHA);
-            continue;
+        if (fr.on && in_front) {
+            code_f = chain_add(&fr, f32, pf, amin, tstop, clamped, splats, g, p, o, watch, mf);
+            if (code_f == TR_BLEND || code_f == TR_BLEND_CLAMPED) last = (int32_t)(k + 1);
         }
-        double Tn = rnd(T * rnd(1.0 - alpha, f32), f32);
-        double mt = fabs(Tn - tstop) / tstop;
-        o->m_stop = fmin(o->m_stop, mt);
-        if (g == watch) o->m_self = fmin(o->m_self, mt);
-        if (Tn <= tstop) {
-            SET_CODE(TR_STOP);
-            k++;
-            break;
-        }
-        double w = rnd(alpha * T, f32);
-        for (int ch = 0; ch < 3; ++ch) C[ch] += w * sfield(splats, g, S_R + ch, p);
-        Z += w * z;
-        T = Tn;
-        last = (int32_t)(k + 1);
-        SET_CODE(clamped ? TR_BLEND_CLAMPED : TR_BLEND);
+        if (bk.on && (soft || in_back))
+            code_b = chain_add(&bk, f32, pb, amin, tstop, clamped, splats, g, p, o, watch, mb);
+        if (trace) trace[k] = (uint8_t)(code_f | (code_b << 3));
+        if (g == watch) o->self_code = code_f ? code_f : code_b;
     }
     if (trace_len) *trace_len = k;
-    for (int ch = 0; ch < 3; ++ch) o->rgb[ch] = C[ch] + T * (covered ? cm[ch] : bg[ch]);
-    o->depth = Z + (covered ? T * D : 0.0);
-    o->alpha = 1.0 - T * (covered ? 0.0 : 1.0);
-    o->T = T;
+    const double ua = 1.0 - acov;
+    for (int ch = 0; ch < 3; ++ch) {
+        double behind = ua > 0.0 ? ua * (bk.C[ch] + bk.T * bg[ch]) : 0.0;
+        o->rgb[ch] = fr.C[ch] + fr.T * (M[ch] + behind);
+    }
+    o->depth = fr.Z + fr.T * ((acov > 0.0 ? acov * D : 0.0) + (ua > 0.0 ? ua * bk.Z : 0.0));
+    o->alpha = 1.0 - fr.T * ua * bk.T;
+    o->T = fr.T;
     o->n_contrib = last;
 }
 
-/* Forward composite of the listed tiles (all when tiles == NULL) with the
- * full lists of orc_tile_lists (tile_start over all T tiles).  Outputs are
- * full-frame arrays; only pixels of the listed tiles are written.  margins
- * (optional, [H*W*5]) get the per-pixel decision margins (depth, alpha skip,
- * clamp, stop, sigma) of the fp32 evaluation.                              */
+/* the mesh layer of one pixel: the antialiased one (coverage image given,
+ * colour premultiplied) or the binary one of the z-buffer */
+static double mesh_layer(const float* mesh_cov, const float* mesh_rgb, const int32_t* face_id, int64_t pix,
+                         double M[3])
+{
+    double a = mesh_cov ? (double)mesh_cov[pix] : (face_id[pix] >= 0 ? 1.0 : 0.0);
+    for (int ch = 0; ch < 3; ++ch) M[ch] = mesh_cov || a > 0.0 ? (double)mesh_rgb[3 * pix + ch] : 0.0;
+    return a;
+}
+
+/* Full-frame compositing (tiles listed, or all).  The mesh layer is
+ * (mesh_cov, mesh_rgb premultiplied, mesh_depth) when mesh_cov is given (the
+ * antialiased layer), else coverage face_id >= 0 with colour mesh_rgb.     */
 void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats,
                        const int64_t* tile_start, const int32_t* entries,
                        const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
-                       const int32_t* tiles, int32_t n_tiles_req,
+                       const float* mesh_cov, const int32_t* tiles, int32_t n_tiles_req,
                        float* out_rgb, float* out_depth, float* out_alpha, float* T_final,
                        int32_t* n_contrib, double* margins, const float* depth_model, double softness, int32_t split)
 {
@@ -915,10 +1281,10 @@ void orc_composite_fwd(const orc_camera* c, const float* bg, const float* splats
         for (int j = ty * TILE; j < ty * TILE + TILE && j < c->height; ++j)
             for (int i = tx * TILE; i < tx * TILE + TILE && i < c->width; ++i) {
                 int64_t pix = (int64_t)j * c->width + i;
-                int cov = face_id[pix] >= 0;
-                double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
+                double M[3];
+                double a = mesh_layer(mesh_cov, mesh_rgb, face_id, pix, M);
                 pix_t o;
-                composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, (double)mesh_depth[pix], cov, cm,
+                composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, (double)mesh_depth[pix], a, M,
                                 bgd, NULL, &o, NULL, NULL, -1);
                 for (int ch = 0; ch < 3; ++ch) out_rgb[3 * pix + ch] = (float)o.rgb[ch];
                 out_depth[pix] = (float)o.depth;
@@ -983,7 +1349,7 @@ static int tie_pixel(const pix_t* o, double band)
 void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats, const int32_t* radii,
                       const int64_t* tile_start, const int32_t* entries,
                       const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id,
-                      const float* g_rgb, const float* g_depth, const float* g_alpha,
+                      const float* mesh_cov, const float* g_rgb, const float* g_depth, const float* g_alpha,
                       int32_t n_req, const int32_t* req_gid, const int32_t* req_field,
                       const double* req_h, double tie_band, double* grad, int32_t* status,
                       const float* depth_model, double softness, int32_t split)
@@ -1031,9 +1397,9 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
                     for (int j = ty * TILE; j < ty * TILE + TILE && j < c->height && st == FD_OK; ++j)
                         for (int i = tx * TILE; i < tx * TILE + TILE && i < c->width; ++i) {
                             int64_t pix = (int64_t)j * c->width + i;
-                            int cov = face_id[pix] >= 0;
                             double D = mesh_depth[pix];
-                            double cm[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
+                            double cm[3];
+                            double cov = mesh_layer(mesh_cov, mesh_rgb, face_id, pix, cm);
                             pix_t o32, o0, op, om;
                             int64_t n32, n0, np_, nm;
                             composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, D, cov, cm, bgd, NULL, &o32, tr[0], &n32, g);
@@ -1068,13 +1434,22 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
 }
 
 /* dL/d(vertex position or colour) through the interpolated mesh depth and
- * colour (face ids held fixed).  req_field 0..2 = world x, y, z of the vertex,
- * 3..5 = its r, g, b.  Pixels whose face uses the vertex are re-evaluated:
- * depth and colour in double from the perturbed mesh, then the composite in
- * double with that depth.  The fp32 reference decisions use mesh_depth as
- * given.  Status codes as for orc_composite_fd.                           */
+ * colour (face ids held fixed) and, with antialiasing (adj given), through the
+ * silhouette crossings.  req_field 0..2 = world x, y, z of the vertex, 3..5 =
+ * its r, g, b.  Re-evaluated: the depth and colour (in double, from the moved
+ * mesh) of the pixels whose face uses the vertex, the antialiased layer of
+ * those pixels and their 4-neighbours, and the composite (double) of every
+ * such pixel.  The fp32 reference decisions use mesh_depth / mesh_rgb as
+ * given.  Status codes as for orc_composite_fd; the antialiasing decisions
+ * (occluder, exit edge, silhouette, side) count as decisions.             */
+static int cmp_i64(const void* a, const void* b)
+{
+    int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+    return (x > y) - (x < y);
+}
+
 void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t nV, const int32_t* F,
-                 int32_t nF, const float* vcol, const int32_t* face_id, const float* splats,
+                 int32_t nF, const float* vcol, const int32_t* face_id, const int32_t* adj, const float* splats,
                  const int64_t* tile_start, const int32_t* entries, const float* mesh_depth,
                  const float* mesh_rgb, const float* g_rgb, const float* g_depth, const float* g_alpha,
                  int32_t n_req, const int32_t* req_vid, const int32_t* req_field, const double* req_h,
@@ -1117,60 +1492,122 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
         for (int32_t q = 0; q < n_req; ++q) {
             int vid = req_vid[q], field = req_field[q];
             double h = req_h[q];
-            double lp = 0.0, lm = 0.0, lp2 = 0.0, lm2 = 0.0;
-            int st = FD_OK, any = 0;
-            for (int64_t fk = vstart[vid]; fk < vstart[vid + 1] && st == FD_OK; ++fk) {
-                int f = vface[fk];
-                for (int64_t pk = fstart[f]; pk < fstart[f + 1]; ++pk) {
-                    int64_t pix = fpix[pk];
-                    int i = (int)(pix % c->width), j = (int)(pix / c->width);
-                    int64_t tile = (int64_t)(j / TILE) * TW + i / TILE;
-                    const int32_t* list = entries + tile_start[tile];
-                    int64_t n = tile_start[tile + 1] - tile_start[tile];
-                    double Dv[5], cmv[5][3];
-                    for (int sgn = 0; sgn < 5; ++sgn) {
-                        double X[3][3], C3[3][3], D, w[3];
-                        load_tri(V, F, f, X);
-                        for (int k = 0; k < 3; ++k)
-                            for (int d = 0; d < 3; ++d) C3[k][d] = vcol[3 * (int64_t)F[3 * f + k] + d];
-                        const double steps[5] = {0.0, h, -h, 0.5 * h, -0.5 * h};
-                        double delta = steps[sgn];
-                        for (int k = 0; k < 3; ++k) {
-                            if (F[3 * f + k] != vid) continue;
-                            if (field < 3) X[k][field] += delta;
-                            else C3[k][field - 3] += delta;
-                        }
-                        tri64 t;
-                        tri_setup_f64(c, X, &t);
-                        interp_f64(&t, i + 0.5, j + 0.5, &D, w);
-                        Dv[sgn] = D;
-                        for (int ch = 0; ch < 3; ++ch)
-                            cmv[sgn][ch] = w[0] * C3[0][ch] + w[1] * C3[1][ch] + w[2] * C3[2][ch];
+            const double steps[5] = {0.0, h, -h, 0.5 * h, -0.5 * h};
+            /* P1: the pixels of the vertex's faces, sorted */
+            int64_t n1 = 0;
+            for (int64_t fk = vstart[vid]; fk < vstart[vid + 1]; ++fk)
+                n1 += fstart[vface[fk] + 1] - fstart[vface[fk]];
+            int64_t* p1 = (int64_t*)malloc(sizeof(int64_t) * (n1 > 0 ? n1 : 1));
+            n1 = 0;
+            for (int64_t fk = vstart[vid]; fk < vstart[vid + 1]; ++fk)
+                for (int64_t pk = fstart[vface[fk]]; pk < fstart[vface[fk] + 1]; ++pk) p1[n1++] = fpix[pk];
+            qsort(p1, (size_t)n1, sizeof(int64_t), cmp_i64);
+            int64_t u1 = 0; /* a face that names the vertex twice lists its pixels twice */
+            for (int64_t k = 0; k < n1; ++k)
+                if (k == 0 || p1[k] != p1[k - 1]) p1[u1++] = p1[k];
+            n1 = u1;
+            /* depth and colour of P1 at each step, in double */
+            double* ovd = (double*)malloc(sizeof(double) * 5 * (n1 > 0 ? n1 : 1));
+            double* ovc = (double*)malloc(sizeof(double) * 15 * (n1 > 0 ? n1 : 1));
+            for (int64_t k = 0; k < n1; ++k) {
+                int64_t pix = p1[k];
+                int f = face_id[pix];
+                int i = (int)(pix % c->width), j = (int)(pix / c->width);
+                for (int sgn = 0; sgn < 5; ++sgn) {
+                    double X[3][3], C3[3][3], D, w[3];
+                    load_tri(V, F, f, X);
+                    for (int kk = 0; kk < 3; ++kk)
+                        for (int d = 0; d < 3; ++d) C3[kk][d] = vcol[3 * (int64_t)F[3 * f + kk] + d];
+                    for (int kk = 0; kk < 3; ++kk) {
+                        if (F[3 * f + kk] != vid) continue;
+                        if (field < 3) X[kk][field] += steps[sgn];
+                        else C3[kk][field - 3] += steps[sgn];
                     }
-                    double cm32[3] = {mesh_rgb[3 * pix], mesh_rgb[3 * pix + 1], mesh_rgb[3 * pix + 2]};
-                    pix_t o32, o0, op, om;
-                    int64_t n32, n0, np_, nm;
-                    composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, mesh_depth[pix], 1, cm32, bgd, NULL, &o32, tr[0], &n32, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[0], 1, cmv[0], bgd, NULL, &o0, tr[1], &n0, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[1], 1, cmv[1], bgd, NULL, &op, tr[2], &np_, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[2], 1, cmv[2], bgd, NULL, &om, tr[3], &nm, -1);
-                    /* depth-test decisions: the PRECISION check below compares them
-                     * exactly; alpha / stop / sigma decisions within rounding: a tie */
-                    if (tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
-                    if (!same_trace(tr[0], n32, tr[1], n0)) { st = FD_PRECISION; break; }
-                    if (!same_trace(tr[1], n0, tr[2], np_) || !same_trace(tr[1], n0, tr[3], nm)) {
-                        st = FD_FLIP;
-                        break;
-                    }
-                    lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
-                    lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[3], 1, cmv[3], bgd, NULL, &op, NULL, NULL, -1);
-                    composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dv[4], 1, cmv[4], bgd, NULL, &om, NULL, NULL, -1);
-                    lp2 += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
-                    lm2 += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
-                    any = 1;
+                    tri64 t;
+                    tri_setup_f64(c, X, &t);
+                    interp_f64(&t, i + 0.5, j + 0.5, &D, w);
+                    ovd[sgn * n1 + k] = D;
+                    for (int ch = 0; ch < 3; ++ch)
+                        ovc[3 * (sgn * n1 + k) + ch] = w[0] * C3[0][ch] + w[1] * C3[1][ch] + w[2] * C3[2][ch];
                 }
             }
+            /* P2: P1 and, with antialiasing, its 4-neighbours */
+            int64_t n2 = adj ? 5 * n1 : n1;
+            int64_t* p2 = (int64_t*)malloc(sizeof(int64_t) * (n2 > 0 ? n2 : 1));
+            n2 = 0;
+            for (int64_t k = 0; k < n1; ++k) {
+                int64_t pix = p1[k];
+                p2[n2++] = pix;
+                if (!adj) continue;
+                int i = (int)(pix % c->width), j = (int)(pix / c->width);
+                if (i > 0) p2[n2++] = pix - 1;
+                if (i + 1 < c->width) p2[n2++] = pix + 1;
+                if (j > 0) p2[n2++] = pix - c->width;
+                if (j + 1 < c->height) p2[n2++] = pix + c->width;
+            }
+            qsort(p2, (size_t)n2, sizeof(int64_t), cmp_i64);
+            int64_t u2 = 0;
+            for (int64_t k = 0; k < n2; ++k)
+                if (k == 0 || p2[k] != p2[k - 1]) p2[u2++] = p2[k];
+            n2 = u2;
+            double lp = 0.0, lm = 0.0, lp2 = 0.0, lm2 = 0.0;
+            int st = FD_OK, any = n1 > 0;
+            for (int64_t k = 0; k < n2 && st == FD_OK; ++k) {
+                int64_t pix = p2[k];
+                int i = (int)(pix % c->width), j = (int)(pix / c->width);
+                int64_t tile = (int64_t)(j / TILE) * TW + i / TILE;
+                const int32_t* list = entries + tile_start[tile];
+                int64_t n = tile_start[tile + 1] - tile_start[tile];
+                /* the mesh layer: fp32 reference (as given) and at each step */
+                double a32, M32[3], D32, a[5], M[5][3], Dl[5];
+                int cd32[4] = {0, 0, 0, 0}, cd[5][4];
+                if (adj) {
+                    aa_view w32 = {c, V, F, adj, face_id, mesh_depth, mesh_rgb, -1, 0, 0.0, NULL, NULL, NULL, 0};
+                    aa_pixel(&w32, 1, i, j, &a32, M32, &D32, cd32);
+                    for (int sgn = 0; sgn < 5; ++sgn) {
+                        aa_view wd = {c, V, F, adj, face_id, mesh_depth, mesh_rgb, field < 3 ? vid : -1, field,
+                                      steps[sgn], p1, ovd + sgn * n1, ovc + 3 * sgn * n1, n1};
+                        aa_pixel(&wd, 0, i, j, &a[sgn], M[sgn], &Dl[sgn], cd[sgn]);
+                    }
+                } else {
+                    int64_t kk = k; /* P2 = P1 */
+                    a32 = 1.0;
+                    D32 = mesh_depth[pix];
+                    for (int ch = 0; ch < 3; ++ch) M32[ch] = mesh_rgb[3 * pix + ch];
+                    for (int sgn = 0; sgn < 5; ++sgn) {
+                        a[sgn] = 1.0;
+                        Dl[sgn] = ovd[sgn * n1 + kk];
+                        for (int ch = 0; ch < 3; ++ch) M[sgn][ch] = ovc[3 * (sgn * n1 + kk) + ch];
+                        for (int s4 = 0; s4 < 4; ++s4) cd[sgn][s4] = 0;
+                    }
+                }
+                if (memcmp(cd32, cd[0], sizeof(cd32)) != 0) { st = FD_PRECISION; break; }
+                if (memcmp(cd[0], cd[1], sizeof(cd32)) != 0 || memcmp(cd[0], cd[2], sizeof(cd32)) != 0) {
+                    st = FD_FLIP;
+                    break;
+                }
+                pix_t o32, o0, op, om;
+                int64_t n32, n0, np_, nm;
+                composite_pixel(1, i + 0.5, j + 0.5, list, n, splats, sm, D32, a32, M32, bgd, NULL, &o32, tr[0], &n32, -1);
+                composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dl[0], a[0], M[0], bgd, NULL, &o0, tr[1], &n0, -1);
+                composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dl[1], a[1], M[1], bgd, NULL, &op, tr[2], &np_, -1);
+                composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dl[2], a[2], M[2], bgd, NULL, &om, tr[3], &nm, -1);
+                /* depth-test decisions: the PRECISION check below compares them
+                 * exactly; alpha / stop / sigma decisions within rounding: a tie */
+                if (tie_pixel(&o32, tie_band)) { st = FD_TIE; break; }
+                if (!same_trace(tr[0], n32, tr[1], n0)) { st = FD_PRECISION; break; }
+                if (!same_trace(tr[1], n0, tr[2], np_) || !same_trace(tr[1], n0, tr[3], nm)) {
+                    st = FD_FLIP;
+                    break;
+                }
+                lp += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
+                lm += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
+                composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dl[3], a[3], M[3], bgd, NULL, &op, NULL, NULL, -1);
+                composite_pixel(0, i + 0.5, j + 0.5, list, n, splats, sm, Dl[4], a[4], M[4], bgd, NULL, &om, NULL, NULL, -1);
+                lp2 += pixel_loss(&op, g_rgb, g_depth, g_alpha, pix);
+                lm2 += pixel_loss(&om, g_rgb, g_depth, g_alpha, pix);
+            }
+            free(p1); free(p2); free(ovd); free(ovc);
             if (st == FD_OK && !any) st = FD_UNUSED;
             double gv = 0.0;
             if (st == FD_OK) st = richardson(lp, lm, lp2, lm2, h, &gv);
@@ -1183,16 +1620,17 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
 }
 
 /* Single-pixel composite, exported for closed-form checks of the routine
- * itself (list of Gaussian ids into splats, f32 = 1 for the fp32 mode).
+ * itself (list of Gaussian ids into splats, f32 = 1 for the fp32 mode) over
+ * a mesh layer of coverage cov, premultiplied colour M and depth D.
  * out: rgb[3], depth, alpha, T, n_contrib.                                */
 void orc_composite_one(int32_t f32, double px, double py, const int32_t* list, int64_t n,
-                       const float* splats, double D, int32_t covered, const double* cm,
+                       const float* splats, double D, double cov, const double* M,
                        const double* bg, double* out, const float* depth_model, double softness, int32_t split)
 {
     soft_t smv = {depth_model, softness, split != 0};
     const soft_t* sm = depth_model && softness > 0.0 ? &smv : NULL;
     pix_t o;
-    composite_pixel(f32, px, py, list, n, splats, sm, D, covered, cm, bg, NULL, &o, NULL, NULL, -1);
+    composite_pixel(f32, px, py, list, n, splats, sm, D, cov, M, bg, NULL, &o, NULL, NULL, -1);
     out[0] = o.rgb[0]; out[1] = o.rgb[1]; out[2] = o.rgb[2];
     out[3] = o.depth; out[4] = o.alpha; out[5] = o.T; out[6] = o.n_contrib;
 }
