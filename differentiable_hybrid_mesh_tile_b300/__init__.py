@@ -52,6 +52,11 @@ class gm_opts(C.Structure):
                 ("tile_test", C.c_int32), ("softness", C.c_float), ("soft_split", C.c_int32)]
 
 
+class gm_aa_layer(C.Structure):
+    _fields_ = [("cov", C.c_void_p), ("back", C.c_void_p), ("T_back", C.c_void_p), ("n_back", C.c_void_p),
+                ("v_cov", C.c_void_p), ("v_rgb", C.c_void_p)]
+
+
 _VP = C.c_void_p
 _I32 = C.c_int32
 _SIGS = {
@@ -66,8 +71,13 @@ _SIGS = {
     "gm_bin_sort_gaussians_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
     "gm_bin_sort_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
                                         C.c_size_t, _VP]),
-    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 14),
-    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16 + [_I32, _VP, _I32] + [_VP] * 5),
+    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 15),
+    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16 + [_I32, _VP, _I32] + [_VP] * 6),
+    "gm_mesh_edges_workspace_size": (C.c_size_t, [_I32]),
+    "gm_mesh_edges": (C.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, C.c_size_t, _VP]),
+    "gm_antialias": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 10),
+    "gm_antialias_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 11),
+    "gm_interp_mesh_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 7),
     "gm_bin_triangles_noalloc": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP]),
     "gm_last_error": (C.c_char_p, []),
 }
@@ -262,19 +272,64 @@ def gm_bin_sort_gaussians(cam: gm_camera, opts: gm_opts, splats, radii, tile_far
     return k.value if sync else None
 
 
+def _aa_ref(aa):
+    return None if aa is None else C.byref(aa)
+
+
+def make_aa_layer(cov, back, T_back, n_back, v_cov=None, v_rgb=None) -> gm_aa_layer:
+    """gm_aa_layer over torch CUDA tensors (the antialiased layer's coverage and
+    the back-chain buffers; v_cov / v_rgb for the backward)."""
+    a = gm_aa_layer()
+    a.cov, a.back, a.T_back, a.n_back = _p(cov, F32), _p(back, F32), _p(T_back, F32), _p(n_back, I32)
+    a.v_cov, a.v_rgb = _p(v_cov, F32), _p(v_rgb, F32)
+    return a
+
+
+def gm_mesh_edges_workspace_size(nF: int) -> int:
+    return int(lib().gm_mesh_edges_workspace_size(nF))
+
+
+def gm_mesh_edges(F, nV, adj, counters, ws):
+    _check(lib().gm_mesh_edges(_p(F, I32), F.shape[0], int(nV), _p(adj, I32), _p(counters, I32), _p(ws),
+                               ws.numel() * ws.element_size(), _stream()), "gm_mesh_edges")
+
+
+def gm_antialias(cam: gm_camera, V, F, adj, face_id, mesh_depth, mesh_rgb, cov, rgb_aa, depth_aa, tile_far,
+                 tile_full):
+    _check(lib().gm_antialias(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(adj, I32),
+                              _p(face_id, I32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(cov, F32), _p(rgb_aa, F32),
+                              _p(depth_aa, F32), _p(tile_far, F32), _p(tile_full, U8), _stream()), "gm_antialias")
+
+
+def gm_antialias_bwd(cam: gm_camera, V, F, adj, face_id, mesh_depth, mesh_rgb, v_cov, v_rgb_aa, v_depth_aa,
+                     v_mesh_rgb, v_mesh_depth, v_verts):
+    _check(lib().gm_antialias_bwd(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(adj, I32),
+                                  _p(face_id, I32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(v_cov, F32),
+                                  _p(v_rgb_aa, F32), _p(v_depth_aa, F32), _p(v_mesh_rgb, F32), _p(v_mesh_depth, F32),
+                                  _p(v_verts, F32), _stream()), "gm_antialias_bwd")
+
+
+def gm_interp_mesh_bwd(cam: gm_camera, V, F, vcol, face_id, v_mesh_rgb, v_mesh_depth, v_verts, v_vcol):
+    _check(lib().gm_interp_mesh_bwd(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(vcol, F32),
+                                    _p(face_id, I32), _p(v_mesh_rgb, F32), _p(v_mesh_depth, F32), _p(v_verts, F32),
+                                    _p(v_vcol, F32), _stream()), "gm_interp_mesh_bwd")
+
+
 def gm_composite_hybrid_fwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
-                            out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None, depth_model=None):
+                            out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None, depth_model=None,
+                            aa=None):
     _check(lib().gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
                                          _p(gids, I32), _p(splats, F32), _p(depth_model, F32),
                                          _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
                                          _p(out_rgb, F32), _p(out_depth, F32), _p(out_alpha, F32), _p(T_final, F32),
-                                         _p(n_contrib, I32), _p(stats, I64), _stream()), "gm_composite_hybrid_fwd")
+                                         _p(n_contrib, I32), _aa_ref(aa), _p(stats, I64), _stream()),
+           "gm_composite_hybrid_fwd")
 
 
 def gm_composite_hybrid_bwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
                             T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, V=None, F=None, vcol=None,
                             v_verts=None, v_vcol=None, stats=None, depth_model=None, v_depth_model=None,
-                            v_mesh_depth=None):
+                            v_mesh_depth=None, aa=None):
     nV = 0 if V is None else V.shape[0]
     nF = 0 if F is None else F.shape[0]
     _check(lib().gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
@@ -283,7 +338,8 @@ def gm_composite_hybrid_bwd(cam: gm_camera, opts: gm_opts, tile_range, gids, spl
                                          _p(T_final, F32), _p(n_contrib, I32), _p(g_rgb, F32), _p(g_depth, F32),
                                          _p(g_alpha, F32), _p(v_splats, F32), _p(v_depth_model, F32),
                                          _p(v_mesh_depth, F32), _p(V, F32), nV, _p(F, I32), nF,
-                                         _p(vcol, F32), _p(v_verts, F32), _p(v_vcol, F32), _p(stats, I64), _stream()),
+                                         _p(vcol, F32), _p(v_verts, F32), _p(v_vcol, F32), _aa_ref(aa), _p(stats, I64),
+                                         _stream()),
            "gm_composite_hybrid_bwd")
 
 
@@ -306,6 +362,13 @@ class HybridRenderer:
     backward (joined back into the caller's stream before anything reads
     their results; a captured graph keeps the two branches).
 
+    ``antialias=True`` adds the analytic edge antialiasing of the mesh layer
+    (``gm_antialias``; edge adjacency from ``gm_mesh_edges`` at upload): the
+    Gaussians composite over a layer of fractional coverage at silhouettes and
+    the backward pass adds the silhouette vertex gradients
+    (``gm_antialias_bwd``, then ``gm_interp_mesh_bwd``), all on the caller's
+    stream.
+
     ``softness > 0`` selects the soft split at the mesh surface (front
     fraction ``soft_split``: GM_SPLIT_PHI or GM_SPLIT_LOGISTIC): the
     projection also writes each Gaussian's depth model (``depth_model``), the
@@ -315,7 +378,7 @@ class HybridRenderer:
     """
 
     def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
-                 concurrent=True, tile_test=True, softness=0.0, soft_split=GM_SPLIT_PHI):
+                 concurrent=True, tile_test=True, softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False):
         self.cam_desc = cam
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
@@ -332,6 +395,7 @@ class HybridRenderer:
             raise ValueError("softness must be >= 0")
         self.soft = self.softness > 0.0
         self.soft_split = int(soft_split)
+        self.antialias = bool(antialias)
         self._side = None
         self.tri_cap = 0
         self.g_cap = 0
@@ -352,8 +416,22 @@ class HybridRenderer:
         self.out_alpha = torch.empty(H, W, dtype=F32, device=d)
         self.T_final = torch.empty(H, W, dtype=F32, device=d)
         self.n_contrib = torch.empty(H, W, dtype=I32, device=d)
-        self.v_mesh_depth = torch.zeros(H, W, dtype=F32, device=d) if self.soft else None
+        self.v_mesh_depth = torch.zeros(H, W, dtype=F32, device=d) if self.soft or self.antialias else None
         self.depth_model = self.v_depth_model = None
+        if self.antialias:
+            self.cov = torch.zeros(H, W, dtype=F32, device=d)
+            self.rgb_aa = torch.zeros(H, W, 3, dtype=F32, device=d)
+            self.depth_aa = torch.zeros(H, W, dtype=F32, device=d)
+            self.back = torch.zeros(H, W, 4, dtype=F32, device=d)
+            self.T_back = torch.zeros(H, W, dtype=F32, device=d)
+            self.n_back = torch.zeros(H, W, dtype=I32, device=d)
+            self.v_cov = torch.zeros(H, W, dtype=F32, device=d)
+            self.v_rgb_aa = torch.zeros(H, W, 3, dtype=F32, device=d)
+            self.v_mesh_rgb = torch.zeros(H, W, 3, dtype=F32, device=d)
+            self.v_interp_depth = torch.zeros(H, W, dtype=F32, device=d)
+            self.aa = make_aa_layer(self.cov, self.back, self.T_back, self.n_back, self.v_cov, self.v_rgb_aa)
+        else:
+            self.aa = None
 
     def set_camera(self, cam):
         assert int(cam.width) == self.W and int(cam.height) == self.H
@@ -377,6 +455,14 @@ class HybridRenderer:
         self.sh_degree = int(gaussians.sh_degree)
         self._alloc_gauss(int(self.means.shape[0]))
         self._alloc_tri(max(self.tri_cap, 1))
+        if self.antialias:
+            self.adj = torch.empty(self.F.shape[0], 3, dtype=I32, device=d)
+            nb = gm_mesh_edges_workspace_size(int(self.F.shape[0]))
+            ws = torch.empty((nb + 15) // 16 * 16 + 16, dtype=U8, device=d)
+            cnt = torch.zeros(4, dtype=I32, device=d)
+            gm_mesh_edges(self.F, self.V.shape[0], self.adj, cnt, ws)
+            if int(cnt[GM_CNT_FLAGS].item()) & GM_FLAG_TIMEOUT:
+                raise GmError(GM_ERR_TIMEOUT, "gm_mesh_edges", "a sort wait gave up")
 
     def _alloc_gauss(self, N):
         d = self.dev
@@ -435,6 +521,9 @@ class HybridRenderer:
         gm_zbuffer(cam, self.V, self.F, self.tri_range, self.tri_ids, self.face_id)
         gm_interp_mesh(cam, self.V, self.F, self.vcol, self.face_id, self.mesh_depth, self.mesh_rgb, self.tile_far,
                        self.tile_full)
+        if self.antialias:
+            gm_antialias(cam, self.V, self.F, self.adj, self.face_id, self.mesh_depth, self.mesh_rgb, self.cov,
+                         self.rgb_aa, self.depth_aa, self.tile_far, self.tile_full)
         if self.concurrent:
             main.wait_stream(side)
         for attempt in range(2):
@@ -448,14 +537,40 @@ class HybridRenderer:
                 if e.status != GM_ERR_CAPACITY or attempt:
                     raise
                 self._alloc_g(self._grow(int(self.g_counters[GM_CNT_K].item())))
-        gm_composite_hybrid_fwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
+        md, mc = (self.depth_aa, self.rgb_aa) if self.antialias else (self.mesh_depth, self.mesh_rgb)
+        gm_composite_hybrid_fwd(cam, opts, self.g_range, self.gids, self.splats, md, mc,
                                 self.face_id, self.out_rgb, self.out_depth, self.out_alpha, self.T_final,
-                                self.n_contrib, depth_model=self.depth_model)
+                                self.n_contrib, depth_model=self.depth_model, aa=self.aa)
         return self.out_rgb, self.out_depth, self.out_alpha
+
+    def _ensure_mesh_grads(self):
+        if not hasattr(self, "v_verts") or self.v_verts.shape != self.V.shape:
+            self.v_verts = torch.zeros_like(self.V)
+            self.v_vcol = torch.zeros_like(self.vcol)
 
     def backward(self, g_rgb, g_depth, g_alpha, mesh_grads: bool = True):
         cam, opts = self.cam, self.opts
         main = torch.cuda.current_stream(self.dev)
+        if self.antialias:
+            # Gaussians and the layer, then the layer to the interpolated colour / depth and
+            # the silhouettes, then the interpolation: one stream
+            self.v_splats.zero_()
+            if self.soft:
+                self.v_depth_model.zero_()
+            gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.depth_aa, self.rgb_aa,
+                                    self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha,
+                                    self.v_splats, depth_model=self.depth_model, v_depth_model=self.v_depth_model,
+                                    v_mesh_depth=self.v_mesh_depth, aa=self.aa)
+            if not mesh_grads:
+                return self.v_splats, None, None
+            self._ensure_mesh_grads()
+            self.v_verts.zero_()
+            self.v_vcol.zero_()
+            gm_antialias_bwd(cam, self.V, self.F, self.adj, self.face_id, self.mesh_depth, self.mesh_rgb, self.v_cov,
+                             self.v_rgb_aa, self.v_mesh_depth, self.v_mesh_rgb, self.v_interp_depth, self.v_verts)
+            gm_interp_mesh_bwd(cam, self.V, self.F, self.vcol, self.face_id, self.v_mesh_rgb, self.v_interp_depth,
+                               self.v_verts, self.v_vcol)
+            return self.v_splats, self.v_verts, self.v_vcol
         if self.soft:
             # the mesh part reads dL/dD that the Gaussian part writes: one call, one stream
             if mesh_grads:
@@ -534,9 +649,11 @@ class MultiViewRenderer:
     """
 
     def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4,
-                 softness=0.0, soft_split=GM_SPLIT_PHI):
+                 softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False):
         self.views = [HybridRenderer(c, bg=bg, cull_occluded=cull_occluded, device=device, concurrent=False,
-                                     tile_test=tile_test, softness=softness, soft_split=soft_split) for c in cams]
+                                     tile_test=tile_test, softness=softness, soft_split=soft_split,
+                                     antialias=antialias) for c in cams]
+        self.antialias = bool(antialias)
         self.soft = self.views[0].soft
         self.V = len(self.views)
         self.dev = torch.device(device)
@@ -573,6 +690,8 @@ class MultiViewRenderer:
             if k:
                 for name in ("V", "F", "vcol", "means", "log_scales", "quats", "logits", "colors", "sh_degree"):
                     setattr(r, name, getattr(v0, name))
+                if self.antialias:
+                    r.adj = v0.adj
                 r.N = N
                 r._alloc_g(max(r.g_cap, 1))
                 r._alloc_tri(max(r.tri_cap, 1))
@@ -611,12 +730,16 @@ class MultiViewRenderer:
                                  sync=False)
                 gm_zbuffer(cam, r.V, r.F, r.tri_range, r.tri_ids, r.face_id)
                 gm_interp_mesh(cam, r.V, r.F, r.vcol, r.face_id, r.mesh_depth, r.mesh_rgb, r.tile_far, r.tile_full)
+                if r.antialias:
+                    gm_antialias(cam, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov, r.rgb_aa,
+                                 r.depth_aa, r.tile_far, r.tile_full)
                 s.wait_event(projected)
                 gm_bin_sort_gaussians(cam, opts, r.splats, r.radii, r.tile_far, r.tile_full, r.keys, r.gids,
                                       r.g_range, r.g_cap, r.g_counters, r.g_ws, sync=False)
-                gm_composite_hybrid_fwd(cam, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
+                md, mc = (r.depth_aa, r.rgb_aa) if r.antialias else (r.mesh_depth, r.mesh_rgb)
+                gm_composite_hybrid_fwd(cam, opts, r.g_range, r.gids, r.splats, md, mc, r.face_id,
                                         r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
-                                        depth_model=r.depth_model)
+                                        depth_model=r.depth_model, aa=r.aa)
         for s in pool:
             main.wait_stream(s)
         return [(r.out_rgb, r.out_depth, r.out_alpha) for r in self.views]
@@ -638,6 +761,16 @@ class MultiViewRenderer:
             s = pool[k % len(pool)]
             s.wait_event(start)
             with torch.cuda.stream(s):
+                if r.antialias:
+                    gm_composite_hybrid_bwd(r.cam, r.opts, r.g_range, r.gids, r.splats, r.depth_aa, r.rgb_aa,
+                                            r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
+                                            depth_model=r.depth_model, v_depth_model=r.v_depth_model,
+                                            v_mesh_depth=r.v_mesh_depth, aa=r.aa)
+                    gm_antialias_bwd(r.cam, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.v_cov,
+                                     r.v_rgb_aa, r.v_mesh_depth, r.v_mesh_rgb, r.v_interp_depth, self.v_verts)
+                    gm_interp_mesh_bwd(r.cam, r.V, r.F, r.vcol, r.face_id, r.v_mesh_rgb, r.v_interp_depth,
+                                       self.v_verts, self.v_vcol)
+                    continue
                 gm_composite_hybrid_bwd(r.cam, r.opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb,
                                         r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
                                         r.V, r.F, r.vcol, self.v_verts, self.v_vcol, depth_model=r.depth_model,

@@ -27,6 +27,20 @@ int cuda_fail(cudaError_t e, const char* where)
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+gm::AaLayer layer_of(const gm_aa_layer* aa)
+{
+    gm::AaLayer l{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    if (aa && aa->cov) {
+        l.cov = aa->cov;
+        l.back = reinterpret_cast<float4*>(aa->back);
+        l.T_back = aa->T_back;
+        l.n_back = aa->n_back;
+        l.v_cov = aa->v_cov;
+        l.v_rgb = aa->v_rgb;
+    }
+    return l;
+}
+
 int check_cam(const gm_camera* cam)
 {
     if (!cam) return fail(GM_ERR_INVALID_ARG, "camera is NULL");
@@ -284,11 +298,76 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
     return finish_binning(counters, K_host, cap, s);
 }
 
+size_t gm_mesh_edges_workspace_size(int32_t nF)
+{
+    return nF < 0 ? 0 : gm::mesh_edges_ws_bytes(nF);
+}
+
+int gm_mesh_edges(const int32_t* F, int32_t nF, int32_t nV, int32_t* adj, int32_t* counters, void* ws,
+                  size_t ws_bytes, void* stream)
+{
+    g_err[0] = 0;
+    GM_REQUIRE(nF >= 0 && nV >= 0, "negative size");
+    GM_REQUIRE(nF == 0 || (F && adj), "F / adj is NULL");
+    GM_REQUIRE(counters, "counters is NULL");
+    GM_REQUIRE(nF <= (1 << 29), "too many faces");
+    GM_REQUIRE(nF == 0 || (ws && ws_bytes >= gm::mesh_edges_ws_bytes(nF)), "workspace too small");
+    cudaError_t e = gm::mesh_edges(F, nF, nV, adj, counters, ws, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_mesh_edges");
+}
+
+int gm_antialias(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                 const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
+                 float* cov, float* rgb_aa, float* depth_aa, float* tile_far, uint8_t* tile_full, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
+    GM_REQUIRE(nF == 0 || (V && F && adj), "V / F / adj is NULL");
+    GM_REQUIRE(face_id && mesh_depth && mesh_rgb, "an input is NULL");
+    GM_REQUIRE(cov && rgb_aa && depth_aa && tile_far && tile_full, "an output is NULL");
+    cudaError_t e = gm::antialias(gm::make_cam(*cam), V, nV, F, nF, adj, face_id, mesh_depth, mesh_rgb, cov, rgb_aa,
+                                  depth_aa, tile_far, tile_full, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_antialias");
+}
+
+int gm_antialias_bwd(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                     const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
+                     const float* v_cov, const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb,
+                     float* v_mesh_depth, float* v_verts, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
+    GM_REQUIRE(nF == 0 || (V && F && adj), "V / F / adj is NULL");
+    GM_REQUIRE(face_id && mesh_depth && mesh_rgb && v_cov && v_rgb_aa && v_depth_aa, "an input is NULL");
+    GM_REQUIRE(v_mesh_rgb && v_mesh_depth && (v_verts || nV == 0), "an output is NULL");
+    cudaError_t e = gm::antialias_bwd(gm::make_cam(*cam), V, nV, F, nF, adj, face_id, mesh_depth, mesh_rgb, v_cov,
+                                      v_rgb_aa, v_depth_aa, v_mesh_rgb, v_mesh_depth, v_verts, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_antialias_bwd");
+}
+
+int gm_interp_mesh_bwd(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                       const float* vcol, const int32_t* face_id, const float* v_mesh_rgb,
+                       const float* v_mesh_depth, float* v_verts, float* v_vcol, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
+    GM_REQUIRE(nF == 0 || (V && F && vcol), "V / F / vcol is NULL");
+    GM_REQUIRE(face_id && v_mesh_rgb && v_mesh_depth, "an input is NULL");
+    GM_REQUIRE(nV == 0 || (v_verts && v_vcol), "an output is NULL");
+    if (nF == 0) return GM_OK;
+    cudaError_t e = gm::interp_bwd(gm::make_cam(*cam), V, nV, F, nF, vcol, face_id, v_mesh_rgb, v_mesh_depth, v_verts,
+                                   v_vcol, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_interp_mesh_bwd");
+}
+
 int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N, const int32_t* tile_range,
                             const int32_t* gids, const float* splats, const float* depth_model,
                             const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id, float* out_rgb,
-                            float* out_depth, float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats,
-                            void* stream)
+                            float* out_depth, float* out_alpha, float* T_final, int32_t* n_contrib,
+                            const gm_aa_layer* aa, uint64_t* stats, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
@@ -296,8 +375,12 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     GM_REQUIRE(opts->softness >= 0.0f, "negative softness");
     GM_REQUIRE(opts->soft_split == GM_SPLIT_PHI || opts->soft_split == GM_SPLIT_LOGISTIC, "soft_split %d unknown",
                opts->soft_split);
-    GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id, "an input is NULL");
+    const bool aa_on = aa && aa->cov;
+    GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && (face_id || aa_on), "an input is NULL");
     GM_REQUIRE(out_rgb && out_depth && out_alpha && T_final && n_contrib, "an output is NULL");
+    if (aa_on)
+        GM_REQUIRE(aa->back && aligned16(aa->back) && aa->T_back && aa->n_back,
+                   "the antialiased layer needs back (16-byte aligned), T_back and n_back");
     GM_REQUIRE(N >= 0, "negative N");
     GM_REQUIRE(N == 0 || (splats && gids), "splats / gids is NULL");
     GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
@@ -307,7 +390,7 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, opts->softness, opts->soft_split, tile_range,
                                       gids, splats,
                                       depth_model, mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
-                                      T_final, n_contrib, stats, (cudaStream_t)stream);
+                                      T_final, n_contrib, layer_of(aa), stats, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_fwd");
 }
 
@@ -317,7 +400,7 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const float* T_final, const int32_t* n_contrib, const float* g_rgb, const float* g_depth,
                             const float* g_alpha, float* v_splats, float* v_depth_model, float* v_mesh_depth,
                             const float* V, int32_t nV, const int32_t* F, int32_t nF, const float* vcol,
-                            float* v_verts, float* v_vcol, uint64_t* stats, void* stream)
+                            float* v_verts, float* v_vcol, const gm_aa_layer* aa, uint64_t* stats, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
@@ -329,7 +412,16 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     if (soft && v_splats && N > 0)
         GM_REQUIRE(depth_model && aligned16(depth_model) && v_depth_model && aligned16(v_depth_model),
                    "the soft split needs 16-byte aligned depth_model and v_depth_model");
-    GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && face_id && T_final && n_contrib, "an input is NULL");
+    const bool aa_on = aa && aa->cov;
+    GM_REQUIRE(tile_range && mesh_depth && mesh_rgb && (face_id || aa_on) && T_final && n_contrib,
+               "an input is NULL");
+    if (aa_on) {
+        GM_REQUIRE(aa->back && aligned16(aa->back) && aa->T_back && aa->n_back && aa->v_cov && aa->v_rgb,
+                   "the antialiased layer needs back (16-byte aligned), T_back, n_back, v_cov and v_rgb");
+        GM_REQUIRE(v_mesh_depth, "the antialiased layer's gradient needs v_mesh_depth");
+        GM_REQUIRE(!V && !F && !vcol && !v_verts && !v_vcol,
+                   "with the antialiased layer the mesh gradients come from gm_antialias_bwd");
+    }
     GM_REQUIRE(g_rgb && g_depth && g_alpha, "an upstream gradient is NULL");
     GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
     GM_REQUIRE(!v_splats || aligned16(v_splats), "v_splats must be 16-byte aligned");
@@ -345,7 +437,7 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
         e = gm::composite_bwd(c, opts->bg, N, opts->softness, opts->soft_split, tile_range, gids, splats, depth_model,
                               mesh_depth,
                               mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model,
-                              soft ? v_mesh_depth : nullptr, stats, s);
+                              soft || aa_on ? v_mesh_depth : nullptr, layer_of(aa), stats, s);
     if (e == cudaSuccess && mesh_grads && nF > 0)
         e = gm::mesh_bwd(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, soft ? v_mesh_depth : nullptr,
                          v_verts, v_vcol, s);

@@ -198,7 +198,7 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id, float* __restrict__ out_rgb,
                 float* __restrict__ out_depth, float* __restrict__ out_alpha, float* __restrict__ T_final,
-                int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ stats)
+                int32_t* __restrict__ n_contrib, const float* __restrict__ aa_cov, unsigned long long* __restrict__ stats)
 {
     __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
     __shared__ float4 sD[SOFT ? CTA_THREADS : 1];
@@ -211,7 +211,8 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     bool cov = false;
     if (inside) {
         D = mesh_depth[pix];
-        cov = face_id[pix] >= 0;
+        // the antialiased layer has a split depth wherever any mesh reaches the pixel
+        cov = aa_cov ? D < INFINITY : face_id[pix] >= 0;
     }
     // soft split at this pixel: covered by the mesh (elsewhere D = +inf, f = 1)
     const bool soft = SOFT && cov;
@@ -307,16 +308,27 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     }
     if (inside) {
         float tr, tg, tb;
-        if (cov) {
-            tr = mesh_rgb[3 * pix]; tg = mesh_rgb[3 * pix + 1]; tb = mesh_rgb[3 * pix + 2];
+        if (aa_cov) {
+            // the layer (coverage a, premultiplied colour) over the background; the
+            // colour and depth composited behind it are added by k_composite_back
+            const float a = aa_cov[pix], ua = 1.0f - a;
+            tr = fmaf(ua, bg.x, mesh_rgb[3 * pix]);
+            tg = fmaf(ua, bg.y, mesh_rgb[3 * pix + 1]);
+            tb = fmaf(ua, bg.z, mesh_rgb[3 * pix + 2]);
+            out_depth[pix] = a > 0.0f ? fmaf(T, a * D, Z) : Z;
+            out_alpha[pix] = 1.0f - T * ua;
         } else {
-            tr = bg.x; tg = bg.y; tb = bg.z;
+            if (cov) {
+                tr = mesh_rgb[3 * pix]; tg = mesh_rgb[3 * pix + 1]; tb = mesh_rgb[3 * pix + 2];
+            } else {
+                tr = bg.x; tg = bg.y; tb = bg.z;
+            }
+            out_depth[pix] = cov ? fmaf(T, D, Z) : Z;
+            out_alpha[pix] = cov ? 1.0f : 1.0f - T;
         }
         out_rgb[3 * pix] = fmaf(T, tr, Cr);
         out_rgb[3 * pix + 1] = fmaf(T, tg, Cg);
         out_rgb[3 * pix + 2] = fmaf(T, tb, Cb);
-        out_depth[pix] = cov ? fmaf(T, D, Z) : Z;
-        out_alpha[pix] = cov ? 1.0f : 1.0f - T;
         T_final[pix] = T;
         n_contrib[pix] = last;
     }
@@ -436,7 +448,7 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
                 const float* __restrict__ g_rgb, const float* __restrict__ g_depth, const float* __restrict__ g_alpha,
                 float* __restrict__ v_splats, float* __restrict__ v_depth_model, float* __restrict__ v_mesh_depth,
-                unsigned long long* __restrict__ stats)
+                AaLayer aa, unsigned long long* __restrict__ stats)
 {
     constexpr int NACC = SOFT ? NGRAD + 4 : NGRAD;
     __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
@@ -460,12 +472,26 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     float vD = 0.0f;  // soft split: dL/d mesh depth at this pixel
     if (inside) {
         D = mesh_depth[pix];
-        cov = face_id[pix] >= 0;
+        cov = aa.cov ? D < INFINITY : face_id[pix] >= 0;
         T = T_final[pix];
         last = n_contrib[pix];
         gr = g_rgb[3 * pix]; gg = g_rgb[3 * pix + 1]; gb = g_rgb[3 * pix + 2];
         gz = g_depth[pix];
-        if (cov) {
+        if (aa.cov) {
+            // behind the front chain: the layer, and through 1 - a what lies behind it
+            // (the back chain's colour, depth and transmittance, then the background)
+            const float a = aa.cov[pix], ua = 1.0f - a;
+            float Tb = 1.0f, Eb = bg.x * gr + bg.y * gg + bg.z * gb;
+            if (cov && a < 1.0f) {
+                const float4 bk = aa.back[pix];
+                Tb = aa.T_back[pix];
+                Eb = fmaf(Tb, Eb, bk.x * gr + bk.y * gg + bk.z * gb + bk.w * gz);
+            }
+            const float own = mesh_rgb[3 * pix] * gr + mesh_rgb[3 * pix + 1] * gg + mesh_rgb[3 * pix + 2] * gb +
+                              (a > 0.0f ? a * D * gz : 0.0f);
+            behind = T * fmaf(ua, Eb, own);
+            aterm = g_alpha[pix] * T * ua * Tb;
+        } else if (cov) {
             behind = T * (mesh_rgb[3 * pix] * gr + mesh_rgb[3 * pix + 1] * gg + mesh_rgb[3 * pix + 2] * gb + D * gz);
         } else {
             behind = T * (bg.x * gr + bg.y * gg + bg.z * gb);
@@ -642,12 +668,193 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     if (SOFT && inside && v_mesh_depth) v_mesh_depth[pix] = vD;
 }
 
+// ----------------------------------------------------- the back chain -----
+//
+// Behind a fractional mesh layer (antialiased coverage 0 < a < 1, a split
+// depth D) the Gaussians' back parts are composited into a second chain
+// (Hybrid rendering, two-layer equation): under the hard split the Gaussians
+// at or behind D, under the soft split every Gaussian with alpha (1 - f).
+// One thread per pixel walks its tile's list (few pixels have such a layer);
+// the forward adds T_front (1 - a)(C_b + (T_b - 1) bg) to the colour the main
+// pass wrote, and the backward adds the Gaussians' gradients (global atomics)
+// and writes the layer's gradients (dL/da, dL/dM, dL/dD).
+
+// first list position whose Gaussian is not in front of D (the list is sorted
+// by centre depth; an invalid id counts as in front)
+__device__ __forceinline__ int first_behind(const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                                            int N, int lo, int hi, float D)
+{
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const int g = gids[mid];
+        const float z = (g >= 0 && g < N) ? splats[3 * (int64_t)g + 2].y : -INFINITY;
+        if (z < D) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <bool SOFT>
+__global__ void __launch_bounds__(256)
+k_composite_back_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
+                     const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                     const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
+                     const float* __restrict__ cov, const float* __restrict__ T_final, float* __restrict__ out_rgb,
+                     float* __restrict__ out_depth, float* __restrict__ out_alpha, float4* __restrict__ back,
+                     float* __restrict__ T_back, int32_t* __restrict__ n_back)
+{
+    const int64_t pix = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (pix >= (int64_t)c.W * c.H) return;
+    const float a = cov[pix], D = mesh_depth[pix];
+    if (!(D < INFINITY) || !(a < 1.0f)) return;
+    const int i = (int)(pix % c.W), j = (int)(pix / c.W);
+    const float px = (float)i + 0.5f, py = (float)j + 0.5f;
+    const int2 r = tile_range[(j / TILE) * c.TW + i / TILE];
+    const int start = SOFT ? r.x : first_behind(gids, splats, N, r.x, r.y, D);
+    float T = 1.0f, Cr = 0.f, Cg = 0.f, Cb = 0.f, Z = 0.f;
+    int last = 0;
+    for (int k = start; k < r.y; ++k) {
+        const int g = gids[k];
+        if (g < 0 || g >= N) continue;
+        float4 A, B, C, Hh;
+        stage(splats, g, A, B, C, Hh);
+        if (!SOFT && C.y < D) continue;
+        const Eval e = eval_splat(A, B, px, py);
+        if (e.skip) continue;
+        float part = e.alpha;
+        if (SOFT) {
+            const float4 Dm = stage_depth_model(depth_model, g, sp, C.y);
+            const float zs = fmaf(Dm.x, e.dx, fmaf(Dm.y, e.dy, C.y));
+            part = e.alpha * (1.0f - sp.front((D - zs) * Dm.z));
+            if (part < ALPHA_MIN) continue;
+        }
+        const float Tn = __fmul_rn(T, __fsub_rn(1.0f, part));
+        if (Tn <= T_STOP) break;
+        const float w = part * T;
+        Cr = fmaf(w, B.z, Cr);
+        Cg = fmaf(w, B.w, Cg);
+        Cb = fmaf(w, C.x, Cb);
+        Z = fmaf(w, C.y, Z);
+        T = Tn;
+        last = k - r.x + 1;
+    }
+    back[pix] = make_float4(Cr, Cg, Cb, Z);
+    T_back[pix] = T;
+    n_back[pix] = last;
+    const float s = T_final[pix] * (1.0f - a), tm1 = T - 1.0f;
+    out_rgb[3 * pix] = fmaf(s, fmaf(tm1, bg.x, Cr), out_rgb[3 * pix]);
+    out_rgb[3 * pix + 1] = fmaf(s, fmaf(tm1, bg.y, Cg), out_rgb[3 * pix + 1]);
+    out_rgb[3 * pix + 2] = fmaf(s, fmaf(tm1, bg.z, Cb), out_rgb[3 * pix + 2]);
+    out_depth[pix] = fmaf(s, Z, out_depth[pix]);
+    out_alpha[pix] = 1.0f - s * T;
+}
+
+template <bool SOFT>
+__global__ void __launch_bounds__(256)
+k_composite_back_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
+                     const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                     const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
+                     const float* __restrict__ mesh_rgb, const float* __restrict__ T_final,
+                     const float* __restrict__ g_rgb, const float* __restrict__ g_depth,
+                     const float* __restrict__ g_alpha, AaLayer aa, float* __restrict__ v_splats,
+                     float* __restrict__ v_depth_model, float* __restrict__ v_mesh_depth)
+{
+    const int64_t pix = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (pix >= (int64_t)c.W * c.H) return;
+    const float a = aa.cov[pix], D = mesh_depth[pix], Tf = T_final[pix], ua = 1.0f - a;
+    const bool has_mesh = D < INFINITY, frac = has_mesh && a < 1.0f;
+    const float gr = g_rgb[3 * pix], gg = g_rgb[3 * pix + 1], gb = g_rgb[3 * pix + 2], gz = g_depth[pix],
+                ga = g_alpha[pix];
+    float Tb = 1.0f, Eb = bg.x * gr + bg.y * gg + bg.z * gb;
+    float4 bk = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (frac) {
+        bk = aa.back[pix];
+        Tb = aa.T_back[pix];
+        Eb = fmaf(Tb, Eb, bk.x * gr + bk.y * gg + bk.z * gb + bk.w * gz);
+    }
+    // the layer: rgb = C + T (M + (1 - a)(C_b + T_b bg)), depth = Z + T (a D + (1 - a) Z_b),
+    // alpha = 1 - T (1 - a) T_b
+    aa.v_rgb[3 * pix] = Tf * gr;
+    aa.v_rgb[3 * pix + 1] = Tf * gg;
+    aa.v_rgb[3 * pix + 2] = Tf * gb;
+    aa.v_cov[pix] = has_mesh ? Tf * (fmaf(gz, D, -Eb) + ga * Tb) : 0.0f;
+    float vD = (SOFT ? v_mesh_depth[pix] : 0.0f) + (a > 0.0f && has_mesh ? Tf * a * gz : 0.0f);
+    const int nb = frac ? aa.n_back[pix] : 0;
+    if (nb > 0) {
+        // the back chain, back to front, with the upstream gradient scaled by T (1 - a)
+        const int i = (int)(pix % c.W), j = (int)(pix / c.W);
+        const float px = (float)i + 0.5f, py = (float)j + 0.5f;
+        const int2 r = tile_range[(j / TILE) * c.TW + i / TILE];
+        const int start = SOFT ? r.x : first_behind(gids, splats, N, r.x, r.y, D);
+        const float s = Tf * ua;
+        const float hr = s * gr, hg = s * gg, hb = s * gb, hz = s * gz;
+        float T = Tb, behind = Tb * (bg.x * hr + bg.y * hg + bg.z * hb);
+        const float aterm = s * ga * Tb;
+        for (int k = min(r.x + nb, r.y) - 1; k >= start; --k) {
+            const int g = gids[k];
+            if (g < 0 || g >= N) continue;
+            float4 A, B, C, Hh;
+            stage(splats, g, A, B, C, Hh);
+            if (!SOFT && C.y < D) continue;
+            const Eval e = eval_splat(A, B, px, py);
+            if (e.skip) continue;
+            float part = e.alpha, f = 0.0f, x = 0.0f;
+            float4 Dm = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (SOFT) {
+                Dm = stage_depth_model(depth_model, g, sp, C.y);
+                const float zs = fmaf(Dm.x, e.dx, fmaf(Dm.y, e.dy, C.y));
+                x = (D - zs) * Dm.z;
+                f = sp.front(x);
+                part = e.alpha * (1.0f - f);
+                if (part < ALPHA_MIN) continue;
+            }
+            const float rom = __fdividef(1.0f, 1.0f - part);
+            const float Tp = T * rom;
+            const float w = part * Tp;
+            const float front = B.z * hr + B.w * hg + C.x * hb + C.y * hz;
+            const float dLdp = Tp * front + (aterm - behind) * rom;  // dL / d(the back part)
+            behind = fmaf(w, front, behind);
+            T = Tp;
+            // record gradient: sigma = (a dx^2 + c dy^2) / 2 + b dx dy of the record's conic
+            const float4* rec = splats + 3 * (int64_t)g;
+            const float4 s0 = rec[0], s1 = rec[1];
+            float vg[10] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, w * hr, w * hg, w * hb, w * hz};
+            const float dLdal = SOFT ? dLdp * (1.0f - f) : dLdp;
+            if (!e.clamped) {
+                const float ds = -dLdal * e.alpha;  // d alpha / d sigma = -alpha
+                vg[0] = -ds * (s0.z * e.dx + s0.w * e.dy);
+                vg[1] = -ds * (s0.w * e.dx + s1.x * e.dy);
+                vg[2] = 0.5f * ds * e.dx * e.dx;
+                vg[3] = ds * e.dx * e.dy;
+                vg[4] = 0.5f * ds * e.dy * e.dy;
+                vg[5] = dLdal * e.G;
+            }
+            if (SOFT) {  // the back part alpha (1 - f(x)): dL/dx = -dLdp alpha f'(x)
+                const float psi = -dLdp * e.alpha * sp.density(x, f);
+                const float pz = psi * Dm.z;
+                vg[0] += pz * Dm.x;
+                vg[1] += pz * Dm.y;
+                vg[9] -= pz;
+                vD += pz;
+                atomicAdd(reinterpret_cast<float4*>(v_depth_model) + g,
+                          make_float4(-pz * e.dx, -pz * e.dy, -psi * x * Dm.z * sp.softness, 0.0f));
+            }
+            float4* dst = reinterpret_cast<float4*>(v_splats + 12 * (int64_t)g);
+            atomicAdd(dst, make_float4(vg[0], vg[1], vg[2], vg[3]));
+            atomicAdd(dst + 1, make_float4(vg[4], vg[5], vg[6], vg[7]));
+            atomicAdd(dst + 2, make_float4(vg[8], vg[9], 0.0f, 0.0f));
+        }
+    }
+    v_mesh_depth[pix] = vD;
+}
+
 }  // namespace
 
 cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
-                          float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s)
+                          float* out_alpha, float* T_final, int32_t* n_contrib, const AaLayer& aa, uint64_t* stats,
+                          cudaStream_t s)
 {
     const bool soft = softness > 0.0f;
     auto kern = soft ? (stats ? k_composite_fwd<true, true> : k_composite_fwd<false, true>)
@@ -656,7 +863,16 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness
         c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
         gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
-        face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, reinterpret_cast<unsigned long long*>(stats));
+        face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, aa.cov, reinterpret_cast<unsigned long long*>(stats));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !aa.cov) return e;
+    const int64_t P = (int64_t)c.W * c.H;
+    const unsigned grid = (unsigned)((P + 255) / 256);
+    auto back = soft ? k_composite_back_fwd<true> : k_composite_back_fwd<false>;
+    back<<<grid, 256, 0, s>>>(c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1},
+                              reinterpret_cast<const int2*>(tile_range), gids, reinterpret_cast<const float4*>(splats),
+                              reinterpret_cast<const float4*>(depth_model), mesh_depth, aa.cov, T_final, out_rgb,
+                              out_depth, out_alpha, aa.back, aa.T_back, aa.n_back);
     return cudaGetLastError();
 }
 
@@ -664,8 +880,8 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, const float* T_final,
                           const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
-                          float* v_splats, float* v_depth_model, float* v_mesh_depth, uint64_t* stats,
-                          cudaStream_t s)
+                          float* v_splats, float* v_depth_model, float* v_mesh_depth, const AaLayer& aa,
+                          uint64_t* stats, cudaStream_t s)
 {
     const bool soft = softness > 0.0f;
     auto kern = soft ? (stats ? k_composite_bwd<true, true> : k_composite_bwd<false, true>)
@@ -674,8 +890,17 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
         c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
         gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
-        face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth,
+        face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth, aa,
         reinterpret_cast<unsigned long long*>(stats));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !aa.cov) return e;
+    const int64_t P = (int64_t)c.W * c.H;
+    const unsigned grid = (unsigned)((P + 255) / 256);
+    auto back = soft ? k_composite_back_bwd<true> : k_composite_back_bwd<false>;
+    back<<<grid, 256, 0, s>>>(c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1},
+                              reinterpret_cast<const int2*>(tile_range), gids, reinterpret_cast<const float4*>(splats),
+                              reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb, T_final, g_rgb,
+                              g_depth, g_alpha, aa, v_splats, v_depth_model, v_mesh_depth);
     return cudaGetLastError();
 }
 

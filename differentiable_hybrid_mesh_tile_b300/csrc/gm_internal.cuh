@@ -206,15 +206,41 @@ cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
 
+// The antialiased mesh layer and the buffers of its back chain (Hybrid
+// rendering, two-layer equation).  cov == nullptr: coverage is face_id >= 0
+// and the compositing is the one-layer form.
+struct AaLayer {
+    const float* cov;  // [H][W] coverage a; mesh_rgb is then premultiplied, mesh_depth the split depth
+    float4* back;      // [H][W] colour and depth composited behind the layer (forward out, backward in)
+    float* T_back;     // [H][W] transmittance of that chain
+    int32_t* n_back;   // [H][W] 1 + list position of its last composited Gaussian
+    float* v_cov;      // [H][W] backward out: dL/da
+    float* v_rgb;      // [H][W][3] backward out: dL/dM
+};
+
+size_t mesh_edges_ws_bytes(int nF);
+cudaError_t mesh_edges(const int32_t* F, int nF, int nV, int32_t* adj, int32_t* counters, void* ws, cudaStream_t s);
+cudaError_t antialias(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* adj,
+                      const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, float* cov,
+                      float* rgb_aa, float* depth_aa, float* tile_far, uint8_t* tile_full, cudaStream_t s);
+cudaError_t antialias_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* adj,
+                          const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, const float* v_cov,
+                          const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb, float* v_mesh_depth,
+                          float* v_verts, cudaStream_t s);
+cudaError_t interp_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
+                       const int32_t* face_id, const float* v_mesh_rgb, const float* v_mesh_depth, float* v_verts,
+                       float* v_vcol, cudaStream_t s);
+
 cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
-                          float* out_alpha, float* T_final, int32_t* n_contrib, uint64_t* stats, cudaStream_t s);
+                          float* out_alpha, float* T_final, int32_t* n_contrib, const AaLayer& aa, uint64_t* stats,
+                          cudaStream_t s);
 cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, const float* T_final,
                           const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
-                          float* v_splats, float* v_depth_model, float* v_mesh_depth, uint64_t* stats,
-                          cudaStream_t s);
+                          float* v_splats, float* v_depth_model, float* v_mesh_depth, const AaLayer& aa,
+                          uint64_t* stats, cudaStream_t s);
 
 }  // namespace gm

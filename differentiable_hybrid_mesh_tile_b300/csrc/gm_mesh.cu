@@ -302,6 +302,10 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// DIRECT: g_rgb / g_depth are already dL/d(interpolated colour, depth) per pixel
+// (from the antialiasing's backward); otherwise they are the image's upstream
+// gradient, weighted here by the transmittance in front of the mesh.
+template <bool DIRECT>
 __global__ void __launch_bounds__(TILE_PIX)
 k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
            const float* __restrict__ vcol, const int32_t* __restrict__ face_id, const float* __restrict__ T_final,
@@ -325,10 +329,10 @@ k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
         for (int k = 0; k < 3; ++k)
 #pragma unroll
             for (int ch = 0; ch < 3; ++ch) C[k][ch] = __ldg(vcol + 3 * (int64_t)vid[k] + ch);
-        const float T = T_final[pix];
+        const float T = DIRECT ? 1.0f : T_final[pix];
         const float gc[3] = {T * g_rgb[3 * pix], T * g_rgb[3 * pix + 1], T * g_rgb[3 * pix + 2]};
         // dL/dD: through the depth output (T D), and through the soft split when given
-        const float gD = T * g_depth[pix] + (v_mesh_depth ? v_mesh_depth[pix] : 0.0f);
+        const float gD = T * g_depth[pix] + (!DIRECT && v_mesh_depth ? v_mesh_depth[pix] : 0.0f);
         interp_grad(c, X, C, (float)i + 0.5f, (float)j + 0.5f, gD, gc, gX, gC);
     }
     // one set of atomics per distinct face in the warp
@@ -440,8 +444,17 @@ cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int
                      const int32_t* face_id, const float* T_final, const float* g_rgb, const float* g_depth,
                      const float* v_mesh_depth, float* v_verts, float* v_vcol, cudaStream_t s)
 {
-    k_mesh_bwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, v_mesh_depth,
-                                                 v_verts, v_vcol);
+    k_mesh_bwd<false><<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth,
+                                                        v_mesh_depth, v_verts, v_vcol);
+    return cudaGetLastError();
+}
+
+cudaError_t interp_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
+                       const int32_t* face_id, const float* v_mesh_rgb, const float* v_mesh_depth, float* v_verts,
+                       float* v_vcol, cudaStream_t s)
+{
+    k_mesh_bwd<true><<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, V, nV, F, nF, vcol, face_id, nullptr, v_mesh_rgb,
+                                                       v_mesh_depth, nullptr, v_verts, v_vcol);
     return cudaGetLastError();
 }
 

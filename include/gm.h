@@ -92,6 +92,20 @@ typedef struct gm_opts {
 #define GM_SPLIT_PHI 0
 #define GM_SPLIT_LOGISTIC 1
 
+/* The antialiased mesh layer (gm_antialias) and the buffers of the chain of
+ * Gaussians composited behind it, for gm_composite_hybrid_fwd / _bwd.  All
+ * images row-major [H][W], device memory owned by the caller. */
+typedef struct gm_aa_layer {
+    const float* cov;  /* [H][W] coverage a in [0, 1]; the call's mesh_rgb is then the
+                          premultiplied colour M = a c and mesh_depth the split depth */
+    float* back;       /* [H][W][4], 16-byte aligned: colour and depth composited behind the
+                          layer (written by the forward, read by the backward) */
+    float* T_back;     /* [H][W]: that chain's transmittance (forward out, backward in) */
+    int32_t* n_back;   /* [H][W]: 1 + list position of its last composited Gaussian */
+    float* v_cov;      /* [H][W] backward out: dL/da */
+    float* v_rgb;      /* [H][W][3] backward out: dL/dM */
+} gm_aa_layer;
+
 /*
  * Projected-Gaussian record ("splat"), GM_SPLAT_STRIDE floats, 16-byte aligned:
  *   [0] mean2d x  [1] mean2d y      (pixels)
@@ -151,6 +165,76 @@ int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* 
 int gm_interp_mesh(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
                    const float* vcol, const int32_t* face_id, float* mesh_depth, float* mesh_rgb,
                    float* tile_far, uint8_t* tile_full, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_mesh_edges -- edge adjacency for the antialiasing (Mesh rasterizer,
+ * item 3: internal edges of a connected surface are left untouched).
+ *   adj [nF][3] i32 out: the face that shares edge k of face f (edge k joins
+ *   corners k+1 and k+2 mod 3, the edge opposite corner k), -1 when no other
+ *   face does, -2 when more than one does.  Depends on F only (compute once
+ *   per mesh topology).  Vertex ids must lie in [0, nV).
+ *   ws / ws_bytes: device scratch of at least gm_mesh_edges_workspace_size(nF)
+ *   bytes; counters: device int32[4] (flags: a sort wait that gave up sets
+ *   GM_FLAG_TIMEOUT).
+ * ---------------------------------------------------------------------- */
+size_t gm_mesh_edges_workspace_size(int32_t nF);
+int gm_mesh_edges(const int32_t* F, int32_t nF, int32_t nV, int32_t* adj, int32_t* counters, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_antialias -- Mesh rasterizer, item 3: analytic edge antialiasing (as in
+ * nvdiffrast; Limitations: a per-axis 1D approximation, exact for straight
+ * edges away from corners).  For each pair of neighbouring pixels (along x
+ * and y) that see different faces, the nearer surface (smaller mesh_depth,
+ * none when equal) is followed from its pixel's centre towards the other
+ * centre through its faces -- across internal edges: one face across, lying
+ * on the other side of the edge in the image -- until it leaves by a
+ * silhouette edge (no face across, more than one, or one folded onto the
+ * same side), at most 8 faces; a pair along x only takes an edge more
+ * vertical than horizontal in the image, a pair along y the others.  The
+ * crossing t (0 at the nearer pixel's centre, 1 at the other's) gives the
+ * weight w = |t - 0.5|, which moves the layer (a, M) of one pixel towards the
+ * other pixel's (coverage 1 and colour c where the mesh covers a pixel, 0
+ * elsewhere): the other pixel when t >= 0.5 (the surface reaches into it),
+ * the nearer one when t < 0.5 (the surface leaves part of it).  Weights add
+ * up per pixel; a is clamped to [0, 1].  A pixel the mesh does not cover and
+ * a surface reaches takes that surface pixel's depth as its split depth.
+ *   Inputs: face_id / mesh_depth / mesh_rgb of gm_zbuffer + gm_interp_mesh,
+ *   adj of gm_mesh_edges.  Outputs [H][W]: cov (a), rgb_aa [H][W][3] (M),
+ *   depth_aa (split depth, +inf where no mesh), and per tile tile_far (the
+ *   largest split depth) / tile_full (every pixel has a = 1), which replace
+ *   those of gm_interp_mesh for the occlusion cull.
+ *   Decisions are taken in fp32 with the z-buffer's operations; the crossing
+ *   t in fp64.
+ * ---------------------------------------------------------------------- */
+int gm_antialias(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                 const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
+                 float* cov, float* rgb_aa, float* depth_aa, float* tile_far, uint8_t* tile_full, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_antialias_bwd -- gradients of gm_antialias: from dL/d(cov, rgb_aa,
+ * depth_aa) (v_cov, v_rgb_aa, v_depth_aa [H][W], [H][W][3], [H][W], e.g. the
+ * layer gradients of gm_composite_hybrid_bwd) to
+ *   v_mesh_rgb [H][W][3], v_mesh_depth [H][W] (written): dL/d the
+ *   interpolated colour and depth of each pixel, for gm_interp_mesh_bwd;
+ *   v_verts [nV][3] (+=): dL/d the world positions of the silhouette edges'
+ *   vertices through the crossings t (the weights' other dependence).
+ *   Same mesh inputs as the forward call.  A weight that falls on a pixel
+ *   whose coverage was clamped carries no coverage gradient.
+ * ---------------------------------------------------------------------- */
+int gm_antialias_bwd(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                     const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
+                     const float* v_cov, const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb,
+                     float* v_mesh_depth, float* v_verts, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_interp_mesh_bwd -- backward of gm_interp_mesh for given per-pixel
+ * gradients v_mesh_rgb [H][W][3] and v_mesh_depth [H][W] of the interpolated
+ * colour and depth (face ids held fixed): v_verts, v_vcol [nV][3] (+=).
+ * ---------------------------------------------------------------------- */
+int gm_interp_mesh_bwd(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                       const float* vcol, const int32_t* face_id, const float* v_mesh_rgb,
+                       const float* v_mesh_depth, float* v_verts, float* v_vcol, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_project_gaussians -- EWA projection and colour of each Gaussian
@@ -263,6 +347,16 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
  * required, 16-byte aligned), scales its alpha: alpha f replaces alpha in the
  * skip, the stop and the sums (the back parts lie behind the opaque mesh).
  * Uncovered pixels are unchanged.  depth_model is ignored when softness = 0.
+ * Antialiased layer (aa != NULL, aa->cov given; Hybrid rendering, the
+ * two-layer equation): the mesh layer has coverage a = aa->cov in [0, 1],
+ * premultiplied colour M = mesh_rgb and split depth D = mesh_depth (the
+ * outputs of gm_antialias); Gaussians split at D composite in front of it
+ * (the chain above) and, where 0 < a < 1, behind it in a second chain C_b,
+ * Z_b, T_b (hard split: those at or behind D; soft split: alpha (1 - f)):
+ *   out_rgb = C + T (M + (1 - a)(C_b + T_b bg)), out_depth = Z + T (a D +
+ *   (1 - a) Z_b), out_alpha = 1 - T (1 - a) T_b.
+ *   aa->back / T_back / n_back receive the back chain (read only where
+ *   0 < a < 1 and D is finite).  face_id is not read.
  * opts->soft_split picks f = Phi (GM_SPLIT_PHI) or the logistic 1 / (1 +
  * exp(-1.702 x)) (GM_SPLIT_LOGISTIC) as the front fraction.
  * Each warp's 8 x 4 pixel block passes over the Gaussians with z_c - R -
@@ -274,7 +368,8 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const int32_t* tile_range, const int32_t* gids, const float* splats,
                             const float* depth_model, const float* mesh_depth, const float* mesh_rgb,
                             const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
-                            float* T_final, int32_t* n_contrib, uint64_t* stats, void* stream);
+                            float* T_final, int32_t* n_contrib, const gm_aa_layer* aa, uint64_t* stats,
+                            void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_composite_hybrid_bwd -- Hybrid rendering ("everything is
@@ -298,6 +393,12 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  *   mesh gradients): dL/dD through the split, written by the Gaussian part
  *   (v_splats != NULL) and read by the mesh part (v_verts != NULL), so a
  *   call with only the mesh part must follow one with the Gaussian part.
+ *   Antialiased layer (aa as for the forward, with aa->back / T_back / n_back
+ *   as the forward wrote them): the Gaussian gradients of both chains; the
+ *   layer's gradients aa->v_cov (dL/da), aa->v_rgb (dL/dM) and, in
+ *   v_mesh_depth (required), dL/dD (the depth output and the soft split) --
+ *   the input of gm_antialias_bwd; the mesh arguments must then be NULL
+ *   (the mesh gradients come from gm_antialias_bwd and gm_interp_mesh_bwd).
  * ---------------------------------------------------------------------- */
 int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N,
                             const int32_t* tile_range, const int32_t* gids, const float* splats,
@@ -306,7 +407,7 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
                             float* v_depth_model, float* v_mesh_depth, const float* V, int32_t nV,
                             const int32_t* F, int32_t nF, const float* vcol, float* v_verts,
-                            float* v_vcol, uint64_t* stats, void* stream);
+                            float* v_vcol, const gm_aa_layer* aa, uint64_t* stats, void* stream);
 
 /* ------------------------------------------------------------------------
  * Batched views (several cameras of one scene, e.g. the views of a training

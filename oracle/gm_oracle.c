@@ -1438,8 +1438,8 @@ void orc_composite_fd(const orc_camera* c, const float* bg, const float* splats,
  * silhouette crossings.  req_field 0..2 = world x, y, z of the vertex, 3..5 =
  * its r, g, b.  Re-evaluated: the depth and colour (in double, from the moved
  * mesh) of the pixels whose face uses the vertex, the antialiased layer of
- * those pixels and their 4-neighbours, and the composite (double) of every
- * such pixel.  The fp32 reference decisions use mesh_depth / mesh_rgb as
+ * every pixel within 2 px of the image box of such a face, and the composite
+ * (double) of every such pixel.  The fp32 reference decisions use mesh_depth / mesh_rgb as
  * given.  Status codes as for orc_composite_fd; the antialiasing decisions
  * (occluder, exit edge, silhouette, side) count as decisions.             */
 static int cmp_i64(const void* a, const void* b)
@@ -1531,20 +1531,39 @@ void orc_mesh_fd(const orc_camera* c, const float* bg, const float* V, int32_t n
                         ovc[3 * (sgn * n1 + k) + ch] = w[0] * C3[0][ch] + w[1] * C3[1][ch] + w[2] * C3[2][ch];
                 }
             }
-            /* P2: P1 and, with antialiasing, its 4-neighbours */
-            int64_t n2 = adj ? 5 * n1 : n1;
+            /* P2: P1 and, with antialiasing, every pixel within 2 px of the image
+             * box of a face that uses the vertex (a pair's segment may cross such a
+             * face -- also one that covers no pixel centre -- on its way to a
+             * silhouette edge, or end at one of its edges) */
+            int64_t n2 = n1;
+            int box[64][4];
+            int nbox = 0;
+            if (adj) {
+                for (int64_t fk = vstart[vid]; fk < vstart[vid + 1] && nbox < 64; ++fk) {
+                    int f = vface[fk];
+                    double X[3][3];
+                    load_tri(V, F, f, X);
+                    tri64 t;
+                    tri_setup_f64(c, X, &t);
+                    int ok = 1;
+                    for (int kk = 0; kk < 3; ++kk) ok &= t.z[kk] > (double)c->near_plane;
+                    if (!ok) continue;
+                    double u0 = fmin(fmin(t.u[0], t.u[1]), t.u[2]), u1 = fmax(fmax(t.u[0], t.u[1]), t.u[2]);
+                    double v0 = fmin(fmin(t.v[0], t.v[1]), t.v[2]), v1 = fmax(fmax(t.v[0], t.v[1]), t.v[2]);
+                    int b[4] = {(int)fmax(floor(u0) - 2, 0), (int)fmax(floor(v0) - 2, 0),
+                                (int)fmin(ceil(u1) + 2, c->width - 1), (int)fmin(ceil(v1) + 2, c->height - 1)};
+                    if (b[0] > b[2] || b[1] > b[3]) continue;
+                    for (int kk = 0; kk < 4; ++kk) box[nbox][kk] = b[kk];
+                    n2 += (int64_t)(b[2] - b[0] + 1) * (b[3] - b[1] + 1);
+                    nbox++;
+                }
+            }
             int64_t* p2 = (int64_t*)malloc(sizeof(int64_t) * (n2 > 0 ? n2 : 1));
             n2 = 0;
-            for (int64_t k = 0; k < n1; ++k) {
-                int64_t pix = p1[k];
-                p2[n2++] = pix;
-                if (!adj) continue;
-                int i = (int)(pix % c->width), j = (int)(pix / c->width);
-                if (i > 0) p2[n2++] = pix - 1;
-                if (i + 1 < c->width) p2[n2++] = pix + 1;
-                if (j > 0) p2[n2++] = pix - c->width;
-                if (j + 1 < c->height) p2[n2++] = pix + c->width;
-            }
+            for (int64_t k = 0; k < n1; ++k) p2[n2++] = p1[k];
+            for (int bq = 0; bq < nbox; ++bq)
+                for (int j = box[bq][1]; j <= box[bq][3]; ++j)
+                    for (int i = box[bq][0]; i <= box[bq][2]; ++i) p2[n2++] = (int64_t)j * c->width + i;
             qsort(p2, (size_t)n2, sizeof(int64_t), cmp_i64);
             int64_t u2 = 0;
             for (int64_t k = 0; k < n2; ++k)

@@ -65,6 +65,97 @@ def run_mesh(cam, mesh):
                 mesh_rgb=host(mrgb), tile_far=host(tfar), tile_full=host(tfull), counters=host(cnt))
 
 
+def run_mesh_edges(F, nV):
+    """GPU gm_mesh_edges: adjacency [nF][3] as numpy."""
+    Fd = dev(F, torch.int32)
+    adj = torch.full((max(len(F), 1), 3), -9, dtype=torch.int32, device="cuda")
+    ws = torch.empty(gm.gm_mesh_edges_workspace_size(len(F)) + 16, dtype=torch.uint8, device="cuda")
+    cnt = torch.zeros(4, dtype=torch.int32, device="cuda")
+    gm.gm_mesh_edges(Fd, nV, adj, cnt, ws)
+    assert int(host(cnt)[2]) == 0
+    return host(adj)[:len(F)]
+
+
+def run_antialias(cam, mesh, m):
+    """GPU gm_antialias over the GPU mesh images m (run_mesh): the layer and the
+    per-tile bounds, plus the adjacency used."""
+    c = gm.make_camera(cam)
+    adj = run_mesh_edges(mesh.faces, len(mesh.verts))
+    H, W, T = cam.height, cam.width, n_tiles(cam)
+    cov = torch.full((H, W), -3.0, dtype=torch.float32, device="cuda")
+    rgb = torch.full((H, W, 3), -3.0, dtype=torch.float32, device="cuda")
+    depth = torch.full((H, W), -3.0, dtype=torch.float32, device="cuda")
+    tf = torch.full((T,), -3.0, dtype=torch.float32, device="cuda")
+    tu = torch.full((T,), 7, dtype=torch.uint8, device="cuda")
+    gm.gm_antialias(c, dev(mesh.verts, torch.float32), dev(mesh.faces, torch.int32), dev(adj, torch.int32),
+                    dev(m["face_id"], torch.int32), dev(m["mesh_depth"], torch.float32),
+                    dev(m["mesh_rgb"], torch.float32), cov, rgb, depth, tf, tu)
+    return dict(adj=adj, cov=host(cov), rgb_aa=host(rgb), depth_aa=host(depth), tile_far=host(tf),
+                tile_full=host(tu))
+
+
+def run_composite_aa(cam, bg, tile_range, gids, splats, aa, softness=0.0, depth_model=None, soft_split=0):
+    """GPU composite over the antialiased layer aa (run_antialias)."""
+    c = gm.make_camera(cam)
+    o = gm.make_opts(bg, True, -1, True, softness, soft_split)
+    H, W = cam.height, cam.width
+    out = {k: torch.full(s, -3.0, dtype=torch.float32, device="cuda")
+           for k, s in [("rgb", (H, W, 3)), ("depth", (H, W)), ("alpha", (H, W)), ("T", (H, W))]}
+    nc = torch.full((H, W), -3, dtype=torch.int32, device="cuda")
+    buf = dict(cov=dev(aa["cov"], torch.float32), back=torch.zeros(H, W, 4, dtype=torch.float32, device="cuda"),
+               T_back=torch.zeros(H, W, dtype=torch.float32, device="cuda"),
+               n_back=torch.zeros(H, W, dtype=torch.int32, device="cuda"),
+               v_cov=torch.zeros(H, W, dtype=torch.float32, device="cuda"),
+               v_rgb=torch.zeros(H, W, 3, dtype=torch.float32, device="cuda"))
+    layer = gm.make_aa_layer(buf["cov"], buf["back"], buf["T_back"], buf["n_back"], buf["v_cov"], buf["v_rgb"])
+    args = [dev(tile_range, torch.int32), dev(gids if len(gids) else np.zeros(1, np.int32), torch.int32),
+            dev(splats if len(splats) else np.zeros((1, 12), np.float32), torch.float32),
+            dev(aa["depth_aa"], torch.float32), dev(aa["rgb_aa"], torch.float32), None]
+    dm = None
+    if depth_model is not None:
+        dm = dev(depth_model if len(depth_model) else np.zeros((1, 4), np.float32), torch.float32)
+    gm.gm_composite_hybrid_fwd(c, o, *args, out["rgb"], out["depth"], out["alpha"], out["T"], nc, depth_model=dm,
+                               aa=layer)
+    res = {k: host(v) for k, v in out.items()}
+    res["n_contrib"] = host(nc)
+    res.update(back=host(buf["back"]), T_back=host(buf["T_back"]), n_back=host(buf["n_back"]))
+    res["_args"] = args
+    res["_dev"] = dict(T=out["T"], n_contrib=nc)
+    res["_soft"] = (softness, dm, soft_split)
+    res["_aa"] = (layer, buf)
+    return res
+
+
+def run_backward_aa(cam, bg, fwd, grads, N, mesh, m, adj):
+    """GPU backward over the antialiased layer: composite (Gaussians + layer),
+    then gm_antialias_bwd and gm_interp_mesh_bwd.  Returns v_splats (+ the depth
+    model's), v_verts, v_vcol and the layer gradients."""
+    c = gm.make_camera(cam)
+    softness, dm, split = fwd["_soft"]
+    o = gm.make_opts(bg, True, -1, True, softness, split)
+    layer, buf = fwd["_aa"]
+    H, W = cam.height, cam.width
+    v_splats = torch.zeros(max(N, 1), 12, dtype=torch.float32, device="cuda")
+    v_dm = torch.zeros(max(N, 1), 4, dtype=torch.float32, device="cuda") if softness > 0 else None
+    v_md = torch.full((H, W), 5.0, dtype=torch.float32, device="cuda")
+    g_rgb, g_depth, g_alpha = (dev(x, torch.float32) for x in grads)
+    gm.gm_composite_hybrid_bwd(c, o, *fwd["_args"], fwd["_dev"]["T"], fwd["_dev"]["n_contrib"], g_rgb, g_depth,
+                               g_alpha, v_splats, depth_model=dm, v_depth_model=v_dm, v_mesh_depth=v_md, aa=layer)
+    V, F, vcol = dev(mesh.verts, torch.float32), dev(mesh.faces, torch.int32), dev(mesh.vcol, torch.float32)
+    v_verts, v_vcol = torch.zeros_like(V), torch.zeros_like(vcol)
+    v_c = torch.full((H, W, 3), 7.0, dtype=torch.float32, device="cuda")
+    v_d = torch.full((H, W), 7.0, dtype=torch.float32, device="cuda")
+    fid = dev(m["face_id"], torch.int32)
+    gm.gm_antialias_bwd(c, V, F, dev(adj, torch.int32), fid, dev(m["mesh_depth"], torch.float32),
+                        dev(m["mesh_rgb"], torch.float32), buf["v_cov"], buf["v_rgb"], v_md, v_c, v_d, v_verts)
+    gm.gm_interp_mesh_bwd(c, V, F, vcol, fid, v_c, v_d, v_verts, v_vcol)
+    out = dict(v_splats=host(v_splats)[:N], v_verts=host(v_verts), v_vcol=host(v_vcol), v_cov=host(buf["v_cov"]),
+               v_rgb_aa=host(buf["v_rgb"]), v_depth_aa=host(v_md), v_mesh_rgb=host(v_c), v_mesh_depth=host(v_d))
+    if v_dm is not None:
+        out["v_depth_model"] = host(v_dm)[:N]
+    return out
+
+
 def run_project(cam, g, bg=(1, 1, 1), depth_model=False):
     """GPU projection: splats, radii, tiles_touched (+ the soft split's depth
     model [N][4] when depth_model is set)."""
