@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-multiview", action="store_true", help="skip the batched 8-view measurement")
     ap.add_argument("--no-soft", action="store_true", help="skip the soft-split measurement")
+    ap.add_argument("--no-aa", action="store_true", help="skip the antialiased-mesh measurement")
     ap.add_argument("--cpu-tiles", type=int, default=48, help="tiles of the frame the CPU oracle renders")
     return ap.parse_args()
 
@@ -415,13 +416,16 @@ def run_gm(args, ws, rank, local):
     soft = None
     if not args.no_soft:
         soft = run_soft(args, scene, grads_np, flush, dist)
+    aa = None
+    if not args.no_aa:
+        aa = run_antialiased(args, scene, grads_np, flush, dist)
     multiview = None
     if not args.no_multiview:
         multiview = run_multiview(args, flush, dist)
 
     return dict(value=value, fwd=fwd_value, ms_step=ms_step, ms_fwd=ms_fwd, ms_eager=ms_eager, stages=stages, roofline=roof,
                 clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_tri=K_tri, K_g=K_g, K_pre=K_pre,
-                multiview=multiview, soft=soft,
+                multiview=multiview, soft=soft, aa=aa,
                 pairs_f=pairs_f, pairs_b=pairs_b, blend_f=blend_f, blend_b=blend_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
                 gpu_name=props.name)
 
@@ -481,6 +485,74 @@ def run_soft(args, scene, grads_np, flush, dist, softness=1.0):
     return {"softness": softness, "steps": steps, "ms_per_step": ms_step,
             "mpix_s": W * H / 1e6 / (ms_step / 1e3), "composite_fwd_ms": ms_fwd, "composite_bwd_ms": ms_bwd,
             "tile_entries": K, "overflow": overflow}
+
+
+def run_antialiased(args, scene, grads_np, flush, dist):
+    """The same workload with the analytic edge antialiasing of the mesh layer:
+    one forward + backward step (mesh gradients included) as a CUDA graph, and
+    its antialiasing-specific calls timed eagerly with events: the layer, the
+    compositing over it (front and back chains), the layer's backward and the
+    interpolation backward."""
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    cam = scene.camera
+    W, H = cam.width, cam.height
+    r = gm.HybridRenderer(cam, bg=scene.bg, antialias=True)
+    r.upload(scene.mesh, scene.gaussians)
+    g_dev = [torch.as_tensor(x).cuda() for x in grads_np]
+    r.forward(sync=True)
+    r.backward(*g_dev)
+    graph = r.capture_step(*g_dev)
+    steps = max(3, min(args.steps, 100))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 2)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+    cam_c, opts = r.cam, r.opts
+
+    def layer():
+        gm.gm_antialias(cam_c, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov, r.rgb_aa, r.depth_aa,
+                        r.tile_far, r.tile_full)
+
+    def fwd():
+        gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.depth_aa, r.rgb_aa, r.face_id,
+                                   r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib, aa=r.aa)
+
+    def bwd():
+        gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.depth_aa, r.rgb_aa, r.face_id,
+                                   r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats,
+                                   v_mesh_depth=r.v_mesh_depth, aa=r.aa)
+
+    def layer_bwd():
+        gm.gm_antialias_bwd(cam_c, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov, r.depth_aa,
+                            r.v_cov, r.v_rgb_aa, r.v_mesh_depth, r.v_mesh_rgb, r.v_interp_depth, r.v_verts)
+
+    def interp_bwd():
+        gm.gm_interp_mesh_bwd(cam_c, r.V, r.F, r.vcol, r.face_id, r.v_mesh_rgb, r.v_interp_depth, r.v_verts,
+                              r.v_vcol)
+
+    ms_step = timed(graph.replay)
+    stage = {k: timed(fn) for k, fn in (("antialias", layer), ("composite_fwd", fwd), ("composite_bwd", bwd),
+                                        ("antialias_bwd", layer_bwd), ("interp_bwd", interp_bwd))}
+    overflow = r.overflowed()
+    cov = r.cov
+    frac = int(((cov > 0) & (cov < 1)).sum().item())
+    ms_step = max_over_ranks([ms_step], dist, "cuda")[0]
+    del graph
+    return {"steps": steps, "ms_per_step": ms_step, "mpix_s": W * H / 1e6 / (ms_step / 1e3), "stages_ms": stage,
+            "fractional_px": frac, "overflow": overflow}
 
 
 def run_multiview(args, flush, dist):
@@ -696,7 +768,7 @@ def main():
                        res["K_pre"], "pairs_evaluated_fwd": res["pairs_f"], "pairs_composited_fwd": res["blend_f"],
                        "pairs_evaluated_bwd": res["pairs_b"], "pairs_composited_bwd": res["blend_b"]},
             "overflow": res["overflow"], "gpu": res["gpu_name"], "wall_s_timed": res["wall"],
-            "multiview": res["multiview"], "soft_split": res["soft"],
+            "multiview": res["multiview"], "soft_split": res["soft"], "antialias": res["aa"],
         }
         print(json.dumps(line))
     if dist is not None:

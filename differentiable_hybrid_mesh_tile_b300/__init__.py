@@ -76,7 +76,7 @@ _SIGS = {
     "gm_mesh_edges_workspace_size": (C.c_size_t, [_I32]),
     "gm_mesh_edges": (C.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, C.c_size_t, _VP]),
     "gm_antialias": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 10),
-    "gm_antialias_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 11),
+    "gm_antialias_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 13),
     "gm_interp_mesh_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 7),
     "gm_bin_triangles_noalloc": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP]),
     "gm_last_error": (C.c_char_p, []),
@@ -301,10 +301,11 @@ def gm_antialias(cam: gm_camera, V, F, adj, face_id, mesh_depth, mesh_rgb, cov, 
                               _p(depth_aa, F32), _p(tile_far, F32), _p(tile_full, U8), _stream()), "gm_antialias")
 
 
-def gm_antialias_bwd(cam: gm_camera, V, F, adj, face_id, mesh_depth, mesh_rgb, v_cov, v_rgb_aa, v_depth_aa,
-                     v_mesh_rgb, v_mesh_depth, v_verts):
+def gm_antialias_bwd(cam: gm_camera, V, F, adj, face_id, mesh_depth, mesh_rgb, cov, depth_aa, v_cov, v_rgb_aa,
+                     v_depth_aa, v_mesh_rgb, v_mesh_depth, v_verts):
     _check(lib().gm_antialias_bwd(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(adj, I32),
-                                  _p(face_id, I32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(v_cov, F32),
+                                  _p(face_id, I32), _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(cov, F32),
+                                  _p(depth_aa, F32), _p(v_cov, F32),
                                   _p(v_rgb_aa, F32), _p(v_depth_aa, F32), _p(v_mesh_rgb, F32), _p(v_mesh_depth, F32),
                                   _p(v_verts, F32), _stream()), "gm_antialias_bwd")
 
@@ -566,8 +567,9 @@ class HybridRenderer:
             self._ensure_mesh_grads()
             self.v_verts.zero_()
             self.v_vcol.zero_()
-            gm_antialias_bwd(cam, self.V, self.F, self.adj, self.face_id, self.mesh_depth, self.mesh_rgb, self.v_cov,
-                             self.v_rgb_aa, self.v_mesh_depth, self.v_mesh_rgb, self.v_interp_depth, self.v_verts)
+            gm_antialias_bwd(cam, self.V, self.F, self.adj, self.face_id, self.mesh_depth, self.mesh_rgb, self.cov,
+                             self.depth_aa, self.v_cov, self.v_rgb_aa, self.v_mesh_depth, self.v_mesh_rgb,
+                             self.v_interp_depth, self.v_verts)
             gm_interp_mesh_bwd(cam, self.V, self.F, self.vcol, self.face_id, self.v_mesh_rgb, self.v_interp_depth,
                                self.v_verts, self.v_vcol)
             return self.v_splats, self.v_verts, self.v_vcol
@@ -766,8 +768,9 @@ class MultiViewRenderer:
                                             r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
                                             depth_model=r.depth_model, v_depth_model=r.v_depth_model,
                                             v_mesh_depth=r.v_mesh_depth, aa=r.aa)
-                    gm_antialias_bwd(r.cam, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.v_cov,
-                                     r.v_rgb_aa, r.v_mesh_depth, r.v_mesh_rgb, r.v_interp_depth, self.v_verts)
+                    gm_antialias_bwd(r.cam, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov,
+                                     r.depth_aa, r.v_cov, r.v_rgb_aa, r.v_mesh_depth, r.v_mesh_rgb, r.v_interp_depth,
+                                     self.v_verts)
                     gm_interp_mesh_bwd(r.cam, r.V, r.F, r.vcol, r.face_id, r.v_mesh_rgb, r.v_interp_depth,
                                        self.v_verts, self.v_vcol)
                     continue

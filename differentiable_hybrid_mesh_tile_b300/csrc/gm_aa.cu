@@ -13,8 +13,10 @@
 // internal edge, the axis of the edge, the side of the crossing) is taken in
 // fp32 with the rasterizer's own correctly rounded operations, so it is the
 // one any IEEE evaluation of the same formulas takes; the crossing t itself is
-// evaluated in fp64 (few pixel pairs reach it), free of the cancellation that
-// fp32 screen coordinates of the order of a thousand pixels would bring.
+// evaluated in double-float arithmetic (about 48 significant bits from pairs of
+// fp32 values; fp64 runs at a small fraction of the fp32 rate on this GPU),
+// free of the cancellation that fp32 screen coordinates of the order of a
+// thousand pixels would bring.
 #include "gm_internal.cuh"
 
 namespace gm {
@@ -73,23 +75,78 @@ __device__ __forceinline__ bool vtx_f32(const Cam& c, const float* __restrict__ 
     return true;
 }
 
-// camera-space position and screen position of vertex vid in fp64
-__device__ __forceinline__ void vtx_f64(const Cam& c, const float* __restrict__ V, int vid, double xc[3], double& u,
-                                        double& v)
+// Double-float arithmetic: a value is hi + lo with |lo| <= ulp(hi) / 2, built on
+// the error-free transformations two-sum (Knuth: a + b = s + e exactly) and
+// two-product (Dekker's, here with a fused multiply-add: a b = p + e exactly).
+struct DF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b)
 {
-    const double X = __ldg(V + 3 * (int64_t)vid), Y = __ldg(V + 3 * (int64_t)vid + 1), Z = __ldg(V + 3 * (int64_t)vid + 2);
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-        xc[r] = __dadd_rn(__dadd_rn(__dadd_rn(__dmul_rn((double)c.R[3 * r], X), __dmul_rn((double)c.R[3 * r + 1], Y)),
-                                    __dmul_rn((double)c.R[3 * r + 2], Z)),
-                          (double)c.t[r]);
-    u = __dadd_rn(__ddiv_rn(__dmul_rn((double)c.fx, xc[0]), xc[2]), (double)c.cx);
-    v = __dadd_rn(__ddiv_rn(__dmul_rn((double)c.fy, xc[1]), xc[2]), (double)c.cy);
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
 }
 
-__device__ __forceinline__ double edge64(double ua, double va, double ub, double vb, double px, double py)
+__device__ __forceinline__ DF fast_two_sum(float a, float b)  // |a| >= |b|
 {
-    return __dsub_rn(__dmul_rn(__dsub_rn(ub, ua), __dsub_rn(py, va)), __dmul_rn(__dsub_rn(vb, va), __dsub_rn(px, ua)));
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ DF two_prod(float a, float b)
+{
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b)
+{
+    DF s = two_sum(a.hi, b.hi);
+    const DF t = two_sum(a.lo, b.lo);
+    s = fast_two_sum(s.hi, __fadd_rn(s.lo, t.hi));
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, t.lo));
+}
+
+__device__ __forceinline__ DF df_neg(DF a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ DF df_sub(DF a, DF b) { return df_add(a, df_neg(b)); }
+
+__device__ __forceinline__ DF df_mul(DF a, DF b)
+{
+    DF p = two_prod(a.hi, b.hi);
+    return fast_two_sum(p.hi, __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo)));
+}
+
+// a / b: a correctly rounded fp32 quotient refined twice by the exact remainder
+__device__ __forceinline__ DF df_div(DF a, DF b)
+{
+    const float q1 = __fdiv_rn(a.hi, b.hi);
+    DF r = df_sub(a, df_mul(b, DF{q1, 0.0f}));
+    const float q2 = __fdiv_rn(r.hi, b.hi);
+    r = df_sub(r, df_mul(b, DF{q2, 0.0f}));
+    const float q3 = __fdiv_rn(r.hi, b.hi);
+    return df_add(fast_two_sum(q1, q2), DF{q3, 0.0f});
+}
+
+// screen position of vertex vid in double-float (the vertex and camera are fp32)
+__device__ __forceinline__ void vtx_df(const Cam& c, const float* __restrict__ V, int vid, DF& u, DF& v)
+{
+    const float X = __ldg(V + 3 * (int64_t)vid), Y = __ldg(V + 3 * (int64_t)vid + 1), Z = __ldg(V + 3 * (int64_t)vid + 2);
+    DF xc[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+        xc[r] = df_add(df_add(df_add(two_prod(c.R[3 * r], X), two_prod(c.R[3 * r + 1], Y)), two_prod(c.R[3 * r + 2], Z)),
+                       DF{c.t[r], 0.0f});
+    u = df_add(df_div(df_mul(DF{c.fx, 0.0f}, xc[0]), xc[2]), DF{c.cx, 0.0f});
+    v = df_add(df_div(df_mul(DF{c.fy, 0.0f}, xc[1]), xc[2]), DF{c.cy, 0.0f});
+}
+
+// e(a -> b, p) = (ub - ua)(py - va) - (vb - va)(px - ua)
+__device__ __forceinline__ DF edge_df(DF ua, DF va, DF ub, DF vb, float px, float py)
+{
+    return df_sub(df_mul(df_sub(ub, ua), df_sub(DF{py, 0.0f}, va)), df_mul(df_sub(vb, va), df_sub(DF{px, 0.0f}, ua)));
 }
 
 struct Mesh {
@@ -104,7 +161,8 @@ struct Mesh {
 
 struct PairHit {
     int64_t occ, other;  // the occluder's pixel and the other one
-    double t;            // crossing, from the occluder's centre (0) to the other's (1)
+    float t;             // crossing, from the occluder's centre (0) to the other's (1)
+    float eo, en;        // the silhouette edge's function at the two centres (t = eo / (eo - en))
     int face, k;         // the silhouette edge: edge k (corners k+1, k+2) of this face
     bool far_side;       // t >= 0.5 (fp32 decision): the weight falls on the other pixel
 };
@@ -178,16 +236,17 @@ __device__ bool aa_pair(const Cam& c, const Mesh& m, int64_t pp, int64_t pq, Pai
     const int a = (exit_k + 1) % 3, b = (exit_k + 2) % 3;
     const float du = __fsub_rn(u[b], u[a]), dv = __fsub_rn(v[b], v[a]);
     if ((oj == nj) != (fabsf(dv) > fabsf(du))) return false;
-    double xc[3], ua, va, ub, vb;
-    vtx_f64(c, m.V, __ldg(m.F + 3 * (int64_t)X + a), xc, ua, va);
-    vtx_f64(c, m.V, __ldg(m.F + 3 * (int64_t)X + b), xc, ub, vb);
-    const double eo = edge64(ua, va, ub, vb, (double)ox, (double)oy);
-    const double en = edge64(ua, va, ub, vb, (double)nx, (double)ny);
-    double t = __ddiv_rn(eo, __dsub_rn(eo, en));
-    t = t < 0.0 ? 0.0 : (t > 1.0 ? 1.0 : t);
+    DF ua, va, ub, vb;
+    vtx_df(c, m.V, __ldg(m.F + 3 * (int64_t)X + a), ua, va);
+    vtx_df(c, m.V, __ldg(m.F + 3 * (int64_t)X + b), ub, vb);
+    const DF eo = edge_df(ua, va, ub, vb, ox, oy);
+    const DF en = edge_df(ua, va, ub, vb, nx, ny);
+    const float t = df_div(eo, df_sub(eo, en)).hi;
     h.occ = o;
     h.other = nb;
-    h.t = t;
+    h.t = t < 0.0f ? 0.0f : (t > 1.0f ? 1.0f : t);
+    h.eo = eo.hi;
+    h.en = en.hi;
     h.face = X;
     h.k = exit_k;
     h.far_side = best >= 0.5f;
@@ -227,7 +286,7 @@ __device__ float aa_layer(const Cam& c, const Mesh& m, int i, int j, float M[3],
         if (!aa_pair(c, m, pp, pq, h)) continue;
         const bool onto_me = h.far_side ? h.other == pp : h.occ == pp;
         if (!onto_me) continue;
-        const float w = (float)fabs(h.t - 0.5);
+        const float w = fabsf(h.t - 0.5f);
         float co[3], cn[3];
         load_rgb(m.rgb, h.occ, co);
         if (h.occ == pp) {  // the surface leaves part of this pixel
@@ -293,122 +352,131 @@ k_antialias(Cam c, Mesh m, float* __restrict__ cov, float* __restrict__ rgb_aa, 
 
 // ------------------------------------------------------------ backward ----
 
-// dL/d(screen positions of the edge's ends) -> dL/d world positions, added
-__device__ void scatter_vertex_grad(const Cam& c, const float* __restrict__ V, int vid, double gu, double gv,
+// dL/d(screen position of a vertex) -> dL/d its world position, added
+__device__ void scatter_vertex_grad(const Cam& c, const float* __restrict__ V, int vid, float gu, float gv,
                                     float* __restrict__ v_verts)
 {
-    double xc[3], u, v;
-    vtx_f64(c, V, vid, xc, u, v);
-    const double iz = 1.0 / xc[2];
-    const double gx = gu * (double)c.fx * iz, gy = gv * (double)c.fy * iz;
-    const double gz = -(gu * (u - (double)c.cx) + gv * (v - (double)c.cy)) * iz;
+    const float X = __ldg(V + 3 * (int64_t)vid), Y = __ldg(V + 3 * (int64_t)vid + 1), Z = __ldg(V + 3 * (int64_t)vid + 2);
+    const float x = fmaf(c.R[0], X, fmaf(c.R[1], Y, fmaf(c.R[2], Z, c.t[0])));
+    const float y = fmaf(c.R[3], X, fmaf(c.R[4], Y, fmaf(c.R[5], Z, c.t[1])));
+    const float z = fmaf(c.R[6], X, fmaf(c.R[7], Y, fmaf(c.R[8], Z, c.t[2])));
+    const float iz = 1.0f / z;
+    // u = fx x / z + cx, v = fy y / z + cy
+    const float gx = gu * c.fx * iz, gy = gv * c.fy * iz;
+    const float gz = -(gu * c.fx * x + gv * c.fy * y) * iz * iz;
 #pragma unroll
-    for (int d = 0; d < 3; ++d) {
-        const double g = (double)c.R[d] * gx + (double)c.R[3 + d] * gy + (double)c.R[6 + d] * gz;
-        atomicAdd(v_verts + 3 * (int64_t)vid + d, (float)g);
-    }
+    for (int d = 0; d < 3; ++d)
+        atomicAdd(v_verts + 3 * (int64_t)vid + d, c.R[d] * gx + c.R[3 + d] * gy + c.R[6 + d] * gz);
 }
 
-// Per pixel: dL/d its interpolated colour and depth (through its own layer and
-// the layers of the neighbours its pairs move), and, for the pairs it owns
-// (right and down neighbour), dL/d the silhouette vertices through the
-// crossing t.  Weights that fall on a pixel whose coverage left [0, 1] carry
-// no coverage gradient (the clamp).
-__global__ void __launch_bounds__(TILE_PIX)
-k_antialias_bwd(Cam c, Mesh m, const float* __restrict__ v_cov, const float* __restrict__ v_rgb_aa,
-                const float* __restrict__ v_depth_aa, float* __restrict__ v_mesh_rgb, float* __restrict__ v_mesh_depth,
-                float* __restrict__ v_verts)
+// Per pixel, the terms of its own layer: M0 = a0 c (dL/dc += a0 dL/dM) and, where
+// the mesh covers the pixel, D_aa = D.  Written; the pair kernel then adds.
+__global__ void __launch_bounds__(256)
+k_aa_bwd_own(int64_t P, const int32_t* __restrict__ face_id, const float* __restrict__ v_rgb_aa,
+             const float* __restrict__ v_depth_aa, float* __restrict__ v_mesh_rgb, float* __restrict__ v_mesh_depth)
 {
-    const int tile = blockIdx.x;
-    const int tx = tile % c.TW, ty = tile / c.TW;
-    const int i = tx * TILE + (threadIdx.x & (TILE - 1));
-    const int j = ty * TILE + (threadIdx.x >> 4);
-    if (i >= c.W || j >= c.H) return;
-    const int64_t pp = (int64_t)j * c.W + i;
-    const bool cov = m.face_id[pp] >= 0;
-    const float a0 = cov ? 1.0f : 0.0f;
-    float vc[3], vM[3];
-    load_rgb(v_rgb_aa, pp, vM);
+    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= P) return;
+    const bool cov = face_id[p] >= 0;
 #pragma unroll
-    for (int ch = 0; ch < 3; ++ch) vc[ch] = a0 * vM[ch];
-    float vD = cov ? v_depth_aa[pp] : 0.0f;
-    const int di[4] = {-1, 1, 0, 0}, dj[4] = {0, 0, -1, 1};
+    for (int ch = 0; ch < 3; ++ch) v_mesh_rgb[3 * p + ch] = cov ? v_rgb_aa[3 * p + ch] : 0.0f;
+    v_mesh_depth[p] = cov ? v_depth_aa[p] : 0.0f;
+}
+
+// Each pair once, by the pixel on its left / top: the weight w moved the target's
+// layer, (a, M)(tgt) += w ((a, M)(from) - (a0, M0)(tgt)) with the surface pixel's
+// layer (1, c_o) on one side and the other pixel's (a0, a0 c) on the other.  Adds
+// dL/d the two colours (and the depth an uncovered target took from the surface
+// pixel) to the pixels' gradients, and dL/dt of the crossing to the silhouette
+// edge's vertices.  A target whose coverage sits at 0 or 1 after the clamp
+// passes no coverage gradient.
+__global__ void __launch_bounds__(256)
+k_aa_bwd_pairs(Cam c, Mesh m, const float* __restrict__ cov, const float* __restrict__ depth_aa,
+               const float* __restrict__ v_cov, const float* __restrict__ v_rgb_aa,
+               const float* __restrict__ v_depth_aa, float* __restrict__ v_mesh_rgb,
+               float* __restrict__ v_mesh_depth, float* __restrict__ v_verts)
+{
+    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= (int64_t)c.W * c.H) return;
+    const int i = (int)(p % c.W), j = (int)(p / c.W);
 #pragma unroll 1
-    for (int s = 0; s < 4; ++s) {
-        const int qi = i + di[s], qj = j + dj[s];
-        if (qi < 0 || qj < 0 || qi >= c.W || qj >= c.H) continue;
-        const int64_t pq = (int64_t)qj * c.W + qi;
-        if (m.face_id[pq] == m.face_id[pp]) continue;
+    for (int s = 0; s < 2; ++s) {
+        const int qi = i + (s == 0), qj = j + (s == 1);
+        if (qi >= c.W || qj >= c.H) continue;
+        const int64_t q = (int64_t)qj * c.W + qi;
+        if (m.face_id[q] == m.face_id[p]) continue;
         PairHit h;
-        if (!aa_pair(c, m, pp, pq, h)) continue;
+        if (!aa_pair(c, m, p, q, h)) continue;
         const int64_t tgt = h.far_side ? h.other : h.occ;
-        const float w = (float)fabs(h.t - 0.5);
-        float vMt[3];
-        load_rgb(v_rgb_aa, tgt, vMt);
-        const bool cov_o = true, cov_n = m.face_id[h.other] >= 0;
-        (void)cov_o;
-        // this pixel's colour in the moved layer
-        if (tgt == pp) {
-            const float k = h.occ == pp ? -w : -w * a0;
+        const float w = fabsf(h.t - 0.5f);
+        const bool cov_n = m.face_id[h.other] >= 0;
+        const float an = cov_n ? 1.0f : 0.0f;
+        float vM[3], co[3], cn[3];
+        load_rgb(v_rgb_aa, tgt, vM);
+        load_rgb(m.rgb, h.occ, co);
+        load_rgb(m.rgb, h.other, cn);
+        float dLdw;
+        const float at = cov[tgt];
+        const float va = (at > 0.0f && at < 1.0f) ? v_cov[tgt] : 0.0f;
+        if (tgt == h.occ) {  // (a, M)(o) += w ((a0, a0 c)(n) - (1, c_o))
 #pragma unroll
-            for (int ch = 0; ch < 3; ++ch) vc[ch] = fmaf(k, vM[ch], vc[ch]);
-        } else {
-            const float k = h.occ == pp ? w : w * a0;
-#pragma unroll
-            for (int ch = 0; ch < 3; ++ch) vc[ch] = fmaf(k, vMt[ch], vc[ch]);
-        }
-        // an uncovered neighbour that took this pixel's depth
-        if (tgt == pq && h.occ == pp && m.face_id[pq] < 0 && w > 0.0f) {
-            float Mq[3], Dq;
-            int64_t src;
-            aa_layer(c, m, qi, qj, Mq, Dq, &src);
-            if (src == pp) vD += v_depth_aa[pq];
-        }
-        // the crossing, for the pairs this pixel owns
-        if (s == 1 || s == 3) {
-            float Mt[3], Dt;
-            const float at = aa_layer(c, m, (int)(tgt % c.W), (int)(tgt / c.W), Mt, Dt, nullptr);
-            const float va = (at >= 0.0f && at <= 1.0f) ? v_cov[tgt] : 0.0f;
-            float co[3], cn[3];
-            load_rgb(m.rgb, h.occ, co);
-            load_rgb(m.rgb, h.other, cn);
-            const float an = cov_n ? 1.0f : 0.0f;
-            float dLdw;
-            if (tgt == h.occ) {  // (a, M) += w ((a0, M0)(other) - (1, c_o))
-                dLdw = va * (an - 1.0f);
-#pragma unroll
-                for (int ch = 0; ch < 3; ++ch) dLdw = fmaf(vMt[ch], an * cn[ch] - co[ch], dLdw);
-            } else {  // (a, M) += w ((1, c_o) - (a0, M0)(other))
-                dLdw = va * (1.0f - an);
-#pragma unroll
-                for (int ch = 0; ch < 3; ++ch) dLdw = fmaf(vMt[ch], co[ch] - an * cn[ch], dLdw);
+            for (int ch = 0; ch < 3; ++ch) {
+                atomicAdd(v_mesh_rgb + 3 * h.occ + ch, -w * vM[ch]);
+                if (cov_n) atomicAdd(v_mesh_rgb + 3 * h.other + ch, w * vM[ch]);
             }
-            const double dLdt = h.t >= 0.5 ? (double)dLdw : -(double)dLdw;
-            if (dLdt != 0.0 && h.t > 0.0 && h.t < 1.0) {
-                const int ka = (h.k + 1) % 3, kb = (h.k + 2) % 3;
-                const int vida = __ldg(m.F + 3 * (int64_t)h.face + ka), vidb = __ldg(m.F + 3 * (int64_t)h.face + kb);
-                double xc[3], ua, va_, ub, vb;
-                vtx_f64(c, m.V, vida, xc, ua, va_);
-                vtx_f64(c, m.V, vidb, xc, ub, vb);
-                const double ox = (double)(h.occ % c.W) + 0.5, oy = (double)(h.occ / c.W) + 0.5;
-                const double nx = (double)(h.other % c.W) + 0.5, ny = (double)(h.other / c.W) + 0.5;
-                const double eo = edge64(ua, va_, ub, vb, ox, oy), en = edge64(ua, va_, ub, vb, nx, ny);
-                const double den = (eo - en) * (eo - en);
-                const double geo = dLdt * (-en / den), gen = dLdt * (eo / den);
-                // e(p) = (ub - ua)(py - va) - (vb - va)(px - ua)
-                const double gua = geo * (vb - oy) + gen * (vb - ny);
-                const double gub = geo * (oy - va_) + gen * (ny - va_);
-                const double gva = geo * (ox - ub) + gen * (nx - ub);
-                const double gvb = geo * (ua - ox) + gen * (ua - nx);
-                scatter_vertex_grad(c, m.V, vida, gua, gva, v_verts);
-                scatter_vertex_grad(c, m.V, vidb, gub, gvb, v_verts);
+            dLdw = va * (an - 1.0f);
+#pragma unroll
+            for (int ch = 0; ch < 3; ++ch) dLdw = fmaf(vM[ch], an * cn[ch] - co[ch], dLdw);
+        } else {  // (a, M)(n) += w ((1, c_o) - (a0, a0 c)(n))
+#pragma unroll
+            for (int ch = 0; ch < 3; ++ch) {
+                atomicAdd(v_mesh_rgb + 3 * h.occ + ch, w * vM[ch]);
+                if (cov_n) atomicAdd(v_mesh_rgb + 3 * h.other + ch, -w * vM[ch]);
             }
+            dLdw = va * (1.0f - an);
+#pragma unroll
+            for (int ch = 0; ch < 3; ++ch) dLdw = fmaf(vM[ch], co[ch] - an * cn[ch], dLdw);
+            // an uncovered pixel takes the depth of the first (left, right, up, down)
+            // of its nearest reaching surface pixels
+            const float Do = m.depth[h.occ];
+            if (!cov_n && w > 0.0f && __float_as_uint(depth_aa[tgt]) == __float_as_uint(Do)) {
+                const int ti = (int)(tgt % c.W), tj = (int)(tgt / c.W);
+                const int di[4] = {-1, 1, 0, 0}, dj[4] = {0, 0, -1, 1};
+                bool first = true;
+                for (int r = 0; r < 4; ++r) {
+                    const int ri = ti + di[r], rj = tj + dj[r];
+                    if (ri < 0 || rj < 0 || ri >= c.W || rj >= c.H) continue;
+                    const int64_t pr = (int64_t)rj * c.W + ri;
+                    if (pr == h.occ) break;
+                    if (m.face_id[pr] < 0 || __float_as_uint(m.depth[pr]) != __float_as_uint(Do)) continue;
+                    PairHit h2;  // an earlier neighbour at the same depth: does it reach the pixel?
+                    if (aa_pair(c, m, tgt, pr, h2) && h2.occ == pr && h2.far_side && fabsf(h2.t - 0.5f) > 0.0f) {
+                        first = false;
+                        break;
+                    }
+                }
+                if (first) atomicAdd(v_mesh_depth + h.occ, v_depth_aa[tgt]);
+            }
+        }
+        // through the crossing: t = eo / (eo - en), w = |t - 0.5|
+        const float dLdt = h.t >= 0.5f ? dLdw : -dLdw;
+        if (dLdt != 0.0f && h.t > 0.0f && h.t < 1.0f) {
+            const int ka = (h.k + 1) % 3, kb = (h.k + 2) % 3;
+            const int vida = __ldg(m.F + 3 * (int64_t)h.face + ka), vidb = __ldg(m.F + 3 * (int64_t)h.face + kb);
+            float ua, va_, ub, vb;
+            vtx_f32(c, m.V, m.nV, vida, ua, va_);
+            vtx_f32(c, m.V, m.nV, vidb, ub, vb);
+            const float ox = (float)(h.occ % c.W) + 0.5f, oy = (float)(h.occ / c.W) + 0.5f;
+            const float nx = (float)(h.other % c.W) + 0.5f, ny = (float)(h.other / c.W) + 0.5f;
+            const float d = h.eo - h.en;
+            const float geo = dLdt * (-h.en / (d * d)), gen = dLdt * (h.eo / (d * d));
+            // e(p) = (ub - ua)(py - va) - (vb - va)(px - ua)
+            scatter_vertex_grad(c, m.V, vida, geo * (vb - oy) + gen * (vb - ny), geo * (ox - ub) + gen * (nx - ub),
+                                v_verts);
+            scatter_vertex_grad(c, m.V, vidb, geo * (oy - va_) + gen * (ny - va_),
+                                geo * (ua - ox) + gen * (ua - nx), v_verts);
         }
     }
-    v_mesh_rgb[3 * pp] = vc[0];
-    v_mesh_rgb[3 * pp + 1] = vc[1];
-    v_mesh_rgb[3 * pp + 2] = vc[2];
-    v_mesh_depth[pp] = vD;
 }
 
 }  // namespace
@@ -462,13 +530,16 @@ cudaError_t antialias(const Cam& c, const float* V, int nV, const int32_t* F, in
 }
 
 cudaError_t antialias_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* adj,
-                          const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, const float* v_cov,
-                          const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb, float* v_mesh_depth,
-                          float* v_verts, cudaStream_t s)
+                          const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, const float* cov,
+                          const float* depth_aa, const float* v_cov, const float* v_rgb_aa, const float* v_depth_aa,
+                          float* v_mesh_rgb, float* v_mesh_depth, float* v_verts, cudaStream_t s)
 {
     const Mesh m{V, F, adj, face_id, mesh_depth, mesh_rgb, nV, nF};
-    k_antialias_bwd<<<c.TW * c.TH, TILE_PIX, 0, s>>>(c, m, v_cov, v_rgb_aa, v_depth_aa, v_mesh_rgb, v_mesh_depth,
-                                                      v_verts);
+    const int64_t P = (int64_t)c.W * c.H;
+    const unsigned grid = (unsigned)((P + 255) / 256);
+    k_aa_bwd_own<<<grid, 256, 0, s>>>(P, face_id, v_rgb_aa, v_depth_aa, v_mesh_rgb, v_mesh_depth);
+    k_aa_bwd_pairs<<<grid, 256, 0, s>>>(c, m, cov, depth_aa, v_cov, v_rgb_aa, v_depth_aa, v_mesh_rgb, v_mesh_depth,
+                                         v_verts);
     return cudaGetLastError();
 }
 

@@ -333,17 +333,19 @@ int gm_antialias(const gm_camera* cam, const float* V, int32_t nV, const int32_t
 
 int gm_antialias_bwd(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
                      const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
-                     const float* v_cov, const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb,
-                     float* v_mesh_depth, float* v_verts, void* stream)
+                     const float* cov, const float* depth_aa, const float* v_cov, const float* v_rgb_aa,
+                     const float* v_depth_aa, float* v_mesh_rgb, float* v_mesh_depth, float* v_verts, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
     GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
     GM_REQUIRE(nF == 0 || (V && F && adj), "V / F / adj is NULL");
-    GM_REQUIRE(face_id && mesh_depth && mesh_rgb && v_cov && v_rgb_aa && v_depth_aa, "an input is NULL");
+    GM_REQUIRE(face_id && mesh_depth && mesh_rgb && cov && depth_aa && v_cov && v_rgb_aa && v_depth_aa,
+               "an input is NULL");
     GM_REQUIRE(v_mesh_rgb && v_mesh_depth && (v_verts || nV == 0), "an output is NULL");
-    cudaError_t e = gm::antialias_bwd(gm::make_cam(*cam), V, nV, F, nF, adj, face_id, mesh_depth, mesh_rgb, v_cov,
-                                      v_rgb_aa, v_depth_aa, v_mesh_rgb, v_mesh_depth, v_verts, (cudaStream_t)stream);
+    cudaError_t e = gm::antialias_bwd(gm::make_cam(*cam), V, nV, F, nF, adj, face_id, mesh_depth, mesh_rgb, cov,
+                                      depth_aa, v_cov, v_rgb_aa, v_depth_aa, v_mesh_rgb, v_mesh_depth, v_verts,
+                                      (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_antialias_bwd");
 }
 

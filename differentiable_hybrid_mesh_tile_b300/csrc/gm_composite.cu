@@ -674,10 +674,15 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
 // depth D) the Gaussians' back parts are composited into a second chain
 // (Hybrid rendering, two-layer equation): under the hard split the Gaussians
 // at or behind D, under the soft split every Gaussian with alpha (1 - f).
-// One thread per pixel walks its tile's list (few pixels have such a layer);
-// the forward adds T_front (1 - a)(C_b + (T_b - 1) bg) to the colour the main
-// pass wrote, and the backward adds the Gaussians' gradients (global atomics)
-// and writes the layer's gradients (dL/da, dL/dM, dL/dD).
+// Such pixels are few (silhouettes), so one warp takes one tile: its lanes take
+// the tile's fractional pixels 32 at a time, and the warp stages the tile's
+// list 32 entries at a time in shared memory (one coalesced load per entry,
+// shared by every lane).  The forward adds T_front (1 - a)(C_b + (T_b - 1) bg)
+// to the colour the main pass wrote; the backward adds the Gaussians'
+// gradients (global atomics) and writes the layer's gradients (dL/da, dL/dM,
+// dL/dD).
+
+constexpr int BACK_WARPS = 4;
 
 // first list position whose Gaussian is not in front of D (the list is sorted
 // by centre depth; an invalid id counts as in front)
@@ -694,8 +699,57 @@ __device__ __forceinline__ int first_behind(const int32_t* __restrict__ gids, co
     return lo;
 }
 
+struct BackStage {
+    float4 A[32], B[32], C[32], Dm[32];
+    int g[32];
+    uint8_t frac[TILE_PIX];
+};
+
+// the tile's pixels whose layer has a back chain (0 < a < 1 and a split depth),
+// compacted into st.frac; returns their number
+__device__ __forceinline__ int gather_frac(const Cam& c, int tile, const float* __restrict__ cov,
+                                           const float* __restrict__ mesh_depth, BackStage& st, int lane)
+{
+    const int tx = tile % c.TW, ty = tile / c.TW;
+    int n = 0;
+#pragma unroll 1
+    for (int k = 0; k < TILE_PIX / 32; ++k) {
+        const int tp = k * 32 + lane;
+        const int i = tx * TILE + (tp & (TILE - 1)), j = ty * TILE + (tp >> 4);
+        bool f = false;
+        if (i < c.W && j < c.H) {
+            const int64_t pix = (int64_t)j * c.W + i;
+            f = mesh_depth[pix] < INFINITY && cov[pix] < 1.0f;
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, f);
+        if (f) st.frac[n + __popc(m & ((1u << lane) - 1))] = (uint8_t)tp;
+        n += __popc(m);
+    }
+    __syncwarp();
+    return n;
+}
+
+// stages list entries k0 .. k0 + 31 (those < kend) of the tile: lane l loads entry k0 + l
 template <bool SOFT>
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ void stage_back(const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                                           const float4* __restrict__ depth_model, int N, const Split& sp, int k0,
+                                           int kend, BackStage& st, int lane)
+{
+    __syncwarp();
+    const int k = k0 + lane;
+    int g = k < kend ? gids[k] : -1;
+    if (g < 0 || g >= N) g = -1;
+    st.g[lane] = g;
+    if (g >= 0) {
+        float4 Hh;
+        stage(splats, g, st.A[lane], st.B[lane], st.C[lane], Hh);
+        if (SOFT) st.Dm[lane] = stage_depth_model(depth_model, g, sp, st.C[lane].y);
+    }
+    __syncwarp();
+}
+
+template <bool SOFT>
+__global__ void __launch_bounds__(32 * BACK_WARPS)
 k_composite_back_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
                      const int32_t* __restrict__ gids, const float4* __restrict__ splats,
                      const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
@@ -703,149 +757,223 @@ k_composite_back_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__
                      float* __restrict__ out_depth, float* __restrict__ out_alpha, float4* __restrict__ back,
                      float* __restrict__ T_back, int32_t* __restrict__ n_back)
 {
-    const int64_t pix = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (pix >= (int64_t)c.W * c.H) return;
-    const float a = cov[pix], D = mesh_depth[pix];
-    if (!(D < INFINITY) || !(a < 1.0f)) return;
-    const int i = (int)(pix % c.W), j = (int)(pix / c.W);
-    const float px = (float)i + 0.5f, py = (float)j + 0.5f;
-    const int2 r = tile_range[(j / TILE) * c.TW + i / TILE];
-    const int start = SOFT ? r.x : first_behind(gids, splats, N, r.x, r.y, D);
-    float T = 1.0f, Cr = 0.f, Cg = 0.f, Cb = 0.f, Z = 0.f;
-    int last = 0;
-    for (int k = start; k < r.y; ++k) {
-        const int g = gids[k];
-        if (g < 0 || g >= N) continue;
-        float4 A, B, C, Hh;
-        stage(splats, g, A, B, C, Hh);
-        if (!SOFT && C.y < D) continue;
-        const Eval e = eval_splat(A, B, px, py);
-        if (e.skip) continue;
-        float part = e.alpha;
-        if (SOFT) {
-            const float4 Dm = stage_depth_model(depth_model, g, sp, C.y);
-            const float zs = fmaf(Dm.x, e.dx, fmaf(Dm.y, e.dy, C.y));
-            part = e.alpha * (1.0f - sp.front((D - zs) * Dm.z));
-            if (part < ALPHA_MIN) continue;
+    __shared__ BackStage stages[BACK_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x * BACK_WARPS + warp;
+    if (tile >= c.TW * c.TH) return;
+    BackStage& st = stages[warp];
+    const int nfrac = gather_frac(c, tile, cov, mesh_depth, st, lane);
+    const int2 r = tile_range[tile];
+    const int tx = tile % c.TW, ty = tile / c.TW;
+#pragma unroll 1
+    for (int base = 0; base < nfrac; base += 32) {
+        const bool act = base + lane < nfrac;
+        int64_t pix = 0;
+        float px = 0.f, py = 0.f, D = INFINITY;
+        if (act) {
+            const int tp = st.frac[base + lane];
+            const int i = tx * TILE + (tp & (TILE - 1)), j = ty * TILE + (tp >> 4);
+            pix = (int64_t)j * c.W + i;
+            px = (float)i + 0.5f;
+            py = (float)j + 0.5f;
+            D = mesh_depth[pix];
         }
-        const float Tn = __fmul_rn(T, __fsub_rn(1.0f, part));
-        if (Tn <= T_STOP) break;
-        const float w = part * T;
-        Cr = fmaf(w, B.z, Cr);
-        Cg = fmaf(w, B.w, Cg);
-        Cb = fmaf(w, C.x, Cb);
-        Z = fmaf(w, C.y, Z);
-        T = Tn;
-        last = k - r.x + 1;
+        float Dmin = D;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Dmin = fminf(Dmin, __shfl_xor_sync(0xffffffffu, Dmin, o));
+        const int start = SOFT ? r.x : first_behind(gids, splats, N, r.x, r.y, Dmin);
+        float T = 1.0f, Cr = 0.f, Cg = 0.f, Cb = 0.f, Z = 0.f;
+        int last = 0;
+        bool done = !act;
+#pragma unroll 1
+        for (int k0 = start; k0 < r.y; k0 += 32) {
+            if (__all_sync(0xffffffffu, done)) break;
+            stage_back<SOFT>(gids, splats, depth_model, N, sp, k0, r.y, st, lane);
+            const int n = min(32, r.y - k0);
+            for (int e = 0; e < n && !done; ++e) {
+                if (st.g[e] < 0) continue;
+                const float4 C = st.C[e];
+                if (!SOFT && C.y < D) continue;
+                const float4 B = st.B[e];
+                const Eval ev = eval_splat(st.A[e], B, px, py);
+                if (ev.skip) continue;
+                float part = ev.alpha;
+                if (SOFT) {
+                    const float4 Dm = st.Dm[e];
+                    const float zs = fmaf(Dm.x, ev.dx, fmaf(Dm.y, ev.dy, C.y));
+                    part = ev.alpha * (1.0f - sp.front((D - zs) * Dm.z));
+                    if (part < ALPHA_MIN) continue;
+                }
+                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, part));
+                if (Tn <= T_STOP) {
+                    done = true;
+                    break;
+                }
+                const float w = part * T;
+                Cr = fmaf(w, B.z, Cr);
+                Cg = fmaf(w, B.w, Cg);
+                Cb = fmaf(w, C.x, Cb);
+                Z = fmaf(w, C.y, Z);
+                T = Tn;
+                last = k0 + e - r.x + 1;
+            }
+        }
+        if (act) {
+            const float a = cov[pix];
+            back[pix] = make_float4(Cr, Cg, Cb, Z);
+            T_back[pix] = T;
+            n_back[pix] = last;
+            const float s = T_final[pix] * (1.0f - a), tm1 = T - 1.0f;
+            out_rgb[3 * pix] = fmaf(s, fmaf(tm1, bg.x, Cr), out_rgb[3 * pix]);
+            out_rgb[3 * pix + 1] = fmaf(s, fmaf(tm1, bg.y, Cg), out_rgb[3 * pix + 1]);
+            out_rgb[3 * pix + 2] = fmaf(s, fmaf(tm1, bg.z, Cb), out_rgb[3 * pix + 2]);
+            out_depth[pix] = fmaf(s, Z, out_depth[pix]);
+            out_alpha[pix] = 1.0f - s * T;
+        }
     }
-    back[pix] = make_float4(Cr, Cg, Cb, Z);
-    T_back[pix] = T;
-    n_back[pix] = last;
-    const float s = T_final[pix] * (1.0f - a), tm1 = T - 1.0f;
-    out_rgb[3 * pix] = fmaf(s, fmaf(tm1, bg.x, Cr), out_rgb[3 * pix]);
-    out_rgb[3 * pix + 1] = fmaf(s, fmaf(tm1, bg.y, Cg), out_rgb[3 * pix + 1]);
-    out_rgb[3 * pix + 2] = fmaf(s, fmaf(tm1, bg.z, Cb), out_rgb[3 * pix + 2]);
-    out_depth[pix] = fmaf(s, Z, out_depth[pix]);
-    out_alpha[pix] = 1.0f - s * T;
 }
 
+// The layer's gradients at every pixel (the antialiased layer's own terms),
+// before the back chains' gradients.
 template <bool SOFT>
 __global__ void __launch_bounds__(256)
-k_composite_back_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
-                     const int32_t* __restrict__ gids, const float4* __restrict__ splats,
-                     const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
-                     const float* __restrict__ mesh_rgb, const float* __restrict__ T_final,
-                     const float* __restrict__ g_rgb, const float* __restrict__ g_depth,
-                     const float* __restrict__ g_alpha, AaLayer aa, float* __restrict__ v_splats,
-                     float* __restrict__ v_depth_model, float* __restrict__ v_mesh_depth)
+k_layer_grad(int64_t P, float3 bg, const float* __restrict__ mesh_depth, const float* __restrict__ T_final,
+             const float* __restrict__ g_rgb, const float* __restrict__ g_depth, const float* __restrict__ g_alpha,
+             AaLayer aa, float* __restrict__ v_mesh_depth)
 {
     const int64_t pix = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (pix >= (int64_t)c.W * c.H) return;
-    const float a = aa.cov[pix], D = mesh_depth[pix], Tf = T_final[pix], ua = 1.0f - a;
+    if (pix >= P) return;
+    const float a = aa.cov[pix], D = mesh_depth[pix], Tf = T_final[pix];
     const bool has_mesh = D < INFINITY, frac = has_mesh && a < 1.0f;
-    const float gr = g_rgb[3 * pix], gg = g_rgb[3 * pix + 1], gb = g_rgb[3 * pix + 2], gz = g_depth[pix],
-                ga = g_alpha[pix];
+    const float gr = g_rgb[3 * pix], gg = g_rgb[3 * pix + 1], gb = g_rgb[3 * pix + 2], gz = g_depth[pix];
     float Tb = 1.0f, Eb = bg.x * gr + bg.y * gg + bg.z * gb;
-    float4 bk = make_float4(0.f, 0.f, 0.f, 0.f);
     if (frac) {
-        bk = aa.back[pix];
+        const float4 bk = aa.back[pix];
         Tb = aa.T_back[pix];
         Eb = fmaf(Tb, Eb, bk.x * gr + bk.y * gg + bk.z * gb + bk.w * gz);
     }
-    // the layer: rgb = C + T (M + (1 - a)(C_b + T_b bg)), depth = Z + T (a D + (1 - a) Z_b),
+    // rgb = C + T (M + (1 - a)(C_b + T_b bg)), depth = Z + T (a D + (1 - a) Z_b),
     // alpha = 1 - T (1 - a) T_b
     aa.v_rgb[3 * pix] = Tf * gr;
     aa.v_rgb[3 * pix + 1] = Tf * gg;
     aa.v_rgb[3 * pix + 2] = Tf * gb;
-    aa.v_cov[pix] = has_mesh ? Tf * (fmaf(gz, D, -Eb) + ga * Tb) : 0.0f;
-    float vD = (SOFT ? v_mesh_depth[pix] : 0.0f) + (a > 0.0f && has_mesh ? Tf * a * gz : 0.0f);
-    const int nb = frac ? aa.n_back[pix] : 0;
-    if (nb > 0) {
-        // the back chain, back to front, with the upstream gradient scaled by T (1 - a)
-        const int i = (int)(pix % c.W), j = (int)(pix / c.W);
-        const float px = (float)i + 0.5f, py = (float)j + 0.5f;
-        const int2 r = tile_range[(j / TILE) * c.TW + i / TILE];
-        const int start = SOFT ? r.x : first_behind(gids, splats, N, r.x, r.y, D);
-        const float s = Tf * ua;
-        const float hr = s * gr, hg = s * gg, hb = s * gb, hz = s * gz;
-        float T = Tb, behind = Tb * (bg.x * hr + bg.y * hg + bg.z * hb);
-        const float aterm = s * ga * Tb;
-        for (int k = min(r.x + nb, r.y) - 1; k >= start; --k) {
-            const int g = gids[k];
-            if (g < 0 || g >= N) continue;
-            float4 A, B, C, Hh;
-            stage(splats, g, A, B, C, Hh);
-            if (!SOFT && C.y < D) continue;
-            const Eval e = eval_splat(A, B, px, py);
-            if (e.skip) continue;
-            float part = e.alpha, f = 0.0f, x = 0.0f;
-            float4 Dm = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (SOFT) {
-                Dm = stage_depth_model(depth_model, g, sp, C.y);
-                const float zs = fmaf(Dm.x, e.dx, fmaf(Dm.y, e.dy, C.y));
-                x = (D - zs) * Dm.z;
-                f = sp.front(x);
-                part = e.alpha * (1.0f - f);
-                if (part < ALPHA_MIN) continue;
-            }
-            const float rom = __fdividef(1.0f, 1.0f - part);
-            const float Tp = T * rom;
-            const float w = part * Tp;
-            const float front = B.z * hr + B.w * hg + C.x * hb + C.y * hz;
-            const float dLdp = Tp * front + (aterm - behind) * rom;  // dL / d(the back part)
-            behind = fmaf(w, front, behind);
-            T = Tp;
-            // record gradient: sigma = (a dx^2 + c dy^2) / 2 + b dx dy of the record's conic
-            const float4* rec = splats + 3 * (int64_t)g;
-            const float4 s0 = rec[0], s1 = rec[1];
-            float vg[10] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, w * hr, w * hg, w * hb, w * hz};
-            const float dLdal = SOFT ? dLdp * (1.0f - f) : dLdp;
-            if (!e.clamped) {
-                const float ds = -dLdal * e.alpha;  // d alpha / d sigma = -alpha
-                vg[0] = -ds * (s0.z * e.dx + s0.w * e.dy);
-                vg[1] = -ds * (s0.w * e.dx + s1.x * e.dy);
-                vg[2] = 0.5f * ds * e.dx * e.dx;
-                vg[3] = ds * e.dx * e.dy;
-                vg[4] = 0.5f * ds * e.dy * e.dy;
-                vg[5] = dLdal * e.G;
-            }
-            if (SOFT) {  // the back part alpha (1 - f(x)): dL/dx = -dLdp alpha f'(x)
-                const float psi = -dLdp * e.alpha * sp.density(x, f);
-                const float pz = psi * Dm.z;
-                vg[0] += pz * Dm.x;
-                vg[1] += pz * Dm.y;
-                vg[9] -= pz;
-                vD += pz;
-                atomicAdd(reinterpret_cast<float4*>(v_depth_model) + g,
-                          make_float4(-pz * e.dx, -pz * e.dy, -psi * x * Dm.z * sp.softness, 0.0f));
-            }
-            float4* dst = reinterpret_cast<float4*>(v_splats + 12 * (int64_t)g);
-            atomicAdd(dst, make_float4(vg[0], vg[1], vg[2], vg[3]));
-            atomicAdd(dst + 1, make_float4(vg[4], vg[5], vg[6], vg[7]));
-            atomicAdd(dst + 2, make_float4(vg[8], vg[9], 0.0f, 0.0f));
+    aa.v_cov[pix] = has_mesh ? Tf * (fmaf(gz, D, -Eb) + g_alpha[pix] * Tb) : 0.0f;
+    v_mesh_depth[pix] = (SOFT ? v_mesh_depth[pix] : 0.0f) + (a > 0.0f && has_mesh ? Tf * a * gz : 0.0f);
+}
+
+template <bool SOFT>
+__global__ void __launch_bounds__(32 * BACK_WARPS)
+k_composite_back_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
+                     const int32_t* __restrict__ gids, const float4* __restrict__ splats,
+                     const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
+                     const float* __restrict__ T_final, const float* __restrict__ g_rgb,
+                     const float* __restrict__ g_depth, const float* __restrict__ g_alpha, AaLayer aa,
+                     float* __restrict__ v_splats, float* __restrict__ v_depth_model, float* __restrict__ v_mesh_depth)
+{
+    __shared__ BackStage stages[BACK_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x * BACK_WARPS + warp;
+    if (tile >= c.TW * c.TH) return;
+    BackStage& st = stages[warp];
+    const int nfrac = gather_frac(c, tile, aa.cov, mesh_depth, st, lane);
+    const int2 r = tile_range[tile];
+    const int tx = tile % c.TW, ty = tile / c.TW;
+#pragma unroll 1
+    for (int base = 0; base < nfrac; base += 32) {
+        const bool act = base + lane < nfrac;
+        int64_t pix = 0;
+        float px = 0.f, py = 0.f, D = INFINITY;
+        int top = -1;  // the last list position of this lane's back chain
+        float hr = 0.f, hg = 0.f, hb = 0.f, hz = 0.f, T = 1.0f, behind = 0.f, aterm = 0.f;
+        if (act) {
+            const int tp = st.frac[base + lane];
+            const int i = tx * TILE + (tp & (TILE - 1)), j = ty * TILE + (tp >> 4);
+            pix = (int64_t)j * c.W + i;
+            px = (float)i + 0.5f;
+            py = (float)j + 0.5f;
+            D = mesh_depth[pix];
+            top = r.x + aa.n_back[pix] - 1;
+            // the back chain, back to front, with the upstream gradient scaled by T (1 - a)
+            const float s = T_final[pix] * (1.0f - aa.cov[pix]);
+            hr = s * g_rgb[3 * pix];
+            hg = s * g_rgb[3 * pix + 1];
+            hb = s * g_rgb[3 * pix + 2];
+            hz = s * g_depth[pix];
+            T = aa.T_back[pix];
+            behind = T * (bg.x * hr + bg.y * hg + bg.z * hb);
+            aterm = s * g_alpha[pix] * T;
         }
+        float Dmin = D;
+        int tmax = top;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            Dmin = fminf(Dmin, __shfl_xor_sync(0xffffffffu, Dmin, o));
+            tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+        }
+        const int start = SOFT ? r.x : first_behind(gids, splats, N, r.x, r.y, Dmin);
+        float vD = 0.0f;
+#pragma unroll 1
+        for (int k1 = min(tmax, r.y - 1); k1 >= start; k1 -= 32) {
+            const int k0 = max(start, k1 - 31);
+            stage_back<SOFT>(gids, splats, depth_model, N, sp, k0, k1 + 1, st, lane);
+            for (int e = k1 - k0; e >= 0; --e) {
+                const int k = k0 + e;
+                if (k > top || st.g[e] < 0) continue;
+                const float4 C = st.C[e];
+                if (!SOFT && C.y < D) continue;
+                const float4 A = st.A[e], B = st.B[e];
+                const Eval ev = eval_splat(A, B, px, py);
+                if (ev.skip) continue;
+                float part = ev.alpha, f = 0.0f, x = 0.0f;
+                float4 Dm = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (SOFT) {
+                    Dm = st.Dm[e];
+                    const float zs = fmaf(Dm.x, ev.dx, fmaf(Dm.y, ev.dy, C.y));
+                    x = (D - zs) * Dm.z;
+                    f = sp.front(x);
+                    part = ev.alpha * (1.0f - f);
+                    if (part < ALPHA_MIN) continue;
+                }
+                const float rom = __fdividef(1.0f, 1.0f - part);
+                const float Tp = T * rom;
+                const float w = part * Tp;
+                const float front = B.z * hr + B.w * hg + C.x * hb + C.y * hz;
+                const float dLdp = Tp * front + (aterm - behind) * rom;  // dL / d(the back part)
+                behind = fmaf(w, front, behind);
+                T = Tp;
+                // record gradient: sigma = (a dx^2 + c dy^2) / 2 + b dx dy of the record's conic
+                const int g = st.g[e];
+                const float4* rec = splats + 3 * (int64_t)g;
+                const float4 s0 = rec[0], s1 = rec[1];
+                float vg[10] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, w * hr, w * hg, w * hb, w * hz};
+                const float dLdal = SOFT ? dLdp * (1.0f - f) : dLdp;
+                if (!ev.clamped) {
+                    const float ds = -dLdal * ev.alpha;  // d alpha / d sigma = -alpha
+                    vg[0] = -ds * (s0.z * ev.dx + s0.w * ev.dy);
+                    vg[1] = -ds * (s0.w * ev.dx + s1.x * ev.dy);
+                    vg[2] = 0.5f * ds * ev.dx * ev.dx;
+                    vg[3] = ds * ev.dx * ev.dy;
+                    vg[4] = 0.5f * ds * ev.dy * ev.dy;
+                    vg[5] = dLdal * ev.G;
+                }
+                if (SOFT) {  // the back part alpha (1 - f(x)): dL/dx = -dLdp alpha f'(x)
+                    const float psi = -dLdp * ev.alpha * sp.density(x, f);
+                    const float pz = psi * Dm.z;
+                    vg[0] += pz * Dm.x;
+                    vg[1] += pz * Dm.y;
+                    vg[9] -= pz;
+                    vD += pz;
+                    atomicAdd(reinterpret_cast<float4*>(v_depth_model) + g,
+                              make_float4(-pz * ev.dx, -pz * ev.dy, -psi * x * Dm.z * sp.softness, 0.0f));
+                }
+                float4* dst = reinterpret_cast<float4*>(v_splats + 12 * (int64_t)g);
+                atomicAdd(dst, make_float4(vg[0], vg[1], vg[2], vg[3]));
+                atomicAdd(dst + 1, make_float4(vg[4], vg[5], vg[6], vg[7]));
+                atomicAdd(dst + 2, make_float4(vg[8], vg[9], 0.0f, 0.0f));
+            }
+        }
+        if (act && SOFT) v_mesh_depth[pix] += vD;
     }
-    v_mesh_depth[pix] = vD;
 }
 
 }  // namespace
@@ -869,7 +997,9 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness
     const int64_t P = (int64_t)c.W * c.H;
     const unsigned grid = (unsigned)((P + 255) / 256);
     auto back = soft ? k_composite_back_fwd<true> : k_composite_back_fwd<false>;
-    back<<<grid, 256, 0, s>>>(c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1},
+    const unsigned tgrid = (unsigned)((c.TW * c.TH + BACK_WARPS - 1) / BACK_WARPS);
+    (void)grid;
+    back<<<tgrid, 32 * BACK_WARPS, 0, s>>>(c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1},
                               reinterpret_cast<const int2*>(tile_range), gids, reinterpret_cast<const float4*>(splats),
                               reinterpret_cast<const float4*>(depth_model), mesh_depth, aa.cov, T_final, out_rgb,
                               out_depth, out_alpha, aa.back, aa.T_back, aa.n_back);
@@ -896,11 +1026,16 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
     if (e != cudaSuccess || !aa.cov) return e;
     const int64_t P = (int64_t)c.W * c.H;
     const unsigned grid = (unsigned)((P + 255) / 256);
+    auto lg = soft ? k_layer_grad<true> : k_layer_grad<false>;
+    lg<<<grid, 256, 0, s>>>(P, make_float3(bg[0], bg[1], bg[2]), mesh_depth, T_final, g_rgb, g_depth, g_alpha, aa,
+                            v_mesh_depth);
     auto back = soft ? k_composite_back_bwd<true> : k_composite_back_bwd<false>;
-    back<<<grid, 256, 0, s>>>(c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1},
-                              reinterpret_cast<const int2*>(tile_range), gids, reinterpret_cast<const float4*>(splats),
-                              reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb, T_final, g_rgb,
-                              g_depth, g_alpha, aa, v_splats, v_depth_model, v_mesh_depth);
+    const unsigned tgrid = (unsigned)((c.TW * c.TH + BACK_WARPS - 1) / BACK_WARPS);
+    back<<<tgrid, 32 * BACK_WARPS, 0, s>>>(c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1},
+                                           reinterpret_cast<const int2*>(tile_range), gids,
+                                           reinterpret_cast<const float4*>(splats),
+                                           reinterpret_cast<const float4*>(depth_model), mesh_depth, T_final, g_rgb,
+                                           g_depth, g_alpha, aa, v_splats, v_depth_model, v_mesh_depth);
     return cudaGetLastError();
 }
 

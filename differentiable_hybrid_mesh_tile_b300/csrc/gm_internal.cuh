@@ -224,9 +224,9 @@ cudaError_t antialias(const Cam& c, const float* V, int nV, const int32_t* F, in
                       const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, float* cov,
                       float* rgb_aa, float* depth_aa, float* tile_far, uint8_t* tile_full, cudaStream_t s);
 cudaError_t antialias_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* adj,
-                          const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, const float* v_cov,
-                          const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb, float* v_mesh_depth,
-                          float* v_verts, cudaStream_t s);
+                          const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb, const float* cov,
+                          const float* depth_aa, const float* v_cov, const float* v_rgb_aa, const float* v_depth_aa,
+                          float* v_mesh_rgb, float* v_mesh_depth, float* v_verts, cudaStream_t s);
 cudaError_t interp_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,
                        const int32_t* face_id, const float* v_mesh_rgb, const float* v_mesh_depth, float* v_verts,
                        float* v_vcol, cudaStream_t s);

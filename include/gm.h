@@ -5,17 +5,22 @@
  *
  * The method is the hybrid renderer of "A Lightweight and Differentiable
  * Renderer for Joint Mesh and 3D Gaussian Splat Scenes" (Design Details:
- * Mesh rasterizer items 1-2, Hybrid rendering), restricted to a hard depth
- * test between each Gaussian and the mesh and a fully opaque, non-antialiased
- * mesh layer.  The renderer's call (rgb, depth, alpha from a mesh, Gaussians
- * and a camera pose) is split into seven steps; a forward pass is
+ * Mesh rasterizer items 1-3, Hybrid rendering).  By default each Gaussian is
+ * depth-tested against the mesh (hard split) and the mesh layer is opaque and
+ * not antialiased; options add the soft split at the mesh surface
+ * (gm_opts.softness) and analytic edge antialiasing (gm_antialias and the
+ * gm_aa_layer argument).  The renderer's call (rgb, depth, alpha from a mesh,
+ * Gaussians and a camera pose) is split into seven steps; a forward pass is
  *
  *   gm_bin_triangles -> gm_zbuffer -> gm_interp_mesh          (mesh layer)
+ *     [-> gm_antialias, with gm_mesh_edges once per mesh]
  *   gm_project_gaussians -> gm_bin_sort_gaussians             (Gaussians)
  *   gm_composite_hybrid_fwd                                   (image)
  *
  * and gm_composite_hybrid_bwd returns the gradients of a loss with respect to
- * the projected Gaussians and to the mesh's vertex positions and colours.
+ * the projected Gaussians and to the mesh's vertex positions and colours
+ * (with antialiasing through gm_antialias_bwd and gm_interp_mesh_bwd);
+ * gm_project_gaussians_bwd carries the Gaussians' to their 3D parameters.
  *
  * Conventions shared by every call
  *   - Camera: pinhole, world -> camera  X_c = R X_w + t  (R row-major),
@@ -205,7 +210,7 @@ int gm_mesh_edges(const int32_t* F, int32_t nF, int32_t nV, int32_t* adj, int32_
  *   largest split depth) / tile_full (every pixel has a = 1), which replace
  *   those of gm_interp_mesh for the occlusion cull.
  *   Decisions are taken in fp32 with the z-buffer's operations; the crossing
- *   t in fp64.
+ *   t in double-float arithmetic (pairs of fp32 values, ~48 bits).
  * ---------------------------------------------------------------------- */
 int gm_antialias(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
                  const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
@@ -214,7 +219,8 @@ int gm_antialias(const gm_camera* cam, const float* V, int32_t nV, const int32_t
 /* ------------------------------------------------------------------------
  * gm_antialias_bwd -- gradients of gm_antialias: from dL/d(cov, rgb_aa,
  * depth_aa) (v_cov, v_rgb_aa, v_depth_aa [H][W], [H][W][3], [H][W], e.g. the
- * layer gradients of gm_composite_hybrid_bwd) to
+ * layer gradients of gm_composite_hybrid_bwd), given the forward call's cov
+ * and depth_aa, to
  *   v_mesh_rgb [H][W][3], v_mesh_depth [H][W] (written): dL/d the
  *   interpolated colour and depth of each pixel, for gm_interp_mesh_bwd;
  *   v_verts [nV][3] (+=): dL/d the world positions of the silhouette edges'
@@ -224,8 +230,8 @@ int gm_antialias(const gm_camera* cam, const float* V, int32_t nV, const int32_t
  * ---------------------------------------------------------------------- */
 int gm_antialias_bwd(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
                      const int32_t* adj, const int32_t* face_id, const float* mesh_depth, const float* mesh_rgb,
-                     const float* v_cov, const float* v_rgb_aa, const float* v_depth_aa, float* v_mesh_rgb,
-                     float* v_mesh_depth, float* v_verts, void* stream);
+                     const float* cov, const float* depth_aa, const float* v_cov, const float* v_rgb_aa,
+                     const float* v_depth_aa, float* v_mesh_rgb, float* v_mesh_depth, float* v_verts, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_interp_mesh_bwd -- backward of gm_interp_mesh for given per-pixel

@@ -123,6 +123,7 @@ def run_composite_aa(cam, bg, tile_range, gids, splats, aa, softness=0.0, depth_
     res["_dev"] = dict(T=out["T"], n_contrib=nc)
     res["_soft"] = (softness, dm, soft_split)
     res["_aa"] = (layer, buf)
+    res["_depth_aa"] = args[3]
     return res
 
 
@@ -147,7 +148,8 @@ def run_backward_aa(cam, bg, fwd, grads, N, mesh, m, adj):
     v_d = torch.full((H, W), 7.0, dtype=torch.float32, device="cuda")
     fid = dev(m["face_id"], torch.int32)
     gm.gm_antialias_bwd(c, V, F, dev(adj, torch.int32), fid, dev(m["mesh_depth"], torch.float32),
-                        dev(m["mesh_rgb"], torch.float32), buf["v_cov"], buf["v_rgb"], v_md, v_c, v_d, v_verts)
+                        dev(m["mesh_rgb"], torch.float32), buf["cov"], fwd["_depth_aa"], buf["v_cov"], buf["v_rgb"],
+                        v_md, v_c, v_d, v_verts)
     gm.gm_interp_mesh_bwd(c, V, F, vcol, fid, v_c, v_d, v_verts, v_vcol)
     out = dict(v_splats=host(v_splats)[:N], v_verts=host(v_verts), v_vcol=host(v_vcol), v_cov=host(buf["v_cov"]),
                v_rgb_aa=host(buf["v_rgb"]), v_depth_aa=host(v_md), v_mesh_rgb=host(v_c), v_mesh_depth=host(v_d))
