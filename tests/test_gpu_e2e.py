@@ -217,3 +217,101 @@ def test_graph_replay_matches_eager():
     # gradients accumulate with float atomics in a run-dependent order
     for a, b in zip(v, (r.v_splats, r.v_verts, r.v_vcol)):
         torch.testing.assert_close(a, b, rtol=1e-4, atol=5e-5)
+
+
+@pytest.mark.parametrize("softness,antialias", [(1.0, False), (0.0, True), (1.0, True)],
+                         ids=["soft", "antialias", "soft_antialias"])
+def test_full_size_options(softness, antialias, orc):
+    """The 1080p frame with the soft split and / or the antialiased mesh layer, as
+    the benchmark renders it (HybridRenderer, its bins and launch configuration):
+    the layer against the oracle's on the GPU's own face ids, depths and colours,
+    and on 24 seeded tiles the composite against the oracle's on the GPU's
+    projected Gaussians and layer; then 40 Gaussians x 10 record fields (and, with
+    the layer, 12 silhouette vertices) against central finite differences."""
+    H.need_gpu()
+    scene = get_scene("soup_1080p")
+    cam = scene.camera
+    r = gm.HybridRenderer(cam, bg=scene.bg, softness=softness, antialias=antialias)
+    r.upload(scene.mesh, scene.gaussians)
+    r.forward(sync=True)
+    torch.cuda.synchronize()
+    fid, md, mrgb = r.face_id.cpu().numpy(), r.mesh_depth.cpu().numpy(), r.mesh_rgb.cpu().numpy()
+    sp, rad = r.splats.cpu().numpy(), r.radii.cpu().numpy()
+    dm = r.depth_model.cpu().numpy() if softness > 0 else None
+    T = orc.n_tiles(cam)
+    tiles = scenes.sample_tiles(41, T, 24)
+    pix = _tile_pixels(cam, tiles)
+    if antialias:
+        cov, rgb_aa, depth_aa, _ = orc.antialias(cam, scene.mesh.verts, scene.mesh.faces, r.adj.cpu().numpy(), fid,
+                                                 md, mrgb)
+        np.testing.assert_allclose(r.cov.cpu().numpy(), cov, atol=2e-6, rtol=0)
+        np.testing.assert_allclose(r.rgb_aa.cpu().numpy(), rgb_aa, atol=2e-6, rtol=0)
+        np.testing.assert_array_equal(r.depth_aa.cpu().numpy(), depth_aa)
+        layer = dict(mesh_cov=r.cov.cpu().numpy())
+        lmd, lrgb = r.depth_aa.cpu().numpy(), r.rgb_aa.cpu().numpy()
+    else:
+        layer, lmd, lrgb = {}, md, mrgb
+    lists = orc.tile_lists(cam, sp, rad, tiles)
+    o = orc.composite_fwd(cam, scene.bg, sp, lists, lmd, lrgb, fid, tiles, depth_model=dm, softness=softness,
+                          **layer)
+    tie = H.tie_pixels(o["margins"]).reshape(-1)[pix]
+    for k, g in (("rgb", r.out_rgb), ("depth", r.out_depth), ("alpha", r.out_alpha)):
+        err = np.abs(g.cpu().numpy().reshape(len(fid.reshape(-1)), -1)[pix] - o[k].reshape(len(fid.reshape(-1)), -1)[pix])
+        err = err.max(-1)
+        assert np.all(err[~tie] <= 1e-4), (k, err[~tie].max())
+    assert tie.sum() <= max(2, len(pix) // 200)
+    # gradients
+    grads = scenes.upstream_grads(5, cam.width, cam.height)
+    gt = [torch.as_tensor(x).cuda() for x in grads]
+    v_splats, v_verts, v_vcol = r.backward(*gt)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(13)
+    vis = np.nonzero(rad > 0)[0]
+    pick = np.sort(rng.choice(vis, 40, replace=False))
+    TW = (cam.width + 15) // 16
+    gt_tiles = set()
+    for gi in pick:
+        x0 = int(max(0, np.floor((sp[gi, 0] - rad[gi]) / 16))); x1 = int(min(TW, np.ceil((sp[gi, 0] + rad[gi]) / 16)))
+        y0 = int(max(0, np.floor((sp[gi, 1] - rad[gi]) / 16))); y1 = int(min(T // TW, np.ceil((sp[gi, 1] + rad[gi]) / 16)))
+        gt_tiles.update(ty * TW + tx for ty in range(y0, y1) for tx in range(x0, x1))
+    glists = orc.tile_lists(cam, sp, rad, np.array(sorted(gt_tiles)))
+    gid, fld = np.repeat(pick, 10), np.tile(np.arange(10), len(pick))
+    s = sp[gid]
+    hs = np.select([fld <= 1, fld <= 4, fld == 5, fld <= 8],
+                   [1e-3, 1e-4 * np.maximum(np.abs(s[:, 2]), np.abs(s[:, 4])), 1e-4, 1e-2], 1e-5 * s[:, 9])
+    if softness > 0:
+        hs[fld == 9] = 1e-3 * dm[gid[fld == 9], 2]
+    fd, st = orc.composite_fd(cam, np.float64(scene.bg), sp, rad, glists, lmd, lrgb, fid, grads, gid, fld, hs,
+                              depth_model=dm, softness=softness, **layer)
+    got = v_splats.cpu().numpy()[gid, fld].astype(np.float64)
+    ok = st == 0
+    bad = ok & (np.abs(got - fd) > 1e-5 + 1e-3 * np.abs(fd))
+    print("1080p options soft=%g aa=%d: %d splat fields checked, %d excluded" % (softness, antialias, ok.sum(),
+                                                                                   (~ok).sum()))
+    assert not bad.any(), [(gid[k], fld[k], got[k], fd[k]) for k in np.nonzero(bad)[0][:5]]
+    assert ok.sum() >= 0.75 * len(st)
+    if not antialias:
+        return
+    # silhouette vertices: vertices of faces with fractional pixels
+    covp = r.cov.cpu().numpy()
+    frac = (covp > 0) & (covp < 1) & (fid >= 0)
+    sil = np.unique(scene.mesh.faces[np.unique(fid[frac])].reshape(-1))
+    vpick = np.sort(rng.choice(sil, 12, replace=False))
+    vid, vf = np.repeat(vpick, 3), np.tile(np.arange(3), len(vpick))
+    vh = np.full(len(vid), 2e-5)
+    vlists = orc.tile_lists(cam, sp, rad, None)  # every tile: the oracle picks the pixels it re-evaluates
+    args = (sp, vlists, md.reshape(-1), mrgb.reshape(-1, 3), grads, vid, vf, vh)
+    soft = dict(depth_model=dm, softness=softness) if softness > 0 else {}
+    vfd, vst = orc.mesh_fd(cam, np.float64(scene.bg), scene.mesh.verts, scene.mesh.faces, scene.mesh.vcol,
+                           fid.reshape(-1), *args, adj=r.adj.cpu().numpy(), **soft)
+    sens = np.zeros(len(vid))
+    for V2 in H.input_ulp_perturbations(cam, scene.mesh.verts, draws=2):
+        v2, st2 = orc.mesh_fd(cam, np.float64(scene.bg), V2, scene.mesh.faces, scene.mesh.vcol, fid.reshape(-1),
+                              *args, adj=r.adj.cpu().numpy(), **soft)
+        sens = np.maximum(sens, np.where(st2 == 0, np.abs(v2 - vfd), np.inf))
+    vgot = v_verts.cpu().numpy()[vid, vf]
+    vok = (vst == 0) & np.isfinite(sens)
+    vbad = vok & (np.abs(vgot - vfd) > 1e-5 + 1e-3 * np.abs(vfd) + 4 * sens)
+    print("1080p options: %d silhouette vertex fields checked, %d excluded" % (vok.sum(), (~vok).sum()))
+    assert not vbad.any(), [(vid[k], vf[k], vgot[k], vfd[k]) for k in np.nonzero(vbad)[0][:5]]
+    assert vok.sum() >= 0.5 * len(vst)
