@@ -626,49 +626,75 @@ def run_multiview(args, flush, dist):
 
 
 def run_e2e(args, r, scene, grads_np, flush, ws, dist):
-    """Same step through the public calls with host buffers: pinned H2D of the
-    inputs and upstream gradients, the seven calls, D2H of image and gradients."""
+    """Same step through the public calls with host buffers: every step copies its
+    inputs (all Gaussian and mesh parameters, the upstream gradients) from pinned
+    host memory, runs the seven calls and the backward, and copies the image and
+    all gradients back.  Steps are pipelined over two renderers (two sets of
+    device buffers) and three streams: step k+1's uploads overlap step k's
+    compute and step k-1's downloads (a buffer set is refilled only after its
+    previous step's downloads finished).  The timed region spans the first
+    upload to the last download; inputs (294 MB a step) exceed the L2."""
     import torch
-    ins = [(r.means, scene.gaussians.means), (r.log_scales, scene.gaussians.log_scales),
-           (r.quats, scene.gaussians.quats), (r.logits, scene.gaussians.logits), (r.colors, scene.gaussians.colors),
-           (r.V, scene.mesh.verts), (r.F, scene.mesh.faces), (r.vcol, scene.mesh.vcol)]
-    host_in = [(d, torch.as_tensor(np.ascontiguousarray(h)).pin_memory()) for d, h in ins]
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    r2 = gm.HybridRenderer(r.cam_desc, bg=scene.bg, cull_occluded=True, device="cuda")
+    r2.upload(scene.mesh, scene.gaussians)
+    r2.forward(sync=True)
+    rends = [r, r2]
+    host_in = [torch.as_tensor(np.ascontiguousarray(h)).pin_memory()
+               for h in (scene.gaussians.means, scene.gaussians.log_scales, scene.gaussians.quats,
+                         scene.gaussians.logits, scene.gaussians.colors, scene.mesh.verts, scene.mesh.faces,
+                         scene.mesh.vcol)]
     g_host = [torch.as_tensor(x).pin_memory() for x in grads_np]
-    g_dev = [torch.empty_like(x, device="cuda") for x in g_host]
-    outs = [r.out_rgb, r.out_depth, r.out_alpha, r.v_splats, r.v_verts, r.v_vcol]
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    h2d = sum(h.numel() * h.element_size() for _, h in host_in) + sum(x.numel() * x.element_size() for x in g_host)
-    d2h = sum(o.numel() * o.element_size() for o in outs)
-    stream = torch.cuda.current_stream()
+    g_dev = [[torch.empty_like(x, device="cuda") for x in g_host] for _ in rends]
+    dev_in = [[q.means, q.log_scales, q.quats, q.logits, q.colors, q.V, q.F, q.vcol] for q in rends]
+    for q in rends:  # the mesh-gradient buffers exist after one backward
+        q.backward(*[x.cuda() for x in g_host])
+    outs = [[q.out_rgb, q.out_depth, q.out_alpha, q.v_splats, q.v_verts, q.v_vcol] for q in rends]
+    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[0]] for _ in rends]
+    h2d = sum(h.numel() * h.element_size() for h in host_in) + sum(x.numel() * x.element_size() for x in g_host)
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        for d, h in host_in:
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(g_dev, g_host):
-            d.copy_(h, non_blocking=True)
-        r.forward(sync=False)
-        r.backward(*g_dev)
-        for h, d in zip(host_out, outs):
-            h.copy_(d, non_blocking=True)
+    def run(n):
+        ev_up = [torch.cuda.Event() for _ in range(n)]
+        ev_comp = [torch.cuda.Event() for _ in range(n)]
+        ev_down = [torch.cuda.Event() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        up.wait_stream(comp)
+        t0.record(up)
+        for k in range(n):
+            b = k % 2
+            with torch.cuda.stream(up):
+                if k >= 2:
+                    up.wait_event(ev_down[k - 2])  # the buffer set's previous step is fully read back
+                for d, h in zip(dev_in[b], host_in):
+                    d.copy_(h, non_blocking=True)
+                for d, h in zip(g_dev[b], g_host):
+                    d.copy_(h, non_blocking=True)
+                ev_up[k].record(up)
+            comp.wait_event(ev_up[k])
+            rends[b].forward(sync=False)
+            rends[b].backward(*g_dev[b])
+            ev_comp[k].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_comp[k])
+                for h, d in zip(host_out[b], outs[b]):
+                    h.copy_(d, non_blocking=True)
+                ev_down[k].record(down)
+        t1.record(down)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
 
-    for _ in range(max(2, args.warmup)):
-        flush.zero_()
-        e2e_step()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        times.append(a.elapsed_time(b))
-    ms = max_over_ranks([float(np.mean(times))], dist, "cuda")[0]
+    run(max(2, args.warmup))
+    steps = max(4, args.steps)
+    ms = run(steps) / steps
+    ms = max_over_ranks([ms], dist, "cuda")[0]
     val = job_throughput(ws, r.W * r.H, ms)
     return {"value": val, "unit": "Mpix/s", "ms_per_step": ms, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "timing": "pipelined over two buffer sets: uploads of step k+1, compute of step k and downloads of "
+                      "step k-1 overlap; first upload to last download"}
 
 
 # -------------------------------------------------------------- CPU arm ---
