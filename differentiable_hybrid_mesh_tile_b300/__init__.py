@@ -71,6 +71,9 @@ _SIGS = {
     "gm_bin_sort_gaussians_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
     "gm_bin_sort_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
                                         C.c_size_t, _VP]),
+    "gm_bin_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
+                                   C.c_size_t, _VP]),
+    "gm_sort_gaussians_by_depth": (C.c_int, [_VP, _I32, _VP, _VP, _I32, _VP, _VP, C.c_size_t, _VP]),
     "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 15),
     "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16 + [_I32, _VP, _I32] + [_VP] * 6),
     "gm_mesh_edges_workspace_size": (C.c_size_t, [_I32]),
@@ -316,6 +319,27 @@ def gm_interp_mesh_bwd(cam: gm_camera, V, F, vcol, face_id, v_mesh_rgb, v_mesh_d
                                     _p(v_vcol, F32), _stream()), "gm_interp_mesh_bwd")
 
 
+def gm_sort_gaussians_by_depth(cam: gm_camera, splats, radii, cap: int, counters, ws):
+    _check(lib().gm_sort_gaussians_by_depth(C.byref(cam), radii.shape[0], _p(splats, F32), _p(radii, I32), cap,
+                                            _p(counters, I32), _p(ws), ws.numel() * ws.element_size(), _stream()),
+           "gm_sort_gaussians_by_depth")
+
+
+def gm_bin_gaussians(cam: gm_camera, opts: gm_opts, splats, radii, tile_far, tile_full, keys, gids, tile_range,
+                     cap: int, counters, ws, sync: bool = True):
+    """The second half of gm_bin_sort_gaussians (after gm_sort_gaussians_by_depth
+    on the same workspace)."""
+    k = C.c_int32(0)
+    st = lib().gm_bin_gaussians(C.byref(cam), C.byref(opts), radii.shape[0], _p(splats, F32), _p(radii, I32),
+                                _p(tile_far, F32), _p(tile_full, U8), _p(keys, I64), _p(gids, I32),
+                                _p(tile_range, I32), cap, _p(counters, I32), C.byref(k) if sync else None,
+                                _p(ws), ws.numel() * ws.element_size(), _stream())
+    if st == GM_ERR_CAPACITY:
+        raise GmError(st, "gm_bin_gaussians", "capacity %d < needed %d" % (cap, k.value))
+    _check(st, "gm_bin_gaussians")
+    return k.value if sync else None
+
+
 def gm_composite_hybrid_fwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
                             out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None, depth_model=None,
                             aa=None):
@@ -507,8 +531,11 @@ class HybridRenderer:
         if self.concurrent:
             side.wait_stream(main)
         with torch.cuda.stream(side):
+            # the projection and the Gaussians' depth pre-sort need no mesh: they run
+            # beside the mesh layer
             gm_project_gaussians(cam, opts, self.means, self.log_scales, self.quats, self.logits, self.colors,
                                  self.splats, self.radii, self.tiles_touched, self.depth_model)
+            gm_sort_gaussians_by_depth(cam, self.splats, self.radii, self.g_cap, self.g_counters, self.g_ws)
         for attempt in range(2):
             try:
                 k = gm_bin_triangles(cam, self.V, self.F, self.tri_range, self.tri_ids, self.tri_cap,
@@ -529,9 +556,11 @@ class HybridRenderer:
             main.wait_stream(side)
         for attempt in range(2):
             try:
-                k = gm_bin_sort_gaussians(cam, opts, self.splats, self.radii, self.tile_far, self.tile_full,
-                                          self.keys, self.gids, self.g_range, self.g_cap, self.g_counters,
-                                          self.g_ws, sync=sync)
+                if attempt:  # a new workspace: its depth pre-sort again
+                    gm_sort_gaussians_by_depth(cam, self.splats, self.radii, self.g_cap, self.g_counters, self.g_ws)
+                k = gm_bin_gaussians(cam, opts, self.splats, self.radii, self.tile_far, self.tile_full,
+                                     self.keys, self.gids, self.g_range, self.g_cap, self.g_counters,
+                                     self.g_ws, sync=sync)
                 self.K_gauss = k
                 break
             except GmError as e:

@@ -271,6 +271,48 @@ size_t gm_bin_sort_gaussians_workspace_size(int32_t N, int32_t cap, int32_t widt
     return gm::gauss_bin_ws_bytes(N < 0 ? 0 : N, cap < 0 ? 0 : cap);
 }
 
+int gm_sort_gaussians_by_depth(const gm_camera* cam, int32_t N, const float* splats, const int32_t* radii,
+                               int32_t cap, int32_t* counters, void* ws, size_t ws_bytes, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(N >= 0 && cap >= 0, "negative size");
+    GM_REQUIRE(N == 0 || (splats && radii), "splats / radii is NULL");
+    GM_REQUIRE(N == 0 || aligned16(splats), "splats must be 16-byte aligned");
+    GM_REQUIRE(counters, "counters is NULL");
+    const size_t need = gm::gauss_bin_ws_bytes(N, cap);
+    GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
+    GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
+    cudaError_t e = gm::gauss_depth_sort(gm::make_cam(*cam), N, splats, radii, cap, counters, ws,
+                                         (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_sort_gaussians_by_depth");
+}
+
+int gm_bin_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* splats,
+                     const int32_t* radii, const float* tile_far, const uint8_t* tile_full, uint64_t* keys,
+                     int32_t* gids, int32_t* tile_range, int32_t cap, int32_t* counters, int32_t* K_host,
+                     void* ws, size_t ws_bytes, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(opts, "opts is NULL");
+    GM_REQUIRE(N >= 0 && cap >= 0, "negative size");
+    GM_REQUIRE(N == 0 || (splats && radii), "splats / radii is NULL");
+    GM_REQUIRE(N == 0 || aligned16(splats), "splats must be 16-byte aligned");
+    GM_REQUIRE(!opts->cull_occluded || (tile_far && tile_full), "cull_occluded needs tile_far and tile_full");
+    GM_REQUIRE(tile_range && counters, "tile_range / counters is NULL");
+    GM_REQUIRE(cap == 0 || (keys && gids), "keys / gids is NULL");
+    const size_t need = gm::gauss_bin_ws_bytes(N, cap);
+    GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
+    GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool cull = opts->cull_occluded != 0 && !(opts->softness > 0.0f);
+    cudaError_t e = gm::gauss_bin(gm::make_cam(*cam), cull, opts->tile_test != 0, N, splats, radii, tile_far,
+                                  tile_full, keys, gids, tile_range, cap, counters, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gm_bin_gaussians");
+    return finish_binning(counters, K_host, cap, s);
+}
+
 int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* splats,
                           const int32_t* radii, const float* tile_far, const uint8_t* tile_full, uint64_t* keys,
                           int32_t* gids, int32_t* tile_range, int32_t cap, int32_t* counters, int32_t* K_host,

@@ -272,13 +272,35 @@ __device__ __forceinline__ void divmod_small(int t, int w, float inv_w, int& q, 
 // Gaussian does not hold up the other 31 lanes.
 constexpr int SMALL_RECT = 16;
 
+// Depth keys of the pre-sort: the centre depth's bits for a Gaussian whose tile
+// rectangle is not empty, all ones otherwise (it emits nothing and sorts last);
+// ids as values.  Needs no mesh, so it can run before the mesh layer exists.
+__global__ void __launch_bounds__(256)
+k_gauss_depth_keys(Cam c, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
+                   uint64_t* __restrict__ dkey, int32_t* __restrict__ dval, int32_t* n_dev)
+{
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g == 0) *n_dev = N;
+    if (g >= N) return;
+    const int r = radii[g];
+    bool vis = false;
+    float depth = 0.0f;
+    if (r > 0) {
+        const float4 s0 = splats[3 * (int64_t)g];
+        depth = splats[3 * (int64_t)g + 2].y;
+        int x0, y0, x1, y1;
+        vis = gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1);
+    }
+    dkey[g] = vis ? (uint64_t)__float_as_uint(depth) : 0xffffffffull;
+    dval[g] = g;
+}
+
 // Per Gaussian: the number of tiles it is binned to after the cull and the
 // tile test, and its depth key (float bits of the centre depth; 0xffffffff
 // when it emits nothing) for the depth pre-sort.
 __global__ void __launch_bounds__(256)
 k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
-              int32_t* __restrict__ counts, uint32_t* __restrict__ kept, uint64_t* __restrict__ dkey,
-              int32_t* __restrict__ dval, int32_t* n_dev, int32_t* counters)
+              int32_t* __restrict__ counts, uint32_t* __restrict__ kept, int32_t* counters)
 {
     __shared__ int s_pre[8];
     __shared__ BinShape s_shape[256];
@@ -286,7 +308,6 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int wbase = threadIdx.x & ~31;
-    if (g == 0) *n_dev = N;
     int pre = 0, post = 0;
     uint32_t mask = 0;
     int x0 = 0, y0 = 0, x1 = 0, y1 = 0;
@@ -366,8 +387,6 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
     if (g < N) {
         counts[g] = post;
         kept[g] = mask;
-        dkey[g] = post > 0 ? (uint64_t)__float_as_uint(sh.depth) : 0xffffffffull;
-        dval[g] = g;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
@@ -574,40 +593,65 @@ size_t gauss_bin_ws_bytes(int N, int cap)
 // reached in two stable LSD sorts: the N Gaussians by depth (32 bits), then,
 // after emitting each Gaussian's tiles in that order, the K entries by tile
 // only (ceil(log2 T) bits) -- instead of one 32 + log2 T bit sort of K keys.
-cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
-                           const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
-                           int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
+struct GaussWs {
+    ScanWs sw;
+    int32_t *counts, *offsets;
+    uint32_t* kept;
+    uint64_t *dkey, *dkey_alt;
+    int32_t *dval, *dval_alt, *n_dev;
+    SortWs so;
+};
+
+static GaussWs carve_gauss_ws(void* ws, int N, int cap)
 {
     int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
+    GaussWs w;
     uint8_t* b = (uint8_t*)ws;
-    ScanWs sw;
-    b += carve_scan_ws(b, n, sw);
-    int32_t* counts = (int32_t*)b;
+    b += carve_scan_ws(b, n, w.sw);
+    w.counts = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
-    int32_t* offsets = (int32_t*)b;
+    w.offsets = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
-    uint32_t* kept = (uint32_t*)b;
+    w.kept = (uint32_t*)b;
     b += a256(sizeof(uint32_t) * n);
-    uint64_t* dkey = (uint64_t*)b;
+    w.dkey = (uint64_t*)b;
     b += a256(sizeof(uint64_t) * n);
-    uint64_t* dkey_alt = (uint64_t*)b;
+    w.dkey_alt = (uint64_t*)b;
     b += a256(sizeof(uint64_t) * n);
-    int32_t* dval = (int32_t*)b;
+    w.dval = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
-    int32_t* dval_alt = (int32_t*)b;
+    w.dval_alt = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
-    int32_t* n_dev = (int32_t*)b;
+    w.n_dev = (int32_t*)b;
     b += 256;
-    SortWs so;
-    carve_sort_ws(b, n > k ? n : k, so);
+    carve_sort_ws(b, n > k ? n : k, w.so);
+    return w;
+}
 
+cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int32_t* radii, int cap,
+                             int32_t* counters, void* ws, cudaStream_t s)
+{
+    GaussWs w = carve_gauss_ws(ws, N, cap);
     cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || N <= 0) return e;
+    k_gauss_depth_keys<<<(N + 255) / 256, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dkey,
+                                                        w.dval, w.n_dev);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 4 passes: even, the result is back in dkey / dval
+    return radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s);
+}
+
+cudaError_t gauss_bin(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
+                      const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
+                      int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
+{
+    GaussWs w = carve_gauss_ws(ws, N, cap);
+    cudaError_t e = cudaSuccess;
     const int T = c.TW * c.TH;
     const int tb = tile_bits(T);
     const int passes = sort_passes(32, 32 + tb);
-    uint64_t* ek = passes % 2 ? so.keys_alt : keys;
-    int32_t* ev = passes % 2 ? so.vals_alt : gids;
+    uint64_t* ek = passes % 2 ? w.so.keys_alt : keys;
+    int32_t* ev = passes % 2 ? w.so.vals_alt : gids;
     if (N > 0) {
         auto* s4 = reinterpret_cast<const float4*>(splats);
         const int grid = (N + 255) / 256;
@@ -617,25 +661,33 @@ cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const
         rule.tile_far = tile_far;
         rule.tile_full = tile_full;
         rule.TW = c.TW;
-        k_gauss_count<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, counts, kept, dkey, dval, n_dev, counters);
+        k_gauss_count<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, w.counts, w.kept, counters);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        // depth pre-sort of the Gaussians (4 passes: even, the result is back in dkey / dval)
-        if ((e = radix_sort(dkey, dval, dkey_alt, dval_alt, N, 0, 32, n_dev, counters, so, s)) != cudaSuccess) return e;
-        if ((e = exclusive_scan(counts, dval, offsets, N, counters, sw, s)) != cudaSuccess) return e;
-        k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, dval, counts, kept, offsets, cap, counters, ek,
-                                          ev);
+        if ((e = exclusive_scan(w.counts, w.dval, w.offsets, N, counters, w.sw, s)) != cudaSuccess) return e;
+        k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, w.dval, w.counts, w.kept, w.offsets, cap, counters,
+                                          ek, ev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (tb > 0) {
             if (passes % 2)
-                e = radix_sort(so.keys_alt, so.vals_alt, keys, gids, cap, 32, 32 + tb, counters + GM_CNT_K, counters,
-                               so, s);
+                e = radix_sort(w.so.keys_alt, w.so.vals_alt, keys, gids, cap, 32, 32 + tb, counters + GM_CNT_K,
+                               counters, w.so, s);
             else
-                e = radix_sort(keys, gids, so.keys_alt, so.vals_alt, cap, 32, 32 + tb, counters + GM_CNT_K, counters,
-                               so, s);
+                e = radix_sort(keys, gids, w.so.keys_alt, w.so.vals_alt, cap, 32, 32 + tb, counters + GM_CNT_K,
+                               counters, w.so, s);
             if (e != cudaSuccess) return e;
         }
     }
     return tile_ranges(keys, N > 0 ? cap : 0, counters, tile_range, T, s);
+}
+
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
+                           const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
+                           int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
+{
+    cudaError_t e = gauss_depth_sort(c, N, splats, radii, cap, counters, ws, s);
+    if (e != cudaSuccess) return e;
+    return gauss_bin(c, cull, tile_test, N, splats, radii, tile_far, tile_full, keys, gids, tile_range, cap, counters,
+                     ws, s);
 }
 
 }  // namespace gm

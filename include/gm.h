@@ -328,6 +328,24 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
                           int32_t* counters, int32_t* K_host, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * gm_sort_gaussians_by_depth + gm_bin_gaussians -- gm_bin_sort_gaussians in
+ * two halves, for callers that overlap the first with the mesh layer: the
+ * depth pre-sort of the Gaussians (centre depth, ascending; ids break ties;
+ * Gaussians whose tile rectangle is empty last) needs only splats / radii;
+ * the binning, culling, emission and tile sort need tile_far / tile_full.
+ * Call both, in this order, with the same N, cap and workspace (nothing else
+ * may use the workspace in between); the results equal gm_bin_sort_gaussians'.
+ * gm_sort_gaussians_by_depth zeroes counters; gm_bin_gaussians reports the
+ * entry count and flags there (and in K_host, as gm_bin_sort_gaussians).
+ * ---------------------------------------------------------------------- */
+int gm_sort_gaussians_by_depth(const gm_camera* cam, int32_t N, const float* splats, const int32_t* radii,
+                               int32_t cap, int32_t* counters, void* ws, size_t ws_bytes, void* stream);
+int gm_bin_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const float* splats,
+                     const int32_t* radii, const float* tile_far, const uint8_t* tile_full, uint64_t* keys,
+                     int32_t* gids, int32_t* tile_range, int32_t cap, int32_t* counters, int32_t* K_host,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * gm_composite_hybrid_fwd -- Hybrid rendering, compositing with a hard
  * split: per pixel, front to back over its tile's sorted Gaussians, each
  * drawn only where its centre depth is in front of the mesh (z < D);

@@ -247,3 +247,37 @@ def test_tile_test_drops_only_unreachable_pairs(case, orc):
     assert worst < 1.0 / 255.0
     if name == "soup_small":
         assert ti["K"] < 0.9 * ex["K"]
+
+
+def test_split_binning_equals_one_call():
+    """gm_sort_gaussians_by_depth + gm_bin_gaussians (the two halves the renderer
+    overlaps with the mesh layer) give bit-identical keys, ids, ranges and counts
+    to gm_bin_sort_gaussians, with and without the cull."""
+    H.need_gpu()
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    s = scenes.sphere512()
+    cam = s.camera
+    m = H.run_mesh(cam, s.mesh)
+    sp, rad, _ = H.run_project(cam, s.gaussians, s.bg)
+    c = gm.make_camera(cam)
+    T = H.n_tiles(cam)
+    for cull in (False, True):
+        o = gm.make_opts(s.bg, cull, -1, True)
+        ref = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull=cull, tile_test=True)
+        cap = ref["cap"]
+        keys = torch.zeros(cap, dtype=torch.int64, device="cuda")
+        gids = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+        tr = torch.full((T, 2), -5, dtype=torch.int32, device="cuda")
+        cnt = torch.full((4,), -9, dtype=torch.int32, device="cuda")
+        ws = torch.empty(gm.gm_bin_sort_gaussians_workspace_size(len(rad), cap, cam.width, cam.height),
+                         dtype=torch.uint8, device="cuda")
+        spd, radd = H.dev(sp, torch.float32), H.dev(rad, torch.int32)
+        gm.gm_sort_gaussians_by_depth(c, spd, radd, cap, cnt, ws)
+        K = gm.gm_bin_gaussians(c, o, spd, radd, H.dev(m["tile_far"], torch.float32),
+                                H.dev(m["tile_full"], torch.uint8), keys, gids, tr, cap, cnt, ws)
+        assert K == ref["K"]
+        np.testing.assert_array_equal(H.host(keys)[:K].view(np.uint64), ref["keys"])
+        np.testing.assert_array_equal(H.host(gids)[:K], ref["gids"])
+        np.testing.assert_array_equal(H.host(tr), ref["tile_range"])
+        np.testing.assert_array_equal(H.host(cnt), ref["counters"])
