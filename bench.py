@@ -160,10 +160,10 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 PROFILED_TRAFFIC = {
     "composite_bwd": {
         "kernel": "k_composite_bwd",
-        "bytes": 160724992 + 11533312,
+        "bytes": 160982272 + 11324160,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "6830216f1bf4844931d28e37435aeb645848e4fdba96c2b25f2c3212e818e284",
+                "97f89d799ca63d2f4e92b6d11415b23a7a9c28e3db4fd5654e118c19a132427a",
         },
         "profile": "profiles/composite_bwd_soup_1080p.md",
     },
