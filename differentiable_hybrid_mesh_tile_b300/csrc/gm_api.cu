@@ -173,7 +173,8 @@ int gm_project_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, c
             GM_REQUIRE(aligned16(colors), "SH coefficients must be 16-byte aligned");
     }
     GM_REQUIRE(!depth_model || aligned16(depth_model), "depth_model must be 16-byte aligned");
-    cudaError_t e = gm::project(gm::make_cam(*cam), opts->sh_degree, N, means, log_scales, quats, logits, colors, splats,
+    cudaError_t e = gm::project(gm::make_cam(*cam), opts->sh_degree, opts->softness, opts->soft_split, N, means,
+                                log_scales, quats, logits, colors, splats,
                                 radii, tiles_touched, depth_model, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians");
 }
@@ -227,7 +228,8 @@ int gm_project_gaussians_views(const gm_camera* cams, int32_t V, const gm_opts* 
     }
     gm::Cam c[GM_MAX_VIEWS];
     for (int v = 0; v < V; ++v) c[v] = gm::make_cam(cams[v]);
-    cudaError_t e = gm::project_views(c, V, opts->sh_degree, N, means, log_scales, quats, logits, colors, splats, radii,
+    cudaError_t e = gm::project_views(c, V, opts->sh_degree, opts->softness, opts->soft_split, N, means, log_scales,
+                                      quats, logits, colors, splats, radii,
                                       tiles_touched, depth_model, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_project_gaussians_views");
 }
@@ -306,8 +308,9 @@ int gm_bin_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const
     GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    const bool cull = opts->cull_occluded != 0 && !(opts->softness > 0.0f);
-    cudaError_t e = gm::gauss_bin(gm::make_cam(*cam), cull, opts->tile_test != 0, N, splats, radii, tile_far,
+    // the soft split culls on the record's hide depth (field 10, from gm_project_gaussians)
+    const bool cull = opts->cull_occluded != 0, soft = opts->softness > 0.0f;
+    cudaError_t e = gm::gauss_bin(gm::make_cam(*cam), cull, soft, opts->tile_test != 0, N, splats, radii, tile_far,
                                   tile_full, keys, gids, tile_range, cap, counters, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "gm_bin_gaussians");
     return finish_binning(counters, K_host, cap, s);
@@ -332,8 +335,9 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     // the soft split lets a Gaussian behind the mesh show through a little: no cull
-    const bool cull = opts->cull_occluded != 0 && !(opts->softness > 0.0f);
-    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), cull, opts->tile_test != 0, N, splats,
+    // the soft split culls on the record's hide depth (field 10, from gm_project_gaussians)
+    const bool cull = opts->cull_occluded != 0, soft = opts->softness > 0.0f;
+    cudaError_t e = gm::gauss_bin_sort(gm::make_cam(*cam), cull, soft, opts->tile_test != 0, N, splats,
                                        radii, tile_far,
                                        tile_full, keys, gids, tile_range, cap, counters, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "gm_bin_sort_gaussians");

@@ -131,9 +131,23 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
     }
 }
 
+// The record's field 10 under the soft split: the depth beyond which the
+// mesh hides the Gaussian (z_c - R - tail sigma_z softness, less a rounding
+// margin; the compositing's own bound, computed from the same stored values).
+// 0 under the hard split (the occlusion cull then uses the centre depth).
+struct SoftCull {
+    float softness, tail;  // softness 0: hard split
+};
+
+__device__ __forceinline__ float hide_depth(const SoftCull& sc, float z, const float4& dm)
+{
+    const float band = dm.z * sc.softness;
+    return z - fmaf(sc.tail, band, dm.w) * 1.0001f - 2e-6f * fabsf(z);
+}
+
 template <int DEG>
 __global__ void __launch_bounds__(256)
-k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+k_project(Cam c, ProjConsts pc, SoftCull sc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
           const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
           float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched,
           float4* __restrict__ depth_model)
@@ -143,6 +157,7 @@ k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const fl
     float4 o0, o1, o2, dm;
     int rad, touched;
     project_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad, touched);
+    if (sc.softness > 0.0f && rad > 0) o2.z = hide_depth(sc, o2.y, dm);
     splats[3 * (int64_t)g] = o0;
     splats[3 * (int64_t)g + 1] = o1;
     splats[3 * (int64_t)g + 2] = o2;
@@ -156,7 +171,7 @@ k_project(Cam c, ProjConsts pc, int N, const float* __restrict__ means, const fl
 // them in L1 / L2); outputs are [view][N] arrays.
 template <int DEG>
 __global__ void __launch_bounds__(256)
-k_project_views(ViewBatch vb, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
+k_project_views(ViewBatch vb, SoftCull sc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
                 const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
                 float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched,
                 float4* __restrict__ depth_model)
@@ -168,6 +183,7 @@ k_project_views(ViewBatch vb, int N, const float* __restrict__ means, const floa
         int rad, touched;
         project_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad,
                               touched);
+        if (sc.softness > 0.0f && rad > 0) o2.z = hide_depth(sc, o2.y, dm);
         const int64_t i = (int64_t)v * N + g;
         splats[3 * i] = o0;
         splats[3 * i + 1] = o1;
@@ -183,6 +199,7 @@ k_project_views(ViewBatch vb, int N, const float* __restrict__ means, const floa
 // Which tiles of a Gaussian's rectangle get an entry.
 struct BinRule {
     bool cull;        // drop tiles where the mesh hides the Gaussian (tile_full, depth >= tile_far)
+    bool soft;        // soft split: hidden when the record's field 10 (hide depth) lies beyond tile_far
     bool tile_test;   // drop tiles no pixel centre of which the Gaussian reaches with alpha >= 1/255
     const float* __restrict__ tile_far;
     const uint8_t* __restrict__ tile_full;
@@ -195,6 +212,7 @@ struct BinShape {
     float nba, nbc;         // -b / a, -b / c: vertex of sigma along a line of constant v / u
     float smax;             // alpha >= 1/255 needs sigma <= ln(255 o); smax adds a margin
     float depth;
+    float hide;             // record field 10: hide depth under the soft split (0: none)
     bool degenerate;        // conic not positive definite: every tile is kept
 };
 
@@ -210,7 +228,9 @@ __device__ __forceinline__ BinShape bin_shape(const float4* __restrict__ splats,
     // (compositing) can never keep a pair this test drops
     const float thr = logf(255.0f * s1.y);
     b.smax = thr + 1e-3f * fabsf(thr) + 1e-4f;
-    b.depth = splats[3 * (int64_t)g + 2].y;
+    const float4 s2 = splats[3 * (int64_t)g + 2];
+    b.depth = s2.y;
+    b.hide = s2.z;
     return b;
 }
 
@@ -222,6 +242,7 @@ __device__ __forceinline__ BinShape shfl_shape(const BinShape& s, int j)
     o.c = __shfl_sync(0xffffffffu, s.c, j); o.smax = __shfl_sync(0xffffffffu, s.smax, j);
     o.nba = __shfl_sync(0xffffffffu, s.nba, j); o.nbc = __shfl_sync(0xffffffffu, s.nbc, j);
     o.depth = __shfl_sync(0xffffffffu, s.depth, j);
+    o.hide = __shfl_sync(0xffffffffu, s.hide, j);
     o.degenerate = __shfl_sync(0xffffffffu, (int)s.degenerate, j) != 0;
     return o;
 }
@@ -253,7 +274,11 @@ __device__ __forceinline__ float tile_min_sigma(const BinShape& s, int tx, int t
 __device__ __forceinline__ bool keep_tile(const BinRule& r, const BinShape& s, int tx, int ty)
 {
     const int t = ty * r.TW + tx;
-    if (r.cull && __ldg(r.tile_full + t) && s.depth >= __ldg(r.tile_far + t)) return false;
+    if (r.cull && __ldg(r.tile_full + t)) {
+        const float far = __ldg(r.tile_far + t);
+        // the soft split's per-pixel skip takes the same bound against each pixel's depth
+        if (r.soft ? s.hide > far + 4e-6f * fabsf(far) : s.depth >= far) return false;
+    }
     return !r.tile_test || tile_min_sigma(s, tx, ty) <= s.smax;
 }
 
@@ -524,17 +549,24 @@ size_t a256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 }  // namespace
 
-cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
-                    const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
-                    int32_t* tiles_touched, float* depth_model, cudaStream_t s)
+static SoftCull soft_cull(float softness, int split)
+{
+    // the compositing's tail bound of the front fraction: Phi(-2.75), logistic at -3.5
+    return SoftCull{softness > 0.0f ? softness : 0.0f, split == 1 ? 3.5f : 2.75f};
+}
+
+cudaError_t project(const Cam& c, int sh_degree, float softness, int split, int N, const float* means,
+                    const float* log_scales, const float* quats, const float* logits, const float* colors,
+                    float* splats, int32_t* radii, int32_t* tiles_touched, float* depth_model, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
     const ProjConsts pc = make_proj_consts(c);
+    const SoftCull sc = soft_cull(softness, split);
     const int grid = (N + 255) / 256;
     auto* q4 = reinterpret_cast<const float4*>(quats);
     auto* s4 = reinterpret_cast<float4*>(splats);
     auto* dm4 = reinterpret_cast<float4*>(depth_model);
-#define GM_PROJ(D) k_project<D><<<grid, 256, 0, s>>>(c, pc, N, means, log_scales, q4, logits, colors, s4, radii, \
+#define GM_PROJ(D) k_project<D><<<grid, 256, 0, s>>>(c, pc, sc, N, means, log_scales, q4, logits, colors, s4, radii, \
                                                      tiles_touched, dm4)
     switch (sh_degree) {
         case -1: GM_PROJ(-1); break;
@@ -548,11 +580,13 @@ cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, cons
     return cudaGetLastError();
 }
 
-cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const float* means, const float* log_scales,
-                          const float* quats, const float* logits, const float* colors, float* splats,
-                          int32_t* radii, int32_t* tiles_touched, float* depth_model, cudaStream_t s)
+cudaError_t project_views(const Cam* cams, int V, int sh_degree, float softness, int split, int N,
+                          const float* means, const float* log_scales, const float* quats, const float* logits,
+                          const float* colors, float* splats, int32_t* radii, int32_t* tiles_touched,
+                          float* depth_model, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
+    const SoftCull sc = soft_cull(softness, split);
     const int grid = (N + 255) / 256;
     auto* q4 = reinterpret_cast<const float4*>(quats);
     for (int v0 = 0; v0 < V; v0 += MAX_VIEWS) {
@@ -565,7 +599,7 @@ cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const fl
         const int64_t off = (int64_t)v0 * N;
         auto* s4 = reinterpret_cast<float4*>(splats + 12 * off);
         auto* dm4 = depth_model ? reinterpret_cast<float4*>(depth_model + 4 * off) : nullptr;
-#define GM_PROJ_V(D) k_project_views<D><<<grid, 256, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, s4, \
+#define GM_PROJ_V(D) k_project_views<D><<<grid, 256, 0, s>>>(vb, sc, N, means, log_scales, q4, logits, colors, s4, \
                                                              radii + off, tiles_touched + off, dm4)
         switch (sh_degree) {
             case -1: GM_PROJ_V(-1); break;
@@ -641,7 +675,8 @@ cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int
     return radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s);
 }
 
-cudaError_t gauss_bin(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
+cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N, const float* splats,
+                      const int32_t* radii,
                       const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                       int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
 {
@@ -657,6 +692,7 @@ cudaError_t gauss_bin(const Cam& c, bool cull, bool tile_test, int N, const floa
         const int grid = (N + 255) / 256;
         BinRule rule;
         rule.cull = cull;
+        rule.soft = soft;
         rule.tile_test = tile_test;
         rule.tile_far = tile_far;
         rule.tile_full = tile_full;
@@ -680,14 +716,14 @@ cudaError_t gauss_bin(const Cam& c, bool cull, bool tile_test, int N, const floa
     return tile_ranges(keys, N > 0 ? cap : 0, counters, tile_range, T, s);
 }
 
-cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
-                           const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
-                           int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool soft, bool tile_test, int N, const float* splats,
+                           const int32_t* radii, const float* tile_far, const uint8_t* tile_full, uint64_t* keys,
+                           int32_t* gids, int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
 {
     cudaError_t e = gauss_depth_sort(c, N, splats, radii, cap, counters, ws, s);
     if (e != cudaSuccess) return e;
-    return gauss_bin(c, cull, tile_test, N, splats, radii, tile_far, tile_full, keys, gids, tile_range, cap, counters,
-                     ws, s);
+    return gauss_bin(c, cull, soft, tile_test, N, splats, radii, tile_far, tile_full, keys, gids, tile_range, cap,
+                     counters, ws, s);
 }
 
 }  // namespace gm

@@ -186,12 +186,15 @@ cudaError_t mesh_bwd(const Cam& c, const float* V, int nV, const int32_t* F, int
                      const int32_t* face_id, const float* T_final, const float* g_rgb, const float* g_depth,
                      const float* v_mesh_depth, float* v_verts, float* v_vcol, cudaStream_t s);
 
-cudaError_t project(const Cam& c, int sh_degree, int N, const float* means, const float* log_scales,
-                    const float* quats, const float* logits, const float* colors, float* splats, int32_t* radii,
-                    int32_t* tiles_touched, float* depth_model, cudaStream_t s);
-cudaError_t project_views(const Cam* cams, int V, int sh_degree, int N, const float* means, const float* log_scales,
-                          const float* quats, const float* logits, const float* colors, float* splats,
-                          int32_t* radii, int32_t* tiles_touched, float* depth_model, cudaStream_t s);
+// softness > 0 (split 0: Phi, 1: logistic): record field 10 receives the soft
+// split's hide depth for the occlusion cull
+cudaError_t project(const Cam& c, int sh_degree, float softness, int split, int N, const float* means,
+                    const float* log_scales, const float* quats, const float* logits, const float* colors,
+                    float* splats, int32_t* radii, int32_t* tiles_touched, float* depth_model, cudaStream_t s);
+cudaError_t project_views(const Cam* cams, int V, int sh_degree, float softness, int split, int N,
+                          const float* means, const float* log_scales, const float* quats, const float* logits,
+                          const float* colors, float* splats, int32_t* radii, int32_t* tiles_touched,
+                          float* depth_model, cudaStream_t s);
 cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, const float* means,
                               const float* log_scales, const float* quats, const float* logits, const float* colors,
                               const int32_t* radii, const float* v_splats, const float* v_depth_model,
@@ -206,10 +209,12 @@ size_t gauss_bin_ws_bytes(int N, int cap);
 // else using the workspace in between): the depth pre-sort needs no mesh
 cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int32_t* radii, int cap,
                              int32_t* counters, void* ws, cudaStream_t s);
-cudaError_t gauss_bin(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
+cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N, const float* splats,
+                      const int32_t* radii,
                       const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                       int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
-cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool tile_test, int N, const float* splats, const int32_t* radii,
+cudaError_t gauss_bin_sort(const Cam& c, bool cull, bool soft, bool tile_test, int N, const float* splats,
+                           const int32_t* radii,
                            const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                            int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s);
 

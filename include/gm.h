@@ -117,7 +117,11 @@ typedef struct gm_aa_layer {
  *   [2] conic a   [3] conic b   [4] conic c   (inverse 2D covariance:
  *        sigma(d) = (a dx^2 + c dy^2) / 2 + b dx dy)
  *   [5] opacity   [6..8] RGB    [9] camera-space depth of the centre
- *   [10], [11] reserved (0)
+ *   [10] the soft split's hide depth z_c - R - t sigma_z softness (written by
+ *        gm_project_gaussians when opts->softness > 0; 0 otherwise): beyond it
+ *        the mesh hides the Gaussian (the soft occlusion cull reads it; 0
+ *        disables that cull)
+ *   [11] reserved (0)
  * Gradient buffers of the same layout hold dL/d of each field.
  */
 
@@ -308,7 +312,10 @@ int gm_project_gaussians_bwd(const gm_camera* cam, const gm_opts* opts, int32_t 
  * Every (Gaussian, tile) pair of a rectangle gets the 64-bit key
  *   (tile id << 32) | bits(depth)
  * and the Gaussian id as value; with opts->cull_occluded a pair is dropped
- * when tile_full[tile] and depth >= tile_far[tile]; with opts->tile_test a
+ * when tile_full[tile] and depth >= tile_far[tile] (under the soft split,
+ * opts->softness > 0: when the record's hide depth, field 10, exceeds
+ * tile_far[tile] by more than 4e-6 relative -- the bound the soft
+ * compositing itself skips by); with opts->tile_test a
  * pair is dropped when the smallest sigma over the tile's square of pixel
  * centres exceeds ln(255 opacity) by a margin (0.1 % + 1e-4): the Gaussian
  * cannot reach alpha >= 1/255 at any of those pixels, so the image and the

@@ -158,11 +158,12 @@ def run_backward_aa(cam, bg, fwd, grads, N, mesh, m, adj):
     return out
 
 
-def run_project(cam, g, bg=(1, 1, 1), depth_model=False):
+def run_project(cam, g, bg=(1, 1, 1), depth_model=False, softness=0.0, soft_split=0):
     """GPU projection: splats, radii, tiles_touched (+ the soft split's depth
-    model [N][4] when depth_model is set)."""
+    model [N][4] when depth_model is set; with softness > 0 the records carry
+    the soft cull's hide depth in field 10)."""
     c = gm.make_camera(cam)
-    o = gm.make_opts(bg, True, g.sh_degree)
+    o = gm.make_opts(bg, True, g.sh_degree, True, softness, soft_split)
     N = len(g.means)
     splats = torch.full((N, 12), 7.0, dtype=torch.float32, device="cuda")
     radii = torch.full((N,), -3, dtype=torch.int32, device="cuda")
@@ -176,9 +177,10 @@ def run_project(cam, g, bg=(1, 1, 1), depth_model=False):
     return host(splats), host(radii), host(touched)
 
 
-def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=None, sync=True, tile_test=False):
+def run_bin(cam, splats, radii, tile_far=None, tile_full=None, cull=False, cap=None, sync=True, tile_test=False,
+            softness=0.0):
     c = gm.make_camera(cam)
-    o = gm.make_opts((1, 1, 1), cull, -1, tile_test)
+    o = gm.make_opts((1, 1, 1), cull, -1, tile_test, softness)
     N = len(radii)
     T = n_tiles(cam)
     tf = dev(np.full(T, np.inf, np.float32) if tile_far is None else tile_far, torch.float32)

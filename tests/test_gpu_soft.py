@@ -144,6 +144,28 @@ def test_reach_bounds_the_depth_slope(run):
     assert worst > 0.5
 
 
+def test_soft_cull_changes_nothing(run):
+    """The soft split's occlusion cull (records carrying their hide depth, full
+    tiles) only removes list entries every pixel of the tile would skip: the
+    image is bit-identical to the unculled bins', with fewer entries."""
+    name, s, r = run
+    cam, m = r["cam"], r["mesh"]
+    split = r["split"]
+    sp, rad, tt, dm = H.run_project(cam, s.gaussians, s.bg, depth_model=True, softness=SOFTNESS, soft_split=split)
+    np.testing.assert_array_equal(sp[:, :10], r["splats"][:, :10])  # only field 10 differs
+    vis = rad > 0
+    assert np.all(sp[vis, 10] < sp[vis, 9]) and np.all(sp[~vis, 10] == 0.0)
+    b1 = H.run_bin(cam, sp, rad, m["tile_far"], m["tile_full"], cull=True, softness=SOFTNESS)
+    f1 = H.run_composite(cam, s.bg, b1["tile_range"], b1["gids"], sp, m["mesh_depth"], m["mesh_rgb"],
+                         m["face_id"], softness=SOFTNESS, depth_model=dm, soft_split=split)
+    f0 = r["fwd"]
+    for k in ("rgb", "depth", "alpha", "T"):
+        np.testing.assert_array_equal(f0[k], f1[k])
+    print("%s: K %d -> %d with the soft cull" % (name, r["bins"]["K"], b1["K"]))
+    if m["tile_full"].any():
+        assert b1["K"] < r["bins"]["K"]
+
+
 def test_hidden_gaussian_skip_changes_nothing(run):
     """The per-block skip of Gaussians hidden behind the mesh only removes work:
     with every reach set to +inf (nothing skipped) the forward pass is bit-identical
