@@ -44,12 +44,12 @@ k_tri_emit(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
 
 // ---------------------------------------------------------- z-buffer ------
 
+// A staged triangle, four 16-byte vectors (one shared-memory load each):
+// (u0, v0, u1, v1), (u2, v2, area, w0), (w1, w2, face id, -), pixel-centre box
+// (x0, x1, y0, y1); w_k = 1 / (area z_k): depth reciprocal = sum_k e_k w_k.
 struct TriRec {
-    float u0, v0, u1, v1, u2, v2;
-    float area;
-    float w0, w1, w2;  // 1 / (area z_k): depth reciprocal = sum_k e_k w_k
-    int fid;
-    int x0, x1, y0, y1;
+    float4 p, q, w;
+    int4 box;
 };
 
 __global__ void __launch_bounds__(TILE_PIX)
@@ -78,16 +78,13 @@ k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict_
             // an id outside [0, nF) (possible only when the sort that built the
             // lists gave up a bounded wait) is skipped
             if (f >= 0 && f < nF && tri_setup(c, V, nV, F, f, t)) {
-                q.u0 = t.u[0]; q.v0 = t.v[0]; q.u1 = t.u[1]; q.v1 = t.v[1]; q.u2 = t.u[2]; q.v2 = t.v[2];
-                q.area = t.area;
-                q.w0 = 1.0f / (t.area * t.z[0]);
-                q.w1 = 1.0f / (t.area * t.z[1]);
-                q.w2 = 1.0f / (t.area * t.z[2]);
-                q.fid = f;
-                q.x0 = t.x0; q.x1 = t.x1; q.y0 = t.y0; q.y1 = t.y1;
+                q.p = make_float4(t.u[0], t.v[0], t.u[1], t.v[1]);
+                q.q = make_float4(t.u[2], t.v[2], t.area, 1.0f / (t.area * t.z[0]));
+                q.w = make_float4(1.0f / (t.area * t.z[1]), 1.0f / (t.area * t.z[2]), __int_as_float(f), 0.0f);
+                q.box = make_int4(t.x0, t.x1, t.y0, t.y1);
             } else {
-                q.fid = -1;
-                q.x0 = 1; q.x1 = 0; q.y0 = 1; q.y1 = 0;
+                q.w = make_float4(0.0f, 0.0f, __int_as_float(-1), 0.0f);
+                q.box = make_int4(1, 0, 1, 0);
             }
         }
         __syncthreads();
@@ -97,25 +94,28 @@ k_zbuffer(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict_
             const int kk = m * 32 + lane;
             bool h = false;
             if (kk < n) {
-                const TriRec& q = sm[kk];
-                h = q.x1 >= bx && q.x0 <= bx + 7 && q.y1 >= by && q.y0 <= by + 3;
+                const int4 bb = sm[kk].box;
+                h = bb.y >= bx && bb.x <= bx + 7 && bb.w >= by && bb.z <= by + 3;
             }
             uint32_t mask = __ballot_sync(0xffffffffu, h);
             while (mask) {
                 const int k = m * 32 + __ffs(mask) - 1;
                 mask &= mask - 1;
-                const TriRec& q = sm[k];
-                if (!inside || i < q.x0 || i > q.x1 || j < q.y0 || j > q.y1) continue;
-                float e0 = edge_rn(q.u1, q.v1, q.u2, q.v2, px, py);
-                float e1 = edge_rn(q.u2, q.v2, q.u0, q.v0, px, py);
-                float e2 = edge_rn(q.u0, q.v0, q.u1, q.v1, px, py);
-                bool in = q.area > 0.0f ? (e0 >= 0.0f && e1 >= 0.0f && e2 >= 0.0f)
-                                        : (e0 <= 0.0f && e1 <= 0.0f && e2 <= 0.0f);
+                const int4 bb = sm[k].box;
+                if (!inside || i < bb.x || i > bb.y || j < bb.z || j > bb.w) continue;
+                const float4 a = sm[k].p, b = sm[k].q;
+                // vertices (a.x, a.y), (a.z, a.w), (b.x, b.y); area b.z
+                float e0 = edge_rn(a.z, a.w, b.x, b.y, px, py);
+                float e1 = edge_rn(b.x, b.y, a.x, a.y, px, py);
+                float e2 = edge_rn(a.x, a.y, a.z, a.w, px, py);
+                bool in = b.z > 0.0f ? (e0 >= 0.0f && e1 >= 0.0f && e2 >= 0.0f)
+                                     : (e0 <= 0.0f && e1 <= 0.0f && e2 <= 0.0f);
                 if (!in) continue;
-                float inv_d = fmaf(e0, q.w0, fmaf(e1, q.w1, e2 * q.w2));
+                const float4 w = sm[k].w;
+                float inv_d = fmaf(e0, b.w, fmaf(e1, w.x, e2 * w.y));
                 if (inv_d > best) {  // lists ascend in face id: an equal depth keeps the smaller id
                     best = inv_d;
-                    best_f = q.fid;
+                    best_f = __float_as_int(w.z);
                 }
             }
         }
