@@ -336,6 +336,7 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
 
 constexpr int NGRAD = 10;
 constexpr int GROUP = 4;
+constexpr unsigned FULL = 0xffffffffu;
 
 // One level of a reduce-scatter over the lanes xor o: of each pair of values
 // (a, b) the lane keeps the one its bit o selects and adds its partner's copy
@@ -343,95 +344,70 @@ constexpr int GROUP = 4;
 __device__ __forceinline__ float rs_combine(float a, float b, int lane, int o)
 {
     const bool hi = lane & o;
-    return (hi ? b : a) + __shfl_xor_sync(0xffffffffu, hi ? a : b, o);
+    return (hi ? b : a) + __shfl_xor_sync(FULL, hi ? a : b, o);
 }
 
-// The per-lane gradient terms of a group of four entries: 40 values, value i
-// < 32 is component i >> 2 of entry i & 3 (0 ds dx, 1 ds dy, 2 ds dx^2 / 2,
-// 3 ds dx dy, 4 ds dy^2 / 2, 5 dL/d opacity, 6 w g_r, 7 w g_g), value 32 + i
-// is component 8 + (i >> 2) (w g_b, w g_depth) of entry i & 3.
-// With the soft split, four more per entry: 10 pz, 11 pz dx, 12 pz dy, 13 psx,
-// where pz = dL/dx kappa and psx = dL/dx x for the split's argument x.
-struct GroupTerms {
-    float pw[GROUP], pvo[GROUP], pds[GROUP], pdx[GROUP], pdy[GROUP];
-    float pz[GROUP], psx[GROUP];
-    float gr, gg, gb, gz;
-    __device__ __forceinline__ float v(int i) const
-    {
-        const int q = i < 32 ? i >> 2 : 8 + ((i - 32) >> 2), e = i & 3;
-        switch (q) {
-            case 0: return pds[e] * pdx[e];
-            case 1: return pds[e] * pdy[e];
-            case 2: return 0.5f * pds[e] * pdx[e] * pdx[e];
-            case 3: return pds[e] * pdx[e] * pdy[e];
-            case 4: return 0.5f * pds[e] * pdy[e] * pdy[e];
-            case 5: return pvo[e];
-            case 6: return pw[e] * gr;
-            case 7: return pw[e] * gg;
-            case 8: return pw[e] * gb;
-            case 9: return pw[e] * gz;
-            case 10: return pz[e];
-            case 11: return pz[e] * pdx[e];
-            case 12: return pz[e] * pdy[e];
-            case 13: return psx[e];
-            default: return 0.0f;
-        }
-    }
-};
-
-// Reduce-scatter of values 0..31 over the warp: lane L ends with the warp sum
-// of value L (levels xor 16, 8, 4, 2, 1; 31 shuffles).  Node I of level L
-// combines nodes I and I + 32 / 2^L of level L - 1; the tree is walked depth
-// first so that few partial sums are live at once.
-template <int L, int I, int BASE = 0>
-__device__ __forceinline__ float rs32(const GroupTerms& g, int lane)
+// Accumulator slots of a staged entry: sums over the CTA's pixels of the
+// per-pixel terms, ds = dL/d sigma, (dx, dy) = pixel centre - mean, w = alpha
+// T_front:
+//   0 ds dx, 1 ds dy, 2 ds dx^2 / 2, 3 ds dx dy, 4 ds dy^2 / 2, 5 ds,
+//   6 w g_r, 7 w g_g, 8 w g_b, 9 w g_depth;
+// with the soft split four more, 10 pz, 11 pz dx, 12 pz dy, 13 psx, where pz =
+// dL/dx kappa and psx = dL/dx x for the split's argument x.
+//
+// The sums become the record's gradient (components 0..9 of the record
+// layout) when the entry leaves the stage:
+//   sigma = -l / log2e, l = a2 dx^2 + b2 dx dy + c2 dy^2, so d sigma / d mean =
+//   -(a dx + b dy, b dx + c dy) with a = -2 a2 / log2e, b = -b2 / log2e,
+//   c = -2 c2 / log2e; and dL/d opacity = sum dL/d alpha G = -sum ds / opacity
+//   (ds = -dL/d alpha alpha, alpha = opacity G where alpha is not clamped; both
+//   terms are zero where it is).
+__device__ __forceinline__ void record_grad(const float* acc, const float4& A, const float4& B, float* out)
 {
-    if constexpr (L == 0) {
-        return g.v(BASE + I);
-    } else {
-        const float a = rs32<L - 1, I, BASE>(g, lane);
-        const float b = rs32<L - 1, I + (32 >> L), BASE>(g, lane);
-        return rs_combine(a, b, lane, 16 >> (L - 1));
-    }
+    const float tx = acc[0] * (1.0f / LOG2E), ty = acc[1] * (1.0f / LOG2E);
+    out[0] = 2.0f * A.z * tx + A.w * ty;
+    out[1] = A.w * tx + 2.0f * B.x * ty;
+    out[2] = acc[2];
+    out[3] = acc[3];
+    out[4] = acc[4];
+    out[5] = B.y > 0.0f ? -acc[5] / B.y : 0.0f;
+#pragma unroll
+    for (int q = 6; q < NGRAD; ++q) out[q] = acc[q];
 }
 
-// Values 32..39 over levels xor 16, 8, 4: lane L ends with the sum over its
-// eight-lane orbit of value 32 + ((L >> 2) & 7); a butterfly over xor 2, 1
-// completes the warp sum.
-template <int L, int I>
-__device__ __forceinline__ float rs8(const GroupTerms& g, int lane)
-{
-    if constexpr (L == 0) {
-        return g.v(32 + I);
-    } else {
-        const float a = rs8<L - 1, I>(g, lane);
-        const float b = rs8<L - 1, I + (8 >> L)>(g, lane);
-        return rs_combine(a, b, lane, 16 >> (L - 1));
-    }
-}
-
-// Adds a staged entry's accumulated gradient (components 0..9 of the record
-// layout) to its Gaussian's row of v_splats: three 16-byte vector atomics, the
-// last of which adds zero to the two padding floats.
-__device__ __forceinline__ void flush_grad(float* __restrict__ v_splats, int g, const float* acc)
+// Adds a gradient row (components 0..9) to its Gaussian's row of v_splats:
+// three 16-byte vector atomics, the last of which adds zero to the two padding
+// floats.
+__device__ __forceinline__ void add_grad_row(float* __restrict__ v_splats, int g, const float* v)
 {
     float4* dst = reinterpret_cast<float4*>(v_splats + 12 * (int64_t)g);
-    atomicAdd(dst, make_float4(acc[0], acc[1], acc[2], acc[3]));
-    atomicAdd(dst + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
-    atomicAdd(dst + 2, make_float4(acc[8], acc[9], 0.0f, 0.0f));
+    atomicAdd(dst, make_float4(v[0], v[1], v[2], v[3]));
+    atomicAdd(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+    atomicAdd(dst + 2, make_float4(v[8], v[9], 0.0f, 0.0f));
 }
 
-// The soft split's sums of one entry, acc[10..13] = (sum pz, sum pz dx,
-// sum pz dy, sum psx), become gradients: the split's argument x = (D - z*)
-// kappa, z* = z_c + g . (p - mean2d), so dL/d mean2d += pz g, dL/d z_c -= pz,
-// dL/d g -= pz d, dL/d sigma_z = -psx / sigma_z (kappa = 1 / (sigma_z s)).
-__device__ __forceinline__ void flush_grad_soft(float* __restrict__ v_splats, float* __restrict__ v_depth_model,
-                                                int g, float* acc, float4 Dm, float softness)
+__device__ __forceinline__ void flush_grad(float* __restrict__ v_splats, int g, const float* acc, const float4& A,
+                                           const float4& B)
 {
-    acc[0] += acc[10] * Dm.x;
-    acc[1] += acc[10] * Dm.y;
-    acc[9] -= acc[10];
-    flush_grad(v_splats, g, acc);
+    float v[NGRAD];
+    record_grad(acc, A, B, v);
+    add_grad_row(v_splats, g, v);
+}
+
+// With the soft split the sums 10..13 add their part: the split's argument x =
+// (D - z*) kappa, z* = z_c + g . (p - mean2d), so dL/d mean2d += pz g, dL/d z_c
+// -= pz, dL/d g -= pz d, dL/d sigma_z = -psx / sigma_z (kappa = 1 / (sigma_z
+// softness)).
+__device__ __forceinline__ void flush_grad_soft(float* __restrict__ v_splats, float* __restrict__ v_depth_model,
+                                                int g, const float* acc, const float4& A, const float4& B,
+                                                const float4& Dm, float softness)
+{
+    float v[NGRAD];
+    record_grad(acc, A, B, v);
+    v[0] += acc[10] * Dm.x;
+    v[1] += acc[10] * Dm.y;
+    v[9] -= acc[10];
+    add_grad_row(v_splats, g, v);
     atomicAdd(reinterpret_cast<float4*>(v_depth_model) + g,
               make_float4(-acc[11], -acc[12], -acc[13] * Dm.z * softness, 0.0f));
 }
@@ -516,10 +492,10 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         // thread on its own slot, so one barrier covers both
         if ((int)threadIdx.x < n_prev && sG[threadIdx.x] >= 0) {
             if (SOFT)
-                flush_grad_soft(v_splats, v_depth_model, sG[threadIdx.x], sAcc[threadIdx.x], sD[threadIdx.x],
-                                sp.softness);
+                flush_grad_soft(v_splats, v_depth_model, sG[threadIdx.x], sAcc[threadIdx.x], sA[threadIdx.x],
+                                sB[threadIdx.x], sD[threadIdx.x], sp.softness);
             else
-                flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x]);
+                flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x], sA[threadIdx.x], sB[threadIdx.x]);
         }
         if (b_end <= r.x) break;
         const int b0 = max(r.x, b_end - CTA_THREADS);
@@ -559,13 +535,13 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                         kj[jj] = -1;
                     }
                 }
-                // per entry: w = alpha T_front, vo = dL/d opacity, ds = dL/d sigma
-                // (soft split: pz = dL/dx kappa, psx = dL/dx x)
-                float pw[GROUP], pvo[GROUP], pds[GROUP], pz[GROUP], psx[GROUP];
+                // per entry: w = alpha T_front, ds = dL/d sigma (soft split: pz = dL/dx
+                // kappa, psx = dL/dx x)
+                float pw[GROUP], pds[GROUP], pz[GROUP], psx[GROUP];
                 bool any = false;
 #pragma unroll
                 for (int jj = 0; jj < GROUP; ++jj) {
-                    pw[jj] = pvo[jj] = pds[jj] = pz[jj] = psx[jj] = 0.0f;
+                    pw[jj] = pds[jj] = pz[jj] = psx[jj] = 0.0f;
                     const int k = kj[jj];
                     if (k < 0 || !inside || b0 - r.x + k >= last) continue;
                     const float4 C3 = sC[k];
@@ -594,11 +570,9 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                     behind = fmaf(w, front, behind);
                     T = Tp;
                     pw[jj] = w;
-                    const float dLdal = SOFT ? dLda * f : dLda;  // dL / d alpha
-                    if (!e.clamped) {  // alpha clamped at 0.99 has no opacity / sigma gradient
-                        pvo[jj] = dLdal * e.G;
-                        pds[jj] = -dLdal * e.alpha;  // d alpha / d sigma = -alpha
-                    }
+                    // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
+                    // d alpha / d sigma = -alpha
+                    if (!e.clamped) pds[jj] = -(SOFT ? dLda * f : dLda) * e.alpha;
                     if (soft) {  // dL/dx = dLda alpha f'(x)
                         const float psi = dLda * e.alpha * sp.density(x, f);
                         pz[jj] = psi * kap;
@@ -606,54 +580,98 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                         vD += psi * kap;
                     }
                 }
-                if (__any_sync(0xffffffffu, any)) {
-                    // the ten gradient components of the four entries summed over the
-                    // warp by one reduce-scatter of 40 values (41 shuffles); the mean
-                    // gradient follows from Sx = sum ds dx, Sy = sum ds dy:
-                    // d sigma / d mean = -(a dx + b dy, b dx + c dy) with a = -2 a2 / log2e,
-                    // b = -b2 / log2e, c = -2 c2 / log2e
-                    GroupTerms gt;
+                if (__any_sync(FULL, any)) {
+                    // Warp sums of the four entries' terms by a reduce-scatter over the
+                    // lanes.  The terms are products whose factors a lane picks by its
+                    // bits 4 and 3 (h4, h3), so the first two levels (lanes xor 16, then
+                    // xor 8) need no select: with X = (1, dx), Y = (1, dy) and G =
+                    // ((g_r, g_g), (g_b, g_depth)), the lane keeps ds X[h4] Y[h3] and
+                    // w G[h4][h3] and sends its partners the other products.  Level 3
+                    // (xor 4) then picks the ds- or the w-term, levels 4 and 5 the
+                    // entry: lane L ends with term (L >> 2) of entry L & 3.  The
+                    // ds dx^2 / 2, ds dy^2 / 2 terms (with the soft split also pz dx, pz
+                    // dy) take a second, shorter reduction of the same form; the soft
+                    // split's pz and psx a third.
+                    const bool h4 = lane & 16, h3 = lane & 8;
+                    const float P0 = h4 ? gb : gr, P1 = h4 ? gz : gg, Q0 = h4 ? gr : gb, Q1 = h4 ? gg : gz;
+                    const float Gkk = h3 ? P1 : P0, Gks = h3 ? P0 : P1, Gsk = h3 ? Q1 : Q0, Gss = h3 ? Q0 : Q1;
+                    float RA[GROUP], RB[GROUP], R2[GROUP];
 #pragma unroll
                     for (int jj = 0; jj < GROUP; ++jj) {
-                        gt.pw[jj] = pw[jj];
-                        gt.pvo[jj] = pvo[jj];
-                        gt.pds[jj] = pds[jj];
                         // pixel offsets recomputed (the same roundings as eval_splat)
-                        // rather than kept live through the group: fewer registers
-                        const float2 mean = *reinterpret_cast<const float2*>(&sA[kj[jj] < 0 ? 0 : kj[jj]]);
-                        gt.pdx[jj] = __fsub_rn(px, mean.x);
-                        gt.pdy[jj] = __fsub_rn(py, mean.y);
-                    }
-                    gt.gr = gr; gt.gg = gg; gt.gb = gb; gt.gz = gz;
-                    if (SOFT) {
-#pragma unroll
-                        for (int jj = 0; jj < GROUP; ++jj) {
-                            gt.pz[jj] = pz[jj];
-                            gt.psx[jj] = psx[jj];
+                        // rather than kept live through the group: fewer registers; a
+                        // missing entry (all terms zero) borrows the first one's mean
+                        const float2 mean = *reinterpret_cast<const float2*>(&sA[kj[jj] < 0 ? kj[0] : kj[jj]]);
+                        const float dx = __fsub_rn(px, mean.x), dy = __fsub_rn(py, mean.y);
+                        const float ds = pds[jj], w = pw[jj];
+                        const float dsx = ds * dx;
+                        const float Ak = h4 ? dsx : ds, As = h4 ? ds : dsx;  // ds X[h4], ds X[!h4]
+                        const float Yk = h3 ? dy : 1.0f, Ys = h3 ? 1.0f : dy;  // Y[h3], Y[!h3]
+                        float K = Ak * Yk + __shfl_xor_sync(FULL, As * Yk, 16);
+                        float S = Ak * Ys + __shfl_xor_sync(FULL, As * Ys, 16);
+                        RA[jj] = K + __shfl_xor_sync(FULL, S, 8);
+                        K = w * Gkk + __shfl_xor_sync(FULL, w * Gsk, 16);
+                        S = w * Gks + __shfl_xor_sync(FULL, w * Gss, 16);
+                        RB[jj] = K + __shfl_xor_sync(FULL, S, 8);
+                        // ds dx^2 / 2 kept by h4 = 0, ds dy^2 / 2 by h4 = 1; with the soft
+                        // split also pz dx, pz dy: u[b4] F[b3] with u = (dx, dy), F = (u ds / 2,
+                        // pz), two select-free levels like the first reduction's
+                        const float hds = 0.5f * ds, uk = h4 ? dy : dx, us = h4 ? dx : dy;
+                        const float hk = hds * uk, hs = hds * us;
+                        if (SOFT) {
+                            const float z = pz[jj];
+                            K = uk * (h3 ? z : hk) + __shfl_xor_sync(FULL, us * (h3 ? z : hs), 16);
+                            S = uk * (h3 ? hk : z) + __shfl_xor_sync(FULL, us * (h3 ? hs : z), 16);
+                            R2[jj] = K + __shfl_xor_sync(FULL, S, 8);
+                        } else {
+                            R2[jj] = hk * uk + __shfl_xor_sync(FULL, hs * us, 16);
                         }
                     }
-                    float tot = rs32<5, 0>(gt, lane);  // component lane >> 2 of entry lane & 3
-                    const int q = lane >> 2, e = lane & 3;
-                    const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
-                    const float other = __shfl_xor_sync(0xffffffffu, tot, 4);  // Sx <-> Sy of the entry
-                    if (q < 2 && k >= 0) {
-                        const float a2 = sA[k].z, b2 = sA[k].w, c2 = sB[k].x;
-                        const float tx = (q == 0 ? tot : other) * (1.0f / LOG2E);
-                        const float ty = (q == 0 ? other : tot) * (1.0f / LOG2E);
-                        tot = q == 0 ? 2.0f * a2 * tx + b2 * ty : b2 * tx + 2.0f * c2 * ty;
+                    {   // levels 3..5: the term kind, then the entry
+                        const float T0 = rs_combine(RA[0], RB[0], lane, 4), T1 = rs_combine(RA[1], RB[1], lane, 4);
+                        const float T2 = rs_combine(RA[2], RB[2], lane, 4), T3 = rs_combine(RA[3], RB[3], lane, 4);
+                        const float U0 = rs_combine(T0, T2, lane, 2), U1 = rs_combine(T1, T3, lane, 2);
+                        const float tot = rs_combine(U0, U1, lane, 1);
+                        const int e = lane & 3;
+                        const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
+                        // slot of ds X[h4] Y[h3] (lane bit 2 clear) or w G[h4][h3] (set)
+                        const int slot = (lane & 4) ? 6 + (h4 ? 2 : 0) + (h3 ? 1 : 0)
+                                                    : (h4 ? (h3 ? 3 : 0) : (h3 ? 1 : 5));
+                        if (k >= 0 && tot != 0.0f) atomicAdd(&sAcc[k][slot], tot);
                     }
-                    if (k >= 0 && tot != 0.0f) atomicAdd(&sAcc[k][q], tot);
-                    if (SOFT) {
-                        // values 32..55 (components 8..13): a second full reduce-scatter
-                        const float t2 = rs32<5, 0, 32>(gt, lane);
-                        if (q < 6 && k >= 0 && t2 != 0.0f) atomicAdd(&sAcc[k][8 + q], t2);
+                    if (!SOFT) {  // ds dx^2 / 2, ds dy^2 / 2: the entry by lane bits 3, 2,
+                                  // then a butterfly over bits 1, 0
+                        const float V0 = rs_combine(R2[0], R2[2], lane, 8), V1 = rs_combine(R2[1], R2[3], lane, 8);
+                        float t2 = rs_combine(V0, V1, lane, 4);
+                        t2 += __shfl_xor_sync(FULL, t2, 2);
+                        t2 += __shfl_xor_sync(FULL, t2, 1);
+                        const int e = (lane >> 2) & 3;
+                        const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
+                        if ((lane & 3) == 0 && k >= 0 && t2 != 0.0f) atomicAdd(&sAcc[k][h4 ? 4 : 2], t2);
                     } else {
-                        float t8 = rs8<3, 0>(gt, lane);
-                        t8 += __shfl_xor_sync(0xffffffffu, t8, 2);
-                        t8 += __shfl_xor_sync(0xffffffffu, t8, 1);
-                        const int j = (lane >> 2) & 7, e8 = j & 3;
-                        const int k8 = e8 == 0 ? kj[0] : e8 == 1 ? kj[1] : e8 == 2 ? kj[2] : kj[3];
-                        if ((lane & 3) == 0 && k8 >= 0 && t8 != 0.0f) atomicAdd(&sAcc[k8][8 + (j >> 2)], t8);
+                        {   // ds dx^2 / 2, ds dy^2 / 2, pz dx, pz dy: the entry by lane bits 2,
+                            // 1, then a butterfly over bit 0
+                            const float W0 = rs_combine(R2[0], R2[2], lane, 4), W1 = rs_combine(R2[1], R2[3], lane, 4);
+                            float t2 = rs_combine(W0, W1, lane, 2);
+                            t2 += __shfl_xor_sync(FULL, t2, 1);
+                            const int e = (lane >> 1) & 3;
+                            const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
+                            const int slot = h3 ? (h4 ? 12 : 11) : (h4 ? 4 : 2);
+                            if ((lane & 1) == 0 && k >= 0 && t2 != 0.0f) atomicAdd(&sAcc[k][slot], t2);
+                        }
+                        // pz (kept by h4 = 0), psx (h4 = 1): the entry by lane bits 3, 2, then a
+                        // butterfly over bits 1, 0
+                        float R3[GROUP];
+#pragma unroll
+                        for (int jj = 0; jj < GROUP; ++jj)
+                            R3[jj] = (h4 ? psx[jj] : pz[jj]) + __shfl_xor_sync(FULL, h4 ? pz[jj] : psx[jj], 16);
+                        const float V0 = rs_combine(R3[0], R3[2], lane, 8), V1 = rs_combine(R3[1], R3[3], lane, 8);
+                        float t3 = rs_combine(V0, V1, lane, 4);
+                        t3 += __shfl_xor_sync(FULL, t3, 2);
+                        t3 += __shfl_xor_sync(FULL, t3, 1);
+                        const int e = (lane >> 2) & 3;
+                        const int k = e == 0 ? kj[0] : e == 1 ? kj[1] : e == 2 ? kj[2] : kj[3];
+                        if ((lane & 3) == 0 && k >= 0 && t3 != 0.0f) atomicAdd(&sAcc[k][h4 ? 13 : 10], t3);
                     }
                 }
             }
