@@ -160,10 +160,10 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 PROFILED_TRAFFIC = {
     "composite_bwd": {
         "kernel": "k_composite_bwd",
-        "bytes": 160982272 + 11324160,
+        "bytes": 160749312 + 11179776,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "97f89d799ca63d2f4e92b6d11415b23a7a9c28e3db4fd5654e118c19a132427a",
+                "2aa73d489c78fde28e92d9d1bd7884a5c795cf219f7a9c8230d5ec1339c06e46",
         },
         "profile": "profiles/composite_bwd_soup_1080p.md",
     },

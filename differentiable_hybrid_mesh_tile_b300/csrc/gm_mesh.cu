@@ -295,12 +295,21 @@ __device__ __forceinline__ void interp_grad(const Cam& c, const float X[3][3], c
     }
 }
 
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+// Per-face sums of a warp's pixel gradients.  Each pixel has 18 values (the
+// position and the colour gradient of the face's three vertices); the lanes
+// park them in shared memory, then take the (face, component) sums of the
+// warp's distinct faces 32 at a time: each adds its component over the face's
+// pixels and issues one global atomic.  A warp with K faces thus costs
+// ceil(18 K / 32) rounds instead of 18 K warp-wide sums.
+constexpr int MB_WARPS = TILE_PIX / 32;
+constexpr int MB_VALS = 18;
+
+struct MeshBwdStage {
+    float val[MB_WARPS][MB_VALS][33];  // [warp][component][lane], padded: conflict-free reads across components
+    int vid[MB_WARPS][3][32];
+    uint32_t peers[MB_WARPS][32];
+    uint8_t lead[MB_WARPS][32];
+};
 
 // DIRECT: g_rgb / g_depth are already dL/d(interpolated colour, depth) per pixel
 // (from the antialiasing's backward); otherwise they are the image's upstream
@@ -312,11 +321,12 @@ k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
            const float* __restrict__ g_rgb, const float* __restrict__ g_depth,
            const float* __restrict__ v_mesh_depth, float* __restrict__ v_verts, float* __restrict__ v_vcol)
 {
+    __shared__ MeshBwdStage st;
     const int tile = blockIdx.x;
     const int tx = tile % c.TW, ty = tile / c.TW;
     const int i = tx * TILE + (threadIdx.x & (TILE - 1));
     const int j = ty * TILE + (threadIdx.x >> 4);
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int f = -1;
     if (i < c.W && j < c.H) f = face_id[(int64_t)j * c.W + i];
     float gX[3][3], gC[3][3];
@@ -334,38 +344,38 @@ k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
         // dL/dD: through the depth output (T D), and through the soft split when given
         const float gD = T * g_depth[pix] + (!DIRECT && v_mesh_depth ? v_mesh_depth[pix] : 0.0f);
         interp_grad(c, X, C, (float)i + 0.5f, (float)j + 0.5f, gD, gc, gX, gC);
-    }
-    // one set of atomics per distinct face in the warp
-    unsigned pending = __ballot_sync(0xffffffffu, act);
-    while (pending) {
-        const int leader = __ffs(pending) - 1;
-        const int fl = __shfl_sync(0xffffffffu, f, leader);
-        const bool mine = act && f == fl;
-        const unsigned m = __ballot_sync(0xffffffffu, mine);
-        if (__popc(m) == 1) {
-            if (lane == leader) {
 #pragma unroll
-                for (int k = 0; k < 3; ++k)
+        for (int k = 0; k < 3; ++k) {
+            st.vid[w][k][lane] = vid[k];
 #pragma unroll
-                    for (int d = 0; d < 3; ++d) {
-                        atomicAdd(v_verts + 3 * (int64_t)vid[k] + d, gX[k][d]);
-                        atomicAdd(v_vcol + 3 * (int64_t)vid[k] + d, gC[k][d]);
-                    }
+            for (int d = 0; d < 3; ++d) {
+                st.val[w][3 * k + d][lane] = gX[k][d];
+                st.val[w][9 + 3 * k + d][lane] = gC[k][d];
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 3; ++k)
-#pragma unroll
-                for (int d = 0; d < 3; ++d) {
-                    float a = warp_sum(mine ? gX[k][d] : 0.0f);
-                    float b = warp_sum(mine ? gC[k][d] : 0.0f);
-                    if (lane == leader) {
-                        atomicAdd(v_verts + 3 * (int64_t)vid[k] + d, a);
-                        atomicAdd(v_vcol + 3 * (int64_t)vid[k] + d, b);
-                    }
-                }
         }
-        pending &= ~m;
+    }
+    // the lanes of each face; a face's lowest lane leads it
+    const uint32_t peers = __match_any_sync(0xffffffffu, act ? f : -1);
+    const bool leader = act && lane == __ffs(peers) - 1;
+    const uint32_t leaders = __ballot_sync(0xffffffffu, leader);
+    if (leader) {
+        st.peers[w][lane] = peers;
+        st.lead[w][__popc(leaders & ((1u << lane) - 1u))] = (uint8_t)lane;
+    }
+    __syncwarp();
+    const int items = MB_VALS * __popc(leaders);
+    for (int t = lane; t < items; t += 32) {
+        const int fi = t / MB_VALS, q = t - fi * MB_VALS;
+        const int ld = st.lead[w][fi];
+        uint32_t m = st.peers[w][ld];
+        float sum = 0.0f;
+        while (m) {
+            sum += st.val[w][q][__ffs(m) - 1];
+            m &= m - 1;
+        }
+        const int k = (q % 9) / 3, d = q % 3;
+        float* dst = q < 9 ? v_verts : v_vcol;
+        if (sum != 0.0f) atomicAdd(dst + 3 * (int64_t)st.vid[w][k][ld] + d, sum);
     }
 }
 
