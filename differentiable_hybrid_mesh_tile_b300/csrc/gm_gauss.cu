@@ -271,14 +271,18 @@ __device__ __forceinline__ float tile_min_sigma(const BinShape& s, int tx, int t
     return best;
 }
 
+// Whether the mesh hides the Gaussian (centre depth, hide depth) in tile t.
+__device__ __forceinline__ bool tile_hidden(const BinRule& r, int t, float depth, float hide)
+{
+    if (!r.cull || !__ldg(r.tile_full + t)) return false;
+    const float far = __ldg(r.tile_far + t);
+    // the soft split's per-pixel skip takes the same bound against each pixel's depth
+    return r.soft ? hide > far + 4e-6f * fabsf(far) : depth >= far;
+}
+
 __device__ __forceinline__ bool keep_tile(const BinRule& r, const BinShape& s, int tx, int ty)
 {
-    const int t = ty * r.TW + tx;
-    if (r.cull && __ldg(r.tile_full + t)) {
-        const float far = __ldg(r.tile_far + t);
-        // the soft split's per-pixel skip takes the same bound against each pixel's depth
-        if (r.soft ? s.hide > far + 4e-6f * fabsf(far) : s.depth >= far) return false;
-    }
+    if (tile_hidden(r, ty * r.TW + tx, s.depth, s.hide)) return false;
     return !r.tile_test || tile_min_sigma(s, tx, ty) <= s.smax;
 }
 
@@ -320,101 +324,95 @@ k_gauss_depth_keys(Cam c, int N, const float4* __restrict__ splats, const int32_
     dval[g] = g;
 }
 
-// Per Gaussian: the number of tiles it is binned to after the cull and the
-// tile test, and its depth key (float bits of the centre depth; 0xffffffff
-// when it emits nothing) for the depth pre-sort.
+// What the binning keeps of a Gaussian, one record per position of the depth
+// order: a = (x0, y0, rectangle width, Gaussian id), b = (rectangle area in
+// tiles, tile mask, centre-depth bits, hide-depth bits).  For a rectangle of
+// at most SMALL_RECT tiles the mask holds the tiles (row-major bit order) the
+// per-tile ellipse test keeps; larger rectangles are tested tile by tile when
+// they are binned.  An empty rectangle or an invalid id has area 0.
+struct GaussRec {
+    int4 a, b;
+};
+
+// Per position i of the depth order: the Gaussian's tile rectangle and the
+// ellipse test of its tiles.  Needs no mesh, so it runs before the mesh layer
+// exists; only the occlusion cull waits for it.
 __global__ void __launch_bounds__(256)
-k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
-              int32_t* __restrict__ counts, uint32_t* __restrict__ kept, int32_t* counters)
+k_gauss_shape(Cam c, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
+              const int32_t* __restrict__ order, GaussRec* __restrict__ rec, int32_t* counters)
 {
     __shared__ int s_pre[8];
     __shared__ BinShape s_shape[256];
-    __shared__ int4 s_rect[256];  // x0, y0, width, -
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ int4 s_rect[256];  // x0, y0, width, 1 / width bits
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int wbase = threadIdx.x & ~31;
-    int pre = 0, post = 0;
-    uint32_t mask = 0;
-    int x0 = 0, y0 = 0, x1 = 0, y1 = 0;
+    int g = -1, pre = 0, x0 = 0, y0 = 0, x1 = 0, y1 = 0;
     BinShape sh = {};
-    if (g < N) {
-        const int r = radii[g];
-        if (r > 0) {
-            sh = bin_shape(splats, g);
-            if (gauss_rect(c, sh.mx, sh.my, r, x0, y0, x1, y1)) pre = (x1 - x0) * (y1 - y0);
+    if (i < N) {
+        const int gi = order[i];
+        if (gi >= 0 && gi < N) {
+            const int r = radii[gi];
+            if (r > 0) {
+                sh = bin_shape(splats, gi);
+                if (gauss_rect(c, sh.mx, sh.my, r, x0, y0, x1, y1)) {
+                    pre = (x1 - x0) * (y1 - y0);
+                    g = gi;
+                }
+            }
         }
     }
-    if (!rule.cull && !rule.tile_test) {
-        post = pre;
-        mask = 0xffffffffu;
-    } else {
-        // the (Gaussian, tile) pairs of the warp's small rectangles, flattened so
-        // that each lane tests one pair per round whatever the rectangle sizes
-        const int a = pre <= SMALL_RECT ? pre : 0;
-        int o = a;  // inclusive prefix sum over the lanes
+    BinRule rule = {};
+    rule.tile_test = true;
+    rule.TW = c.TW;
+    // the (Gaussian, tile) pairs of the warp's small rectangles, flattened so that
+    // each lane tests one pair per round whatever the rectangle sizes
+    uint32_t mask = 0;
+    const int a = pre <= SMALL_RECT ? pre : 0;
+    int o = a;  // inclusive prefix sum over the lanes
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, o, d);
-            if (lane >= d) o += y;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, o, d);
+        if (lane >= d) o += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, o, 31);
+    o -= a;  // exclusive
+    s_shape[threadIdx.x] = sh;
+    s_rect[threadIdx.x] = make_int4(x0, y0, x1 - x0, __float_as_int(__frcp_rn((float)max(x1 - x0, 1))));
+    __syncwarp();
+    for (int base = 0; base < total; base += 32) {
+        const int p = base + lane;
+        // owner of pair p: the last lane whose first pair is at or before p (all
+        // lanes take part in the search; lanes past the last pair test nothing)
+        int j = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+            const int oj = __shfl_sync(0xffffffffu, o, j + step);
+            if (oj <= p) j += step;
         }
-        const int total = __shfl_sync(0xffffffffu, o, 31);
-        o -= a;  // exclusive
-        s_shape[threadIdx.x] = sh;
-        s_rect[threadIdx.x] = make_int4(x0, y0, x1 - x0, __float_as_int(__frcp_rn((float)max(x1 - x0, 1))));
-        __syncwarp();
-        for (int base = 0; base < total; base += 32) {
-            const int p = base + lane;
-            // owner of pair p: the last lane whose first pair is at or before p (all
-            // lanes take part in the search; lanes past the last pair test nothing)
-            int j = 0;
-#pragma unroll
-            for (int step = 16; step > 0; step >>= 1) {
-                const int oj = __shfl_sync(0xffffffffu, o, j + step);
-                if (oj <= p) j += step;
-            }
-            const int oj = __shfl_sync(0xffffffffu, o, j);
-            bool keep = false;
-            if (p < total) {
-                const int4 rc = s_rect[wbase + j];
-                const int t_in = p - oj;
-                int row, col;
-                divmod_small(t_in, rc.z, __int_as_float(rc.w), row, col);
-                keep = keep_tile(rule, s_shape[wbase + j], rc.x + col, rc.y + row);
-            }
-            const uint32_t km = __ballot_sync(0xffffffffu, keep);
-            // this lane's own pairs in the round: positions [lo, hi) of km
-            const int lo = max(o, base) - base, hi = min(o + a, base + 32) - base;
-            if (lo < hi) {
-                const uint32_t bits = (hi - lo == 32 ? km : (km >> lo) & ((1u << (hi - lo)) - 1u));
-                mask |= bits << (lo + base - o);
-            }
+        const int oj = __shfl_sync(0xffffffffu, o, j);
+        bool keep = false;
+        if (p < total) {
+            const int4 rc = s_rect[wbase + j];
+            const int t_in = p - oj;
+            int row, col;
+            divmod_small(t_in, rc.z, __int_as_float(rc.w), row, col);
+            keep = keep_tile(rule, s_shape[wbase + j], rc.x + col, rc.y + row);
         }
-        post = __popc(mask);
-        uint32_t big = __ballot_sync(0xffffffffu, pre > SMALL_RECT);
-        while (big) {
-            const int j = __ffs(big) - 1;
-            big &= big - 1;
-            const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
-            const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, pre, j);
-            const BinShape js = shfl_shape(sh, j);
-            const float jinv = __frcp_rn((float)jw);
-            int cnt = 0;
-            for (int t = lane; t < jarea; t += 32) {
-                int row, col;
-                divmod_small(t, jw, jinv, row, col);
-                cnt += keep_tile(rule, js, jx0 + col, jy0 + row);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-            if (lane == j) post = cnt;
+        const uint32_t km = __ballot_sync(0xffffffffu, keep);
+        // this lane's own pairs in the round: positions [lo, hi) of km
+        const int lo = max(o, base) - base, hi = min(o + a, base + 32) - base;
+        if (lo < hi) {
+            const uint32_t bits = (hi - lo == 32 ? km : (km >> lo) & ((1u << (hi - lo)) - 1u));
+            mask |= bits << (lo + base - o);
         }
     }
-    if (g < N) {
-        counts[g] = post;
-        kept[g] = mask;
+    if (i < N) {
+        rec[i].a = make_int4(x0, y0, x1 - x0, g);
+        rec[i].b = make_int4(pre, (int)mask, __float_as_int(sh.depth), __float_as_int(sh.hide));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    for (int d = 16; d > 0; d >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, d);
     if (lane == 0) s_pre[threadIdx.x >> 5] = pre;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -424,16 +422,76 @@ k_gauss_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, con
     }
 }
 
-// Emits the (tile << 32 | depth bits, id) entries of the i-th Gaussian in
-// ascending (depth, id) order at offsets[i]: entries come out depth-sorted,
-// so a stable sort on the tile bits alone completes the (tile, depth, id) order.
-// The tiles kept are exactly those k_gauss_count counted: its bit mask for
-// small rectangles, the same predicate for large ones.
+// Per position i of the depth order: the tiles the Gaussian is binned to now
+// that the mesh's tile bounds exist -- for a small rectangle its ellipse-kept
+// tiles less those the mesh hides, for a large one every tile of the rectangle
+// tested again by the whole warp -- as a count (for the scan) and, for a small
+// rectangle, the kept mask (for the emission).
 __global__ void __launch_bounds__(256)
-k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
-             const int32_t* __restrict__ order, const int32_t* __restrict__ counts,
-             const uint32_t* __restrict__ kept, const int32_t* __restrict__ offsets, int cap, int32_t* counters,
-             uint64_t* __restrict__ keys, int32_t* __restrict__ vals)
+k_gauss_cull(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
+             int32_t* __restrict__ counts, uint32_t* __restrict__ kept)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    int4 ra = make_int4(0, 0, 0, -1), rb = make_int4(0, 0, 0, 0);
+    if (i < N) {
+        ra = rec[i].a;
+        rb = rec[i].b;
+    }
+    const int area = rb.x;
+    uint32_t mask = 0;
+    int post = 0;
+    if (area > 0 && area <= SMALL_RECT) {
+        mask = rule.tile_test ? (uint32_t)rb.y : ((1u << area) - 1u);
+        if (rule.cull) {
+            const float depth = __int_as_float(rb.z), hide = __int_as_float(rb.w);
+            const float inv = __frcp_rn((float)ra.z);
+            for (uint32_t m = mask; m; m &= m - 1) {
+                const int pos = __ffs(m) - 1;
+                int row, col;
+                divmod_small(pos, ra.z, inv, row, col);
+                if (tile_hidden(rule, (ra.y + row) * c.TW + ra.x + col, depth, hide)) mask &= ~(1u << pos);
+            }
+        }
+        post = __popc(mask);
+    }
+    // large rectangles (near-camera Gaussians): the whole warp, 32 tiles at a time
+    BinShape sh = {};
+    if (area > SMALL_RECT) sh = bin_shape(splats, ra.w);
+    uint32_t big = __ballot_sync(0xffffffffu, area > SMALL_RECT);
+    while (big) {
+        const int j = __ffs(big) - 1;
+        big &= big - 1;
+        const int jx0 = __shfl_sync(0xffffffffu, ra.x, j), jy0 = __shfl_sync(0xffffffffu, ra.y, j);
+        const int jw = __shfl_sync(0xffffffffu, ra.z, j), jarea = __shfl_sync(0xffffffffu, area, j);
+        const BinShape js = shfl_shape(sh, j);
+        const float jinv = __frcp_rn((float)jw);
+        int cnt = 0;
+        for (int t = lane; t < jarea; t += 32) {
+            int row, col;
+            divmod_small(t, jw, jinv, row, col);
+            cnt += keep_tile(rule, js, jx0 + col, jy0 + row);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        if (lane == j) post = cnt;
+    }
+    if (i < N) {
+        counts[i] = post;
+        kept[i] = mask;
+    }
+}
+
+// Emits the (tile << 32 | depth bits, id) entries of the Gaussian at position
+// i of the depth order, in ascending (depth, id) order, at offsets[i]: entries
+// come out depth-sorted, so a stable sort on the tile bits alone completes the
+// (tile, depth, id) order.  The tiles kept are exactly those k_gauss_cull
+// counted: its mask for small rectangles, the same predicate for large ones.
+__global__ void __launch_bounds__(256)
+k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
+             const int32_t* __restrict__ counts, const uint32_t* __restrict__ kept,
+             const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
+             int32_t* __restrict__ vals)
 {
     __shared__ int4 s_a[256];   // x0, y0, width, Gaussian id
     __shared__ int2 s_b[256];   // depth bits, first output slot
@@ -442,27 +500,26 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
     const int lane = threadIdx.x & 31;
     const int wbase = threadIdx.x & ~31;
     if (i == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
-    int g = -1, x0 = 0, y0 = 0, x1 = 0, y1 = 0, area = 0;
+    int4 ra = make_int4(0, 0, 0, -1);
+    int area = 0, dbits = 0;
     BinShape sh = {};
     uint32_t mask = 0;
     int64_t o = 0;
-    float depth = 0.0f;
     if (i < N) {
-        g = order[i];
-        if (g >= 0 && g < N && counts[g] > 0) {
-            const float4 s0 = splats[3 * (int64_t)g];
-            depth = splats[3 * (int64_t)g + 2].y;
-            if (gauss_rect(c, s0.x, s0.y, radii[g], x0, y0, x1, y1)) area = (x1 - x0) * (y1 - y0);
+        const int4 rb = rec[i].b;
+        if (rb.x > 0 && counts[i] > 0) {
+            ra = rec[i].a;
+            area = rb.x;
+            dbits = rb.z;
             o = offsets[i];
-            mask = kept[g];
-            if (area > SMALL_RECT) sh = bin_shape(splats, g);  // the big-rectangle path tests again
+            mask = kept[i];
+            if (area > SMALL_RECT) sh = bin_shape(splats, ra.w);  // the big-rectangle path tests again
         }
     }
-    const uint32_t dbits = __float_as_uint(depth);
     {
         // the kept tiles of the warp's small rectangles, flattened: one entry per
         // lane per round, consecutive lanes writing consecutive slots
-        const uint32_t m = (area > 0 && area <= SMALL_RECT) ? mask & ((1u << area) - 1u) : 0u;
+        const uint32_t m = (area > 0 && area <= SMALL_RECT) ? mask : 0u;
         const int a = __popc(m);
         int p0 = a;  // inclusive prefix sum over the lanes
 #pragma unroll
@@ -472,8 +529,8 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
         }
         const int total = __shfl_sync(0xffffffffu, p0, 31);
         p0 -= a;
-        s_a[threadIdx.x] = make_int4(x0, y0, x1 - x0, g);
-        s_b[threadIdx.x] = make_int2((int)dbits, (int)o);
+        s_a[threadIdx.x] = ra;
+        s_b[threadIdx.x] = make_int2(dbits, (int)o);
         s_m[threadIdx.x] = m;
         __syncwarp();
         for (int base = 0; base < total; base += 32) {
@@ -497,15 +554,15 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
                         pos += st;
                     }
                 }
-                const int4 ra = s_a[wbase + j];
-                const int2 rb = s_b[wbase + j];
-                const int64_t dst = (int64_t)rb.y + r;
+                const int4 qa = s_a[wbase + j];
+                const int2 qb = s_b[wbase + j];
+                const int64_t dst = (int64_t)qb.y + r;
                 if (dst >= 0 && dst < cap) {
                     int row, col;
-                    divmod_small(pos, ra.z, __frcp_rn((float)ra.z), row, col);
-                    const int t = (ra.y + row) * c.TW + ra.x + col;
-                    keys[dst] = ((uint64_t)(uint32_t)t << 32) | (uint32_t)rb.x;
-                    vals[dst] = ra.w;
+                    divmod_small(pos, qa.z, __frcp_rn((float)qa.z), row, col);
+                    const int t = (qa.y + row) * c.TW + qa.x + col;
+                    keys[dst] = ((uint64_t)(uint32_t)t << 32) | (uint32_t)qb.x;
+                    vals[dst] = qa.w;
                 }
             }
         }
@@ -514,9 +571,9 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
     while (big) {
         const int j = __ffs(big) - 1;
         big &= big - 1;
-        const int jx0 = __shfl_sync(0xffffffffu, x0, j), jy0 = __shfl_sync(0xffffffffu, y0, j);
-        const int jw = __shfl_sync(0xffffffffu, x1, j) - jx0, jarea = __shfl_sync(0xffffffffu, area, j);
-        const int jg = __shfl_sync(0xffffffffu, g, j);
+        const int jx0 = __shfl_sync(0xffffffffu, ra.x, j), jy0 = __shfl_sync(0xffffffffu, ra.y, j);
+        const int jw = __shfl_sync(0xffffffffu, ra.z, j), jarea = __shfl_sync(0xffffffffu, area, j);
+        const int jg = __shfl_sync(0xffffffffu, ra.w, j);
         const BinShape js = shfl_shape(sh, j);
         const uint32_t jbits = __float_as_uint(js.depth);
         const float jinv = __frcp_rn((float)jw);
@@ -620,19 +677,23 @@ size_t gauss_bin_ws_bytes(int N, int cap)
 {
     int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
     return scan_ws_bytes(n) + 3 * a256(sizeof(int32_t) * n) + 2 * a256(sizeof(uint64_t) * n) +
-           2 * a256(sizeof(int32_t) * n) + 256 + sort_ws_bytes(n > k ? n : k);
+           2 * a256(sizeof(int32_t) * n) + a256(sizeof(GaussRec) * n) + 256 + sort_ws_bytes(n > k ? n : k);
 }
 
 // Tile binning of the Gaussians.  The entries' order (tile, depth, id) is
 // reached in two stable LSD sorts: the N Gaussians by depth (32 bits), then,
 // after emitting each Gaussian's tiles in that order, the K entries by tile
 // only (ceil(log2 T) bits) -- instead of one 32 + log2 T bit sort of K keys.
+// The first half (depth sort, rectangles and ellipse tests, one record per
+// position of the depth order) needs no mesh; the second (occlusion cull,
+// scan, emission, tile sort) reads the records in order, with no gathers.
 struct GaussWs {
     ScanWs sw;
     int32_t *counts, *offsets;
     uint32_t* kept;
     uint64_t *dkey, *dkey_alt;
     int32_t *dval, *dval_alt, *n_dev;
+    GaussRec* rec;
     SortWs so;
 };
 
@@ -656,6 +717,8 @@ static GaussWs carve_gauss_ws(void* ws, int N, int cap)
     b += a256(sizeof(int32_t) * n);
     w.dval_alt = (int32_t*)b;
     b += a256(sizeof(int32_t) * n);
+    w.rec = (GaussRec*)b;
+    b += a256(sizeof(GaussRec) * n);
     w.n_dev = (int32_t*)b;
     b += 256;
     carve_sort_ws(b, n > k ? n : k, w.so);
@@ -672,7 +735,11 @@ cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int
                                                         w.dval, w.n_dev);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4 passes: even, the result is back in dkey / dval
-    return radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s);
+    e = radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s);
+    if (e != cudaSuccess) return e;
+    k_gauss_shape<<<(N + 255) / 256, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dval,
+                                                   w.rec, counters);
+    return cudaGetLastError();
 }
 
 cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N, const float* splats,
@@ -697,11 +764,11 @@ cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N,
         rule.tile_far = tile_far;
         rule.tile_full = tile_full;
         rule.TW = c.TW;
-        k_gauss_count<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, w.counts, w.kept, counters);
+        k_gauss_cull<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = exclusive_scan(w.counts, w.dval, w.offsets, N, counters, w.sw, s)) != cudaSuccess) return e;
-        k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, radii, w.dval, w.counts, w.kept, w.offsets, cap, counters,
-                                          ek, ev);
+        if ((e = exclusive_scan(w.counts, nullptr, w.offsets, N, counters, w.sw, s)) != cudaSuccess) return e;
+        k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept, w.offsets, cap, counters, ek,
+                                          ev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (tb > 0) {
             if (passes % 2)

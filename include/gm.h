@@ -338,8 +338,9 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
  * gm_sort_gaussians_by_depth + gm_bin_gaussians -- gm_bin_sort_gaussians in
  * two halves, for callers that overlap the first with the mesh layer: the
  * depth pre-sort of the Gaussians (centre depth, ascending; ids break ties;
- * Gaussians whose tile rectangle is empty last) needs only splats / radii;
- * the binning, culling, emission and tile sort need tile_far / tile_full.
+ * Gaussians whose tile rectangle is empty last), their tile rectangles and
+ * the per-tile ellipse test need only splats / radii; the occlusion cull,
+ * emission and tile sort need tile_far / tile_full.
  * Call both, in this order, with the same N, cap and workspace (nothing else
  * may use the workspace in between); the results equal gm_bin_sort_gaussians'.
  * gm_sort_gaussians_by_depth zeroes counters; gm_bin_gaussians reports the

@@ -140,6 +140,8 @@ def test_bin_sort_teacher_forced_exact(bcase, cull, orc):
     cnt = np.diff(start)
     np.testing.assert_array_equal(tr[:, 1] - tr[:, 0], cnt)
     np.testing.assert_array_equal(tr[cnt > 0, 0], start[:-1][cnt > 0])
+    if name == "sphere512":  # rectangles of more than 16 tiles take the warp-wide path
+        assert (np.bincount(gids) > 16).any()
     print("%s cull=%d: K=%d (pre-cull %d), %d sort partitions" % (name, cull, len(keys), pre, -(-len(keys) // 3840)))
 
 
