@@ -364,9 +364,9 @@ def run_gm(args, ws, rank, local):
     work = {
         # bytes the stage must move at least once
         "project": ("hbm", N * (12 + 12 + 16 + 4 + col_bytes) + N * (48 + 4 + 4)),
-        # count: mean+depth+radius in, count + depth key + id out; depth sort: histogram +
-        # 4 passes of key+id; scan of the counts in depth order; emit: order, count,
-        # offset, splat in, one key+id per entry out; tile sort; ranges
+        # rectangles and tests: mean+depth+radius in, count + depth key + id out; depth sort:
+        # histogram + 4 passes of key+id; scan of the counts in depth order; emit: order,
+        # count, offset, splat in, one key+id per entry out; tile sort; ranges
         "bin_sort": ("hbm", N * (20 + 16) + N * (8 + 4 * 24) + N * 12 + N * 32 + K_g * 12
                      + K_g * (8 + passes_g * 24) + K_g * 8 + T * 8),
         "tri_bin": ("hbm", F * (12 + 36) * 2 + F * 12 + K_tri * 12 + K_tri * 8 + passes_t * K_tri * 24
