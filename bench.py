@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--no-multiview", action="store_true", help="skip the batched 8-view measurement")
     ap.add_argument("--no-soft", action="store_true", help="skip the soft-split measurement")
     ap.add_argument("--no-aa", action="store_true", help="skip the antialiased-mesh measurement")
-    ap.add_argument("--cpu-tiles", type=int, default=48, help="tiles of the frame the CPU oracle renders")
+    ap.add_argument("--cpu-tiles", type=int, default=600,
+                    help="tiles of the frame the CPU oracle renders (about 10 s of oracle work at 1080p)")
     return ap.parse_args()
 
 
@@ -341,6 +342,10 @@ def run_gm(args, ws, rank, local):
     fwd_value = job_throughput(ws, W * H, ms_fwd)
     stage_ms = {names[i]: float(st[:, i].mean()) for i in range(len(names))}
     stage_ms["project_bwd"] = ms_project_bwd
+    # median and p10 - p90 spread of each stage over the timed eager steps
+    pb_ms = np.array([a.elapsed_time(b) for a, b in pev])
+    spread = {names[i]: [float(np.percentile(st[:, i], q)) for q in (50, 10, 90)] for i in range(len(names))}
+    spread["project_bwd"] = [float(np.percentile(pb_ms, q)) for q in (50, 10, 90)]
 
     # ---- roofline of each stage (algorithmic work per launch / measured duration)
     import json as _json
@@ -396,6 +401,8 @@ def run_gm(args, ws, rank, local):
             stages[k] = {"bound": "alu", "ms": stage_ms[k], "achieved": ach, "peak": alu_peak, "unit": "Tops/s",
                          "frac": ach / alu_peak, "algorithmic": amount}
     stages["zbuffer"] = {"bound": "alu", "ms": stage_ms["zbuffer"], "note": "reported, no target"}
+    for k in stages:
+        stages[k]["ms_median_p10_p90"] = spread[k]
     top = max((k for k in work if k != "project_bwd"), key=lambda k: stage_ms[k])
     roof = dict(stages[top])
     roof.update(kernel=top, traffic=profiled_traffic(top), peak_source=hbm_src if roof["bound"] == "hbm" else
@@ -404,10 +411,10 @@ def run_gm(args, ws, rank, local):
     roof.pop("algorithmic", None)
 
     # kernels per step: triangle bins (count, scan, emit, histogram, histogram scan,
-    # passes, ranges), z-buffer, interpolation, projection, Gaussian bins (count,
-    # depth sort: histogram + scan + 4 passes, scan, emit, tile sort: histogram +
-    # scan + passes, ranges), forward, backward (Gaussians + mesh)
-    launches = (6 + passes_t) + 1 + 1 + 1 + (1 + 6 + 1 + 1 + 2 + passes_g + 1) + 1 + 2
+    # passes, ranges), z-buffer, interpolation, projection, Gaussian bins (depth keys,
+    # depth sort: histogram + scan + 4 passes, rectangles, cull, scan, emit, tile
+    # sort: histogram + scan + passes, ranges), forward, backward (Gaussians + mesh)
+    launches = (6 + passes_t) + 1 + 1 + 1 + (1 + 6 + 1 + 1 + 1 + 1 + 2 + passes_g + 1) + 1 + 2
 
     e2e = None
     if not args.no_e2e:
@@ -621,6 +628,8 @@ def run_multiview(args, flush, dist):
                         "Gaussians (SH degree %d), forward + backward of all views + projection backward"
                         % (len(sc.mesh.faces), len(g.means), g.sh_degree),
             "views": len(cams), "steps": steps, "ms_per_step": ms_batch, "mpix_s": px / 1e6 / (ms_batch / 1e3),
+            "ms_per_view": ms_batch / len(cams), "views_per_s": len(cams) / (ms_batch / 1e3),
+            "batches_per_s": 1e3 / ms_batch,
             "sequential_ms_per_step": ms_seq, "sequential_mpix_s": px / 1e6 / (ms_seq / 1e3),
             "overflow": overflow}
 
@@ -719,11 +728,13 @@ def omp_threads():
 
 
 def cpu_baseline(args, scene):
-    px, dt, _ = oracle_sample(scene, args.cpu_tiles)
+    import oracle
+    n = min(args.cpu_tiles, oracle.n_tiles(scene.camera))
+    px, dt, _ = oracle_sample(scene, n)
     return {"value": px / 1e6 / dt, "unit": "Mpix/s", "cores": omp_threads(), "kind": "oracle",
             "sample": "forward of %d seeded tiles (%d px) of the %dx%d frame: brute-force z-buffer over all "
                       "%d triangles, projection of all %d Gaussians, full per-tile sort, fp32 composite; %.1f s"
-                      % (args.cpu_tiles, px, scene.camera.width, scene.camera.height, len(scene.mesh.faces),
+                      % (n, px, scene.camera.width, scene.camera.height, len(scene.mesh.faces),
                          len(scene.gaussians.means), dt)}
 
 
