@@ -213,8 +213,7 @@ def run_gm(args, ws, rank, local):
     stats_b = torch.zeros(2, dtype=torch.int64, device="cuda")
 
     cam_c, opts = r.cam, r.opts
-    names = ["tri_bin", "zbuffer", "interp", "project", "bin_sort", "composite_fwd", "grad_zero", "composite_bwd",
-             "mesh_bwd"]
+    names = ["zbuffer", "interp", "project", "bin_sort", "composite_fwd", "grad_zero", "composite_bwd", "mesh_bwd"]
 
     def step(evs=None, count=False):
         def mark(k):
@@ -222,36 +221,34 @@ def run_gm(args, ws, rank, local):
                 evs[k].record(stream)
 
         mark(0)
-        gm.gm_bin_triangles(cam_c, r.V, r.F, r.tri_range, r.tri_ids, r.tri_cap, r.tri_counters, r.tri_ws, sync=False)
+        gm.gm_zbuffer_direct(cam_c, r.V, r.F, r.face_id, r.zb_ws)
         mark(1)
-        gm.gm_zbuffer(cam_c, r.V, r.F, r.tri_range, r.tri_ids, r.face_id)
-        mark(2)
         gm.gm_interp_mesh(cam_c, r.V, r.F, r.vcol, r.face_id, r.mesh_depth, r.mesh_rgb, r.tile_far, r.tile_full)
-        mark(3)
+        mark(2)
         gm.gm_project_gaussians(cam_c, opts, r.means, r.log_scales, r.quats, r.logits, r.colors, r.splats, r.radii,
                                 r.tiles_touched)
-        mark(4)
+        mark(3)
         gm.gm_bin_sort_gaussians(cam_c, opts, r.splats, r.radii, r.tile_far, r.tile_full, r.keys, r.gids, r.g_range,
                                  r.g_cap, r.g_counters, r.g_ws, sync=False)
-        mark(5)
+        mark(4)
         gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
                                    stats_f if count else None)
-        mark(6)
+        mark(5)
         r.v_splats.zero_()
         r.v_verts.zero_()
         r.v_vcol.zero_()
-        mark(7)
+        mark(6)
         # the backward call split in two (Gaussian gradients, then mesh gradients) so
         # that each kernel gets its own events; the timed graph step makes one call
         gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats, None, None,
                                    None, None, None, stats_b if count else None)
-        mark(8)
+        mark(7)
         gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], None, r.V, r.F,
                                    r.vcol, r.v_verts, r.v_vcol, None)
-        mark(9)
+        mark(8)
 
     # sizing pass (host read-back of K, capacities grow), then warm-up without syncs
     r.forward(sync=True)
@@ -263,7 +260,6 @@ def run_gm(args, ws, rank, local):
     torch.cuda.synchronize()
     pairs_f, blend_f = (int(x) for x in stats_f.tolist())
     pairs_b, blend_b = (int(x) for x in stats_b.tolist())
-    K_tri = int(r.tri_counters[0].item())
     K_g = int(r.g_counters[0].item())
     K_pre = int(r.g_counters[1].item())
     covered = int((r.face_id >= 0).sum().item())
@@ -365,7 +361,6 @@ def run_gm(args, ws, rank, local):
     T = r.T
     tbits = max((T - 1).bit_length(), 0)
     passes_g = math.ceil(tbits / 8)   # tile passes after the 4-pass depth pre-sort
-    passes_t = math.ceil(tbits / 8)
     work = {
         # bytes the stage must move at least once
         "project": ("hbm", N * (12 + 12 + 16 + 4 + col_bytes) + N * (48 + 4 + 4)),
@@ -374,8 +369,6 @@ def run_gm(args, ws, rank, local):
         # count, offset, splat in, one key+id per entry out; tile sort; ranges
         "bin_sort": ("hbm", N * (20 + 16) + N * (8 + 4 * 24) + N * 12 + N * 32 + K_g * 12
                      + K_g * (8 + passes_g * 24) + K_g * 8 + T * 8),
-        "tri_bin": ("hbm", F * (12 + 36) * 2 + F * 12 + K_tri * 12 + K_tri * 8 + passes_t * K_tri * 24
-                    + K_tri * 8 + T * 8),
         "interp": ("hbm", W * H * (4 + 4 + 12) + T * 5),
         # FP32 lane operations: 18 per evaluated (pixel, Gaussian) pair forward (alpha and
         # the tests), 60 per composited pair backward (the gradient terms)
@@ -410,11 +403,11 @@ def run_gm(args, ws, rank, local):
     roof.pop("ms", None)
     roof.pop("algorithmic", None)
 
-    # kernels per step: triangle bins (count, scan, emit, histogram, histogram scan,
-    # passes, ranges), z-buffer, interpolation, projection, Gaussian bins (depth keys,
-    # depth sort: histogram + scan + 4 passes, rectangles, cull, scan, emit, tile
-    # sort: histogram + scan + passes, ranges), forward, backward (Gaussians + mesh)
-    launches = (6 + passes_t) + 1 + 1 + 1 + (1 + 6 + 1 + 1 + 1 + 1 + 2 + passes_g + 1) + 1 + 2
+    # kernels per step: z-buffer (small triangles, large triangles, resolve),
+    # interpolation, projection, Gaussian bins (depth keys, depth sort: histogram +
+    # scan + 4 passes, rectangles, cull, scan, emit, tile sort: histogram + scan +
+    # passes, ranges), forward, backward (Gaussians + mesh)
+    launches = 3 + 1 + 1 + (1 + 6 + 1 + 1 + 1 + 1 + 2 + passes_g + 1) + 1 + 2
 
     e2e = None
     if not args.no_e2e:
@@ -431,7 +424,7 @@ def run_gm(args, ws, rank, local):
         multiview = run_multiview(args, flush, dist)
 
     return dict(value=value, fwd=fwd_value, ms_step=ms_step, ms_fwd=ms_fwd, ms_eager=ms_eager, stages=stages, roofline=roof,
-                clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_tri=K_tri, K_g=K_g, K_pre=K_pre,
+                clocks=clocks, launches=launches, wall=wall, overflow=overflow, K_g=K_g, K_pre=K_pre,
                 multiview=multiview, soft=soft, aa=aa,
                 pairs_f=pairs_f, pairs_b=pairs_b, blend_f=blend_f, blend_b=blend_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
                 gpu_name=props.name)
@@ -801,7 +794,7 @@ def main():
             "fps_fwd_bwd": 1e3 / res["ms_step"],
             "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["launches"] * args.steps, "clocks": res["clocks"],
-            "counts": {"K_triangle_tile": res["K_tri"], "K_gauss_tile": res["K_g"], "K_gauss_tile_precull":
+            "counts": {"K_gauss_tile": res["K_g"], "K_gauss_tile_precull":
                        res["K_pre"], "pairs_evaluated_fwd": res["pairs_f"], "pairs_composited_fwd": res["blend_f"],
                        "pairs_evaluated_bwd": res["pairs_b"], "pairs_composited_bwd": res["blend_b"]},
             "overflow": res["overflow"], "gpu": res["gpu_name"], "wall_s_timed": res["wall"],

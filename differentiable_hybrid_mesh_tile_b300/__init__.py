@@ -63,6 +63,8 @@ _SIGS = {
     "gm_bin_triangles_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32]),
     "gm_bin_triangles": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, C.c_size_t, _VP]),
     "gm_zbuffer": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP]),
+    "gm_zbuffer_direct_workspace_size": (C.c_size_t, [_I32, _I32, _I32]),
+    "gm_zbuffer_direct": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, C.c_size_t, _VP]),
     "gm_interp_mesh": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "gm_project_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "gm_project_gaussians_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 8 + [_I32] + [_VP] * 6),
@@ -198,6 +200,15 @@ def gm_bin_triangles_noalloc(cam: gm_camera, V, F, tile_range, tri_ids, cap: int
 def gm_zbuffer(cam: gm_camera, V, F, tile_range, tri_ids, face_id):
     _check(lib().gm_zbuffer(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(tile_range, I32),
                             _p(tri_ids, I32), _p(face_id, I32), _stream()), "gm_zbuffer")
+
+
+def gm_zbuffer_direct_workspace_size(nF: int, width: int, height: int) -> int:
+    return int(lib().gm_zbuffer_direct_workspace_size(nF, width, height))
+
+
+def gm_zbuffer_direct(cam: gm_camera, V, F, face_id, ws):
+    _check(lib().gm_zbuffer_direct(C.byref(cam), _p(V, F32), V.shape[0], _p(F, I32), F.shape[0], _p(face_id, I32),
+                                   _p(ws), ws.numel() * ws.element_size(), _stream()), "gm_zbuffer_direct")
 
 
 def gm_interp_mesh(cam: gm_camera, V, F, vcol, face_id, mesh_depth, mesh_rgb, tile_far, tile_full):
@@ -394,6 +405,10 @@ class HybridRenderer:
     (``gm_antialias_bwd``, then ``gm_interp_mesh_bwd``), all on the caller's
     stream.
 
+    ``zbuffer="direct"`` (default) finds the face ids with ``gm_zbuffer_direct``
+    (no triangle lists); ``zbuffer="tile"`` with ``gm_bin_triangles`` and
+    ``gm_zbuffer``.  Both give the same face ids.
+
     ``softness > 0`` selects the soft split at the mesh surface (front
     fraction ``soft_split``: GM_SPLIT_PHI or GM_SPLIT_LOGISTIC): the
     projection also writes each Gaussian's depth model (``depth_model``), the
@@ -403,7 +418,8 @@ class HybridRenderer:
     """
 
     def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
-                 concurrent=True, tile_test=True, softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False):
+                 concurrent=True, tile_test=True, softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False,
+                 zbuffer="direct"):
         self.cam_desc = cam
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
@@ -421,6 +437,10 @@ class HybridRenderer:
         self.soft = self.softness > 0.0
         self.soft_split = int(soft_split)
         self.antialias = bool(antialias)
+        if zbuffer not in ("direct", "tile"):
+            raise ValueError("zbuffer must be 'direct' or 'tile'")
+        self.zbuffer = zbuffer
+        self.K_tri = None
         self._side = None
         self.tri_cap = 0
         self.g_cap = 0
@@ -479,7 +499,7 @@ class HybridRenderer:
         self.colors = t(gaussians.colors, F32)
         self.sh_degree = int(gaussians.sh_degree)
         self._alloc_gauss(int(self.means.shape[0]))
-        self._alloc_tri(max(self.tri_cap, 1))
+        self._alloc_mesh_ws()
         if self.antialias:
             self.adj = torch.empty(self.F.shape[0], 3, dtype=I32, device=d)
             nb = gm_mesh_edges_workspace_size(int(self.F.shape[0]))
@@ -509,6 +529,14 @@ class HybridRenderer:
         nb = gm_bin_sort_gaussians_workspace_size(self.N, cap, self.W, self.H)
         self.g_ws = torch.empty((nb + 15) // 16 * 16, dtype=U8, device=d)
 
+    def _alloc_mesh_ws(self):
+        """Triangle-list buffers (tile z-buffer) or the direct z-buffer's workspace."""
+        if self.zbuffer == "tile":
+            self._alloc_tri(max(self.tri_cap, 1))
+        else:
+            nb = gm_zbuffer_direct_workspace_size(int(self.F.shape[0]), self.W, self.H)
+            self.zb_ws = torch.empty((nb + 15) // 16 * 16, dtype=U8, device=self.dev)
+
     def _alloc_tri(self, cap):
         d = self.dev
         self.tri_cap = cap
@@ -524,6 +552,23 @@ class HybridRenderer:
             self._side = torch.cuda.Stream(device=self.dev)
         return self._side
 
+    def _zbuffer(self, sync: bool):
+        """face_id: gm_zbuffer_direct, or triangle lists (grown on demand) and gm_zbuffer."""
+        cam = self.cam
+        if self.zbuffer == "direct":
+            gm_zbuffer_direct(cam, self.V, self.F, self.face_id, self.zb_ws)
+            return
+        for attempt in range(2):
+            try:
+                self.K_tri = gm_bin_triangles(cam, self.V, self.F, self.tri_range, self.tri_ids, self.tri_cap,
+                                              self.tri_counters, self.tri_ws, sync=sync)
+                break
+            except GmError as e:
+                if e.status != GM_ERR_CAPACITY or attempt:
+                    raise
+                self._alloc_tri(self._grow(int(self.tri_counters[GM_CNT_K].item())))
+        gm_zbuffer(cam, self.V, self.F, self.tri_range, self.tri_ids, self.face_id)
+
     def forward(self, sync: bool = True):
         cam, opts = self.cam, self.opts
         main = torch.cuda.current_stream(self.dev)
@@ -536,17 +581,7 @@ class HybridRenderer:
             gm_project_gaussians(cam, opts, self.means, self.log_scales, self.quats, self.logits, self.colors,
                                  self.splats, self.radii, self.tiles_touched, self.depth_model)
             gm_sort_gaussians_by_depth(cam, self.splats, self.radii, self.g_cap, self.g_counters, self.g_ws)
-        for attempt in range(2):
-            try:
-                k = gm_bin_triangles(cam, self.V, self.F, self.tri_range, self.tri_ids, self.tri_cap,
-                                     self.tri_counters, self.tri_ws, sync=sync)
-                self.K_tri = k
-                break
-            except GmError as e:
-                if e.status != GM_ERR_CAPACITY or attempt:
-                    raise
-                self._alloc_tri(self._grow(int(self.tri_counters[GM_CNT_K].item())))
-        gm_zbuffer(cam, self.V, self.F, self.tri_range, self.tri_ids, self.face_id)
+        self._zbuffer(sync)
         gm_interp_mesh(cam, self.V, self.F, self.vcol, self.face_id, self.mesh_depth, self.mesh_rgb, self.tile_far,
                        self.tile_full)
         if self.antialias:
@@ -680,10 +715,10 @@ class MultiViewRenderer:
     """
 
     def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4,
-                 softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False):
+                 softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False, zbuffer="direct"):
         self.views = [HybridRenderer(c, bg=bg, cull_occluded=cull_occluded, device=device, concurrent=False,
                                      tile_test=tile_test, softness=softness, soft_split=soft_split,
-                                     antialias=antialias) for c in cams]
+                                     antialias=antialias, zbuffer=zbuffer) for c in cams]
         self.antialias = bool(antialias)
         self.soft = self.views[0].soft
         self.V = len(self.views)
@@ -725,7 +760,7 @@ class MultiViewRenderer:
                     r.adj = v0.adj
                 r.N = N
                 r._alloc_g(max(r.g_cap, 1))
-                r._alloc_tri(max(r.tri_cap, 1))
+                r._alloc_mesh_ws()
             r.splats, r.radii, r.tiles_touched = self.splats[k], self.radii[k], self.tiles_touched[k]
             r.v_splats = self.v_splats[k]
             if self.soft:
@@ -757,9 +792,7 @@ class MultiViewRenderer:
             s.wait_event(start)
             with torch.cuda.stream(s):
                 cam, opts = r.cam, r.opts
-                gm_bin_triangles(cam, r.V, r.F, r.tri_range, r.tri_ids, r.tri_cap, r.tri_counters, r.tri_ws,
-                                 sync=False)
-                gm_zbuffer(cam, r.V, r.F, r.tri_range, r.tri_ids, r.face_id)
+                r._zbuffer(sync=False)
                 gm_interp_mesh(cam, r.V, r.F, r.vcol, r.face_id, r.mesh_depth, r.mesh_rgb, r.tile_far, r.tile_full)
                 if r.antialias:
                     gm_antialias(cam, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov, r.rgb_aa,

@@ -141,6 +141,27 @@ int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* 
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_zbuffer");
 }
 
+size_t gm_zbuffer_direct_workspace_size(int32_t nF, int32_t width, int32_t height)
+{
+    return gm::zbuffer_direct_ws_bytes(nF, width > 0 ? width : 0, height > 0 ? height : 0);
+}
+
+int gm_zbuffer_direct(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                      int32_t* face_id, void* ws, size_t ws_bytes, void* stream)
+{
+    g_err[0] = 0;
+    if (int st = check_cam(cam)) return st;
+    GM_REQUIRE(nV >= 0 && nF >= 0, "negative size");
+    GM_REQUIRE(nV == 0 || V, "V is NULL");
+    GM_REQUIRE(nF == 0 || F, "F is NULL");
+    GM_REQUIRE(face_id, "face_id is NULL");
+    const size_t need = gm::zbuffer_direct_ws_bytes(nF, cam->width, cam->height);
+    GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
+    GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
+    cudaError_t e = gm::zbuffer_direct(gm::make_cam(*cam), V, nV, F, nF, face_id, ws, (cudaStream_t)stream);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_zbuffer_direct");
+}
+
 int gm_interp_mesh(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF, const float* vcol,
                    const int32_t* face_id, float* mesh_depth, float* mesh_rgb, float* tile_far, uint8_t* tile_full,
                    void* stream)

@@ -286,16 +286,6 @@ __device__ __forceinline__ bool keep_tile(const BinRule& r, const BinShape& s, i
     return !r.tile_test || tile_min_sigma(s, tx, ty) <= s.smax;
 }
 
-// q = t / w and r = t % w for 0 <= t < 2^21 and w >= 1 with one fp32 multiply:
-// (t + 0.5) / w lies at least 0.5 / w from every integer, far more than the
-// rounding error of (t + 0.5) * rn(1 / w).  (Integer division by a variable
-// costs tens of instructions.)
-__device__ __forceinline__ void divmod_small(int t, int w, float inv_w, int& q, int& r)
-{
-    q = t < (1 << 21) ? (int)(((float)t + 0.5f) * inv_w) : t / w;
-    r = t - q * w;
-}
-
 // Rectangles up to this many tiles are walked by their own thread; larger ones
 // (near-camera Gaussians) by the whole warp, 32 tiles at a time, so one large
 // Gaussian does not hold up the other 31 lanes.

@@ -97,6 +97,16 @@ __device__ __forceinline__ bool tri_setup(const Cam& c, const float* __restrict_
     return true;
 }
 
+// q = t / w and r = t % w for t >= 0 and w >= 1, below 2^21 with one fp32 multiply:
+// (t + 0.5) / w lies at least 0.5 / w from every integer, far more than the
+// rounding error of (t + 0.5) * rn(1 / w).  (Integer division by a variable
+// costs tens of instructions.)
+__device__ __forceinline__ void divmod_small(int t, int w, float inv_w, int& q, int& r)
+{
+    q = t < (1 << 21) ? (int)(((float)t + 0.5f) * inv_w) : t / w;
+    r = t - q * w;
+}
+
 // Tile rectangle [x0, x1) x [y0, y1) of a projected Gaussian of radius r:
 // floor((m - r) / 16) .. ceil((m + r) / 16), clamped to the tile grid.
 __device__ __forceinline__ bool gauss_rect(const Cam& c, float mx, float my, int r, int& x0, int& y0,
@@ -177,6 +187,9 @@ int set_last_error(int code, const char* fmt, ...);
 size_t tri_bin_ws_bytes(int nF, int cap);
 cudaError_t tri_bin(const Cam& c, const float* V, int nV, const int32_t* F, int nF, int32_t* tile_range,
                     int32_t* tri_ids, int cap, int32_t* counters, void* ws, cudaStream_t s);
+size_t zbuffer_direct_ws_bytes(int nF, int W, int H);
+cudaError_t zbuffer_direct(const Cam& c, const float* V, int nV, const int32_t* F, int nF, int32_t* face_id,
+                           void* ws, cudaStream_t s);
 cudaError_t zbuffer(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const int32_t* tile_range,
                     const int32_t* tri_ids, int32_t* face_id, cudaStream_t s);
 cudaError_t interp(const Cam& c, const float* V, int nV, const int32_t* F, int nF, const float* vcol,

@@ -13,6 +13,7 @@
  * Gaussians and a camera pose) is split into seven steps; a forward pass is
  *
  *   gm_bin_triangles -> gm_zbuffer -> gm_interp_mesh          (mesh layer)
+ *     (or gm_zbuffer_direct -> gm_interp_mesh: the same face ids, no lists)
  *     [-> gm_antialias, with gm_mesh_edges once per mesh]
  *   gm_project_gaussians -> gm_bin_sort_gaussians             (Gaussians)
  *   gm_composite_hybrid_fwd                                   (image)
@@ -159,6 +160,23 @@ int gm_bin_triangles(const gm_camera* cam, const float* V, int32_t nV, const int
  * ---------------------------------------------------------------------- */
 int gm_zbuffer(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
                const int32_t* tile_range, const int32_t* tri_ids, int32_t* face_id, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gm_zbuffer_direct -- gm_zbuffer without triangle lists: the same coverage,
+ * depth and tie rules over every (triangle, box pixel) pair, the nearest
+ * surface kept per pixel with an atomic minimum of (reciprocal depth, face
+ * id).  face_id equals gm_zbuffer's bit for bit (for the lists
+ * gm_bin_triangles builds of the same mesh).  No gm_bin_triangles call is
+ * needed.  Triangles that a vertex puts at or in front of the near plane, of
+ * zero area or outside the image are skipped, as by gm_bin_triangles.
+ *   face_id [H][W] i32 out (-1 = uncovered).
+ *   ws: gm_zbuffer_direct_workspace_size(nF, width, height) bytes, 16-byte
+ *   aligned (8 bytes per pixel plus 100 bytes per face); nothing else may
+ *   use it during the call.
+ * ---------------------------------------------------------------------- */
+size_t gm_zbuffer_direct_workspace_size(int32_t nF, int32_t width, int32_t height);
+int gm_zbuffer_direct(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F, int32_t nF,
+                      int32_t* face_id, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_interp_mesh -- Mesh rasterizer, item 2 (depth and vertex colours

@@ -65,6 +65,17 @@ def run_mesh(cam, mesh):
                 mesh_rgb=host(mrgb), tile_far=host(tfar), tile_full=host(tfull), counters=host(cnt))
 
 
+def run_zbuffer_direct(cam, mesh):
+    """GPU gm_zbuffer_direct: face ids [H][W] as numpy."""
+    c = gm.make_camera(cam)
+    V, F = dev(mesh.verts, torch.float32), dev(mesh.faces, torch.int32)
+    nb = gm.gm_zbuffer_direct_workspace_size(len(mesh.faces), cam.width, cam.height)
+    ws = torch.empty((nb + 15) // 16 * 16, dtype=torch.uint8, device="cuda")
+    fid = torch.full((cam.height, cam.width), -7, dtype=torch.int32, device="cuda")
+    gm.gm_zbuffer_direct(c, V, F, fid, ws)
+    return host(fid)
+
+
 def run_mesh_edges(F, nV):
     """GPU gm_mesh_edges: adjacency [nF][3] as numpy."""
     Fd = dev(F, torch.int32)

@@ -121,6 +121,11 @@ def test_null_and_size_checks(lib):
     assert st == gm.GM_ERR_INVALID_ARG and b"workspace" in lib.gm_last_error()
     st = lib.gm_antialias(C.byref(cam), C.c_void_p(256), 3, C.c_void_p(256), 1, None, *([C.c_void_p(256)] * 8), None)
     assert st == gm.GM_ERR_INVALID_ARG and b"adj" in lib.gm_last_error()
+    # direct z-buffer: workspace too small
+    st = lib.gm_zbuffer_direct(C.byref(cam), C.c_void_p(256), 3, C.c_void_p(256), 1, C.c_void_p(256),
+                               C.c_void_p(256), 64, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"workspace" in lib.gm_last_error()
+    assert gm.gm_zbuffer_direct_workspace_size(10, 64, 48) >= 8 * 64 * 48 + 10 * 100
     # misaligned v_depth_model in the projection backward
     st = lib.gm_project_gaussians_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 7), C.c_void_p(260),
                                       0, *([C.c_void_p(256)] * 5), None)
