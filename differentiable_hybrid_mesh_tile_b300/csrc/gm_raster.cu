@@ -10,8 +10,9 @@
 // for rounding, so both give the same face ids bit for bit.
 //
 // Triangles whose pixel-centre box holds at most SMALL_TRI pixels: a warp sets
-// up 32 consecutive faces in shared memory and takes all their (triangle,
-// pixel) pairs 32 at a time, one pixel per lane per round.  Larger triangles
+// up 32 consecutive faces in shared memory and takes their box rows in runs of
+// RUN consecutive pixels, one run per lane per round (the owner lookup and the
+// record loads once per run; each edge function's row term once per run).  Larger triangles
 // go to a queue that persistent blocks work through in chunks of CHUNK pixels;
 // a block that finds no new triangle helps with the chunks of unfinished ones,
 // so one full-screen triangle still spreads over several blocks.
@@ -21,6 +22,7 @@ namespace gm {
 namespace {
 
 constexpr int SMALL_TRI = 2048;
+constexpr int RUN = 4;
 constexpr int CHUNK = 1024;
 constexpr int ZB_THREADS = 256;
 constexpr int HELP_PASSES = 8;  // each queued triangle is offered to up to this many blocks
@@ -36,7 +38,7 @@ struct ZTri {
     float4 c;  // edge 0 (v1 -> v2): du, dv; edge 1 (v2 -> v0): du, dv
     float4 d;  // edge 2 (v0 -> v1): du, dv; w1, w2
     int4 e;    // box x0, y0, box width, face id
-    int4 g;    // 1 / width (float bits), box pixels, -, -
+    int4 g;    // 1 / width (float bits), box pixels, runs per box row, 1 / runs per row (float bits)
 };
 
 __device__ __forceinline__ ZTri make_ztri(const Tri& t, int f)
@@ -50,7 +52,8 @@ __device__ __forceinline__ ZTri make_ztri(const Tri& t, int f)
                       1.0f / (t.area * t.z[2]));
     const int w = t.x1 - t.x0 + 1, h = t.y1 - t.y0 + 1;
     z.e = make_int4(t.x0, t.y0, w, f);
-    z.g = make_int4(__float_as_int(__frcp_rn((float)w)), w * h, 0, 0);
+    const int rw = (w + RUN - 1) / RUN;
+    z.g = make_int4(__float_as_int(__frcp_rn((float)w)), w * h, rw, __float_as_int(__frcp_rn((float)rw)));
     return z;
 }
 
@@ -76,6 +79,34 @@ __device__ __forceinline__ void zb_pixel(const ZTri& z, int i, int j, int W, uns
     atomicMin(key + (int64_t)j * W + i, k);
 }
 
+// Up to RUN pixels (i0 .. i0 + n - 1, row j) of the triangle: the edge
+// functions as edge_pre computes them, with the row term du (py - va) of each
+// edge formed once.
+__device__ __forceinline__ void zb_run(const ZTri& z, int i0, int j, int n, int W,
+                                       unsigned long long* __restrict__ key)
+{
+    const float py = (float)j + 0.5f;
+    const float r0 = __fmul_rn(z.c.x, __fsub_rn(py, z.a.w));
+    const float r1 = __fmul_rn(z.c.z, __fsub_rn(py, z.b.y));
+    const float r2 = __fmul_rn(z.d.x, __fsub_rn(py, z.a.y));
+    const bool pos = z.b.z > 0.0f;
+    unsigned long long* row = key + (int64_t)j * W;
+#pragma unroll
+    for (int k = 0; k < RUN; ++k) {
+        if (k >= n) break;
+        const int i = i0 + k;
+        const float px = (float)i + 0.5f;
+        const float e0 = __fsub_rn(r0, __fmul_rn(z.c.y, __fsub_rn(px, z.a.z)));
+        const float e1 = __fsub_rn(r1, __fmul_rn(z.c.w, __fsub_rn(px, z.b.x)));
+        const float e2 = __fsub_rn(r2, __fmul_rn(z.d.y, __fsub_rn(px, z.a.x)));
+        const bool in = pos ? (e0 >= 0.0f && e1 >= 0.0f && e2 >= 0.0f) : (e0 <= 0.0f && e1 <= 0.0f && e2 <= 0.0f);
+        if (!in) continue;
+        const float inv_d = fmaf(e0, z.b.w, fmaf(e1, z.d.z, e2 * z.d.w));
+        if (!(inv_d > 0.0f)) continue;
+        atomicMin(row + i, ((unsigned long long)(~__float_as_uint(inv_d)) << 32) | (uint32_t)z.e.w);
+    }
+}
+
 // Pixel r (row-major) of the triangle's box.
 __device__ __forceinline__ void box_pixel(const ZTri& z, int r, int& i, int& j)
 {
@@ -99,7 +130,7 @@ k_zb_small(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
             const ZTri z = make_ztri(t, f);
             if (z.g.y <= SMALL_TRI) {
                 s[threadIdx.x] = z;
-                area = z.g.y;
+                area = z.g.z * (t.y1 - t.y0 + 1);  // runs of the box
             } else {  // queued for the chunked pass (at most nF of them)
                 const int q = atomicAdd(ctl + ZB_NLARGE, 1);
                 large[q] = z;
@@ -107,7 +138,7 @@ k_zb_small(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
             }
         }
     }
-    // the (triangle, pixel) pairs of the warp's small triangles, flattened
+    // the (triangle, run) pairs of the warp's small triangles, flattened
     int o = area;  // inclusive prefix sum over the lanes
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -129,9 +160,10 @@ k_zb_small(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict
         const int oj = __shfl_sync(0xffffffffu, o, j);
         if (p < total) {
             const ZTri& z = s[wbase + j];
-            int pi, pj;
-            box_pixel(z, p - oj, pi, pj);
-            zb_pixel(z, pi, pj, c.W, key);
+            int row, seg;
+            divmod_small(p - oj, z.g.z, __int_as_float(z.g.w), row, seg);
+            const int c0 = seg * RUN;
+            zb_run(z, z.e.x + c0, z.e.y + row, min(RUN, z.e.z - c0), c.W, key);
         }
     }
 }
