@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--no-multiview", action="store_true", help="skip the batched 8-view measurement")
     ap.add_argument("--no-soft", action="store_true", help="skip the soft-split measurement")
     ap.add_argument("--no-aa", action="store_true", help="skip the antialiased-mesh measurement")
-    ap.add_argument("--cpu-tiles", type=int, default=600,
+    ap.add_argument("--cpu-tiles", type=int, default=1200,
                     help="tiles of the frame the CPU oracle renders (about 10 s of oracle work at 1080p)")
     return ap.parse_args()
 
