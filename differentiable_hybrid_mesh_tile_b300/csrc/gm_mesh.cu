@@ -314,8 +314,11 @@ struct MeshBwdStage {
 // DIRECT: g_rgb / g_depth are already dL/d(interpolated colour, depth) per pixel
 // (from the antialiasing's backward); otherwise they are the image's upstream
 // gradient, weighted here by the transmittance in front of the mesh.
+//
+// At most 64 registers (4 CTAs of 256 threads per SM): the kernel waits on the
+// gathers of the faces' vertices and colours, and more resident warps hide them.
 template <bool DIRECT>
-__global__ void __launch_bounds__(TILE_PIX)
+__global__ void __launch_bounds__(TILE_PIX, 4)
 k_mesh_bwd(Cam c, const float* __restrict__ V, int nV, const int32_t* __restrict__ F, int nF,
            const float* __restrict__ vcol, const int32_t* __restrict__ face_id, const float* __restrict__ T_final,
            const float* __restrict__ g_rgb, const float* __restrict__ g_depth,
