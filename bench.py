@@ -268,7 +268,7 @@ def run_gm(args, ws, rank, local):
         step()
     torch.cuda.synchronize()
 
-    # the timed step: one CUDA graph replay of the seven calls (captured once);
+    # the timed step: one CUDA graph replay of the path's calls (captured once);
     # per-stage times come from eager runs with events between the calls
     graph = r.capture_step(*g_dev)
     for _ in range(args.warmup):
@@ -630,7 +630,7 @@ def run_multiview(args, flush, dist):
 def run_e2e(args, r, scene, grads_np, flush, ws, dist):
     """Same step through the public calls with host buffers: every step copies its
     inputs (all Gaussian and mesh parameters, the upstream gradients) from pinned
-    host memory, runs the seven calls and the backward, and copies the image and
+    host memory, runs the forward and backward calls, and copies the image and
     all gradients back.  Steps are pipelined over two renderers (two sets of
     device buffers) and three streams: step k+1's uploads overlap step k's
     compute and step k-1's downloads (a buffer set is refilled only after its
@@ -788,9 +788,11 @@ def main():
             "warmup": args.warmup, "ms_per_step": res["ms_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(args, scene, ws),
             "fwd_mpix_s": res["fwd"], "ms_fwd": res["ms_fwd"], "fps_fwd": 1e3 / res["ms_fwd"],
-            "ms_per_step_eager": res["ms_eager"], "timing": "CUDA-graph replay of the seven calls per step; "
-            "stages from eager runs with events between calls; project_bwd (3D-parameter gradients) timed "
-            "separately, not in the step",
+            "ms_per_step_eager": res["ms_eager"],
+            "timing": "CUDA-graph replay of the path's calls per step (direct z-buffer, interpolation, "
+                      "projection, Gaussian binning in two halves, composite forward, composite backward); "
+                      "stages from eager runs with events between calls; project_bwd (3D-parameter gradients) "
+                      "timed separately, not in the step",
             "fps_fwd_bwd": 1e3 / res["ms_step"],
             "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["launches"] * args.steps, "clocks": res["clocks"],
