@@ -152,3 +152,12 @@ def test_header_constants_match_binding():
     body = re.search(r"typedef struct gm_opts \{(.*?)\} gm_opts;", text, re.S).group(1)
     names = re.findall(r"^\s*(?:float|int32_t)\s+(\w+)(?:\[\d+\])?;", body, re.M)
     assert names == [f[0] for f in gm.gm_opts._fields_]
+
+
+def test_renderer_rejects_unknown_zbuffer():
+    """The renderers take zbuffer="direct" (no triangle lists) or "tile"; anything
+    else is refused before any device memory is touched."""
+    from differentiable_hybrid_mesh_tile_b300 import scenes
+    cam = scenes.look_at((0, 0, 3), (0, 0, 0), 64, 48, 50, 50)
+    with pytest.raises(ValueError):
+        gm.HybridRenderer(cam, zbuffer="lists")
