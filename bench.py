@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-aa", action="store_true", help="skip the antialiased-mesh measurement")
     ap.add_argument("--cpu-tiles", type=int, default=1200,
                     help="tiles of the frame the CPU oracle renders (about 10 s of oracle work at 1080p)")
+    ap.add_argument("--ref-tiles", type=int, default=400,
+                    help="tiles per step of --impl reference (the oracle's per-call cost stays a small share)")
     return ap.parse_args()
 
 
@@ -155,9 +157,9 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
-# stage's kernel on soup_1080p, from one ncu capture (summary and command in the
-# named profile).  A figure holds only for the kernel sources it was taken on:
-# when any of them has changed since, the traffic is reported as null.
+# stage's kernel on soup_1080p, from one ncu capture of that kernel.  A figure
+# holds only for the kernel sources it was taken on: when any of them has
+# changed since, the traffic is reported as null.
 PROFILED_TRAFFIC = {
     "composite_bwd": {
         "kernel": "k_composite_bwd",
@@ -166,7 +168,6 @@ PROFILED_TRAFFIC = {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
                 "2aa73d489c78fde28e92d9d1bd7884a5c795cf219f7a9c8230d5ec1339c06e46",
         },
-        "profile": "profiles/composite_bwd_soup_1080p.md",
     },
 }
 
@@ -396,6 +397,18 @@ def run_gm(args, ws, rank, local):
     stages["zbuffer"] = {"bound": "alu", "ms": stage_ms["zbuffer"], "note": "reported, no target"}
     for k in stages:
         stages[k]["ms_median_p10_p90"] = spread[k]
+    # the tile-list rasterizer (not in the step: the renderer's default is the
+    # direct z-buffer): triangle bins against HBM (per triangle its three vertices
+    # and indices read, per entry its id written and sorted), the tile z-buffer
+    # reported
+    ms_tb, ms_tz, K_t, tz_spread = run_tile_zbuffer(args, scene, flush, dist)
+    tb_bytes = F * 48 + K_t * 8
+    stages["tri_bin"] = {"bound": "hbm", "ms": ms_tb, "achieved": tb_bytes / (ms_tb / 1e3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": tb_bytes / (ms_tb / 1e3) / 1e9 / hbm_peak,
+                         "algorithmic": tb_bytes, "entries": K_t, "ms_median_p10_p90": tz_spread[0],
+                         "note": "tile-list path (zbuffer='tile'), not in the timed step"}
+    stages["tile_zbuffer"] = {"bound": "alu", "ms": ms_tz, "note": "reported, no target; tile-list path, not in "
+                              "the timed step", "ms_median_p10_p90": tz_spread[1]}
     top = max((k for k in work if k != "project_bwd"), key=lambda k: stage_ms[k])
     roof = dict(stages[top])
     roof.update(kernel=top, traffic=profiled_traffic(top), peak_source=hbm_src if roof["bound"] == "hbm" else
@@ -428,6 +441,53 @@ def run_gm(args, ws, rank, local):
                 multiview=multiview, soft=soft, aa=aa,
                 pairs_f=pairs_f, pairs_b=pairs_b, blend_f=blend_f, blend_b=blend_b, e2e=e2e, W=W, H=H, N=N, F=F, rank=rank, ws=ws, dist=dist,
                 gpu_name=props.name)
+
+
+def run_tile_zbuffer(args, scene, flush, dist):
+    """The tile-list rasterizer kept beside the direct z-buffer: triangle binning
+    (gm_bin_triangles: projection, tile counts, scan, emission, sort, ranges)
+    and the tile z-buffer (gm_zbuffer), each timed eagerly with events on the
+    same frame.  Returns (tri_bin ms, zbuffer ms, entries K_t)."""
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    cam = scene.camera
+    r = gm.HybridRenderer(cam, bg=scene.bg, zbuffer="tile")
+    r.upload(scene.mesh, scene.gaussians)
+    r.forward(sync=True)  # sizes the triangle lists
+    stream = torch.cuda.current_stream()
+    c = r.cam
+    steps = max(3, min(args.steps, 100))
+
+    def bins():
+        gm.gm_bin_triangles(c, r.V, r.F, r.tri_range, r.tri_ids, r.tri_cap, r.tri_counters, r.tri_ws, sync=False)
+
+    def zb():
+        gm.gm_zbuffer(c, r.V, r.F, r.tri_range, r.tri_ids, r.face_id)
+
+    out = []
+    for fn in (bins, zb):
+        for _ in range(max(args.warmup, 2)):
+            flush.zero_()
+            bins()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            if fn is zb:
+                bins()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        out.append(ts)
+    K_t = int(r.tri_counters[0].item())
+    assert not r.overflowed()
+    ms_bin, ms_zb = max_over_ranks([float(np.mean(out[0])), float(np.mean(out[1]))], dist, "cuda")
+    spread = [[float(np.percentile(t, q)) for q in (50, 10, 90)] for t in out]
+    return ms_bin, ms_zb, K_t, spread
 
 
 def run_soft(args, scene, grads_np, flush, dist, softness=1.0):
@@ -725,10 +785,12 @@ def cpu_baseline(args, scene):
     n = min(args.cpu_tiles, oracle.n_tiles(scene.camera))
     px, dt, _ = oracle_sample(scene, n)
     return {"value": px / 1e6 / dt, "unit": "Mpix/s", "cores": omp_threads(), "kind": "oracle",
-            "sample": "forward of %d seeded tiles (%d px) of the %dx%d frame: brute-force z-buffer over all "
-                      "%d triangles, projection of all %d Gaussians, full per-tile sort, fp32 composite; %.1f s"
-                      % (n, px, scene.camera.width, scene.camera.height, len(scene.mesh.faces),
-                         len(scene.gaussians.means), dt)}
+            "pass": "forward",
+            "sample": "forward only (the oracle's gradients are finite differences, not a throughput path; "
+                      "compare with fwd_mpix_s) of %d seeded tiles (%d px) of the %dx%d frame: brute-force "
+                      "z-buffer over all %d triangles, projection of all %d Gaussians, full per-tile sort, fp32 "
+                      "composite; %.1f s" % (n, px, scene.camera.width, scene.camera.height,
+                                             len(scene.mesh.faces), len(scene.gaussians.means), dt)}
 
 
 def run_reference(args):
@@ -737,7 +799,10 @@ def run_reference(args):
         return
     from differentiable_hybrid_mesh_tile_b300 import scenes
     scene = scenes.make(args.config)
-    n_tiles = 4
+    n_tiles = args.ref_tiles
+    # the oracle's cost per call that does not depend on the sample (projection of
+    # every Gaussian, the lists' set-up): one call on a single tile
+    _, fixed_s, _ = oracle_sample(scene, 1, seed=99)
     for k in range(args.warmup):
         oracle_sample(scene, n_tiles, seed=100 + k)
     times, pxs = [], []
@@ -748,13 +813,15 @@ def run_reference(args):
     ms = 1e3 * float(np.mean(times))
     val = float(np.sum(pxs)) / 1e6 / float(np.sum(times))
     cfg = config_dict(args, scene, ws)
-    sample = "forward of %d seeded tiles per step (~%d px) of the %dx%d frame" % (
-        n_tiles, int(np.mean(pxs)), scene.camera.width, scene.camera.height)
+    sample = ("forward only, %d seeded tiles per step (~%d px) of the %dx%d frame; each step also pays the "
+              "oracle's per-call cost (projection of all %d Gaussians, list set-up: %.2f s of the %.2f s step)"
+              % (n_tiles, int(np.mean(pxs)), scene.camera.width, scene.camera.height, len(scene.gaussians.means),
+                 fixed_s, float(np.mean(times))))
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "Mpix/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": val, "unit": "Mpix/s", "cores": omp_threads(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "pass": "forward"},
             "e2e": {"value": val, "unit": "Mpix/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

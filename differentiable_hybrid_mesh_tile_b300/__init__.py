@@ -84,6 +84,8 @@ _SIGS = {
     "gm_antialias_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 13),
     "gm_interp_mesh_bwd": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 7),
     "gm_bin_triangles_noalloc": (C.c_int, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP]),
+    "gm_set_wait_limit": (C.c_int, [C.c_uint32]),
+    "gm_get_wait_limit": (C.c_int, [C.POINTER(C.c_uint32)]),
     "gm_last_error": (C.c_char_p, []),
 }
 
@@ -195,6 +197,21 @@ def gm_bin_triangles_noalloc(cam: gm_camera, V, F, tile_range, tri_ids, cap: int
         raise GmError(st, "gm_bin_triangles_noalloc", "capacity %d < needed %d" % (cap, k.value))
     _check(st, "gm_bin_triangles_noalloc")
     return k.value if sync else None
+
+
+GM_WAIT_LIMIT_DEFAULT = 1 << 22
+
+
+def gm_set_wait_limit(polls: int):
+    """Bound on the polls of the sorts' inter-block waits on the current device
+    (gm.h: gm_set_wait_limit); set it only while no libgm kernel runs."""
+    _check(lib().gm_set_wait_limit(C.c_uint32(int(polls))), "gm_set_wait_limit")
+
+
+def gm_get_wait_limit() -> int:
+    v = C.c_uint32(0)
+    _check(lib().gm_get_wait_limit(C.byref(v)), "gm_get_wait_limit")
+    return int(v.value)
 
 
 def gm_zbuffer(cam: gm_camera, V, F, tile_range, tri_ids, face_id):

@@ -100,6 +100,19 @@ extern "C" {
 
 const char* gm_last_error(void) { return g_err; }
 
+int gm_set_wait_limit(uint32_t polls)
+{
+    cudaError_t e = gm::set_wait_limit(polls);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_set_wait_limit");
+}
+
+int gm_get_wait_limit(uint32_t* polls)
+{
+    GM_REQUIRE(polls, "polls is NULL");
+    cudaError_t e = gm::get_wait_limit(polls);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_get_wait_limit");
+}
+
 size_t gm_bin_triangles_workspace_size(int32_t nF, int32_t cap, int32_t width, int32_t height)
 {
     (void)width;

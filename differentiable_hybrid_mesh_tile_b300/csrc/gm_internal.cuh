@@ -137,7 +137,7 @@ constexpr int SORT_PART = SORT_THREADS * SORT_IPT;
 constexpr int SORT_MAX_PASSES = 8;
 
 // bounded inter-block wait: polls before a waiting block gives up
-constexpr uint32_t SPIN_LIMIT = 1u << 22;
+constexpr uint32_t SPIN_LIMIT = GM_WAIT_LIMIT_DEFAULT;
 
 struct ScanWs {
     uint32_t* desc;    // [parts]
@@ -180,6 +180,9 @@ cudaError_t tile_ranges(const uint64_t* keys, int cap, const int32_t* counters, 
 
 int num_sms();
 int set_last_error(int code, const char* fmt, ...);
+// the bounded waits' poll limit on the current device (gm_set_wait_limit)
+cudaError_t set_wait_limit(uint32_t polls);
+cudaError_t get_wait_limit(uint32_t* polls);
 
 // ---------------------------------------------------------------------------
 // Host launchers of the path's steps (enqueue on stream s, no synchronisation)

@@ -7,9 +7,11 @@
 // 8-bit digit that ranks a partition in shared memory (warp multisplit),
 // gets each digit's global offset by look-back over earlier partitions and
 // writes the partition out digit-run by digit-run.  Every inter-block wait is
-// bounded: after SPIN_LIMIT polls the block sets GM_FLAG_TIMEOUT in the
-// caller's counters and carries on, so no launch can hang.
+// bounded: after g_wait_limit polls (SPIN_LIMIT unless gm_set_wait_limit
+// changed it) the block sets GM_FLAG_TIMEOUT in the caller's counters and
+// carries on, so no launch can hang.
 #include <algorithm>
+#include <mutex>
 #include <utility>
 
 #include <cuda/atomic>
@@ -22,6 +24,9 @@ namespace {
 constexpr uint32_t F_AGG = 1u << 30;
 constexpr uint32_t F_PRE = 2u << 30;
 constexpr uint32_t V_MASK = (1u << 30) - 1;
+
+// Polls a waiting block makes before it gives up (per device; gm_set_wait_limit).
+__device__ uint32_t g_wait_limit = SPIN_LIMIT;
 
 __device__ __forceinline__ uint32_t ld_relaxed(uint32_t* p)
 {
@@ -65,17 +70,21 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp
 }
 
 // Walks back from partition p - 1 summing aggregates until an inclusive
-// prefix is found.  Bounded: gives up after SPIN_LIMIT polls of one slot.
+// prefix is found.  Bounded: gives up after g_wait_limit polls of one slot.
+// A block that gives up returns the sum of the aggregates it has seen, which
+// is at most the true prefix, so every offset built from it stays below the
+// true one (the callers' writes stay inside their buffers).
 __device__ __forceinline__ uint32_t look_back(uint32_t* desc, int p, int stride, int32_t* counters)
 {
     uint32_t excl = 0;
     int q = p - 1;
     uint32_t spins = 0;
+    const uint32_t limit = g_wait_limit;
     while (q >= 0) {
         uint32_t d = ld_relaxed(desc + (int64_t)q * stride);
         uint32_t flag = d & ~V_MASK;
         if (flag == 0) {
-            if (++spins > SPIN_LIMIT) {
+            if (++spins > limit) {
                 atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_TIMEOUT);
                 break;
             }
@@ -299,16 +308,59 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 }  // namespace
 
+namespace {
+
+// Per-device state of the host side: SM count and whether k_onesweep's
+// dynamic shared-memory limit has been raised (a function attribute is set per
+// device).  Guarded by one mutex: host threads may call from several devices.
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {};
+bool g_onesweep_attr[kMaxDevices] = {};
+std::mutex g_dev_mu;
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// raises k_onesweep's dynamic shared-memory limit on the current device once
+cudaError_t onesweep_attr()
+{
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_onesweep_attr[dev]) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(OnesweepSmem));
+    if (e == cudaSuccess) g_onesweep_attr[dev] = true;
+    return e;
+}
+
+}  // namespace
+
 int num_sms()
 {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 148;
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_sms[dev] <= 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+        g_sms[dev] = sms;
     }
-    return sms;
+    return g_sms[dev];
+}
+
+cudaError_t set_wait_limit(uint32_t polls)
+{
+    return cudaMemcpyToSymbol(g_wait_limit, &polls, sizeof(polls));
+}
+
+cudaError_t get_wait_limit(uint32_t* polls)
+{
+    return cudaMemcpyFromSymbol(polls, g_wait_limit, sizeof(*polls));
 }
 
 static int scan_parts(int64_t n) { return (int)((n + SCAN_PART - 1) / SCAN_PART); }
@@ -380,11 +432,8 @@ cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int
     int hgrid = (int)std::min<int64_t>(((int64_t)cap + 255) / 256, (int64_t)sms * 4);
     k_hist<<<hgrid, 256, 0, s>>>(k0, n_dev, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
     k_hist_scan<<<1, 256, 0, s>>>(ws.hist, passes);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(OnesweepSmem));
-        attr = true;
-    }
+    e = onesweep_attr();
+    if (e != cudaSuccess) return e;
     const int grid = std::min(ws.max_parts, sms * 4);
     uint64_t* kin = k0; int32_t* vin = v0;
     uint64_t* kout = k1; int32_t* vout = v1;

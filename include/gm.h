@@ -504,13 +504,36 @@ int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_op
  * then cached per device), so make that first call before any stream
  * capture.  All calls share the one array (each call clears what must start
  * at zero): calls that overlap on the GPU -- concurrent streams or host
- * threads -- race and corrupt each other's results.  Everything else as
+ * threads -- race and corrupt each other's results.  The cached address
+ * belongs to the device's context at the first call: it does not survive
+ * cudaDeviceReset (or any reset of the primary context), after which this
+ * entry point must not be called again in the same process.  Everything else as
  * gm_bin_triangles; no cudaMalloc / cudaFree or allocating library call.
  * ---------------------------------------------------------------------- */
 #define GM_NOALLOC_TRI_SCRATCH_BYTES (32u << 20)
 int gm_bin_triangles_noalloc(const gm_camera* cam, const float* V, int32_t nV, const int32_t* F,
                              int32_t nF, int32_t* tile_range, int32_t* tri_ids, int32_t cap,
                              int32_t* counters, int32_t* K_host, void* stream);
+
+/* ----------------------------------------------------------------------
+ * gm_set_wait_limit / gm_get_wait_limit -- the bound on the inter-block waits
+ * of the scans and radix sorts (the decoupled look-back of gm_bin_triangles,
+ * gm_bin_sort_gaussians, gm_sort_gaussians_by_depth, gm_bin_gaussians and
+ * gm_mesh_edges).  A waiting block polls its predecessor's descriptor at
+ * most `polls` times (default GM_WAIT_LIMIT_DEFAULT), then sets
+ * GM_FLAG_TIMEOUT in the call's counters and carries on with a prefix that is
+ * at most the true one, so every write stays inside the caller's buffers;
+ * the call's result is then not a valid sort (GM_ERR_TIMEOUT with K_host).
+ * The pages have no counterpart: this exists to test the failure path (a
+ * limit of 0 makes any block that finds its predecessor unpublished give up).
+ * The setting belongs to the current device and holds until changed; set it
+ * only while no libgm kernel runs on that device.  Synchronous
+ * (cudaMemcpyToSymbol / FromSymbol).  Errors: GM_ERR_CUDA, or
+ * GM_ERR_INVALID_ARG for a NULL `polls`.
+ * ---------------------------------------------------------------------- */
+#define GM_WAIT_LIMIT_DEFAULT (1u << 22)
+int gm_set_wait_limit(uint32_t polls);
+int gm_get_wait_limit(uint32_t* polls);
 
 /* Message describing the calling thread's last failure ("" if none). */
 const char* gm_last_error(void);

@@ -209,7 +209,7 @@ def test_backward_matches_finite_differences(name, n_gauss, n_vert, softness, or
     verts = np.unique(np.concatenate([rng.choice(vs, min(len(vs), n_vert // 2), replace=False),
                                       rng.choice(va, min(len(va), n_vert // 2), replace=False)]))
     vid, vf = np.repeat(verts, 6), np.tile(np.arange(6), len(verts))
-    vh = np.where(vf < 3, 2e-5, 1e-2)
+    vh = np.where(vf < 3, 1e-6, 1e-2)
     args = (cam, np.float64(s.bg))
     rest = (s.mesh.faces, s.mesh.vcol, m["face_id"].reshape(-1), r["splats"], lists, m["mesh_depth"].reshape(-1),
             m["mesh_rgb"].reshape(-1, 3), grads, vid, vf, vh)
@@ -230,9 +230,11 @@ def test_backward_matches_finite_differences(name, n_gauss, n_vert, softness, or
         {orc.FD_STATUS.get(v, "ulp-sensitivity"): int((vst[~vok] == v).sum()) for v in np.unique(vst[~vok])}))
     assert not vbad.any()
     # a vertex moves the depth of every pixel of its faces and the silhouettes near
-    # them: on the 512 px sphere, where the Gaussians lie on the surface, many of those
-    # pixels flip a depth test within the step and are reported, not compared
-    assert vok.sum() >= 0.4 * len(vst) and (vok & on_sil & (vf < 3)).sum() > 10
+    # them: on the 512 px sphere, where the Gaussians lie on the surface, some of
+    # those pixels flip a depth test or a crossing decision within the step and are
+    # reported, not compared (with a position step of 1e-6, 83 % of these requests
+    # are smooth for the oracle on its own inputs)
+    assert vok.sum() >= 0.65 * len(vst) and (vok & on_sil & (vf < 3)).sum() > 20
 
 
 def test_renderer_antialias_matches_calls():

@@ -7,9 +7,11 @@ Gaussians and mesh vertices / colours).
 Tolerances: rgb, depth and alpha within 1e-4 absolute; gradients within
 1e-5 absolute + 1e-3 relative of the finite-difference value.  Pixels where
 an fp32 decision of the oracle lies within rounding of its threshold (alpha
-vs 1/255 within 2e-6 relative -- the GPU's exp differs from the oracle's by a
-few ulp --, transmittance vs 1e-4 within 1e-4 relative) are counted, reported
-and left out of the value check; their number must stay tiny."""
+vs 1/255 within 8e-6 relative -- the GPU's exp, 2^l with l from a pre-scaled
+conic, differs from the oracle's by a few ulp --, transmittance vs 1e-4
+within 1e-4 relative, sigma within 1e-5 of 0: gpu_helpers.tie_pixels) are
+counted, reported and left out of the value check; their number must stay
+tiny."""
 
 import numpy as np
 import pytest
@@ -159,7 +161,7 @@ def test_backward_matches_finite_differences(name, n_gauss, n_vert, orc):
         verts = np.sort(rng.choice(verts, n_vert, replace=False))
     vid = np.repeat(verts, 6)
     vf = np.tile(np.arange(6), len(verts))
-    vh = np.where(vf < 3, 2e-5, 1e-2)
+    vh = np.where(vf < 3, 1e-6, 1e-2)
     vfd, vst = orc.mesh_fd(cam, np.float64(s.bg), s.mesh.verts, s.mesh.faces, s.mesh.vcol, m["face_id"].reshape(-1),
                            r["splats"], lists, m["mesh_depth"].reshape(-1), m["mesh_rgb"].reshape(-1, 3), grads,
                            vid, vf, vh)
@@ -183,8 +185,10 @@ def test_backward_matches_finite_differences(name, n_gauss, n_vert, orc):
                                         for v in np.unique(vst[~vok])}))
     assert not vbad.any()
     # Gaussians lying on the mesh surface flip depth-test decisions within +-h
-    # for many vertices of the 512 px sphere: those are reported, not checked
-    assert vok.sum() >= 0.6 * len(vst)
+    # for some vertices of the 512 px sphere: those are reported, not checked
+    # (a position step of 1e-6 keeps them few: 92 % of these requests are
+    # smooth for the oracle on its own inputs)
+    assert vok.sum() >= 0.75 * len(vst)
 
 
 def test_linear_in_colour_exactly():

@@ -187,6 +187,33 @@ def test_capacity_overflow_is_reported_and_contained(orc):
     assert np.all(H.host(gids)[cap:] == -1) and np.all(H.host(keys)[cap:] == 0)
 
 
+def _largest_dropped_alpha(cam, osp, dg, dt, n_max=20000, seed=2):
+    """Largest o exp(-sigma) in double, over the in-image pixel centres of tile
+    dt[k], of Gaussian dg[k] (the oracle's projection osp), on a seeded sample
+    of at most n_max pairs."""
+    TW = (cam.width + 15) // 16
+    rng = np.random.default_rng(seed)
+    if len(dg) > n_max:
+        sel = rng.choice(len(dg), n_max, replace=False)
+        dg, dt = dg[sel], dt[sel]
+    off = np.arange(16) + 0.5
+    worst = 0.0
+    for lo in range(0, len(dg), 4096):
+        g, t = dg[lo:lo + 4096], dt[lo:lo + 4096]
+        rec = osp[g].astype(np.float64)
+        tx, ty = (t % TW) * 16, (t // TW) * 16
+        xs = tx[:, None] + off[None, :]
+        ys = ty[:, None] + off[None, :]
+        dx = xs[:, None, :] - rec[:, 0, None, None]
+        dy = ys[:, :, None] - rec[:, 1, None, None]
+        sig = 0.5 * (rec[:, 2, None, None] * dx * dx + rec[:, 4, None, None] * dy * dy) + rec[:, 3, None, None] * dx * dy
+        inside = (xs[:, None, :] < cam.width) & (ys[:, :, None] < cam.height)
+        a = rec[:, 5, None, None] * np.exp(-np.maximum(sig, 0.0))
+        a = np.where(inside & (sig >= 0), a, 0.0)
+        worst = max(worst, float(a.max()) if a.size else 0.0)
+    return worst
+
+
 def _tile_test_cases():
     soup = scenes.soup1080(n_gauss=150_000, n_tri=30_000)
     cam = scenes.look_at((0, 0, 6), (0, 0, 0), 480, 272, 300, 300)
@@ -224,26 +251,7 @@ def test_tile_test_drops_only_unreachable_pairs(case, orc):
     dg = np.concatenate(dropped_g)
     dt = np.concatenate(dropped_t)
     osp, _, _, _ = orc.project(cam, s.gaussians)
-    rng = np.random.default_rng(2)
-    if len(dg) > 20000:
-        sel = rng.choice(len(dg), 20000, replace=False)
-        dg, dt = dg[sel], dt[sel]
-    # max over the tile's in-image pixel centres of o exp(-sigma), in double
-    off = np.arange(16) + 0.5
-    worst = 0.0
-    for lo in range(0, len(dg), 4096):
-        g, t = dg[lo:lo + 4096], dt[lo:lo + 4096]
-        rec = osp[g].astype(np.float64)
-        tx, ty = (t % TW) * 16, (t // TW) * 16
-        xs = tx[:, None] + off[None, :]
-        ys = ty[:, None] + off[None, :]
-        dx = xs[:, None, :] - rec[:, 0, None, None]
-        dy = ys[:, :, None] - rec[:, 1, None, None]
-        sig = 0.5 * (rec[:, 2, None, None] * dx * dx + rec[:, 4, None, None] * dy * dy) + rec[:, 3, None, None] * dx * dy
-        inside = (xs[:, None, :] < cam.width) & (ys[:, :, None] < cam.height)
-        a = rec[:, 5, None, None] * np.exp(-np.maximum(sig, 0.0))
-        a = np.where(inside & (sig >= 0), a, 0.0)
-        worst = max(worst, float(a.max()) if a.size else 0.0)
+    worst = _largest_dropped_alpha(cam, osp, dg, dt)
     print("%s: K %d -> %d (%.1f %% dropped); largest alpha of a dropped pair %.3g" % (
         name, ex["K"], ti["K"], 100.0 * (1 - ti["K"] / max(ex["K"], 1)), worst))
     assert worst < 1.0 / 255.0
@@ -283,3 +291,79 @@ def test_split_binning_equals_one_call():
         np.testing.assert_array_equal(H.host(gids)[:K], ref["gids"])
         np.testing.assert_array_equal(H.host(tr), ref["tile_range"])
         np.testing.assert_array_equal(H.host(cnt), ref["counters"])
+
+
+@pytest.fixture(scope="module")
+def bench_bins():
+    """The 1080p workload (1,000,000 Gaussians with degree-3 SH, 200,000-triangle
+    soup) as the renderer the benchmark times bins it: its projected records,
+    mesh tile bounds and its own bins (tile test and occlusion cull on)."""
+    H.need_gpu()
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    s = scenes.soup1080()
+    r = gm.HybridRenderer(s.camera, bg=s.bg)
+    r.upload(s.mesh, s.gaussians)
+    r.forward(sync=True)
+    K = int(r.K_gauss)
+    out = dict(scene=s, sp=H.host(r.splats), rad=H.host(r.radii), tile_far=H.host(r.tile_far),
+               tile_full=H.host(r.tile_full), keys=H.host(r.keys)[:K].view(np.uint64), gids=H.host(r.gids)[:K],
+               tile_range=H.host(r.g_range), K=K, counters=H.host(r.g_counters))
+    del r
+    torch_sync()
+    return out
+
+
+def torch_sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("cull", [False, True])
+def test_bin_sort_exact_at_bench_size(bench_bins, cull, orc):
+    """Rectangle bins of the full 1080p workload (6.5 M entries before the cull,
+    four depth passes over 1 M keys and two tile passes) equal the oracle's
+    bit for bit: keys, ids, tile ranges and counts, with and without the cull."""
+    b = bench_bins
+    cam = b["scene"].camera
+    g = H.run_bin(cam, b["sp"], b["rad"], b["tile_far"], b["tile_full"], cull)
+    keys, gids, pre = orc.bin_gaussians(cam, b["sp"], b["rad"], b["tile_far"], b["tile_full"], cull)
+    assert g["K"] == len(keys) and g["counters"][1] == pre and g["counters"][2] == 0
+    np.testing.assert_array_equal(g["keys"], keys)
+    np.testing.assert_array_equal(g["gids"], gids)
+    start, _ = H.lists_from_bins(cam, keys, gids)
+    tr = g["tile_range"]
+    cnt = np.diff(start)
+    np.testing.assert_array_equal(tr[:, 1] - tr[:, 0], cnt)
+    np.testing.assert_array_equal(tr[cnt > 0, 0], start[:-1][cnt > 0])
+    print("1080p cull=%d: K=%d (pre-cull %d)" % (cull, len(keys), pre))
+
+
+def test_renderer_bins_at_bench_size_thin_the_exact_bins(bench_bins, orc):
+    """The renderer's own bins in the benchmark's configuration (tile test and
+    cull on) are the oracle's exact culled bins with entries removed: the same
+    keys in the same order for what is kept, consistent tile ranges, and every
+    removed (Gaussian, tile) pair below alpha 1/255 at every pixel centre of
+    its tile (a seeded sample of 20,000, in double)."""
+    b = bench_bins
+    s = b["scene"]
+    cam = s.camera
+    keys, gids, pre = orc.bin_gaussians(cam, b["sp"], b["rad"], b["tile_far"], b["tile_full"], True)
+    assert b["counters"][1] == pre and b["counters"][2] == 0 and b["counters"][0] == b["K"]
+    ce = ((keys >> np.uint64(32)).astype(np.int64) << 32) | gids.astype(np.int64)
+    cr = ((b["keys"] >> np.uint64(32)).astype(np.int64) << 32) | b["gids"].astype(np.int64)
+    keep = np.isin(ce, cr)
+    assert keep.sum() == len(cr)
+    np.testing.assert_array_equal(ce[keep], cr)          # same entries in the same order
+    np.testing.assert_array_equal(keys[keep], b["keys"])  # with the same depth bits
+    start, _ = H.lists_from_bins(cam, b["keys"], b["gids"])
+    cnt = np.diff(start)
+    tr = b["tile_range"]
+    np.testing.assert_array_equal(tr[:, 1] - tr[:, 0], cnt)
+    np.testing.assert_array_equal(tr[cnt > 0, 0], start[:-1][cnt > 0])
+    osp, _, _, _ = orc.project(cam, s.gaussians)
+    dg = gids[~keep]
+    dt = (keys[~keep] >> np.uint64(32)).astype(np.int64)
+    worst = _largest_dropped_alpha(cam, osp, dg, dt)
+    print("1080p renderer bins: %d exact culled entries, %d kept (%.1f %% dropped by the tile test); largest alpha "
+          "of a dropped pair %.3g" % (len(keys), len(cr), 100.0 * (1 - len(cr) / len(keys)), worst))
+    assert worst < 1.0 / 255.0

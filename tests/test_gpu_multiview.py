@@ -1,4 +1,4 @@
-"""Batched views (§8(f) NEXT-4; page "A Lightweight and Differentiable Renderer
+"""Batched views (page "A Lightweight and Differentiable Renderer
 for Joint Mesh and 3D Gaussian Splat Scenes", Hybrid rendering: the renderer
 is run per camera; a training batch holds several cameras of one scene).
 

@@ -304,7 +304,7 @@ def test_soft_backward_matches_finite_differences(name, n_gauss, n_vert, split, 
         verts = np.sort(rng.choice(verts, n_vert, replace=False))
     vid = np.repeat(verts, 6)
     vf = np.tile(np.arange(6), len(verts))
-    vh = np.where(vf < 3, 2e-5, 1e-2)
+    vh = np.where(vf < 3, 1e-6, 1e-2)
     args = (cam, np.float64(s.bg))
     rest = (s.mesh.faces, s.mesh.vcol, m["face_id"].reshape(-1), r["splats"], lists, m["mesh_depth"].reshape(-1),
             m["mesh_rgb"].reshape(-1, 3), grads, vid, vf, vh)
@@ -322,7 +322,7 @@ def test_soft_backward_matches_finite_differences(name, n_gauss, n_vert, split, 
         print("  vertex %d field %d: gpu %.7g fd %.7g" % (vid[k], vf[k], vgot[k], vfd[k]))
     print("%s: %d mesh parameters checked, %d excluded" % (name, vok.sum(), (~vok).sum()))
     assert not vbad.any()
-    assert vok.sum() >= 0.6 * len(vst)
+    assert vok.sum() >= 0.75 * len(vst)
 
 
 def test_renderer_soft_matches_calls():
