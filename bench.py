@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-multiview", action="store_true", help="skip the batched 8-view measurement")
     ap.add_argument("--no-soft", action="store_true", help="skip the soft-split measurement")
     ap.add_argument("--no-aa", action="store_true", help="skip the antialiased-mesh measurement")
+    ap.add_argument("--no-staged", action="store_true",
+                    help="backward composite gathers its records instead of bulk-copying the forward's staged ones")
     ap.add_argument("--cpu-tiles", type=int, default=1200,
                     help="tiles of the frame the CPU oracle renders (about 10 s of oracle work at 1080p)")
     ap.add_argument("--ref-tiles", type=int, default=400,
@@ -204,7 +206,7 @@ def run_gm(args, ws, rank, local):
     scene = scenes.make(args.config)
     cam = scene.camera
     W, H = cam.width, cam.height
-    r = gm.HybridRenderer(cam, bg=scene.bg, cull_occluded=True, device="cuda")
+    r = gm.HybridRenderer(cam, bg=scene.bg, cull_occluded=True, device="cuda", staged=not args.no_staged)
     r.upload(scene.mesh, scene.gaussians)
     grads_np = scenes.upstream_grads(0, W, H)
     g_dev = [torch.as_tensor(x).cuda() for x in grads_np]
@@ -234,7 +236,7 @@ def run_gm(args, ws, rank, local):
         mark(4)
         gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
-                                   stats_f if count else None)
+                                   stats_f if count else None, staged=r.staged)
         mark(5)
         r.v_splats.zero_()
         r.v_verts.zero_()
@@ -244,7 +246,7 @@ def run_gm(args, ws, rank, local):
         # that each kernel gets its own events; the timed graph step makes one call
         gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats, None, None,
-                                   None, None, None, stats_b if count else None)
+                                   None, None, None, stats_b if count else None, staged=r.staged)
         mark(7)
         gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], None, r.V, r.F,
@@ -527,13 +529,13 @@ def run_soft(args, scene, grads_np, flush, dist, softness=1.0):
     def fwd():
         gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
-                                   depth_model=r.depth_model)
+                                   depth_model=r.depth_model, staged=r.staged)
 
     def bwd():
         gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb, r.face_id,
                                    r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats,
                                    depth_model=r.depth_model, v_depth_model=r.v_depth_model,
-                                   v_mesh_depth=r.v_mesh_depth)
+                                   v_mesh_depth=r.v_mesh_depth, staged=r.staged)
 
     ms_step = timed(graph.replay)
     ms_fwd = timed(fwd)
@@ -588,12 +590,13 @@ def run_antialiased(args, scene, grads_np, flush, dist):
 
     def fwd():
         gm.gm_composite_hybrid_fwd(cam_c, opts, r.g_range, r.gids, r.splats, r.depth_aa, r.rgb_aa, r.face_id,
-                                   r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib, aa=r.aa)
+                                   r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib, aa=r.aa,
+                                   staged=r.staged)
 
     def bwd():
         gm.gm_composite_hybrid_bwd(cam_c, opts, r.g_range, r.gids, r.splats, r.depth_aa, r.rgb_aa, r.face_id,
                                    r.T_final, r.n_contrib, g_dev[0], g_dev[1], g_dev[2], r.v_splats,
-                                   v_mesh_depth=r.v_mesh_depth, aa=r.aa)
+                                   v_mesh_depth=r.v_mesh_depth, aa=r.aa, staged=r.staged)
 
     def layer_bwd():
         gm.gm_antialias_bwd(cam_c, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov, r.depth_aa,

@@ -57,6 +57,11 @@ class gm_aa_layer(C.Structure):
                 ("v_cov", C.c_void_p), ("v_rgb", C.c_void_p)]
 
 
+class gm_staged(C.Structure):
+    """Staged-record buffer of the tile lists (gm.h: gm_staged)."""
+    _fields_ = [("recs", C.c_void_p), ("cap", C.c_int32)]
+
+
 _VP = C.c_void_p
 _I32 = C.c_int32
 _SIGS = {
@@ -76,8 +81,10 @@ _SIGS = {
     "gm_bin_gaussians": (C.c_int, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
                                    C.c_size_t, _VP]),
     "gm_sort_gaussians_by_depth": (C.c_int, [_VP, _I32, _VP, _VP, _I32, _VP, _VP, C.c_size_t, _VP]),
-    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 15),
-    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16 + [_I32, _VP, _I32] + [_VP] * 6),
+    "gm_composite_hybrid_fwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16),
+    "gm_composite_hybrid_bwd": (C.c_int, [_VP, _VP, _I32] + [_VP] * 16 + [_I32, _VP, _I32] + [_VP] * 7),
+    "gm_staged_bytes": (C.c_size_t, [_I32, C.c_float]),
+    "gm_get_copy_status": (C.c_int, [C.POINTER(C.c_uint32), _I32]),
     "gm_mesh_edges_workspace_size": (C.c_size_t, [_I32]),
     "gm_mesh_edges": (C.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, C.c_size_t, _VP]),
     "gm_antialias": (C.c_int, [_VP, _VP, _I32, _VP, _I32] + [_VP] * 10),
@@ -368,21 +375,44 @@ def gm_bin_gaussians(cam: gm_camera, opts: gm_opts, splats, radii, tile_far, til
     return k.value if sync else None
 
 
+def gm_staged_bytes(cap: int, softness: float = 0.0) -> int:
+    return int(lib().gm_staged_bytes(int(cap), float(softness)))
+
+
+def make_staged(recs, cap: int) -> gm_staged:
+    """gm_staged over a 16-byte aligned device buffer of gm_staged_bytes(cap, softness) bytes."""
+    s = gm_staged()
+    s.recs = _p(recs)
+    s.cap = int(cap)
+    return s
+
+
+def gm_get_copy_status(clear: bool = False) -> int:
+    v = C.c_uint32(0)
+    _check(lib().gm_get_copy_status(C.byref(v), int(bool(clear))), "gm_get_copy_status")
+    return int(v.value)
+
+
+def _staged_ref(st):
+    return None if st is None else C.byref(st)
+
+
 def gm_composite_hybrid_fwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
                             out_rgb, out_depth, out_alpha, T_final, n_contrib, stats=None, depth_model=None,
-                            aa=None):
+                            aa=None, staged=None):
     _check(lib().gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
                                          _p(gids, I32), _p(splats, F32), _p(depth_model, F32),
                                          _p(mesh_depth, F32), _p(mesh_rgb, F32), _p(face_id, I32),
                                          _p(out_rgb, F32), _p(out_depth, F32), _p(out_alpha, F32), _p(T_final, F32),
-                                         _p(n_contrib, I32), _aa_ref(aa), _p(stats, I64), _stream()),
+                                         _p(n_contrib, I32), _aa_ref(aa), _staged_ref(staged), _p(stats, I64),
+                                         _stream()),
            "gm_composite_hybrid_fwd")
 
 
 def gm_composite_hybrid_bwd(cam: gm_camera, opts: gm_opts, tile_range, gids, splats, mesh_depth, mesh_rgb, face_id,
                             T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, V=None, F=None, vcol=None,
                             v_verts=None, v_vcol=None, stats=None, depth_model=None, v_depth_model=None,
-                            v_mesh_depth=None, aa=None):
+                            v_mesh_depth=None, aa=None, staged=None):
     nV = 0 if V is None else V.shape[0]
     nF = 0 if F is None else F.shape[0]
     _check(lib().gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), splats.shape[0], _p(tile_range, I32),
@@ -391,8 +421,8 @@ def gm_composite_hybrid_bwd(cam: gm_camera, opts: gm_opts, tile_range, gids, spl
                                          _p(T_final, F32), _p(n_contrib, I32), _p(g_rgb, F32), _p(g_depth, F32),
                                          _p(g_alpha, F32), _p(v_splats, F32), _p(v_depth_model, F32),
                                          _p(v_mesh_depth, F32), _p(V, F32), nV, _p(F, I32), nF,
-                                         _p(vcol, F32), _p(v_verts, F32), _p(v_vcol, F32), _aa_ref(aa), _p(stats, I64),
-                                         _stream()),
+                                         _p(vcol, F32), _p(v_verts, F32), _p(v_vcol, F32), _aa_ref(aa),
+                                         _staged_ref(staged), _p(stats, I64), _stream()),
            "gm_composite_hybrid_bwd")
 
 
@@ -426,6 +456,10 @@ class HybridRenderer:
     (no triangle lists); ``zbuffer="tile"`` with ``gm_bin_triangles`` and
     ``gm_zbuffer``.  Both give the same face ids.
 
+    ``staged=True`` (default) gives the forward composite a staged-record
+    buffer (``gm_staged``) that the backward composite then reads with bulk
+    copies; ``staged=False`` makes the backward gather the records itself.
+
     ``softness > 0`` selects the soft split at the mesh surface (front
     fraction ``soft_split``: GM_SPLIT_PHI or GM_SPLIT_LOGISTIC): the
     projection also writes each Gaussian's depth model (``depth_model``), the
@@ -436,8 +470,10 @@ class HybridRenderer:
 
     def __init__(self, cam, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", headroom=1.25,
                  concurrent=True, tile_test=True, softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False,
-                 zbuffer="direct"):
+                 zbuffer="direct", staged=True):
         self.cam_desc = cam
+        self.use_staged = bool(staged)
+        self.staged = None
         self.cam = make_camera(cam)
         self.W, self.H = int(cam.width), int(cam.height)
         self.TW, self.TH = (self.W + TILE - 1) // TILE, (self.H + TILE - 1) // TILE
@@ -545,6 +581,10 @@ class HybridRenderer:
         self.gids = torch.empty(cap, dtype=I32, device=d)
         nb = gm_bin_sort_gaussians_workspace_size(self.N, cap, self.W, self.H)
         self.g_ws = torch.empty((nb + 15) // 16 * 16, dtype=U8, device=d)
+        if self.use_staged:
+            nb = gm_staged_bytes(cap, self.softness)
+            self.staged_buf = torch.empty((nb + 15) // 16 * 16, dtype=U8, device=d)
+            self.staged = make_staged(self.staged_buf, cap)
 
     def _alloc_mesh_ws(self):
         """Triangle-list buffers (tile z-buffer) or the direct z-buffer's workspace."""
@@ -622,7 +662,7 @@ class HybridRenderer:
         md, mc = (self.depth_aa, self.rgb_aa) if self.antialias else (self.mesh_depth, self.mesh_rgb)
         gm_composite_hybrid_fwd(cam, opts, self.g_range, self.gids, self.splats, md, mc,
                                 self.face_id, self.out_rgb, self.out_depth, self.out_alpha, self.T_final,
-                                self.n_contrib, depth_model=self.depth_model, aa=self.aa)
+                                self.n_contrib, depth_model=self.depth_model, aa=self.aa, staged=self.staged)
         return self.out_rgb, self.out_depth, self.out_alpha
 
     def _ensure_mesh_grads(self):
@@ -642,7 +682,7 @@ class HybridRenderer:
             gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.depth_aa, self.rgb_aa,
                                     self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha,
                                     self.v_splats, depth_model=self.depth_model, v_depth_model=self.v_depth_model,
-                                    v_mesh_depth=self.v_mesh_depth, aa=self.aa)
+                                    v_mesh_depth=self.v_mesh_depth, aa=self.aa, staged=self.staged)
             if not mesh_grads:
                 return self.v_splats, None, None
             self._ensure_mesh_grads()
@@ -668,7 +708,8 @@ class HybridRenderer:
             gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
                                     self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha,
                                     self.v_splats, *mesh, depth_model=self.depth_model,
-                                    v_depth_model=self.v_depth_model, v_mesh_depth=self.v_mesh_depth)
+                                    v_depth_model=self.v_depth_model, v_mesh_depth=self.v_mesh_depth,
+                                    staged=self.staged)
             return (self.v_splats,) + ((self.v_verts, self.v_vcol) if mesh_grads else (None, None))
         if mesh_grads:
             if not hasattr(self, "v_verts") or self.v_verts.shape != self.V.shape:
@@ -685,7 +726,8 @@ class HybridRenderer:
                                         g_alpha, None, self.V, self.F, self.vcol, self.v_verts, self.v_vcol)
         self.v_splats.zero_()
         gm_composite_hybrid_bwd(cam, opts, self.g_range, self.gids, self.splats, self.mesh_depth, self.mesh_rgb,
-                                self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha, self.v_splats)
+                                self.face_id, self.T_final, self.n_contrib, g_rgb, g_depth, g_alpha, self.v_splats,
+                                staged=self.staged)
         if mesh_grads and self.concurrent:
             main.wait_stream(side)
         if mesh_grads:
@@ -732,10 +774,10 @@ class MultiViewRenderer:
     """
 
     def __init__(self, cams, bg=(1.0, 1.0, 1.0), cull_occluded=True, device="cuda", tile_test=True, streams=4,
-                 softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False, zbuffer="direct"):
+                 softness=0.0, soft_split=GM_SPLIT_PHI, antialias=False, zbuffer="direct", staged=True):
         self.views = [HybridRenderer(c, bg=bg, cull_occluded=cull_occluded, device=device, concurrent=False,
                                      tile_test=tile_test, softness=softness, soft_split=soft_split,
-                                     antialias=antialias, zbuffer=zbuffer) for c in cams]
+                                     antialias=antialias, zbuffer=zbuffer, staged=staged) for c in cams]
         self.antialias = bool(antialias)
         self.soft = self.views[0].soft
         self.V = len(self.views)
@@ -820,7 +862,7 @@ class MultiViewRenderer:
                 md, mc = (r.depth_aa, r.rgb_aa) if r.antialias else (r.mesh_depth, r.mesh_rgb)
                 gm_composite_hybrid_fwd(cam, opts, r.g_range, r.gids, r.splats, md, mc, r.face_id,
                                         r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib,
-                                        depth_model=r.depth_model, aa=r.aa)
+                                        depth_model=r.depth_model, aa=r.aa, staged=r.staged)
         for s in pool:
             main.wait_stream(s)
         return [(r.out_rgb, r.out_depth, r.out_alpha) for r in self.views]
@@ -846,7 +888,7 @@ class MultiViewRenderer:
                     gm_composite_hybrid_bwd(r.cam, r.opts, r.g_range, r.gids, r.splats, r.depth_aa, r.rgb_aa,
                                             r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
                                             depth_model=r.depth_model, v_depth_model=r.v_depth_model,
-                                            v_mesh_depth=r.v_mesh_depth, aa=r.aa)
+                                            v_mesh_depth=r.v_mesh_depth, aa=r.aa, staged=r.staged)
                     gm_antialias_bwd(r.cam, r.V, r.F, r.adj, r.face_id, r.mesh_depth, r.mesh_rgb, r.cov,
                                      r.depth_aa, r.v_cov, r.v_rgb_aa, r.v_mesh_depth, r.v_mesh_rgb, r.v_interp_depth,
                                      self.v_verts)
@@ -856,7 +898,8 @@ class MultiViewRenderer:
                 gm_composite_hybrid_bwd(r.cam, r.opts, r.g_range, r.gids, r.splats, r.mesh_depth, r.mesh_rgb,
                                         r.face_id, r.T_final, r.n_contrib, g_rgb, g_depth, g_alpha, r.v_splats,
                                         r.V, r.F, r.vcol, self.v_verts, self.v_vcol, depth_model=r.depth_model,
-                                        v_depth_model=r.v_depth_model, v_mesh_depth=r.v_mesh_depth)
+                                        v_depth_model=r.v_depth_model, v_mesh_depth=r.v_mesh_depth,
+                                        staged=r.staged)
         for s in pool:
             main.wait_stream(s)
         v0 = self.views[0]

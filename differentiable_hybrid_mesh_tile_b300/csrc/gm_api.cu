@@ -100,6 +100,15 @@ extern "C" {
 
 const char* gm_last_error(void) { return g_err; }
 
+size_t gm_staged_bytes(int32_t cap, float softness) { return gm::staged_bytes(cap, softness > 0.0f); }
+
+int gm_get_copy_status(uint32_t* flags, int32_t clear)
+{
+    GM_REQUIRE(flags, "flags is NULL");
+    cudaError_t e = gm::copy_status(flags, clear != 0);
+    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_get_copy_status");
+}
+
 int gm_set_wait_limit(uint32_t polls)
 {
     cudaError_t e = gm::set_wait_limit(polls);
@@ -449,7 +458,7 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const int32_t* gids, const float* splats, const float* depth_model,
                             const float* mesh_depth, const float* mesh_rgb, const int32_t* face_id, float* out_rgb,
                             float* out_depth, float* out_alpha, float* T_final, int32_t* n_contrib,
-                            const gm_aa_layer* aa, uint64_t* stats, void* stream)
+                            const gm_aa_layer* aa, const gm_staged* staged, uint64_t* stats, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
@@ -469,10 +478,13 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     const bool soft = opts->softness > 0.0f;
     GM_REQUIRE(!soft || N == 0 || (depth_model && aligned16(depth_model)),
                "the soft split needs a 16-byte aligned depth_model");
+    if (staged) GM_REQUIRE(staged->recs && aligned16(staged->recs) && staged->cap >= 0,
+                           "staged records need a 16-byte aligned buffer and a capacity >= 0");
     cudaError_t e = gm::composite_fwd(gm::make_cam(*cam), opts->bg, N, opts->softness, opts->soft_split, tile_range,
                                       gids, splats,
                                       depth_model, mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
-                                      T_final, n_contrib, layer_of(aa), stats, (cudaStream_t)stream);
+                                      T_final, n_contrib, layer_of(aa), staged ? staged->recs : nullptr,
+                                      staged ? staged->cap : 0, stats, (cudaStream_t)stream);
     return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_composite_hybrid_fwd");
 }
 
@@ -482,7 +494,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const float* T_final, const int32_t* n_contrib, const float* g_rgb, const float* g_depth,
                             const float* g_alpha, float* v_splats, float* v_depth_model, float* v_mesh_depth,
                             const float* V, int32_t nV, const int32_t* F, int32_t nF, const float* vcol,
-                            float* v_verts, float* v_vcol, const gm_aa_layer* aa, uint64_t* stats, void* stream)
+                            float* v_verts, float* v_vcol, const gm_aa_layer* aa, const gm_staged* staged,
+                            uint64_t* stats, void* stream)
 {
     g_err[0] = 0;
     if (int st = check_cam(cam)) return st;
@@ -507,6 +520,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
     GM_REQUIRE(g_rgb && g_depth && g_alpha, "an upstream gradient is NULL");
     GM_REQUIRE(!splats || aligned16(splats), "splats must be 16-byte aligned");
     GM_REQUIRE(!v_splats || aligned16(v_splats), "v_splats must be 16-byte aligned");
+    if (staged) GM_REQUIRE(staged->recs && aligned16(staged->recs) && staged->cap >= 0,
+                           "staged records need a 16-byte aligned buffer and a capacity >= 0");
     GM_REQUIRE(nV >= 0 && nF >= 0 && N >= 0, "negative size");
     GM_REQUIRE(N == 0 || !v_splats || (splats && gids), "splats / gids is NULL");
     const bool mesh_grads = v_verts || v_vcol;
@@ -519,7 +534,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
         e = gm::composite_bwd(c, opts->bg, N, opts->softness, opts->soft_split, tile_range, gids, splats, depth_model,
                               mesh_depth,
                               mesh_rgb, face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model,
-                              soft || aa_on ? v_mesh_depth : nullptr, layer_of(aa), stats, s);
+                              soft || aa_on ? v_mesh_depth : nullptr, layer_of(aa), staged ? staged->recs : nullptr,
+                              staged ? staged->cap : 0, stats, s);
     if (e == cudaSuccess && mesh_grads && nF > 0)
         e = gm::mesh_bwd(c, V, nV, F, nF, vcol, face_id, T_final, g_rgb, g_depth, soft ? v_mesh_depth : nullptr,
                          v_verts, v_vcol, s);

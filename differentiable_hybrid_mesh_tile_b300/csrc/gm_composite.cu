@@ -28,6 +28,17 @@ constexpr int CTA_WARPS = 4;                  // 8 x 4 blocks per CTA: half a ti
 constexpr int CTA_THREADS = 32 * CTA_WARPS;   // = staging batch
 constexpr int CTAS_PER_TILE = 8 / CTA_WARPS;
 
+// Staged records of a tile list (one per list position, three float4 arrays,
+// a fourth with the soft split's depth model): written by the forward pass,
+// bulk-copied into shared memory by the backward pass.  A == nullptr: none.
+struct Staged {
+    float4* A;
+    float4* B;
+    float4* C;
+    float4* D;
+    int cap;  // list positions the arrays hold
+};
+
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
@@ -35,57 +46,68 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// Staged record.  The conic is stored pre-multiplied so that
+// Staged record, three float4.  The conic is stored pre-multiplied so that
 // exp(-sigma) = 2^l, l = a2 dx^2 + b2 dx dy + c2 dy^2, a2 = -a log2e / 2,
 // b2 = -b log2e, c2 = -c log2e / 2 (a2, c2 < 0 for a positive definite conic):
-//   A = (mx, my, a2, b2), B = (c2, opacity, r, g), C = (b, depth, -, -),
-//   H = (lmin, ka, kc, -): alpha >= 1/255 needs l >= lmin = -log2(255 o);
-//   ka = -1 / (2 a2), kc = -1 / (2 c2) locate the maximum of l along a line.
-__device__ __forceinline__ void stage(const float4* __restrict__ splats, int64_t g, float4& A, float4& B, float4& C,
-                                      float4& H)
+//   A = (mx, my, a2, b2), B = (c2, opacity, r, g), C = (b, depth, id, lmin),
+// id the Gaussian's index (its int bits; -1 for an entry that draws nothing)
+// and lmin = -log2(255 o): alpha >= 1/255 needs l >= lmin (-inf for a
+// degenerate conic, every pixel evaluated; +inf when alpha never reaches 1/255).
+__device__ __forceinline__ void stage_rec(const float4* __restrict__ splats, int g, float4& A, float4& B, float4& C)
 {
-    const float4 s0 = splats[3 * g], s1 = splats[3 * g + 1], s2 = splats[3 * g + 2];
+    if (g < 0) {
+        A = make_float4(0.f, 0.f, 0.f, 0.f);
+        B = make_float4(0.f, 0.f, 0.f, 0.f);
+        C = make_float4(0.f, 0.f, __int_as_float(-1), INFINITY);
+        return;
+    }
+    const float4 s0 = splats[3 * (int64_t)g], s1 = splats[3 * (int64_t)g + 1], s2 = splats[3 * (int64_t)g + 2];
     // s0 = (mx, my, a, b), s1 = (c, o, r, g), s2 = (b, depth, 0, 0)
     A = make_float4(s0.x, s0.y, -0.5f * LOG2E * s0.z, -LOG2E * s0.w);
     B = make_float4(-0.5f * LOG2E * s1.x, s1.y, s1.z, s1.w);
-    C = make_float4(s2.x, s2.y, 0.0f, 0.0f);
     const float o255 = 255.0f * s1.y;
     const float det = s0.z * s1.x - s0.w * s0.w;
+    float lmin;
     if (!(det > 0.0f) || !(s0.z > 0.0f)) {
-        H = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);  // degenerate conic: every pixel is evaluated
+        lmin = -INFINITY;  // degenerate conic: every pixel is evaluated
     } else if (!(o255 >= 1.0f)) {
-        H = make_float4(INFINITY, 0.0f, 0.0f, 0.0f);   // exp(-sigma) <= 1: never reaches 1/255
+        lmin = INFINITY;   // exp(-sigma) <= 1: never reaches 1/255
     } else {
         // lowered by 0.1 % + 1e-4 so that rounding in the block test never drops a
         // pixel the exact evaluation keeps
-        const float lmin = -log2f(o255) * 1.001f - 1e-4f;
-        H = make_float4(lmin, -0.5f / A.z, -0.5f / B.x, 0.0f);
+        lmin = -log2f(o255) * 1.001f - 1e-4f;
     }
+    C = make_float4(s2.x, s2.y, __int_as_float(g), lmin);
 }
+
+__device__ __forceinline__ int rec_id(const float4& C) { return __float_as_int(C.z); }
 
 // Whether the Gaussian can reach alpha >= 1/255 at any pixel centre of the
 // warp's 8 x 4 block (centres x0 .. x0 + 7, y0 .. y0 + 3): the maximum of the
 // concave l over that rectangle is 0 when it holds the mean, else it lies on
-// an edge, where l is a 1D parabola maximised at a clamped vertex.
-__device__ __forceinline__ bool block_hits(const float4& A, const float4& B, const float4& H, float x0, float y0)
+// an edge, where l is a 1D parabola maximised at a clamped vertex.  The
+// vertices need -1 / (2 a2) and -1 / (2 c2); an approximate quotient moves a
+// vertex by a few ulp, which changes l there far less than lmin's margin.
+__device__ __forceinline__ bool block_hits(const float4& A, const float4& B, float lmin, float x0, float y0)
 {
-    if (!(H.x <= 0.0f)) return false;       // invisible
-    if (H.x == -INFINITY) return true;       // degenerate: evaluate
+    if (!(lmin <= 0.0f)) return false;      // invisible
+    if (lmin == -INFINITY) return true;      // degenerate: evaluate
     const float u0 = x0 - A.x, u1 = u0 + 7.0f, v0 = y0 - A.y, v1 = v0 + 3.0f;
     if (u0 <= 0.0f && u1 >= 0.0f && v0 <= 0.0f && v1 >= 0.0f) return true;
     const float a2 = A.z, b2 = A.w, c2 = B.x;
+    const float ka = __fdividef(-0.5f, a2), kc = __fdividef(-0.5f, c2);
     float best = -INFINITY;
     {   // edges u = u0, u1: v* = b2 u kc
-        const float va = fminf(fmaxf(b2 * u0 * H.z, v0), v1), vb = fminf(fmaxf(b2 * u1 * H.z, v0), v1);
+        const float va = fminf(fmaxf(b2 * u0 * kc, v0), v1), vb = fminf(fmaxf(b2 * u1 * kc, v0), v1);
         best = fmaxf(best, fmaf(fmaf(a2, u0, b2 * va), u0, c2 * va * va));
         best = fmaxf(best, fmaf(fmaf(a2, u1, b2 * vb), u1, c2 * vb * vb));
     }
     {   // edges v = v0, v1: u* = b2 v ka
-        const float ua = fminf(fmaxf(b2 * v0 * H.y, u0), u1), ub = fminf(fmaxf(b2 * v1 * H.y, u0), u1);
+        const float ua = fminf(fmaxf(b2 * v0 * ka, u0), u1), ub = fminf(fmaxf(b2 * v1 * ka, u0), u1);
         best = fmaxf(best, fmaf(fmaf(c2, v0, b2 * ua), v0, a2 * ua * ua));
         best = fmaxf(best, fmaf(fmaf(c2, v1, b2 * ub), v1, a2 * ub * ub));
     }
-    return best >= H.x;
+    return best >= lmin;
 }
 
 // alpha of one staged record at pixel centre (px, py).  Both passes call this
@@ -141,12 +163,6 @@ __device__ __forceinline__ PixelMap pixel_of(const Cam& c, int& tile)
     return m;
 }
 
-__device__ __forceinline__ void stage_empty(float4& C, float4& H)
-{
-    H = make_float4(INFINITY, 0.0f, 0.0f, 0.0f);
-    C = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
 // The soft split: its width factor and the form of the front fraction f(x),
 // Phi(x) or the logistic 1 / (1 + exp(-1.702 x)).  Past x <= -tail, f(x) <=
 // 0.0030 (Phi(-2.75)) or 0.0026 (logistic at -3.5), so alpha f <= 0.99 f <
@@ -191,6 +207,16 @@ __device__ __forceinline__ float warp_hide_depth(bool inside, bool cov, float D)
     return isinf(k) ? k : k + 4e-6f * fabsf(k);
 }
 
+// A tile's range clamped to the staged-record buffer [0, cap) (the ranges come
+// from a sort that may have given up a bounded wait; the bulk copies read the
+// records by range, so they must stay inside the buffer).
+__device__ __forceinline__ int2 clamp_range(int2 r, int cap)
+{
+    r.x = min(max(r.x, 0), cap);
+    r.y = min(max(r.y, r.x), cap);
+    return r;
+}
+
 template <bool STATS, bool SOFT>
 __global__ void __launch_bounds__(CTA_THREADS)
 k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
@@ -198,9 +224,10 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
                 const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id, float* __restrict__ out_rgb,
                 float* __restrict__ out_depth, float* __restrict__ out_alpha, float* __restrict__ T_final,
-                int32_t* __restrict__ n_contrib, const float* __restrict__ aa_cov, unsigned long long* __restrict__ stats)
+                int32_t* __restrict__ n_contrib, const float* __restrict__ aa_cov, Staged rec,
+                unsigned long long* __restrict__ stats)
 {
-    __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
+    __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS];
     __shared__ float4 sD[SOFT ? CTA_THREADS : 1];
     int tile;
     const PixelMap pm = pixel_of(c, tile);
@@ -221,19 +248,32 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     int last = 0;
     uint32_t visited = 0, blended = 0;
     bool done = !inside;
-    const int2 r = tile_range[tile];
+    const int2 r = rec.A ? clamp_range(tile_range[tile], rec.cap) : tile_range[tile];
     for (int b = r.x; b < r.y; b += CTA_THREADS) {
         // this barrier also keeps the staging below from overwriting records that
         // another warp of the CTA is still reading from the previous batch
         if (__syncthreads_count(done) == CTA_THREADS) break;
         const int n = min(CTA_THREADS, r.y - b);
         if ((int)threadIdx.x < n) {
-            const int64_t g = gids[b + threadIdx.x];
-            if (g >= 0 && g < N) {
-                stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
-                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, sp, sC[threadIdx.x].y);
-            } else {  // an id outside [0, N): an entry that draws nothing
-                stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
+            int g = gids[b + threadIdx.x];
+            if (g < 0 || g >= N) g = -1;  // an id outside [0, N): an entry that draws nothing
+            float4 A, B, C;
+            stage_rec(splats, g, A, B, C);
+            sA[threadIdx.x] = A;
+            sB[threadIdx.x] = B;
+            sC[threadIdx.x] = C;
+            float4 Dm = make_float4(0.f, 0.f, 0.f, INFINITY);
+            if (SOFT && g >= 0) Dm = stage_depth_model(depth_model, g, sp, C.y);
+            if (SOFT) sD[threadIdx.x] = Dm;
+            if (rec.A) {
+                // the staged records of every batch this CTA takes, in list order, for
+                // the backward pass (both half-tile CTAs write the batches they take;
+                // where they overlap they write the same values)
+                const int64_t e = b + threadIdx.x;
+                rec.A[e] = A;
+                rec.B[e] = B;
+                rec.C[e] = C;
+                if (SOFT) rec.D[e] = Dm;
             }
         }
         __syncthreads();
@@ -243,7 +283,7 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             if (__all_sync(0xffffffffu, done)) break;
             const int kk = m * 32 + (threadIdx.x & 31);
             uint32_t mask =
-                __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0) &&
+                __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0) &&
                                                !(SOFT && sD[kk].w > Dw));
             while (mask) {
                 // two hits at a time: both evaluated (independent) before the
@@ -412,11 +452,150 @@ __device__ __forceinline__ void flush_grad_soft(float* __restrict__ v_splats, fl
               make_float4(-acc[11], -acc[12], -acc[13] * Dm.z * softness, 0.0f));
 }
 
-// Ten CTAs of 128 threads per SM (at most 51 registers a thread): the kernel
-// is bound by instruction latency, and resident warps hide it.  The soft split
-// carries four more terms per entry: eight CTAs (64 registers).
-template <bool STATS, bool SOFT>
-__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : 10)
+// ------------------------------------------- tensor-core reduction ---------
+//
+// Hard split: the warp's sums over its 32 pixels of the gradient terms of a
+// group of eight entries are a small contraction, (8 entries x 32 pixels) x
+// (32 pixels x 6 moments) for ds = dL/d sigma and (8 x 32) x (32 x 4 upstream
+// gradient channels) for w = alpha T, done with warp-level tf32 MMAs
+// (m16n8k8).  With dx = u + i, dy = v + j (u, v the entry's offset at the
+// block's first pixel, i, j the pixel's place in the 8 x 4 block) the six
+// pixel moments 1, i, j, i^2, i j, j^2 of ds give every ds term.  Each fp32
+// value x enters as two tf32 values, hi = tf32(x) and lo = tf32(x - hi)
+// (rows g and g + 8 of the A operand), which keeps about 22 bits; the moments
+// are small integers, exact in tf32, and the upstream gradient is split the
+// same way (columns 0..3 hi, 4..7 lo).
+
+constexpr int RGROUP = 8;  // entries per tensor-core group
+constexpr int RPAD = 36;   // row stride of the per-warp staging (conflict-free fragment loads)
+
+struct RedSmem {
+    float ds[RGROUP][RPAD];  // [group slot][pixel] dL/d sigma
+    float w[RGROUP][RPAD];   // [group slot][pixel] alpha T_front
+    float2 gf[4][32];        // B fragments (b0, b1) of the upstream gradient, per 8-pixel k-block
+};
+
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One 8-pixel k-block of the A operand: rows g (hi) and g + 8 (lo) of group
+// slot g at pixels kb * 8 + c and kb * 8 + c + 4.
+__device__ __forceinline__ void a_frag(const float (&m)[RGROUP][RPAD], int g, int p, uint32_t (&a)[4])
+{
+    const float x0 = m[g][p], x1 = m[g][p + 4];
+    a[0] = to_tf32(x0);
+    a[1] = to_tf32(x0 - __uint_as_float(a[0]));
+    a[2] = to_tf32(x1);
+    a[3] = to_tf32(x1 - __uint_as_float(a[2]));
+}
+
+// pixel moment n (1, i, j, i^2, i j, j^2, 0, 0) of the pixel at (i, j)
+__device__ __forceinline__ float moment(int n, int i, int j)
+{
+    return n == 0 ? 1.0f : n == 1 ? (float)i : n == 2 ? (float)j : n == 3 ? (float)(i * i)
+         : n == 4 ? (float)(i * j) : n == 5 ? (float)(j * j) : 0.0f;
+}
+
+// ---------------------------------------------- bulk-copy staging ---------
+//
+// The backward pass takes each batch of a tile's staged records (written by
+// the forward pass in list order) with bulk copies (cp.async.bulk, the TMA
+// engine's linear mode) into shared memory: one thread issues the copies of a
+// batch, an mbarrier counts their bytes, and the next batch's copies are in
+// flight while the CTA works on the current one (two buffers).  The source is
+// always this GPU's own record buffer.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of the given parity, at most about GM_COPY_WAIT_NS
+// nanoseconds; false when it gave up.
+constexpr uint64_t COPY_WAIT_NS = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > COPY_WAIT_NS) return false;
+    }
+}
+
+// n consecutive 16-byte elements from global src to shared dst, counted on bar
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// generic-proxy accesses of shared memory before this point are ordered before
+// the bulk copies issued after it
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+}  // namespace
+
+// Set when a bulk copy's wait gave up (gm_get_copy_status).
+__device__ uint32_t g_copy_status = 0;
+
+namespace {
+
+// Eight CTAs of 128 threads per SM (64 registers a thread), seven with the
+// bulk-copied records' second buffer (the shared memory of the hard split's
+// tensor-core staging bounds it): the kernel is bound by instruction issue,
+// and resident warps hide the latencies.  BULK: the records come from the
+// forward pass's staged records by bulk copies into two buffers; otherwise
+// each thread gathers and stages one record per batch.
+template <bool STATS, bool SOFT, bool BULK>
+__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : (BULK ? 7 : 8))
 k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
                 const int32_t* __restrict__ gids, const float4* __restrict__ splats,
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
@@ -424,14 +603,21 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
                 const float* __restrict__ g_rgb, const float* __restrict__ g_depth, const float* __restrict__ g_alpha,
                 float* __restrict__ v_splats, float* __restrict__ v_depth_model, float* __restrict__ v_mesh_depth,
-                AaLayer aa, unsigned long long* __restrict__ stats)
+                AaLayer aa, Staged rec, unsigned long long* __restrict__ stats)
 {
     constexpr int NACC = SOFT ? NGRAD + 4 : NGRAD;
-    __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS], sH[CTA_THREADS];
-    __shared__ float4 sD[SOFT ? CTA_THREADS : 1];
-    __shared__ int sG[CTA_THREADS];
+    constexpr int NBUF = BULK ? 2 : 1;
+    __shared__ __align__(16) float4 sA_buf[NBUF][CTA_THREADS];
+    __shared__ __align__(16) float4 sB_buf[NBUF][CTA_THREADS];
+    __shared__ __align__(16) float4 sC_buf[NBUF][CTA_THREADS];
+    __shared__ __align__(16) float4 sD_buf[SOFT ? NBUF : 1][SOFT ? CTA_THREADS : 1];
     __shared__ float sAcc[CTA_THREADS][NACC + 1];
+    __shared__ __align__(8) uint64_t s_bar[NBUF];
     __shared__ int s_max_last;
+    // hard split: the tensor-core reduction's staging per warp, and the moments'
+    // B fragments (b0, b1) per k-block and lane, shared by the warps
+    __shared__ __align__(16) RedSmem sRed[SOFT ? 1 : CTA_WARPS];
+    __shared__ __align__(16) float2 sMf[SOFT ? 1 : 4][32];
     int tile;
     const PixelMap pm = pixel_of(c, tile);
     const int lane = threadIdx.x & 31;
@@ -477,43 +663,113 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     int warp_last = last;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) warp_last = max(warp_last, __shfl_xor_sync(0xffffffffu, warp_last, o));
-    if (threadIdx.x == 0) s_max_last = 0;
+    if constexpr (!SOFT) {
+        // B fragments: moments of pixel (i, j) = (c (+4), kb) for term g; the upstream
+        // gradient's channel g & 3 (hi for g < 4, lo for g >= 4) of pixel kb * 8 + c (+4)
+        const int g = lane >> 2, c = lane & 3, kb = threadIdx.x >> 5;
+        sMf[kb][lane] = make_float2(moment(g, c, kb), moment(g, c + 4, kb));
+        RedSmem& R = sRed[threadIdx.x >> 5];
+        float* gtmp = &R.ds[0][0];  // 128 floats of scratch before the first group
+        gtmp[4 * lane] = gr;
+        gtmp[4 * lane + 1] = gg;
+        gtmp[4 * lane + 2] = gb;
+        gtmp[4 * lane + 3] = gz;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float b[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float x = gtmp[4 * (q * 8 + c + 4 * h) + (g & 3)];
+                const uint32_t hi = to_tf32(x);
+                b[h] = g < 4 ? __uint_as_float(hi) : __uint_as_float(to_tf32(x - __uint_as_float(hi)));
+            }
+            R.gf[q][lane] = make_float2(b[0], b[1]);
+        }
+        __syncwarp();
+    }
+    if (threadIdx.x == 0) {
+        s_max_last = 0;
+        if (BULK) {
+#pragma unroll
+            for (int q = 0; q < NBUF; ++q) mbar_init(&s_bar[q], 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    }
     __syncthreads();
     if (lane == 0 && warp_last > 0) atomicMax(&s_max_last, warp_last);
     __syncthreads();
-    const int2 r = tile_range[tile];
-    const int end = r.x + s_max_last;
+    const int2 r = BULK ? clamp_range(tile_range[tile], rec.cap) : tile_range[tile];
+    const int end = BULK ? min(r.x + s_max_last, r.y) : r.x + s_max_last;
+    const int n_batches = (end - r.x + CTA_THREADS - 1) / CTA_THREADS;
     const bool soft = SOFT && cov;
     const float Dw = SOFT ? warp_hide_depth(inside, cov, D) : INFINITY;
     uint32_t visited = 0, contributed = 0;
+    // batch j holds list positions [max(r.x, end - 128 (j + 1)), end - 128 j)
+    auto issue = [&](int j) {
+        const int hi = end - CTA_THREADS * j, lo = max(r.x, hi - CTA_THREADS);
+        const uint32_t bytes = (uint32_t)(hi - lo) * 16u;
+        const int q = j % NBUF;
+        mbar_arrive_expect_tx(&s_bar[q], bytes * (SOFT ? 4u : 3u));
+        bulk_copy(sA_buf[q], rec.A + lo, bytes, &s_bar[q]);
+        bulk_copy(sB_buf[q], rec.B + lo, bytes, &s_bar[q]);
+        bulk_copy(sC_buf[q], rec.C + lo, bytes, &s_bar[q]);
+        if (SOFT) bulk_copy(sD_buf[SOFT ? q : 0], rec.D + lo, bytes, &s_bar[q]);
+    };
+    if (BULK && threadIdx.x == 0 && n_batches > 0) issue(0);
     int n_prev = 0;
-    for (int b_end = end;; b_end -= CTA_THREADS) {
-        // the previous batch's gradients go out and the next batch comes in, each
-        // thread on its own slot, so one barrier covers both
-        if ((int)threadIdx.x < n_prev && sG[threadIdx.x] >= 0) {
-            if (SOFT)
-                flush_grad_soft(v_splats, v_depth_model, sG[threadIdx.x], sAcc[threadIdx.x], sA[threadIdx.x],
-                                sB[threadIdx.x], sD[threadIdx.x], sp.softness);
-            else
-                flush_grad(v_splats, sG[threadIdx.x], sAcc[threadIdx.x], sA[threadIdx.x], sB[threadIdx.x]);
+    for (int j = 0;; ++j) {
+        const int cur = j % NBUF, prev = (j + NBUF - 1) % NBUF;
+        // the previous batch's gradients go out (each thread its own slot) and, for
+        // the gathering form, the next batch comes in on the same slot
+        if ((int)threadIdx.x < n_prev) {
+            const int g = rec_id(sC_buf[prev][threadIdx.x]);
+            if (g >= 0) {
+                if (SOFT)
+                    flush_grad_soft(v_splats, v_depth_model, g, sAcc[threadIdx.x], sA_buf[prev][threadIdx.x],
+                                    sB_buf[prev][threadIdx.x], sD_buf[SOFT ? prev : 0][threadIdx.x], sp.softness);
+                else
+                    flush_grad(v_splats, g, sAcc[threadIdx.x], sA_buf[prev][threadIdx.x], sB_buf[prev][threadIdx.x]);
+            }
         }
-        if (b_end <= r.x) break;
+        if (j >= n_batches) break;
+        const int b_end = end - CTA_THREADS * j;
         const int b0 = max(r.x, b_end - CTA_THREADS);
         const int n = b_end - b0;
         if ((int)threadIdx.x < n) {
-            int g = gids[b0 + threadIdx.x];
-            if (g < 0 || g >= N) g = -1;  // an entry that draws nothing and gets no gradient
-            sG[threadIdx.x] = g;
-            if (g >= 0) {
-                stage(splats, g, sA[threadIdx.x], sB[threadIdx.x], sC[threadIdx.x], sH[threadIdx.x]);
-                if (SOFT) sD[threadIdx.x] = stage_depth_model(depth_model, g, sp, sC[threadIdx.x].y);
-            } else {
-                stage_empty(sC[threadIdx.x], sH[threadIdx.x]);
+            if (!BULK) {
+                int g = gids[b0 + threadIdx.x];
+                if (g < 0 || g >= N) g = -1;  // an entry that draws nothing and gets no gradient
+                float4 A, B, C;
+                stage_rec(splats, g, A, B, C);
+                sA_buf[0][threadIdx.x] = A;
+                sB_buf[0][threadIdx.x] = B;
+                sC_buf[0][threadIdx.x] = C;
+                if (SOFT && g >= 0) sD_buf[0][threadIdx.x] = stage_depth_model(depth_model, g, sp, C.y);
             }
 #pragma unroll
             for (int q = 0; q < NACC; ++q) sAcc[threadIdx.x][q] = 0.0f;
         }
         __syncthreads();
+        if (BULK) {
+            if (threadIdx.x == 0 && j + 1 < n_batches) {
+                // the other buffer was last read by the flush above: free after the barrier
+                fence_proxy_async_smem();
+                issue(j + 1);
+            }
+            const bool ok = __syncthreads_and(mbar_wait(&s_bar[cur], (uint32_t)(j / NBUF) & 1u));
+            if (!ok) {
+                // a copy did not arrive: report, let the copies in flight land, stop
+                if (threadIdx.x == 0) atomicOr(&g_copy_status, 1u);
+                mbar_wait(&s_bar[cur], (uint32_t)(j / NBUF) & 1u);
+                if (j + 1 < n_batches) mbar_wait(&s_bar[(j + 1) % NBUF], (uint32_t)((j + 1) / NBUF) & 1u);
+                return;
+            }
+        }
+        const float4* __restrict__ sA = sA_buf[cur];
+        const float4* __restrict__ sB = sB_buf[cur];
+        const float4* __restrict__ sC = sC_buf[cur];
+        const float4* __restrict__ sD = sD_buf[SOFT ? cur : 0];
         // this warp only needs the entries in front of its last composited one, and of
         // those only the ones that can reach its pixels (a ballot per 32 entries);
         // they are taken four at a time from the back
@@ -521,8 +777,114 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         for (int m = k_top >> 5; m >= 0; --m) {
             const int kk = m * 32 + lane;
             uint32_t mask =
-                __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sH[kk], pm.x0, pm.y0) &&
+                __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0) &&
                                                !(SOFT && sD[kk].w > Dw));
+            if constexpr (!SOFT) {
+                RedSmem& R = sRed[threadIdx.x >> 5];
+                while (mask) {
+                    int kj[RGROUP];
+#pragma unroll
+                    for (int jj = 0; jj < RGROUP; ++jj) {
+                        if (mask) {
+                            const int bit = 31 - __clz(mask);
+                            kj[jj] = m * 32 + bit;
+                            mask &= ~(1u << bit);
+                        } else {
+                            kj[jj] = -1;
+                        }
+                    }
+                    // per entry, back to front: w = alpha T_front and ds = dL/d sigma at
+                    // this lane's pixel, staged for the contraction
+                    bool any = false;
+#pragma unroll
+                    for (int jj = 0; jj < RGROUP; ++jj) {
+                        float w = 0.0f, ds = 0.0f;
+                        const int k = kj[jj];
+                        if (k >= 0 && inside && b0 - r.x + k < last) {
+                            const float4 C3 = sC[k];
+                            if (C3.y < D) {
+                                if (STATS) ++visited;
+                                const float4 A = sA[k], B = sB[k];
+                                const Eval e = eval_splat(A, B, px, py);
+                                if (!e.skip) {
+                                    if (STATS) ++contributed;
+                                    any = true;
+                                    const float a = e.alpha;
+                                    const float rom = __fdividef(1.0f, 1.0f - a);
+                                    const float Tp = T * rom;  // transmittance in front of it
+                                    w = a * Tp;
+                                    const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
+                                    const float dLda = Tp * front + (aterm - behind) * rom;
+                                    behind = fmaf(w, front, behind);
+                                    T = Tp;
+                                    // alpha clamped at 0.99 has no opacity / sigma gradient;
+                                    // elsewhere d alpha / d sigma = -alpha
+                                    if (!e.clamped) ds = -dLda * a;
+                                }
+                            }
+                        }
+                        R.ds[jj][lane] = ds;
+                        R.w[jj][lane] = w;
+                    }
+                    if (__any_sync(FULL, any)) {
+                        __syncwarp();
+                        const int g = lane >> 2, c = lane & 3;
+                        float dm[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t a[4];
+                            const float2 bm = sMf[q][lane], bg = R.gf[q][lane];
+                            a_frag(R.ds, g, q * 8 + c, a);
+                            mma_tf32(dm, a[0], a[1], a[2], a[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
+                            a_frag(R.w, g, q * 8 + c, a);
+                            mma_tf32(dc, a[0], a[1], a[2], a[3], __float_as_uint(bg.x), __float_as_uint(bg.y));
+                        }
+                        // this lane: group slot g, terms 2c and 2c + 1 (hi rows + lo rows)
+                        const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
+                        float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
+                        e0 += __shfl_xor_sync(FULL, e0, 2);  // the upstream gradient's hi + lo columns
+                        e1 += __shfl_xor_sync(FULL, e1, 2);
+                        int k = kj[0];
+#pragma unroll
+                        for (int jj = 1; jj < RGROUP; ++jj) k = g == jj ? kj[jj] : k;
+                        if (k >= 0) {
+                            // (t0, t1) = (S0, Si) for c = 0, (Sj, Sii) for 1, (Sij, Sjj) for 2
+                            // of S_n = sum ds m_n; with dx = u + i, dy = v + j:
+                            //   sum ds dx = u S0 + Si, sum ds dy = v S0 + Sj,
+                            //   sum ds dx^2 / 2 = u (u S0 / 2 + Si) + Sii / 2,
+                            //   sum ds dx dy = v (u S0 + Si) + u Sj + Sij,
+                            //   sum ds dy^2 / 2 = v^2 S0 / 2 + v Sj + Sjj / 2, sum ds = S0;
+                            // each lane adds its terms' parts, no two lanes of an instruction
+                            // on one slot of one entry
+                            const float2 mean = *reinterpret_cast<const float2*>(&sA[k]);
+                            const float u = pm.x0 - mean.x, v = pm.y0 - mean.y;
+                            float* acc = sAcc[k];
+                            if (c == 0) {
+                                const float p = fmaf(u, t0, t1);
+                                atomicAdd(acc + 0, p);
+                                atomicAdd(acc + 1, v * t0);
+                                atomicAdd(acc + 2, u * fmaf(0.5f * u, t0, t1));
+                                atomicAdd(acc + 3, v * p);
+                                atomicAdd(acc + 4, 0.5f * v * v * t0);
+                                atomicAdd(acc + 5, t0);
+                                atomicAdd(acc + 6, e0);
+                                atomicAdd(acc + 7, e1);
+                            } else if (c == 1) {
+                                atomicAdd(acc + 1, t0);
+                                atomicAdd(acc + 2, 0.5f * t1);
+                                atomicAdd(acc + 3, u * t0);
+                                atomicAdd(acc + 4, v * t0);
+                                atomicAdd(acc + 8, e0);
+                                atomicAdd(acc + 9, e1);
+                            } else if (c == 2) {
+                                atomicAdd(acc + 3, t0);
+                                atomicAdd(acc + 4, 0.5f * t1);
+                            }
+                        }
+                    }
+                    __syncwarp();  // the staging is rewritten by the next group
+                }
+            } else
             while (mask) {
                 int kj[GROUP];
 #pragma unroll
@@ -759,8 +1121,7 @@ __device__ __forceinline__ void stage_back(const int32_t* __restrict__ gids, con
     if (g < 0 || g >= N) g = -1;
     st.g[lane] = g;
     if (g >= 0) {
-        float4 Hh;
-        stage(splats, g, st.A[lane], st.B[lane], st.C[lane], Hh);
+        stage_rec(splats, g, st.A[lane], st.B[lane], st.C[lane]);
         if (SOFT) st.Dm[lane] = stage_depth_model(depth_model, g, sp, st.C[lane].y);
     }
     __syncwarp();
@@ -996,20 +1357,47 @@ k_composite_back_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__
 
 }  // namespace
 
+static Staged staged_of(float* staged, int cap)
+{
+    Staged r{nullptr, nullptr, nullptr, nullptr, 0};
+    if (!staged || cap <= 0) return r;
+    float4* b = reinterpret_cast<float4*>(staged);
+    r.A = b;
+    r.B = b + cap;
+    r.C = b + 2 * (int64_t)cap;
+    r.D = b + 3 * (int64_t)cap;
+    r.cap = cap;
+    return r;
+}
+
+size_t staged_bytes(int cap, bool soft) { return (size_t)(cap > 0 ? cap : 0) * (soft ? 64 : 48); }
+
+cudaError_t copy_status(uint32_t* flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_copy_status, sizeof(uint32_t));
+    if (e == cudaSuccess && clear) {
+        const uint32_t z = 0;
+        e = cudaMemcpyToSymbol(g_copy_status, &z, sizeof(z));
+    }
+    return e;
+}
+
 cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
-                          float* out_alpha, float* T_final, int32_t* n_contrib, const AaLayer& aa, uint64_t* stats,
-                          cudaStream_t s)
+                          float* out_alpha, float* T_final, int32_t* n_contrib, const AaLayer& aa, float* staged,
+                          int staged_cap, uint64_t* stats, cudaStream_t s)
 {
     const bool soft = softness > 0.0f;
     auto kern = soft ? (stats ? k_composite_fwd<true, true> : k_composite_fwd<false, true>)
                      : (stats ? k_composite_fwd<true, false> : k_composite_fwd<false, false>);
+    const Staged rec = staged_of(staged, staged_cap);
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
         c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
         gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
-        face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, aa.cov, reinterpret_cast<unsigned long long*>(stats));
+        face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, aa.cov, rec,
+        reinterpret_cast<unsigned long long*>(stats));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !aa.cov) return e;
     const int64_t P = (int64_t)c.W * c.H;
@@ -1029,16 +1417,20 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
                           const float* mesh_rgb, const int32_t* face_id, const float* T_final,
                           const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
                           float* v_splats, float* v_depth_model, float* v_mesh_depth, const AaLayer& aa,
-                          uint64_t* stats, cudaStream_t s)
+                          const float* staged, int staged_cap, uint64_t* stats, cudaStream_t s)
 {
     const bool soft = softness > 0.0f;
-    auto kern = soft ? (stats ? k_composite_bwd<true, true> : k_composite_bwd<false, true>)
-                     : (stats ? k_composite_bwd<true, false> : k_composite_bwd<false, false>);
+    const Staged rec = staged_of(const_cast<float*>(staged), staged_cap);
+    const bool bulk = rec.A != nullptr;
+    auto kern = soft ? (stats ? (bulk ? k_composite_bwd<true, true, true> : k_composite_bwd<true, true, false>)
+                              : (bulk ? k_composite_bwd<false, true, true> : k_composite_bwd<false, true, false>))
+                     : (stats ? (bulk ? k_composite_bwd<true, false, true> : k_composite_bwd<true, false, false>)
+                              : (bulk ? k_composite_bwd<false, false, true> : k_composite_bwd<false, false, false>));
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
         c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
         gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
-        face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth, aa,
+        face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth, aa, rec,
         reinterpret_cast<unsigned long long*>(stats));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !aa.cov) return e;

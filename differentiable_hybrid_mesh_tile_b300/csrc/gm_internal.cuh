@@ -262,13 +262,17 @@ cudaError_t interp_bwd(const Cam& c, const float* V, int nV, const int32_t* F, i
 cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, float* out_rgb, float* out_depth,
-                          float* out_alpha, float* T_final, int32_t* n_contrib, const AaLayer& aa, uint64_t* stats,
-                          cudaStream_t s);
+                          float* out_alpha, float* T_final, int32_t* n_contrib, const AaLayer& aa, float* staged,
+                          int staged_cap, uint64_t* stats, cudaStream_t s);
 cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness, int split, const int32_t* tile_range,
                           const int32_t* gids, const float* splats, const float* depth_model, const float* mesh_depth,
                           const float* mesh_rgb, const int32_t* face_id, const float* T_final,
                           const int32_t* n_contrib, const float* g_rgb, const float* g_depth, const float* g_alpha,
                           float* v_splats, float* v_depth_model, float* v_mesh_depth, const AaLayer& aa,
-                          uint64_t* stats, cudaStream_t s);
+                          const float* staged, int staged_cap, uint64_t* stats, cudaStream_t s);
+// bytes of a staged-record buffer of cap list positions (48 each, 64 with the soft split)
+size_t staged_bytes(int cap, bool soft);
+// the bulk-copy wait status (bit 0: a wait gave up), optionally cleared
+cudaError_t copy_status(uint32_t* flags, bool clear);
 
 }  // namespace gm

@@ -112,6 +112,33 @@ typedef struct gm_aa_layer {
     float* v_rgb;      /* [H][W][3] backward out: dL/dM */
 } gm_aa_layer;
 
+/* Staged records of the Gaussian tile lists (Hybrid rendering, the
+ * compositing kernel): one record per list position, the compositing's form
+ * of that position's splat (mean, conic pre-scaled for exp2, opacity, colour,
+ * depth, the Gaussian's id and the exponent bound of alpha >= 1/255; with the
+ * soft split also its depth model).  gm_composite_hybrid_fwd writes the
+ * records of every batch it stages; gm_composite_hybrid_bwd then copies each
+ * batch of a tile's list into shared memory with bulk copies instead of
+ * gathering the splats through the ids.  recs: device memory of
+ * gm_staged_bytes(cap, opts->softness) bytes, 16-byte aligned, owned by the
+ * caller, contents private to the library; cap >= the number of entries the
+ * tile ranges address.  The backward call must get the records its forward
+ * call wrote, for the same tile lists, splats and options. */
+typedef struct gm_staged {
+    float* recs;
+    int32_t cap;
+} gm_staged;
+
+/* bytes of a staged-record buffer for cap list positions: 48 per position,
+ * 64 with the soft split (softness > 0) */
+size_t gm_staged_bytes(int32_t cap, float softness);
+
+/* gm_get_copy_status -- the bulk copies of gm_composite_hybrid_bwd wait for
+ * their data at most about one second; a wait that gives up stops that CTA
+ * (its gradients are then incomplete) and sets bit 0 of a device status word.
+ * *flags (host) receives the word; clear != 0 resets it.  Synchronous. */
+int gm_get_copy_status(uint32_t* flags, int32_t clear);
+
 /*
  * Projected-Gaussian record ("splat"), GM_SPLAT_STRIDE floats, 16-byte aligned:
  *   [0] mean2d x  [1] mean2d y      (pixels)
@@ -390,6 +417,9 @@ int gm_bin_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const
  *   stats: NULL, or a device uint64[2] incremented by the number of
  *   (pixel, Gaussian) pairs evaluated [0] and composited [1] (profiling
  *   counts; the caller zeroes them).
+ *   staged: NULL, or the staged-record buffer (gm_staged) this call fills
+ *   for the backward pass; positions past staged->cap are neither written
+ *   nor composited.
  * Soft split (opts->softness > 0; Hybrid rendering, the split at the mesh
  * surface): at a covered pixel there is no hard test; each Gaussian's part
  * in front of the mesh, f = Phi((D - z*(p)) / (sigma_z softness)) with
@@ -418,8 +448,8 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const int32_t* tile_range, const int32_t* gids, const float* splats,
                             const float* depth_model, const float* mesh_depth, const float* mesh_rgb,
                             const int32_t* face_id, float* out_rgb, float* out_depth, float* out_alpha,
-                            float* T_final, int32_t* n_contrib, const gm_aa_layer* aa, uint64_t* stats,
-                            void* stream);
+                            float* T_final, int32_t* n_contrib, const gm_aa_layer* aa, const gm_staged* staged,
+                            uint64_t* stats, void* stream);
 
 /* ------------------------------------------------------------------------
  * gm_composite_hybrid_bwd -- Hybrid rendering ("everything is
@@ -437,6 +467,10 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  *   (with nV = nF = 0) to skip the mesh gradients.
  *   stats: NULL, or a device uint64[2] incremented by the number of (pixel,
  *   Gaussian) pairs evaluated [0] and given gradient terms [1] (profiling).
+ *   staged: NULL (each batch of a tile's list is gathered through gids), or
+ *   the buffer the forward call filled (gm_staged): each batch then arrives
+ *   by bulk copies, the next one in flight while the current one is worked
+ *   on.  The Gaussian part reads it; the mesh part does not.
  *   Soft split (opts->softness > 0): depth_model as for the forward pass;
  *   v_depth_model [N][4] f32 (+=, 16-byte aligned, required with v_splats):
  *   dL/d(g_u, g_v, sigma_z, -); v_mesh_depth [H][W] f32 (required with the
@@ -457,7 +491,8 @@ int gm_composite_hybrid_bwd(const gm_camera* cam, const gm_opts* opts, int32_t N
                             const float* g_rgb, const float* g_depth, const float* g_alpha, float* v_splats,
                             float* v_depth_model, float* v_mesh_depth, const float* V, int32_t nV,
                             const int32_t* F, int32_t nF, const float* vcol, float* v_verts,
-                            float* v_vcol, const gm_aa_layer* aa, uint64_t* stats, void* stream);
+                            float* v_vcol, const gm_aa_layer* aa, const gm_staged* staged, uint64_t* stats,
+                            void* stream);
 
 /* ------------------------------------------------------------------------
  * Batched views (several cameras of one scene, e.g. the views of a training

@@ -83,39 +83,47 @@ def test_null_and_size_checks(lib):
     assert st == gm.GM_ERR_INVALID_ARG
     # incomplete mesh-gradient arguments
     st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 13), None, None,
-                                     None, 3, None, 1, None, C.c_void_p(256), None, None, None, None)
+                                     None, 3, None, 1, None, C.c_void_p(256), None, None, None, None, None)
     assert st == gm.GM_ERR_INVALID_ARG
     # soft split: negative softness; Gaussian gradients without the depth model or its gradient;
     # mesh gradients without dL/d mesh depth
     neg = gm.make_opts(softness=-1.0)
-    st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(neg), 4, *([C.c_void_p(256)] * 12), None, None, None)
+    st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(neg), 4, *([C.c_void_p(256)] * 12), None, None, None,
+                                     None)
     assert st == gm.GM_ERR_INVALID_ARG and b"softness" in lib.gm_last_error()
     soft = gm.make_opts(softness=1.0)
     st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(soft), 4, C.c_void_p(256), C.c_void_p(256),
-                                     C.c_void_p(256), None, *([C.c_void_p(256)] * 8), None, None, None)
+                                     C.c_void_p(256), None, *([C.c_void_p(256)] * 8), None, None, None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"depth_model" in lib.gm_last_error()
     st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(soft), 4, *([C.c_void_p(256)] * 13), None, None,
-                                     None, 0, None, 0, None, None, None, None, None, None)
+                                     None, 0, None, 0, None, None, None, None, None, None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"depth_model" in lib.gm_last_error()
     st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(soft), 4, *([C.c_void_p(256)] * 12), None, None,
                                      None, C.c_void_p(256), 3, C.c_void_p(256), 1, C.c_void_p(256),
-                                     C.c_void_p(256), C.c_void_p(256), None, None, None)
+                                     C.c_void_p(256), C.c_void_p(256), None, None, None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"v_mesh_depth" in lib.gm_last_error()
     bad_split = gm.make_opts(softness=1.0, soft_split=2)
     st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(bad_split), 4, *([C.c_void_p(256)] * 12), None, None,
-                                     None)
+                                     None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"soft_split" in lib.gm_last_error()
     # antialiased layer: misaligned back buffer; mesh arguments given with the layer
     aa = gm.gm_aa_layer()
     aa.cov, aa.back, aa.T_back, aa.n_back, aa.v_cov, aa.v_rgb = 256, 264, 256, 256, 256, 256
     st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 12), C.byref(aa), None,
-                                     None)
+                                     None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"back" in lib.gm_last_error()
     aa.back = 256
     st = lib.gm_composite_hybrid_bwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 16), 3,
                                      C.c_void_p(256), 1, C.c_void_p(256), C.c_void_p(256), C.c_void_p(256),
-                                     C.byref(aa), None, None)
+                                     C.byref(aa), None, None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"gm_antialias_bwd" in lib.gm_last_error()
+    # staged records: misaligned buffer
+    stg = gm.gm_staged()
+    stg.recs, stg.cap = 264, 100
+    st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 12), None,
+                                     C.byref(stg), None, None)
+    assert st == gm.GM_ERR_INVALID_ARG and b"staged" in lib.gm_last_error()
+    assert gm.gm_staged_bytes(1000, 0.0) == 48000 and gm.gm_staged_bytes(1000, 1.0) == 64000
     # edge adjacency: workspace too small; antialiasing without adjacency
     st = lib.gm_mesh_edges(C.c_void_p(256), 10, 12, C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), 16, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"workspace" in lib.gm_last_error()

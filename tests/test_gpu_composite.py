@@ -238,3 +238,40 @@ def test_degenerate_scenes(what, orc):
     grads = scenes.upstream_grads(2, cam.width, cam.height)
     b = H.run_composite_bwd(cam, s.bg, f, grads, len(r["radii"]), s.mesh, mesh_grads=len(s.mesh.faces) > 0)
     assert np.all(np.isfinite(b["v_splats"]))
+
+
+@pytest.mark.parametrize("softness,antialias", [(0.0, False), (1.0, False), (0.0, True)],
+                         ids=["hard", "soft", "antialias"])
+def test_backward_from_staged_records_matches_gathered(softness, antialias):
+    """The backward pass fed by the forward's staged records (bulk copies into
+    shared memory, two batches in flight) gives the gradients of the backward
+    that gathers the records itself, up to the order of float atomic sums,
+    and the forward's image is the same bit for bit either way.  The 512 px
+    sphere has tiles of several 128-entry batches; the 101 x 77 frame has
+    ragged tiles and short lists."""
+    H.need_gpu()
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    sph = scenes.sphere512()
+    ragged = scenes.Scene(sph.name, [scenes.look_at((0.3, 0.5, 2.6), (0, 0, 0), 101, 77, 90, 95, 47.3, 40.1)],
+                          sph.mesh, sph.gaussians, sph.bg)
+    for s in (sph, ragged):
+        cam = s.camera
+        out = []
+        for staged in (True, False):
+            r = gm.HybridRenderer(cam, bg=s.bg, softness=softness, antialias=antialias, staged=staged)
+            r.upload(s.mesh, s.gaussians)
+            r.forward(sync=True)
+            g = [torch.as_tensor(x).cuda() for x in scenes.upstream_grads(8, cam.width, cam.height)]
+            v = r.backward(*g)
+            torch.cuda.synchronize()
+            out.append(([t.clone() for t in (r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib)],
+                        [t.clone() for t in v]))
+            if staged:
+                n_batches = (torch.diff(r.g_range, dim=1) + 127) // 128
+                print("%dx%d: longest tile list %d batches" % (cam.width, cam.height, int(n_batches.max())))
+        for a, b in zip(out[0][0], out[1][0]):
+            assert torch.equal(a, b)
+        for a, b in zip(out[0][1], out[1][1]):
+            torch.testing.assert_close(a, b, rtol=1e-4, atol=1e-6 * max(1.0, float(b.abs().max())))
+    assert gm.gm_get_copy_status(clear=True) == 0

