@@ -275,3 +275,32 @@ def test_backward_from_staged_records_matches_gathered(softness, antialias):
         for a, b in zip(out[0][1], out[1][1]):
             torch.testing.assert_close(a, b, rtol=1e-4, atol=1e-6 * max(1.0, float(b.abs().max())))
     assert gm.gm_get_copy_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("antialias", [False, True], ids=["hard", "antialias"])
+def test_whole_tile_forward_matches_half_tiles(antialias, monkeypatch):
+    """The hard split's forward pass over whole tiles (two pixels a lane, paired
+    fp32 arithmetic) writes the image, T_final, n_contrib and the staged
+    records of the half-tile form (one pixel a lane, GM_FWD_HALF_TILES) bit
+    for bit, on the 512 px sphere and on a ragged 101 x 77 frame."""
+    H.need_gpu()
+    import torch
+    import differentiable_hybrid_mesh_tile_b300 as gm
+    sph = scenes.sphere512()
+    ragged = scenes.Scene(sph.name, [scenes.look_at((0.3, 0.5, 2.6), (0, 0, 0), 101, 77, 90, 95, 47.3, 40.1)],
+                          sph.mesh, sph.gaussians, sph.bg)
+    for s in (sph, ragged):
+        out = []
+        for half in (False, True):
+            if half:
+                monkeypatch.setenv("GM_FWD_HALF_TILES", "1")
+            else:
+                monkeypatch.delenv("GM_FWD_HALF_TILES", raising=False)
+            r = gm.HybridRenderer(s.camera, bg=s.bg, antialias=antialias)
+            r.upload(s.mesh, s.gaussians)
+            r.forward(sync=True)
+            torch.cuda.synchronize()
+            out.append([t.clone() for t in (r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib)])
+        monkeypatch.delenv("GM_FWD_HALF_TILES", raising=False)
+        for a, b in zip(*out):
+            assert torch.equal(a, b)
