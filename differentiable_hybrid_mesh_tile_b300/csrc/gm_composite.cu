@@ -376,193 +376,6 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     }
 }
 
-// --------------------------------------------- hard split, whole tiles -----
-//
-// The hard split's forward pass with one CTA per 16 x 16 tile: each warp takes
-// an 8 x 8 block, two pixels a lane, (i, j) and (i, j + 4).  The two pixels
-// share the column, so they share dx and the pixel-independent factors of a
-// record: their alphas come from paired fp32 operations (add / mul / fma on
-// float2, each half rounded like the scalar form, so every decision is the one
-// eval_splat takes; p - m is formed as p + (-m), which rounds the same).  The
-// staged records are kept in shared memory in pair form -- (-mx, -mx, -my,
-// -my), (a2, a2, b2, b2), (c2, c2, o, o), (r, g, b, depth) and lmin -- so that
-// every pair operand is one 8-byte register pair.
-
-__device__ __forceinline__ bool block_hits8(float mx, float my, float a2, float b2, float c2, float lmin, float x0,
-                                            float y0)
-{
-    if (!(lmin <= 0.0f)) return false;
-    if (lmin == -INFINITY) return true;
-    const float u0 = x0 - mx, u1 = u0 + 7.0f, v0 = y0 - my, v1 = v0 + 7.0f;
-    if (u0 <= 0.0f && u1 >= 0.0f && v0 <= 0.0f && v1 >= 0.0f) return true;
-    const float ka = __fdividef(-0.5f, a2), kc = __fdividef(-0.5f, c2);
-    float best = -INFINITY;
-    {
-        const float va = fminf(fmaxf(b2 * u0 * kc, v0), v1), vb = fminf(fmaxf(b2 * u1 * kc, v0), v1);
-        best = fmaxf(best, fmaf(fmaf(a2, u0, b2 * va), u0, c2 * va * va));
-        best = fmaxf(best, fmaf(fmaf(a2, u1, b2 * vb), u1, c2 * vb * vb));
-    }
-    {
-        const float ua = fminf(fmaxf(b2 * v0 * ka, u0), u1), ub = fminf(fmaxf(b2 * v1 * ka, u0), u1);
-        best = fmaxf(best, fmaf(fmaf(c2, v0, b2 * ua), v0, a2 * ua * ua));
-        best = fmaxf(best, fmaf(fmaf(c2, v1, b2 * ub), v1, a2 * ub * ub));
-    }
-    return best >= lmin;
-}
-
-template <bool STATS>
-__global__ void __launch_bounds__(CTA_THREADS)
-k_composite_fwd_tile(Cam c, float3 bg, int N, const int2* __restrict__ tile_range, const int32_t* __restrict__ gids,
-                     const float4* __restrict__ splats, const float* __restrict__ mesh_depth,
-                     const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
-                     float* __restrict__ out_rgb, float* __restrict__ out_depth, float* __restrict__ out_alpha,
-                     float* __restrict__ T_final, int32_t* __restrict__ n_contrib, const float* __restrict__ aa_cov,
-                     Staged rec, unsigned long long* __restrict__ stats)
-{
-    __shared__ __align__(16) float4 sP0[CTA_THREADS], sP1[CTA_THREADS], sP2[CTA_THREADS], sP3[CTA_THREADS];
-    __shared__ float sL[CTA_THREADS];
-    const int tile = blockIdx.x;
-    const int tx = tile % c.TW, ty = tile / c.TW;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bx = tx * TILE + (warp & 1) * 8, by = ty * TILE + (warp >> 1) * 8;
-    const int i = bx + (lane & 7), j0 = by + (lane >> 3), j1 = j0 + 4;
-    const float x0 = (float)bx + 0.5f, y0 = (float)by + 0.5f;
-    const float2 pxx = make_float2((float)i + 0.5f, (float)i + 0.5f);
-    const float2 pyy = make_float2((float)j0 + 0.5f, (float)j1 + 0.5f);
-    const bool in0 = i < c.W && j0 < c.H, in1 = i < c.W && j1 < c.H;
-    const int64_t pix0 = (int64_t)j0 * c.W + i, pix1 = (int64_t)j1 * c.W + i;
-    float D0 = -INFINITY, D1 = -INFINITY;
-    bool cov0 = false, cov1 = false;
-    if (in0) {
-        D0 = mesh_depth[pix0];
-        cov0 = aa_cov ? D0 < INFINITY : face_id[pix0] >= 0;
-    }
-    if (in1) {
-        D1 = mesh_depth[pix1];
-        cov1 = aa_cov ? D1 < INFINITY : face_id[pix1] >= 0;
-    }
-    float T0 = 1.0f, T1 = 1.0f;
-    float4 S0 = make_float4(0.f, 0.f, 0.f, 0.f), S1 = make_float4(0.f, 0.f, 0.f, 0.f);  // (r, g, b, depth) sums
-    int last0 = 0, last1 = 0;
-    uint32_t visited = 0, blended = 0;
-    bool done0 = !in0, done1 = !in1;
-    const int2 r = rec.A ? clamp_range(tile_range[tile], rec.cap) : tile_range[tile];
-    for (int b = r.x; b < r.y; b += CTA_THREADS) {
-        // this barrier also keeps the staging below from overwriting records that
-        // another warp of the CTA is still reading from the previous batch
-        if (__syncthreads_count(done0 && done1) == CTA_THREADS) break;
-        const int n = min(CTA_THREADS, r.y - b);
-        if ((int)threadIdx.x < n) {
-            int g = gids[b + threadIdx.x];
-            if (g < 0 || g >= N) g = -1;  // an id outside [0, N): an entry that draws nothing
-            float4 A, B, C;
-            stage_rec(splats, g, A, B, C);
-            sP0[threadIdx.x] = make_float4(-A.x, -A.x, -A.y, -A.y);
-            sP1[threadIdx.x] = make_float4(A.z, A.z, A.w, A.w);
-            sP2[threadIdx.x] = make_float4(B.x, B.x, B.y, B.y);
-            sP3[threadIdx.x] = make_float4(B.z, B.w, C.x, C.y);
-            sL[threadIdx.x] = C.w;
-            if (rec.A) {  // the backward pass's staged records, in list order
-                const int64_t e = b + threadIdx.x;
-                rec.A[e] = A;
-                rec.B[e] = B;
-                rec.C[e] = C;
-            }
-        }
-        __syncthreads();
-        for (int m = 0; m * 32 < n; ++m) {
-            if (__all_sync(0xffffffffu, done0 && done1)) break;
-            const int kk = m * 32 + lane;
-            bool hit = false;
-            if (kk < n) {
-                const float4 p0 = sP0[kk], p1 = sP1[kk], p2 = sP2[kk];
-                hit = block_hits8(-p0.x, -p0.z, p1.x, p1.z, p2.x, sL[kk], x0, y0);
-            }
-            uint32_t mask = __ballot_sync(0xffffffffu, hit);
-            while (mask) {
-                const int k = m * 32 + __ffs(mask) - 1;
-                mask &= mask - 1;
-                if (done0 && done1) continue;
-                const float4 p0 = sP0[k], p1 = sP1[k], p2 = sP2[k], p3 = sP3[k];
-                // the two pixels' alphas, operation for operation as eval_splat
-                const float2 dx = __fadd2_rn(pxx, make_float2(p0.x, p0.y));
-                const float2 dy = __fadd2_rn(pyy, make_float2(p0.z, p0.w));
-                const float2 q = __ffma2_rn(make_float2(p2.x, p2.y), __fmul2_rn(dy, dy),
-                                            __fmul2_rn(make_float2(p1.z, p1.w), __fmul2_rn(dx, dy)));
-                const float2 l = __ffma2_rn(make_float2(p1.x, p1.y), __fmul2_rn(dx, dx), q);
-                const float2 oG = __fmul2_rn(make_float2(p2.z, p2.w), make_float2(ex2(l.x), ex2(l.y)));
-                const float z = p3.w;
-                // pixel 0, then pixel 1: hard test (sorted by depth: once a Gaussian
-                // is not in front of the mesh, none after it is), skips, stop
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    bool& done = h ? done1 : done0;
-                    if (done) continue;
-                    if (!(z < (h ? D1 : D0))) {
-                        done = true;
-                        continue;
-                    }
-                    if (STATS) ++visited;
-                    const float lh = h ? l.y : l.x, og = h ? oG.y : oG.x;
-                    const float a = og > ALPHA_MAX ? ALPHA_MAX : og;
-                    if (lh > 0.0f || a < ALPHA_MIN) continue;
-                    float& T = h ? T1 : T0;
-                    const float Tn = __fmul_rn(T, __fsub_rn(1.0f, a));
-                    if (Tn <= T_STOP) {
-                        done = true;
-                        continue;
-                    }
-                    const float w = a * T;
-                    float4& S = h ? S1 : S0;
-                    S.x = fmaf(w, p3.x, S.x);
-                    S.y = fmaf(w, p3.y, S.y);
-                    S.z = fmaf(w, p3.z, S.z);
-                    S.w = fmaf(w, z, S.w);
-                    T = Tn;
-                    (h ? last1 : last0) = b - r.x + k + 1;
-                    if (STATS) ++blended;
-                }
-            }
-        }
-    }
-    if (STATS) {
-        block_count(visited, stats);
-        block_count(blended, stats + 1);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (!(h ? in1 : in0)) continue;
-        const int64_t pix = h ? pix1 : pix0;
-        const float T = h ? T1 : T0, D = h ? D1 : D0;
-        const bool cov = h ? cov1 : cov0;
-        const float4 S = h ? S1 : S0;
-        float tr, tg, tb;
-        if (aa_cov) {
-            // the layer (coverage a, premultiplied colour) over the background; the
-            // colour and depth composited behind it are added by k_composite_back
-            const float a = aa_cov[pix], ua = 1.0f - a;
-            tr = fmaf(ua, bg.x, mesh_rgb[3 * pix]);
-            tg = fmaf(ua, bg.y, mesh_rgb[3 * pix + 1]);
-            tb = fmaf(ua, bg.z, mesh_rgb[3 * pix + 2]);
-            out_depth[pix] = a > 0.0f ? fmaf(T, a * D, S.w) : S.w;
-            out_alpha[pix] = 1.0f - T * ua;
-        } else {
-            if (cov) {
-                tr = mesh_rgb[3 * pix]; tg = mesh_rgb[3 * pix + 1]; tb = mesh_rgb[3 * pix + 2];
-            } else {
-                tr = bg.x; tg = bg.y; tb = bg.z;
-            }
-            out_depth[pix] = cov ? fmaf(T, D, S.w) : S.w;
-            out_alpha[pix] = cov ? 1.0f : 1.0f - T;
-        }
-        out_rgb[3 * pix] = fmaf(T, tr, S.x);
-        out_rgb[3 * pix + 1] = fmaf(T, tg, S.y);
-        out_rgb[3 * pix + 2] = fmaf(T, tb, S.z);
-        T_final[pix] = T;
-        n_contrib[pix] = h ? last1 : last0;
-    }
-}
-
 constexpr int NGRAD = 10;
 constexpr int GROUP = 4;
 constexpr unsigned FULL = 0xffffffffu;
@@ -662,6 +475,7 @@ struct RedSmem {
     float ds[RGROUP][RPAD];  // [group slot][pixel] dL/d sigma
     float w[RGROUP][RPAD];   // [group slot][pixel] alpha T_front
     float2 gf[4][32];        // B fragments (b0, b1) of the upstream gradient, per 8-pixel k-block
+    int kid[RGROUP];         // the group's staged entries (-1: none)
 };
 
 __device__ __forceinline__ uint32_t to_tf32(float x)
@@ -784,7 +598,7 @@ namespace {
 // forward pass's staged records by bulk copies into two buffers; otherwise
 // each thread gathers and stages one record per batch.
 template <bool STATS, bool SOFT, bool BULK, bool MMA>
-__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : (MMA ? (BULK ? 7 : 8) : (BULK ? 9 : 10)))
+__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : (BULK && !MMA ? 9 : 10))
 k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
                 const int32_t* __restrict__ gids, const float4* __restrict__ splats,
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
@@ -795,12 +609,17 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 AaLayer aa, Staged rec, unsigned long long* __restrict__ stats)
 {
     constexpr int NACC = SOFT ? NGRAD + 4 : NGRAD;
-    constexpr int NBUF = BULK ? 2 : 1;
+    // the bulk-copied records take two buffers (the next batch in flight) unless the
+    // tensor-core staging needs the shared memory (then one: each batch's copies
+    // start after the CTA is done with the previous one)
+    constexpr int NBUF = BULK && !MMA ? 2 : 1;
     __shared__ __align__(16) float4 sA_buf[NBUF][CTA_THREADS];
     __shared__ __align__(16) float4 sB_buf[NBUF][CTA_THREADS];
     __shared__ __align__(16) float4 sC_buf[NBUF][CTA_THREADS];
     __shared__ __align__(16) float4 sD_buf[SOFT ? NBUF : 1][SOFT ? CTA_THREADS : 1];
-    __shared__ float sAcc[CTA_THREADS][NACC + 1];
+    // per-entry sums of the CTA's pixels (the tensor-core form adds each warp's
+    // sums to the gradient rows directly and needs none)
+    __shared__ float sAcc[MMA ? 1 : CTA_THREADS][NACC + 1];
     __shared__ __align__(8) uint64_t s_bar[NBUF];
     __shared__ int s_max_last;
     // hard split: the tensor-core reduction's staging per warp, and the moments'
@@ -905,13 +724,13 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         bulk_copy(sC_buf[q], rec.C + lo, bytes, &s_bar[q]);
         if (SOFT) bulk_copy(sD_buf[SOFT ? q : 0], rec.D + lo, bytes, &s_bar[q]);
     };
-    if (BULK && threadIdx.x == 0 && n_batches > 0) issue(0);
+    if (BULK && NBUF == 2 && threadIdx.x == 0 && n_batches > 0) issue(0);
     int n_prev = 0;
     for (int j = 0;; ++j) {
         const int cur = j % NBUF, prev = (j + NBUF - 1) % NBUF;
         // the previous batch's gradients go out (each thread its own slot) and, for
         // the gathering form, the next batch comes in on the same slot
-        if ((int)threadIdx.x < n_prev) {
+        if (!MMA && (int)threadIdx.x < n_prev) {
             const int g = rec_id(sC_buf[prev][threadIdx.x]);
             if (g >= 0) {
                 if (SOFT)
@@ -936,22 +755,33 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 sC_buf[0][threadIdx.x] = C;
                 if (SOFT && g >= 0) sD_buf[0][threadIdx.x] = stage_depth_model(depth_model, g, sp, C.y);
             }
+            if (!MMA) {
 #pragma unroll
-            for (int q = 0; q < NACC; ++q) sAcc[threadIdx.x][q] = 0.0f;
+                for (int q = 0; q < NACC; ++q) sAcc[threadIdx.x][q] = 0.0f;
+            }
         }
         __syncthreads();
         if (BULK) {
-            if (threadIdx.x == 0 && j + 1 < n_batches) {
-                // the other buffer was last read by the flush above: free after the barrier
-                fence_proxy_async_smem();
-                issue(j + 1);
+            if (threadIdx.x == 0) {
+                if (NBUF == 2) {
+                    if (j + 1 < n_batches) {
+                        // the other buffer was last read by the flush above: free after the barrier
+                        fence_proxy_async_smem();
+                        issue(j + 1);
+                    }
+                } else {
+                    // the one buffer was last read before the previous batch's closing barrier
+                    fence_proxy_async_smem();
+                    issue(j);
+                }
             }
             const bool ok = __syncthreads_and(mbar_wait(&s_bar[cur], (uint32_t)(j / NBUF) & 1u));
             if (!ok) {
                 // a copy did not arrive: report, let the copies in flight land, stop
                 if (threadIdx.x == 0) atomicOr(&g_copy_status, 1u);
                 mbar_wait(&s_bar[cur], (uint32_t)(j / NBUF) & 1u);
-                if (j + 1 < n_batches) mbar_wait(&s_bar[(j + 1) % NBUF], (uint32_t)((j + 1) / NBUF) & 1u);
+                if (NBUF == 2 && j + 1 < n_batches)
+                    mbar_wait(&s_bar[(j + 1) % NBUF], (uint32_t)((j + 1) / NBUF) & 1u);
                 return;
             }
         }
@@ -971,24 +801,19 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             if constexpr (MMA) {
                 RedSmem& R = sRed[threadIdx.x >> 5];
                 while (mask) {
-                    int kj[RGROUP];
-#pragma unroll
+                    // per entry of the group, back to front: w = alpha T_front and
+                    // ds = dL/d sigma at this lane's pixel, staged for the contraction
+                    bool any = false;
+#pragma unroll 1
                     for (int jj = 0; jj < RGROUP; ++jj) {
+                        int k = -1;
                         if (mask) {
                             const int bit = 31 - __clz(mask);
-                            kj[jj] = m * 32 + bit;
+                            k = m * 32 + bit;
                             mask &= ~(1u << bit);
-                        } else {
-                            kj[jj] = -1;
                         }
-                    }
-                    // per entry, back to front: w = alpha T_front and ds = dL/d sigma at
-                    // this lane's pixel, staged for the contraction
-                    bool any = false;
-#pragma unroll
-                    for (int jj = 0; jj < RGROUP; ++jj) {
+                        if (lane == 0) R.kid[jj] = k;
                         float w = 0.0f, ds = 0.0f;
-                        const int k = kj[jj];
                         if (k >= 0 && inside && b0 - r.x + k < last) {
                             const float4 C3 = sC[k];
                             if (C3.y < D) {
@@ -1028,47 +853,39 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                             a_frag(R.w, g, q * 8 + c, a);
                             mma_tf32(dc, a[0], a[1], a[2], a[3], __float_as_uint(bg.x), __float_as_uint(bg.y));
                         }
-                        // this lane: group slot g, terms 2c and 2c + 1 (hi rows + lo rows)
+                        // lane (g, c): group slot g, terms 2c and 2c + 1 (hi rows + lo rows):
+                        // S_n = sum ds m_n for c = 0 (S0, Si), 1 (Sj, Sii), 2 (Sij, Sjj); the
+                        // colour sums of channels 2c, 2c + 1 (c < 2 hi, c >= 2 lo columns)
                         const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
                         float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
-                        e0 += __shfl_xor_sync(FULL, e0, 2);  // the upstream gradient's hi + lo columns
+                        e0 += __shfl_xor_sync(FULL, e0, 2);
                         e1 += __shfl_xor_sync(FULL, e1, 2);
-                        int k = kj[0];
-#pragma unroll
-                        for (int jj = 1; jj < RGROUP; ++jj) k = g == jj ? kj[jj] : k;
-                        if (k >= 0) {
-                            // (t0, t1) = (S0, Si) for c = 0, (Sj, Sii) for 1, (Sij, Sjj) for 2
-                            // of S_n = sum ds m_n; with dx = u + i, dy = v + j:
+                        // lane c = 0 collects the entry's six moments and four colour sums
+                        const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
+                        const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
+                        const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
+                        const int k = R.kid[g];
+                        const int gid = k >= 0 ? rec_id(sC[k]) : -1;
+                        if (c == 0 && gid >= 0) {
+                            // with dx = u + i, dy = v + j (u, v at the block's first pixel):
                             //   sum ds dx = u S0 + Si, sum ds dy = v S0 + Sj,
                             //   sum ds dx^2 / 2 = u (u S0 / 2 + Si) + Sii / 2,
                             //   sum ds dx dy = v (u S0 + Si) + u Sj + Sij,
-                            //   sum ds dy^2 / 2 = v^2 S0 / 2 + v Sj + Sjj / 2, sum ds = S0;
-                            // each lane adds its terms' parts, no two lanes of an instruction
-                            // on one slot of one entry
-                            const float2 mean = *reinterpret_cast<const float2*>(&sA[k]);
-                            const float u = pm.x0 - mean.x, v = pm.y0 - mean.y;
-                            float* acc = sAcc[k];
-                            if (c == 0) {
-                                const float p = fmaf(u, t0, t1);
-                                atomicAdd(acc + 0, p);
-                                atomicAdd(acc + 1, v * t0);
-                                atomicAdd(acc + 2, u * fmaf(0.5f * u, t0, t1));
-                                atomicAdd(acc + 3, v * p);
-                                atomicAdd(acc + 4, 0.5f * v * v * t0);
-                                atomicAdd(acc + 5, t0);
-                                atomicAdd(acc + 6, e0);
-                                atomicAdd(acc + 7, e1);
-                            } else if (c == 1) {
-                                atomicAdd(acc + 1, t0);
-                                atomicAdd(acc + 2, 0.5f * t1);
-                                atomicAdd(acc + 3, u * t0);
-                                atomicAdd(acc + 4, v * t0);
-                                atomicAdd(acc + 8, e0);
-                                atomicAdd(acc + 9, e1);
-                            } else if (c == 2) {
-                                atomicAdd(acc + 3, t0);
-                                atomicAdd(acc + 4, 0.5f * t1);
-                            }
+                            //   sum ds dy^2 / 2 = v (v S0 / 2 + Sj) + Sjj / 2, sum ds = S0
+                            const float4 A = sA[k], B = sB[k];
+                            const float u = pm.x0 - A.x, v = pm.y0 - A.y;
+                            float acc[NGRAD];
+                            acc[0] = fmaf(u, t0, t1);
+                            acc[1] = fmaf(v, t0, sj);
+                            acc[2] = fmaf(u, fmaf(0.5f * u, t0, t1), 0.5f * sii);
+                            acc[3] = fmaf(v, acc[0], fmaf(u, sj, sij));
+                            acc[4] = fmaf(v, fmaf(0.5f * v, t0, sj), 0.5f * sjj);
+                            acc[5] = t0;
+                            acc[6] = e0;
+                            acc[7] = e1;
+                            acc[8] = eb;
+                            acc[9] = ez;
+                            flush_grad(v_splats, gid, acc, A, B);
                         }
                     }
                     __syncwarp();  // the staging is rewritten by the next group
@@ -1546,12 +1363,6 @@ k_composite_back_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__
 
 }  // namespace
 
-// The hard split's forward pass takes whole tiles with two pixels a lane
-// (k_composite_fwd_tile) unless GM_FWD_HALF_TILES is set in the environment
-// at the call (then the half-tile kernel, one pixel a lane): both give the
-// same image bit for bit.
-static bool fwd_whole_tiles() { return getenv("GM_FWD_HALF_TILES") == nullptr; }
-
 static Staged staged_of(float* staged, int cap)
 {
     Staged r{nullptr, nullptr, nullptr, nullptr, 0};
@@ -1585,13 +1396,6 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness
 {
     const bool soft = softness > 0.0f;
     const Staged rec = staged_of(staged, staged_cap);
-    if (!soft && fwd_whole_tiles()) {
-        auto k2 = stats ? k_composite_fwd_tile<true> : k_composite_fwd_tile<false>;
-        k2<<<c.TW * c.TH, CTA_THREADS, 0, s>>>(
-            c, make_float3(bg[0], bg[1], bg[2]), N, reinterpret_cast<const int2*>(tile_range), gids,
-            reinterpret_cast<const float4*>(splats), mesh_depth, mesh_rgb, face_id, out_rgb, out_depth, out_alpha,
-            T_final, n_contrib, aa.cov, rec, reinterpret_cast<unsigned long long*>(stats));
-    } else {
     auto kern = soft ? (stats ? k_composite_fwd<true, true> : k_composite_fwd<false, true>)
                      : (stats ? k_composite_fwd<true, false> : k_composite_fwd<false, false>);
     kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
@@ -1600,7 +1404,6 @@ cudaError_t composite_fwd(const Cam& c, const float bg[3], int N, float softness
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
         face_id, out_rgb, out_depth, out_alpha, T_final, n_contrib, aa.cov, rec,
         reinterpret_cast<unsigned long long*>(stats));
-    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !aa.cov) return e;
     const int64_t P = (int64_t)c.W * c.H;

@@ -242,24 +242,35 @@ def test_degenerate_scenes(what, orc):
 
 @pytest.mark.parametrize("softness,antialias", [(0.0, False), (1.0, False), (0.0, True)],
                          ids=["hard", "soft", "antialias"])
-def test_backward_from_staged_records_matches_gathered(softness, antialias):
-    """The backward pass fed by the forward's staged records (bulk copies into
-    shared memory, two batches in flight) gives the gradients of the backward
-    that gathers the records itself, up to the order of float atomic sums,
-    and the forward's image is the same bit for bit either way.  The 512 px
-    sphere has tiles of several 128-entry batches; the 101 x 77 frame has
-    ragged tiles and short lists."""
+def test_backward_forms_agree(softness, antialias, monkeypatch):
+    """The backward pass's forms give the same gradients up to the order of
+    float atomic sums, and the forward's image is the same bit for bit:
+    records bulk-copied from the forward's staged ones or gathered by the
+    backward itself (GM_BWD_GATHER), and, for the hard split, the per-warp
+    sums taken on the tensor cores or by warp shuffles (GM_BWD_SHUFFLE_REDUCE).
+    The 512 px sphere has tiles of several 128-entry batches; the 101 x 77
+    frame has ragged tiles and short lists.  The tensor-core sums (tf32 hi /
+    lo parts, about 22 bits) agree with the shuffle sums within 1e-5
+    relative of the largest gradient."""
     H.need_gpu()
     import torch
     import differentiable_hybrid_mesh_tile_b300 as gm
     sph = scenes.sphere512()
     ragged = scenes.Scene(sph.name, [scenes.look_at((0.3, 0.5, 2.6), (0, 0, 0), 101, 77, 90, 95, 47.3, 40.1)],
                           sph.mesh, sph.gaussians, sph.bg)
+    forms = [dict(), dict(GM_BWD_GATHER="1")]
+    if softness == 0.0:
+        forms += [dict(GM_BWD_SHUFFLE_REDUCE="1"), dict(GM_BWD_GATHER="1", GM_BWD_SHUFFLE_REDUCE="1")]
     for s in (sph, ragged):
         cam = s.camera
         out = []
-        for staged in (True, False):
-            r = gm.HybridRenderer(cam, bg=s.bg, softness=softness, antialias=antialias, staged=staged)
+        for env in forms:
+            for k in ("GM_BWD_GATHER", "GM_BWD_SHUFFLE_REDUCE"):
+                if k in env:
+                    monkeypatch.setenv(k, env[k])
+                else:
+                    monkeypatch.delenv(k, raising=False)
+            r = gm.HybridRenderer(cam, bg=s.bg, softness=softness, antialias=antialias)
             r.upload(s.mesh, s.gaussians)
             r.forward(sync=True)
             g = [torch.as_tensor(x).cuda() for x in scenes.upstream_grads(8, cam.width, cam.height)]
@@ -267,40 +278,14 @@ def test_backward_from_staged_records_matches_gathered(softness, antialias):
             torch.cuda.synchronize()
             out.append(([t.clone() for t in (r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib)],
                         [t.clone() for t in v]))
-            if staged:
+            if not env:
                 n_batches = (torch.diff(r.g_range, dim=1) + 127) // 128
                 print("%dx%d: longest tile list %d batches" % (cam.width, cam.height, int(n_batches.max())))
-        for a, b in zip(out[0][0], out[1][0]):
-            assert torch.equal(a, b)
-        for a, b in zip(out[0][1], out[1][1]):
-            torch.testing.assert_close(a, b, rtol=1e-4, atol=1e-6 * max(1.0, float(b.abs().max())))
+        for k in ("GM_BWD_GATHER", "GM_BWD_SHUFFLE_REDUCE"):
+            monkeypatch.delenv(k, raising=False)
+        for o in out[1:]:
+            for a, b in zip(out[0][0], o[0]):
+                assert torch.equal(a, b)
+            for a, b in zip(out[0][1], o[1]):
+                torch.testing.assert_close(a, b, rtol=1e-4, atol=1e-5 * max(1.0, float(b.abs().max())))
     assert gm.gm_get_copy_status(clear=True) == 0
-
-
-@pytest.mark.parametrize("antialias", [False, True], ids=["hard", "antialias"])
-def test_whole_tile_forward_matches_half_tiles(antialias, monkeypatch):
-    """The hard split's forward pass over whole tiles (two pixels a lane, paired
-    fp32 arithmetic) writes the image, T_final, n_contrib and the staged
-    records of the half-tile form (one pixel a lane, GM_FWD_HALF_TILES) bit
-    for bit, on the 512 px sphere and on a ragged 101 x 77 frame."""
-    H.need_gpu()
-    import torch
-    import differentiable_hybrid_mesh_tile_b300 as gm
-    sph = scenes.sphere512()
-    ragged = scenes.Scene(sph.name, [scenes.look_at((0.3, 0.5, 2.6), (0, 0, 0), 101, 77, 90, 95, 47.3, 40.1)],
-                          sph.mesh, sph.gaussians, sph.bg)
-    for s in (sph, ragged):
-        out = []
-        for half in (False, True):
-            if half:
-                monkeypatch.setenv("GM_FWD_HALF_TILES", "1")
-            else:
-                monkeypatch.delenv("GM_FWD_HALF_TILES", raising=False)
-            r = gm.HybridRenderer(s.camera, bg=s.bg, antialias=antialias)
-            r.upload(s.mesh, s.gaussians)
-            r.forward(sync=True)
-            torch.cuda.synchronize()
-            out.append([t.clone() for t in (r.out_rgb, r.out_depth, r.out_alpha, r.T_final, r.n_contrib)])
-        monkeypatch.delenv("GM_FWD_HALF_TILES", raising=False)
-        for a, b in zip(*out):
-            assert torch.equal(a, b)
