@@ -111,15 +111,15 @@ int gm_get_copy_status(uint32_t* flags, int32_t clear)
 
 int gm_set_wait_limit(uint32_t polls)
 {
-    cudaError_t e = gm::set_wait_limit(polls);
-    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_set_wait_limit");
+    gm::set_wait_limit(polls);
+    return GM_OK;
 }
 
 int gm_get_wait_limit(uint32_t* polls)
 {
     GM_REQUIRE(polls, "polls is NULL");
-    cudaError_t e = gm::get_wait_limit(polls);
-    return e == cudaSuccess ? GM_OK : cuda_fail(e, "gm_get_wait_limit");
+    *polls = gm::wait_limit();
+    return GM_OK;
 }
 
 size_t gm_bin_triangles_workspace_size(int32_t nF, int32_t cap, int32_t width, int32_t height)

@@ -793,104 +793,114 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         // those only the ones that can reach its pixels (a ballot per 32 entries);
         // they are taken four at a time from the back
         const int k_top = min(n, warp_last - (b0 - r.x)) - 1;
+        if constexpr (MMA) {
+            // groups of eight hits, filled across the 32-entry chunks (back to front)
+            RedSmem& R = sRed[threadIdx.x >> 5];
+            int m = k_top >> 5;
+            auto chunk_hits = [&](int mm) {
+                const int kk = mm * 32 + lane;
+                return __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0));
+            };
+            uint32_t mask = m >= 0 ? chunk_hits(m) : 0u;
+            for (;;) {
+                while (!mask && m > 0) mask = chunk_hits(--m);
+                if (!mask) break;
+                // per entry of the group, back to front: w = alpha T_front and
+                // ds = dL/d sigma at this lane's pixel, staged for the contraction
+                bool any = false;
+#pragma unroll 1
+                for (int jj = 0; jj < RGROUP; ++jj) {
+                    while (!mask && m > 0) mask = chunk_hits(--m);
+                    int k = -1;
+                    if (mask) {
+                        const int bit = 31 - __clz(mask);
+                        k = m * 32 + bit;
+                        mask &= ~(1u << bit);
+                    }
+                    if (lane == 0) R.kid[jj] = k;
+                    float w = 0.0f, ds = 0.0f;
+                    if (k >= 0 && inside && b0 - r.x + k < last) {
+                        const float4 C3 = sC[k];
+                        if (C3.y < D) {
+                            if (STATS) ++visited;
+                            const float4 A = sA[k], B = sB[k];
+                            const Eval e = eval_splat(A, B, px, py);
+                            if (!e.skip) {
+                                if (STATS) ++contributed;
+                                any = true;
+                                const float a = e.alpha;
+                                const float rom = __fdividef(1.0f, 1.0f - a);
+                                const float Tp = T * rom;  // transmittance in front of it
+                                w = a * Tp;
+                                const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
+                                const float dLda = Tp * front + (aterm - behind) * rom;
+                                behind = fmaf(w, front, behind);
+                                T = Tp;
+                                // alpha clamped at 0.99 has no opacity / sigma gradient;
+                                // elsewhere d alpha / d sigma = -alpha
+                                if (!e.clamped) ds = -dLda * a;
+                            }
+                        }
+                    }
+                    R.ds[jj][lane] = ds;
+                    R.w[jj][lane] = w;
+                }
+                if (__any_sync(FULL, any)) {
+                    __syncwarp();
+                    const int g = lane >> 2, c = lane & 3;
+                    float dm[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t a[4];
+                        const float2 bm = sMf[q][lane], bg = R.gf[q][lane];
+                        a_frag(R.ds, g, q * 8 + c, a);
+                        mma_tf32(dm, a[0], a[1], a[2], a[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
+                        a_frag(R.w, g, q * 8 + c, a);
+                        mma_tf32(dc, a[0], a[1], a[2], a[3], __float_as_uint(bg.x), __float_as_uint(bg.y));
+                    }
+                    // lane (g, c): group slot g, terms 2c and 2c + 1 (hi rows + lo rows):
+                    // S_n = sum ds m_n for c = 0 (S0, Si), 1 (Sj, Sii), 2 (Sij, Sjj); the
+                    // colour sums of channels 2c, 2c + 1 (c < 2 hi, c >= 2 lo columns)
+                    const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
+                    float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
+                    e0 += __shfl_xor_sync(FULL, e0, 2);
+                    e1 += __shfl_xor_sync(FULL, e1, 2);
+                    // lane c = 0 collects the entry's six moments and four colour sums
+                    const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
+                    const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
+                    const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
+                    const int k = R.kid[g];
+                    const int gid = k >= 0 ? rec_id(sC[k]) : -1;
+                    if (c == 0 && gid >= 0) {
+                        // with dx = u + i, dy = v + j (u, v at the block's first pixel):
+                        //   sum ds dx = u S0 + Si, sum ds dy = v S0 + Sj,
+                        //   sum ds dx^2 / 2 = u (u S0 / 2 + Si) + Sii / 2,
+                        //   sum ds dx dy = v (u S0 + Si) + u Sj + Sij,
+                        //   sum ds dy^2 / 2 = v (v S0 / 2 + Sj) + Sjj / 2, sum ds = S0
+                        const float4 A = sA[k], B = sB[k];
+                        const float u = pm.x0 - A.x, v = pm.y0 - A.y;
+                        float acc[NGRAD];
+                        acc[0] = fmaf(u, t0, t1);
+                        acc[1] = fmaf(v, t0, sj);
+                        acc[2] = fmaf(u, fmaf(0.5f * u, t0, t1), 0.5f * sii);
+                        acc[3] = fmaf(v, acc[0], fmaf(u, sj, sij));
+                        acc[4] = fmaf(v, fmaf(0.5f * v, t0, sj), 0.5f * sjj);
+                        acc[5] = t0;
+                        acc[6] = e0;
+                        acc[7] = e1;
+                        acc[8] = eb;
+                        acc[9] = ez;
+                        flush_grad(v_splats, gid, acc, A, B);
+                    }
+                }
+                __syncwarp();  // the staging is rewritten by the next group
+            }
+        } else
         for (int m = k_top >> 5; m >= 0; --m) {
             const int kk = m * 32 + lane;
             uint32_t mask =
                 __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0) &&
                                                !(SOFT && sD[kk].w > Dw));
-            if constexpr (MMA) {
-                RedSmem& R = sRed[threadIdx.x >> 5];
-                while (mask) {
-                    // per entry of the group, back to front: w = alpha T_front and
-                    // ds = dL/d sigma at this lane's pixel, staged for the contraction
-                    bool any = false;
-#pragma unroll 1
-                    for (int jj = 0; jj < RGROUP; ++jj) {
-                        int k = -1;
-                        if (mask) {
-                            const int bit = 31 - __clz(mask);
-                            k = m * 32 + bit;
-                            mask &= ~(1u << bit);
-                        }
-                        if (lane == 0) R.kid[jj] = k;
-                        float w = 0.0f, ds = 0.0f;
-                        if (k >= 0 && inside && b0 - r.x + k < last) {
-                            const float4 C3 = sC[k];
-                            if (C3.y < D) {
-                                if (STATS) ++visited;
-                                const float4 A = sA[k], B = sB[k];
-                                const Eval e = eval_splat(A, B, px, py);
-                                if (!e.skip) {
-                                    if (STATS) ++contributed;
-                                    any = true;
-                                    const float a = e.alpha;
-                                    const float rom = __fdividef(1.0f, 1.0f - a);
-                                    const float Tp = T * rom;  // transmittance in front of it
-                                    w = a * Tp;
-                                    const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
-                                    const float dLda = Tp * front + (aterm - behind) * rom;
-                                    behind = fmaf(w, front, behind);
-                                    T = Tp;
-                                    // alpha clamped at 0.99 has no opacity / sigma gradient;
-                                    // elsewhere d alpha / d sigma = -alpha
-                                    if (!e.clamped) ds = -dLda * a;
-                                }
-                            }
-                        }
-                        R.ds[jj][lane] = ds;
-                        R.w[jj][lane] = w;
-                    }
-                    if (__any_sync(FULL, any)) {
-                        __syncwarp();
-                        const int g = lane >> 2, c = lane & 3;
-                        float dm[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t a[4];
-                            const float2 bm = sMf[q][lane], bg = R.gf[q][lane];
-                            a_frag(R.ds, g, q * 8 + c, a);
-                            mma_tf32(dm, a[0], a[1], a[2], a[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
-                            a_frag(R.w, g, q * 8 + c, a);
-                            mma_tf32(dc, a[0], a[1], a[2], a[3], __float_as_uint(bg.x), __float_as_uint(bg.y));
-                        }
-                        // lane (g, c): group slot g, terms 2c and 2c + 1 (hi rows + lo rows):
-                        // S_n = sum ds m_n for c = 0 (S0, Si), 1 (Sj, Sii), 2 (Sij, Sjj); the
-                        // colour sums of channels 2c, 2c + 1 (c < 2 hi, c >= 2 lo columns)
-                        const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
-                        float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
-                        e0 += __shfl_xor_sync(FULL, e0, 2);
-                        e1 += __shfl_xor_sync(FULL, e1, 2);
-                        // lane c = 0 collects the entry's six moments and four colour sums
-                        const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
-                        const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
-                        const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
-                        const int k = R.kid[g];
-                        const int gid = k >= 0 ? rec_id(sC[k]) : -1;
-                        if (c == 0 && gid >= 0) {
-                            // with dx = u + i, dy = v + j (u, v at the block's first pixel):
-                            //   sum ds dx = u S0 + Si, sum ds dy = v S0 + Sj,
-                            //   sum ds dx^2 / 2 = u (u S0 / 2 + Si) + Sii / 2,
-                            //   sum ds dx dy = v (u S0 + Si) + u Sj + Sij,
-                            //   sum ds dy^2 / 2 = v (v S0 / 2 + Sj) + Sjj / 2, sum ds = S0
-                            const float4 A = sA[k], B = sB[k];
-                            const float u = pm.x0 - A.x, v = pm.y0 - A.y;
-                            float acc[NGRAD];
-                            acc[0] = fmaf(u, t0, t1);
-                            acc[1] = fmaf(v, t0, sj);
-                            acc[2] = fmaf(u, fmaf(0.5f * u, t0, t1), 0.5f * sii);
-                            acc[3] = fmaf(v, acc[0], fmaf(u, sj, sij));
-                            acc[4] = fmaf(v, fmaf(0.5f * v, t0, sj), 0.5f * sjj);
-                            acc[5] = t0;
-                            acc[6] = e0;
-                            acc[7] = e1;
-                            acc[8] = eb;
-                            acc[9] = ez;
-                            flush_grad(v_splats, gid, acc, A, B);
-                        }
-                    }
-                    __syncwarp();  // the staging is rewritten by the next group
-                }
-            } else
             while (mask) {
                 int kj[GROUP];
 #pragma unroll

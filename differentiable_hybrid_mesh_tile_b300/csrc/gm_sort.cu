@@ -7,100 +7,25 @@
 // 8-bit digit that ranks a partition in shared memory (warp multisplit),
 // gets each digit's global offset by look-back over earlier partitions and
 // writes the partition out digit-run by digit-run.  Every inter-block wait is
-// bounded: after g_wait_limit polls (SPIN_LIMIT unless gm_set_wait_limit
-// changed it) the block sets GM_FLAG_TIMEOUT in the caller's counters and
-// carries on, so no launch can hang.
+// bounded: after wait_limit() polls (SPIN_LIMIT unless gm_set_wait_limit
+// changed it; passed to each launch) the block sets GM_FLAG_TIMEOUT in the
+// caller's counters and carries on, so no launch can hang.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <utility>
 
 #include <cuda/atomic>
 
 #include "gm_internal.cuh"
+#include "gm_lookback.cuh"
 
 namespace gm {
 namespace {
 
-constexpr uint32_t F_AGG = 1u << 30;
-constexpr uint32_t F_PRE = 2u << 30;
-constexpr uint32_t V_MASK = (1u << 30) - 1;
-
-// Polls a waiting block makes before it gives up (per device; gm_set_wait_limit).
-__device__ uint32_t g_wait_limit = SPIN_LIMIT;
-
-__device__ __forceinline__ uint32_t ld_relaxed(uint32_t* p)
-{
-    cuda::atomic_ref<uint32_t, cuda::thread_scope_device> r(*p);
-    return r.load(cuda::memory_order_relaxed);
-}
-
-__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v)
-{
-    cuda::atomic_ref<uint32_t, cuda::thread_scope_device> r(*p);
-    r.store(v, cuda::memory_order_relaxed);
-}
-
-// Exclusive scan of one value per thread over a block of NT threads.
-template <int NT>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t& total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t y = lane < NT / 32 ? s_warp[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
-            if (lane >= o) y += z;
-        }
-        if (lane < NT / 32) s_warp[lane] = y;
-    }
-    __syncthreads();
-    uint32_t before = warp > 0 ? s_warp[warp - 1] : 0;
-    total = s_warp[NT / 32 - 1];
-    __syncthreads();
-    return before + x - v;
-}
-
-// Walks back from partition p - 1 summing aggregates until an inclusive
-// prefix is found.  Bounded: gives up after g_wait_limit polls of one slot.
-// A block that gives up returns the sum of the aggregates it has seen, which
-// is at most the true prefix, so every offset built from it stays below the
-// true one (the callers' writes stay inside their buffers).
-__device__ __forceinline__ uint32_t look_back(uint32_t* desc, int p, int stride, int32_t* counters)
-{
-    uint32_t excl = 0;
-    int q = p - 1;
-    uint32_t spins = 0;
-    const uint32_t limit = g_wait_limit;
-    while (q >= 0) {
-        uint32_t d = ld_relaxed(desc + (int64_t)q * stride);
-        uint32_t flag = d & ~V_MASK;
-        if (flag == 0) {
-            if (++spins > limit) {
-                atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_TIMEOUT);
-                break;
-            }
-            continue;
-        }
-        excl += d & V_MASK;
-        if (flag == F_PRE) break;
-        --q;
-        spins = 0;
-    }
-    return excl;
-}
-
 __global__ void __launch_bounds__(SCAN_THREADS)
 k_scan(const int32_t* __restrict__ in, const int32_t* __restrict__ idx, int32_t* __restrict__ out, int n,
-       uint32_t* desc, uint32_t* ticket, int32_t* counters)
+       uint32_t* desc, uint32_t* ticket, int32_t* counters, uint32_t limit)
 {
     __shared__ uint32_t s_warp[SCAN_THREADS / 32];
     __shared__ int s_part;
@@ -128,7 +53,7 @@ k_scan(const int32_t* __restrict__ in, const int32_t* __restrict__ idx, int32_t*
             s_excl = 0;
         } else {
             st_relaxed(desc + p, F_AGG | (total & V_MASK));
-            uint32_t e = look_back(desc, p, 1, counters);
+            uint32_t e = look_back(desc, p, 1, counters, limit);
             st_relaxed(desc + p, F_PRE | ((e + total) & V_MASK));
             s_excl = e;
         }
@@ -194,7 +119,7 @@ struct OnesweepSmem {
 __global__ void __launch_bounds__(SORT_THREADS, 4)
 k_onesweep(const uint64_t* __restrict__ kin, const int32_t* __restrict__ vin, uint64_t* __restrict__ kout,
            int32_t* __restrict__ vout, const int32_t* __restrict__ n_dev, int32_t* counters, int cap, int shift,
-           const uint32_t* __restrict__ digit_start, uint32_t* desc, uint32_t* ticket)
+           const uint32_t* __restrict__ digit_start, uint32_t* desc, uint32_t* ticket, uint32_t limit)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     OnesweepSmem& S = *reinterpret_cast<OnesweepSmem*>(smem_raw);
@@ -262,7 +187,7 @@ k_onesweep(const uint64_t* __restrict__ kin, const int32_t* __restrict__ vin, ui
                 st_relaxed(slot, F_PRE | count);
             } else {
                 st_relaxed(slot, F_AGG | count);
-                excl = look_back(desc + d, p, 256, counters);
+                excl = look_back(desc + d, p, 256, counters, limit);
                 st_relaxed(slot, F_PRE | ((excl + count) & V_MASK));
             }
             S.gofs[d] = digit_start[d] + excl;
@@ -353,15 +278,13 @@ int num_sms()
     return g_sms[dev];
 }
 
-cudaError_t set_wait_limit(uint32_t polls)
-{
-    return cudaMemcpyToSymbol(g_wait_limit, &polls, sizeof(polls));
-}
+namespace {
+std::atomic<uint32_t> g_wait_limit{SPIN_LIMIT};
+}  // namespace
 
-cudaError_t get_wait_limit(uint32_t* polls)
-{
-    return cudaMemcpyFromSymbol(polls, g_wait_limit, sizeof(*polls));
-}
+void set_wait_limit(uint32_t polls) { g_wait_limit.store(polls); }
+
+uint32_t wait_limit() { return g_wait_limit.load(); }
 
 static int scan_parts(int64_t n) { return (int)((n + SCAN_PART - 1) / SCAN_PART); }
 static int sort_parts(int64_t cap) { return (int)((cap + SORT_PART - 1) / SORT_PART); }
@@ -410,7 +333,8 @@ cudaError_t exclusive_scan(const int32_t* counts, const int32_t* idx, int32_t* o
     cudaError_t e = cudaMemsetAsync(ws.ticket, 0, scan_zero_bytes(ws), s);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaMemsetAsync(counters + GM_CNT_K, 0, sizeof(int32_t), s);
-    k_scan<<<scan_parts(n), SCAN_THREADS, 0, s>>>(counts, idx, offsets, n, ws.desc, ws.ticket, counters);
+    k_scan<<<scan_parts(n), SCAN_THREADS, 0, s>>>(counts, idx, offsets, n, ws.desc, ws.ticket, counters,
+                                                  wait_limit());
     return cudaGetLastError();
 }
 
@@ -419,18 +343,26 @@ int sort_passes(int begin_bit, int end_bit)
     return end_bit > begin_bit ? (end_bit - begin_bit + 7) / 8 : 0;
 }
 
+cudaError_t clear_sort_hist(const SortWs& ws, cudaStream_t s)
+{
+    return cudaMemsetAsync(ws.hist, 0, (uint8_t*)ws.desc - (uint8_t*)ws.hist, s);  // histograms and tickets
+}
+
+int64_t sort_desc_words(const SortWs& ws, int passes) { return (int64_t)passes * ws.max_parts * 256; }
+
 cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int cap, int begin_bit, int end_bit,
-                       const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s)
+                       const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s, bool have_hist)
 {
     const int passes = sort_passes(begin_bit, end_bit);
     if (passes == 0 || cap <= 0) return cudaSuccess;
     if (passes > SORT_MAX_PASSES) return cudaErrorInvalidValue;
-    size_t zero = (uint8_t*)ws.desc - (uint8_t*)ws.hist;  // histograms and tickets
-    cudaError_t e = cudaMemsetAsync(ws.hist, 0, zero, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     const int sms = num_sms();
-    int hgrid = (int)std::min<int64_t>(((int64_t)cap + 255) / 256, (int64_t)sms * 4);
-    k_hist<<<hgrid, 256, 0, s>>>(k0, n_dev, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
+    if (!have_hist) {
+        if ((e = clear_sort_hist(ws, s)) != cudaSuccess) return e;
+        int hgrid = (int)std::min<int64_t>(((int64_t)cap + 255) / 256, (int64_t)sms * 4);
+        k_hist<<<hgrid, 256, 0, s>>>(k0, n_dev, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
+    }
     k_hist_scan<<<1, 256, 0, s>>>(ws.hist, passes);
     e = onesweep_attr();
     if (e != cudaSuccess) return e;
@@ -440,7 +372,7 @@ cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int
     for (int p = 0; p < passes; ++p) {
         k_onesweep<<<grid, SORT_THREADS, sizeof(OnesweepSmem), s>>>(
             kin, vin, kout, vout, n_dev, counters, cap, begin_bit + 8 * p, ws.hist + p * 256,
-            ws.desc + (size_t)p * ws.max_parts * 256, ws.tickets + p);
+            ws.desc + (size_t)p * ws.max_parts * 256, ws.tickets + p, wait_limit());
         std::swap(kin, kout);
         std::swap(vin, vout);
     }

@@ -561,10 +561,10 @@ int gm_bin_triangles_noalloc(const gm_camera* cam, const float* V, int32_t nV, c
  * the call's result is then not a valid sort (GM_ERR_TIMEOUT with K_host).
  * The pages have no counterpart: this exists to test the failure path (a
  * limit of 0 makes any block that finds its predecessor unpublished give up).
- * The setting belongs to the current device and holds until changed; set it
- * only while no libgm kernel runs on that device.  Synchronous
- * (cudaMemcpyToSymbol / FromSymbol).  Errors: GM_ERR_CUDA, or
- * GM_ERR_INVALID_ARG for a NULL `polls`.
+ * The setting is process-wide, holds until changed and is read when a call
+ * enqueues its kernels (a captured CUDA graph keeps the value it was captured
+ * with).  Host-only, no device work.  Errors: GM_ERR_INVALID_ARG for a NULL
+ * `polls`.
  * ---------------------------------------------------------------------- */
 #define GM_WAIT_LIMIT_DEFAULT (1u << 22)
 int gm_set_wait_limit(uint32_t polls);
