@@ -5,7 +5,6 @@
 #include <algorithm>
 
 #include "gm_internal.cuh"
-#include "gm_lookback.cuh"
 #include "gm_proj.cuh"
 
 namespace gm {
@@ -413,43 +412,17 @@ k_gauss_shape(Cam c, int N, const float4* __restrict__ splats, const int32_t* __
     }
 }
 
-// After the mesh join, one pass over the depth order (one position a thread,
-// 256 a block, blocks in ticket order):
-//  1. the tiles the Gaussian keeps now that the mesh's tile bounds exist --
-//     for a small rectangle its ellipse-kept tiles less those the mesh hides,
-//     for a large one every tile of the rectangle tested by the whole warp --
-//     and their count;
-//  2. the counts' exclusive scan: within the block, and across blocks by
-//     decoupled look-back over per-block descriptors (bounded waits);
-//  3. the (tile << 32 | depth bits, id) entries at those offsets, in ascending
-//     (depth, id) order, so that a stable sort on the tile bits alone
-//     completes the (tile, depth, id) order; the tile digits of that sort are
-//     counted on the way (its histogram pass is not needed);
-//  4. the last block writes the entry count and flags an overflow.
-// It also clears the tile sort's look-back descriptors (dz words).
+// Per position i of the depth order: the tiles the Gaussian is binned to now
+// that the mesh's tile bounds exist -- for a small rectangle its ellipse-kept
+// tiles less those the mesh hides, for a large one every tile of the rectangle
+// tested again by the whole warp -- as a count (for the scan) and, for a small
+// rectangle, the kept mask (for the emission).
 __global__ void __launch_bounds__(256)
-k_gauss_bin(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
-            int cap, int32_t* counters, uint32_t* desc, uint32_t* ticket, uint32_t limit, int hist_passes,
-            uint32_t* __restrict__ hist, uint32_t* __restrict__ dz, int64_t dz_words, uint64_t* __restrict__ keys,
-            int32_t* __restrict__ vals)
+k_gauss_cull(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
+             int32_t* __restrict__ counts, uint32_t* __restrict__ kept)
 {
-    __shared__ int s_part;
-    __shared__ uint32_t s_warp[8];
-    __shared__ uint32_t s_excl;
-    __shared__ uint32_t s_hist[3][256];
-    __shared__ int4 s_a[256];   // x0, y0, width, Gaussian id
-    __shared__ int2 s_b[256];   // depth bits, first output slot
-    __shared__ uint32_t s_m[256];
-    if (threadIdx.x == 0) s_part = (int)atomicAdd(ticket, 1u);
-    for (int t = threadIdx.x; t < 3 * 256; t += 256) (&s_hist[0][0])[t] = 0u;
-    for (int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x; t < dz_words; t += (int64_t)gridDim.x * 256) dz[t] = 0u;
-    __syncthreads();
-    const int p = s_part;
-    const int i = p * 256 + threadIdx.x;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
-    const int wbase = threadIdx.x & ~31;
-
-    // 1. kept tiles and their count
     int4 ra = make_int4(0, 0, 0, -1), rb = make_int4(0, 0, 0, 0);
     if (i < N) {
         ra = rec[i].a;
@@ -472,11 +445,13 @@ k_gauss_bin(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const
         }
         post = __popc(mask);
     }
+    // large rectangles (near-camera Gaussians): the whole warp, 32 tiles at a time
     BinShape sh = {};
     if (area > SMALL_RECT) sh = bin_shape(splats, ra.w);
-    const uint32_t bigs = __ballot_sync(0xffffffffu, area > SMALL_RECT);
-    for (uint32_t big = bigs; big; big &= big - 1) {
+    uint32_t big = __ballot_sync(0xffffffffu, area > SMALL_RECT);
+    while (big) {
         const int j = __ffs(big) - 1;
+        big &= big - 1;
         const int jx0 = __shfl_sync(0xffffffffu, ra.x, j), jy0 = __shfl_sync(0xffffffffu, ra.y, j);
         const int jw = __shfl_sync(0xffffffffu, ra.z, j), jarea = __shfl_sync(0xffffffffu, area, j);
         const BinShape js = shfl_shape(sh, j);
@@ -491,28 +466,46 @@ k_gauss_bin(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const
         for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
         if (lane == j) post = cnt;
     }
+    if (i < N) {
+        counts[i] = post;
+        kept[i] = mask;
+    }
+}
 
-    // 2. offsets
-    uint32_t total;
-    const uint32_t ex = block_excl_scan<256>((uint32_t)post, s_warp, total);
-    if (threadIdx.x == 0) {
-        if (p == 0) {
-            st_relaxed(desc, F_PRE | (total & V_MASK));
-            s_excl = 0;
-        } else {
-            st_relaxed(desc + p, F_AGG | (total & V_MASK));
-            const uint32_t e = look_back(desc, p, 1, counters, limit);
-            st_relaxed(desc + p, F_PRE | ((e + total) & V_MASK));
-            s_excl = e;
+// Emits the (tile << 32 | depth bits, id) entries of the Gaussian at position
+// i of the depth order, in ascending (depth, id) order, at offsets[i]: entries
+// come out depth-sorted, so a stable sort on the tile bits alone completes the
+// (tile, depth, id) order.  The tiles kept are exactly those k_gauss_cull
+// counted: its mask for small rectangles, the same predicate for large ones.
+__global__ void __launch_bounds__(256)
+k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
+             const int32_t* __restrict__ counts, const uint32_t* __restrict__ kept,
+             const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
+             int32_t* __restrict__ vals)
+{
+    __shared__ int4 s_a[256];   // x0, y0, width, Gaussian id
+    __shared__ int2 s_b[256];   // depth bits, first output slot
+    __shared__ uint32_t s_m[256];
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int wbase = threadIdx.x & ~31;
+    if (i == 0 && counters[GM_CNT_K] > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
+    int4 ra = make_int4(0, 0, 0, -1);
+    int area = 0, dbits = 0;
+    BinShape sh = {};
+    uint32_t mask = 0;
+    int64_t o = 0;
+    if (i < N) {
+        const int4 rb = rec[i].b;
+        if (rb.x > 0 && counts[i] > 0) {
+            ra = rec[i].a;
+            area = rb.x;
+            dbits = rb.z;
+            o = offsets[i];
+            mask = kept[i];
+            if (area > SMALL_RECT) sh = bin_shape(splats, ra.w);  // the big-rectangle path tests again
         }
     }
-    __syncthreads();
-    const int64_t o = (int64_t)s_excl + ex;
-
-    // 3. the entries, and the tile digits of the sort that follows
-    auto count_digits = [&](uint32_t t) {
-        for (int q = 0; q < hist_passes; ++q) atomicAdd(&s_hist[q][(t >> (8 * q)) & 0xffu], 1u);
-    };
     {
         // the kept tiles of the warp's small rectangles, flattened: one entry per
         // lane per round, consecutive lanes writing consecutive slots
@@ -524,23 +517,23 @@ k_gauss_bin(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const
             const int y = __shfl_up_sync(0xffffffffu, p0, d);
             if (lane >= d) p0 += y;
         }
-        const int wtotal = __shfl_sync(0xffffffffu, p0, 31);
+        const int total = __shfl_sync(0xffffffffu, p0, 31);
         p0 -= a;
         s_a[threadIdx.x] = ra;
-        s_b[threadIdx.x] = make_int2(rb.z, (int)o);
+        s_b[threadIdx.x] = make_int2(dbits, (int)o);
         s_m[threadIdx.x] = m;
         __syncwarp();
-        for (int base = 0; base < wtotal; base += 32) {
-            const int q = base + lane;
+        for (int base = 0; base < total; base += 32) {
+            const int p = base + lane;
             int j = 0;
 #pragma unroll
             for (int step = 16; step > 0; step >>= 1) {
                 const int pj = __shfl_sync(0xffffffffu, p0, j + step);
-                if (pj <= q) j += step;
+                if (pj <= p) j += step;
             }
             const int pj = __shfl_sync(0xffffffffu, p0, j);
-            if (q < wtotal) {
-                const int r = q - pj;  // the r-th kept tile of lane j's rectangle
+            if (p < total) {
+                const int r = p - pj;  // the r-th kept tile of lane j's rectangle
                 const uint32_t mj = s_m[wbase + j];
                 int pos = 0, rr = r;
 #pragma unroll
@@ -557,16 +550,17 @@ k_gauss_bin(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const
                 if (dst >= 0 && dst < cap) {
                     int row, col;
                     divmod_small(pos, qa.z, __frcp_rn((float)qa.z), row, col);
-                    const uint32_t t = (uint32_t)((qa.y + row) * c.TW + qa.x + col);
-                    keys[dst] = ((uint64_t)t << 32) | (uint32_t)qb.x;
+                    const int t = (qa.y + row) * c.TW + qa.x + col;
+                    keys[dst] = ((uint64_t)(uint32_t)t << 32) | (uint32_t)qb.x;
                     vals[dst] = qa.w;
-                    count_digits(t);
                 }
             }
         }
     }
-    for (uint32_t big = bigs; big; big &= big - 1) {
+    uint32_t big = __ballot_sync(0xffffffffu, area > SMALL_RECT);
+    while (big) {
         const int j = __ffs(big) - 1;
+        big &= big - 1;
         const int jx0 = __shfl_sync(0xffffffffu, ra.x, j), jy0 = __shfl_sync(0xffffffffu, ra.y, j);
         const int jw = __shfl_sync(0xffffffffu, ra.z, j), jarea = __shfl_sync(0xffffffffu, area, j);
         const int jg = __shfl_sync(0xffffffffu, ra.w, j);
@@ -588,24 +582,11 @@ k_gauss_bin(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
             const int64_t dst = jo + __popc(km & ((1u << lane) - 1u));
             if (keep && dst >= 0 && dst < cap) {
-                const uint32_t t = (uint32_t)(ty * c.TW + tx);
-                keys[dst] = ((uint64_t)t << 32) | jbits;
+                keys[dst] = ((uint64_t)(uint32_t)(ty * c.TW + tx) << 32) | jbits;
                 vals[dst] = jg;
-                count_digits(t);
             }
             jo += __popc(km);
         }
-    }
-    __syncthreads();
-    for (int t = threadIdx.x; t < hist_passes * 256; t += 256) {
-        const uint32_t v = (&s_hist[0][0])[t];
-        if (v) atomicAdd(hist + t, v);
-    }
-    // 4. the entry count, from the last block
-    if (p == (int)gridDim.x - 1 && threadIdx.x == 0) {
-        const int64_t K = (int64_t)s_excl + total;
-        counters[GM_CNT_K] = (int32_t)K;
-        if (K > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
     }
 }
 
@@ -685,9 +666,8 @@ cudaError_t project_views(const Cam* cams, int V, int sh_degree, float softness,
 size_t gauss_bin_ws_bytes(int N, int cap)
 {
     int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
-    const int64_t bparts = (n + 255) / 256;
-    return 256 + a256(sizeof(uint32_t) * bparts) + 2 * a256(sizeof(uint64_t) * n) + 2 * a256(sizeof(int32_t) * n) +
-           a256(sizeof(GaussRec) * n) + 256 + sort_ws_bytes(n > k ? n : k);
+    return scan_ws_bytes(n) + 3 * a256(sizeof(int32_t) * n) + 2 * a256(sizeof(uint64_t) * n) +
+           2 * a256(sizeof(int32_t) * n) + a256(sizeof(GaussRec) * n) + 256 + sort_ws_bytes(n > k ? n : k);
 }
 
 // Tile binning of the Gaussians.  The entries' order (tile, depth, id) is
@@ -696,11 +676,11 @@ size_t gauss_bin_ws_bytes(int N, int cap)
 // only (ceil(log2 T) bits) -- instead of one 32 + log2 T bit sort of K keys.
 // The first half (depth sort, rectangles and ellipse tests, one record per
 // position of the depth order) needs no mesh; the second (occlusion cull,
-// scan and emission in one pass, tile sort) reads the records in order, with
-// no gathers.
+// scan, emission, tile sort) reads the records in order, with no gathers.
 struct GaussWs {
-    uint32_t* bticket;  // [1] ticket of k_gauss_bin's blocks (the first 256 bytes)
-    uint32_t* bdesc;    // [bparts] their look-back descriptors
+    ScanWs sw;
+    int32_t *counts, *offsets;
+    uint32_t* kept;
     uint64_t *dkey, *dkey_alt;
     int32_t *dval, *dval_alt, *n_dev;
     GaussRec* rec;
@@ -710,13 +690,15 @@ struct GaussWs {
 static GaussWs carve_gauss_ws(void* ws, int N, int cap)
 {
     int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
-    const int64_t bparts = (n + 255) / 256;
     GaussWs w;
     uint8_t* b = (uint8_t*)ws;
-    w.bticket = (uint32_t*)b;
-    b += 256;
-    w.bdesc = (uint32_t*)b;
-    b += a256(sizeof(uint32_t) * bparts);
+    b += carve_scan_ws(b, n, w.sw);
+    w.counts = (int32_t*)b;
+    b += a256(sizeof(int32_t) * n);
+    w.offsets = (int32_t*)b;
+    b += a256(sizeof(int32_t) * n);
+    w.kept = (uint32_t*)b;
+    b += a256(sizeof(uint32_t) * n);
     w.dkey = (uint64_t*)b;
     b += a256(sizeof(uint64_t) * n);
     w.dkey_alt = (uint64_t*)b;
@@ -772,19 +754,19 @@ cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N,
         rule.tile_far = tile_far;
         rule.tile_full = tile_full;
         rule.TW = c.TW;
-        // the blocks' ticket and descriptors, and the tile sort's histograms and tickets
-        if ((e = cudaMemsetAsync(w.bticket, 0, 256 + sizeof(uint32_t) * (size_t)grid, s)) != cudaSuccess) return e;
-        if ((e = clear_sort_hist(w.so, s)) != cudaSuccess) return e;
-        k_gauss_bin<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, cap, counters, w.bdesc, w.bticket, wait_limit(),
-                                         passes, w.so.hist, w.so.desc, sort_desc_words(w.so, passes), ek, ev);
+        k_gauss_cull<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = exclusive_scan(w.counts, nullptr, w.offsets, N, counters, w.sw, s)) != cudaSuccess) return e;
+        k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept, w.offsets, cap, counters, ek,
+                                          ev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (tb > 0) {
             if (passes % 2)
                 e = radix_sort(w.so.keys_alt, w.so.vals_alt, keys, gids, cap, 32, 32 + tb, counters + GM_CNT_K,
-                               counters, w.so, s, true);
+                               counters, w.so, s);
             else
                 e = radix_sort(keys, gids, w.so.keys_alt, w.so.vals_alt, cap, 32, 32 + tb, counters + GM_CNT_K,
-                               counters, w.so, s, true);
+                               counters, w.so, s);
             if (e != cudaSuccess) return e;
         }
     }

@@ -1,5 +1,5 @@
-// Decoupled look-back over per-partition descriptors, shared by the scans and
-// radix sorts (gm_sort.cu) and the fused Gaussian binning (gm_gauss.cu).
+// Decoupled look-back over per-partition descriptors, used by the scans and
+// radix sorts (gm_sort.cu).
 //
 // A descriptor is a 32-bit word: its top two bits say whether it holds the
 // partition's own aggregate (F_AGG) or its inclusive prefix (F_PRE), the low
