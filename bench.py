@@ -158,25 +158,27 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
     return n_ranks * pixels_per_rank / 1e6 / (ms / 1e3)
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
-# stage's kernel on soup_1080p, from one ncu capture of that kernel.  A figure
-# holds only for the kernel sources it was taken on: when any of them has
-# changed since, the traffic is reported as null.
-PROFILED_TRAFFIC = {
+# Counters of one launch of a stage's kernel on soup_1080p, from one ncu capture
+# of that kernel: DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) and
+# shared-memory wavefronts (l1tex__data_pipe_lsu_wavefronts_mem_shared.sum).  A
+# figure holds only for the kernel sources it was taken on: when any of them
+# has changed since, it is reported as null.
+PROFILED = {
     "composite_bwd": {
         "kernel": "k_composite_bwd",
-        "bytes": 160749312 + 11179776,
+        "dram_bytes": 186321664 + 11989760,
+        "smem_wavefronts": 74898058,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "2aa73d489c78fde28e92d9d1bd7884a5c795cf219f7a9c8230d5ec1339c06e46",
+                "f739810c0b99f11e23ceaa04b208f267f0ffe7d60ed068919e2d53b61e2a3ff6",
         },
     },
 }
 
 
-def profiled_traffic(stage):
+def profiled(stage, key):
     import hashlib
-    rec = PROFILED_TRAFFIC.get(stage)
+    rec = PROFILED.get(stage)
     if rec is None:
         return None
     for path, sha in rec["sources"].items():
@@ -186,7 +188,7 @@ def profiled_traffic(stage):
                     return None
         except OSError:
             return None
-    return rec["bytes"]
+    return rec[key]
 
 
 # --------------------------------------------------------------- GPU arm --
@@ -397,6 +399,14 @@ def run_gm(args, ws, rank, local):
             stages[k] = {"bound": "alu", "ms": stage_ms[k], "achieved": ach, "peak": alu_peak, "unit": "Tops/s",
                          "frac": ach / alu_peak, "algorithmic": amount}
     stages["zbuffer"] = {"bound": "alu", "ms": stage_ms["zbuffer"], "note": "reported, no target"}
+    # compositing's shared-memory side: wavefronts of one launch (ncu) against one
+    # wavefront per SM per clock over the stage's measured time
+    for k in ("composite_fwd", "composite_bwd"):
+        wf = profiled(k, "smem_wavefronts")
+        if wf is not None:
+            cap = sms * clk_mhz * 1e6 * stage_ms[k] / 1e3
+            stages[k]["smem"] = {"wavefronts": wf, "peak_per_s": sms * clk_mhz * 1e6, "frac": wf / cap,
+                                 "source": "ncu capture of the same kernel source (wavefronts per launch)"}
     for k in stages:
         stages[k]["ms_median_p10_p90"] = spread[k]
     # the tile-list rasterizer (not in the step: the renderer's default is the
@@ -413,7 +423,7 @@ def run_gm(args, ws, rank, local):
                               "the timed step", "ms_median_p10_p90": tz_spread[1]}
     top = max((k for k in work if k != "project_bwd"), key=lambda k: stage_ms[k])
     roof = dict(stages[top])
-    roof.update(kernel=top, traffic=profiled_traffic(top), peak_source=hbm_src if roof["bound"] == "hbm" else
+    roof.update(kernel=top, traffic=profiled(top, "dram_bytes"), peak_source=hbm_src if roof["bound"] == "hbm" else
                 "SMs x 128 FP32 lanes x median SM clock under load")
     roof.pop("ms", None)
     roof.pop("algorithmic", None)
