@@ -311,9 +311,9 @@ int gm_project_gaussians_bwd_views(const gm_camera* cams, int32_t V, const gm_op
 
 size_t gm_bin_sort_gaussians_workspace_size(int32_t N, int32_t cap, int32_t width, int32_t height)
 {
-    const int64_t T = (int64_t)((width > 0 ? width : 1) + GM_TILE - 1) / GM_TILE *
-                      (((height > 0 ? height : 1) + GM_TILE - 1) / GM_TILE);
-    return gm::gauss_bin_ws_bytes(N < 0 ? 0 : N, cap < 0 ? 0 : cap, (int)(T < (1 << 24) ? T : (1 << 24)));
+    (void)width;
+    (void)height;
+    return gm::gauss_bin_ws_bytes(N < 0 ? 0 : N, cap < 0 ? 0 : cap);
 }
 
 int gm_sort_gaussians_by_depth(const gm_camera* cam, int32_t N, const float* splats, const int32_t* radii,
@@ -325,7 +325,7 @@ int gm_sort_gaussians_by_depth(const gm_camera* cam, int32_t N, const float* spl
     GM_REQUIRE(N == 0 || (splats && radii), "splats / radii is NULL");
     GM_REQUIRE(N == 0 || aligned16(splats), "splats must be 16-byte aligned");
     GM_REQUIRE(counters, "counters is NULL");
-    const size_t need = gm::gauss_bin_ws_bytes(N, cap, gm::make_cam(*cam).TW * gm::make_cam(*cam).TH);
+    const size_t need = gm::gauss_bin_ws_bytes(N, cap);
     GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaError_t e = gm::gauss_depth_sort(gm::make_cam(*cam), N, splats, radii, cap, counters, ws,
@@ -347,7 +347,7 @@ int gm_bin_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, const
     GM_REQUIRE(!opts->cull_occluded || (tile_far && tile_full), "cull_occluded needs tile_far and tile_full");
     GM_REQUIRE(tile_range && counters, "tile_range / counters is NULL");
     GM_REQUIRE(cap == 0 || (keys && gids), "keys / gids is NULL");
-    const size_t need = gm::gauss_bin_ws_bytes(N, cap, gm::make_cam(*cam).TW * gm::make_cam(*cam).TH);
+    const size_t need = gm::gauss_bin_ws_bytes(N, cap);
     GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
@@ -373,7 +373,7 @@ int gm_bin_sort_gaussians(const gm_camera* cam, const gm_opts* opts, int32_t N, 
     GM_REQUIRE(!opts->cull_occluded || (tile_far && tile_full), "cull_occluded needs tile_far and tile_full");
     GM_REQUIRE(tile_range && counters, "tile_range / counters is NULL");
     GM_REQUIRE(cap == 0 || (keys && gids), "keys / gids is NULL");
-    const size_t need = gm::gauss_bin_ws_bytes(N, cap, gm::make_cam(*cam).TW * gm::make_cam(*cam).TH);
+    const size_t need = gm::gauss_bin_ws_bytes(N, cap);
     GM_REQUIRE(ws && ws_bytes >= need, "workspace of %zu bytes needed", need);
     GM_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;

@@ -4,10 +4,7 @@
 // (tile | depth) keys with the per-tile occlusion cull.
 #include <algorithm>
 
-#include <stdlib.h>
-
 #include "gm_internal.cuh"
-#include "gm_lookback.cuh"
 #include "gm_proj.cuh"
 
 namespace gm {
@@ -593,362 +590,6 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
     }
 }
 
-// ------------------------------------------------ per-tile bucket sort -----
-//
-// After the mesh join the entries are formed tile by tile instead of by a
-// device-wide sort on the tile bits: each kept (Gaussian, tile) pair is
-// counted per tile (atomics), the tile counts are scanned into the tile
-// ranges, each pair drops its depth-order position i into its tile's bucket
-// (atomics, any order), and one CTA per tile sorts its bucket by i in shared
-// memory (stable LSD radix, 8-bit digits; i is unique, so the result is the
-// (depth, id) order exactly) and writes the (tile << 32 | depth bits, id)
-// entries.  The ranges are the scan's, with no pass over the sorted keys.
-
-// Kept tiles of the small rectangles of a warp, flattened over the lanes (one
-// (Gaussian, tile) pair per lane per round); fn(i_lane, tile) for each.
-template <typename Fn>
-__device__ __forceinline__ void for_kept_small(const Cam& c, uint32_t m, const int4& ra, int lane, int4* s_a,
-                                               uint32_t* s_m, Fn fn)
-{
-    const int wbase = threadIdx.x & ~31;
-    const int a = __popc(m);
-    int p0 = a;  // inclusive prefix sum over the lanes
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, p0, d);
-        if (lane >= d) p0 += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, p0, 31);
-    p0 -= a;
-    s_a[threadIdx.x] = ra;
-    s_m[threadIdx.x] = m;
-    __syncwarp();
-    for (int base = 0; base < total; base += 32) {
-        const int p = base + lane;
-        int j = 0;
-#pragma unroll
-        for (int step = 16; step > 0; step >>= 1) {
-            const int pj = __shfl_sync(0xffffffffu, p0, j + step);
-            if (pj <= p) j += step;
-        }
-        const int pj = __shfl_sync(0xffffffffu, p0, j);
-        if (p < total) {
-            const int r = p - pj;  // the r-th kept tile of lane j's rectangle
-            const uint32_t mj = s_m[wbase + j];
-            int pos = 0, rr = r;
-#pragma unroll
-            for (int st = 8; st > 0; st >>= 1) {
-                const int cnt = __popc((mj >> pos) & ((1u << st) - 1u));
-                if (cnt <= rr) {
-                    rr -= cnt;
-                    pos += st;
-                }
-            }
-            const int4 qa = s_a[wbase + j];
-            int row, col;
-            divmod_small(pos, qa.z, __frcp_rn((float)qa.z), row, col);
-            fn(j, (qa.y + row) * c.TW + qa.x + col);
-        }
-    }
-    __syncwarp();
-}
-
-// Kept tiles of the warp's large rectangles (each tested again, by the whole
-// warp, 32 tiles at a time); fn(tile) for each.
-template <typename Fn>
-__device__ __forceinline__ void for_kept_big(const Cam& c, const BinRule& rule, const float4* __restrict__ splats,
-                                             int area, const int4& ra, int lane, Fn fn)
-{
-    BinShape sh = {};
-    if (area > SMALL_RECT) sh = bin_shape(splats, ra.w);
-    uint32_t big = __ballot_sync(0xffffffffu, area > SMALL_RECT);
-    while (big) {
-        const int j = __ffs(big) - 1;
-        big &= big - 1;
-        const int jx0 = __shfl_sync(0xffffffffu, ra.x, j), jy0 = __shfl_sync(0xffffffffu, ra.y, j);
-        const int jw = __shfl_sync(0xffffffffu, ra.z, j), jarea = __shfl_sync(0xffffffffu, area, j);
-        const BinShape js = shfl_shape(sh, j);
-        const float jinv = __frcp_rn((float)jw);
-        for (int base = 0; base < jarea; base += 32) {
-            const int t_in = base + lane;
-            if (t_in < jarea) {
-                int row, col;
-                divmod_small(t_in, jw, jinv, row, col);
-                if (keep_tile(rule, js, jx0 + col, jy0 + row)) fn(j, (jy0 + row) * c.TW + jx0 + col);
-            }
-        }
-    }
-}
-
-// The small rectangles' kept masks (the ellipse-kept tiles less those the mesh
-// hides); 0 for large ones and empty positions.
-__device__ __forceinline__ uint32_t kept_mask(const Cam& c, const BinRule& rule, const int4& ra, const int4& rb)
-{
-    const int area = rb.x;
-    if (!(area > 0 && area <= SMALL_RECT)) return 0u;
-    uint32_t mask = rule.tile_test ? (uint32_t)rb.y : ((1u << area) - 1u);
-    if (rule.cull) {
-        const float depth = __int_as_float(rb.z), hide = __int_as_float(rb.w);
-        const float inv = __frcp_rn((float)ra.z);
-        for (uint32_t m = mask; m; m &= m - 1) {
-            const int pos = __ffs(m) - 1;
-            int row, col;
-            divmod_small(pos, ra.z, inv, row, col);
-            if (tile_hidden(rule, (ra.y + row) * c.TW + ra.x + col, depth, hide)) mask &= ~(1u << pos);
-        }
-    }
-    return mask;
-}
-
-// Counts each kept (Gaussian, tile) pair in its tile; keeps the small
-// rectangles' masks for the scatter.
-__global__ void __launch_bounds__(256)
-k_tile_count(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
-             uint32_t* __restrict__ kept, int32_t* __restrict__ tile_cnt)
-{
-    __shared__ int4 s_a[256];
-    __shared__ uint32_t s_m[256];
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    const int lane = threadIdx.x & 31;
-    int4 ra = make_int4(0, 0, 1, -1), rb = make_int4(0, 0, 0, 0);
-    if (i < N) {
-        ra = rec[i].a;
-        rb = rec[i].b;
-    }
-    const uint32_t mask = kept_mask(c, rule, ra, rb);
-    if (i < N) kept[i] = mask;
-    for_kept_small(c, mask, ra, lane, s_a, s_m, [&](int, int t) { atomicAdd(tile_cnt + t, 1); });
-    for_kept_big(c, rule, splats, rb.x, ra, lane, [&](int, int t) { atomicAdd(tile_cnt + t, 1); });
-}
-
-// Exclusive scan of the tile counts (one CTA, chunks of 4096 tiles): the tile
-// ranges (clamped to cap), the scatter cursors, the entry count and the
-// overflow flag.
-__global__ void __launch_bounds__(1024)
-k_tile_offsets(int T, const int32_t* __restrict__ tile_cnt, int cap, int32_t* counters, int32_t* __restrict__ cursor,
-               int2* __restrict__ range)
-{
-    __shared__ uint32_t s_warp[32];
-    __shared__ int64_t s_run;
-    if (threadIdx.x == 0) s_run = 0;
-    __syncthreads();
-    for (int base = 0; base < T; base += 4 * 1024) {
-        int v[4];
-        uint32_t sum = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int t = base + 4 * (int)threadIdx.x + k;
-            v[k] = t < T ? tile_cnt[t] : 0;
-            sum += (uint32_t)v[k];
-        }
-        uint32_t total;
-        const uint32_t ex = block_excl_scan<1024>(sum, s_warp, total);
-        int64_t o = s_run + ex;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int t = base + 4 * (int)threadIdx.x + k;
-            if (t < T) {
-                const int64_t e = o + v[k];
-                cursor[t] = (int32_t)(o < 0x7fffffffll ? o : 0x7fffffffll);
-                range[t] = make_int2((int)(o < cap ? o : cap), (int)(e < cap ? e : cap));
-            }
-            o += v[k];
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) s_run += total;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        counters[GM_CNT_K] = (int32_t)(s_run < 0x7fffffffll ? s_run : 0x7fffffffll);
-        if (s_run > cap) atomicOr(counters + GM_CNT_FLAGS, GM_FLAG_OVERFLOW);
-    }
-}
-
-// Drops the depth-order position of each kept (Gaussian, tile) pair into its
-// tile's bucket, at a slot taken from the tile's cursor (slots at or past cap
-// are dropped: the overflow flag is set).
-__global__ void __launch_bounds__(256)
-k_tile_scatter(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
-               const uint32_t* __restrict__ kept, int32_t* __restrict__ cursor, int cap, uint32_t* __restrict__ bucket)
-{
-    __shared__ int4 s_a[256];
-    __shared__ uint32_t s_m[256];
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    const int lane = threadIdx.x & 31;
-    int4 ra = make_int4(0, 0, 1, -1), rb = make_int4(0, 0, 0, 0);
-    uint32_t mask = 0;
-    if (i < N) {
-        rb = rec[i].b;
-        if (rb.x > 0) {
-            ra = rec[i].a;
-            mask = kept[i];
-        } else {
-            rb.x = 0;
-        }
-    }
-    const int ibase = blockIdx.x * blockDim.x + (threadIdx.x & ~31);
-    auto drop = [&](int j, int t) {
-        const int slot = atomicAdd(cursor + t, 1);
-        if (slot >= 0 && slot < cap) bucket[slot] = (uint32_t)(ibase + j);
-    };
-    for_kept_small(c, mask, ra, lane, s_a, s_m, drop);
-    for_kept_big(c, rule, splats, rb.x, ra, lane, drop);
-}
-
-constexpr int TS_THREADS = 256;
-constexpr int TS_IPT = 8;
-constexpr int TS_CHUNK = TS_THREADS * TS_IPT;
-
-struct TileSortSmem {
-    uint32_t keys[TS_CHUNK];
-    uint32_t keys2[TS_CHUNK];
-    uint32_t whist[TS_THREADS / 32][256];
-    uint32_t lstart[256];
-    uint32_t base[256];
-    uint32_t s_warp[TS_THREADS / 32];
-};
-
-// Stable ranking of one chunk of up to TS_CHUNK keys by the digit at shift:
-// item (warp, k, lane) holds key[k]; pos[k] is its place in the chunk's digit
-// order; cnt (thread d) the chunk's count of digit d.  Same warp multisplit as
-// the device-wide sort's passes.
-__device__ __forceinline__ void rank_chunk(const uint32_t (&key)[TS_IPT], int shift, TileSortSmem& S,
-                                           uint32_t (&pos)[TS_IPT], uint32_t& cnt)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int q = threadIdx.x; q < (TS_THREADS / 32) * 256; q += TS_THREADS) (&S.whist[0][0])[q] = 0;
-    __syncthreads();
-    uint32_t rank[TS_IPT];
-#pragma unroll
-    for (int k = 0; k < TS_IPT; ++k) {
-        const uint32_t d = (key[k] >> shift) & 0xffu;
-        uint32_t peers = 0xffffffffu;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const uint32_t bit = (d >> b) & 1u;
-            const uint32_t bal = __ballot_sync(0xffffffffu, bit);
-            peers &= bit ? bal : ~bal;
-        }
-        const uint32_t before = S.whist[warp][d];
-        __syncwarp();
-        if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
-        __syncwarp();
-        rank[k] = (d << 16) | (before + __popc(peers & lt_mask));
-    }
-    __syncthreads();
-    {
-        const int d = threadIdx.x;
-        uint32_t run = 0;
-#pragma unroll
-        for (int w = 0; w < TS_THREADS / 32; ++w) {
-            const uint32_t x = S.whist[w][d];
-            S.whist[w][d] = run;
-            run += x;
-        }
-        cnt = run;
-        uint32_t tot;
-        S.lstart[d] = block_excl_scan<TS_THREADS>(run, S.s_warp, tot);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < TS_IPT; ++k) {
-        const uint32_t d = rank[k] >> 16;
-        pos[k] = S.lstart[d] + S.whist[warp][d] + (rank[k] & 0xffffu);
-    }
-}
-
-// One CTA per tile: its bucket sorted ascending (key_bits significant bits),
-// then the entries written.  A bucket of up to TS_CHUNK positions is sorted in
-// shared memory; a longer one by passes over global memory in chunks, with alt
-// (the same slots of a second buffer) as the other side of each pass.
-__global__ void __launch_bounds__(TS_THREADS)
-k_tile_sort(const int2* __restrict__ range, int key_bits, uint32_t* __restrict__ bucket, uint32_t* __restrict__ alt,
-            const GaussRec* __restrict__ rec, int N, uint64_t* __restrict__ keys, int32_t* __restrict__ vals)
-{
-    __shared__ TileSortSmem S;
-    const int t = blockIdx.x;
-    const int2 r = range[t];
-    const int n = r.y - r.x;
-    if (n <= 0) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int passes = (key_bits + 7) / 8;
-    auto item = [&](int k) { return warp * 256 + k * 32 + lane; };  // chunk index of item (warp, k, lane)
-    const uint32_t* sorted;  // the sorted positions, n of them
-    if (n <= TS_CHUNK) {
-        for (int q = threadIdx.x; q < TS_CHUNK; q += TS_THREADS) S.keys[q] = q < n ? bucket[r.x + q] : 0xffffffffu;
-        __syncthreads();
-        uint32_t* src = S.keys;
-        uint32_t* dst = S.keys2;
-        for (int p = 0; p < passes; ++p) {
-            uint32_t key[TS_IPT], pos[TS_IPT], cnt;
-#pragma unroll
-            for (int k = 0; k < TS_IPT; ++k) key[k] = src[item(k)];
-            rank_chunk(key, 8 * p, S, pos, cnt);
-#pragma unroll
-            for (int k = 0; k < TS_IPT; ++k) dst[pos[k]] = key[k];
-            __syncthreads();
-            uint32_t* x = src;
-            src = dst;
-            dst = x;
-        }
-        sorted = src;
-    } else {
-        uint32_t* src = bucket + r.x;
-        uint32_t* dst = alt + r.x;
-        for (int p = 0; p < passes; ++p) {
-            const int shift = 8 * p;
-            // the segment's digit counts, then each chunk ranked and placed after the
-            // earlier chunks' keys of the same digit (chunks in order: stable)
-            S.base[threadIdx.x] = 0;
-            __syncthreads();
-            for (int q = threadIdx.x; q < n; q += TS_THREADS) atomicAdd(&S.base[(src[q] >> shift) & 0xffu], 1u);
-            __syncthreads();
-            {
-                uint32_t tot;
-                const uint32_t b = block_excl_scan<TS_THREADS>(S.base[threadIdx.x], S.s_warp, tot);
-                S.base[threadIdx.x] = b;
-            }
-            __syncthreads();
-            for (int c0 = 0; c0 < n; c0 += TS_CHUNK) {
-                const int m = min(TS_CHUNK, n - c0);
-                uint32_t key[TS_IPT], pos[TS_IPT], cnt;
-#pragma unroll
-                for (int k = 0; k < TS_IPT; ++k) key[k] = item(k) < m ? src[c0 + item(k)] : 0xffffffffu;
-                rank_chunk(key, shift, S, pos, cnt);
-                // the padding (digit 255, after every real item of the chunk) is not written
-                const uint32_t pad = (uint32_t)(TS_CHUNK - m);
-#pragma unroll
-                for (int k = 0; k < TS_IPT; ++k) {
-                    if (item(k) < m) {
-                        const uint32_t d = (key[k] >> shift) & 0xffu;
-                        dst[S.base[d] + (pos[k] - S.lstart[d])] = key[k];
-                    }
-                }
-                __syncthreads();
-                if (threadIdx.x == 255) cnt -= pad;  // digit 255: the padding items sort last
-                S.base[threadIdx.x] += cnt;
-                __syncthreads();
-            }
-            uint32_t* x = src;
-            src = dst;
-            dst = x;
-            __syncthreads();
-        }
-        sorted = src;
-    }
-    for (int q = threadIdx.x; q < n; q += TS_THREADS) {
-        const uint32_t i = sorted[q];
-        int4 a = make_int4(0, 0, 0, -1), b = make_int4(0, 0, 0, 0);
-        if (i < (uint32_t)N) {
-            a = rec[i].a;
-            b = rec[i].b;
-        }
-        keys[r.x + q] = ((uint64_t)(uint32_t)t << 32) | (uint32_t)b.z;
-        vals[r.x + q] = a.w;
-    }
-}
-
 int tile_bits(int n_tiles) { return n_tiles > 1 ? 32 - __builtin_clz((unsigned)(n_tiles - 1)) : 0; }
 
 size_t a256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -1022,20 +663,20 @@ cudaError_t project_views(const Cam* cams, int V, int sh_degree, float softness,
     return cudaSuccess;
 }
 
-size_t gauss_bin_ws_bytes(int N, int cap, int T)
+size_t gauss_bin_ws_bytes(int N, int cap)
 {
-    int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1, t = T > 0 ? T : 1;
+    int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
     return scan_ws_bytes(n) + 3 * a256(sizeof(int32_t) * n) + 2 * a256(sizeof(uint64_t) * n) +
-           2 * a256(sizeof(int32_t) * n) + a256(sizeof(GaussRec) * n) + 256 + sort_ws_bytes(n > k ? n : k) +
-           2 * a256(sizeof(int32_t) * t) + 2 * a256(sizeof(uint32_t) * k);
+           2 * a256(sizeof(int32_t) * n) + a256(sizeof(GaussRec) * n) + 256 + sort_ws_bytes(n > k ? n : k);
 }
 
-// Tile binning of the Gaussians.  The entries' order (tile, depth, id): the N
-// Gaussians are sorted by depth (32 bits) first; after the mesh join each kept
-// (Gaussian, tile) pair goes to its tile's bucket and each tile's bucket is
-// sorted by depth-order position (the per-tile bucket sort above).  The first
-// half (depth sort, rectangles and ellipse tests, one record per position of
-// the depth order) needs no mesh; the second reads the records in order.
+// Tile binning of the Gaussians.  The entries' order (tile, depth, id) is
+// reached in two stable LSD sorts: the N Gaussians by depth (32 bits), then,
+// after emitting each Gaussian's tiles in that order, the K entries by tile
+// only (ceil(log2 T) bits) -- instead of one 32 + log2 T bit sort of K keys.
+// The first half (depth sort, rectangles and ellipse tests, one record per
+// position of the depth order) needs no mesh; the second (occlusion cull,
+// scan, emission, tile sort) reads the records in order, with no gathers.
 struct GaussWs {
     ScanWs sw;
     int32_t *counts, *offsets;
@@ -1044,13 +685,11 @@ struct GaussWs {
     int32_t *dval, *dval_alt, *n_dev;
     GaussRec* rec;
     SortWs so;
-    int32_t *tile_cnt, *cursor;
-    uint32_t *bucket, *bucket_alt;
 };
 
-static GaussWs carve_gauss_ws(void* ws, int N, int cap, int T)
+static GaussWs carve_gauss_ws(void* ws, int N, int cap)
 {
-    int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1, t = T > 0 ? T : 1;
+    int64_t n = N > 0 ? N : 1, k = cap > 0 ? cap : 1;
     GaussWs w;
     uint8_t* b = (uint8_t*)ws;
     b += carve_scan_ws(b, n, w.sw);
@@ -1072,21 +711,14 @@ static GaussWs carve_gauss_ws(void* ws, int N, int cap, int T)
     b += a256(sizeof(GaussRec) * n);
     w.n_dev = (int32_t*)b;
     b += 256;
-    b += carve_sort_ws(b, n > k ? n : k, w.so);
-    w.tile_cnt = (int32_t*)b;
-    b += a256(sizeof(int32_t) * t);
-    w.cursor = (int32_t*)b;
-    b += a256(sizeof(int32_t) * t);
-    w.bucket = (uint32_t*)b;
-    b += a256(sizeof(uint32_t) * k);
-    w.bucket_alt = (uint32_t*)b;
+    carve_sort_ws(b, n > k ? n : k, w.so);
     return w;
 }
 
 cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int32_t* radii, int cap,
                              int32_t* counters, void* ws, cudaStream_t s)
 {
-    GaussWs w = carve_gauss_ws(ws, N, cap, c.TW * c.TH);
+    GaussWs w = carve_gauss_ws(ws, N, cap);
     cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
     if (e != cudaSuccess || N <= 0) return e;
     k_gauss_depth_keys<<<(N + 255) / 256, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dkey,
@@ -1105,33 +737,9 @@ cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N,
                       const float* tile_far, const uint8_t* tile_full, uint64_t* keys, int32_t* gids,
                       int32_t* tile_range, int cap, int32_t* counters, void* ws, cudaStream_t s)
 {
-    const int T = c.TW * c.TH;
-    GaussWs w = carve_gauss_ws(ws, N, cap, T);
+    GaussWs w = carve_gauss_ws(ws, N, cap);
     cudaError_t e = cudaSuccess;
-    if (!getenv("GM_BIN_TILE_RADIX")) {
-        // per-tile buckets
-        if ((e = cudaMemsetAsync(w.tile_cnt, 0, sizeof(int32_t) * (size_t)T, s)) != cudaSuccess) return e;
-        if (N <= 0) {
-            if ((e = cudaMemsetAsync(counters + GM_CNT_K, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
-            return cudaMemsetAsync(tile_range, 0, sizeof(int32_t) * 2 * (size_t)T, s);
-        }
-        auto* s4 = reinterpret_cast<const float4*>(splats);
-        const int grid = (N + 255) / 256;
-        BinRule rule;
-        rule.cull = cull;
-        rule.soft = soft;
-        rule.tile_test = tile_test;
-        rule.tile_far = tile_far;
-        rule.tile_full = tile_full;
-        rule.TW = c.TW;
-        k_tile_count<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.kept, w.tile_cnt);
-        k_tile_offsets<<<1, 1024, 0, s>>>(T, w.tile_cnt, cap, counters, w.cursor, reinterpret_cast<int2*>(tile_range));
-        k_tile_scatter<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.kept, w.cursor, cap, w.bucket);
-        const int key_bits = N > 1 ? 32 - __builtin_clz((unsigned)(N - 1)) : 1;
-        k_tile_sort<<<T, TS_THREADS, 0, s>>>(reinterpret_cast<const int2*>(tile_range), key_bits, w.bucket,
-                                             w.bucket_alt, w.rec, N, keys, gids);
-        return cudaGetLastError();
-    }
+    const int T = c.TW * c.TH;
     const int tb = tile_bits(T);
     const int passes = sort_passes(32, 32 + tb);
     uint64_t* ek = passes % 2 ? w.so.keys_alt : keys;

@@ -221,7 +221,7 @@ cudaError_t project_bwd(const Cam& c, int sh_degree, int N, const float* means, 
                         const float* quats, const float* logits, const float* colors, const int32_t* radii,
                         const float* v_splats, const float* v_depth_model, bool accumulate, float* v_means,
                         float* v_log_scales, float* v_quats, float* v_logits, float* v_colors, cudaStream_t s);
-size_t gauss_bin_ws_bytes(int N, int cap, int T);
+size_t gauss_bin_ws_bytes(int N, int cap);
 // the two halves of gauss_bin_sort (same workspace, in this order, with nothing
 // else using the workspace in between): the depth pre-sort needs no mesh
 cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int32_t* radii, int cap,
