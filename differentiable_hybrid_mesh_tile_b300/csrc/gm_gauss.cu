@@ -26,6 +26,15 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
     dm = o0;
     rad = 0;
     touched = 0;
+    if (DEG >= 1) {
+        // the SH row is read only after the culling tests and the covariance: ask
+        // for its cache lines now (a row of 3 (DEG + 1)^2 floats spans at most two
+        // 128-byte lines), so that its loads later find them in L2
+        constexpr int ROW = 3 * (DEG + 1) * (DEG + 1);
+        const float* row = colors + (int64_t)g * ROW;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + ROW - 1));
+    }
     const float mx = __ldg(means + 3 * (int64_t)g), my = __ldg(means + 3 * (int64_t)g + 1),
                 mz = __ldg(means + 3 * (int64_t)g + 2);
     const float tx = fmaf(c.R[0], mx, fmaf(c.R[1], my, fmaf(c.R[2], mz, c.t[0])));
@@ -295,23 +304,45 @@ constexpr int SMALL_RECT = 16;
 // rectangle is not empty, all ones otherwise (it emits nothing and sorts last);
 // ids as values.  Needs no mesh, so it can run before the mesh layer exists.
 __global__ void __launch_bounds__(256)
+// The keys' digit histograms of the four 8-bit passes of the depth sort are
+// counted here (block sums in shared memory, then global atomics), and the
+// passes' look-back descriptors cleared (desc_words words from desc): the sort
+// needs no histogram pass over the keys.
 k_gauss_depth_keys(Cam c, int N, const float4* __restrict__ splats, const int32_t* __restrict__ radii,
-                   uint64_t* __restrict__ dkey, int32_t* __restrict__ dval, int32_t* n_dev)
+                   uint64_t* __restrict__ dkey, int32_t* __restrict__ dval, int32_t* n_dev,
+                   uint32_t* __restrict__ hist, uint32_t* __restrict__ desc, int max_parts)
 {
+    __shared__ uint32_t s_hist[4][256];
+    for (int t = threadIdx.x; t < 4 * 256; t += blockDim.x) (&s_hist[0][0])[t] = 0u;
+    // the passes' descriptors: pass p uses ceil(N / SORT_PART) * 256 words at p * max_parts * 256
+    const int64_t parts = ((int64_t)N + SORT_PART - 1) / SORT_PART, per = parts * 256;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < 4 * per;
+         t += (int64_t)gridDim.x * blockDim.x)
+        desc[(t / per) * (int64_t)max_parts * 256 + t % per] = 0u;
+    __syncthreads();
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     if (g == 0) *n_dev = N;
-    if (g >= N) return;
-    const int r = radii[g];
-    bool vis = false;
-    float depth = 0.0f;
-    if (r > 0) {
-        const float4 s0 = splats[3 * (int64_t)g];
-        depth = splats[3 * (int64_t)g + 2].y;
-        int x0, y0, x1, y1;
-        vis = gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1);
+    if (g < N) {
+        const int r = radii[g];
+        bool vis = false;
+        float depth = 0.0f;
+        if (r > 0) {
+            const float4 s0 = splats[3 * (int64_t)g];
+            depth = splats[3 * (int64_t)g + 2].y;
+            int x0, y0, x1, y1;
+            vis = gauss_rect(c, s0.x, s0.y, r, x0, y0, x1, y1);
+        }
+        const uint32_t key = vis ? __float_as_uint(depth) : 0xffffffffu;
+        dkey[g] = (uint64_t)key;
+        dval[g] = g;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 0xffu], 1u);
     }
-    dkey[g] = vis ? (uint64_t)__float_as_uint(depth) : 0xffffffffull;
-    dval[g] = g;
+    __syncthreads();
+    for (int t = threadIdx.x; t < 4 * 256; t += blockDim.x) {
+        const uint32_t v = (&s_hist[0][0])[t];
+        if (v) atomicAdd(hist + t, v);
+    }
 }
 
 // What the binning keeps of a Gaussian, one record per position of the depth
@@ -721,11 +752,12 @@ cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int
     GaussWs w = carve_gauss_ws(ws, N, cap);
     cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
     if (e != cudaSuccess || N <= 0) return e;
+    if ((e = clear_sort_hist(w.so, s)) != cudaSuccess) return e;
     k_gauss_depth_keys<<<(N + 255) / 256, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dkey,
-                                                        w.dval, w.n_dev);
+                                                        w.dval, w.n_dev, w.so.hist, w.so.desc, w.so.max_parts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4 passes: even, the result is back in dkey / dval
-    e = radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s);
+    e = radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s, true);
     if (e != cudaSuccess) return e;
     k_gauss_shape<<<(N + 255) / 256, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dval,
                                                    w.rec, counters);

@@ -171,9 +171,16 @@ cudaError_t exclusive_scan(const int32_t* counts, const int32_t* idx, int32_t* o
 // up sets GM_FLAG_TIMEOUT in counters.  Input is in (k0, v0); the result is
 // in (k0, v0) when the number of passes is even and in the alternate buffers
 // otherwise -- sort_passes() tells which.
+// have_hist: the caller counted every pass's digit histogram into ws.hist
+// (zeroed first by clear_sort_hist, which also resets the passes' tickets) and
+// zeroed the passes' look-back descriptors (for pass p, the n_parts * 256 words
+// at ws.desc + p * ws.max_parts * 256, n_parts = ceil(n / SORT_PART)); else the
+// sort does both itself.
 int sort_passes(int begin_bit, int end_bit);
 cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int cap, int begin_bit,
-                       int end_bit, const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s);
+                       int end_bit, const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s,
+                       bool have_hist = false);
+cudaError_t clear_sort_hist(const SortWs& ws, cudaStream_t s);
 // tile_range[T][2] from sorted keys (tile id in the high 32 bits); range zeroed first
 cudaError_t tile_ranges(const uint64_t* keys, int cap, const int32_t* counters, int32_t* tile_range,
                         int n_tiles, cudaStream_t s);

@@ -343,18 +343,24 @@ int sort_passes(int begin_bit, int end_bit)
     return end_bit > begin_bit ? (end_bit - begin_bit + 7) / 8 : 0;
 }
 
+cudaError_t clear_sort_hist(const SortWs& ws, cudaStream_t s)
+{
+    return cudaMemsetAsync(ws.hist, 0, (uint8_t*)ws.desc - (uint8_t*)ws.hist, s);  // histograms and tickets
+}
+
 cudaError_t radix_sort(uint64_t* k0, int32_t* v0, uint64_t* k1, int32_t* v1, int cap, int begin_bit, int end_bit,
-                       const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s)
+                       const int32_t* n_dev, int32_t* counters, const SortWs& ws, cudaStream_t s, bool have_hist)
 {
     const int passes = sort_passes(begin_bit, end_bit);
     if (passes == 0 || cap <= 0) return cudaSuccess;
     if (passes > SORT_MAX_PASSES) return cudaErrorInvalidValue;
-    size_t zero = (uint8_t*)ws.desc - (uint8_t*)ws.hist;  // histograms and tickets
-    cudaError_t e = cudaMemsetAsync(ws.hist, 0, zero, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     const int sms = num_sms();
-    int hgrid = (int)std::min<int64_t>(((int64_t)cap + 255) / 256, (int64_t)sms * 4);
-    k_hist<<<hgrid, 256, 0, s>>>(k0, n_dev, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
+    if (!have_hist) {
+        if ((e = clear_sort_hist(ws, s)) != cudaSuccess) return e;
+        int hgrid = (int)std::min<int64_t>(((int64_t)cap + 255) / 256, (int64_t)sms * 4);
+        k_hist<<<hgrid, 256, 0, s>>>(k0, n_dev, cap, begin_bit, passes, ws.hist, ws.desc, ws.max_parts);
+    }
     k_hist_scan<<<1, 256, 0, s>>>(ws.hist, passes);
     e = onesweep_attr();
     if (e != cudaSuccess) return e;
