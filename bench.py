@@ -168,6 +168,7 @@ PROFILED = {
         "kernel": "k_composite_fwd",
         "dram_bytes": 86685184 + 96054784,
         "smem_wavefronts": 28375157,
+        "warp_instructions": 327398405,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
                 "f739810c0b99f11e23ceaa04b208f267f0ffe7d60ed068919e2d53b61e2a3ff6",
@@ -177,6 +178,7 @@ PROFILED = {
         "kernel": "k_composite_bwd",
         "dram_bytes": 186321664 + 11989760,
         "smem_wavefronts": 74898058,
+        "warp_instructions": 639191346,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
                 "f739810c0b99f11e23ceaa04b208f267f0ffe7d60ed068919e2d53b61e2a3ff6",
@@ -409,13 +411,20 @@ def run_gm(args, ws, rank, local):
                          "frac": ach / alu_peak, "algorithmic": amount}
     stages["zbuffer"] = {"bound": "alu", "ms": stage_ms["zbuffer"], "note": "reported, no target"}
     # compositing's shared-memory side: wavefronts of one launch (ncu) against one
-    # wavefront per SM per clock over the stage's measured time
+    # wavefront per SM per clock over the stage's measured time; and its instruction
+    # issue: warp instructions of one launch against four schedulers per SM issuing
+    # one each per clock (the bound these kernels meet)
     for k in ("composite_fwd", "composite_bwd"):
         wf = profiled(k, "smem_wavefronts")
         if wf is not None:
             cap = sms * clk_mhz * 1e6 * stage_ms[k] / 1e3
             stages[k]["smem"] = {"wavefronts": wf, "peak_per_s": sms * clk_mhz * 1e6, "frac": wf / cap,
                                  "source": "ncu capture of the same kernel source (wavefronts per launch)"}
+        wi = profiled(k, "warp_instructions")
+        if wi is not None:
+            cap = 4 * sms * clk_mhz * 1e6 * stage_ms[k] / 1e3
+            stages[k]["issue"] = {"warp_instructions": wi, "peak_per_s": 4 * sms * clk_mhz * 1e6, "frac": wi / cap,
+                                  "source": "ncu capture of the same kernel source (instructions per launch)"}
     for k in stages:
         stages[k]["ms_median_p10_p90"] = spread[k]
     # the tile-list rasterizer (not in the step: the renderer's default is the

@@ -320,9 +320,10 @@ k_gauss_depth_keys(Cam c, int N, const float4* __restrict__ splats, const int32_
          t += (int64_t)gridDim.x * blockDim.x)
         desc[(t / per) * (int64_t)max_parts * 256 + t % per] = 0u;
     __syncthreads();
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;
-    if (g == 0) *n_dev = N;
-    if (g < N) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *n_dev = N;
+    // a grid of a few CTAs per SM, each over many Gaussians, so that the block sums
+    // reach the global histograms with few atomics
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < N; g += gridDim.x * blockDim.x) {
         const int r = radii[g];
         bool vis = false;
         float depth = 0.0f;
@@ -753,8 +754,9 @@ cudaError_t gauss_depth_sort(const Cam& c, int N, const float* splats, const int
     cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
     if (e != cudaSuccess || N <= 0) return e;
     if ((e = clear_sort_hist(w.so, s)) != cudaSuccess) return e;
-    k_gauss_depth_keys<<<(N + 255) / 256, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dkey,
-                                                        w.dval, w.n_dev, w.so.hist, w.so.desc, w.so.max_parts);
+    const int kgrid = (int)std::min<int64_t>(((int64_t)N + 255) / 256, (int64_t)num_sms() * 4);
+    k_gauss_depth_keys<<<kgrid, 256, 0, s>>>(c, N, reinterpret_cast<const float4*>(splats), radii, w.dkey, w.dval,
+                                             w.n_dev, w.so.hist, w.so.desc, w.so.max_parts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4 passes: even, the result is back in dkey / dval
     e = radix_sort(w.dkey, w.dval, w.dkey_alt, w.dval_alt, N, 0, 32, w.n_dev, counters, w.so, s, true);
