@@ -171,7 +171,7 @@ PROFILED = {
         "warp_instructions": 327398405,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "f739810c0b99f11e23ceaa04b208f267f0ffe7d60ed068919e2d53b61e2a3ff6",
+                "b11240fb5b2a1b31534a279027391a779b76ed44d6104793dc2a6ccb66bafaf4",
         },
     },
     "composite_bwd": {
@@ -181,7 +181,7 @@ PROFILED = {
         "warp_instructions": 639191346,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "f739810c0b99f11e23ceaa04b208f267f0ffe7d60ed068919e2d53b61e2a3ff6",
+                "b11240fb5b2a1b31534a279027391a779b76ed44d6104793dc2a6ccb66bafaf4",
         },
     },
 }

@@ -518,9 +518,11 @@ __device__ __forceinline__ float moment(int n, int i, int j)
 // The backward pass takes each batch of a tile's staged records (written by
 // the forward pass in list order) with bulk copies (cp.async.bulk, the TMA
 // engine's linear mode) into shared memory: one thread issues the copies of a
-// batch, an mbarrier counts their bytes, and the next batch's copies are in
-// flight while the CTA works on the current one (two buffers).  The source is
-// always this GPU's own record buffer.
+// batch and an mbarrier counts their bytes.  With two buffers the next batch's
+// copies are in flight while the CTA works on the current one; with one (the
+// tensor-core form, whose staging needs the shared memory) they start after the
+// CTA is done with the previous batch, while the other CTAs of the SM run.  The
+// source is always this GPU's own record buffer.
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -553,8 +555,8 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Waits for the phase of the given parity, at most about GM_COPY_WAIT_NS
-// nanoseconds; false when it gave up.
+// Waits for the phase of the given parity, at most about COPY_WAIT_NS
+// nanoseconds (by the global timer); false when it gave up.
 constexpr uint64_t COPY_WAIT_NS = 1000000000ull;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
@@ -591,12 +593,14 @@ __device__ uint32_t g_copy_status = 0;
 
 namespace {
 
-// Eight CTAs of 128 threads per SM (64 registers a thread), seven with the
-// bulk-copied records' second buffer (the shared memory of the hard split's
-// tensor-core staging bounds it): the kernel is bound by instruction issue,
-// and resident warps hide the latencies.  BULK: the records come from the
-// forward pass's staged records by bulk copies into two buffers; otherwise
-// each thread gathers and stages one record per batch.
+// The kernel is bound by instruction issue, and resident warps hide its
+// latencies: the hard split runs ten CTAs of 128 threads per SM (48 registers,
+// 20.6 KB of shared memory with the tensor-core staging), nine with the shuffle
+// sums and two record buffers, the soft split eight (64 registers: four more
+// terms per entry).  BULK: the records come from the forward pass's staged
+// records by bulk copies; otherwise each thread gathers and stages one record
+// per batch.  MMA: the warp sums of a group of entries on the tensor cores (hard
+// split); otherwise by the shuffle reduce-scatter into a per-CTA accumulator.
 template <bool STATS, bool SOFT, bool BULK, bool MMA>
 __global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : (BULK && !MMA ? 9 : 10))
 k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
