@@ -7,8 +7,10 @@
 // shared memory in batches of 128.
 //
 // Each warp first asks, per staged record, whether the Gaussian's ellipse of
-// alpha >= 1/255 meets its 8 x 4 pixel block, and then visits only those
-// records (the other pairs would be skipped anyway).
+// alpha >= 1/255 meets its 8 x 4 pixel block, lists those records in shared
+// memory, and then visits only them (the other pairs would be skipped anyway),
+// every lane evaluating every listed record and keeping, by selects rather than
+// branches, what applies to its pixel.
 //
 // Half-tile CTAs: the warps of a CTA wait for one another at every batch and
 // at exit, so the slowest 8 x 4 block holds the CTA; four blocks per CTA
@@ -29,6 +31,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr int CTA_WARPS = 4;                  // 8 x 4 blocks per CTA: half a tile
 constexpr int CTA_THREADS = 32 * CTA_WARPS;   // = staging batch
 constexpr int CTAS_PER_TILE = 8 / CTA_WARPS;
+constexpr uint8_t NO_HIT = 0xff;              // padding of a warp's hit list
 
 // Staged records of a tile list (one per list position, three float4 arrays,
 // a fourth with the soft split's depth model): written by the forward pass,
@@ -231,8 +234,10 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
 {
     __shared__ float4 sA[CTA_THREADS], sB[CTA_THREADS], sC[CTA_THREADS];
     __shared__ float4 sD[SOFT ? CTA_THREADS : 1];
+    __shared__ uint8_t sList[CTA_WARPS][CTA_THREADS + 2];  // each warp's hits of the current batch
     int tile;
     const PixelMap pm = pixel_of(c, tile);
+    const int lane = threadIdx.x & 31;
     const bool inside = pm.i < c.W && pm.j < c.H;
     const int64_t pix = (int64_t)pm.j * c.W + pm.i;
     const float px = (float)pm.i + 0.5f, py = (float)pm.j + 0.5f;
@@ -279,68 +284,65 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             }
         }
         __syncthreads();
-        // walk this warp's hits: a ballot per 32 staged records marks those that can
-        // reach its pixels; the warp visits only those, in list order
+        // this warp's hits of the batch (the staged records whose ellipse reaches its
+        // block), listed front to back and padded with NO_HIT to whole pairs
+        uint8_t* __restrict__ L = sList[threadIdx.x >> 5];
+        int cnt = 0;
         for (int m = 0; m * 32 < n; ++m) {
+            const int kk = m * 32 + lane;
+            const bool hit = kk < n && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0) && !(SOFT && sD[kk].w > Dw);
+            const uint32_t mask = __ballot_sync(0xffffffffu, hit);
+            if (hit) L[cnt + __popc(mask & ((1u << lane) - 1u))] = (uint8_t)kk;
+            cnt += __popc(mask);
+        }
+        if (lane < 2) L[cnt + lane] = NO_HIT;
+        __syncwarp();
+        const int pos0 = b - r.x;  // list position of staged record 0
+        for (int p = 0; p < cnt; p += 2) {
             if (__all_sync(0xffffffffu, done)) break;
-            const int kk = m * 32 + (threadIdx.x & 31);
-            uint32_t mask =
-                __ballot_sync(0xffffffffu, kk < n && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0) &&
-                                               !(SOFT && sD[kk].w > Dw));
-            while (mask) {
-                // two hits at a time: both evaluated (independent) before the
-                // transmittance chain takes them in list order
-                int kk2[2];
-                kk2[0] = m * 32 + __ffs(mask) - 1;
-                mask &= mask - 1;
-                kk2[1] = -1;
-                if (mask) {
-                    kk2[1] = m * 32 + __ffs(mask) - 1;
-                    mask &= mask - 1;
-                }
-                if (done) continue;
-                float4 Cq[2], Bq[2];
-                Eval ev[2];
+            // two hits at a time, both evaluated before the transmittance chain takes
+            // them in list order; every lane evaluates both and keeps what applies to
+            // its pixel (a NO_HIT entry reads a staged record and keeps nothing)
+            const uint32_t k2 = *reinterpret_cast<const uint16_t*>(L + p);
+            const int kq[2] = {(int)(k2 & 0xffu), (int)(k2 >> 8)};
+            float4 Cq[2], Bq[2];
+            Eval ev[2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int k = kk2[h] < 0 ? kk2[0] : kk2[h];
-                    Cq[h] = sC[k];
-                    const float4 A = sA[k];
-                    Bq[h] = sB[k];
-                    ev[h] = eval_splat(A, Bq[h], px, py);
-                }
+            for (int h = 0; h < 2; ++h) {
+                const int ks = kq[h] & (CTA_THREADS - 1);
+                Cq[h] = sC[ks];
+                const float4 A = sA[ks];
+                Bq[h] = sB[ks];
+                ev[h] = eval_splat(A, Bq[h], px, py);
+            }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (done || kk2[h] < 0) continue;
-                    // hard test, sorted by depth: once a Gaussian is not in front of the
-                    // mesh, none after it is
-                    if (!soft && !(Cq[h].y < D)) {
-                        done = true;
-                        continue;
-                    }
-                    if (STATS) ++visited;
-                    if (ev[h].skip) continue;
-                    float a = ev[h].alpha;
-                    if (soft) {  // the Gaussian's part in front of the mesh
-                        const float4 Dm = sD[kk2[h]];
-                        const float zs = fmaf(Dm.x, ev[h].dx, fmaf(Dm.y, ev[h].dy, Cq[h].y));
-                        a *= sp.front((D - zs) * Dm.z);
-                        if (a < ALPHA_MIN) continue;
-                    }
-                    const float Tn = __fmul_rn(T, __fsub_rn(1.0f, a));
-                    if (Tn <= T_STOP) {
-                        done = true;
-                        continue;
-                    }
-                    const float w = a * T;
-                    Cr = fmaf(w, Bq[h].z, Cr);
-                    Cg = fmaf(w, Bq[h].w, Cg);
-                    Cb = fmaf(w, Cq[h].x, Cb);
-                    Z = fmaf(w, Cq[h].y, Z);
-                    T = Tn;
-                    last = b - r.x + kk2[h] + 1;
-                    if (STATS) ++blended;
+            for (int h = 0; h < 2; ++h) {
+                const bool live = kq[h] != NO_HIT && !done;
+                // hard test, sorted by depth: once a Gaussian is not in front of the
+                // mesh, none after it is
+                const bool occluded = !soft && !(Cq[h].y < D);
+                if (STATS) visited += live && !occluded;
+                done = done || (live && occluded);
+                bool use = live && !occluded && !ev[h].skip;
+                float a = ev[h].alpha;
+                if (SOFT && soft && use) {  // the Gaussian's part in front of the mesh
+                    const float4 Dm = sD[kq[h]];
+                    const float zs = fmaf(Dm.x, ev[h].dx, fmaf(Dm.y, ev[h].dy, Cq[h].y));
+                    a *= sp.front((D - zs) * Dm.z);
+                    use = a >= ALPHA_MIN;
                 }
+                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, a));
+                const bool stop = Tn <= T_STOP;
+                done = done || (use && stop);
+                const bool blend = use && !stop;
+                const float w = a * T;
+                Cr = blend ? fmaf(w, Bq[h].z, Cr) : Cr;
+                Cg = blend ? fmaf(w, Bq[h].w, Cg) : Cg;
+                Cb = blend ? fmaf(w, Cq[h].x, Cb) : Cb;
+                Z = blend ? fmaf(w, Cq[h].y, Z) : Z;
+                T = blend ? Tn : T;
+                last = blend ? pos0 + kq[h] + 1 : last;
+                if (STATS) blended += blend;
             }
         }
     }
@@ -475,7 +477,6 @@ struct RedSmem {
     float ds[RGROUP][RPAD];  // [group slot][pixel] dL/d sigma
     float w[RGROUP][RPAD];   // [group slot][pixel] alpha T_front
     float2 gf[4][32];        // B fragments (b0, b1) of the upstream gradient, per 8-pixel k-block
-    int kid[RGROUP];         // the group's staged entries (-1: none)
 };
 
 __device__ __forceinline__ uint32_t to_tf32(float x)
@@ -595,7 +596,7 @@ namespace {
 
 // The kernel is bound by instruction issue, and resident warps hide its
 // latencies: the hard split runs ten CTAs of 128 threads per SM (48 registers,
-// 20.6 KB of shared memory with the tensor-core staging), nine with the shuffle
+// 20.5 KB of shared memory with the tensor-core staging and the hit lists), nine with the shuffle
 // sums and two record buffers, the soft split eight (64 registers: four more
 // terms per entry).  BULK: the records come from the forward pass's staged
 // records by bulk copies; otherwise each thread gathers and stages one record
@@ -630,6 +631,8 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     // B fragments (b0, b1) per k-block and lane, shared by the warps
     __shared__ __align__(16) RedSmem sRed[MMA ? CTA_WARPS : 1];
     __shared__ __align__(16) float2 sMf[MMA ? 4 : 1][32];
+    // hard split: each warp's hits of the current batch (staged entry indices)
+    __shared__ uint8_t sList[MMA ? CTA_WARPS : 1][MMA ? CTA_THREADS + RGROUP : 1];
     int tile;
     const PixelMap pm = pixel_of(c, tile);
     const int lane = threadIdx.x & 31;
@@ -798,56 +801,56 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         // they are taken four at a time from the back
         const int k_top = min(n, warp_last - (b0 - r.x)) - 1;
         if constexpr (MMA) {
-            // groups of eight hits, filled across the 32-entry chunks (back to front)
+            // the warp's hits of this batch (entries up to k_top whose ellipse reaches
+            // its block), listed back to front, padded with NO_HIT to whole groups
             RedSmem& R = sRed[threadIdx.x >> 5];
-            int m = k_top >> 5;
-            auto chunk_hits = [&](int mm) {
-                const int kk = mm * 32 + lane;
-                return __ballot_sync(0xffffffffu, kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0));
-            };
-            uint32_t mask = m >= 0 ? chunk_hits(m) : 0u;
-            for (;;) {
-                while (!mask && m > 0) mask = chunk_hits(--m);
-                if (!mask) break;
-                // per entry of the group, back to front: w = alpha T_front and
-                // ds = dL/d sigma at this lane's pixel, staged for the contraction
+            uint8_t* __restrict__ L = sList[threadIdx.x >> 5];
+            int cnt = 0;
+            for (int m = k_top >> 5; m >= 0; --m) {
+                const int kk = m * 32 + lane;
+                const bool hit = kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0);
+                const uint32_t mask = __ballot_sync(FULL, hit);
+                // hits above this lane in the chunk come first
+                if (hit) L[cnt + __popc(mask >> lane) - 1] = (uint8_t)kk;
+                cnt += __popc(mask);
+            }
+            if (lane < RGROUP) L[cnt + lane] = NO_HIT;
+            __syncwarp();
+            const int pos0 = b0 - r.x;  // list position of staged entry 0
+            for (int base = 0; base < cnt; base += RGROUP) {
+                // per entry of the group, back to front: w = alpha T_front and ds =
+                // dL/d sigma at this lane's pixel, staged for the contraction.  Every
+                // lane evaluates every entry (most groups' entries reach some lane of
+                // the block) and keeps the result where the entry is composited there.
                 bool any = false;
-#pragma unroll 1
+#pragma unroll
                 for (int jj = 0; jj < RGROUP; ++jj) {
-                    while (!mask && m > 0) mask = chunk_hits(--m);
-                    int k = -1;
-                    if (mask) {
-                        const int bit = 31 - __clz(mask);
-                        k = m * 32 + bit;
-                        mask &= ~(1u << bit);
+
+                    const int k = L[base + jj];
+
+                    const int ks = k & (CTA_THREADS - 1);  // NO_HIT reads a staged record and keeps nothing
+                    const float4 C3 = sC[ks], A = sA[ks], B = sB[ks];
+                    const Eval e = eval_splat(A, B, px, py);
+                    // positions before the pixel's last composited one are all in front of the mesh
+                    const bool seen = k != NO_HIT && pos0 + k < last && C3.y < D;
+                    const bool take = seen && !e.skip;
+                    if (STATS) {
+                        visited += seen;
+                        contributed += take;
                     }
-                    if (lane == 0) R.kid[jj] = k;
-                    float w = 0.0f, ds = 0.0f;
-                    if (k >= 0 && inside && b0 - r.x + k < last) {
-                        const float4 C3 = sC[k];
-                        if (C3.y < D) {
-                            if (STATS) ++visited;
-                            const float4 A = sA[k], B = sB[k];
-                            const Eval e = eval_splat(A, B, px, py);
-                            if (!e.skip) {
-                                if (STATS) ++contributed;
-                                any = true;
-                                const float a = e.alpha;
-                                const float rom = __fdividef(1.0f, 1.0f - a);
-                                const float Tp = T * rom;  // transmittance in front of it
-                                w = a * Tp;
-                                const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
-                                const float dLda = Tp * front + (aterm - behind) * rom;
-                                behind = fmaf(w, front, behind);
-                                T = Tp;
-                                // alpha clamped at 0.99 has no opacity / sigma gradient;
-                                // elsewhere d alpha / d sigma = -alpha
-                                if (!e.clamped) ds = -dLda * a;
-                            }
-                        }
-                    }
-                    R.ds[jj][lane] = ds;
-                    R.w[jj][lane] = w;
+                    const float a = e.alpha;
+                    const float rom = __fdividef(1.0f, 1.0f - a);
+                    const float Tp = T * rom;  // transmittance in front of it
+                    const float w = a * Tp;
+                    const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
+                    const float dLda = Tp * front + (aterm - behind) * rom;
+                    behind = take ? fmaf(w, front, behind) : behind;
+                    T = take ? Tp : T;
+                    any |= take;
+                    // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
+                    // d alpha / d sigma = -alpha
+                    R.ds[jj][lane] = take && !e.clamped ? -dLda * a : 0.0f;
+                    R.w[jj][lane] = take ? w : 0.0f;
                 }
                 if (__any_sync(FULL, any)) {
                     __syncwarp();
@@ -873,8 +876,8 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                     const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
                     const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
                     const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
-                    const int k = R.kid[g];
-                    const int gid = k >= 0 ? rec_id(sC[k]) : -1;
+                    const int k = L[base + g];
+                    const int gid = k != NO_HIT ? rec_id(sC[k]) : -1;
                     if (c == 0 && gid >= 0) {
                         // with dx = u + i, dy = v + j (u, v at the block's first pixel):
                         //   sum ds dx = u S0 + Si, sum ds dy = v S0 + Sj,
