@@ -317,7 +317,7 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const bool live = kq[h] != NO_HIT && !done;
+                const bool live = (h == 0 || kq[h] != NO_HIT) && !done;  // only the second can be padding
                 // hard test, sorted by depth: once a Gaussian is not in front of the
                 // mesh, none after it is
                 const bool occluded = !soft && !(Cq[h].y < D);
@@ -465,17 +465,29 @@ __device__ __forceinline__ void flush_grad_soft(float* __restrict__ v_splats, fl
 // (m16n8k8).  With dx = u + i, dy = v + j (u, v the entry's offset at the
 // block's first pixel, i, j the pixel's place in the 8 x 4 block) the six
 // pixel moments 1, i, j, i^2, i j, j^2 of ds give every ds term.  Each fp32
-// value x enters as two tf32 values, hi = tf32(x) and lo = tf32(x - hi)
-// (rows g and g + 8 of the A operand), which keeps about 22 bits; the moments
-// are small integers, exact in tf32, and the upstream gradient is split the
-// same way (columns 0..3 hi, 4..7 lo).
+// value x enters as two tf32 values (rows g and g + 8 of the A operand): hi =
+// x with its 13 low mantissa bits cleared, and lo = x - hi (exact in fp32)
+// cleared the same way, which keeps about 20 bits (|x - hi - lo| <= 2^-20 |x|);
+// a bit mask costs one instruction where a rounding conversion costs several.
+// The moments are small integers, exact in tf32, and the upstream gradient is
+// split once per CTA with rounding conversions (columns 0..3 hi, 4..7 lo).
 
 constexpr int RGROUP = 8;  // entries per tensor-core group
-constexpr int RPAD = 36;   // row stride of the per-warp staging (conflict-free fragment loads)
+constexpr int RPAD = 40;   // row stride of the per-warp staging (conflict-free 8-byte fragment loads)
+
+// The staging rows hold a warp's 32 pixels in fragment order: pixel q * 8 + i
+// (k-block q, i < 8) at column q * 8 + 2 i for i < 4 and q * 8 + 2 (i - 4) + 1
+// otherwise, so that the two pixels c and c + 4 of a lane's A fragment are
+// adjacent (one 8-byte load).
+__device__ __forceinline__ int frag_col(int pixel)
+{
+    const int i = pixel & 7;
+    return (pixel & ~7) + (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+}
 
 struct RedSmem {
-    float ds[RGROUP][RPAD];  // [group slot][pixel] dL/d sigma
-    float w[RGROUP][RPAD];   // [group slot][pixel] alpha T_front
+    float ds[RGROUP][RPAD];  // [group slot][frag_col(pixel)] dL/d sigma
+    float w[RGROUP][RPAD];   // [group slot][frag_col(pixel)] alpha T_front
     float2 gf[4][32];        // B fragments (b0, b1) of the upstream gradient, per 8-pixel k-block
 };
 
@@ -497,14 +509,17 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // One 8-pixel k-block of the A operand: rows g (hi) and g + 8 (lo) of group
-// slot g at pixels kb * 8 + c and kb * 8 + c + 4.
+// slot g at pixels kb * 8 + c and kb * 8 + c + 4 (columns p = kb * 8 + 2 c and
+// p + 1 of the staging).
 __device__ __forceinline__ void a_frag(const float (&m)[RGROUP][RPAD], int g, int p, uint32_t (&a)[4])
 {
-    const float x0 = m[g][p], x1 = m[g][p + 4];
-    a[0] = to_tf32(x0);
-    a[1] = to_tf32(x0 - __uint_as_float(a[0]));
-    a[2] = to_tf32(x1);
-    a[3] = to_tf32(x1 - __uint_as_float(a[2]));
+    const float2 x = *reinterpret_cast<const float2*>(&m[g][p]);
+    const float x0 = x.x, x1 = x.y;
+    a[0] = __float_as_uint(x0) & 0xffffe000u;
+    a[1] = __float_as_uint(x0 - __uint_as_float(a[0])) & 0xffffe000u;
+    a[2] = __float_as_uint(x1) & 0xffffe000u;
+    a[3] = __float_as_uint(x1 - __uint_as_float(a[2])) & 0xffffe000u;
+
 }
 
 // pixel moment n (1, i, j, i^2, i j, j^2, 0, 0) of the pixel at (i, j)
@@ -816,7 +831,11 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             }
             if (lane < RGROUP) L[cnt + lane] = NO_HIT;
             __syncwarp();
-            const int pos0 = b0 - r.x;  // list position of staged entry 0
+            // entries [0, lastk) of the batch lie before the pixel's last composited one
+            // (all of them in front of the mesh, which ended the pixel's forward chain);
+            // NO_HIT >= CTA_THREADS >= lastk
+            const int lastk = min(last - (b0 - r.x), CTA_THREADS);
+            const int col = frag_col(lane);
             for (int base = 0; base < cnt; base += RGROUP) {
                 // per entry of the group, back to front: w = alpha T_front and ds =
                 // dL/d sigma at this lane's pixel, staged for the contraction.  Every
@@ -825,14 +844,11 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 bool any = false;
 #pragma unroll
                 for (int jj = 0; jj < RGROUP; ++jj) {
-
                     const int k = L[base + jj];
-
                     const int ks = k & (CTA_THREADS - 1);  // NO_HIT reads a staged record and keeps nothing
                     const float4 C3 = sC[ks], A = sA[ks], B = sB[ks];
                     const Eval e = eval_splat(A, B, px, py);
-                    // positions before the pixel's last composited one are all in front of the mesh
-                    const bool seen = k != NO_HIT && pos0 + k < last && C3.y < D;
+                    const bool seen = k < lastk;
                     const bool take = seen && !e.skip;
                     if (STATS) {
                         visited += seen;
@@ -849,8 +865,8 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                     any |= take;
                     // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
                     // d alpha / d sigma = -alpha
-                    R.ds[jj][lane] = take && !e.clamped ? -dLda * a : 0.0f;
-                    R.w[jj][lane] = take ? w : 0.0f;
+                    R.ds[jj][col] = take && !e.clamped ? -dLda * a : 0.0f;
+                    R.w[jj][col] = take ? w : 0.0f;
                 }
                 if (__any_sync(FULL, any)) {
                     __syncwarp();
@@ -860,9 +876,9 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                     for (int q = 0; q < 4; ++q) {
                         uint32_t a[4];
                         const float2 bm = sMf[q][lane], bg = R.gf[q][lane];
-                        a_frag(R.ds, g, q * 8 + c, a);
+                        a_frag(R.ds, g, q * 8 + 2 * c, a);
                         mma_tf32(dm, a[0], a[1], a[2], a[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
-                        a_frag(R.w, g, q * 8 + c, a);
+                        a_frag(R.w, g, q * 8 + 2 * c, a);
                         mma_tf32(dc, a[0], a[1], a[2], a[3], __float_as_uint(bg.x), __float_as_uint(bg.y));
                     }
                     // lane (g, c): group slot g, terms 2c and 2c + 1 (hi rows + lo rows):
