@@ -166,22 +166,22 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 PROFILED = {
     "composite_fwd": {
         "kernel": "k_composite_fwd",
-        "dram_bytes": 86685184 + 96054784,
-        "smem_wavefronts": 28375157,
-        "warp_instructions": 327398405,
+        "dram_bytes": 86578688 + 96558848,
+        "smem_wavefronts": 34879233,
+        "warp_instructions": 262407224,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "b11240fb5b2a1b31534a279027391a779b76ed44d6104793dc2a6ccb66bafaf4",
+                "f5fc079eb7d174e9a112d70793eaed347e7128e06119b57e3373522da375fd33",
         },
     },
     "composite_bwd": {
         "kernel": "k_composite_bwd",
-        "dram_bytes": 186321664 + 11989760,
-        "smem_wavefronts": 74898058,
-        "warp_instructions": 639191346,
+        "dram_bytes": 186315776 + 12181248,
+        "smem_wavefronts": 79798525,
+        "warp_instructions": 421492889,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "b11240fb5b2a1b31534a279027391a779b76ed44d6104793dc2a6ccb66bafaf4",
+                "f5fc079eb7d174e9a112d70793eaed347e7128e06119b57e3373522da375fd33",
         },
     },
 }
