@@ -10,7 +10,10 @@
 // alpha >= 1/255 meets its 8 x 4 pixel block, lists those records in shared
 // memory, and then visits only them (the other pairs would be skipped anyway),
 // every lane evaluating every listed record and keeping, by selects rather than
-// branches, what applies to its pixel.
+// branches, what applies to its pixel.  With staged records the forward pass
+// also writes each warp's lists out, and the backward pass (hard split) takes
+// the forward's batches in reverse with those lists instead of testing the
+// records again.
 //
 // Half-tile CTAs: the warps of a CTA wait for one another at every batch and
 // at exit, so the slowest 8 x 4 block holds the CTA; four blocks per CTA
@@ -36,11 +39,16 @@ constexpr uint8_t NO_HIT = 0xff;              // padding of a warp's hit list
 // Staged records of a tile list (one per list position, three float4 arrays,
 // a fourth with the soft split's depth model): written by the forward pass,
 // bulk-copied into shared memory by the backward pass.  A == nullptr: none.
+// With the hard split the space of the fourth array holds instead each warp's
+// hit lists: for warp w of a tile (0..7) and a batch starting at list position
+// b, the staged indices of the batch's records that reach the warp's block, in
+// list order, at L[w * cap + b ..], then NO_HIT up to the batch's end.
 struct Staged {
     float4* A;
     float4* B;
     float4* C;
     float4* D;
+    uint8_t* L;
     int cap;  // list positions the arrays hold
 };
 
@@ -297,6 +305,12 @@ k_composite_fwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         }
         if (lane < 2) L[cnt + lane] = NO_HIT;
         __syncwarp();
+        if (!SOFT && rec.L) {  // the list, for the backward pass (slot of warp w of the tile: w * cap)
+            const int wit = (blockIdx.x % CTAS_PER_TILE) * CTA_WARPS + (threadIdx.x >> 5);
+            uint8_t* __restrict__ dst = rec.L + (int64_t)wit * rec.cap + b;
+#pragma unroll 1
+            for (int t = lane; t < n; t += 32) dst[t] = t < cnt ? L[t] : NO_HIT;
+        }
         const int pos0 = b - r.x;  // list position of staged record 0
         for (int p = 0; p < cnt; p += 2) {
             if (__all_sync(0xffffffffu, done)) break;
@@ -735,9 +749,23 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     const bool soft = SOFT && cov;
     const float Dw = SOFT ? warp_hide_depth(inside, cov, D) : INFINITY;
     uint32_t visited = 0, contributed = 0;
-    // batch j holds list positions [max(r.x, end - 128 (j + 1)), end - 128 j)
+    // the forward pass's hit lists (hard split, staged records): then the batches
+    // are the forward's, taken back to front -- batch j holds list positions
+    // [r.x + 128 (J - 1 - j), ..) up to end, J = n_batches; otherwise batch j
+    // holds [max(r.x, end - 128 (j + 1)), end - 128 j)
+    const bool fwd_lists = MMA && BULK && rec.L != nullptr;
+    auto window = [&](int j, int& lo, int& hi) {
+        if (fwd_lists) {
+            lo = r.x + CTA_THREADS * (n_batches - 1 - j);
+            hi = min(lo + CTA_THREADS, end);
+        } else {
+            hi = end - CTA_THREADS * j;
+            lo = max(r.x, hi - CTA_THREADS);
+        }
+    };
     auto issue = [&](int j) {
-        const int hi = end - CTA_THREADS * j, lo = max(r.x, hi - CTA_THREADS);
+        int lo, hi;
+        window(j, lo, hi);
         const uint32_t bytes = (uint32_t)(hi - lo) * 16u;
         const int q = j % NBUF;
         mbar_arrive_expect_tx(&s_bar[q], bytes * (SOFT ? 4u : 3u));
@@ -763,8 +791,8 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             }
         }
         if (j >= n_batches) break;
-        const int b_end = end - CTA_THREADS * j;
-        const int b0 = max(r.x, b_end - CTA_THREADS);
+        int b0, b_end;
+        window(j, b0, b_end);
         const int n = b_end - b0;
         if ((int)threadIdx.x < n) {
             if (!BULK) {
@@ -821,13 +849,32 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             RedSmem& R = sRed[threadIdx.x >> 5];
             uint8_t* __restrict__ L = sList[threadIdx.x >> 5];
             int cnt = 0;
-            for (int m = k_top >> 5; m >= 0; --m) {
-                const int kk = m * 32 + lane;
-                const bool hit = kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0);
-                const uint32_t mask = __ballot_sync(FULL, hit);
-                // hits above this lane in the chunk come first
-                if (hit) L[cnt + __popc(mask >> lane) - 1] = (uint8_t)kk;
-                cnt += __popc(mask);
+            if (fwd_lists) {
+                // the forward's list of this batch (ascending, NO_HIT after its end):
+                // the entries up to k_top are a prefix of it, reversed here
+                if (k_top >= 0) {
+                    const int wit = (blockIdx.x % CTAS_PER_TILE) * CTA_WARPS + (threadIdx.x >> 5);
+                    const uint8_t* __restrict__ src = rec.L + (int64_t)wit * rec.cap + b0;
+                    int v[CTA_THREADS / 32];
+#pragma unroll
+                    for (int i = 0; i < CTA_THREADS / 32; ++i) {
+                        const int t = 32 * i + lane;
+                        v[i] = t < n ? src[t] : NO_HIT;
+                        cnt += __popc(__ballot_sync(FULL, v[i] <= k_top));
+                    }
+#pragma unroll
+                    for (int i = 0; i < CTA_THREADS / 32; ++i)
+                        if (v[i] <= k_top) L[cnt - 1 - (32 * i + lane)] = (uint8_t)v[i];
+                }
+            } else {
+                for (int m = k_top >> 5; m >= 0; --m) {
+                    const int kk = m * 32 + lane;
+                    const bool hit = kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0);
+                    const uint32_t mask = __ballot_sync(FULL, hit);
+                    // hits above this lane in the chunk come first
+                    if (hit) L[cnt + __popc(mask >> lane) - 1] = (uint8_t)kk;
+                    cnt += __popc(mask);
+                }
             }
             if (lane < RGROUP) L[cnt + lane] = NO_HIT;
             __syncwarp();
@@ -1398,18 +1445,19 @@ k_composite_back_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__
 
 static Staged staged_of(float* staged, int cap)
 {
-    Staged r{nullptr, nullptr, nullptr, nullptr, 0};
+    Staged r{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     if (!staged || cap <= 0) return r;
     float4* b = reinterpret_cast<float4*>(staged);
     r.A = b;
     r.B = b + cap;
     r.C = b + 2 * (int64_t)cap;
-    r.D = b + 3 * (int64_t)cap;
+    r.D = b + 3 * (int64_t)cap;                  // soft split: depth models
+    r.L = reinterpret_cast<uint8_t*>(r.D);       // hard split: 8 hit-list bytes a position
     r.cap = cap;
     return r;
 }
 
-size_t staged_bytes(int cap, bool soft) { return (size_t)(cap > 0 ? cap : 0) * (soft ? 64 : 48); }
+size_t staged_bytes(int cap, bool soft) { return (size_t)(cap > 0 ? cap : 0) * (soft ? 64 : 56); }
 
 cudaError_t copy_status(uint32_t* flags, bool clear)
 {

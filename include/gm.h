@@ -116,10 +116,13 @@ typedef struct gm_aa_layer {
  * compositing kernel): one record per list position, the compositing's form
  * of that position's splat (mean, conic pre-scaled for exp2, opacity, colour,
  * depth, the Gaussian's id and the exponent bound of alpha >= 1/255; with the
- * soft split also its depth model).  gm_composite_hybrid_fwd writes the
- * records of every batch it stages; gm_composite_hybrid_bwd then copies each
- * batch of a tile's list into shared memory with bulk copies instead of
- * gathering the splats through the ids.  recs: device memory of
+ * soft split also its depth model; with the hard split instead, for each of
+ * the tile's 8 x 4 pixel blocks, which records of each batch reach it).
+ * gm_composite_hybrid_fwd writes the records (and the hard split's hit lists)
+ * of every batch it stages; gm_composite_hybrid_bwd then copies each batch of
+ * a tile's list into shared memory with bulk copies instead of gathering the
+ * splats through the ids, and takes the forward's hit lists instead of
+ * testing the records again.  recs: device memory of
  * gm_staged_bytes(cap, opts->softness) bytes, 16-byte aligned, owned by the
  * caller, contents private to the library; cap >= the number of entries the
  * tile ranges address.  The backward call must get the records its forward
@@ -129,7 +132,7 @@ typedef struct gm_staged {
     int32_t cap;
 } gm_staged;
 
-/* bytes of a staged-record buffer for cap list positions: 48 per position,
+/* bytes of a staged-record buffer for cap list positions: 56 per position,
  * 64 with the soft split (softness > 0) */
 size_t gm_staged_bytes(int32_t cap, float softness);
 

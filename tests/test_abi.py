@@ -123,7 +123,7 @@ def test_null_and_size_checks(lib):
     st = lib.gm_composite_hybrid_fwd(C.byref(cam), C.byref(opts), 4, *([C.c_void_p(256)] * 12), None,
                                      C.byref(stg), None, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"staged" in lib.gm_last_error()
-    assert gm.gm_staged_bytes(1000, 0.0) == 48000 and gm.gm_staged_bytes(1000, 1.0) == 64000
+    assert gm.gm_staged_bytes(1000, 0.0) == 56000 and gm.gm_staged_bytes(1000, 1.0) == 64000
     # edge adjacency: workspace too small; antialiasing without adjacency
     st = lib.gm_mesh_edges(C.c_void_p(256), 10, 12, C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), 16, None)
     assert st == gm.GM_ERR_INVALID_ARG and b"workspace" in lib.gm_last_error()
