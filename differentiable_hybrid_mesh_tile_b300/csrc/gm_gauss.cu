@@ -10,15 +10,51 @@
 namespace gm {
 namespace {
 
+// SH rows of 3 (DEG + 1)^2 floats that are whole float4s (degrees 1 and 3) are
+// staged per CTA in shared memory: read from DRAM by coalesced 16-byte loads
+// of the CTA's contiguous rows, issued before any other work, and kept at an
+// odd stride of float4s so that each lane's reads of its own row are free of
+// bank conflicts.
+template <int DEG>
+struct ShStage {
+    static constexpr int K = DEG < 0 ? 1 : (DEG + 1) * (DEG + 1);
+    static constexpr int ROW4 = (DEG >= 1 && (3 * K) % 4 == 0) ? 3 * K / 4 : 0;  // float4s a row; 0: not staged
+    static constexpr int STRIDE = ROW4 % 2 ? ROW4 : ROW4 + 1;                     // float4s between staged rows
+};
+
+constexpr int PROJ_THREADS = 128;
+
+// Stages the SH rows of Gaussians [g0, g0 + PROJ_THREADS) (those below N) in
+// sh; every thread of the CTA calls it, then waits at a barrier.
+template <int DEG>
+__device__ __forceinline__ void stage_sh_rows(const float* __restrict__ colors, int g0, int N, float4* sh)
+{
+    constexpr int ROW4 = ShStage<DEG>::ROW4, STRIDE = ShStage<DEG>::STRIDE;
+    const int rows = min(PROJ_THREADS, N - g0);
+    const float4* __restrict__ src = reinterpret_cast<const float4*>(colors) + (int64_t)g0 * ROW4;
+    float4 v[ROW4 ? ROW4 : 1];
+#pragma unroll
+    for (int m = 0; m < ROW4; ++m) {
+        const int i = m * PROJ_THREADS + threadIdx.x;
+        if (i < rows * ROW4) v[m] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int m = 0; m < ROW4; ++m) {
+        const int i = m * PROJ_THREADS + threadIdx.x;
+        if (i < rows * ROW4) sh[(i / ROW4) * STRIDE + i % ROW4] = v[m];
+    }
+}
+
 // The record, radius and tile count of Gaussian g seen by camera c.
 // DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
+// sh_row: the Gaussian's SH row staged in shared memory (ShStage), or null.
 template <int DEG>
 __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts& pc, int g,
                                                  const float* __restrict__ means,
                                                  const float* __restrict__ log_scales,
                                                  const float4* __restrict__ quats, const float* __restrict__ logits,
                                                  const float* __restrict__ colors, float4& o0, float4& o1, float4& o2,
-                                                 float4& dm, int& rad, int& touched)
+                                                 float4& dm, int& rad, int& touched, const float4* sh_row = nullptr)
 {
     o0 = make_float4(0.f, 0.f, 0.f, 0.f);
     o1 = o0;
@@ -26,7 +62,7 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
     dm = o0;
     rad = 0;
     touched = 0;
-    if (DEG >= 1) {
+    if (DEG >= 1 && !sh_row) {
         // the SH row is read only after the culling tests and the covariance: ask
         // for its cache lines now (a row of 3 (DEG + 1)^2 floats spans at most two
         // 128-byte lines), so that its loads later find them in L2
@@ -37,20 +73,25 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
     }
     const float mx = __ldg(means + 3 * (int64_t)g), my = __ldg(means + 3 * (int64_t)g + 1),
                 mz = __ldg(means + 3 * (int64_t)g + 2);
+    // every per-Gaussian input is requested before the tests that may not need it,
+    // so that the loads overlap
+    const float4 q = __ldg(quats + g);
+    float s[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) s[k] = __ldg(log_scales + 3 * (int64_t)g + k);
+    const float logit = __ldg(logits + g);
     const float tx = fmaf(c.R[0], mx, fmaf(c.R[1], my, fmaf(c.R[2], mz, c.t[0])));
     const float ty = fmaf(c.R[3], mx, fmaf(c.R[4], my, fmaf(c.R[5], mz, c.t[1])));
     const float tz = fmaf(c.R[6], mx, fmaf(c.R[7], my, fmaf(c.R[8], mz, c.t[2])));
     if (tz > c.znear && tz <= c.zfar) {
         // M = R(q) diag(exp(log_s)); camera-frame factor WM = R_cw M
-        const float4 q = __ldg(quats + g);
         const float qi = 1.0f / sqrtf(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
         const float w = q.x * qi, x = q.y * qi, y = q.z * qi, z = q.w * qi;
         const float Rq[3][3] = {{1.f - 2.f * (y * y + z * z), 2.f * (x * y - w * z), 2.f * (x * z + w * y)},
                                 {2.f * (x * y + w * z), 1.f - 2.f * (x * x + z * z), 2.f * (y * z - w * x)},
                                 {2.f * (x * z - w * y), 2.f * (y * z + w * x), 1.f - 2.f * (x * x + y * y)}};
-        float s[3];
 #pragma unroll
-        for (int k = 0; k < 3; ++k) s[k] = expf(__ldg(log_scales + 3 * (int64_t)g + k));
+        for (int k = 0; k < 3; ++k) s[k] = expf(s[k]);
         float WM[3][3];
 #pragma unroll
         for (int r = 0; r < 3; ++r)
@@ -83,7 +124,7 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
             if (gauss_rect(c, u, v, rad, x0, y0, x1, y1)) {
                 touched = (x1 - x0) * (y1 - y0);
                 const float idet = 1.0f / det;
-                const float op = 1.0f / (1.0f + expf(-__ldg(logits + g)));
+                const float op = 1.0f / (1.0f + expf(-logit));
                 float rgb[3];
                 if (DEG < 0) {
 #pragma unroll
@@ -101,7 +142,7 @@ __device__ __forceinline__ void project_gaussian(const Cam& c, const ProjConsts&
                         const float4* cf4 = reinterpret_cast<const float4*>(cf);
 #pragma unroll
                         for (int v4 = 0; v4 < 3 * K / 4; ++v4) {
-                            const float4 e = __ldg(cf4 + v4);
+                            const float4 e = sh_row ? sh_row[v4] : __ldg(cf4 + v4);
                             const float ev[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
                             for (int l = 0; l < 4; ++l) {
@@ -155,17 +196,24 @@ __device__ __forceinline__ float hide_depth(const SoftCull& sc, float z, const f
 }
 
 template <int DEG>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(PROJ_THREADS)
 k_project(Cam c, ProjConsts pc, SoftCull sc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
           const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
           float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched,
           float4* __restrict__ depth_model)
 {
+    constexpr int ROW4 = ShStage<DEG>::ROW4;
+    __shared__ float4 s_sh[ROW4 ? PROJ_THREADS * ShStage<DEG>::STRIDE : 1];
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if constexpr (ROW4 > 0) {
+        stage_sh_rows<DEG>(colors, blockIdx.x * blockDim.x, N, s_sh);
+        __syncthreads();
+    }
     if (g >= N) return;
     float4 o0, o1, o2, dm;
     int rad, touched;
-    project_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad, touched);
+    project_gaussian<DEG>(c, pc, g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad, touched,
+                          ROW4 ? s_sh + threadIdx.x * ShStage<DEG>::STRIDE : nullptr);
     if (sc.softness > 0.0f && rad > 0) o2.z = hide_depth(sc, o2.y, dm);
     splats[3 * (int64_t)g] = o0;
     splats[3 * (int64_t)g + 1] = o1;
@@ -641,12 +689,12 @@ cudaError_t project(const Cam& c, int sh_degree, float softness, int split, int 
     if (N <= 0) return cudaSuccess;
     const ProjConsts pc = make_proj_consts(c);
     const SoftCull sc = soft_cull(softness, split);
-    const int grid = (N + 255) / 256;
+    const int grid = (N + PROJ_THREADS - 1) / PROJ_THREADS;
     auto* q4 = reinterpret_cast<const float4*>(quats);
     auto* s4 = reinterpret_cast<float4*>(splats);
     auto* dm4 = reinterpret_cast<float4*>(depth_model);
-#define GM_PROJ(D) k_project<D><<<grid, 256, 0, s>>>(c, pc, sc, N, means, log_scales, q4, logits, colors, s4, radii, \
-                                                     tiles_touched, dm4)
+#define GM_PROJ(D) k_project<D><<<grid, PROJ_THREADS, 0, s>>>(c, pc, sc, N, means, log_scales, q4, logits, colors, \
+                                                              s4, radii, tiles_touched, dm4)
     switch (sh_degree) {
         case -1: GM_PROJ(-1); break;
         case 0: GM_PROJ(0); break;
