@@ -166,22 +166,22 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 PROFILED = {
     "composite_fwd": {
         "kernel": "k_composite_fwd",
-        "dram_bytes": 86578688 + 96558848,
-        "smem_wavefronts": 34879233,
-        "warp_instructions": 262407224,
+        "dram_bytes": 88629248 + 108866560,
+        "smem_wavefronts": 35299137,
+        "warp_instructions": 266292620,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "f5fc079eb7d174e9a112d70793eaed347e7128e06119b57e3373522da375fd33",
+                "018ccab955d4fd114a1ef6206662ecb6dc5c0fe61eb639cb24494cff94da5983",
         },
     },
     "composite_bwd": {
         "kernel": "k_composite_bwd",
-        "dram_bytes": 186315776 + 12181248,
-        "smem_wavefronts": 79798525,
-        "warp_instructions": 421492889,
+        "dram_bytes": 200817920 + 12926208,
+        "smem_wavefronts": 76019432,
+        "warp_instructions": 397417341,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "f5fc079eb7d174e9a112d70793eaed347e7128e06119b57e3373522da375fd33",
+                "018ccab955d4fd114a1ef6206662ecb6dc5c0fe61eb639cb24494cff94da5983",
         },
     },
 }
