@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "gm_internal.cuh"
+#include "gm_lookback.cuh"
 #include "gm_proj.cuh"
 
 namespace gm {
@@ -495,12 +496,13 @@ k_gauss_shape(Cam c, int N, const float4* __restrict__ splats, const int32_t* __
 // Per position i of the depth order: the tiles the Gaussian is binned to now
 // that the mesh's tile bounds exist -- for a small rectangle its ellipse-kept
 // tiles less those the mesh hides, for a large one every tile of the rectangle
-// tested again by the whole warp -- as a count (for the scan) and, for a small
-// rectangle, the kept mask (for the emission).
+// tested again by the whole warp -- as a count and, for a small rectangle, the
+// kept mask (for the emission); and per CTA the sum of its counts.
 __global__ void __launch_bounds__(256)
 k_gauss_cull(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
-             int32_t* __restrict__ counts, uint32_t* __restrict__ kept)
+             int32_t* __restrict__ counts, uint32_t* __restrict__ kept, int32_t* __restrict__ block_sums)
 {
+    __shared__ int s_sum[8];
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     int4 ra = make_int4(0, 0, 0, -1), rb = make_int4(0, 0, 0, 0);
@@ -550,22 +552,57 @@ k_gauss_cull(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
         counts[i] = post;
         kept[i] = mask;
     }
+    int sum = post;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    if (lane == 0) s_sum[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int w = 0; w < 8; ++w) t += s_sum[w];
+        block_sums[blockIdx.x] = t;
+    }
+}
+
+// The CTAs' count sums (one per 256 positions of the depth order) into their
+// exclusive prefixes, in place, and the total into counters[GM_CNT_K]: the
+// emission adds a CTA's prefix to the scan of its own counts.  One CTA.
+constexpr int PREFIX_THREADS = 1024;
+
+__global__ void __launch_bounds__(PREFIX_THREADS)
+k_block_prefix(int32_t* __restrict__ sums, int nb, int32_t* counters)
+{
+    __shared__ uint32_t s_warp[PREFIX_THREADS / 32];
+    const int per = (nb + PREFIX_THREADS - 1) / PREFIX_THREADS;
+    const int b0 = threadIdx.x * per;
+    uint32_t local = 0;
+    for (int k = 0; k < per && b0 + k < nb; ++k) local += (uint32_t)sums[b0 + k];
+    uint32_t total;
+    uint32_t run = block_excl_scan<PREFIX_THREADS>(local, s_warp, total);
+    for (int k = 0; k < per && b0 + k < nb; ++k) {
+        const uint32_t v = (uint32_t)sums[b0 + k];
+        sums[b0 + k] = (int32_t)run;
+        run += v;
+    }
+    if (threadIdx.x == 0) counters[GM_CNT_K] = (int32_t)min(total, (uint32_t)INT32_MAX);
 }
 
 // Emits the (tile << 32 | depth bits, id) entries of the Gaussian at position
-// i of the depth order, in ascending (depth, id) order, at offsets[i]: entries
+// i of the depth order, in ascending (depth, id) order, at its offset (the
+// CTA's prefix plus the scan of the CTA's counts): entries
 // come out depth-sorted, so a stable sort on the tile bits alone completes the
 // (tile, depth, id) order.  The tiles kept are exactly those k_gauss_cull
 // counted: its mask for small rectangles, the same predicate for large ones.
 __global__ void __launch_bounds__(256)
 k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, const GaussRec* __restrict__ rec,
              const int32_t* __restrict__ counts, const uint32_t* __restrict__ kept,
-             const int32_t* __restrict__ offsets, int cap, int32_t* counters, uint64_t* __restrict__ keys,
+             const int32_t* __restrict__ block_prefix, int cap, int32_t* counters, uint64_t* __restrict__ keys,
              int32_t* __restrict__ vals)
 {
     __shared__ int4 s_a[256];   // x0, y0, width, Gaussian id
     __shared__ int2 s_b[256];   // depth bits, first output slot
     __shared__ uint32_t s_m[256];
+    __shared__ uint32_t s_warp[8];
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int wbase = threadIdx.x & ~31;
@@ -574,14 +611,15 @@ k_gauss_emit(Cam c, BinRule rule, int N, const float4* __restrict__ splats, cons
     int area = 0, dbits = 0;
     BinShape sh = {};
     uint32_t mask = 0;
-    int64_t o = 0;
+    const int cnt_i = i < N ? counts[i] : 0;
+    uint32_t cta_total;
+    const int64_t o = (int64_t)block_prefix[blockIdx.x] + block_excl_scan<256>((uint32_t)cnt_i, s_warp, cta_total);
     if (i < N) {
         const int4 rb = rec[i].b;
-        if (rb.x > 0 && counts[i] > 0) {
+        if (rb.x > 0 && cnt_i > 0) {
             ra = rec[i].a;
             area = rb.x;
             dbits = rb.z;
-            o = offsets[i];
             mask = kept[i];
             if (area > SMALL_RECT) sh = bin_shape(splats, ra.w);  // the big-rectangle path tests again
         }
@@ -836,9 +874,12 @@ cudaError_t gauss_bin(const Cam& c, bool cull, bool soft, bool tile_test, int N,
         rule.tile_far = tile_far;
         rule.tile_full = tile_full;
         rule.TW = c.TW;
-        k_gauss_cull<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept);
+        // the offsets: per-CTA count sums (cull), their prefixes (one CTA), then each
+        // emission CTA's own scan -- no inter-block waits
+        k_gauss_cull<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept, w.offsets);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = exclusive_scan(w.counts, nullptr, w.offsets, N, counters, w.sw, s)) != cudaSuccess) return e;
+        k_block_prefix<<<1, PREFIX_THREADS, 0, s>>>(w.offsets, grid, counters);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         k_gauss_emit<<<grid, 256, 0, s>>>(c, rule, N, s4, w.rec, w.counts, w.kept, w.offsets, cap, counters, ek,
                                           ev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
