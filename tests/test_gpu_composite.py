@@ -245,13 +245,15 @@ def test_degenerate_scenes(what, orc):
 def test_backward_forms_agree(softness, antialias, monkeypatch):
     """The backward pass's forms give the same gradients up to the order of
     float atomic sums, and the forward's image is the same bit for bit:
-    records bulk-copied from the forward's staged ones or gathered by the
-    backward itself (GM_BWD_GATHER), and, for the hard split, the per-warp
-    sums taken on the tensor cores or by warp shuffles (GM_BWD_SHUFFLE_REDUCE).
-    The 512 px sphere has tiles of several 128-entry batches; the 101 x 77
-    frame has ragged tiles and short lists.  The tensor-core sums (tf32 hi /
-    lo parts, about 22 bits) agree with the shuffle sums within 1e-5
-    relative of the largest gradient."""
+    records bulk-copied from the forward's staged ones (with the hard split
+    and the tensor-core sums, the forward's hit lists too) or gathered by the
+    backward itself, which then tests the records against its blocks
+    (GM_BWD_GATHER), and, for the hard split, the per-warp sums taken on the
+    tensor cores or by warp shuffles (GM_BWD_SHUFFLE_REDUCE).  The 512 px
+    sphere has tiles of several 128-entry batches; the 101 x 77 frame has
+    ragged tiles and short lists.  The tensor-core sums (tf32 hi / lo parts,
+    about 20 bits) agree with the shuffle sums within 1e-5 relative of the
+    largest gradient."""
     H.need_gpu()
     import torch
     import differentiable_hybrid_mesh_tile_b300 as gm
