@@ -824,6 +824,9 @@ def cpu_baseline(args, scene):
                                              len(scene.mesh.faces), len(scene.gaussians.means), dt)}
 
 
+REF_BUDGET_S = 150.0
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -834,6 +837,12 @@ def run_reference(args):
     # the oracle's cost per call that does not depend on the sample (projection of
     # every Gaussian, the lists' set-up): one call on a single tile
     _, fixed_s, _ = oracle_sample(scene, 1, seed=99)
+    # the sample is bounded so that the whole run stays within a few minutes (about
+    # REF_BUDGET_S of timed and warm-up steps): fewer tiles a step for large --steps
+    _, full_s, _ = oracle_sample(scene, n_tiles, seed=98)
+    per_tile = max(full_s - fixed_s, 1e-6) / n_tiles
+    per_step = REF_BUDGET_S / max(1, args.steps + args.warmup)
+    n_tiles = int(min(n_tiles, max(16, (per_step - fixed_s) / per_tile)))
     for k in range(args.warmup):
         oracle_sample(scene, n_tiles, seed=100 + k)
     times, pxs = [], []
