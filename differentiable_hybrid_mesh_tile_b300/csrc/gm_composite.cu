@@ -176,6 +176,23 @@ __device__ __forceinline__ PixelMap pixel_of(const Cam& c, int& tile)
     return m;
 }
 
+// The standard normal distribution function by the rational approximation of
+// Abramowitz and Stegun, Handbook of Mathematical Functions, formula 26.2.17:
+// for x >= 0, Phi(x) = 1 - phi(x) t (b1 + b2 t + b3 t^2 + b4 t^3 + b5 t^4) with
+// t = 1 / (1 + p x) and phi the normal density, |error| < 7.5e-8; Phi(-x) =
+// 1 - Phi(x).  The tail below 0 is formed directly (no cancellation).
+__device__ __forceinline__ float normal_cdf(float x)
+{
+    constexpr float P = 0.2316419f;
+    constexpr float B1 = 0.319381530f, B2 = -0.356563782f, B3 = 1.781477937f, B4 = -1.821255978f,
+                    B5 = 1.330274429f;
+    const float ax = fabsf(x);
+    const float t = __fdividef(1.0f, fmaf(P, ax, 1.0f));
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, B5, B4), B3), B2), B1);
+    const float q = 0.3989422804014327f * ex2(-0.5f * LOG2E * ax * ax) * poly;  // 1 - Phi(|x|)
+    return x >= 0.0f ? 1.0f - q : q;
+}
+
 // The soft split: its width factor and the form of the front fraction f(x),
 // Phi(x) or the logistic 1 / (1 + exp(-1.702 x)).  Past x <= -tail, f(x) <=
 // 0.0030 (Phi(-2.75)) or 0.0026 (logistic at -3.5), so alpha f <= 0.99 f <
@@ -186,7 +203,7 @@ struct Split {
     __device__ __forceinline__ float tail() const { return logistic ? 3.5f : 2.75f; }
     __device__ __forceinline__ float front(float x) const
     {
-        return logistic ? 1.0f / (1.0f + __expf(-1.702f * x)) : normcdff(x);
+        return logistic ? 1.0f / (1.0f + __expf(-1.702f * x)) : normal_cdf(x);
     }
     // df/dx, given f = front(x)
     __device__ __forceinline__ float density(float x, float f) const
