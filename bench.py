@@ -171,7 +171,7 @@ PROFILED = {
         "warp_instructions": 266292620,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "018ccab955d4fd114a1ef6206662ecb6dc5c0fe61eb639cb24494cff94da5983",
+                "af3a5748b33d703decafa7258baa6fadc87aaf1c350c9687421885e86facd75d",
         },
     },
     "composite_bwd": {
@@ -181,7 +181,7 @@ PROFILED = {
         "warp_instructions": 397417341,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "018ccab955d4fd114a1ef6206662ecb6dc5c0fe61eb639cb24494cff94da5983",
+                "af3a5748b33d703decafa7258baa6fadc87aaf1c350c9687421885e86facd75d",
         },
     },
 }
