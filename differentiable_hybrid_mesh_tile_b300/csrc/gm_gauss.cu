@@ -11,41 +11,6 @@
 namespace gm {
 namespace {
 
-// SH rows of 3 (DEG + 1)^2 floats that are whole float4s (degrees 1 and 3) are
-// staged per CTA in shared memory: read from DRAM by coalesced 16-byte loads
-// of the CTA's contiguous rows, issued before any other work, and kept at an
-// odd stride of float4s so that each lane's reads of its own row are free of
-// bank conflicts.
-template <int DEG>
-struct ShStage {
-    static constexpr int K = DEG < 0 ? 1 : (DEG + 1) * (DEG + 1);
-    static constexpr int ROW4 = (DEG >= 1 && (3 * K) % 4 == 0) ? 3 * K / 4 : 0;  // float4s a row; 0: not staged
-    static constexpr int STRIDE = ROW4 % 2 ? ROW4 : ROW4 + 1;                     // float4s between staged rows
-};
-
-constexpr int PROJ_THREADS = 128;
-
-// Stages the SH rows of Gaussians [g0, g0 + PROJ_THREADS) (those below N) in
-// sh; every thread of the CTA calls it, then waits at a barrier.
-template <int DEG>
-__device__ __forceinline__ void stage_sh_rows(const float* __restrict__ colors, int g0, int N, float4* sh)
-{
-    constexpr int ROW4 = ShStage<DEG>::ROW4, STRIDE = ShStage<DEG>::STRIDE;
-    const int rows = min(PROJ_THREADS, N - g0);
-    const float4* __restrict__ src = reinterpret_cast<const float4*>(colors) + (int64_t)g0 * ROW4;
-    float4 v[ROW4 ? ROW4 : 1];
-#pragma unroll
-    for (int m = 0; m < ROW4; ++m) {
-        const int i = m * PROJ_THREADS + threadIdx.x;
-        if (i < rows * ROW4) v[m] = __ldg(src + i);
-    }
-#pragma unroll
-    for (int m = 0; m < ROW4; ++m) {
-        const int i = m * PROJ_THREADS + threadIdx.x;
-        if (i < rows * ROW4) sh[(i / ROW4) * STRIDE + i % ROW4] = v[m];
-    }
-}
-
 // The record, radius and tile count of Gaussian g seen by camera c.
 // DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
 // sh_row: the Gaussian's SH row staged in shared memory (ShStage), or null.
@@ -225,22 +190,29 @@ k_project(Cam c, ProjConsts pc, SoftCull sc, int N, const float* __restrict__ me
 }
 
 // Several views in one launch: each thread takes one Gaussian through every
-// view of the batch, so its parameters come from DRAM once (later views find
-// them in L1 / L2); outputs are [view][N] arrays.
+// view of the batch, so its parameters come from DRAM once (its SH row staged
+// in shared memory for all views, the rest found in L1 / L2 by later views);
+// outputs are [view][N] arrays.
 template <int DEG>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(PROJ_THREADS)
 k_project_views(ViewBatch vb, SoftCull sc, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
                 const float4* __restrict__ quats, const float* __restrict__ logits, const float* __restrict__ colors,
                 float4* __restrict__ splats, int32_t* __restrict__ radii, int32_t* __restrict__ tiles_touched,
                 float4* __restrict__ depth_model)
 {
+    constexpr int ROW4 = ShStage<DEG>::ROW4;
+    __shared__ float4 s_sh[ROW4 ? PROJ_THREADS * ShStage<DEG>::STRIDE : 1];
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if constexpr (ROW4 > 0) {
+        stage_sh_rows<DEG>(colors, blockIdx.x * blockDim.x, N, s_sh);
+        __syncthreads();
+    }
     if (g >= N) return;
     for (int v = 0; v < vb.n; ++v) {
         float4 o0, o1, o2, dm;
         int rad, touched;
         project_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors, o0, o1, o2, dm, rad,
-                              touched);
+                              touched, ROW4 ? s_sh + threadIdx.x * ShStage<DEG>::STRIDE : nullptr);
         if (sc.softness > 0.0f && rad > 0) o2.z = hide_depth(sc, o2.y, dm);
         const int64_t i = (int64_t)v * N + g;
         splats[3 * i] = o0;
@@ -752,7 +724,7 @@ cudaError_t project_views(const Cam* cams, int V, int sh_degree, float softness,
 {
     if (N <= 0) return cudaSuccess;
     const SoftCull sc = soft_cull(softness, split);
-    const int grid = (N + 255) / 256;
+    const int grid = (N + PROJ_THREADS - 1) / PROJ_THREADS;
     auto* q4 = reinterpret_cast<const float4*>(quats);
     for (int v0 = 0; v0 < V; v0 += MAX_VIEWS) {
         ViewBatch vb;
@@ -764,8 +736,9 @@ cudaError_t project_views(const Cam* cams, int V, int sh_degree, float softness,
         const int64_t off = (int64_t)v0 * N;
         auto* s4 = reinterpret_cast<float4*>(splats + 12 * off);
         auto* dm4 = depth_model ? reinterpret_cast<float4*>(depth_model + 4 * off) : nullptr;
-#define GM_PROJ_V(D) k_project_views<D><<<grid, 256, 0, s>>>(vb, sc, N, means, log_scales, q4, logits, colors, s4, \
-                                                             radii + off, tiles_touched + off, dm4)
+#define GM_PROJ_V(D)                                                                                       \
+    k_project_views<D><<<grid, PROJ_THREADS, 0, s>>>(vb, sc, N, means, log_scales, q4, logits, colors, s4,      \
+                                                     radii + off, tiles_touched + off, dm4)
         switch (sh_degree) {
             case -1: GM_PROJ_V(-1); break;
             case 0: GM_PROJ_V(0); break;

@@ -69,6 +69,41 @@ inline ProjConsts make_proj_consts(const Cam& c)
 }
 
 // Cameras of one batched launch (passed by value as a kernel parameter).
+// SH rows of 3 (DEG + 1)^2 floats that are whole float4s (degrees 1 and 3) are
+// staged per CTA in shared memory: read from DRAM by coalesced 16-byte loads
+// of the CTA's contiguous rows, issued before any other work, and kept at an
+// odd stride of float4s so that each lane's reads of its own row are free of
+// bank conflicts.
+template <int DEG>
+struct ShStage {
+    static constexpr int K = DEG < 0 ? 1 : (DEG + 1) * (DEG + 1);
+    static constexpr int ROW4 = (DEG >= 1 && (3 * K) % 4 == 0) ? 3 * K / 4 : 0;  // float4s a row; 0: not staged
+    static constexpr int STRIDE = ROW4 % 2 ? ROW4 : ROW4 + 1;                     // float4s between staged rows
+};
+
+constexpr int PROJ_THREADS = 128;
+
+// Stages the SH rows of Gaussians [g0, g0 + PROJ_THREADS) (those below N) in
+// sh; every thread of the CTA calls it, then waits at a barrier.
+template <int DEG>
+__device__ __forceinline__ void stage_sh_rows(const float* __restrict__ colors, int g0, int N, float4* sh)
+{
+    constexpr int ROW4 = ShStage<DEG>::ROW4, STRIDE = ShStage<DEG>::STRIDE;
+    const int rows = min(PROJ_THREADS, N - g0);
+    const float4* __restrict__ src = reinterpret_cast<const float4*>(colors) + (int64_t)g0 * ROW4;
+    float4 v[ROW4 ? ROW4 : 1];
+#pragma unroll
+    for (int m = 0; m < ROW4; ++m) {
+        const int i = m * PROJ_THREADS + threadIdx.x;
+        if (i < rows * ROW4) v[m] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int m = 0; m < ROW4; ++m) {
+        const int i = m * PROJ_THREADS + threadIdx.x;
+        if (i < rows * ROW4) sh[(i / ROW4) * STRIDE + i % ROW4] = v[m];
+    }
+}
+
 constexpr int MAX_VIEWS = 8;
 struct ViewBatch {
     Cam cam[MAX_VIEWS];

@@ -73,7 +73,8 @@ struct ProjGrad {
 
 // DEG < 0: colours are RGB [N][3]; else SH coefficients [N][(DEG+1)^2][3].
 // radius: of this Gaussian in this view (0 = culled: zero gradient);
-// vsp: its record gradient (3 float4).
+// vsp: its record gradient (3 float4); sh_row: its SH row staged in shared
+// memory (ShStage), or null.
 template <int DEG>
 __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjConsts& pc, int g,
                                                      const float* __restrict__ means,
@@ -83,7 +84,7 @@ __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjCon
                                                      const float* __restrict__ colors, int radius,
                                                      const float4* __restrict__ vsp,
                                                      const float4* __restrict__ vdm, bool first,
-                                                     ProjGrad<DEG>& out)
+                                                     ProjGrad<DEG>& out, const float4* sh_row = nullptr)
 {
     constexpr int K = ProjGrad<DEG>::K;
     // this view's gradient: written into out (first view) or added to it, one
@@ -256,7 +257,7 @@ __device__ __forceinline__ void project_bwd_gaussian(const Cam& c, const ProjCon
                 const float4* src4 = reinterpret_cast<const float4*>(src);
 #pragma unroll
                 for (int v4 = 0; v4 < 3 * K / 4; ++v4) {
-                    const float4 e = __ldg(src4 + v4);
+                    const float4 e = sh_row ? sh_row[v4] : __ldg(src4 + v4);
                     cf[4 * v4] = e.x; cf[4 * v4 + 1] = e.y; cf[4 * v4 + 2] = e.z; cf[4 * v4 + 3] = e.w;
                 }
             } else {
@@ -357,7 +358,7 @@ k_project_bwd(Cam c, ProjConsts pc, int N, const float* __restrict__ means, cons
 // The views of a batch summed in registers (in view order, the order in which
 // per-view calls with accumulation would add them), written once.
 template <int DEG>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(PROJ_THREADS)
 k_project_bwd_views(ViewBatch vb, int N, const float* __restrict__ means, const float* __restrict__ log_scales,
                     const float4* __restrict__ quats, const float* __restrict__ logits,
                     const float* __restrict__ colors, const int32_t* __restrict__ radii,
@@ -366,14 +367,21 @@ k_project_bwd_views(ViewBatch vb, int N, const float* __restrict__ means, const 
                     float* __restrict__ v_log_scales, float4* __restrict__ v_quats, float* __restrict__ v_logits,
                     float* __restrict__ v_colors)
 {
+    // the SH rows of the CTA's Gaussians, staged once for every view
+    constexpr int ROW4 = ShStage<DEG>::ROW4;
+    __shared__ float4 s_sh[ROW4 ? PROJ_THREADS * ShStage<DEG>::STRIDE : 1];
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if constexpr (ROW4 > 0) {
+        stage_sh_rows<DEG>(colors, blockIdx.x * blockDim.x, N, s_sh);
+        __syncthreads();
+    }
     if (g >= N) return;
     ProjGrad<DEG> total;
     for (int v = 0; v < vb.n; ++v) {
         const int64_t i = (int64_t)v * N + g;
         project_bwd_gaussian<DEG>(vb.cam[v], vb.pc[v], g, means, log_scales, quats, logits, colors,
                                   __ldg(radii + i), v_splats + 3 * i, v_depth_model ? v_depth_model + i : nullptr,
-                                  v == 0, total);
+                                  v == 0, total, ROW4 ? s_sh + threadIdx.x * ShStage<DEG>::STRIDE : nullptr);
     }
     store_grad<DEG>(g, total, acc, v_means, v_log_scales, v_quats, v_logits, v_colors);
 }
@@ -414,7 +422,7 @@ cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, cons
                               float* v_colors, cudaStream_t s)
 {
     if (N <= 0) return cudaSuccess;
-    const int grid = (N + 127) / 128;  // 128-thread CTAs: the SH-3 body is register heavy
+    const int grid = (N + PROJ_THREADS - 1) / PROJ_THREADS;  // 128-thread CTAs: the SH-3 body is register heavy
     auto* q4 = reinterpret_cast<const float4*>(quats);
     auto* vq4 = reinterpret_cast<float4*>(v_quats);
     for (int v0 = 0; v0 < V; v0 += MAX_VIEWS) {
@@ -429,7 +437,7 @@ cudaError_t project_bwd_views(const Cam* cams, int V, int sh_degree, int N, cons
         auto* vd4 = v_depth_model ? reinterpret_cast<const float4*>(v_depth_model + 4 * off) : nullptr;
         const bool acc = accumulate || v0 > 0;  // later batches add to the earlier ones
 #define GM_PROJ_BWD_V(D)                                                                                          \
-    k_project_bwd_views<D><<<grid, 128, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, radii + off, vs4,   \
+    k_project_bwd_views<D><<<grid, PROJ_THREADS, 0, s>>>(vb, N, means, log_scales, q4, logits, colors, radii + off, vs4,   \
                                                 vd4, acc, v_means, v_log_scales, vq4, v_logits, v_colors)
         switch (sh_degree) {
             case -1: GM_PROJ_BWD_V(-1); break;
