@@ -171,7 +171,7 @@ PROFILED = {
         "warp_instructions": 266292620,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "af3a5748b33d703decafa7258baa6fadc87aaf1c350c9687421885e86facd75d",
+                "3525e8e2f590fd3682f14a4c533c056221329e6b68363aab83d791f7e7693c99",
         },
     },
     "composite_bwd": {
@@ -181,7 +181,7 @@ PROFILED = {
         "warp_instructions": 397417341,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "af3a5748b33d703decafa7258baa6fadc87aaf1c350c9687421885e86facd75d",
+                "3525e8e2f590fd3682f14a4c533c056221329e6b68363aab83d791f7e7693c99",
         },
     },
 }

@@ -857,8 +857,9 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         const float4* __restrict__ sC = sC_buf[cur];
         const float4* __restrict__ sD = sD_buf[SOFT ? cur : 0];
         // this warp only needs the entries in front of its last composited one, and of
-        // those only the ones that can reach its pixels (a ballot per 32 entries);
-        // they are taken four at a time from the back
+        // those only the ones that can reach its pixels; the tensor-core form takes them
+        // from a hit list in groups of eight, the shuffle form from a ballot per 32
+        // entries four at a time, both from the back
         const int k_top = min(n, warp_last - (b0 - r.x)) - 1;
         if constexpr (MMA) {
             // the warp's hits of this batch (entries up to k_top whose ellipse reaches
