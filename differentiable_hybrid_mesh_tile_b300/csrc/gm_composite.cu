@@ -11,9 +11,9 @@
 // memory, and then visits only them (the other pairs would be skipped anyway),
 // every lane evaluating every listed record and keeping, by selects rather than
 // branches, what applies to its pixel.  With staged records the forward pass
-// also writes each warp's lists out, and the backward pass (hard split) takes
-// the forward's batches in reverse with those lists instead of testing the
-// records again.
+// also writes each warp's lists out, and each warp of the backward pass (hard
+// split) then works through its own lists, back to front, loading the listed
+// records from the staged buffer itself, with no barrier across the CTA.
 //
 // Half-tile CTAs: the warps of a CTA wait for one another at every batch and
 // at exit, so the slowest 8 x 4 block holds the CTA; four blocks per CTA
@@ -562,14 +562,12 @@ __device__ __forceinline__ float moment(int n, int i, int j)
 
 // ---------------------------------------------- bulk-copy staging ---------
 //
-// The backward pass takes each batch of a tile's staged records (written by
-// the forward pass in list order) with bulk copies (cp.async.bulk, the TMA
-// engine's linear mode) into shared memory: one thread issues the copies of a
-// batch and an mbarrier counts their bytes.  With two buffers the next batch's
-// copies are in flight while the CTA works on the current one; with one (the
-// tensor-core form, whose staging needs the shared memory) they start after the
-// CTA is done with the previous batch, while the other CTAs of the SM run.  The
-// source is always this GPU's own record buffer.
+// The backward pass's shuffle-sum form takes each batch of a tile's staged
+// records (written by the forward pass in list order) with bulk copies
+// (cp.async.bulk, the TMA engine's linear mode) into shared memory: one thread
+// issues the copies of a batch and an mbarrier counts their bytes; with two
+// buffers the next batch's copies are in flight while the CTA works on the
+// current one.  The source is always this GPU's own record buffer.
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -641,15 +639,17 @@ __device__ uint32_t g_copy_status = 0;
 namespace {
 
 // The kernel is bound by instruction issue, and resident warps hide its
-// latencies: the hard split runs ten CTAs of 128 threads per SM (48 registers,
-// 20.5 KB of shared memory with the tensor-core staging and the hit lists), nine with the shuffle
-// sums and two record buffers, the soft split eight (64 registers: four more
-// terms per entry).  BULK: the records come from the forward pass's staged
-// records by bulk copies; otherwise each thread gathers and stages one record
-// per batch.  MMA: the warp sums of a group of entries on the tensor cores (hard
-// split); otherwise by the shuffle reduce-scatter into a per-CTA accumulator.
+// latencies: the gathered hard split runs ten CTAs of 128 threads per SM (48
+// registers, 22 KB of shared memory with the tensor-core staging), the shuffle
+// sums with two bulk-copied record buffers nine, the soft split eight (64
+// registers: four more terms per entry).  BULK: the records come from the
+// forward pass's staged records by bulk copies; otherwise each thread gathers
+// and stages one record per batch.  MMA: the warp sums of a group of entries
+// on the tensor cores (hard split); otherwise by the shuffle reduce-scatter
+// into a per-CTA accumulator.  The hard split with staged records (the
+// renderers' default) runs k_composite_bwd_lists instead.
 template <bool STATS, bool SOFT, bool BULK, bool MMA>
-__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : (BULK && !MMA ? 9 : 10))
+__global__ void __launch_bounds__(CTA_THREADS, SOFT ? 8 : (BULK ? 9 : 10))
 k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile_range,
                 const int32_t* __restrict__ gids, const float4* __restrict__ splats,
                 const float4* __restrict__ depth_model, const float* __restrict__ mesh_depth,
@@ -660,10 +660,9 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 AaLayer aa, Staged rec, unsigned long long* __restrict__ stats)
 {
     constexpr int NACC = SOFT ? NGRAD + 4 : NGRAD;
-    // the bulk-copied records take two buffers (the next batch in flight) unless the
-    // tensor-core staging needs the shared memory (then one: each batch's copies
-    // start after the CTA is done with the previous one)
-    constexpr int NBUF = BULK && !MMA ? 2 : 1;
+    static_assert(!(BULK && MMA), "staged records with the tensor-core sums: k_composite_bwd_lists");
+    // the bulk-copied records take two buffers: the next batch in flight
+    constexpr int NBUF = BULK ? 2 : 1;
     __shared__ __align__(16) float4 sA_buf[NBUF][CTA_THREADS];
     __shared__ __align__(16) float4 sB_buf[NBUF][CTA_THREADS];
     __shared__ __align__(16) float4 sC_buf[NBUF][CTA_THREADS];
@@ -766,23 +765,9 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     const bool soft = SOFT && cov;
     const float Dw = SOFT ? warp_hide_depth(inside, cov, D) : INFINITY;
     uint32_t visited = 0, contributed = 0;
-    // the forward pass's hit lists (hard split, staged records): then the batches
-    // are the forward's, taken back to front -- batch j holds list positions
-    // [r.x + 128 (J - 1 - j), ..) up to end, J = n_batches; otherwise batch j
-    // holds [max(r.x, end - 128 (j + 1)), end - 128 j)
-    const bool fwd_lists = MMA && BULK && rec.L != nullptr;
-    auto window = [&](int j, int& lo, int& hi) {
-        if (fwd_lists) {
-            lo = r.x + CTA_THREADS * (n_batches - 1 - j);
-            hi = min(lo + CTA_THREADS, end);
-        } else {
-            hi = end - CTA_THREADS * j;
-            lo = max(r.x, hi - CTA_THREADS);
-        }
-    };
+    // batch j holds list positions [max(r.x, end - 128 (j + 1)), end - 128 j)
     auto issue = [&](int j) {
-        int lo, hi;
-        window(j, lo, hi);
+        const int hi = end - CTA_THREADS * j, lo = max(r.x, hi - CTA_THREADS);
         const uint32_t bytes = (uint32_t)(hi - lo) * 16u;
         const int q = j % NBUF;
         mbar_arrive_expect_tx(&s_bar[q], bytes * (SOFT ? 4u : 3u));
@@ -791,7 +776,7 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         bulk_copy(sC_buf[q], rec.C + lo, bytes, &s_bar[q]);
         if (SOFT) bulk_copy(sD_buf[SOFT ? q : 0], rec.D + lo, bytes, &s_bar[q]);
     };
-    if (BULK && NBUF == 2 && threadIdx.x == 0 && n_batches > 0) issue(0);
+    if (BULK && threadIdx.x == 0 && n_batches > 0) issue(0);
     int n_prev = 0;
     for (int j = 0;; ++j) {
         const int cur = j % NBUF, prev = (j + NBUF - 1) % NBUF;
@@ -808,8 +793,8 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             }
         }
         if (j >= n_batches) break;
-        int b0, b_end;
-        window(j, b0, b_end);
+        const int b_end = end - CTA_THREADS * j;
+        const int b0 = max(r.x, b_end - CTA_THREADS);
         const int n = b_end - b0;
         if ((int)threadIdx.x < n) {
             if (!BULK) {
@@ -830,16 +815,10 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
         __syncthreads();
         if (BULK) {
             if (threadIdx.x == 0) {
-                if (NBUF == 2) {
-                    if (j + 1 < n_batches) {
-                        // the other buffer was last read by the flush above: free after the barrier
-                        fence_proxy_async_smem();
-                        issue(j + 1);
-                    }
-                } else {
-                    // the one buffer was last read before the previous batch's closing barrier
+                if (j + 1 < n_batches) {
+                    // the other buffer was last read by the flush above: free after the barrier
                     fence_proxy_async_smem();
-                    issue(j);
+                    issue(j + 1);
                 }
             }
             const bool ok = __syncthreads_and(mbar_wait(&s_bar[cur], (uint32_t)(j / NBUF) & 1u));
@@ -847,7 +826,7 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
                 // a copy did not arrive: report, let the copies in flight land, stop
                 if (threadIdx.x == 0) atomicOr(&g_copy_status, 1u);
                 mbar_wait(&s_bar[cur], (uint32_t)(j / NBUF) & 1u);
-                if (NBUF == 2 && j + 1 < n_batches)
+                if (j + 1 < n_batches)
                     mbar_wait(&s_bar[(j + 1) % NBUF], (uint32_t)((j + 1) / NBUF) & 1u);
                 return;
             }
@@ -867,32 +846,13 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
             RedSmem& R = sRed[threadIdx.x >> 5];
             uint8_t* __restrict__ L = sList[threadIdx.x >> 5];
             int cnt = 0;
-            if (fwd_lists) {
-                // the forward's list of this batch (ascending, NO_HIT after its end):
-                // the entries up to k_top are a prefix of it, reversed here
-                if (k_top >= 0) {
-                    const int wit = (blockIdx.x % CTAS_PER_TILE) * CTA_WARPS + (threadIdx.x >> 5);
-                    const uint8_t* __restrict__ src = rec.L + (int64_t)wit * rec.cap + b0;
-                    int v[CTA_THREADS / 32];
-#pragma unroll
-                    for (int i = 0; i < CTA_THREADS / 32; ++i) {
-                        const int t = 32 * i + lane;
-                        v[i] = t < n ? src[t] : NO_HIT;
-                        cnt += __popc(__ballot_sync(FULL, v[i] <= k_top));
-                    }
-#pragma unroll
-                    for (int i = 0; i < CTA_THREADS / 32; ++i)
-                        if (v[i] <= k_top) L[cnt - 1 - (32 * i + lane)] = (uint8_t)v[i];
-                }
-            } else {
-                for (int m = k_top >> 5; m >= 0; --m) {
-                    const int kk = m * 32 + lane;
-                    const bool hit = kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0);
-                    const uint32_t mask = __ballot_sync(FULL, hit);
-                    // hits above this lane in the chunk come first
-                    if (hit) L[cnt + __popc(mask >> lane) - 1] = (uint8_t)kk;
-                    cnt += __popc(mask);
-                }
+            for (int m = k_top >> 5; m >= 0; --m) {
+                const int kk = m * 32 + lane;
+                const bool hit = kk <= k_top && block_hits(sA[kk], sB[kk], sC[kk].w, pm.x0, pm.y0);
+                const uint32_t mask = __ballot_sync(FULL, hit);
+                // hits above this lane in the chunk come first
+                if (hit) L[cnt + __popc(mask >> lane) - 1] = (uint8_t)kk;
+                cnt += __popc(mask);
             }
             if (lane < RGROUP) L[cnt + lane] = NO_HIT;
             __syncwarp();
@@ -1151,6 +1111,222 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
     }
     if (SOFT && inside && v_mesh_depth) v_mesh_depth[pix] = vD;
 }
+
+// Hard split with the forward's staged records and hit lists: every warp works
+// through its own lists with no CTA barrier.  For each of the forward's batches
+// (back to front, up to the warp's last composited entry) it reads its list,
+// and for each group of eight listed entries it loads their records from the
+// staged buffer itself (three 16-byte loads a record, one per lane) into a
+// per-warp group buffer; the per-entry chain, the tensor-core sums and the
+// gradient atomics are those of k_composite_bwd.
+struct GroupRec {
+    float4 r[3][RGROUP];  // A, B, C of each group slot
+};
+
+template <bool STATS>
+__global__ void __launch_bounds__(CTA_THREADS, 10)
+k_composite_bwd_lists(Cam c, float3 bg, const int2* __restrict__ tile_range, const float* __restrict__ mesh_depth,
+                      const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
+                      const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
+                      const float* __restrict__ g_rgb, const float* __restrict__ g_depth,
+                      const float* __restrict__ g_alpha, float* __restrict__ v_splats, AaLayer aa, Staged rec,
+                      unsigned long long* __restrict__ stats)
+{
+    __shared__ __align__(16) RedSmem sRed[CTA_WARPS];
+    __shared__ __align__(16) float2 sMf[4][32];
+    __shared__ uint8_t sList[CTA_WARPS][CTA_THREADS + RGROUP];
+    __shared__ __align__(16) GroupRec sG[CTA_WARPS];
+    int tile;
+    const PixelMap pm = pixel_of(c, tile);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const bool inside = pm.i < c.W && pm.j < c.H;
+    const int64_t pix = (int64_t)pm.j * c.W + pm.i;
+    const float px = (float)pm.i + 0.5f, py = (float)pm.j + 0.5f;
+
+    float D = -INFINITY, T = 1.0f, gr = 0.f, gg = 0.f, gb = 0.f, gz = 0.f;
+    int last = 0;
+    // behind = (colour, depth) accumulated behind the current Gaussian, dotted with
+    // this pixel's upstream gradient (g_rgb, g_depth); starts with the terminal layer
+    float behind = 0.f, aterm = 0.f;
+    if (inside) {
+        D = mesh_depth[pix];
+        const bool cov = aa.cov ? D < INFINITY : face_id[pix] >= 0;
+        T = T_final[pix];
+        last = n_contrib[pix];
+        gr = g_rgb[3 * pix]; gg = g_rgb[3 * pix + 1]; gb = g_rgb[3 * pix + 2];
+        gz = g_depth[pix];
+        if (aa.cov) {
+            // behind the front chain: the layer, and through 1 - a what lies behind it
+            // (the back chain's colour, depth and transmittance, then the background)
+            const float a = aa.cov[pix], ua = 1.0f - a;
+            float Tb = 1.0f, Eb = bg.x * gr + bg.y * gg + bg.z * gb;
+            if (cov && a < 1.0f) {
+                const float4 bk = aa.back[pix];
+                Tb = aa.T_back[pix];
+                Eb = fmaf(Tb, Eb, bk.x * gr + bk.y * gg + bk.z * gb + bk.w * gz);
+            }
+            const float own = mesh_rgb[3 * pix] * gr + mesh_rgb[3 * pix + 1] * gg + mesh_rgb[3 * pix + 2] * gb +
+                              (a > 0.0f ? a * D * gz : 0.0f);
+            behind = T * fmaf(ua, Eb, own);
+            aterm = g_alpha[pix] * T * ua * Tb;
+        } else if (cov) {
+            behind = T * (mesh_rgb[3 * pix] * gr + mesh_rgb[3 * pix + 1] * gg + mesh_rgb[3 * pix + 2] * gb + D * gz);
+        } else {
+            behind = T * (bg.x * gr + bg.y * gg + bg.z * gb);
+            aterm = g_alpha[pix] * T;  // out_alpha = 1 - T_final when uncovered
+        }
+    }
+    int warp_last = last;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) warp_last = max(warp_last, __shfl_xor_sync(0xffffffffu, warp_last, o));
+    RedSmem& R = sRed[w];
+    {
+        // B fragments: moments of pixel (i, j) = (c (+4), kb) for term g; the upstream
+        // gradient's channel g & 3 (hi for g < 4, lo for g >= 4) of pixel kb * 8 + c (+4)
+        const int g = lane >> 2, c = lane & 3;
+        for (int kb = w; kb < 4; kb += CTA_WARPS) sMf[kb][lane] = make_float2(moment(g, c, kb), moment(g, c + 4, kb));
+        float* gtmp = &R.ds[0][0];  // 128 floats of scratch before the first group
+        gtmp[4 * lane] = gr;
+        gtmp[4 * lane + 1] = gg;
+        gtmp[4 * lane + 2] = gb;
+        gtmp[4 * lane + 3] = gz;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float b[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float x = gtmp[4 * (q * 8 + c + 4 * h) + (g & 3)];
+                const uint32_t hi = to_tf32(x);
+                b[h] = g < 4 ? __uint_as_float(hi) : __uint_as_float(to_tf32(x - __uint_as_float(hi)));
+            }
+            R.gf[q][lane] = make_float2(b[0], b[1]);
+        }
+        __syncwarp();
+    }
+    __syncthreads();  // the moments' fragments, written by every warp
+    uint32_t visited = 0, contributed = 0;
+    const int2 r = clamp_range(tile_range[tile], rec.cap);
+    const int wend = min(r.x + warp_last, r.y);  // this warp's entries: [r.x, wend)
+    const int nb = (wend - r.x + CTA_THREADS - 1) / CTA_THREADS;
+    const int wit = (blockIdx.x % CTAS_PER_TILE) * CTA_WARPS + w;
+    const uint8_t* __restrict__ lists = rec.L + (int64_t)wit * rec.cap;
+    uint8_t* __restrict__ L = sList[w];
+    GroupRec& G = sG[w];
+    const int col = frag_col(lane);
+    for (int j = nb - 1; j >= 0; --j) {
+        const int b0 = r.x + CTA_THREADS * j;  // the forward's batch j
+        const int n = min(CTA_THREADS, wend - b0);
+        // the forward's list of this batch (ascending, NO_HIT after its end): its
+        // entries below n, reversed
+        int fl[CTA_THREADS / 32];
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < CTA_THREADS / 32; ++i) {
+            const int t = 32 * i + lane;
+            fl[i] = t < n ? __ldg(lists + b0 + t) : NO_HIT;
+            cnt += __popc(__ballot_sync(FULL, fl[i] < n));
+        }
+#pragma unroll
+        for (int i = 0; i < CTA_THREADS / 32; ++i)
+            if (fl[i] < n) L[cnt - 1 - (32 * i + lane)] = (uint8_t)fl[i];
+        if (lane < RGROUP) L[cnt + lane] = NO_HIT;
+        __syncwarp();
+        // entries [0, lastk) of the batch lie before the pixel's last composited one
+        // (all of them in front of the mesh); NO_HIT >= CTA_THREADS >= lastk
+        const int lastk = min(last - (b0 - r.x), CTA_THREADS);
+        // the group's records: lane t < 24 loads array t / 8 of slot t % 8; the next
+        // group's loads are in flight while the warp works on the current one
+        const int sj = lane & (RGROUP - 1), sa = lane / RGROUP;
+        const float4* __restrict__ src = (sa == 0 ? rec.A : sa == 1 ? rec.B : rec.C) + b0;
+        auto load_slot = [&](int base) {
+            const int k = lane < 3 * RGROUP ? L[base + sj] : NO_HIT;
+            return k != NO_HIT ? __ldg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        float4 nxt = load_slot(0);
+        for (int base = 0; base < cnt; base += RGROUP) {
+            if (lane < 3 * RGROUP) G.r[sa][sj] = nxt;
+            __syncwarp();
+            if (base + RGROUP < cnt) nxt = load_slot(base + RGROUP);
+            // per entry of the group, back to front: w = alpha T_front and ds = dL/d
+            // sigma at this lane's pixel, staged for the contraction (every lane
+            // evaluates every entry and keeps its pixel's part by selects)
+            bool any = false;
+#pragma unroll
+            for (int jj = 0; jj < RGROUP; ++jj) {
+                const int k = L[base + jj];
+                const float4 A = G.r[0][jj], B = G.r[1][jj], C3 = G.r[2][jj];
+                const Eval e = eval_splat(A, B, px, py);
+                const bool seen = k < lastk;
+                const bool take = seen && !e.skip;
+                if (STATS) {
+                    visited += seen;
+                    contributed += take;
+                }
+                const float a = e.alpha;
+                const float rom = __fdividef(1.0f, 1.0f - a);
+                const float Tp = T * rom;  // transmittance in front of it
+                const float wv = a * Tp;
+                const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
+                const float dLda = Tp * front + (aterm - behind) * rom;
+                behind = take ? fmaf(wv, front, behind) : behind;
+                T = take ? Tp : T;
+                any |= take;
+                // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
+                // d alpha / d sigma = -alpha
+                R.ds[jj][col] = take && !e.clamped ? -dLda * a : 0.0f;
+                R.w[jj][col] = take ? wv : 0.0f;
+            }
+            if (__any_sync(FULL, any)) {
+                __syncwarp();
+                const int g = lane >> 2, c = lane & 3;
+                float dm[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t af[4];
+                    const float2 bm = sMf[q][lane], bgf = R.gf[q][lane];
+                    a_frag(R.ds, g, q * 8 + 2 * c, af);
+                    mma_tf32(dm, af[0], af[1], af[2], af[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
+                    a_frag(R.w, g, q * 8 + 2 * c, af);
+                    mma_tf32(dc, af[0], af[1], af[2], af[3], __float_as_uint(bgf.x), __float_as_uint(bgf.y));
+                }
+                // lane (g, c): group slot g, terms 2c and 2c + 1 (see k_composite_bwd)
+                const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
+                float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
+                e0 += __shfl_xor_sync(FULL, e0, 2);
+                e1 += __shfl_xor_sync(FULL, e1, 2);
+                const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
+                const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
+                const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
+                const int k = L[base + g];
+                const int gid = k != NO_HIT ? rec_id(G.r[2][g]) : -1;
+                if (c == 0 && gid >= 0) {
+                    const float4 A = G.r[0][g], B = G.r[1][g];
+                    const float u = pm.x0 - A.x, v = pm.y0 - A.y;
+                    float acc[NGRAD];
+                    acc[0] = fmaf(u, t0, t1);
+                    acc[1] = fmaf(v, t0, sj);
+                    acc[2] = fmaf(u, fmaf(0.5f * u, t0, t1), 0.5f * sii);
+                    acc[3] = fmaf(v, acc[0], fmaf(u, sj, sij));
+                    acc[4] = fmaf(v, fmaf(0.5f * v, t0, sj), 0.5f * sjj);
+                    acc[5] = t0;
+                    acc[6] = e0;
+                    acc[7] = e1;
+                    acc[8] = eb;
+                    acc[9] = ez;
+                    flush_grad(v_splats, gid, acc, A, B);
+                }
+            }
+            __syncwarp();  // the group's records and staging are rewritten next
+        }
+        __syncwarp();  // the list is rewritten by the next batch
+    }
+    if (STATS) {
+        block_count(visited, stats);
+        block_count(contributed, stats + 1);
+    }
+}
+
 
 // ----------------------------------------------------- the back chain -----
 //
@@ -1528,14 +1704,21 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
     const Staged rec = staged_of(const_cast<float*>(staged), staged_cap);
     const bool bulk = rec.A != nullptr && !getenv("GM_BWD_GATHER");
     const bool mma = !soft && !getenv("GM_BWD_SHUFFLE_REDUCE");
+    if (bulk && mma) {
+        // the forward's hit lists: every warp through its own lists
+        auto lk = stats ? k_composite_bwd_lists<true> : k_composite_bwd_lists<false>;
+        lk<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
+            c, make_float3(bg[0], bg[1], bg[2]), reinterpret_cast<const int2*>(tile_range), mesh_depth, mesh_rgb,
+            face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, aa, rec,
+            reinterpret_cast<unsigned long long*>(stats));
+    } else {
     using K = decltype(&k_composite_bwd<false, false, false, false>);
     K kern;
     if (soft)
         kern = stats ? (bulk ? k_composite_bwd<true, true, true, false> : k_composite_bwd<true, true, false, false>)
                      : (bulk ? k_composite_bwd<false, true, true, false> : k_composite_bwd<false, true, false, false>);
-    else if (mma)
-        kern = stats ? (bulk ? k_composite_bwd<true, false, true, true> : k_composite_bwd<true, false, false, true>)
-                     : (bulk ? k_composite_bwd<false, false, true, true> : k_composite_bwd<false, false, false, true>);
+    else if (mma)  // gathered records (the staged ones go to k_composite_bwd_lists)
+        kern = stats ? k_composite_bwd<true, false, false, true> : k_composite_bwd<false, false, false, true>;
     else
         kern = stats ? (bulk ? k_composite_bwd<true, false, true, false> : k_composite_bwd<true, false, false, false>)
                      : (bulk ? k_composite_bwd<false, false, true, false> : k_composite_bwd<false, false, false, false>);
@@ -1544,7 +1727,8 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
         gids,
         reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
         face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth, aa,
-        bulk ? rec : Staged{nullptr, nullptr, nullptr, nullptr, 0}, reinterpret_cast<unsigned long long*>(stats));
+        bulk ? rec : Staged{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, reinterpret_cast<unsigned long long*>(stats));
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !aa.cov) return e;
     const int64_t P = (int64_t)c.W * c.H;
