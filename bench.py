@@ -171,17 +171,17 @@ PROFILED = {
         "warp_instructions": 266292620,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "3525e8e2f590fd3682f14a4c533c056221329e6b68363aab83d791f7e7693c99",
+                "86553406188b926f3b0b3ccf33c63d10969ec7d5ddff9f94e58fe5d4d41262a0",
         },
     },
     "composite_bwd": {
-        "kernel": "k_composite_bwd",
-        "dram_bytes": 200817920 + 12926208,
-        "smem_wavefronts": 76019432,
-        "warp_instructions": 397417341,
+        "kernel": "k_composite_bwd_lists",
+        "dram_bytes": 199812352 + 13190144,
+        "smem_wavefronts": 76481313,
+        "warp_instructions": 387267835,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "3525e8e2f590fd3682f14a4c533c056221329e6b68363aab83d791f7e7693c99",
+                "86553406188b926f3b0b3ccf33c63d10969ec7d5ddff9f94e58fe5d4d41262a0",
         },
     },
 }
