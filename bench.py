@@ -171,17 +171,17 @@ PROFILED = {
         "warp_instructions": 266292620,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "86553406188b926f3b0b3ccf33c63d10969ec7d5ddff9f94e58fe5d4d41262a0",
+                "cc19825b0c88827087827f2d459ecfc74a1855d9afcbec91073ffc001754c12e",
         },
     },
     "composite_bwd": {
         "kernel": "k_composite_bwd_lists",
-        "dram_bytes": 199812352 + 13190144,
-        "smem_wavefronts": 76481313,
-        "warp_instructions": 387267835,
+        "dram_bytes": 199804416 + 12902656,
+        "smem_wavefronts": 72106209,
+        "warp_instructions": 380159093,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "86553406188b926f3b0b3ccf33c63d10969ec7d5ddff9f94e58fe5d4d41262a0",
+                "cc19825b0c88827087827f2d459ecfc74a1855d9afcbec91073ffc001754c12e",
         },
     },
 }

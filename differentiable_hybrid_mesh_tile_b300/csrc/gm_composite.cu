@@ -1113,18 +1113,23 @@ k_composite_bwd(Cam c, float3 bg, int N, Split sp, const int2* __restrict__ tile
 }
 
 // Hard split with the forward's staged records and hit lists: every warp works
-// through its own lists with no CTA barrier.  For each of the forward's batches
-// (back to front, up to the warp's last composited entry) it reads its list,
-// and for each group of eight listed entries it loads their records from the
-// staged buffer itself (three 16-byte loads a record, one per lane) into a
-// per-warp group buffer; the per-entry chain, the tensor-core sums and the
-// gradient atomics are those of k_composite_bwd.
+// through its own lists with no CTA barrier.  It reads the lists of the
+// forward's batches back to front, up to the warp's last composited entry, into
+// a ring of pending list positions (descending), and takes them eight at a time
+// whatever batch they come from, so that only the last group is padded; each
+// group's records are loaded from the staged buffer by the warp itself (three
+// 16-byte loads a record, one per lane) into a per-warp group buffer, the next
+// group's loads in flight while the warp works on the current one.  The
+// per-entry chain, the tensor-core sums and the gradient atomics are those of
+// k_composite_bwd.
 struct GroupRec {
     float4 r[3][RGROUP];  // A, B, C of each group slot
 };
+constexpr int PEND_RING = 256;         // pending positions a warp holds: < 2 groups + a batch + padding
+constexpr int PEND_NONE = 0x7fffffff;  // a padding slot
 
 template <bool STATS>
-__global__ void __launch_bounds__(CTA_THREADS, 10)
+__global__ void __launch_bounds__(CTA_THREADS, 9)
 k_composite_bwd_lists(Cam c, float3 bg, const int2* __restrict__ tile_range, const float* __restrict__ mesh_depth,
                       const float* __restrict__ mesh_rgb, const int32_t* __restrict__ face_id,
                       const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
@@ -1134,7 +1139,7 @@ k_composite_bwd_lists(Cam c, float3 bg, const int2* __restrict__ tile_range, con
 {
     __shared__ __align__(16) RedSmem sRed[CTA_WARPS];
     __shared__ __align__(16) float2 sMf[4][32];
-    __shared__ uint8_t sList[CTA_WARPS][CTA_THREADS + RGROUP];
+    __shared__ __align__(16) int sPend[CTA_WARPS][PEND_RING];
     __shared__ __align__(16) GroupRec sG[CTA_WARPS];
     int tile;
     const PixelMap pm = pixel_of(c, tile);
@@ -1207,119 +1212,134 @@ k_composite_bwd_lists(Cam c, float3 bg, const int2* __restrict__ tile_range, con
     __syncthreads();  // the moments' fragments, written by every warp
     uint32_t visited = 0, contributed = 0;
     const int2 r = clamp_range(tile_range[tile], rec.cap);
-    const int wend = min(r.x + warp_last, r.y);  // this warp's entries: [r.x, wend)
-    const int nb = (wend - r.x + CTA_THREADS - 1) / CTA_THREADS;
+    const int wn = min(warp_last, r.y - r.x);  // this warp's entries: positions [0, wn) after r.x
+    int j = (wn + CTA_THREADS - 1) / CTA_THREADS - 1;  // the next of the forward's batches to list
     const int wit = (blockIdx.x % CTAS_PER_TILE) * CTA_WARPS + w;
-    const uint8_t* __restrict__ lists = rec.L + (int64_t)wit * rec.cap;
-    uint8_t* __restrict__ L = sList[w];
+    const uint8_t* __restrict__ lists = rec.L + (int64_t)wit * rec.cap + r.x;
+    int* __restrict__ P = sPend[w];
     GroupRec& G = sG[w];
     const int col = frag_col(lane);
-    for (int j = nb - 1; j >= 0; --j) {
-        const int b0 = r.x + CTA_THREADS * j;  // the forward's batch j
-        const int n = min(CTA_THREADS, wend - b0);
-        // the forward's list of this batch (ascending, NO_HIT after its end): its
-        // entries below n, reversed
-        int fl[CTA_THREADS / 32];
-        int cnt = 0;
+    // the group's records: lane t < 24 loads array t / 8 of slot t % 8
+    const int sj = lane & (RGROUP - 1), sa = lane / RGROUP;
+    const float4* __restrict__ src = (sa == 0 ? rec.A : sa == 1 ? rec.B : rec.C) + r.x;
+    int head = 0, tail = 0;  // pending positions: ring slots [head, tail)
+    // Lists the forward's batches, back to front, until two groups are pending:
+    // each batch's list (ascending, NO_HIT after its end) contributes its entries
+    // below the warp's end, reversed, as positions; after the first batch the
+    // pending positions are padded with PEND_NONE to a whole group.
+    auto refill = [&]() {
+        while (tail - head < 2 * RGROUP && j >= 0) {
+            const int b0 = CTA_THREADS * j;
+            const int n = min(CTA_THREADS, wn - b0);
+            int fl[CTA_THREADS / 32];
+            int cnt = 0;
 #pragma unroll
-        for (int i = 0; i < CTA_THREADS / 32; ++i) {
-            const int t = 32 * i + lane;
-            fl[i] = t < n ? __ldg(lists + b0 + t) : NO_HIT;
-            cnt += __popc(__ballot_sync(FULL, fl[i] < n));
+            for (int i = 0; i < CTA_THREADS / 32; ++i) {
+                const int t = 32 * i + lane;
+                fl[i] = t < n ? __ldg(lists + b0 + t) : NO_HIT;
+                cnt += __popc(__ballot_sync(FULL, fl[i] < n));
+            }
+#pragma unroll
+            for (int i = 0; i < CTA_THREADS / 32; ++i)
+                if (fl[i] < n) P[(tail + cnt - 1 - (32 * i + lane)) & (PEND_RING - 1)] = b0 + fl[i];
+            tail += cnt;
+            --j;
         }
-#pragma unroll
-        for (int i = 0; i < CTA_THREADS / 32; ++i)
-            if (fl[i] < n) L[cnt - 1 - (32 * i + lane)] = (uint8_t)fl[i];
-        if (lane < RGROUP) L[cnt + lane] = NO_HIT;
+        if (j < 0) {
+            const int end = (tail + RGROUP - 1) & ~(RGROUP - 1);
+            if (lane < end - tail) P[(tail + lane) & (PEND_RING - 1)] = PEND_NONE;
+            tail = end;
+        }
         __syncwarp();
-        // entries [0, lastk) of the batch lie before the pixel's last composited one
-        // (all of them in front of the mesh); NO_HIT >= CTA_THREADS >= lastk
-        const int lastk = min(last - (b0 - r.x), CTA_THREADS);
-        // the group's records: lane t < 24 loads array t / 8 of slot t % 8; the next
-        // group's loads are in flight while the warp works on the current one
-        const int sj = lane & (RGROUP - 1), sa = lane / RGROUP;
-        const float4* __restrict__ src = (sa == 0 ? rec.A : sa == 1 ? rec.B : rec.C) + b0;
-        auto load_slot = [&](int base) {
-            const int k = lane < 3 * RGROUP ? L[base + sj] : NO_HIT;
-            return k != NO_HIT ? __ldg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-        };
-        float4 nxt = load_slot(0);
-        for (int base = 0; base < cnt; base += RGROUP) {
-            if (lane < 3 * RGROUP) G.r[sa][sj] = nxt;
-            __syncwarp();
-            if (base + RGROUP < cnt) nxt = load_slot(base + RGROUP);
-            // per entry of the group, back to front: w = alpha T_front and ds = dL/d
-            // sigma at this lane's pixel, staged for the contraction (every lane
-            // evaluates every entry and keeps its pixel's part by selects)
-            bool any = false;
+    };
+    auto load_slot = [&](int base) {
+        const int p = lane < 3 * RGROUP ? P[(base & (PEND_RING - 1)) + sj] : PEND_NONE;
+        return p != PEND_NONE ? __ldg(src + p) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    // dL/d alpha of an entry = T_front front + (aterm - behind) / (1 - alpha): the
+    // chain carries aterm - behind
+    float nbh = aterm - behind;
+    refill();
+    float4 nxt = head < tail ? load_slot(head) : make_float4(0.f, 0.f, 0.f, 0.f);
+    while (head < tail) {
+        if (lane < 3 * RGROUP) G.r[sa][sj] = nxt;
+        refill();  // the next group pending (its loads in flight while the warp works on this one)
+        if (head + RGROUP < tail) nxt = load_slot(head + RGROUP);
+        const int* __restrict__ Pg = P + (head & (PEND_RING - 1));
+        const int4 pa = *reinterpret_cast<const int4*>(Pg), pb = *reinterpret_cast<const int4*>(Pg + 4);
+        const int pos[RGROUP] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        // per entry of the group, back to front: w = alpha T_front and ds = dL/d
+        // sigma at this lane's pixel, staged for the contraction (every lane
+        // evaluates every entry and keeps its pixel's part by selects); an entry
+        // lies before the pixel's last composited one, and so in front of the mesh,
+        // when its position is below the pixel's count (PEND_NONE is not)
+        bool any = false;
 #pragma unroll
-            for (int jj = 0; jj < RGROUP; ++jj) {
-                const int k = L[base + jj];
-                const float4 A = G.r[0][jj], B = G.r[1][jj], C3 = G.r[2][jj];
-                const Eval e = eval_splat(A, B, px, py);
-                const bool seen = k < lastk;
-                const bool take = seen && !e.skip;
-                if (STATS) {
-                    visited += seen;
-                    contributed += take;
-                }
-                const float a = e.alpha;
-                const float rom = __fdividef(1.0f, 1.0f - a);
-                const float Tp = T * rom;  // transmittance in front of it
-                const float wv = a * Tp;
-                const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
-                const float dLda = Tp * front + (aterm - behind) * rom;
-                behind = take ? fmaf(wv, front, behind) : behind;
-                T = take ? Tp : T;
-                any |= take;
-                // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
-                // d alpha / d sigma = -alpha
-                R.ds[jj][col] = take && !e.clamped ? -dLda * a : 0.0f;
-                R.w[jj][col] = take ? wv : 0.0f;
+        for (int jj = 0; jj < RGROUP; ++jj) {
+            const float4 A = G.r[0][jj], B = G.r[1][jj], C3 = G.r[2][jj];
+            const Eval e = eval_splat(A, B, px, py);
+            const bool seen = pos[jj] < last;
+            const bool take = seen && !e.skip;
+            if (STATS) {
+                visited += seen;
+                contributed += take;
             }
-            if (__any_sync(FULL, any)) {
-                __syncwarp();
-                const int g = lane >> 2, c = lane & 3;
-                float dm[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t af[4];
-                    const float2 bm = sMf[q][lane], bgf = R.gf[q][lane];
-                    a_frag(R.ds, g, q * 8 + 2 * c, af);
-                    mma_tf32(dm, af[0], af[1], af[2], af[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
-                    a_frag(R.w, g, q * 8 + 2 * c, af);
-                    mma_tf32(dc, af[0], af[1], af[2], af[3], __float_as_uint(bgf.x), __float_as_uint(bgf.y));
-                }
-                // lane (g, c): group slot g, terms 2c and 2c + 1 (see k_composite_bwd)
-                const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
-                float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
-                e0 += __shfl_xor_sync(FULL, e0, 2);
-                e1 += __shfl_xor_sync(FULL, e1, 2);
-                const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
-                const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
-                const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
-                const int k = L[base + g];
-                const int gid = k != NO_HIT ? rec_id(G.r[2][g]) : -1;
-                if (c == 0 && gid >= 0) {
-                    const float4 A = G.r[0][g], B = G.r[1][g];
-                    const float u = pm.x0 - A.x, v = pm.y0 - A.y;
-                    float acc[NGRAD];
-                    acc[0] = fmaf(u, t0, t1);
-                    acc[1] = fmaf(v, t0, sj);
-                    acc[2] = fmaf(u, fmaf(0.5f * u, t0, t1), 0.5f * sii);
-                    acc[3] = fmaf(v, acc[0], fmaf(u, sj, sij));
-                    acc[4] = fmaf(v, fmaf(0.5f * v, t0, sj), 0.5f * sjj);
-                    acc[5] = t0;
-                    acc[6] = e0;
-                    acc[7] = e1;
-                    acc[8] = eb;
-                    acc[9] = ez;
-                    flush_grad(v_splats, gid, acc, A, B);
-                }
-            }
-            __syncwarp();  // the group's records and staging are rewritten next
+            const float a = e.alpha;
+            const float rom = __fdividef(1.0f, 1.0f - a);
+            const float Tp = T * rom;  // transmittance in front of it
+            const float wv = a * Tp;
+            const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
+            const float dLda = fmaf(Tp, front, nbh * rom);
+            nbh = take ? fmaf(-wv, front, nbh) : nbh;
+            T = take ? Tp : T;
+            any |= take;
+            // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
+            // d alpha / d sigma = -alpha
+            R.ds[jj][col] = take && !e.clamped ? -dLda * a : 0.0f;
+            R.w[jj][col] = take ? wv : 0.0f;
         }
-        __syncwarp();  // the list is rewritten by the next batch
+        if (__any_sync(FULL, any)) {
+            __syncwarp();
+            const int g = lane >> 2, c = lane & 3;
+            float dm[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
+
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t af[4];
+                const float2 bm = sMf[q][lane], bgf = R.gf[q][lane];
+                a_frag(R.ds, g, q * 8 + 2 * c, af);
+                mma_tf32(dm, af[0], af[1], af[2], af[3], __float_as_uint(bm.x), __float_as_uint(bm.y));
+                a_frag(R.w, g, q * 8 + 2 * c, af);
+                mma_tf32(dc, af[0], af[1], af[2], af[3], __float_as_uint(bgf.x), __float_as_uint(bgf.y));
+            }
+            // lane (g, c): group slot g, terms 2c and 2c + 1 (see k_composite_bwd)
+            const float t0 = dm[0] + dm[2], t1 = dm[1] + dm[3];
+            float e0 = dc[0] + dc[2], e1 = dc[1] + dc[3];
+            e0 += __shfl_xor_sync(FULL, e0, 2);
+            e1 += __shfl_xor_sync(FULL, e1, 2);
+            const float sj = __shfl_down_sync(FULL, t0, 1), sii = __shfl_down_sync(FULL, t1, 1);
+            const float sij = __shfl_down_sync(FULL, t0, 2), sjj = __shfl_down_sync(FULL, t1, 2);
+            const float eb = __shfl_down_sync(FULL, e0, 1), ez = __shfl_down_sync(FULL, e1, 1);
+            const int gid = Pg[g] != PEND_NONE ? rec_id(G.r[2][g]) : -1;
+            if (c == 0 && gid >= 0) {
+                const float4 A = G.r[0][g], B = G.r[1][g];
+                const float u = pm.x0 - A.x, v = pm.y0 - A.y;
+                float acc[NGRAD];
+                acc[0] = fmaf(u, t0, t1);
+                acc[1] = fmaf(v, t0, sj);
+                acc[2] = fmaf(u, fmaf(0.5f * u, t0, t1), 0.5f * sii);
+                acc[3] = fmaf(v, acc[0], fmaf(u, sj, sij));
+                acc[4] = fmaf(v, fmaf(0.5f * v, t0, sj), 0.5f * sjj);
+                acc[5] = t0;
+                acc[6] = e0;
+                acc[7] = e1;
+                acc[8] = eb;
+                acc[9] = ez;
+                flush_grad(v_splats, gid, acc, A, B);
+            }
+        }
+        __syncwarp();  // the group's records and staging are rewritten next
+        head += RGROUP;
     }
     if (STATS) {
         block_count(visited, stats);
