@@ -86,9 +86,10 @@ __device__ __forceinline__ void stage_rec(const float4* __restrict__ splats, int
     } else if (!(o255 >= 1.0f)) {
         lmin = INFINITY;   // exp(-sigma) <= 1: never reaches 1/255
     } else {
-        // lowered by 0.1 % + 1e-4 so that rounding in the block test never drops a
-        // pixel the exact evaluation keeps
-        lmin = -log2f(o255) * 1.001f - 1e-4f;
+        // lowered by 0.1 % + 1e-4 so that rounding in the block test and the
+        // approximate logarithm (absolute error near 1e-6 here) never drop a pixel
+        // the exact evaluation keeps
+        lmin = -__log2f(o255) * 1.001f - 1e-4f;
     }
     C = make_float4(s2.x, s2.y, __int_as_float(g), lmin);
 }
@@ -1289,14 +1290,15 @@ k_composite_bwd_lists(Cam c, float3 bg, const int2* __restrict__ tile_range, con
             const float Tp = T * rom;  // transmittance in front of it
             const float wv = a * Tp;
             const float front = B.z * gr + B.w * gg + C3.x * gb + C3.y * gz;
+            const float wt = take ? wv : 0.0f;  // an entry not taken adds nothing to the chain
             const float dLda = fmaf(Tp, front, nbh * rom);
-            nbh = take ? fmaf(-wv, front, nbh) : nbh;
+            nbh = fmaf(-wt, front, nbh);
             T = take ? Tp : T;
             any |= take;
             // alpha clamped at 0.99 has no opacity / sigma gradient; elsewhere
             // d alpha / d sigma = -alpha
             R.ds[jj][col] = take && !e.clamped ? -dLda * a : 0.0f;
-            R.w[jj][col] = take ? wv : 0.0f;
+            R.w[jj][col] = wt;
         }
         if (__any_sync(FULL, any)) {
             __syncwarp();
