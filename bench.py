@@ -166,22 +166,22 @@ def job_throughput(n_ranks, pixels_per_rank, ms):
 PROFILED = {
     "composite_fwd": {
         "kernel": "k_composite_fwd",
-        "dram_bytes": 88629248 + 108866560,
-        "smem_wavefronts": 35299137,
-        "warp_instructions": 266292620,
+        "dram_bytes": 88710656 + 110675712,
+        "smem_wavefronts": 35540993,
+        "warp_instructions": 265224289,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "cc19825b0c88827087827f2d459ecfc74a1855d9afcbec91073ffc001754c12e",
+                "804687b2aeeee6827b0cbaeb2b7c99c60daf0548931a0619ad3fe1e0be453431",
         },
     },
     "composite_bwd": {
         "kernel": "k_composite_bwd_lists",
-        "dram_bytes": 199804416 + 12902656,
-        "smem_wavefronts": 72106209,
-        "warp_instructions": 380159093,
+        "dram_bytes": 199833088 + 12722432,
+        "smem_wavefronts": 72111132,
+        "warp_instructions": 366643095,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "cc19825b0c88827087827f2d459ecfc74a1855d9afcbec91073ffc001754c12e",
+                "804687b2aeeee6827b0cbaeb2b7c99c60daf0548931a0619ad3fe1e0be453431",
         },
     },
 }
