@@ -171,7 +171,7 @@ PROFILED = {
         "warp_instructions": 265224289,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "804687b2aeeee6827b0cbaeb2b7c99c60daf0548931a0619ad3fe1e0be453431",
+                "604d981600a346100fe5246f31f0232a0f7e9cabb05e2defdebe56903e6422b6",
         },
     },
     "composite_bwd": {
@@ -181,7 +181,7 @@ PROFILED = {
         "warp_instructions": 366643095,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "804687b2aeeee6827b0cbaeb2b7c99c60daf0548931a0619ad3fe1e0be453431",
+                "604d981600a346100fe5246f31f0232a0f7e9cabb05e2defdebe56903e6422b6",
         },
     },
 }

@@ -1734,22 +1734,22 @@ cudaError_t composite_bwd(const Cam& c, const float bg[3], int N, float softness
             face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, aa, rec,
             reinterpret_cast<unsigned long long*>(stats));
     } else {
-    using K = decltype(&k_composite_bwd<false, false, false, false>);
-    K kern;
-    if (soft)
-        kern = stats ? (bulk ? k_composite_bwd<true, true, true, false> : k_composite_bwd<true, true, false, false>)
-                     : (bulk ? k_composite_bwd<false, true, true, false> : k_composite_bwd<false, true, false, false>);
-    else if (mma)  // gathered records (the staged ones go to k_composite_bwd_lists)
-        kern = stats ? k_composite_bwd<true, false, false, true> : k_composite_bwd<false, false, false, true>;
-    else
-        kern = stats ? (bulk ? k_composite_bwd<true, false, true, false> : k_composite_bwd<true, false, false, false>)
-                     : (bulk ? k_composite_bwd<false, false, true, false> : k_composite_bwd<false, false, false, false>);
-    kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
-        c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
-        gids,
-        reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
-        face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth, aa,
-        bulk ? rec : Staged{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, reinterpret_cast<unsigned long long*>(stats));
+        using K = decltype(&k_composite_bwd<false, false, false, false>);
+        K kern;
+        if (soft)
+            kern = stats ? (bulk ? k_composite_bwd<true, true, true, false> : k_composite_bwd<true, true, false, false>)
+                         : (bulk ? k_composite_bwd<false, true, true, false> : k_composite_bwd<false, true, false, false>);
+        else if (mma)  // gathered records (the staged ones go to k_composite_bwd_lists)
+            kern = stats ? k_composite_bwd<true, false, false, true> : k_composite_bwd<false, false, false, true>;
+        else
+            kern = stats ? (bulk ? k_composite_bwd<true, false, true, false> : k_composite_bwd<true, false, false, false>)
+                         : (bulk ? k_composite_bwd<false, false, true, false> : k_composite_bwd<false, false, false, false>);
+        kern<<<c.TW * c.TH * CTAS_PER_TILE, CTA_THREADS, 0, s>>>(
+            c, make_float3(bg[0], bg[1], bg[2]), N, Split{softness, split == 1}, reinterpret_cast<const int2*>(tile_range),
+            gids,
+            reinterpret_cast<const float4*>(splats), reinterpret_cast<const float4*>(depth_model), mesh_depth, mesh_rgb,
+            face_id, T_final, n_contrib, g_rgb, g_depth, g_alpha, v_splats, v_depth_model, v_mesh_depth, aa,
+            bulk ? rec : Staged{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, reinterpret_cast<unsigned long long*>(stats));
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !aa.cov) return e;

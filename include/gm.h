@@ -119,10 +119,12 @@ typedef struct gm_aa_layer {
  * soft split also its depth model; with the hard split instead, for each of
  * the tile's 8 x 4 pixel blocks, which records of each batch reach it).
  * gm_composite_hybrid_fwd writes the records (and the hard split's hit lists)
- * of every batch it stages; gm_composite_hybrid_bwd then copies each batch of
- * a tile's list into shared memory with bulk copies instead of gathering the
- * splats through the ids, and takes the forward's hit lists instead of
- * testing the records again.  recs: device memory of
+ * of every batch it stages; gm_composite_hybrid_bwd then reads the records
+ * instead of gathering the splats through the ids: with the hard split each
+ * warp loads the records its hit lists name, with the soft split each batch
+ * of a tile's list comes into shared memory by bulk copies.  With the hard
+ * split it takes the forward's hit lists instead of testing the records
+ * again.  recs: device memory of
  * gm_staged_bytes(cap, opts->softness) bytes, 16-byte aligned, owned by the
  * caller, contents private to the library; cap >= the number of entries the
  * tile ranges address.  The backward call must get the records its forward
@@ -136,8 +138,8 @@ typedef struct gm_staged {
  * 64 with the soft split (softness > 0) */
 size_t gm_staged_bytes(int32_t cap, float softness);
 
-/* gm_get_copy_status -- the bulk copies of gm_composite_hybrid_bwd wait for
- * their data at most about one second; a wait that gives up stops that CTA
+/* gm_get_copy_status -- the bulk copies of gm_composite_hybrid_bwd (soft
+ * split, staged records) wait for their data at most about one second; a wait that gives up stops that CTA
  * (its gradients are then incomplete) and sets bit 0 of a device status word.
  * *flags (host) receives the word; clear != 0 resets it.  Synchronous. */
 int gm_get_copy_status(uint32_t* flags, int32_t clear);
@@ -471,9 +473,11 @@ int gm_composite_hybrid_fwd(const gm_camera* cam, const gm_opts* opts, int32_t N
  *   stats: NULL, or a device uint64[2] incremented by the number of (pixel,
  *   Gaussian) pairs evaluated [0] and given gradient terms [1] (profiling).
  *   staged: NULL (each batch of a tile's list is gathered through gids), or
- *   the buffer the forward call filled (gm_staged): each batch then arrives
- *   by bulk copies, the next one in flight while the current one is worked
- *   on.  The Gaussian part reads it; the mesh part does not.
+ *   the buffer the forward call filled (gm_staged): with the hard split each
+ *   warp then loads the records of its hit lists (the next group's loads in
+ *   flight while it works on the current one); with the soft split each batch
+ *   arrives by bulk copies, the next one in flight while the current one is
+ *   worked on.  The Gaussian part reads it; the mesh part does not.
  *   Soft split (opts->softness > 0): depth_model as for the forward pass;
  *   v_depth_model [N][4] f32 (+=, 16-byte aligned, required with v_splats):
  *   dL/d(g_u, g_v, sigma_z, -); v_mesh_depth [H][W] f32 (required with the
