@@ -171,7 +171,7 @@ PROFILED = {
         "warp_instructions": 265224289,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "604d981600a346100fe5246f31f0232a0f7e9cabb05e2defdebe56903e6422b6",
+                "eb849ce1c0bd1055929771719382f6576c7b38ed380ad4eef47a99da40417272",
         },
     },
     "composite_bwd": {
@@ -181,7 +181,7 @@ PROFILED = {
         "warp_instructions": 366643095,
         "sources": {
             "differentiable_hybrid_mesh_tile_b300/csrc/gm_composite.cu":
-                "604d981600a346100fe5246f31f0232a0f7e9cabb05e2defdebe56903e6422b6",
+                "eb849ce1c0bd1055929771719382f6576c7b38ed380ad4eef47a99da40417272",
         },
     },
 }

@@ -38,7 +38,9 @@ constexpr uint8_t NO_HIT = 0xff;              // padding of a warp's hit list
 
 // Staged records of a tile list (one per list position, three float4 arrays,
 // a fourth with the soft split's depth model): written by the forward pass,
-// bulk-copied into shared memory by the backward pass.  A == nullptr: none.
+// read by the backward pass (loaded per group of listed records with the hard
+// split, bulk-copied into shared memory per batch with the soft split).
+// A == nullptr: none.
 // With the hard split the space of the fourth array holds instead each warp's
 // hit lists: for warp w of a tile (0..7) and a batch starting at list position
 // b, the staged indices of the batch's records that reach the warp's block, in
@@ -239,7 +241,7 @@ __device__ __forceinline__ float warp_hide_depth(bool inside, bool cov, float D)
 }
 
 // A tile's range clamped to the staged-record buffer [0, cap) (the ranges come
-// from a sort that may have given up a bounded wait; the bulk copies read the
+// from a sort that may have given up a bounded wait; the backward reads the
 // records by range, so they must stay inside the buffer).
 __device__ __forceinline__ int2 clamp_range(int2 r, int cap)
 {
@@ -563,7 +565,8 @@ __device__ __forceinline__ float moment(int n, int i, int j)
 
 // ---------------------------------------------- bulk-copy staging ---------
 //
-// The backward pass's shuffle-sum form takes each batch of a tile's staged
+// The backward pass's shuffle-sum form (the soft split's, and the hard split's
+// under GM_BWD_SHUFFLE_REDUCE) takes each batch of a tile's staged
 // records (written by the forward pass in list order) with bulk copies
 // (cp.async.bulk, the TMA engine's linear mode) into shared memory: one thread
 // issues the copies of a batch and an mbarrier counts their bytes; with two
